@@ -1,0 +1,557 @@
+"""Benchmark of the hybrid-SWA attention hot path on GB300.
+
+Default workload (--workload flash_decode): Flash-shaped decode, batch 64,
+64 q heads; one windowed layer (8 KV heads, 128-slot ring, sink) and one
+full-attention layer (4 KV heads, 32768 cached tokens + the new one).  One
+step = the KV write of the new token into both layers (RoPE + value scale)
++ swa_sink_decode + full_attn_decode, for the whole batch.  The JSON line
+also carries a chunked-prefill measurement (8192-token chunk on 122880
+cached tokens, one full + one windowed layer) under "prefill".
+
+Other workloads: prefill, long_decode (batch 16 at 524288 tokens),
+pro_mixed (128 ragged sequences through a 70-layer stack, 10 full : 60
+windowed), tiny (1 sequence, 512 tokens).
+
+All inputs are synthetic (seeded), drawn on the device.  Timing: CUDA events
+on the launching stream; inputs larger than L2 (the full pool is GBs; the
+windowed layer rotates over enough distinct rings to exceed L2).  Prints one
+JSON line on rank 0.  `--impl reference` times the fp64 CPU oracle on a
+bounded sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+SCALE = 1.0 / math.sqrt(192.0)
+METRIC = "decode attn tokens/s + HBM GB/s; prefill attn TFLOP/s; % of GB300 roofline"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# --------------------------------------------------------------------------- helpers
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_traffic(kernel: str):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, if the
+    kernel's source has not changed since the counters were taken."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f).get(kernel)
+    if not d:
+        return None
+    src = os.path.join(ROOT, "sinks_kv_ring_gb300", "csrc", d["source"])
+    if not os.path.exists(src) or hashlib.sha256(open(src, "rb").read()).hexdigest()[:16] != d["sha256_16"]:
+        return None
+    return d["bytes_per_launch"]
+
+
+class Clocks:
+    """nvidia-smi sampling during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.path or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        rows = []
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) >= 9:
+                rows.append(f)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def flush_l2(buf):
+    buf.add_(1)
+
+
+class EventTimer:
+    """Per-call durations of one kind of launch, from CUDA events recorded on
+    the launching stream."""
+
+    def __init__(self):
+        self.pairs = []
+
+    def start(self, stream):
+        a = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        return a
+
+    def stop(self, a, stream):
+        b = torch.cuda.Event(enable_timing=True)
+        b.record(stream)
+        self.pairs.append((a, b))
+
+    def mean_ms(self):
+        if not self.pairs:
+            return None
+        return sum(a.elapsed_time(b) for a, b in self.pairs) / len(self.pairs)
+
+
+# --------------------------------------------------------------------------- workloads
+
+def _fill_pool(kvr, pool, syn, seqs, ctx, table, vscale, chunk=65536):
+    dev = pool.k.device
+    hkv = pool.num_kv_heads
+    for s, n in zip(seqs, ctx):
+        for lo in range(0, n, chunk):
+            hi = min(n, lo + chunk)
+            k = syn.k(hi - lo, hkv, seq=s, start=lo)
+            v = syn.v(hi - lo, hkv, seq=s, start=lo)
+            pos = torch.arange(lo, hi, device=dev)
+            sq = torch.full((hi - lo,), s, dtype=torch.int32, device=dev)
+            kvr.kv_ring_append_rope(k, v, pos, sq, table, vscale, pool)
+
+
+def _fill_rings(kvr, ring, syn, B, p, table, vscale):
+    dev = ring.k.device
+    hkv = ring.num_kv_heads
+    lo = max(0, p - 127)
+    n = p - lo
+    if n <= 0:
+        return
+    for s in range(B):
+        k = syn.k(n, hkv, seq=s, start=lo)
+        v = syn.v(n, hkv, seq=s, start=lo)
+        kvr.kv_ring_append_rope(k, v, torch.arange(lo, p, device=dev), torch.full((n,), s, dtype=torch.int32, device=dev),
+                                table, vscale, ring)
+
+
+class DecodeWorkload:
+    """One decode step over one windowed + one full-attention layer."""
+
+    def __init__(self, kvr, B=64, hq=64, hkv_swa=8, hkv_full=4, ctx=32768, vscale=0.707, seed=1001,
+                 swa_copies=None, device="cuda"):
+        from sinks_kv_ring_gb300.synth import Synth
+        self.kvr, self.B, self.hq, self.ctx = kvr, B, hq, ctx
+        self.hkv_swa, self.hkv_full, self.vscale = hkv_swa, hkv_full, vscale
+        self.p = ctx                      # the new token's position; context = ctx + 1
+        self.max_ctx = ctx + 1
+        dev = device
+        self.t4 = kvr.rope_table(1e4, ctx + 1, device=dev)
+        self.t7 = kvr.rope_table(1e7, ctx + 1, device=dev)
+        syn = Synth(seed, dist="shifted", device=dev)
+        self.pool = kvr.PagedLayout.contiguous(B, hkv_full, self.max_ctx, block_size=64, device=dev, zero=False)
+        _fill_pool(kvr, self.pool, Synth(seed, layer=1, device=dev), range(B), [ctx] * B, self.t7, vscale)
+        ring_bytes = kvr.RingLayout.bytes_per_layer(B, hkv_swa)
+        if swa_copies is None:
+            swa_copies = max(1, min(64, math.ceil(4 * 129e6 / ring_bytes)))
+        self.rings = []
+        base = kvr.RingLayout.empty(B, hkv_swa, device=dev)
+        _fill_rings(kvr, base, syn, B, self.p, self.t4, vscale)
+        for i in range(swa_copies):
+            self.rings.append(base if i == 0 else kvr.RingLayout(base.k.clone(), base.v.clone(), base.slot_pos.clone()))
+        # per-step inputs: q of both layers, the new token's k/v in both layers
+        self.q_swa = syn.q(B, hq, hkv_swa, seq=10_000)
+        self.q_full = Synth(seed, layer=1, device=dev).q(B, hq, hkv_full, seq=10_000)
+        self.k_swa, self.v_swa = syn.k(B, hkv_swa, seq=20_000), syn.v(B, hkv_swa, seq=20_000)
+        self.k_full = Synth(seed, layer=1, device=dev).k(B, hkv_full, seq=20_000)
+        self.v_full = Synth(seed, layer=1, device=dev).v(B, hkv_full, seq=20_000)
+        self.pos = torch.full((B,), self.p, dtype=torch.int64, device=dev)
+        self.seq = torch.arange(B, dtype=torch.int32, device=dev)
+        self.sinks = syn.sinks(hq).to(dev)
+        self.ws = torch.empty(kvr.full_attn_decode_workspace_size(B, hq, hkv_full, self.max_ctx), dtype=torch.uint8,
+                              device=dev)
+        self.out_swa = torch.empty(B, hq, 128, dtype=torch.bfloat16, device=dev)
+        self.out_full = torch.empty(B, hq, 128, dtype=torch.bfloat16, device=dev)
+        self.step_i = 0
+        self.t_full = EventTimer()
+        self.t_swa = EventTimer()
+        self.launches_per_step = 5
+
+    def bytes_full(self):
+        # K/V bytes the full layer must read (every cached position, every KV head)
+        return self.B * self.hkv_full * (self.p + 1) * (192 + 128) * 2
+
+    def bytes_swa(self):
+        return self.B * self.hkv_swa * min(128, self.p + 1) * (192 + 128) * 2
+
+    def step(self, stream, timed=False):
+        kvr = self.kvr
+        ring = self.rings[self.step_i % len(self.rings)]
+        self.step_i += 1
+        kvr.kv_ring_append_rope(self.k_swa, self.v_swa, self.pos, self.seq, self.t4, self.vscale, ring, stream=stream)
+        kvr.kv_ring_append_rope(self.k_full, self.v_full, self.pos, self.seq, self.t7, self.vscale, self.pool,
+                                stream=stream)
+        a = self.t_swa.start(stream) if timed else None
+        kvr.swa_sink_decode(self.q_swa, self.pos, self.seq, ring, self.sinks, self.t4, SCALE, out=self.out_swa,
+                            stream=stream)
+        if timed:
+            self.t_swa.stop(a, stream)
+            a = self.t_full.start(stream)
+        kvr.full_attn_decode(self.q_full, self.pos, self.seq, self.pool, self.t7, SCALE, self.max_ctx,
+                             workspace=self.ws, out=self.out_full, stream=stream)
+        if timed:
+            self.t_full.stop(a, stream)
+
+    def e2e_buffers(self):
+        """Pinned host copies of the per-step inputs and outputs."""
+        pin = lambda t: torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t)
+        ins = [self.q_swa, self.q_full, self.k_swa, self.v_swa, self.k_full, self.v_full, self.pos]
+        outs = [self.out_swa, self.out_full]
+        return [(pin(t), t) for t in ins], [(torch.empty(t.shape, dtype=t.dtype, pin_memory=True), t) for t in outs]
+
+
+class PrefillWorkload:
+    """One 8192-token chunk on top of 122880 cached tokens, one full + one windowed layer."""
+
+    def __init__(self, kvr, P0=122880, C=8192, hq=64, hkv_full=4, hkv_swa=8, vscale=0.707, seed=1002, device="cuda"):
+        from sinks_kv_ring_gb300.synth import Synth
+        self.kvr, self.P0, self.C, self.hq = kvr, P0, C, hq
+        self.hkv_full, self.hkv_swa, self.vscale = hkv_full, hkv_swa, vscale
+        dev = device
+        n = P0 + C
+        self.t4 = kvr.rope_table(1e4, n, device=dev)
+        self.t7 = kvr.rope_table(1e7, n, device=dev)
+        sf, ss = Synth(seed, layer=1, device=dev), Synth(seed, layer=0, device=dev)
+        self.pool = kvr.PagedLayout.contiguous(1, hkv_full, n, block_size=64, device=dev, zero=False)
+        _fill_pool(kvr, self.pool, sf, [0], [P0], self.t7, vscale)
+        self.ring = kvr.RingLayout.empty(1, hkv_swa, device=dev)
+        _fill_rings(kvr, self.ring, ss, 1, P0, self.t4, vscale)
+        self.ring0 = (self.ring.k.clone(), self.ring.v.clone(), self.ring.slot_pos.clone())
+        self.stage = kvr.LinearLayout.empty(C, hkv_swa, device=dev)
+        self.kf, self.vf = sf.k(C, hkv_full, seq=0, start=P0), sf.v(C, hkv_full, seq=0, start=P0)
+        self.ks, self.vs = ss.k(C, hkv_swa, seq=0, start=P0), ss.v(C, hkv_swa, seq=0, start=P0)
+        self.qf = sf.q(C, hq, hkv_full, seq=0, start=P0)
+        self.qs = ss.q(C, hq, hkv_swa, seq=0, start=P0)
+        self.sinks = ss.sinks(hq).to(dev)
+        self.pos = torch.arange(P0, P0 + C, device=dev)
+        self.seq = torch.zeros(C, dtype=torch.int32, device=dev)
+        self.tail = min(C, 128)
+        self.out_f = torch.empty(C, hq, 128, dtype=torch.bfloat16, device=dev)
+        self.out_s = torch.empty(C, hq, 128, dtype=torch.bfloat16, device=dev)
+        self.t_full = EventTimer()
+        self.t_swa = EventTimer()
+        self.launches_per_step = 5
+
+    def flops_full(self):
+        C, P0 = self.C, self.P0
+        pairs = C * P0 + C * (C + 1) // 2
+        return self.hq * pairs * 2 * (192 + 128)
+
+    def flops_swa(self):
+        pairs = sum(min(128, self.P0 + i + 1) for i in range(self.C))
+        return self.hq * pairs * 2 * (192 + 128)
+
+    def step(self, stream, timed=False):
+        kvr = self.kvr
+        # restore the ring's pre-chunk state (the previous step committed the chunk's tail)
+        self.ring.k.copy_(self.ring0[0]); self.ring.v.copy_(self.ring0[1]); self.ring.slot_pos.copy_(self.ring0[2])
+        kvr.kv_ring_append_rope(self.kf, self.vf, self.pos, self.seq, self.t7, self.vscale, self.pool, stream=stream)
+        a = self.t_full.start(stream) if timed else None
+        kvr.full_attn_prefill_chunk(self.qf, self.P0, 0, self.pool, self.t7, SCALE, out=self.out_f, stream=stream)
+        if timed:
+            self.t_full.stop(a, stream)
+        kvr.kv_ring_append_rope(self.ks, self.vs, self.pos, None, self.t4, self.vscale, self.stage, stream=stream)
+        a = self.t_swa.start(stream) if timed else None
+        kvr.swa_sink_prefill_chunk(self.qs, self.P0, 0, self.stage, self.ring, self.sinks, self.t4, SCALE, out=self.out_s,
+                                   stream=stream)
+        if timed:
+            self.t_swa.stop(a, stream)
+        t = self.tail
+        kvr.kv_ring_append_rope(self.ks[-t:], self.vs[-t:], self.pos[-t:], self.seq[-t:], self.t4, self.vscale,
+                                self.ring, stream=stream)
+
+
+# --------------------------------------------------------------------------- runs
+
+def timed_run(work, steps, warmup, stream, flush=None):
+    for _ in range(warmup):
+        work.step(stream)
+    torch.cuda.synchronize()
+    ev = []
+    for _ in range(steps):
+        if flush is not None:
+            flush_l2(flush)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        work.step(stream, timed=True)
+        b.record(stream)
+        ev.append((a, b))
+    torch.cuda.synchronize()
+    return sum(a.elapsed_time(b) for a, b in ev) / len(ev)
+
+
+def e2e_decode(work, steps, warmup, stream):
+    """The same decode step with the per-step inputs copied in from pinned host
+    memory and the outputs copied back, all inside the timed region."""
+    ins, outs = work.e2e_buffers()
+    h2d = sum(h.numel() * h.element_size() for h, _ in ins)
+    d2h = sum(h.numel() * h.element_size() for h, _ in outs)
+
+    def one():
+        with torch.cuda.stream(stream):
+            for h, d in ins:
+                d.copy_(h, non_blocking=True)
+            work.step(stream)
+            for h, d in outs:
+                h.copy_(d, non_blocking=True)
+
+    for _ in range(warmup):
+        one()
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        one()
+    b.record(stream)
+    b.synchronize()
+    return a.elapsed_time(b) / steps, h2d, d2h
+
+
+def cpu_baseline_decode(work, budget_s=12.0, max_seqs=16):
+    """The fp64 oracle on sampled sequences of the decode workload (both layers,
+    all heads), on all host cores; tokens/s."""
+    import numpy as np
+    import oracle
+    from sinks_kv_ring_gb300.synth import Synth
+    cores = os.cpu_count() or 1
+    syn_s, syn_f = Synth(1001, layer=0, device="cuda"), Synth(1001, layer=1, device="cuda")
+    q_s, q_f = work.q_swa.cpu(), work.q_full.cpu()
+    sk = work.sinks.double().cpu().numpy()
+    p = work.p
+    elapsed, done = 0.0, 0
+    for b in range(min(max_seqs, work.B)):
+        # raw K/V by position (host copies of the same seeded draws)
+        kf = torch.cat([syn_f.k(min(65536, p - lo), work.hkv_full, seq=b, start=lo) for lo in range(0, p, 65536)]
+                       + [work.k_full[b:b + 1]]).cpu()
+        vf = torch.cat([syn_f.v(min(65536, p - lo), work.hkv_full, seq=b, start=lo) for lo in range(0, p, 65536)]
+                       + [work.v_full[b:b + 1]]).cpu()
+        lo = max(0, p - 127)
+        ks = torch.cat([syn_s.k(p - lo, work.hkv_swa, seq=b, start=lo), work.k_swa[b:b + 1]]).cpu()
+        vs = torch.cat([syn_s.v(p - lo, work.hkv_swa, seq=b, start=lo), work.v_swa[b:b + 1]]).cpu()
+        t0 = time.perf_counter()
+        oracle.attend_seq(q_f[b:b + 1], [p], kf, vf, 0, 1e7, work.vscale, SCALE, 0, None, nthreads=cores)
+        oracle.attend_seq(q_s[b:b + 1], [p], ks, vs, lo, 1e4, work.vscale, SCALE, 128, sk, nthreads=cores)
+        elapsed += time.perf_counter() - t0
+        done += 1
+        if elapsed >= budget_s:
+            break
+    return {"value": done / elapsed, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"{done} of {work.B} sequences, all 64 heads, one windowed + one full layer at context "
+                      f"{p + 1}; {elapsed:.1f} s of fp64 oracle on {cores} threads"}
+
+
+def run_decode(args, kvr, peaks_d, peaks_src, rank, world):
+    stream = torch.cuda.current_stream()
+    work = DecodeWorkload(kvr, seed=1001 + rank)
+    torch.cuda.synchronize()
+    with Clocks(torch.cuda.current_device()) as ck:
+        ms = timed_run(work, args.steps, args.warmup, stream)
+    clocks = ck.summary()
+    ms_full = work.t_full.mean_ms()
+    ms_swa = work.t_swa.mean_ms()
+    e2e_ms, h2d, d2h = e2e_decode(work, max(3, args.steps // 2), 2, stream)
+    return work, ms, ms_full, ms_swa, clocks, (e2e_ms, h2d, d2h)
+
+
+def run_prefill(kvr, steps, warmup):
+    stream = torch.cuda.current_stream()
+    work = PrefillWorkload(kvr)
+    torch.cuda.synchronize()
+    ms = timed_run(work, steps, warmup, stream)
+    return work, ms
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="flash_decode", choices=["flash_decode", "prefill"])
+    ap.add_argument("--no-prefill", action="store_true", help="skip the prefill sub-measurement")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    import __graft_entry__
+    __graft_entry__.build() if rank == 0 else None
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    import sinks_kv_ring_gb300 as kvr
+    peaks_d, peaks_src = peaks()
+
+    work, ms, ms_full, ms_swa, clocks, (e2e_ms, h2d, d2h) = run_decode(args, kvr, peaks_d, peaks_src, rank, world)
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms, e2e_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms, e2e_ms = float(t[0]), float(t[1])
+    B = work.B
+    value = world * B / (ms / 1e3)
+    hbm = peaks_d["hbm_gbs"]
+    gbs_full = work.bytes_full() / (ms_full / 1e3) / 1e9
+    gbs_swa = work.bytes_swa() / (ms_swa / 1e3) / 1e9
+    res = {
+        "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "flash_decode: batch 64, 64 q heads; windowed layer 8 KV heads ring 128 + sink; "
+                               "full layer 4 KV heads at context 32769; dims 192/192/128; value scale 0.707",
+                   "global_batch": B * world, "seq_len": work.p + 1, "parallelism": f"dp{world}",
+                   "l2": f"inputs > L2: full pool {work.bytes_full() / 1e9:.2f} GB read per step; windowed rings "
+                         f"rotated over {len(work.rings)} copies ({len(work.rings) * work.bytes_swa() / 1e9:.2f} GB)"},
+        "kernels": {
+            "full_attn_decode": {"ms": round(ms_full, 4), "GB/s": round(gbs_full, 1),
+                                 "hbm_frac": round(gbs_full / hbm, 4), "bytes": work.bytes_full()},
+            "swa_sink_decode": {"ms": round(ms_swa, 5), "GB/s": round(gbs_swa, 1),
+                                "hbm_frac": round(gbs_swa / hbm, 4), "bytes": work.bytes_swa()},
+        },
+        "roofline": {"bound": "hbm", "achieved": round(gbs_full, 1), "peak": hbm, "unit": "GB/s",
+                     "frac": round(gbs_full / hbm, 4), "peak_source": peaks_src,
+                     "kernel": "full_attn_decode (split kernel + combine)",
+                     "traffic": kernel_traffic("full_decode_kernel")},
+        "e2e": {"value": round(world * B / (e2e_ms / 1e3), 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": work.launches_per_step * args.steps,
+        "clocks": clocks,
+    }
+    if not args.no_prefill:
+        del work
+        torch.cuda.empty_cache()
+        pw, pms = run_prefill(kvr, max(3, args.steps // 4), 3)
+        tf_full = pw.flops_full() / (pw.t_full.mean_ms() / 1e3) / 1e12
+        tf_swa = pw.flops_swa() / (pw.t_swa.mean_ms() / 1e3) / 1e12
+        pk = peaks_d.get("bf16_tflops_sustained", peaks_d["bf16_tflops"])
+        res["prefill"] = {
+            "workload": "1 sequence, 8192-token chunk on 122880 cached tokens; 64 q heads; full layer 4 KV heads "
+                        "theta 1e7 + windowed layer 8 KV heads theta 1e4, ring 128 + sink",
+            "ms_per_step": round(pms, 3),
+            "full_attn_prefill_chunk": {"ms": round(pw.t_full.mean_ms(), 3), "TFLOP/s": round(tf_full, 1),
+                                        "flop": pw.flops_full()},
+            "swa_sink_prefill_chunk": {"ms": round(pw.t_swa.mean_ms(), 4), "TFLOP/s": round(tf_swa, 1),
+                                       "flop": pw.flops_swa()},
+            "roofline": {"bound": "tensor", "achieved": round(tf_full, 1), "peak": pk, "unit": "TFLOP/s",
+                         "frac": round(tf_full / pk, 4), "peak_source": peaks_src + " (sustained)",
+                         "traffic": kernel_traffic("prefill_kernel_full")},
+        }
+        res["gpu_launches"] += pw.launches_per_step * max(3, args.steps // 4)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        w2 = DecodeWorkload(kvr, seed=1001) if args.no_prefill is False else None
+        res["cpu_baseline"] = cpu_baseline_decode(w2 if w2 is not None else work)
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def run_reference(args, rank, world):
+    """The fp64 CPU oracle, as it stands, on a bounded sample of the decode
+    workload (one sequence per step, both layers, all heads)."""
+    if rank != 0:
+        return
+    import numpy as np
+    import oracle
+    oracle.build()
+    from sinks_kv_ring_gb300.synth import Synth
+    cores = os.cpu_count() or 1
+    B, hq, p = 64, 64, 32768
+    syn_s, syn_f = Synth(1001, layer=0), Synth(1001, layer=1)
+    times = []
+    for i in range(args.warmup + args.steps):
+        b = i % B
+        kf = syn_f.k(p + 1, 4, seq=b)
+        vf = syn_f.v(p + 1, 4, seq=b)
+        ks = syn_s.k(128, 8, seq=b, start=p - 127)
+        vs = syn_s.v(128, 8, seq=b, start=p - 127)
+        qf, qs = syn_f.q(1, hq, 4, seq=10_000 + b), syn_s.q(1, hq, 8, seq=10_000 + b)
+        sk = syn_s.sinks(hq).double().numpy()
+        t0 = time.perf_counter()
+        oracle.attend_seq(qf, [p], kf, vf, 0, 1e7, 0.707, SCALE, 0, None, nthreads=cores)
+        oracle.attend_seq(qs, [p], ks, vs, p - 127, 1e4, 0.707, SCALE, 128, sk, nthreads=cores)
+        dt = time.perf_counter() - t0
+        if i >= args.warmup:
+            times.append(dt)
+    ms = 1e3 * sum(times) / len(times)
+    value = 1.0 / (ms / 1e3)
+    sample = (f"one of the 64 sequences per step (all 64 heads, one windowed + one full layer at context {p + 1}); "
+              f"fp64 oracle on {cores} threads")
+    res = {"impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "tokens/s", "n_gpus": world,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+           "config": {"workload": "flash_decode: batch 64, 64 q heads; windowed layer 8 KV heads ring 128 + sink; "
+                                  "full layer 4 KV heads at context 32769 (oracle: one sequence per step)",
+                      "global_batch": B, "seq_len": p + 1, "parallelism": "host cores"},
+           "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                            "sample": sample},
+           "e2e": {"value": round(value, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(res), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,230 @@
+/*
+ * kvring.h -- C ABI of the hybrid-SWA attention hot path (sm_103a).
+ *
+ * MiMo-V2-style hybrid attention: most layers attend over a sliding window
+ * of W = 128 positions with a learned per-head sink logit, kept in a ring of
+ * 128 slots; a few layers attend over the whole context, kept in a paged pool.
+ * Heads are GQA with 192-wide q/k and 128-wide v; RoPE is rotate-half on the
+ * first 64 dims (theta 1e4 on windowed layers, 1e7 on full layers); v is
+ * multiplied by the value scale when it is written.  Sources: colibri
+ * "MiMo-V2.6", sections "What the engine implements" and "System One mode and
+ * prompt reuse"; gaudi-cookbook "MiMo-V2.6-Flash on Gaudi 2", sections "What
+ * was built" and "The RoPE fix for large positions"; Xiaomi "Full-Pipeline
+ * Inference Optimization for MiMo-V2.5 Series", section 2.1 (dual KV pools).
+ *
+ * Conventions for every call:
+ *  - bf16 tensors are IEEE bfloat16 bit patterns (kvr_bf16), row-major,
+ *    densely packed.  All tensor pointers are DEVICE pointers unless the
+ *    argument says "host".  The caller owns every buffer, including
+ *    workspaces; the library allocates and frees nothing on the device.
+ *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
+ *    default stream).  Buffers must stay valid until the stream has run the
+ *    work.  Calls on one stream execute in order.
+ *  - Arguments are validated on the host before anything is launched; a bad
+ *    argument returns a negative kvr_status and launches nothing.  A launch
+ *    failure returns KVR_ECUDA.  kvr_last_error() gives a message (thread
+ *    local).  The library never aborts or traps.
+ *  - Values only the device can see (positions, sequence ids, block-table
+ *    entries, ring tags) are checked by the kernels: an access that would
+ *    leave its buffer is skipped, the affected output row is written as
+ *    zeros, and a bit is set in the device status word (kvr_device_status).
+ *  - Positions are 0-based absolute token positions.  Head h of a layer with
+ *    Hq query heads and Hkv KV heads reads KV head h / (Hq / Hkv).
+ *
+ * Head geometry is fixed: Dqk = 192, Dv = 128, rotary dims = 64, W = 128.
+ */
+#ifndef KVRING_H
+#define KVRING_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t kvr_bf16;
+typedef int kvr_status;
+
+enum {
+  KVR_OK = 0,
+  KVR_EINVAL = -1,       /* null pointer, bad size, Hq not a multiple of Hkv, wrong layout kind */
+  KVR_ERANGE = -2,       /* a host-known position or length past the RoPE table or the pool */
+  KVR_EWORKSPACE = -3,   /* workspace missing or smaller than the size query returned */
+  KVR_EUNSUPPORTED = -4, /* a shape this build does not handle (e.g. Hq/Hkv > 16) */
+  KVR_ECUDA = -5         /* a CUDA runtime call or launch failed */
+};
+
+#define KVR_DQK 192
+#define KVR_DV 128
+#define KVR_DROT 64
+#define KVR_WINDOW 128
+
+/* Device status bits (kvr_device_status). */
+#define KVR_DEV_BAD_POS 1u    /* a position < 0 or >= the RoPE table length */
+#define KVR_DEV_BAD_SEQ 2u    /* a sequence id outside the layout */
+#define KVR_DEV_BAD_BLOCK 4u  /* a block-table entry outside the pool, or a context past the table */
+
+/* KV storage kinds. */
+enum {
+  KVR_LAYOUT_RING = 1,   /* SWA pool: one ring of 128 slots per (sequence, KV head) */
+  KVR_LAYOUT_PAGED = 2,  /* Full pool: pages of block_size positions per KV head */
+  KVR_LAYOUT_LINEAR = 3  /* staging: rows in call order (a prefill chunk) */
+};
+
+/*
+ * Where one layer's K/V live.
+ *
+ * RING   (colibri "System One mode and prompt reuse": position p sits in slot
+ *        p mod 128, and the ring records the position each slot holds):
+ *        k [num_seqs][Hkv][128][192], v [num_seqs][Hkv][128][128],
+ *        slot_pos [num_seqs][128] int32, -1 = empty.  slot_pos is shared by
+ *        the KV heads of a sequence and is written by kv_ring_append_rope.
+ * PAGED  (the Full KV pool of Xiaomi section 2.1, grown on demand):
+ *        k [num_blocks][Hkv][block_size][192], v [num_blocks][Hkv][block_size][128],
+ *        block_table [num_seqs][max_blocks] int32: position p of sequence s is
+ *        row p % block_size of block block_table[s][p / block_size].
+ *        block_size is a multiple of 16 in [16, 1024].
+ * LINEAR k [num_rows][Hkv][192], v [num_rows][Hkv][128]; row r of a call is
+ *        the r-th token of that call.
+ *
+ * Fields a kind does not use are ignored.  The struct itself is host memory
+ * read during the call only.
+ */
+typedef struct kvr_kv_layout {
+  int32_t kind;
+  int32_t num_kv_heads;
+  kvr_bf16 *k;
+  kvr_bf16 *v;
+  int32_t *slot_pos;           /* RING */
+  const int32_t *block_table;  /* PAGED */
+  int32_t num_seqs;            /* RING, PAGED */
+  int32_t max_blocks;          /* PAGED */
+  int32_t block_size;          /* PAGED */
+  int32_t num_blocks;          /* PAGED */
+  int64_t num_rows;            /* LINEAR */
+} kvr_kv_layout;
+
+/* Message for the last failing call on this thread ("" if none). */
+const char *kvr_last_error(void);
+
+/*
+ * Read the device status word of the current device into *flags (host) and,
+ * if reset != 0, clear it.  Synchronises the device.  Returns KVR_OK or
+ * KVR_ECUDA.
+ */
+kvr_status kvr_device_status(uint32_t *flags, int reset);
+
+/*
+ * RoPE cos/sin table, computed on the host in fp64 and stored as fp32
+ * (gaudi-cookbook "The RoPE fix for large positions": a table built with
+ * fp32 cos/sin goes wrong past about 1.5e5 radians, so it is built on the CPU
+ * in float64).
+ *   host_out [max_pos][32][2] fp32 host memory: host_out[p][i] =
+ *   (cos, sin)(p * theta^(-2i/64)).  Copy it to the device once per theta.
+ * nthreads <= 0 uses the hardware concurrency.  KVR_EINVAL on a null
+ * pointer, max_pos <= 0 or theta <= 1.
+ */
+kvr_status kvr_rope_table_build(double theta, int64_t max_pos, float *host_out, int nthreads);
+
+/*
+ * Fused KV write (colibri "What the engine implements": partial rotate-half
+ * RoPE on the first 64 dims; values multiplied by attention_value_scale).
+ * For each token t and KV head h:
+ *   k'[0:32]  = k[0:32]*c - k[32:64]*s,  k'[32:64] = k[32:64]*c + k[0:32]*s
+ *   (c, s) = rope_cos_sin[pos[t]][i]; k'[64:192] = k[64:192] (bit copy);
+ *   v' = v * value_scale;  fp32 arithmetic, one round-to-nearest-even to bf16.
+ * and writes them to `dst`:
+ *   RING   slot pos[t] % 128 of sequence seq[t], and slot_pos[seq][slot] = pos[t];
+ *   PAGED  row pos[t] % block_size of block block_table[seq[t]][pos[t]/block_size];
+ *   LINEAR row t (seq may be NULL; dst->num_rows >= T).
+ * k [T][Hkv][192], v [T][Hkv][128] bf16; pos [T] int64; seq [T] int32.
+ * rope_cos_sin [max_pos][32][2] fp32 (kvr_rope_table_build).  Hkv must equal
+ * dst->num_kv_heads.  For RING, two tokens of one call must not map to the
+ * same (sequence, slot); which one lands is then unspecified.  T = 0 is a
+ * no-op.
+ */
+kvr_status kv_ring_append_rope(const kvr_bf16 *k, const kvr_bf16 *v, const int64_t *pos,
+                               const int32_t *seq, int32_t T, int32_t Hkv,
+                               const float *rope_cos_sin, int64_t max_pos, float value_scale,
+                               const kvr_kv_layout *dst, void *stream);
+
+/*
+ * Decode over a windowed layer (colibri "What the engine implements": the
+ * sink joins the softmax denominator and nothing else; gaudi-cookbook "What
+ * was built": the window is exactly the last 128 positions).  For sequence
+ * b at position p = pos[b] (whose K/V were already appended) and q head h:
+ *   s_j = (rope(q)[h] . k'_j) * softmax_scale over ring slots j with
+ *         p - 128 < slot_pos[seq[b]][j] <= p,
+ *   out[b][h] = sum_j e^{s_j - m} v'_j / (e^{sinks[h] - m} + sum_j e^{s_j - m}).
+ * q [B][Hq][192] bf16 un-rotated (rotated here with rope_cos_sin row p and
+ * rounded to bf16); ring: a RING layout; sinks [Hq] fp32 (raw logits, not
+ * multiplied by softmax_scale); out [B][Hq][128] bf16.  Hq/Hkv <= 16.
+ * The sink is counted once, in the final normalisation.
+ */
+kvr_status swa_sink_decode(const kvr_bf16 *q, const int64_t *pos, const int32_t *seq, int32_t B,
+                           int32_t Hq, const kvr_kv_layout *ring, const float *sinks,
+                           const float *rope_cos_sin, int64_t max_pos, float softmax_scale,
+                           kvr_bf16 *out, void *stream);
+
+/*
+ * Workspace bytes full_attn_decode needs for B sequences whose contexts
+ * (pos + 1) are at most max_ctx.  Returns 0 on bad arguments.
+ */
+size_t full_attn_decode_workspace_size(int32_t B, int32_t Hq, int32_t Hkv, int64_t max_ctx);
+
+/*
+ * Decode over a full-attention layer: causal attention of the token at
+ * p = pos[b] over positions 0..p of the paged pool, no sink.  Split-K
+ * (flash-decode): the context is cut into splits that run in parallel and
+ * write (max, denominator, numerator) partials to the workspace; a second
+ * kernel merges them by log-sum-exp (Xiaomi section 1.2: decode is
+ * memory-bound, its time set by the KV bytes read).
+ * q [B][Hq][192] bf16 un-rotated; pool: a PAGED layout; out [B][Hq][128] bf16.
+ * Every pos[b] + 1 must be <= max_ctx (else the row is zeroed and
+ * KVR_DEV_BAD_POS set); max_ctx <= max_pos and <= max_blocks*block_size.
+ * workspace: device memory of at least
+ * full_attn_decode_workspace_size(B, Hq, Hkv, max_ctx) bytes, 256-byte
+ * aligned, used as scratch; its contents need no initialisation.
+ */
+kvr_status full_attn_decode(const kvr_bf16 *q, const int64_t *pos, const int32_t *seq, int32_t B,
+                            int32_t Hq, const kvr_kv_layout *pool, const float *rope_cos_sin,
+                            int64_t max_pos, float softmax_scale, int64_t max_ctx,
+                            void *workspace, size_t workspace_bytes, kvr_bf16 *out, void *stream);
+
+/*
+ * Chunked prefill over a windowed layer (gaudi-cookbook "What was built":
+ * banded tiles with an fp32 softmax that includes the sink).  Row i of the
+ * chunk is position P0 + i of sequence `seq`; it attends positions
+ * (P0 + i - 128, P0 + i]: those below P0 from the ring (its state before the
+ * chunk, slot tags checked), those from P0 on from chunk_kv row (pos - P0).
+ * The softmax starts from the sink, so the sink joins the denominator only.
+ * q [C][Hq][192] bf16 un-rotated; chunk_kv: LINEAR, num_rows >= C, holding
+ * this chunk's K/V as written by kv_ring_append_rope; ring: RING;
+ * out [C][Hq][128] bf16.  Afterwards the caller appends the chunk's last
+ * min(C, 128) tokens to the ring.
+ */
+kvr_status swa_sink_prefill_chunk(const kvr_bf16 *q, int64_t P0, int32_t C, int32_t seq, int32_t Hq,
+                                  const kvr_kv_layout *chunk_kv, const kvr_kv_layout *ring,
+                                  const float *sinks, const float *rope_cos_sin, int64_t max_pos,
+                                  float softmax_scale, kvr_bf16 *out, void *stream);
+
+/*
+ * Chunked prefill over a full-attention layer (gaudi-cookbook "Tiled
+ * global-attention prefill": softmax is per query row, so query tiles need no
+ * merge).  Row i of the chunk is position P0 + i of sequence `seq` and
+ * attends positions 0..P0 + i of the paged pool, into which the chunk's own
+ * K/V were already appended.  No sink.
+ * q [C][Hq][192] bf16 un-rotated; pool: PAGED; out [C][Hq][128] bf16.
+ * P0 + C <= max_pos and <= max_blocks*block_size.
+ */
+kvr_status full_attn_prefill_chunk(const kvr_bf16 *q, int64_t P0, int32_t C, int32_t seq, int32_t Hq,
+                                   const kvr_kv_layout *pool, const float *rope_cos_sin,
+                                   int64_t max_pos, float softmax_scale, kvr_bf16 *out,
+                                   void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVRING_H */

@@ -1,0 +1,311 @@
+"""Hybrid-SWA attention with sinks over a ring KV cache, for GB300 (sm_103a).
+
+Thin Python binding over the C ABI of ``libkvring.so`` (``include/kvring.h``).
+It only marshals arguments: every step of the attention path runs in the
+library's CUDA kernels.  PyTorch supplies device memory and streams.  There
+is no fallback: if the library is missing, every call raises.
+
+The five calls (colibri "MiMo-V2.6", "What the engine implements";
+gaudi-cookbook "MiMo-V2.6-Flash on Gaudi 2", "What was built"):
+
+  kv_ring_append_rope     RoPE k (dims 0..63), scale v, write ring / pages / rows
+  swa_sink_decode         one token over a 128-slot ring with a per-head sink
+  full_attn_decode        one token over a paged pool, split-K + LSE combine
+  swa_sink_prefill_chunk  a chunk over ring + chunk rows, sink in the softmax
+  full_attn_prefill_chunk a chunk over a paged pool, causal
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+__all__ = [
+    "KvrError", "RingLayout", "PagedLayout", "LinearLayout", "lib", "rope_table",
+    "kv_ring_append_rope", "swa_sink_decode", "full_attn_decode", "full_attn_decode_workspace_size",
+    "swa_sink_prefill_chunk", "full_attn_prefill_chunk", "device_status",
+    "DQK", "DV", "DROT", "WINDOW",
+]
+
+DQK, DV, DROT, WINDOW = 192, 128, 64, 128
+LAYOUT_RING, LAYOUT_PAGED, LAYOUT_LINEAR = 1, 2, 3
+DEV_BAD_POS, DEV_BAD_SEQ, DEV_BAD_BLOCK = 1, 2, 4
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libkvring.so")
+_lib = None
+_lock = threading.Lock()
+
+
+class KvrError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"kvring error {code}: {msg}")
+        self.code = code
+
+
+class _Layout(ctypes.Structure):
+    _fields_ = [
+        ("kind", ctypes.c_int32),
+        ("num_kv_heads", ctypes.c_int32),
+        ("k", ctypes.c_void_p),
+        ("v", ctypes.c_void_p),
+        ("slot_pos", ctypes.c_void_p),
+        ("block_table", ctypes.c_void_p),
+        ("num_seqs", ctypes.c_int32),
+        ("max_blocks", ctypes.c_int32),
+        ("block_size", ctypes.c_int32),
+        ("num_blocks", ctypes.c_int32),
+        ("num_rows", ctypes.c_int64),
+    ]
+
+
+def lib():
+    """The loaded libkvring.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        with _lock:
+            if _lib is None:
+                if not os.path.exists(LIB_PATH):
+                    raise ImportError(f"{LIB_PATH} is missing: build it with sinks_kv_ring_gb300.build.build()")
+                L = ctypes.CDLL(LIB_PATH)
+                p, i32, i64, f32, f64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_double
+                L.kvr_last_error.restype = ctypes.c_char_p
+                L.kvr_last_error.argtypes = []
+                L.kvr_device_status.restype = ctypes.c_int
+                L.kvr_device_status.argtypes = [p, ctypes.c_int]
+                L.kvr_rope_table_build.restype = ctypes.c_int
+                L.kvr_rope_table_build.argtypes = [f64, i64, p, ctypes.c_int]
+                L.kv_ring_append_rope.restype = ctypes.c_int
+                L.kv_ring_append_rope.argtypes = [p, p, p, p, i32, i32, p, i64, f32, p, p]
+                L.swa_sink_decode.restype = ctypes.c_int
+                L.swa_sink_decode.argtypes = [p, p, p, i32, i32, p, p, p, i64, f32, p, p]
+                L.full_attn_decode_workspace_size.restype = ctypes.c_size_t
+                L.full_attn_decode_workspace_size.argtypes = [i32, i32, i32, i64]
+                L.full_attn_decode.restype = ctypes.c_int
+                L.full_attn_decode.argtypes = [p, p, p, i32, i32, p, p, i64, f32, i64, p, ctypes.c_size_t, p, p]
+                L.swa_sink_prefill_chunk.restype = ctypes.c_int
+                L.swa_sink_prefill_chunk.argtypes = [p, i64, i32, i32, i32, p, p, p, p, i64, f32, p, p]
+                L.full_attn_prefill_chunk.restype = ctypes.c_int
+                L.full_attn_prefill_chunk.argtypes = [p, i64, i32, i32, i32, p, p, i64, f32, p, p]
+                _lib = L
+    return _lib
+
+
+def _check(rc: int):
+    if rc != 0:
+        raise KvrError(rc, lib().kvr_last_error().decode())
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _want(t, name, dtype, dim=None, cuda=True):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if dim is not None and t.dim() != dim:
+        raise ValueError(f"{name} must have {dim} dims, got shape {tuple(t.shape)}")
+    if cuda and not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+class RingLayout:
+    """SWA pool of one layer: k [S, Hkv, 128, 192], v [S, Hkv, 128, 128] bf16,
+    slot_pos [S, 128] int32 (-1 = empty)."""
+
+    def __init__(self, k, v, slot_pos):
+        _want(k, "ring.k", torch.bfloat16, 4)
+        _want(v, "ring.v", torch.bfloat16, 4)
+        _want(slot_pos, "ring.slot_pos", torch.int32, 2)
+        S, H, W, D = k.shape
+        if W != WINDOW or D != DQK or tuple(v.shape) != (S, H, WINDOW, DV) or tuple(slot_pos.shape) != (S, WINDOW):
+            raise ValueError("ring tensors have inconsistent shapes")
+        self.k, self.v, self.slot_pos = k, v, slot_pos
+        self.num_seqs, self.num_kv_heads = S, H
+
+    @classmethod
+    def empty(cls, num_seqs, num_kv_heads, device="cuda"):
+        k = torch.zeros(num_seqs, num_kv_heads, WINDOW, DQK, dtype=torch.bfloat16, device=device)
+        v = torch.zeros(num_seqs, num_kv_heads, WINDOW, DV, dtype=torch.bfloat16, device=device)
+        sp = torch.full((num_seqs, WINDOW), -1, dtype=torch.int32, device=device)
+        return cls(k, v, sp)
+
+    @staticmethod
+    def bytes_per_layer(num_seqs, num_kv_heads, elem_bytes=2):
+        """Ring K+V bytes of one layer (slot tags not counted)."""
+        return num_seqs * num_kv_heads * WINDOW * (DQK + DV) * elem_bytes
+
+    def c(self):
+        return _Layout(LAYOUT_RING, self.num_kv_heads, self.k.data_ptr(), self.v.data_ptr(),
+                       self.slot_pos.data_ptr(), None, self.num_seqs, 0, 0, 0, 0)
+
+
+class PagedLayout:
+    """Full pool of one layer: k [nblk, Hkv, Bsz, 192], v [nblk, Hkv, Bsz, 128]
+    bf16, block_table [S, max_blocks] int32."""
+
+    def __init__(self, k, v, block_table):
+        _want(k, "pool.k", torch.bfloat16, 4)
+        _want(v, "pool.v", torch.bfloat16, 4)
+        _want(block_table, "pool.block_table", torch.int32, 2)
+        nb, H, bsz, D = k.shape
+        if D != DQK or tuple(v.shape) != (nb, H, bsz, DV):
+            raise ValueError("pool tensors have inconsistent shapes")
+        self.k, self.v, self.block_table = k, v, block_table
+        self.num_blocks, self.num_kv_heads, self.block_size = nb, H, bsz
+        self.num_seqs, self.max_blocks = block_table.shape
+
+    @classmethod
+    def contiguous(cls, num_seqs, num_kv_heads, max_ctx, block_size=64, device="cuda", zero=True):
+        """A pool where sequence s owns blocks s*mb .. s*mb+mb-1 in order."""
+        mb = (max_ctx + block_size - 1) // block_size
+        nb = num_seqs * mb
+        alloc = torch.zeros if zero else torch.empty
+        k = alloc(nb, num_kv_heads, block_size, DQK, dtype=torch.bfloat16, device=device)
+        v = alloc(nb, num_kv_heads, block_size, DV, dtype=torch.bfloat16, device=device)
+        bt = torch.arange(nb, dtype=torch.int32, device=device).reshape(num_seqs, mb)
+        return cls(k, v, bt)
+
+    @staticmethod
+    def bytes_per_token(num_kv_heads, elem_bytes=2, v_width=DV):
+        """Pool K+V bytes one token adds per layer (v_width=192 models V zero-padded to 192)."""
+        return num_kv_heads * (DQK + v_width) * elem_bytes
+
+    def c(self):
+        return _Layout(LAYOUT_PAGED, self.num_kv_heads, self.k.data_ptr(), self.v.data_ptr(), None,
+                       self.block_table.data_ptr(), self.num_seqs, self.max_blocks, self.block_size,
+                       self.num_blocks, 0)
+
+
+class LinearLayout:
+    """Staging rows: k [T, Hkv, 192], v [T, Hkv, 128] bf16."""
+
+    def __init__(self, k, v):
+        _want(k, "linear.k", torch.bfloat16, 3)
+        _want(v, "linear.v", torch.bfloat16, 3)
+        T, H, D = k.shape
+        if D != DQK or tuple(v.shape) != (T, H, DV):
+            raise ValueError("linear tensors have inconsistent shapes")
+        self.k, self.v = k, v
+        self.num_rows, self.num_kv_heads = T, H
+
+    @classmethod
+    def empty(cls, rows, num_kv_heads, device="cuda"):
+        return cls(torch.empty(rows, num_kv_heads, DQK, dtype=torch.bfloat16, device=device),
+                   torch.empty(rows, num_kv_heads, DV, dtype=torch.bfloat16, device=device))
+
+    def c(self):
+        return _Layout(LAYOUT_LINEAR, self.num_kv_heads, self.k.data_ptr(), self.v.data_ptr(), None, None,
+                       0, 0, 0, 0, self.num_rows)
+
+
+def rope_table(theta: float, max_pos: int, device="cuda", nthreads: int = 0) -> torch.Tensor:
+    """[max_pos, 32, 2] fp32 (cos, sin) table, evaluated on the host in fp64
+    by the library, then copied to `device`."""
+    host = torch.empty((max_pos, 32, 2), dtype=torch.float32)
+    _check(lib().kvr_rope_table_build(float(theta), int(max_pos), _ptr(host), int(nthreads)))
+    return host if str(device) == "cpu" else host.to(device)
+
+
+def kv_ring_append_rope(k, v, pos, seq, table, value_scale, dst, stream=None):
+    _want(k, "k", torch.bfloat16, 3)
+    _want(v, "v", torch.bfloat16, 3)
+    _want(pos, "pos", torch.int64, 1)
+    if seq is not None:
+        _want(seq, "seq", torch.int32, 1)
+    _want(table, "table", torch.float32, 3)
+    T, H = k.shape[0], k.shape[1]
+    if tuple(k.shape) != (T, H, DQK) or tuple(v.shape) != (T, H, DV) or pos.shape[0] != T:
+        raise ValueError("k/v/pos shapes disagree")
+    if seq is not None and seq.shape[0] != T:
+        raise ValueError("seq shape disagrees")
+    c = dst.c()
+    _check(lib().kv_ring_append_rope(_ptr(k), _ptr(v), _ptr(pos), _ptr(seq), T, H, _ptr(table),
+                                     table.shape[0], float(value_scale), ctypes.byref(c), _stream(stream)))
+
+
+def swa_sink_decode(q, pos, seq, ring, sinks, table, softmax_scale, out=None, stream=None):
+    _want(q, "q", torch.bfloat16, 3)
+    _want(pos, "pos", torch.int64, 1)
+    _want(seq, "seq", torch.int32, 1)
+    _want(sinks, "sinks", torch.float32, 1)
+    _want(table, "table", torch.float32, 3)
+    B, Hq, _ = q.shape
+    if out is None:
+        out = torch.empty(B, Hq, DV, dtype=torch.bfloat16, device=q.device)
+    _want(out, "out", torch.bfloat16, 3)
+    c = ring.c()
+    _check(lib().swa_sink_decode(_ptr(q), _ptr(pos), _ptr(seq), B, Hq, ctypes.byref(c), _ptr(sinks),
+                                 _ptr(table), table.shape[0], float(softmax_scale), _ptr(out), _stream(stream)))
+    return out
+
+
+def full_attn_decode_workspace_size(B, Hq, Hkv, max_ctx) -> int:
+    return int(lib().full_attn_decode_workspace_size(int(B), int(Hq), int(Hkv), int(max_ctx)))
+
+
+def full_attn_decode(q, pos, seq, pool, table, softmax_scale, max_ctx, workspace=None, out=None, stream=None):
+    _want(q, "q", torch.bfloat16, 3)
+    _want(pos, "pos", torch.int64, 1)
+    _want(seq, "seq", torch.int32, 1)
+    _want(table, "table", torch.float32, 3)
+    B, Hq, _ = q.shape
+    if workspace is None:
+        n = full_attn_decode_workspace_size(B, Hq, pool.num_kv_heads, max_ctx)
+        workspace = torch.empty(max(n, 1), dtype=torch.uint8, device=q.device)
+    _want(workspace, "workspace", torch.uint8, 1)
+    if out is None:
+        out = torch.empty(B, Hq, DV, dtype=torch.bfloat16, device=q.device)
+    _want(out, "out", torch.bfloat16, 3)
+    c = pool.c()
+    _check(lib().full_attn_decode(_ptr(q), _ptr(pos), _ptr(seq), B, Hq, ctypes.byref(c), _ptr(table),
+                                  table.shape[0], float(softmax_scale), int(max_ctx), _ptr(workspace),
+                                  workspace.numel(), _ptr(out), _stream(stream)))
+    return out
+
+
+def swa_sink_prefill_chunk(q, P0, seq, chunk_kv, ring, sinks, table, softmax_scale, out=None, stream=None):
+    _want(q, "q", torch.bfloat16, 3)
+    _want(sinks, "sinks", torch.float32, 1)
+    _want(table, "table", torch.float32, 3)
+    C, Hq, _ = q.shape
+    if out is None:
+        out = torch.empty(C, Hq, DV, dtype=torch.bfloat16, device=q.device)
+    _want(out, "out", torch.bfloat16, 3)
+    cc, rc = chunk_kv.c(), ring.c()
+    _check(lib().swa_sink_prefill_chunk(_ptr(q), int(P0), C, int(seq), Hq, ctypes.byref(cc), ctypes.byref(rc),
+                                        _ptr(sinks), _ptr(table), table.shape[0], float(softmax_scale), _ptr(out),
+                                        _stream(stream)))
+    return out
+
+
+def full_attn_prefill_chunk(q, P0, seq, pool, table, softmax_scale, out=None, stream=None):
+    _want(q, "q", torch.bfloat16, 3)
+    _want(table, "table", torch.float32, 3)
+    C, Hq, _ = q.shape
+    if out is None:
+        out = torch.empty(C, Hq, DV, dtype=torch.bfloat16, device=q.device)
+    _want(out, "out", torch.bfloat16, 3)
+    c = pool.c()
+    _check(lib().full_attn_prefill_chunk(_ptr(q), int(P0), C, int(seq), Hq, ctypes.byref(c), _ptr(table),
+                                         table.shape[0], float(softmax_scale), _ptr(out), _stream(stream)))
+    return out
+
+
+def device_status(reset: bool = True) -> int:
+    """Device status bits (DEV_BAD_POS | DEV_BAD_SEQ | DEV_BAD_BLOCK); synchronises."""
+    flags = ctypes.c_uint32(0)
+    _check(lib().kvr_device_status(ctypes.byref(flags), 1 if reset else 0))
+    return int(flags.value)

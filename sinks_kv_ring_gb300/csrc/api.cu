@@ -1,0 +1,299 @@
+// api.cu -- the C ABI declared in include/kvring.h: host-side validation of
+// every argument the host can see, then the kernel launches.  Nothing here
+// allocates device memory.
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "../../include/kvring.h"
+#include "launch.h"
+
+namespace kvr {
+void rope_table_fill(double theta, int64_t max_pos, float *out, int nthreads);
+}
+
+namespace {
+
+thread_local std::string g_err;
+
+kvr_status fail(kvr_status code, const char *fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_err = buf;
+  return code;
+}
+
+kvr_status ok() {
+  g_err.clear();
+  return KVR_OK;
+}
+
+kvr_status cuda_fail(cudaError_t e, const char *what) {
+  return fail(KVR_ECUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+// Device status word, one per device that loads the library.
+__device__ unsigned int g_status_word;
+
+constexpr int MAX_DEV = 64;
+std::mutex g_mu;
+unsigned *g_status_ptr[MAX_DEV];
+int g_sms[MAX_DEV];
+
+// Device address of the status word on the current device (host code may
+// not use the symbol itself as an address).
+cudaError_t status_ptr(unsigned **out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= MAX_DEV) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_status_ptr[dev]) {
+    void *p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_status_word);
+    if (e != cudaSuccess) return e;
+    g_status_ptr[dev] = static_cast<unsigned *>(p);
+  }
+  *out = g_status_ptr[dev];
+  return cudaSuccess;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+kvr::KvView view(const kvr_kv_layout &L) {
+  kvr::KvView v;
+  v.kind = L.kind;
+  v.hkv = L.num_kv_heads;
+  v.k = L.k;
+  v.v = L.v;
+  v.slot_pos = L.slot_pos;
+  v.block_table = L.block_table;
+  v.num_seqs = L.num_seqs;
+  v.max_blocks = L.max_blocks;
+  v.block_size = L.block_size;
+  v.num_blocks = L.num_blocks;
+  v.num_rows = L.num_rows;
+  return v;
+}
+
+kvr_status check_layout(const kvr_kv_layout *L, int want_kind, const char *name) {
+  if (!L) return fail(KVR_EINVAL, "%s: layout is NULL", name);
+  if (want_kind && L->kind != want_kind) return fail(KVR_EINVAL, "%s: layout kind %d, expected %d", name, L->kind, want_kind);
+  if (L->num_kv_heads < 1) return fail(KVR_EINVAL, "%s: num_kv_heads %d", name, L->num_kv_heads);
+  if (!L->k || !L->v) return fail(KVR_EINVAL, "%s: k/v pointer is NULL", name);
+  if (!aligned16(L->k) || !aligned16(L->v)) return fail(KVR_EINVAL, "%s: k/v not 16-byte aligned", name);
+  switch (L->kind) {
+    case KVR_LAYOUT_RING:
+      if (!L->slot_pos) return fail(KVR_EINVAL, "%s: ring slot_pos is NULL", name);
+      if (L->num_seqs < 1) return fail(KVR_EINVAL, "%s: num_seqs %d", name, L->num_seqs);
+      break;
+    case KVR_LAYOUT_PAGED:
+      if (!L->block_table) return fail(KVR_EINVAL, "%s: block_table is NULL", name);
+      if (L->num_seqs < 1 || L->max_blocks < 1 || L->num_blocks < 1)
+        return fail(KVR_EINVAL, "%s: num_seqs/max_blocks/num_blocks must be >= 1", name);
+      if (L->block_size < 16 || L->block_size > 1024 || L->block_size % 16)
+        return fail(KVR_EUNSUPPORTED, "%s: block_size %d (needs a multiple of 16 in [16, 1024])", name, L->block_size);
+      break;
+    case KVR_LAYOUT_LINEAR:
+      if (L->num_rows < 0) return fail(KVR_EINVAL, "%s: num_rows %lld", name, (long long)L->num_rows);
+      break;
+    default:
+      return fail(KVR_EINVAL, "%s: unknown layout kind %d", name, L->kind);
+  }
+  return KVR_OK;
+}
+
+kvr_status check_table(const float *table, int64_t max_pos) {
+  if (!table) return fail(KVR_EINVAL, "rope_cos_sin is NULL");
+  if (!aligned16(table)) return fail(KVR_EINVAL, "rope_cos_sin not 16-byte aligned");
+  if (max_pos < 1 || max_pos > INT32_MAX) return fail(KVR_ERANGE, "max_pos %lld outside [1, 2^31)", (long long)max_pos);
+  return KVR_OK;
+}
+
+kvr_status check_heads(int32_t Hq, int32_t Hkv, int max_group) {
+  if (Hq < 1 || Hkv < 1 || Hq % Hkv) return fail(KVR_EINVAL, "Hq %d is not a positive multiple of Hkv %d", Hq, Hkv);
+  if (max_group && Hq / Hkv > max_group)
+    return fail(KVR_EUNSUPPORTED, "Hq/Hkv = %d; this call handles at most %d query heads per KV head", Hq / Hkv, max_group);
+  return KVR_OK;
+}
+
+cudaStream_t as_stream(void *s) { return static_cast<cudaStream_t>(s); }
+
+}  // namespace
+
+namespace kvr {
+int num_sms() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEV) return 152;
+  if (!g_sms[dev]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1) n = 152;
+    g_sms[dev] = n;
+  }
+  return g_sms[dev];
+}
+}  // namespace kvr
+
+extern "C" {
+
+const char *kvr_last_error(void) { return g_err.c_str(); }
+
+kvr_status kvr_device_status(uint32_t *flags, int reset) {
+  if (!flags) return fail(KVR_EINVAL, "flags is NULL");
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_fail(e, "kvr_device_status");
+  unsigned v = 0;
+  e = cudaMemcpyFromSymbol(&v, g_status_word, sizeof v);
+  if (e != cudaSuccess) return cuda_fail(e, "kvr_device_status");
+  *flags = v;
+  if (reset) {
+    const unsigned zero = 0;
+    e = cudaMemcpyToSymbol(g_status_word, &zero, sizeof zero);
+    if (e != cudaSuccess) return cuda_fail(e, "kvr_device_status");
+  }
+  return ok();
+}
+
+kvr_status kvr_rope_table_build(double theta, int64_t max_pos, float *host_out, int nthreads) {
+  if (!host_out) return fail(KVR_EINVAL, "host_out is NULL");
+  if (max_pos < 1) return fail(KVR_EINVAL, "max_pos %lld", (long long)max_pos);
+  if (!(theta > 1.0)) return fail(KVR_EINVAL, "theta %g", theta);
+  kvr::rope_table_fill(theta, max_pos, host_out, nthreads);
+  return ok();
+}
+
+kvr_status kv_ring_append_rope(const kvr_bf16 *k, const kvr_bf16 *v, const int64_t *pos, const int32_t *seq,
+                               int32_t T, int32_t Hkv, const float *rope_cos_sin, int64_t max_pos,
+                               float value_scale, const kvr_kv_layout *dst, void *stream) {
+  if (T < 0) return fail(KVR_EINVAL, "T %d", T);
+  kvr_status s = check_layout(dst, 0, "dst");
+  if (s) return s;
+  if (Hkv != dst->num_kv_heads) return fail(KVR_EINVAL, "Hkv %d != dst->num_kv_heads %d", Hkv, dst->num_kv_heads);
+  if ((s = check_table(rope_cos_sin, max_pos))) return s;
+  if (T == 0) return ok();
+  if (!k || !v || !pos) return fail(KVR_EINVAL, "k/v/pos is NULL");
+  if (!aligned16(k) || !aligned16(v)) return fail(KVR_EINVAL, "k/v not 16-byte aligned");
+  if (dst->kind != KVR_LAYOUT_LINEAR && !seq) return fail(KVR_EINVAL, "seq is NULL");
+  if (dst->kind == KVR_LAYOUT_LINEAR && dst->num_rows < T)
+    return fail(KVR_EINVAL, "LINEAR dst has %lld rows, T = %d", (long long)dst->num_rows, T);
+  unsigned *st = nullptr;
+  cudaError_t e = status_ptr(&st);
+  if (e != cudaSuccess) return cuda_fail(e, "kv_ring_append_rope");
+  e = kvr::launch_append(k, v, pos, seq, T, Hkv, rope_cos_sin, max_pos, value_scale, view(*dst), st,
+                         as_stream(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "kv_ring_append_rope launch");
+  return ok();
+}
+
+kvr_status swa_sink_decode(const kvr_bf16 *q, const int64_t *pos, const int32_t *seq, int32_t B, int32_t Hq,
+                           const kvr_kv_layout *ring, const float *sinks, const float *rope_cos_sin,
+                           int64_t max_pos, float softmax_scale, kvr_bf16 *out, void *stream) {
+  if (B < 0) return fail(KVR_EINVAL, "B %d", B);
+  kvr_status s = check_layout(ring, KVR_LAYOUT_RING, "ring");
+  if (s) return s;
+  if ((s = check_heads(Hq, ring->num_kv_heads, 16))) return s;
+  if ((s = check_table(rope_cos_sin, max_pos))) return s;
+  if (B == 0) return ok();
+  if (!q || !pos || !seq || !sinks || !out) return fail(KVR_EINVAL, "q/pos/seq/sinks/out is NULL");
+  if (!aligned16(q) || !aligned16(out)) return fail(KVR_EINVAL, "q/out not 16-byte aligned");
+  unsigned *st = nullptr;
+  cudaError_t e = status_ptr(&st);
+  if (e != cudaSuccess) return cuda_fail(e, "swa_sink_decode");
+  e = kvr::launch_swa_decode(q, pos, seq, B, Hq, view(*ring), sinks, rope_cos_sin, max_pos, softmax_scale, out,
+                             st, as_stream(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "swa_sink_decode launch");
+  return ok();
+}
+
+size_t full_attn_decode_workspace_size(int32_t B, int32_t Hq, int32_t Hkv, int64_t max_ctx) {
+  if (B < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv || max_ctx < 1) return 0;
+  return kvr::full_decode_workspace(B, Hq, Hkv, max_ctx);
+}
+
+kvr_status full_attn_decode(const kvr_bf16 *q, const int64_t *pos, const int32_t *seq, int32_t B, int32_t Hq,
+                            const kvr_kv_layout *pool, const float *rope_cos_sin, int64_t max_pos,
+                            float softmax_scale, int64_t max_ctx, void *workspace, size_t workspace_bytes,
+                            kvr_bf16 *out, void *stream) {
+  if (B < 0) return fail(KVR_EINVAL, "B %d", B);
+  kvr_status s = check_layout(pool, KVR_LAYOUT_PAGED, "pool");
+  if (s) return s;
+  if ((s = check_heads(Hq, pool->num_kv_heads, 16))) return s;
+  if ((s = check_table(rope_cos_sin, max_pos))) return s;
+  if (max_ctx < 1 || max_ctx > max_pos)
+    return fail(KVR_ERANGE, "max_ctx %lld outside [1, max_pos=%lld]", (long long)max_ctx, (long long)max_pos);
+  if (max_ctx > (int64_t)pool->max_blocks * pool->block_size)
+    return fail(KVR_ERANGE, "max_ctx %lld exceeds max_blocks*block_size = %lld", (long long)max_ctx,
+                (long long)pool->max_blocks * pool->block_size);
+  if (B == 0) return ok();
+  if (!q || !pos || !seq || !out) return fail(KVR_EINVAL, "q/pos/seq/out is NULL");
+  if (!aligned16(q) || !aligned16(out)) return fail(KVR_EINVAL, "q/out not 16-byte aligned");
+  const size_t need = kvr::full_decode_workspace(B, Hq, pool->num_kv_heads, max_ctx);
+  if (!workspace || workspace_bytes < need)
+    return fail(KVR_EWORKSPACE, "workspace %zu bytes, need %zu", workspace ? workspace_bytes : (size_t)0, need);
+  if (!aligned16(workspace)) return fail(KVR_EINVAL, "workspace not 16-byte aligned");
+  unsigned *st = nullptr;
+  cudaError_t e = status_ptr(&st);
+  if (e != cudaSuccess) return cuda_fail(e, "full_attn_decode");
+  e = kvr::launch_full_decode(q, pos, seq, B, Hq, view(*pool), rope_cos_sin, max_pos, softmax_scale, max_ctx,
+                              workspace, out, st, as_stream(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "full_attn_decode launch");
+  return ok();
+}
+
+kvr_status swa_sink_prefill_chunk(const kvr_bf16 *q, int64_t P0, int32_t C, int32_t seq, int32_t Hq,
+                                  const kvr_kv_layout *chunk_kv, const kvr_kv_layout *ring, const float *sinks,
+                                  const float *rope_cos_sin, int64_t max_pos, float softmax_scale, kvr_bf16 *out,
+                                  void *stream) {
+  if (C < 0 || P0 < 0) return fail(KVR_EINVAL, "C %d, P0 %lld", C, (long long)P0);
+  kvr_status s = check_layout(ring, KVR_LAYOUT_RING, "ring");
+  if (s) return s;
+  if ((s = check_layout(chunk_kv, KVR_LAYOUT_LINEAR, "chunk_kv"))) return s;
+  if (chunk_kv->num_kv_heads != ring->num_kv_heads)
+    return fail(KVR_EINVAL, "chunk_kv has %d KV heads, ring %d", chunk_kv->num_kv_heads, ring->num_kv_heads);
+  if ((s = check_heads(Hq, ring->num_kv_heads, 0))) return s;
+  if ((s = check_table(rope_cos_sin, max_pos))) return s;
+  if (seq < 0 || seq >= ring->num_seqs) return fail(KVR_EINVAL, "seq %d outside [0, %d)", seq, ring->num_seqs);
+  if (P0 + C > max_pos) return fail(KVR_ERANGE, "P0 + C = %lld > max_pos %lld", (long long)(P0 + C), (long long)max_pos);
+  if (chunk_kv->num_rows < C) return fail(KVR_EINVAL, "chunk_kv has %lld rows, C = %d", (long long)chunk_kv->num_rows, C);
+  if (C == 0) return ok();
+  if (!q || !sinks || !out) return fail(KVR_EINVAL, "q/sinks/out is NULL");
+  if (!aligned16(q) || !aligned16(out)) return fail(KVR_EINVAL, "q/out not 16-byte aligned");
+  unsigned *st = nullptr;
+  cudaError_t e = status_ptr(&st);
+  if (e != cudaSuccess) return cuda_fail(e, "swa_sink_prefill_chunk");
+  e = kvr::launch_swa_prefill(q, P0, C, seq, Hq, view(*chunk_kv), view(*ring), sinks, rope_cos_sin, max_pos,
+                              softmax_scale, out, st, as_stream(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "swa_sink_prefill_chunk launch");
+  return ok();
+}
+
+kvr_status full_attn_prefill_chunk(const kvr_bf16 *q, int64_t P0, int32_t C, int32_t seq, int32_t Hq,
+                                   const kvr_kv_layout *pool, const float *rope_cos_sin, int64_t max_pos,
+                                   float softmax_scale, kvr_bf16 *out, void *stream) {
+  if (C < 0 || P0 < 0) return fail(KVR_EINVAL, "C %d, P0 %lld", C, (long long)P0);
+  kvr_status s = check_layout(pool, KVR_LAYOUT_PAGED, "pool");
+  if (s) return s;
+  if ((s = check_heads(Hq, pool->num_kv_heads, 0))) return s;
+  if ((s = check_table(rope_cos_sin, max_pos))) return s;
+  if (seq < 0 || seq >= pool->num_seqs) return fail(KVR_EINVAL, "seq %d outside [0, %d)", seq, pool->num_seqs);
+  if (P0 + C > max_pos) return fail(KVR_ERANGE, "P0 + C = %lld > max_pos %lld", (long long)(P0 + C), (long long)max_pos);
+  if (P0 + C > (int64_t)pool->max_blocks * pool->block_size)
+    return fail(KVR_ERANGE, "P0 + C = %lld exceeds max_blocks*block_size", (long long)(P0 + C));
+  if (C == 0) return ok();
+  if (!q || !out) return fail(KVR_EINVAL, "q/out is NULL");
+  if (!aligned16(q) || !aligned16(out)) return fail(KVR_EINVAL, "q/out not 16-byte aligned");
+  unsigned *st = nullptr;
+  cudaError_t e = status_ptr(&st);
+  if (e != cudaSuccess) return cuda_fail(e, "full_attn_prefill_chunk");
+  e = kvr::launch_full_prefill(q, P0, C, seq, Hq, view(*pool), rope_cos_sin, max_pos, softmax_scale, out, st,
+                               as_stream(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "full_attn_prefill_chunk launch");
+  return ok();
+}
+
+}  // extern "C"

@@ -1,0 +1,46 @@
+// launch.h -- internal launchers called by the C ABI (api.cu) after it has
+// validated every host-visible argument.  Each returns the cudaError_t of its
+// launch.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+
+namespace kvr {
+
+cudaError_t launch_append(const uint16_t *k, const uint16_t *v, const int64_t *pos, const int32_t *seq,
+                          int T, int hkv, const float *table, int64_t max_pos, float value_scale,
+                          const KvView &dst, unsigned *status, cudaStream_t st);
+
+cudaError_t launch_swa_decode(const uint16_t *q, const int64_t *pos, const int32_t *seq, int B, int hq,
+                              const KvView &ring, const float *sinks, const float *table,
+                              int64_t max_pos, float softmax_scale, uint16_t *out, unsigned *status,
+                              cudaStream_t st);
+
+// Split plan of the full-attention decode: contexts up to max_ctx are cut
+// into at most `splits` pieces of `split_len` keys (a multiple of 64).
+struct DecodePlan {
+  int splits;
+  int split_len;
+};
+DecodePlan full_decode_plan(int B, int hkv, long long max_ctx);
+size_t full_decode_workspace(int B, int hq, int hkv, long long max_ctx);
+
+cudaError_t launch_full_decode(const uint16_t *q, const int64_t *pos, const int32_t *seq, int B, int hq,
+                               const KvView &pool, const float *table, int64_t max_pos,
+                               float softmax_scale, long long max_ctx, void *ws, uint16_t *out,
+                               unsigned *status, cudaStream_t st);
+
+cudaError_t launch_full_prefill(const uint16_t *q, int64_t P0, int C, int seq, int hq, const KvView &pool,
+                                const float *table, int64_t max_pos, float softmax_scale, uint16_t *out,
+                                unsigned *status, cudaStream_t st);
+
+cudaError_t launch_swa_prefill(const uint16_t *q, int64_t P0, int C, int seq, int hq, const KvView &chunk,
+                               const KvView &ring, const float *sinks, const float *table,
+                               int64_t max_pos, float softmax_scale, uint16_t *out, unsigned *status,
+                               cudaStream_t st);
+
+int num_sms();
+
+}  // namespace kvr
