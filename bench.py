@@ -312,11 +312,12 @@ class PrefillWorkload:
 
 # --------------------------------------------------------------------------- runs
 
-def timed_run(work, steps, warmup, stream, flush=None):
+def timed_run(work, steps, warmup, stream, flush=None, label="timed"):
     for _ in range(warmup):
         work.step(stream)
     torch.cuda.synchronize()
     ev = []
+    torch.cuda.nvtx.range_push(label)
     for _ in range(steps):
         if flush is not None:
             flush_l2(flush)
@@ -327,6 +328,7 @@ def timed_run(work, steps, warmup, stream, flush=None):
         b.record(stream)
         ev.append((a, b))
     torch.cuda.synchronize()
+    torch.cuda.nvtx.range_pop()
     return sum(a.elapsed_time(b) for a, b in ev) / len(ev)
 
 
@@ -360,8 +362,8 @@ def e2e_decode(work, steps, warmup, stream):
 
 def cpu_baseline_decode(work, budget_s=12.0, max_seqs=16):
     """The fp64 oracle on sampled sequences of the decode workload (both layers,
-    all heads), on all host cores; tokens/s."""
-    import numpy as np
+    all heads), on all host cores; tokens/s.  Sequences are taken in turn
+    (cycling over the first max_seqs) until budget_s of oracle time is spent."""
     import oracle
     from sinks_kv_ring_gb300.synth import Synth
     cores = os.cpu_count() or 1
@@ -369,31 +371,38 @@ def cpu_baseline_decode(work, budget_s=12.0, max_seqs=16):
     q_s, q_f = work.q_swa.cpu(), work.q_full.cpu()
     sk = work.sinks.double().cpu().numpy()
     p = work.p
+    lo = max(0, p - 127)
+    cache = {}
+
+    def inputs(b):
+        if b not in cache:
+            kf = torch.cat([syn_f.k(min(65536, p - s0), work.hkv_full, seq=b, start=s0) for s0 in range(0, p, 65536)]
+                           + [work.k_full[b:b + 1]]).cpu()
+            vf = torch.cat([syn_f.v(min(65536, p - s0), work.hkv_full, seq=b, start=s0) for s0 in range(0, p, 65536)]
+                           + [work.v_full[b:b + 1]]).cpu()
+            ks = torch.cat([syn_s.k(p - lo, work.hkv_swa, seq=b, start=lo), work.k_swa[b:b + 1]]).cpu()
+            vs = torch.cat([syn_s.v(p - lo, work.hkv_swa, seq=b, start=lo), work.v_swa[b:b + 1]]).cpu()
+            cache[b] = (kf, vf, ks, vs)
+        return cache[b]
+
+    nseq = min(max_seqs, work.B)
     elapsed, done = 0.0, 0
-    for b in range(min(max_seqs, work.B)):
-        # raw K/V by position (host copies of the same seeded draws)
-        kf = torch.cat([syn_f.k(min(65536, p - lo), work.hkv_full, seq=b, start=lo) for lo in range(0, p, 65536)]
-                       + [work.k_full[b:b + 1]]).cpu()
-        vf = torch.cat([syn_f.v(min(65536, p - lo), work.hkv_full, seq=b, start=lo) for lo in range(0, p, 65536)]
-                       + [work.v_full[b:b + 1]]).cpu()
-        lo = max(0, p - 127)
-        ks = torch.cat([syn_s.k(p - lo, work.hkv_swa, seq=b, start=lo), work.k_swa[b:b + 1]]).cpu()
-        vs = torch.cat([syn_s.v(p - lo, work.hkv_swa, seq=b, start=lo), work.v_swa[b:b + 1]]).cpu()
+    while elapsed < budget_s:
+        b = done % nseq
+        kf, vf, ks, vs = inputs(b)
         t0 = time.perf_counter()
         oracle.attend_seq(q_f[b:b + 1], [p], kf, vf, 0, 1e7, work.vscale, SCALE, 0, None, nthreads=cores)
         oracle.attend_seq(q_s[b:b + 1], [p], ks, vs, lo, 1e4, work.vscale, SCALE, 128, sk, nthreads=cores)
         elapsed += time.perf_counter() - t0
         done += 1
-        if elapsed >= budget_s:
-            break
-    return {"value": done / elapsed, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-            "sample": f"{done} of {work.B} sequences, all 64 heads, one windowed + one full layer at context "
-                      f"{p + 1}; {elapsed:.1f} s of fp64 oracle on {cores} threads"}
+    return {"value": round(done / elapsed, 3), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"{done} sequence-steps (cycling over {nseq} of the {work.B} sequences), all 64 heads, one "
+                      f"windowed + one full layer at context {p + 1}; {elapsed:.1f} s of fp64 oracle on {cores} threads"}
 
 
-def run_decode(args, kvr, peaks_d, peaks_src, rank, world):
+def run_decode(args, kvr, rank):
     stream = torch.cuda.current_stream()
-    work = DecodeWorkload(kvr, seed=1001 + rank)
+    work = DecodeWorkload(kvr, B=args.batch, seed=1001 + rank)
     torch.cuda.synchronize()
     with Clocks(torch.cuda.current_device()) as ck:
         ms = timed_run(work, args.steps, args.warmup, stream)
@@ -408,19 +417,20 @@ def run_prefill(kvr, steps, warmup):
     stream = torch.cuda.current_stream()
     work = PrefillWorkload(kvr)
     torch.cuda.synchronize()
-    ms = timed_run(work, steps, warmup, stream)
+    ms = timed_run(work, steps, warmup, stream, label="timed")
     return work, ms
 
 
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="flash_decode", choices=["flash_decode", "prefill"])
     ap.add_argument("--no-prefill", action="store_true", help="skip the prefill sub-measurement")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--batch", type=int, default=64, help="decode batch per GPU (64 = the Flash-shaped workload)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -444,7 +454,7 @@ def main():
     import sinks_kv_ring_gb300 as kvr
     peaks_d, peaks_src = peaks()
 
-    work, ms, ms_full, ms_swa, clocks, (e2e_ms, h2d, d2h) = run_decode(args, kvr, peaks_d, peaks_src, rank, world)
+    work, ms, ms_full, ms_swa, clocks, (e2e_ms, h2d, d2h) = run_decode(args, kvr, rank)
     if world > 1:
         import torch.distributed as dist
         t = torch.tensor([ms, e2e_ms], device="cuda")
@@ -459,7 +469,7 @@ def main():
         "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": "flash_decode: batch 64, 64 q heads; windowed layer 8 KV heads ring 128 + sink; "
+        "config": {"workload": f"flash_decode: batch {B}, 64 q heads; windowed layer 8 KV heads ring 128 + sink; "
                                "full layer 4 KV heads at context 32769; dims 192/192/128; value scale 0.707",
                    "global_batch": B * world, "seq_len": work.p + 1, "parallelism": f"dp{world}",
                    "l2": f"inputs > L2: full pool {work.bytes_full() / 1e9:.2f} GB read per step; windowed rings "
@@ -479,10 +489,14 @@ def main():
         "gpu_launches": work.launches_per_step * args.steps,
         "clocks": clocks,
     }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        res["cpu_baseline"] = cpu_baseline_decode(work)
     if not args.no_prefill:
         del work
         torch.cuda.empty_cache()
-        pw, pms = run_prefill(kvr, max(3, args.steps // 4), 3)
+        psteps = min(5, args.steps)
+        with Clocks(torch.cuda.current_device()) as pck:
+            pw, pms = run_prefill(kvr, psteps, 3)
         tf_full = pw.flops_full() / (pw.t_full.mean_ms() / 1e3) / 1e12
         tf_swa = pw.flops_swa() / (pw.t_swa.mean_ms() / 1e3) / 1e12
         pk = peaks_d.get("bf16_tflops_sustained", peaks_d["bf16_tflops"])
@@ -498,10 +512,9 @@ def main():
                          "frac": round(tf_full / pk, 4), "peak_source": peaks_src + " (sustained)",
                          "traffic": kernel_traffic("prefill_kernel_full")},
         }
-        res["gpu_launches"] += pw.launches_per_step * max(3, args.steps // 4)
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        w2 = DecodeWorkload(kvr, seed=1001) if args.no_prefill is False else None
-        res["cpu_baseline"] = cpu_baseline_decode(w2 if w2 is not None else work)
+        res["prefill"]["steps"] = psteps
+        res["prefill"]["clocks"] = pck.summary()
+        res["gpu_launches"] += pw.launches_per_step * psteps
     if rank == 0:
         print(json.dumps(res), flush=True)
     if world > 1:
@@ -544,7 +557,7 @@ def run_reference(args, rank, world):
     res = {"impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "tokens/s", "n_gpus": world,
            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True,
            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-           "config": {"workload": "flash_decode: batch 64, 64 q heads; windowed layer 8 KV heads ring 128 + sink; "
+           "config": {"workload": f"flash_decode: batch {B}, 64 q heads; windowed layer 8 KV heads ring 128 + sink; "
                                   "full layer 4 KV heads at context 32769 (oracle: one sequence per step)",
                       "global_batch": B, "seq_len": p + 1, "parallelism": "host cores"},
            "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s", "cores": cores, "kind": "oracle",
