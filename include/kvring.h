@@ -193,6 +193,44 @@ kvr_status full_attn_decode(const kvr_bf16 *q, const int64_t *pos, const int32_t
                             void *workspace, size_t workspace_bytes, kvr_bf16 *out, void *stream);
 
 /*
+ * Size of the fixed device scratch array used by full_attn_decode_noalloc:
+ * 32 MiB, held on every device that loads this library until the process
+ * exits.
+ */
+#define KVR_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+
+/*
+ * full_attn_decode for callers that cannot allocate device memory.  The
+ * pages describe no such call: it exists for callers that are handed only
+ * their input and output buffers, with no allocator and no workspace --
+ * e.g. a plugin whose host passes tensors but owns all device memory, or a
+ * server that reserves the whole GPU for KV pools at start-up and forbids
+ * allocations afterwards.
+ *
+ * Same arguments and results as full_attn_decode, minus the workspace: the
+ * split partials go to a fixed array inside the library's device image
+ * (KVR_NOALLOC_SCRATCH_BYTES).  Nothing is allocated or freed, on the device
+ * or through any library.  A call whose partials would not fit, i.e.
+ * full_attn_decode_workspace_size(B, Hq, Hkv, max_ctx) >
+ * KVR_NOALLOC_SCRATCH_BYTES, returns KVR_EWORKSPACE and launches nothing.
+ *
+ * The array is shared by every call in the process and keeps whatever the
+ * last call left in it; no part of it needs to start at zero (each partial
+ * the merge reads is written earlier in the same call).  Calls that can
+ * overlap on the GPU -- on different streams, or from different host
+ * threads without ordering -- race on the array and give wrong results:
+ * order them (for example, issue them all on one stream).
+ *
+ * The first call on each device looks up the array's device address with
+ * cudaGetSymbolAddress (with that device current); make that first call
+ * before any stream capture begins.
+ */
+kvr_status full_attn_decode_noalloc(const kvr_bf16 *q, const int64_t *pos, const int32_t *seq, int32_t B,
+                                    int32_t Hq, const kvr_kv_layout *pool, const float *rope_cos_sin,
+                                    int64_t max_pos, float softmax_scale, int64_t max_ctx, kvr_bf16 *out,
+                                    void *stream);
+
+/*
  * Chunked prefill over a windowed layer (gaudi-cookbook "What was built":
  * banded tiles with an fp32 softmax that includes the sink).  Row i of the
  * chunk is position P0 + i of sequence `seq`; it attends positions

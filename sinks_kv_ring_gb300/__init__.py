@@ -25,7 +25,7 @@ import torch
 __all__ = [
     "KvrError", "RingLayout", "PagedLayout", "LinearLayout", "lib", "rope_table",
     "kv_ring_append_rope", "swa_sink_decode", "full_attn_decode", "full_attn_decode_workspace_size",
-    "swa_sink_prefill_chunk", "full_attn_prefill_chunk", "device_status",
+    "swa_sink_prefill_chunk", "full_attn_prefill_chunk", "device_status", "full_attn_decode_noalloc",
     "DQK", "DV", "DROT", "WINDOW",
 ]
 
@@ -85,6 +85,8 @@ def lib():
                 L.full_attn_decode_workspace_size.argtypes = [i32, i32, i32, i64]
                 L.full_attn_decode.restype = ctypes.c_int
                 L.full_attn_decode.argtypes = [p, p, p, i32, i32, p, p, i64, f32, i64, p, ctypes.c_size_t, p, p]
+                L.full_attn_decode_noalloc.restype = ctypes.c_int
+                L.full_attn_decode_noalloc.argtypes = [p, p, p, i32, i32, p, p, i64, f32, i64, p, p]
                 L.swa_sink_prefill_chunk.restype = ctypes.c_int
                 L.swa_sink_prefill_chunk.argtypes = [p, i64, i32, i32, i32, p, p, p, p, i64, f32, p, p]
                 L.full_attn_prefill_chunk.restype = ctypes.c_int
@@ -273,6 +275,30 @@ def full_attn_decode(q, pos, seq, pool, table, softmax_scale, max_ctx, workspace
     _check(lib().full_attn_decode(_ptr(q), _ptr(pos), _ptr(seq), B, Hq, ctypes.byref(c), _ptr(table),
                                   table.shape[0], float(softmax_scale), int(max_ctx), _ptr(workspace),
                                   workspace.numel(), _ptr(out), _stream(stream)))
+    return out
+
+
+NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
+
+
+def full_attn_decode_noalloc(q, pos, seq, pool, table, softmax_scale, max_ctx, out=None, stream=None):
+    """full_attn_decode for callers that may not allocate device memory: the
+    split partials go to a fixed 32 MiB array inside the library instead of a
+    workspace.  Calls that may run at the same time on the GPU share that
+    array and must be ordered (e.g. one stream).  The first call on a device
+    looks the array up; make it before any stream capture."""
+    _want(q, "q", torch.bfloat16, 3)
+    _want(pos, "pos", torch.int64, 1)
+    _want(seq, "seq", torch.int32, 1)
+    _want(table, "table", torch.float32, 3)
+    B, Hq, _ = q.shape
+    if out is None:
+        out = torch.empty(B, Hq, DV, dtype=torch.bfloat16, device=q.device)
+    _want(out, "out", torch.bfloat16, 3)
+    c = pool.c()
+    _check(lib().full_attn_decode_noalloc(_ptr(q), _ptr(pos), _ptr(seq), B, Hq, ctypes.byref(c), _ptr(table),
+                                          table.shape[0], float(softmax_scale), int(max_ctx), _ptr(out),
+                                          _stream(stream)))
     return out
 
 

@@ -297,3 +297,75 @@ kvr_status full_attn_prefill_chunk(const kvr_bf16 *q, int64_t P0, int32_t C, int
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Decode without a caller-provided workspace.
+//
+// Some callers get only their input and output buffers and may not allocate
+// device memory (no allocator handed to them, or all memory reserved up front).
+// For them full_attn_decode_noalloc keeps its split partials in this fixed
+// array, which lives in the library's device image on every device that loads
+// the library.  Host code must not use the symbol as an address: the device
+// address is looked up once per device with cudaGetSymbolAddress.
+
+namespace {
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[KVR_NOALLOC_SCRATCH_BYTES];
+
+std::mutex g_noalloc_mu;
+void *g_noalloc_ptr[MAX_DEV];
+
+// Device address of g_noalloc_scratch on the current device; looked up on the
+// first call made on that device.
+cudaError_t noalloc_scratch(void **out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= MAX_DEV) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void *p = nullptr;
+    e = cudaGetSymbolAddress((void **)&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return e;
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return cudaSuccess;
+}
+
+}  // namespace
+
+extern "C" kvr_status full_attn_decode_noalloc(const kvr_bf16 *q, const int64_t *pos, const int32_t *seq,
+                                               int32_t B, int32_t Hq, const kvr_kv_layout *pool,
+                                               const float *rope_cos_sin, int64_t max_pos, float softmax_scale,
+                                               int64_t max_ctx, kvr_bf16 *out, void *stream) {
+  if (B < 0) return fail(KVR_EINVAL, "B %d", B);
+  kvr_status s = check_layout(pool, KVR_LAYOUT_PAGED, "pool");
+  if (s) return s;
+  if ((s = check_heads(Hq, pool->num_kv_heads, 16))) return s;
+  if ((s = check_table(rope_cos_sin, max_pos))) return s;
+  if (max_ctx < 1 || max_ctx > max_pos)
+    return fail(KVR_ERANGE, "max_ctx %lld outside [1, max_pos=%lld]", (long long)max_ctx, (long long)max_pos);
+  if (max_ctx > (int64_t)pool->max_blocks * pool->block_size)
+    return fail(KVR_ERANGE, "max_ctx %lld exceeds max_blocks*block_size = %lld", (long long)max_ctx,
+                (long long)pool->max_blocks * pool->block_size);
+  if (B == 0) return ok();
+  if (!q || !pos || !seq || !out) return fail(KVR_EINVAL, "q/pos/seq/out is NULL");
+  if (!aligned16(q) || !aligned16(out)) return fail(KVR_EINVAL, "q/out not 16-byte aligned");
+  const size_t need = kvr::full_decode_workspace(B, Hq, pool->num_kv_heads, max_ctx);
+  if (need > (size_t)KVR_NOALLOC_SCRATCH_BYTES)
+    return fail(KVR_EWORKSPACE,
+                "full_attn_decode_noalloc: this batch needs %zu bytes of scratch, the fixed array holds %zu; "
+                "use full_attn_decode with a workspace, or a smaller batch or max_ctx",
+                need, (size_t)KVR_NOALLOC_SCRATCH_BYTES);
+  void *scratch = nullptr;
+  cudaError_t e = noalloc_scratch(&scratch);
+  if (e != cudaSuccess) return cuda_fail(e, "full_attn_decode_noalloc: cudaGetSymbolAddress");
+  unsigned *st = nullptr;
+  e = status_ptr(&st);
+  if (e != cudaSuccess) return cuda_fail(e, "full_attn_decode_noalloc");
+  e = kvr::launch_full_decode(q, pos, seq, B, Hq, view(*pool), rope_cos_sin, max_pos, softmax_scale, max_ctx,
+                              scratch, out, st, as_stream(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "full_attn_decode_noalloc launch");
+  return ok();
+}
