@@ -413,9 +413,9 @@ def run_decode(args, kvr, rank):
     return work, ms, ms_full, ms_swa, clocks, (e2e_ms, h2d, d2h)
 
 
-def run_prefill(kvr, steps, warmup):
+def run_prefill(kvr, steps, warmup, P0=122880, C=8192):
     stream = torch.cuda.current_stream()
-    work = PrefillWorkload(kvr)
+    work = PrefillWorkload(kvr, P0=P0, C=C)
     torch.cuda.synchronize()
     ms = timed_run(work, steps, warmup, stream, label="timed")
     return work, ms
@@ -431,6 +431,8 @@ def main():
     ap.add_argument("--no-prefill", action="store_true", help="skip the prefill sub-measurement")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--batch", type=int, default=64, help="decode batch per GPU (64 = the Flash-shaped workload)")
+    ap.add_argument("--prefill-p0", type=int, default=122880, help="cached tokens before the prefill chunk")
+    ap.add_argument("--prefill-c", type=int, default=8192, help="prefill chunk length")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -453,6 +455,8 @@ def main():
         dist.barrier()
     import sinks_kv_ring_gb300 as kvr
     peaks_d, peaks_src = peaks()
+    if args.workload == "prefill":
+        return prefill_only(args, kvr, peaks_d, peaks_src, rank, world)
 
     work, ms, ms_full, ms_swa, clocks, (e2e_ms, h2d, d2h) = run_decode(args, kvr, rank)
     if world > 1:
@@ -521,6 +525,40 @@ def main():
         import torch.distributed as dist
         dist.barrier()
         dist.destroy_process_group()
+
+
+def prefill_only(args, kvr, peaks_d, peaks_src, rank, world):
+    """Chunked prefill as the step: KV write of the chunk into both layers +
+    full_attn_prefill_chunk + swa_sink_prefill_chunk + ring commit."""
+    steps = args.steps
+    with Clocks(torch.cuda.current_device()) as ck:
+        pw, pms = run_prefill(kvr, steps, args.warmup, P0=args.prefill_p0, C=args.prefill_c)
+    ms_f, ms_s = pw.t_full.mean_ms(), pw.t_swa.mean_ms()
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([pms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        pms = float(t[0])
+    flops = pw.flops_full() + pw.flops_swa()
+    pk = peaks_d.get("bf16_tflops_sustained", peaks_d["bf16_tflops"])
+    tf_full = pw.flops_full() / (ms_f / 1e3) / 1e12
+    res = {"metric": METRIC, "value": round(world * flops / (pms / 1e3) / 1e12, 1), "unit": "TFLOP/s",
+           "n_gpus": world, "steps": steps, "warmup": args.warmup, "ms_per_step": round(pms, 3),
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+           "config": {"workload": f"prefill: 1 sequence, {pw.C}-token chunk on {pw.P0} cached tokens; 64 q heads; "
+                                  "full layer 4 KV heads + windowed layer 8 KV heads (ring 128 + sink)",
+                      "parallelism": f"dp{world}", "l2": "K/V of the full layer re-read from L2 by every query tile"},
+           "kernels": {"full_attn_prefill_chunk": {"ms": round(ms_f, 3), "TFLOP/s": round(tf_full, 1),
+                                                   "flop": pw.flops_full()},
+                       "swa_sink_prefill_chunk": {"ms": round(ms_s, 4),
+                                                  "TFLOP/s": round(pw.flops_swa() / (ms_s / 1e3) / 1e12, 1),
+                                                  "flop": pw.flops_swa()}},
+           "roofline": {"bound": "tensor", "achieved": round(tf_full, 1), "peak": pk, "unit": "TFLOP/s",
+                        "frac": round(tf_full / pk, 4), "peak_source": peaks_src + " (sustained)",
+                        "kernel": "full_prefill_tc_kernel", "traffic": kernel_traffic("full_prefill_tc_kernel")},
+           "gpu_launches": pw.launches_per_step * steps, "clocks": ck.summary()}
+    if rank == 0:
+        print(json.dumps(res), flush=True)
 
 
 def run_reference(args, rank, world):

@@ -1,14 +1,17 @@
-// prefill.cu -- chunked prefill over a full-attention layer (paged pool) and
-// over a windowed layer (ring before the chunk + the chunk itself, with sink).
+// prefill.cu -- chunked prefill over a windowed layer: the ring's state
+// before the chunk plus the chunk's own rows, with the sink.
 //
-// gaudi-cookbook "MiMo-V2.6-Flash on Gaudi 2": "Tiled global-attention
-// prefill" (softmax is per query row, so tiles over query rows need no
-// merge) and "What was built" (windowed prefill with an fp32 softmax whose
-// denominator includes the sink).  The query rows of one CTA are 64
-// consecutive (position, head) pairs of one KV head's group, so every K/V
-// tile staged in shared memory serves all the heads that read it.  The
-// softmax state of a windowed row starts from the sink: (m, l, o) =
-// (sink, 1, 0), which puts e^{sink} in the denominator and nowhere else.
+// gaudi-cookbook "MiMo-V2.6-Flash on Gaudi 2": "What was built" (windowed
+// prefill with an fp32 softmax whose denominator includes the sink) and
+// "Tiled global-attention prefill" (softmax is per query row, so tiles over
+// query rows need no merge).  A row attends at most 128 keys, so the whole
+// layer is about 1/1000 of a full layer's products at an 8192-token chunk;
+// it runs on the warp-level bf16 MMA (mma.sync) with an online softmax.
+// The query rows of one CTA are 64 consecutive (position, head) pairs of one
+// KV head's group, so every K/V tile staged in shared memory serves all the
+// heads that read it.  The softmax state of a row starts from the sink:
+// (m, l, o) = (sink, 1, 0), which puts e^{sink} in the denominator and
+// nowhere else.
 #include "launch.h"
 
 namespace kvr {
@@ -25,20 +28,6 @@ constexpr int PF_STAGES = 2;
 constexpr int PF_SMEM = PF_ROWS * DQK * 2 + PF_STAGES * PF_STAGE;
 
 // Where key position j of the current sequence lives.
-struct PagedSrc {
-  const uint16_t *k, *v;
-  const int32_t *bt;  // this sequence's block-table row
-  int hkv, kv, bsz, num_blocks;
-  __device__ __forceinline__ bool locate(long long j, const uint16_t *&kp, const uint16_t *&vp) const {
-    const int blk = bt[j / bsz];
-    if (blk < 0 || blk >= num_blocks) return false;
-    const long long row = ((long long)blk * hkv + kv) * bsz + (j % bsz);
-    kp = k + row * DQK;
-    vp = v + row * DV;
-    return true;
-  }
-};
-
 struct SwaSrc {
   const uint16_t *rk, *rv;   // ring of this (sequence, KV head): [128][192], [128][128]
   const int32_t *slot_pos;   // [128] of this sequence
@@ -111,7 +100,6 @@ __global__ void __launch_bounds__(PF_WARPS * 32, 2)
   uint8_t *sQ = smem;
   uint8_t *sStage = smem + PF_ROWS * DQK * 2;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int tiles_per_kv = (C * G + PF_ROWS - 1) / PF_ROWS;
   const int kv = blockIdx.x % hkv;
   const long long f0 = (long long)(blockIdx.x / hkv) * PF_ROWS;
   const long long nrows = (long long)C * G;
@@ -121,7 +109,6 @@ __global__ void __launch_bounds__(PF_WARPS * 32, 2)
     src.rk += (long long)kv * WIN * DQK;
     src.rv += (long long)kv * WIN * DV;
   }
-  (void)tiles_per_kv;
 
   // Positions covered by this CTA.
   const long long i_first = f0 / G;
@@ -298,22 +285,6 @@ cudaError_t set_smem(K kernel, int bytes) {
 }
 
 }  // namespace
-
-cudaError_t launch_full_prefill(const uint16_t *q, int64_t P0, int C, int seq, int hq, const KvView &pool,
-                                const float *table, int64_t max_pos, float softmax_scale, uint16_t *out,
-                                unsigned *status, cudaStream_t st) {
-  (void)max_pos;
-  const int hkv = pool.hkv, G = hq / hkv;
-  auto kern = prefill_kernel<PagedSrc, false>;
-  cudaError_t e = set_smem(kern, PF_SMEM);
-  if (e != cudaSuccess) return e;
-  PagedSrc src{pool.k, pool.v, pool.block_table + (long long)seq * pool.max_blocks, hkv, 0, pool.block_size,
-               pool.num_blocks};
-  const long long tiles = ((long long)C * G + PF_ROWS - 1) / PF_ROWS;
-  kern<<<(unsigned)(tiles * hkv), PF_WARPS * 32, PF_SMEM, st>>>(q, P0, C, hq, G, hkv, src, nullptr, table,
-                                                                 softmax_scale * LOG2E, out, status);
-  return cudaGetLastError();
-}
 
 cudaError_t launch_swa_prefill(const uint16_t *q, int64_t P0, int C, int seq, int hq, const KvView &chunk,
                                const KvView &ring, const float *sinks, const float *table,

@@ -1,0 +1,464 @@
+// prefill_tc.cu -- chunked prefill over a full-attention layer on the
+// Blackwell tensor cores: TMA tile loads, tcgen05.mma with accumulators in
+// TMEM, fp32 online softmax in registers.
+//
+// gaudi-cookbook "MiMo-V2.6-Flash on Gaudi 2", "Tiled global-attention
+// prefill": softmax is per query row, so independent tiles of query rows
+// need no merge; row i of the chunk (position P0 + i) attends positions
+// 0..P0 + i.  Xiaomi "Full-Pipeline Inference Optimization", section 1.1:
+// chunked prefill is compute-bound, so this is the one contraction of the
+// path that is sized for the tensor cores.
+//
+// One CTA = two query tiles of 128 rows (the rows are consecutive
+// (position, head) pairs of one KV head's GQA group), one SM, 320 threads:
+//   warps 0-3  softmax of tile 0 (thread = row = TMEM lane)
+//   warps 4-7  softmax of tile 1
+//   warp  8    TMEM owner and MMA issuer (lane 0)
+//   warp  9    TMA producer (lane 0)
+// TMEM (512 columns): S0 | S1 | O0 | O1, 128 fp32 columns each.  The bf16
+// probabilities P of a tile are written over the first 64 columns of its S
+// and feed the P.V product straight from TMEM.
+// Shared memory: Q0, Q1 (3 x 16 KB each, 128-byte swizzled K-major) and a
+// ring of eight 16 KB slots.  Every K/V tile of 128 keys is five slot loads:
+// K dims 0-63, 64-127, 128-191 (K-major, for S = Q K^T) and V dims 0-63,
+// 64-127 (MN-major, for O += P V).
+// MMA order per key tile j (the two tiles ping-pong, so one tile's softmax
+// overlaps the other tile's products):
+//   O0 += P0(j-1) V(j-1);  S0 = Q0 K(j)^T;  O1 += P1(j-1) V(j-1);  S1 = Q1 K(j)^T
+// Softmax keeps a per-row reference max and rescales O in TMEM only when the
+// row max grows by more than 2^8, so most tiles never touch O.
+#include <cuda.h>
+
+#include "launch.h"
+#include "tc_ptx.cuh"
+
+namespace kvr {
+namespace {
+
+using namespace tc;
+
+constexpr int TC_THREADS = 320;
+constexpr int TC_SLOT = 16384;                 // 128 rows x 128 bytes
+constexpr int TC_NSLOT = 8;
+constexpr int TC_QTILE = 3 * TC_SLOT;          // 128 rows x 192 dims
+constexpr int TC_OFF_RING = 2 * TC_QTILE;      // 96 KB
+constexpr int TC_OFF_BAR = TC_OFF_RING + TC_NSLOT * TC_SLOT;  // 224 KB
+constexpr int TC_SMEM = TC_OFF_BAR + 256 + 1024;              // + barriers + alignment slack
+constexpr unsigned ST_TIMEOUT = 8u;
+constexpr float NEG_INF = -INFINITY;
+constexpr float RESCALE_THRESHOLD = 8.0f;      // log2 units
+
+// barrier area layout (byte offsets)
+constexpr int B_FULL = 0;       // [8]
+constexpr int B_EMPTY = 64;     // [8]
+constexpr int B_SFULL = 128;    // [2]
+constexpr int B_PREADY = 144;   // [2]
+constexpr int B_OFINAL = 160;   // [2]
+constexpr int B_TMEM = 176;     // u32: TMEM base address
+constexpr int B_ABORT = 180;    // u32: set when a wait timed out
+constexpr int B_DRAIN = 192;    // all MMAs of the CTA done (before TMEM is freed)
+
+// One lane waits, the whole warp learns the outcome (keeps the warp converged
+// for the .sync.aligned tcgen05 operations that follow).
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile uint32_t *abort,
+                                          uint64_t limit_ns = 2000000000ull) {
+  int ok = 0;
+  if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, abort, limit_ns) ? 1 : 0;
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  if (ok) {
+    // The phase is complete; every lane observes it itself (acquire).
+    for (int i = 0; i < 1024 && !mbar_try(bar, parity); ++i) {
+    }
+  }
+  return ok != 0;
+}
+
+struct TcArgs {
+  const uint16_t *q;
+  long long P0;
+  int C, hq, G, hkv;
+  const int32_t *bt;  // block-table row of the sequence
+  int bsz, num_blocks;
+  long long total_rows;  // rows of the pool tensors (num_blocks * hkv * bsz)
+  const float *table;
+  float scale_log2;
+  uint16_t *out;
+  unsigned *status;
+};
+
+__global__ void __launch_bounds__(TC_THREADS, 1)
+    full_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
+                           const TcArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t *gbase = smem_raw + (base - raw);
+  const uint32_t sQ0 = base, sQ1 = base + TC_QTILE, sRing = base + TC_OFF_RING, sBar = base + TC_OFF_BAR;
+  volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(gbase + TC_OFF_BAR + B_ABORT);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  const int kv = blockIdx.x % a.hkv;
+  const long long f0 = (long long)(blockIdx.x / a.hkv) * 256;
+  const long long nrows = (long long)a.C * a.G;
+  const long long i_last = min(nrows - 1, f0 + 255) / a.G;
+  const long long key_hi = a.P0 + i_last + 1;         // keys 0 .. key_hi-1
+  const int ntiles = (int)((key_hi + 127) / 128);
+  const long long pmin = a.P0 + f0 / a.G;            // smallest row position in the CTA
+
+  // ---- set-up: barriers, TMEM, rotated Q tiles
+  if (tid == 0) {
+    for (int i = 0; i < TC_NSLOT; ++i) {
+      mbar_init(sBar + B_FULL + 8 * i, 1);
+      mbar_init(sBar + B_EMPTY + 8 * i, 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(sBar + B_SFULL + 8 * i, 1);
+      mbar_init(sBar + B_PREADY + 8 * i, 128);
+      mbar_init(sBar + B_OFINAL + 8 * i, 1);
+    }
+    mbar_init(sBar + B_DRAIN, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 8) {
+    tmem_alloc(sBar + B_TMEM, 512);
+    tmem_relinquish();
+  }
+  // Q rows: CTA row r -> tile r / 128, TMEM lane r % 128; flat row f0 + r is
+  // position (f0 + r) / G, head (f0 + r) % G of this KV head's group.
+  for (int it = tid; it < 256 * 20; it += TC_THREADS) {
+    const int r = it / 20, c = it % 20;
+    const long long f = f0 + r;
+    const bool live = f < nrows;
+    const long long i = live ? f / a.G : 0;
+    const int g = live ? (int)(f % a.G) : 0;
+    const uint16_t *qh = a.q + (i * a.hq + (long long)kv * a.G + g) * DQK;
+    const int t = r & 127;
+    uint8_t *qt = gbase + (r >> 7) * TC_QTILE;
+    auto chunk_ptr = [&](int ch) {  // 16-byte chunk ch (0..23) of row t, 128-byte swizzle
+      return reinterpret_cast<uint4 *>(qt + (ch >> 3) * TC_SLOT + t * 128 + (((ch & 7) ^ (t & 7)) << 4));
+    };
+    const uint4 zero = make_uint4(0, 0, 0, 0);
+    if (c < 4) {
+      uint4 o1 = zero, o2 = zero;
+      if (live) {
+        const float4 *tr = reinterpret_cast<const float4 *>(a.table + (a.P0 + i) * 64 + 16 * c);
+        float cs[16];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const float4 fv = tr[u];
+          cs[4 * u] = fv.x; cs[4 * u + 1] = fv.y; cs[4 * u + 2] = fv.z; cs[4 * u + 3] = fv.w;
+        }
+        const uint4 *s4 = reinterpret_cast<const uint4 *>(qh);
+        rope_pair8(s4[c], s4[c + 4], cs, o1, o2);
+      }
+      *chunk_ptr(c) = o1;
+      *chunk_ptr(c + 4) = o2;
+    } else {
+      const int ch = c + 4;
+      *chunk_ptr(ch) = live ? reinterpret_cast<const uint4 *>(qh)[ch] : zero;
+    }
+  }
+  fence_proxy_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(gbase + TC_OFF_BAR + B_TMEM);
+
+  if (warp == 9) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      const int low = a.bsz & -a.bsz;
+      const int rb = low < 128 ? low : 128;      // rows per box: divides the page size and 128
+      const int nb = 128 / rb;
+      const long long nloads = 5LL * ntiles;
+      long long L = 0;
+      for (; L < nloads; ++L) {
+        const int t = (int)(L / 5), part = (int)(L % 5);
+        const int slot = (int)(L % TC_NSLOT);
+        const uint32_t round = (uint32_t)(L / TC_NSLOT);
+        if (!mbar_wait(sBar + B_EMPTY + 8 * slot, (round & 1u) ^ 1u, abort_flag)) break;
+        const uint32_t full = sBar + B_FULL + 8 * slot;
+        mbar_expect_tx(full, TC_SLOT);
+        const void *map = part < 3 ? (const void *)&tmk : (const void *)&tmv;
+        const int x = 64 * (part < 3 ? part : part - 3);
+        for (int b = 0; b < nb; ++b) {
+          const long long key = 128LL * t + (long long)b * rb;
+          long long y = a.total_rows;  // past the end: the TMA unit fills zeros
+          if (key < key_hi) {
+            const int blk = a.bt[key / a.bsz];
+            if (blk >= 0 && blk < a.num_blocks)
+              y = ((long long)blk * a.hkv + kv) * a.bsz + (key % a.bsz);
+            else
+              flag(a.status, ST_BAD_BLOCK);
+          }
+          tma_load_2d(sRing + slot * TC_SLOT + b * rb * 128, map, x, (int)y, full);
+        }
+      }
+      // On an abort, let the loads already issued land before the CTA exits
+      // (bounded by time only: the abort flag is already set).
+      volatile uint32_t local = 0;
+      for (long long M = L - 1; M >= 0 && M >= L - TC_NSLOT; --M) {
+        const int slot = (int)(M % TC_NSLOT);
+        local = 0;
+        mbar_wait(sBar + B_FULL + 8 * slot, (uint32_t)(M / TC_NSLOT) & 1u, &local, 1000000000ull);
+      }
+    }
+  } else if (warp == 8) {
+    // ------------------------------------------------------------ MMA issuer
+    const uint32_t id_qk = idesc_bf16(128, 128, 0, 0);
+    const uint32_t id_pv = idesc_bf16(128, 64, 0, 1);
+    bool ok = true;
+    auto wait_full = [&](long long L) {
+      return warp_wait(sBar + B_FULL + 8 * (int)(L % TC_NSLOT), (uint32_t)(L / TC_NSLOT) & 1u, abort_flag);
+    };
+    // S_i = Q_i K(t)^T : 12 MMAs of K = 16 over three 64-dim slots.
+    auto issue_S = [&](int i, int t, bool release) {
+      for (int kb = 0; kb < 3 && ok; ++kb) {
+        const long long L = 5LL * t + kb;
+        if (!wait_full(L)) { ok = false; break; }
+        tc_fence_after();
+        if (lane == 0) {
+          const uint32_t sk = sRing + (uint32_t)(L % TC_NSLOT) * TC_SLOT;
+          const uint32_t sq = (i ? sQ1 : sQ0) + kb * TC_SLOT;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_ss(tmem + 128 * i, sdesc_sw128(sq + 32 * kk, 16, 1024), sdesc_sw128(sk + 32 * kk, 16, 1024), id_qk,
+                   (kb | kk) != 0);
+          if (release) mma_commit(sBar + B_EMPTY + 8 * (int)(L % TC_NSLOT));
+        }
+        __syncwarp();
+      }
+      if (ok && lane == 0) mma_commit(sBar + B_SFULL + 8 * i);
+      __syncwarp();
+    };
+    // O_i += P_i(t) V(t) : two halves of the value dims, 8 MMAs of K = 16 keys each.
+    auto issue_PV = [&](int i, int t, bool release) {
+      if (!ok) return;
+      if (!warp_wait(sBar + B_PREADY + 8 * i, (uint32_t)t & 1u, abort_flag)) { ok = false; return; }
+      tc_fence_after();
+      for (int db = 0; db < 2 && ok; ++db) {
+        const long long L = 5LL * t + 3 + db;
+        if (!wait_full(L)) { ok = false; break; }
+        const uint32_t sv = sRing + (uint32_t)(L % TC_NSLOT) * TC_SLOT;
+        if (i == 0 && t == ntiles - 1 && 128LL * t + 128 > key_hi) {
+          // Rows past the last key may hold stale bytes of the page; P is 0
+          // there, but 0 * NaN is not, so zero them before the product.
+          const int first = (int)(key_hi - 128LL * t);
+          uint8_t *g = gbase + TC_OFF_RING + (int)(L % TC_NSLOT) * TC_SLOT;
+          for (int e = first * 8 + lane; e < 128 * 8; e += 32)
+            reinterpret_cast<uint4 *>(g)[e] = make_uint4(0, 0, 0, 0);
+          fence_proxy_async_smem();
+          __syncwarp();
+          tc_fence_after();
+        }
+        if (lane == 0) {
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_ts(tmem + 256 + 128 * i + 64 * db, tmem + 128 * i + 8 * kk, sdesc_sw128(sv + 2048 * kk, 8192, 1024),
+                   id_pv, (t > 0 || kk > 0) ? 1u : 0u);
+          if (release) mma_commit(sBar + B_EMPTY + 8 * (int)(L % TC_NSLOT));
+        }
+        __syncwarp();
+      }
+    };
+    issue_S(0, 0, false);
+    issue_S(1, 0, true);
+    for (int t = 1; t < ntiles && ok; ++t) {
+      issue_PV(0, t - 1, false);
+      issue_S(0, t, false);
+      issue_PV(1, t - 1, true);
+      issue_S(1, t, true);
+    }
+    issue_PV(0, ntiles - 1, false);
+    if (ok && lane == 0) mma_commit(sBar + B_OFINAL);
+    __syncwarp();
+    issue_PV(1, ntiles - 1, true);
+    if (ok && lane == 0) mma_commit(sBar + B_OFINAL + 8);
+    __syncwarp();
+    // Every MMA issued must be finished before TMEM is released.
+    if (lane == 0) {
+      volatile uint32_t local = 0;  // bounded by time only, even after an abort
+      mma_commit(sBar + B_DRAIN);
+      mbar_wait(sBar + B_DRAIN, 0, &local, 1000000000ull);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ softmax (warps 0-7)
+    const int wg = warp >> 2;
+    const int row = tid & 127;                       // TMEM lane = row of the tile
+    const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
+    const uint32_t tS = tmem + lane_base + 128 * wg;
+    const uint32_t tO = tmem + lane_base + 256 + 128 * wg;
+    const long long f = f0 + 128 * wg + row;
+    const bool live = f < nrows;
+    const long long fc = live ? f : nrows - 1;
+    const long long pr = a.P0 + fc / a.G;
+    const int g = (int)(fc % a.G);
+    const float sl2 = a.scale_log2;
+    float m_ref = NEG_INF, l = 0.f;
+    bool ok = true;
+    for (int t = 0; t < ntiles; ++t) {
+      if (!warp_wait(sBar + B_SFULL + 8 * wg, (uint32_t)t & 1u, abort_flag)) { ok = false; break; }
+      tc_fence_after();
+      uint32_t s[4][32];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld32(tS + 32 * c, s[c]);
+      tmem_wait_ld();
+      const long long j0 = 128LL * t;
+      if (j0 + 127 > pmin) {  // the diagonal (and the end of the keys) is in this tile
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            if (j0 + 32 * c + e > pr) s[c][e] = __float_as_uint(NEG_INF);
+      }
+      float mx = NEG_INF;
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+#pragma unroll
+        for (int e = 0; e < 32; ++e) mx = fmaxf(mx, __uint_as_float(s[c][e]));
+      const float m_new = fmaxf(m_ref, mx * sl2);
+      float factor = 1.f;
+      bool resc = false;
+      if (m_ref == NEG_INF) {
+        m_ref = m_new;  // nothing accumulated yet (all earlier P were 0)
+      } else if (m_new > m_ref + RESCALE_THRESHOLD) {
+        factor = ex2(m_ref - m_new);
+        m_ref = m_new;
+        resc = true;
+      }
+      const float b = m_ref == NEG_INF ? 0.f : m_ref;
+      float sum = 0.f;
+      uint32_t pk[2][32];
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          const float p0 = ex2(fmaf(__uint_as_float(s[c][e]), sl2, -b));
+          const float p1 = ex2(fmaf(__uint_as_float(s[c][e + 1]), sl2, -b));
+          sum += p0 + p1;
+          pk[c >> 1][(c & 1) * 16 + e / 2] = pack_bf16(p0, p1);
+        }
+      l = l * factor + sum;
+      if (__any_sync(0xffffffffu, resc)) {
+        // O is quiescent: its last product finished before S(t) did, and the
+        // next one waits for this tile's P.
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          uint32_t o[32];
+          tmem_ld32(tO + 32 * c, o);
+          tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * factor);
+          tmem_st32(tO + 32 * c, o);
+        }
+      }
+      tmem_st32(tS, pk[0]);
+      tmem_st32(tS + 32, pk[1]);
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(sBar + B_PREADY + 8 * wg);
+    }
+    if (ok && warp_wait(sBar + B_OFINAL + 8 * wg, 0, abort_flag)) {
+      tc_fence_after();
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      uint16_t *orow = a.out + ((pr - a.P0) * a.hq + (long long)kv * a.G + g) * DV;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t o[32];
+        tmem_ld32(tO + 32 * c, o);
+        tmem_wait_ld();
+        if (live) {
+          uint4 *dst = reinterpret_cast<uint4 *>(orow + 32 * c);
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            uint4 w;
+            w.x = pack_bf16(__uint_as_float(o[8 * u + 0]) * inv, __uint_as_float(o[8 * u + 1]) * inv);
+            w.y = pack_bf16(__uint_as_float(o[8 * u + 2]) * inv, __uint_as_float(o[8 * u + 3]) * inv);
+            w.z = pack_bf16(__uint_as_float(o[8 * u + 4]) * inv, __uint_as_float(o[8 * u + 5]) * inv);
+            w.w = pack_bf16(__uint_as_float(o[8 * u + 6]) * inv, __uint_as_float(o[8 * u + 7]) * inv);
+            dst[u] = w;
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (*abort_flag && tid == 0) flag(a.status, ST_TIMEOUT);
+  if (warp == 8) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+// 2-D map over a pool tensor viewed as [rows][width] bf16, box 64 x box_rows,
+// 128-byte swizzle.
+bool make_map(CUtensorMap *m, const void *ptr, long long rows, int width, int box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)width, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)width * 2};
+  cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+cudaError_t launch_full_prefill(const uint16_t *q, int64_t P0, int C, int seq, int hq, const KvView &pool,
+                                const float *table, int64_t max_pos, float softmax_scale, uint16_t *out,
+                                unsigned *status, cudaStream_t st) {
+  (void)max_pos;
+  const int hkv = pool.hkv, G = hq / hkv;
+  const long long rows = (long long)pool.num_blocks * hkv * pool.block_size;
+  if (rows >= (1LL << 31)) return cudaErrorInvalidValue;
+  const int low = pool.block_size & -pool.block_size;
+  const int box_rows = low < 128 ? low : 128;
+  CUtensorMap mk, mv;
+  if (!make_map(&mk, pool.k, rows, DQK, box_rows) || !make_map(&mv, pool.v, rows, DV, box_rows))
+    return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(full_prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM);
+  if (e != cudaSuccess) return e;
+  TcArgs a;
+  a.q = q;
+  a.P0 = P0;
+  a.C = C;
+  a.hq = hq;
+  a.G = G;
+  a.hkv = hkv;
+  a.bt = pool.block_table + (long long)seq * pool.max_blocks;
+  a.bsz = pool.block_size;
+  a.num_blocks = pool.num_blocks;
+  a.total_rows = rows;
+  a.table = table;
+  a.scale_log2 = softmax_scale * LOG2E;
+  a.out = out;
+  a.status = status;
+  const long long ctas = ((long long)C * G + 255) / 256 * hkv;
+  full_prefill_tc_kernel<<<(unsigned)ctas, TC_THREADS, TC_SMEM, st>>>(mk, mv, a);
+  return cudaGetLastError();
+}
+
+}  // namespace kvr

@@ -354,3 +354,36 @@ def test_full_prefill_with_context_and_groups(hq, hkv, tables):
     k, v = raw_kv(syn, hkv, 0, 0, P0 + C)
     want = oracle.attend_seq(q[rows], np.array(rows) + P0, k, v, 0, 1e7, 0.612, SCALE, 0, None)
     compare_rows(out[rows], want, "full prefill with context")
+
+
+@pytest.mark.parametrize("bsz", [16, 48, 96, 192, 256])
+def test_full_prefill_block_sizes(bsz, tables):
+    # Page sizes that are not 128: the key tiles are assembled from several
+    # pages (or part of one), with a shuffled block table.
+    syn = Synth(2901 + bsz, dist="shifted", device=DEV)
+    hq, hkv, P0, C = 32, 2, 1500, 300
+    pool = kvr.PagedLayout.contiguous(1, hkv, P0 + C + bsz, block_size=bsz)
+    perm = torch.randperm(pool.num_blocks, generator=torch.Generator().manual_seed(bsz)).to(torch.int32)
+    pool.block_table.copy_(perm.reshape(pool.block_table.shape).to(DEV))
+    fill_paged(pool, syn, [0], [P0 + C], tables[1e7], 0.707)
+    q = syn.q(C, hq, hkv, seq=0, start=P0)
+    out = kvr.full_attn_prefill_chunk(q, P0, 0, pool, tables[1e7], SCALE)
+    rows = [0, 7, 8, 150, 255, 256, 299]
+    k, v = raw_kv(syn, hkv, 0, 0, P0 + C)
+    want = oracle.attend_seq(q[rows], np.array(rows) + P0, k, v, 0, 1e7, 0.707, SCALE, 0, None)
+    compare_rows(out[rows], want, f"full prefill bsz={bsz}")
+    assert kvr.device_status() == 0
+
+
+def test_full_prefill_many_tiles_all_rows(tables):
+    # Several CTAs along the chunk and a few hundred key tiles; every row checked.
+    syn = Synth(3001, dist="plain", device=DEV)
+    hq, hkv, P0, C = 16, 1, 9000, 200
+    pool = kvr.PagedLayout.contiguous(1, hkv, P0 + C, block_size=64)
+    fill_paged(pool, syn, [0], [P0 + C], tables[1e7], 0.612)
+    q = syn.q(C, hq, hkv, seq=0, start=P0)
+    out = kvr.full_attn_prefill_chunk(q, P0, 0, pool, tables[1e7], SCALE)
+    k, v = raw_kv(syn, hkv, 0, 0, P0 + C)
+    want = oracle.attend_seq(q, np.arange(P0, P0 + C), k, v, 0, 1e7, 0.612, SCALE, 0, None)
+    compare(out, want, "full prefill many tiles")
+    compare_rows(out, want, "full prefill many tiles")
