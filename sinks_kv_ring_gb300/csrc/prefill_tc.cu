@@ -58,19 +58,13 @@ constexpr int B_TMEM = 176;     // u32: TMEM base address
 constexpr int B_ABORT = 180;    // u32: set when a wait timed out
 constexpr int B_DRAIN = 192;    // all MMAs of the CTA done (before TMEM is freed)
 
-// One lane waits, the whole warp learns the outcome (keeps the warp converged
-// for the .sync.aligned tcgen05 operations that follow).
+// Every lane waits on the barrier; the warp agrees on the outcome so that it
+// stays converged for the warp-collective (.sync.aligned / elect.sync)
+// instructions that follow.
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile uint32_t *abort,
                                           uint64_t limit_ns = 2000000000ull) {
-  int ok = 0;
-  if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, abort, limit_ns) ? 1 : 0;
-  ok = __shfl_sync(0xffffffffu, ok, 0);
-  if (ok) {
-    // The phase is complete; every lane observes it itself (acquire).
-    for (int i = 0; i < 1024 && !mbar_try(bar, parity); ++i) {
-    }
-  }
-  return ok != 0;
+  const bool ok = mbar_wait(bar, parity, abort, limit_ns);
+  return __all_sync(0xffffffffu, ok);
 }
 
 struct TcArgs {
@@ -86,6 +80,7 @@ struct TcArgs {
   unsigned *status;
 };
 
+// 10 warps share 4 schedulers (3 warps on some), which caps registers at 168.
 __global__ void __launch_bounds__(TC_THREADS, 1)
     full_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                            const TcArgs a) {
@@ -167,36 +162,49 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 
   if (warp == 9) {
     // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
-      const int low = a.bsz & -a.bsz;
-      const int rb = low < 128 ? low : 128;      // rows per box: divides the page size and 128
-      const int nb = 128 / rb;
-      const long long nloads = 5LL * ntiles;
-      long long L = 0;
-      for (; L < nloads; ++L) {
-        const int t = (int)(L / 5), part = (int)(L % 5);
-        const int slot = (int)(L % TC_NSLOT);
-        const uint32_t round = (uint32_t)(L / TC_NSLOT);
-        if (!mbar_wait(sBar + B_EMPTY + 8 * slot, (round & 1u) ^ 1u, abort_flag)) break;
-        const uint32_t full = sBar + B_FULL + 8 * slot;
-        mbar_expect_tx(full, TC_SLOT);
-        const void *map = part < 3 ? (const void *)&tmk : (const void *)&tmv;
-        const int x = 64 * (part < 3 ? part : part - 3);
-        for (int b = 0; b < nb; ++b) {
-          const long long key = 128LL * t + (long long)b * rb;
-          long long y = a.total_rows;  // past the end: the TMA unit fills zeros
-          if (key < key_hi) {
-            const int blk = a.bt[key / a.bsz];
-            if (blk >= 0 && blk < a.num_blocks)
-              y = ((long long)blk * a.hkv + kv) * a.bsz + (key % a.bsz);
-            else
-              flag(a.status, ST_BAD_BLOCK);
-          }
-          tma_load_2d(sRing + slot * TC_SLOT + b * rb * 128, map, x, (int)y, full);
+    // The whole warp runs the loop (converged); elect.sync issues.  Lane b
+    // holds the tensor-map row of box b of a key tile; the next tile's rows
+    // are fetched (block table) while the current tile's loads go out.
+    const int low = a.bsz & -a.bsz;
+    const int rb = low < 128 ? low : 128;      // rows per box: divides the page size and 128
+    const int nb = 128 / rb;
+    const int total = (int)a.total_rows;       // < 2^31, checked by the launcher
+    const int khi = (int)key_hi;
+    auto box_row = [&](int t) {
+      int y = total;                           // past the end: the TMA unit fills zeros
+      if (lane < nb) {
+        const int key = 128 * t + lane * rb;
+        if (key < khi) {
+          const int blk = a.bt[key / a.bsz];
+          if (blk >= 0 && blk < a.num_blocks)
+            y = (blk * a.hkv + kv) * a.bsz + key % a.bsz;
+          else
+            flag(a.status, ST_BAD_BLOCK);
         }
       }
-      // On an abort, let the loads already issued land before the CTA exits
-      // (bounded by time only: the abort flag is already set).
+      return y;
+    };
+    int y_next = box_row(0);
+    long long L = 0;
+    bool ok = true;
+    for (int t = 0; t < ntiles && ok; ++t) {
+      const int y_cur = y_next;
+      if (t + 1 < ntiles) y_next = box_row(t + 1);
+      for (int part = 0; part < 5; ++part, ++L) {
+        const int slot = (int)(L % TC_NSLOT);
+        const uint32_t round = (uint32_t)(L / TC_NSLOT);
+        if (!warp_wait(sBar + B_EMPTY + 8 * slot, (round & 1u) ^ 1u, abort_flag)) { ok = false; break; }
+        const uint32_t full = sBar + B_FULL + 8 * slot;
+        mbar_expect_tx_elect(full, TC_SLOT);
+        const void *map = part < 3 ? (const void *)&tmk : (const void *)&tmv;
+        const int x = 64 * (part < 3 ? part : part - 3);
+        for (int b = 0; b < nb; ++b)
+          tma_load_2d_elect(sRing + slot * TC_SLOT + b * rb * 128, map, x, __shfl_sync(0xffffffffu, y_cur, b), full);
+      }
+    }
+    // On an abort, let the loads already issued land before the CTA exits
+    // (bounded by time only: the abort flag is already set).
+    if (lane == 0) {
       volatile uint32_t local = 0;
       for (long long M = L - 1; M >= 0 && M >= L - TC_NSLOT; --M) {
         const int slot = (int)(M % TC_NSLOT);
@@ -204,82 +212,96 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         mbar_wait(sBar + B_FULL + 8 * slot, (uint32_t)(M / TC_NSLOT) & 1u, &local, 1000000000ull);
       }
     }
+    __syncwarp();
   } else if (warp == 8) {
     // ------------------------------------------------------------ MMA issuer
+    // The whole warp runs the loop (converged, operands warp-uniform) and
+    // elect.sync issues each MMA and commit.  Descriptors are precomputed and
+    // advanced by adding address offsets >> 4.
     const uint32_t id_qk = idesc_bf16(128, 128, 0, 0);
-    const uint32_t id_pv = idesc_bf16(128, 64, 0, 1);
+    const uint32_t id_pv64 = idesc_bf16(128, 64, 0, 1);
+    const uint32_t id_pv128 = idesc_bf16(128, 128, 0, 1);
+    const uint64_t dq0 = sdesc_sw128(sQ0, 16, 1024), dq1 = sdesc_sw128(sQ1, 16, 1024);
+    const uint64_t dring_k = sdesc_sw128(sRing, 16, 1024);
+    const uint64_t dring_v = sdesc_sw128(sRing, TC_SLOT, 1024);  // LBO = next slot (the other value half)
     bool ok = true;
+    auto slot_of = [](long long L) { return (uint32_t)(L % TC_NSLOT); };
     auto wait_full = [&](long long L) {
-      return warp_wait(sBar + B_FULL + 8 * (int)(L % TC_NSLOT), (uint32_t)(L / TC_NSLOT) & 1u, abort_flag);
+      return warp_wait(sBar + B_FULL + 8 * slot_of(L), (uint32_t)(L / TC_NSLOT) & 1u, abort_flag);
     };
     // S_i = Q_i K(t)^T : 12 MMAs of K = 16 over three 64-dim slots.
     auto issue_S = [&](int i, int t, bool release) {
-      for (int kb = 0; kb < 3 && ok; ++kb) {
+      const uint64_t dq = i ? dq1 : dq0;
+      const uint32_t d = tmem + 128 * i;
+      for (int kb = 0; kb < 3; ++kb) {
         const long long L = 5LL * t + kb;
-        if (!wait_full(L)) { ok = false; break; }
+        if (!wait_full(L)) { ok = false; return; }
         tc_fence_after();
-        if (lane == 0) {
-          const uint32_t sk = sRing + (uint32_t)(L % TC_NSLOT) * TC_SLOT;
-          const uint32_t sq = (i ? sQ1 : sQ0) + kb * TC_SLOT;
+        const uint64_t a0 = dq + (uint64_t)((kb * TC_SLOT) >> 4);
+        const uint64_t b0 = dring_k + (uint64_t)((slot_of(L) * TC_SLOT) >> 4);
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            mma_ss(tmem + 128 * i, sdesc_sw128(sq + 32 * kk, 16, 1024), sdesc_sw128(sk + 32 * kk, 16, 1024), id_qk,
-                   (kb | kk) != 0);
-          if (release) mma_commit(sBar + B_EMPTY + 8 * (int)(L % TC_NSLOT));
-        }
-        __syncwarp();
+        for (int kk = 0; kk < 4; ++kk) mma_ss_elect(d, a0 + 2 * kk, b0 + 2 * kk, id_qk, (kb | kk) != 0);
+        if (release) mma_commit_elect(sBar + B_EMPTY + 8 * slot_of(L));
       }
-      if (ok && lane == 0) mma_commit(sBar + B_SFULL + 8 * i);
-      __syncwarp();
+      mma_commit_elect(sBar + B_SFULL + 8 * i);
     };
-    // O_i += P_i(t) V(t) : two halves of the value dims, 8 MMAs of K = 16 keys each.
+    // O_i += P_i(t) V(t): 8 MMAs of K = 16 keys, N = 128 value dims when the
+    // two value halves sit in adjacent slots, else two N = 64 passes.
     auto issue_PV = [&](int i, int t, bool release) {
-      if (!ok) return;
       if (!warp_wait(sBar + B_PREADY + 8 * i, (uint32_t)t & 1u, abort_flag)) { ok = false; return; }
-      tc_fence_after();
-      for (int db = 0; db < 2 && ok; ++db) {
-        const long long L = 5LL * t + 3 + db;
-        if (!wait_full(L)) { ok = false; break; }
-        const uint32_t sv = sRing + (uint32_t)(L % TC_NSLOT) * TC_SLOT;
+      const long long L0 = 5LL * t + 3;
+      for (int db = 0; db < 2; ++db) {
+        if (!wait_full(L0 + db)) { ok = false; return; }
         if (i == 0 && t == ntiles - 1 && 128LL * t + 128 > key_hi) {
           // Rows past the last key may hold stale bytes of the page; P is 0
           // there, but 0 * NaN is not, so zero them before the product.
           const int first = (int)(key_hi - 128LL * t);
-          uint8_t *g = gbase + TC_OFF_RING + (int)(L % TC_NSLOT) * TC_SLOT;
-          for (int e = first * 8 + lane; e < 128 * 8; e += 32)
-            reinterpret_cast<uint4 *>(g)[e] = make_uint4(0, 0, 0, 0);
+          uint4 *g = reinterpret_cast<uint4 *>(gbase + TC_OFF_RING + slot_of(L0 + db) * TC_SLOT);
+          for (int e = first * 8 + lane; e < 128 * 8; e += 32) g[e] = make_uint4(0, 0, 0, 0);
           fence_proxy_async_smem();
           __syncwarp();
-          tc_fence_after();
         }
-        if (lane == 0) {
+      }
+      tc_fence_after();
+      const uint32_t ap = tmem + 128 * i;
+      const uint32_t d = tmem + 256 + 128 * i;
+      const uint32_t s0 = slot_of(L0), s1 = slot_of(L0 + 1);
+      const uint32_t acc0 = t > 0 ? 1u : 0u;
+      if (s1 == s0 + 1) {
+        const uint64_t b0 = dring_v + (uint64_t)((s0 * TC_SLOT) >> 4);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) mma_ts_elect(d, ap + 8 * kk, b0 + 128 * kk, id_pv128, kk > 0 ? 1u : acc0);
+      } else {
+#pragma unroll
+        for (int db = 0; db < 2; ++db) {
+          const uint64_t b0 = dring_v + (uint64_t)(((db ? s1 : s0) * TC_SLOT) >> 4);
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
-            mma_ts(tmem + 256 + 128 * i + 64 * db, tmem + 128 * i + 8 * kk, sdesc_sw128(sv + 2048 * kk, 8192, 1024),
-                   id_pv, (t > 0 || kk > 0) ? 1u : 0u);
-          if (release) mma_commit(sBar + B_EMPTY + 8 * (int)(L % TC_NSLOT));
+            mma_ts_elect(d + 64 * db, ap + 8 * kk, b0 + 128 * kk, id_pv64, kk > 0 ? 1u : acc0);
         }
-        __syncwarp();
+      }
+      if (release) {
+        mma_commit_elect(sBar + B_EMPTY + 8 * s0);
+        mma_commit_elect(sBar + B_EMPTY + 8 * s1);
       }
     };
     issue_S(0, 0, false);
-    issue_S(1, 0, true);
+    if (ok) issue_S(1, 0, true);
     for (int t = 1; t < ntiles && ok; ++t) {
       issue_PV(0, t - 1, false);
-      issue_S(0, t, false);
-      issue_PV(1, t - 1, true);
-      issue_S(1, t, true);
+      if (ok) issue_S(0, t, false);
+      if (ok) issue_PV(1, t - 1, true);
+      if (ok) issue_S(1, t, true);
     }
-    issue_PV(0, ntiles - 1, false);
-    if (ok && lane == 0) mma_commit(sBar + B_OFINAL);
-    __syncwarp();
-    issue_PV(1, ntiles - 1, true);
-    if (ok && lane == 0) mma_commit(sBar + B_OFINAL + 8);
-    __syncwarp();
-    // Every MMA issued must be finished before TMEM is released.
+    if (ok) issue_PV(0, ntiles - 1, false);
+    if (ok) mma_commit_elect(sBar + B_OFINAL);
+    if (ok) issue_PV(1, ntiles - 1, true);
+    if (ok) mma_commit_elect(sBar + B_OFINAL + 8);
+    // Every MMA issued must be finished before TMEM is released (bounded by
+    // time only, even after an abort).
+    mma_commit_elect(sBar + B_DRAIN);
     if (lane == 0) {
-      volatile uint32_t local = 0;  // bounded by time only, even after an abort
-      mma_commit(sBar + B_DRAIN);
+      volatile uint32_t local = 0;
       mbar_wait(sBar + B_DRAIN, 0, &local, 1000000000ull);
     }
     __syncwarp();
@@ -313,11 +335,16 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           for (int e = 0; e < 32; ++e)
             if (j0 + 32 * c + e > pr) s[c][e] = __float_as_uint(NEG_INF);
       }
-      float mx = NEG_INF;
+      // Row max with eight independent chains.
+      float mxv[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) mxv[u] = NEG_INF;
 #pragma unroll
       for (int c = 0; c < 4; ++c)
 #pragma unroll
-        for (int e = 0; e < 32; ++e) mx = fmaxf(mx, __uint_as_float(s[c][e]));
+        for (int e = 0; e < 32; ++e) mxv[e & 7] = fmaxf(mxv[e & 7], __uint_as_float(s[c][e]));
+      const float mx = fmaxf(fmaxf(fmaxf(mxv[0], mxv[1]), fmaxf(mxv[2], mxv[3])),
+                             fmaxf(fmaxf(mxv[4], mxv[5]), fmaxf(mxv[6], mxv[7])));
       const float m_new = fmaxf(m_ref, mx * sl2);
       float factor = 1.f;
       bool resc = false;
@@ -329,7 +356,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         resc = true;
       }
       const float b = m_ref == NEG_INF ? 0.f : m_ref;
-      float sum = 0.f;
+      float sumv[4] = {0.f, 0.f, 0.f, 0.f};
       uint32_t pk[2][32];
 #pragma unroll
       for (int c = 0; c < 4; ++c)
@@ -337,10 +364,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         for (int e = 0; e < 32; e += 2) {
           const float p0 = ex2(fmaf(__uint_as_float(s[c][e]), sl2, -b));
           const float p1 = ex2(fmaf(__uint_as_float(s[c][e + 1]), sl2, -b));
-          sum += p0 + p1;
+          sumv[(e >> 1) & 3] += p0 + p1;
           pk[c >> 1][(c & 1) * 16 + e / 2] = pack_bf16(p0, p1);
         }
-      l = l * factor + sum;
+      l = l * factor + ((sumv[0] + sumv[1]) + (sumv[2] + sumv[3]));
+      tmem_st32(tS, pk[0]);
+      tmem_st32(tS + 32, pk[1]);
       if (__any_sync(0xffffffffu, resc)) {
         // O is quiescent: its last product finished before S(t) did, and the
         // next one waits for this tile's P.
@@ -354,8 +383,6 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           tmem_st32(tO + 32 * c, o);
         }
       }
-      tmem_st32(tS, pk[0]);
-      tmem_st32(tS + 32, pk[1]);
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(sBar + B_PREADY + 8 * wg);
