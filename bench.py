@@ -118,6 +118,27 @@ class Clocks:
                 "reasons": reasons, "samples": len(rows)}
 
 
+def rank_seed(base: int, rank: int) -> int:
+    """Each rank draws its own batch (weak scaling: per-GPU work is fixed)."""
+    return base + rank
+
+
+def max_over_ranks(vals, world: int, device):
+    """Element-wise max over ranks (timings); the only collective of the bench,
+    outside the attention data path."""
+    if world <= 1:
+        return [float(v) for v in vals]
+    import torch.distributed as dist
+    t = torch.tensor([float(v) for v in vals], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def job_throughput(units_per_rank: float, world: int, ms_max: float) -> float:
+    """Whole-job units per second: all ranks' units over the slowest rank's time."""
+    return world * units_per_rank / (ms_max / 1e3)
+
+
 def flush_l2(buf):
     buf.add_(1)
 
@@ -402,7 +423,7 @@ def cpu_baseline_decode(work, budget_s=12.0, max_seqs=16):
 
 def run_decode(args, kvr, rank):
     stream = torch.cuda.current_stream()
-    work = DecodeWorkload(kvr, B=args.batch, seed=1001 + rank)
+    work = DecodeWorkload(kvr, B=args.batch, seed=rank_seed(1001, rank))
     torch.cuda.synchronize()
     with Clocks(torch.cuda.current_device()) as ck:
         ms = timed_run(work, args.steps, args.warmup, stream)
@@ -459,13 +480,9 @@ def main():
         return prefill_only(args, kvr, peaks_d, peaks_src, rank, world)
 
     work, ms, ms_full, ms_swa, clocks, (e2e_ms, h2d, d2h) = run_decode(args, kvr, rank)
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms, e2e_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms, e2e_ms = float(t[0]), float(t[1])
+    ms, e2e_ms = max_over_ranks([ms, e2e_ms], world, "cuda")
     B = work.B
-    value = world * B / (ms / 1e3)
+    value = job_throughput(B, world, ms)
     hbm = peaks_d["hbm_gbs"]
     gbs_full = work.bytes_full() / (ms_full / 1e3) / 1e9
     gbs_swa = work.bytes_swa() / (ms_swa / 1e3) / 1e9
@@ -488,7 +505,7 @@ def main():
                      "frac": round(gbs_full / hbm, 4), "peak_source": peaks_src,
                      "kernel": "full_attn_decode (split kernel + combine)",
                      "traffic": kernel_traffic("full_decode_kernel")},
-        "e2e": {"value": round(world * B / (e2e_ms / 1e3), 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+        "e2e": {"value": round(job_throughput(B, world, e2e_ms), 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": work.launches_per_step * args.steps,
         "clocks": clocks,
@@ -534,15 +551,11 @@ def prefill_only(args, kvr, peaks_d, peaks_src, rank, world):
     with Clocks(torch.cuda.current_device()) as ck:
         pw, pms = run_prefill(kvr, steps, args.warmup, P0=args.prefill_p0, C=args.prefill_c)
     ms_f, ms_s = pw.t_full.mean_ms(), pw.t_swa.mean_ms()
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([pms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        pms = float(t[0])
+    pms = max_over_ranks([pms], world, "cuda")[0]
     flops = pw.flops_full() + pw.flops_swa()
     pk = peaks_d.get("bf16_tflops_sustained", peaks_d["bf16_tflops"])
     tf_full = pw.flops_full() / (ms_f / 1e3) / 1e12
-    res = {"metric": METRIC, "value": round(world * flops / (pms / 1e3) / 1e12, 1), "unit": "TFLOP/s",
+    res = {"metric": METRIC, "value": round(job_throughput(flops, world, pms) / 1e12, 1), "unit": "TFLOP/s",
            "n_gpus": world, "steps": steps, "warmup": args.warmup, "ms_per_step": round(pms, 3),
            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
            "config": {"workload": f"prefill: 1 sequence, {pw.C}-token chunk on {pw.P0} cached tokens; 64 q heads; "
