@@ -197,6 +197,7 @@ kvr_status swa_sink_decode(const kvr_bf16 *q, const int64_t *pos, const int32_t 
   kvr_status s = check_layout(ring, KVR_LAYOUT_RING, "ring");
   if (s) return s;
   if ((s = check_heads(Hq, ring->num_kv_heads, 16))) return s;
+  if (Hq > 1024) return fail(KVR_EUNSUPPORTED, "Hq %d > 1024", Hq);
   if ((s = check_table(rope_cos_sin, max_pos))) return s;
   if (B == 0) return ok();
   if (!q || !pos || !seq || !sinks || !out) return fail(KVR_EINVAL, "q/pos/seq/sinks/out is NULL");

@@ -3,11 +3,16 @@
 // launch.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "common.cuh"
 
 namespace kvr {
+
+// 2-D tensor map over a bf16 tensor viewed as [rows][width], box of 64
+// elements x box_rows rows, 128-byte swizzle.  False if encoding fails.
+bool make_tma_map_2d(CUtensorMap *m, const void *ptr, long long rows, int width, int box_rows);
 
 cudaError_t launch_append(const uint16_t *k, const uint16_t *v, const int64_t *pos, const int32_t *seq,
                           int T, int hkv, const float *table, int64_t max_pos, float value_scale,

@@ -421,37 +421,6 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   }
 }
 
-typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
-                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  if (!fn) {
-    void *p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(p);
-  }
-  return fn;
-}
-
-// 2-D map over a pool tensor viewed as [rows][width] bf16, box 64 x box_rows,
-// 128-byte swizzle.
-bool make_map(CUtensorMap *m, const void *ptr, long long rows, int width, int box_rows) {
-  EncodeTiledFn fn = encode_fn();
-  if (!fn) return false;
-  cuuint64_t dims[2] = {(cuuint64_t)width, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)width * 2};
-  cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
-  cuuint32_t estr[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 }  // namespace
 
 cudaError_t launch_full_prefill(const uint16_t *q, int64_t P0, int C, int seq, int hq, const KvView &pool,
@@ -464,7 +433,7 @@ cudaError_t launch_full_prefill(const uint16_t *q, int64_t P0, int C, int seq, i
   const int low = pool.block_size & -pool.block_size;
   const int box_rows = low < 128 ? low : 128;
   CUtensorMap mk, mv;
-  if (!make_map(&mk, pool.k, rows, DQK, box_rows) || !make_map(&mv, pool.v, rows, DV, box_rows))
+  if (!make_tma_map_2d(&mk, pool.k, rows, DQK, box_rows) || !make_tma_map_2d(&mv, pool.v, rows, DV, box_rows))
     return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(full_prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM);
   if (e != cudaSuccess) return e;
