@@ -423,7 +423,7 @@ def cpu_baseline_decode(work, budget_s=12.0, max_seqs=16):
 
 def run_decode(args, kvr, rank):
     stream = torch.cuda.current_stream()
-    work = DecodeWorkload(kvr, B=args.batch, seed=rank_seed(1001, rank))
+    work = DecodeWorkload(kvr, B=args.batch, ctx=args.ctx, seed=rank_seed(1001, rank))
     torch.cuda.synchronize()
     with Clocks(torch.cuda.current_device()) as ck:
         ms = timed_run(work, args.steps, args.warmup, stream)
@@ -448,15 +448,25 @@ def main():
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="flash_decode", choices=["flash_decode", "prefill"])
+    ap.add_argument("--workload", default="flash_decode",
+                    choices=["flash_decode", "long_decode", "prefill", "pro_mixed"])
     ap.add_argument("--no-prefill", action="store_true", help="skip the prefill sub-measurement")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--batch", type=int, default=64, help="decode batch per GPU (64 = the Flash-shaped workload)")
+    ap.add_argument("--batch", type=int, default=None, help="decode batch per GPU (default: the workload's)")
+    ap.add_argument("--ctx", type=int, default=None, help="cached tokens per sequence (default: the workload's)")
     ap.add_argument("--prefill-p0", type=int, default=122880, help="cached tokens before the prefill chunk")
     ap.add_argument("--prefill-c", type=int, default=8192, help="prefill chunk length")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    if args.workload == "long_decode":
+        args.batch = args.batch or 16
+        args.ctx = args.ctx or 524288
+        if "--steps" not in sys.argv:
+            args.steps = 200
+    else:
+        args.batch = args.batch or 64
+        args.ctx = args.ctx or 32768
 
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -478,6 +488,8 @@ def main():
     peaks_d, peaks_src = peaks()
     if args.workload == "prefill":
         return prefill_only(args, kvr, peaks_d, peaks_src, rank, world)
+    if args.workload == "pro_mixed":
+        return pro_mixed(args, kvr, peaks_d, peaks_src, rank, world)
 
     work, ms, ms_full, ms_swa, clocks, (e2e_ms, h2d, d2h) = run_decode(args, kvr, rank)
     ms, e2e_ms = max_over_ranks([ms, e2e_ms], world, "cuda")
@@ -490,8 +502,8 @@ def main():
         "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": f"flash_decode: batch {B}, 64 q heads; windowed layer 8 KV heads ring 128 + sink; "
-                               "full layer 4 KV heads at context 32769; dims 192/192/128; value scale 0.707",
+        "config": {"workload": f"{args.workload}: batch {B}, 64 q heads; windowed layer 8 KV heads ring 128 + sink; "
+                               f"full layer 4 KV heads at context {work.p + 1}; dims 192/192/128; value scale 0.707",
                    "global_batch": B * world, "seq_len": work.p + 1, "parallelism": f"dp{world}",
                    "l2": f"inputs > L2: full pool {work.bytes_full() / 1e9:.2f} GB read per step; windowed rings "
                          f"rotated over {len(work.rings)} copies ({len(work.rings) * work.bytes_swa() / 1e9:.2f} GB)"},
@@ -511,8 +523,8 @@ def main():
         "clocks": clocks,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        res["cpu_baseline"] = cpu_baseline_decode(work)
-    if not args.no_prefill:
+        res["cpu_baseline"] = cpu_baseline_decode(work, max_seqs=16 if args.workload == "flash_decode" else 2)
+    if not args.no_prefill and args.workload == "flash_decode":
         del work
         torch.cuda.empty_cache()
         psteps = min(5, args.steps)
@@ -570,6 +582,143 @@ def prefill_only(args, kvr, peaks_d, peaks_src, rank, world):
                         "frac": round(tf_full / pk, 4), "peak_source": peaks_src + " (sustained)",
                         "kernel": "full_prefill_tc_kernel", "traffic": kernel_traffic("full_prefill_tc_kernel")},
            "gpu_launches": pw.launches_per_step * steps, "clocks": ck.summary()}
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+
+
+class ProMixedWorkload:
+    """One decode step over a 70-layer stack (layer i is full-attention iff
+    i % 7 == 6: 10 full, 60 windowed), 128 sequences with contexts
+    log-uniform over [1K, 1M], 64 q heads, windowed 8 KV heads, full 4 KV
+    heads, value scale 0.612.  Full layers share `n_pools` distinct pools
+    (layer l -> pool l mod n_pools; every pool is far larger than L2, so each
+    layer still streams its full bytes from HBM)."""
+
+    def __init__(self, kvr, B=128, hq=64, layers=70, vscale=0.612, seed=1004, n_pools=None, device="cuda"):
+        from sinks_kv_ring_gb300.synth import Synth, ragged_contexts
+        self.kvr, self.B, self.hq, self.vscale = kvr, B, hq, vscale
+        self.hkv_full, self.hkv_swa = 4, 8
+        dev = device
+        self.ctx = ragged_contexts(B, 1024, 1 << 20, seed)        # cached tokens per sequence
+        self.max_ctx = max(self.ctx) + 1
+        self.kinds = ["full" if i % 7 == 6 else "swa" for i in range(layers)]
+        self.t4 = kvr.rope_table(1e4, self.max_ctx, device=dev)
+        self.t7 = kvr.rope_table(1e7, self.max_ctx, device=dev)
+        bsz = 64
+        mb = [(c + 1 + bsz - 1) // bsz for c in self.ctx]
+        nblk = sum(mb)
+        pool_bytes = nblk * self.hkv_full * bsz * 640
+        free = torch.cuda.mem_get_info()[0]
+        if n_pools is None:
+            n_pools = max(1, min(10, int((free - 16e9) * 0.85 // pool_bytes)))
+        self.n_pools = n_pools
+        bt = torch.zeros(B, max(mb), dtype=torch.int32)
+        off = 0
+        for b, m in enumerate(mb):
+            bt[b, :m] = torch.arange(off, off + m, dtype=torch.int32)
+            off += m
+        bt = bt.to(dev)
+        syn_f = Synth(seed, layer=1, device=dev)
+        k0 = torch.empty(nblk, self.hkv_full, bsz, 192, dtype=torch.bfloat16, device=dev)
+        v0 = torch.empty(nblk, self.hkv_full, bsz, 128, dtype=torch.bfloat16, device=dev)
+        first = kvr.PagedLayout(k0, v0, bt)
+        _fill_pool(kvr, first, syn_f, range(B), self.ctx, self.t7, vscale)
+        self.pools = [first] + [kvr.PagedLayout(k0.clone(), v0.clone(), bt) for _ in range(n_pools - 1)]
+        syn_s = Synth(seed, layer=0, device=dev)
+        ring0 = kvr.RingLayout.empty(B, self.hkv_swa, device=dev)
+        for b, c in enumerate(self.ctx):
+            lo = max(0, c - 127)
+            kk, vv = syn_s.k(c - lo, self.hkv_swa, seq=b, start=lo), syn_s.v(c - lo, self.hkv_swa, seq=b, start=lo)
+            kvr.kv_ring_append_rope(kk, vv, torch.arange(lo, c, device=dev),
+                                    torch.full((c - lo,), b, dtype=torch.int32, device=dev), self.t4, vscale, ring0)
+        n_swa = self.kinds.count("swa")
+        self.rings = [ring0] + [kvr.RingLayout(ring0.k.clone(), ring0.v.clone(), ring0.slot_pos.clone())
+                                for _ in range(n_swa - 1)]
+        self.pos = torch.tensor(self.ctx, dtype=torch.int64, device=dev)   # the new token's position
+        self.seq = torch.arange(B, dtype=torch.int32, device=dev)
+        self.q = syn_s.q(B, hq, self.hkv_swa, seq=50_000)
+        self.k_new = {h: syn_s.k(B, h, seq=60_000) for h in (4, 8)}
+        self.v_new = {h: syn_s.v(B, h, seq=60_000) for h in (4, 8)}
+        self.sinks = syn_s.sinks(hq).to(dev)
+        self.ws = torch.empty(kvr.full_attn_decode_workspace_size(B, hq, self.hkv_full, self.max_ctx),
+                              dtype=torch.uint8, device=dev)
+        self.out = torch.empty(B, hq, 128, dtype=torch.bfloat16, device=dev)
+        self.launches_per_step = sum(4 if k == "full" else 2 for k in self.kinds)
+        self.graph = None
+
+    def bytes_per_step(self):
+        full = sum(c + 1 for c in self.ctx) * self.hkv_full * 640
+        swa = sum(min(128, c + 1) for c in self.ctx) * self.hkv_swa * 640
+        return self.kinds.count("full") * full + self.kinds.count("swa") * swa
+
+    def buckets(self):
+        edges = [(0, 65536, "0-64K"), (65536, 262144, "64K-256K"), (262144, 1 << 21, "256K-1M")]
+        out = {}
+        for lo, hi, name in edges:
+            sel = [c for c in self.ctx if lo <= c + 1 < hi]
+            out[name] = {"sequences": len(sel), "tokens": int(sum(sel))}
+        return out
+
+    def _eager_step(self, stream):
+        kvr = self.kvr
+        fi = si = 0
+        for kind in self.kinds:
+            if kind == "full":
+                pool = self.pools[fi % self.n_pools]
+                fi += 1
+                kvr.kv_ring_append_rope(self.k_new[4], self.v_new[4], self.pos, self.seq, self.t7, self.vscale, pool,
+                                        stream=stream)
+                kvr.full_attn_decode(self.q, self.pos, self.seq, pool, self.t7, SCALE, self.max_ctx,
+                                     workspace=self.ws, out=self.out, stream=stream)
+            else:
+                ring = self.rings[si]
+                si += 1
+                kvr.kv_ring_append_rope(self.k_new[8], self.v_new[8], self.pos, self.seq, self.t4, self.vscale, ring,
+                                        stream=stream)
+                kvr.swa_sink_decode(self.q, self.pos, self.seq, ring, self.sinks, self.t4, SCALE, out=self.out,
+                                    stream=stream)
+
+    def capture(self):
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            self._eager_step(s)          # warm (attributes, maps)
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph):
+            self._eager_step(torch.cuda.current_stream())
+        torch.cuda.synchronize()
+
+    def step(self, stream, timed=False):
+        self.graph.replay()
+
+
+def pro_mixed(args, kvr, peaks_d, peaks_src, rank, world):
+    work = ProMixedWorkload(kvr, seed=rank_seed(1004, rank))
+    work.capture()
+    stream = torch.cuda.current_stream()
+    steps = args.steps if "--steps" in sys.argv else 20
+    with Clocks(torch.cuda.current_device()) as ck:
+        ms = timed_run(work, steps, args.warmup, stream)
+    ms = max_over_ranks([ms], world, "cuda")[0]
+    gbs = work.bytes_per_step() / (ms / 1e3) / 1e9
+    hbm = peaks_d["hbm_gbs"]
+    res = {"metric": METRIC, "value": round(job_throughput(work.B, world, ms), 1), "unit": "tokens/s",
+           "n_gpus": world, "steps": steps, "warmup": args.warmup, "ms_per_step": round(ms, 3),
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+           "config": {"workload": "pro_mixed: 128 sequences, contexts log-uniform 1K-1M (seed 1004); 70 layers "
+                                  "(i % 7 == 6 full: 10 full, 60 windowed); 64 q heads, windowed 8 KV heads, full 4 "
+                                  "KV heads; value scale 0.612; one decode step as one CUDA graph",
+                      "global_batch": work.B * world, "seq_len": work.max_ctx, "parallelism": f"dp{world}",
+                      "buckets": work.buckets(), "distinct_full_pools": work.n_pools,
+                      "total_context_tokens": int(sum(work.ctx)),
+                      "l2": "inputs > L2: each full layer streams its pool (tens of GB); 60 distinct rings"},
+           "hbm_gbs": round(gbs, 1),
+           "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s",
+                        "frac": round(gbs / hbm, 4), "peak_source": peaks_src, "kernel": "whole 70-layer step",
+                        "traffic": None},
+           "gpu_launches": work.launches_per_step * steps, "clocks": ck.summary()}
     if rank == 0:
         print(json.dumps(res), flush=True)
 

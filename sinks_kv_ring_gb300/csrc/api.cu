@@ -127,6 +127,23 @@ cudaStream_t as_stream(void *s) { return static_cast<cudaStream_t>(s); }
 }  // namespace
 
 namespace kvr {
+namespace {
+constexpr int MAX_KSLOT = 16;
+unsigned char g_smem_done[MAX_DEV][MAX_KSLOT];
+}  // namespace
+
+cudaError_t ensure_smem_limit(int slot, const void *func, int bytes) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= MAX_DEV || slot < 0 || slot >= MAX_KSLOT) return cudaErrorInvalidValue;
+  if (g_smem_done[dev][slot]) return cudaSuccess;
+  std::lock_guard<std::mutex> lk(g_mu);
+  e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) g_smem_done[dev][slot] = 1;
+  return e;
+}
+
 int num_sms() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEV) return 152;

@@ -240,7 +240,7 @@ cudaError_t launch_full_decode(const uint16_t *q, const int64_t *pos, const int3
                                const KvView &pool, const float *table, int64_t max_pos,
                                float softmax_scale, long long max_ctx, void *ws, uint16_t *out,
                                unsigned *status, cudaStream_t st) {
-  cudaError_t e = cudaFuncSetAttribute(full_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, FD_SMEM);
+  cudaError_t e = ensure_smem_limit(0, (const void *)full_decode_kernel, FD_SMEM);
   if (e != cudaSuccess) return e;
   const int hkv = pool.hkv, G = hq / hkv;
   const DecodePlan pl = full_decode_plan(B, hkv, max_ctx);

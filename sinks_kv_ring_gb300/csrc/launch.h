@@ -14,6 +14,11 @@ namespace kvr {
 // elements x box_rows rows, 128-byte swizzle.  False if encoding fails.
 bool make_tma_map_2d(CUtensorMap *m, const void *ptr, long long rows, int width, int box_rows);
 
+// Raise a kernel's dynamic shared-memory limit once per (kernel slot, device);
+// later launches make no attribute call (so they can sit in a stream capture).
+// `slot` is a small distinct integer per kernel.
+cudaError_t ensure_smem_limit(int slot, const void *func, int bytes);
+
 cudaError_t launch_append(const uint16_t *k, const uint16_t *v, const int64_t *pos, const int32_t *seq,
                           int T, int hkv, const float *table, int64_t max_pos, float value_scale,
                           const KvView &dst, unsigned *status, cudaStream_t st);

@@ -279,10 +279,6 @@ __global__ void __launch_bounds__(PF_WARPS * 32, 2)
   (void)status;
 }
 
-template <class K>
-cudaError_t set_smem(K kernel, int bytes) {
-  return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-}
 
 }  // namespace
 
@@ -293,7 +289,7 @@ cudaError_t launch_swa_prefill(const uint16_t *q, int64_t P0, int C, int seq, in
   (void)max_pos;
   const int hkv = ring.hkv, G = hq / hkv;
   auto kern = prefill_kernel<SwaSrc, true>;
-  cudaError_t e = set_smem(kern, PF_SMEM);
+  cudaError_t e = ensure_smem_limit(3, (const void *)kern, PF_SMEM);
   if (e != cudaSuccess) return e;
   SwaSrc src{ring.k + (long long)seq * hkv * WIN * DQK, ring.v + (long long)seq * hkv * WIN * DV,
              ring.slot_pos + (long long)seq * WIN, chunk.k, chunk.v, hkv, 0, P0};

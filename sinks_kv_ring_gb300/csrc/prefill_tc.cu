@@ -435,7 +435,7 @@ cudaError_t launch_full_prefill(const uint16_t *q, int64_t P0, int C, int seq, i
   CUtensorMap mk, mv;
   if (!make_tma_map_2d(&mk, pool.k, rows, DQK, box_rows) || !make_tma_map_2d(&mv, pool.v, rows, DV, box_rows))
     return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(full_prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM);
+  cudaError_t e = ensure_smem_limit(2, (const void *)full_prefill_tc_kernel, TC_SMEM);
   if (e != cudaSuccess) return e;
   TcArgs a;
   a.q = q;

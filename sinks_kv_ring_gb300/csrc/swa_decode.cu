@@ -343,7 +343,7 @@ cudaError_t launch_swa_decode(const uint16_t *q, const int64_t *pos, const int32
   CUtensorMap mk, mv;
   if (!make_tma_map_2d(&mk, ring.k, rows, DQK, WIN) || !make_tma_map_2d(&mv, ring.v, rows, DV, WIN))
     return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(swa_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SD_SMEM);
+  cudaError_t e = ensure_smem_limit(1, (const void *)swa_decode_kernel, SD_SMEM);
   if (e != cudaSuccess) return e;
   SdArgs a;
   a.q = q;

@@ -1,0 +1,135 @@
+"""GPU parity at the full workload sizes, in the launch configuration bench.py
+times: sampled outputs against the fp64 oracle.
+
+* Flash-shaped decode: batch 64, 64 q heads, windowed layer (8 KV heads) and
+  full layer (4 KV heads) at context 32769 -- sampled sequences, all heads.
+* Chunked prefill: 8192-token chunk on 122880 cached tokens -- sampled rows
+  (first, last, window and tile boundaries), all heads, both layer kinds.
+* Long-context decode: batch 16 at context 524289 -- sampled sequences.
+
+Raw K/V are regenerated from the same seeded draws the bench used (never read
+back from the CUDA path).
+"""
+import math
+import os
+import sys
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+
+from kvr_cases import compare_rows
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+pytestmark = pytest.mark.gpu
+SCALE = 1.0 / math.sqrt(192.0)
+
+
+@pytest.fixture(scope="module")
+def kvr():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from sinks_kv_ring_gb300 import build
+    build.build()
+    import sinks_kv_ring_gb300 as k
+    k.device_status(reset=True)
+    return k
+
+
+def _pool_raw(syn, hkv, b, n, chunk=65536):
+    """Raw K/V of positions 0..n-1 as bench._fill_pool drew them."""
+    ks = [syn.k(min(chunk, n - lo), hkv, seq=b, start=lo) for lo in range(0, n, chunk)]
+    vs = [syn.v(min(chunk, n - lo), hkv, seq=b, start=lo) for lo in range(0, n, chunk)]
+    return torch.cat(ks), torch.cat(vs)
+
+
+def _decode_check(kvr, work, seqs, label):
+    import bench
+    from sinks_kv_ring_gb300.synth import Synth
+    stream = torch.cuda.current_stream()
+    work.step(stream)
+    torch.cuda.synchronize()
+    assert kvr.device_status() == 0
+    p = work.p
+    syn_f = Synth(1001, layer=1, device="cuda")
+    syn_s = Synth(1001, layer=0, device="cuda")
+    sk = work.sinks.double().cpu().numpy()
+    lo = max(0, p - 127)
+    for b in seqs:
+        kf, vf = _pool_raw(syn_f, work.hkv_full, b, p)
+        kf = torch.cat([kf, work.k_full[b:b + 1]])
+        vf = torch.cat([vf, work.v_full[b:b + 1]])
+        want = oracle.attend_seq(work.q_full[b:b + 1], [p], kf, vf, 0, 1e7, work.vscale, SCALE, 0, None)
+        compare_rows(work.out_full[b:b + 1], want, f"{label} full b={b}")
+        ks = torch.cat([syn_s.k(p - lo, work.hkv_swa, seq=b, start=lo), work.k_swa[b:b + 1]])
+        vs = torch.cat([syn_s.v(p - lo, work.hkv_swa, seq=b, start=lo), work.v_swa[b:b + 1]])
+        want = oracle.attend_seq(work.q_swa[b:b + 1], [p], ks, vs, lo, 1e4, work.vscale, SCALE, 128, sk)
+        compare_rows(work.out_swa[b:b + 1], want, f"{label} swa b={b}")
+
+
+def test_flash_decode_full_size_sampled(kvr):
+    import bench
+    work = bench.DecodeWorkload(kvr, B=64, ctx=32768, seed=1001, swa_copies=1)
+    _decode_check(kvr, work, [0, 17, 63], "flash decode")
+    # the no-allocation variant on the same full-size batch
+    out2 = kvr.full_attn_decode_noalloc(work.q_full, work.pos, work.seq, work.pool, work.t7, SCALE, work.max_ctx)
+    torch.cuda.synchronize()
+    assert torch.equal(out2, work.out_full)
+    del work
+    torch.cuda.empty_cache()
+
+
+def test_long_context_decode_full_size_sampled(kvr):
+    import bench
+    work = bench.DecodeWorkload(kvr, B=16, ctx=524288, seed=1001, swa_copies=1)
+    _decode_check(kvr, work, [0, 15], "long decode")
+    del work
+    torch.cuda.empty_cache()
+
+
+def test_chunked_prefill_full_size_sampled(kvr):
+    import bench
+    from sinks_kv_ring_gb300.synth import Synth
+    work = bench.PrefillWorkload(kvr, P0=122880, C=8192, seed=1002)
+    work.step(torch.cuda.current_stream())
+    torch.cuda.synchronize()
+    assert kvr.device_status() == 0
+    P0, C = work.P0, work.C
+    rows = [0, 1, 126, 127, 128, 255, 256, 4095, 8190, 8191]
+    sf, ss = Synth(1002, layer=1, device="cuda"), Synth(1002, layer=0, device="cuda")
+    # full layer: keys 0 .. P0 + C - 1
+    kf, vf = _pool_raw(sf, work.hkv_full, 0, P0)
+    kf, vf = torch.cat([kf, work.kf]), torch.cat([vf, work.vf])
+    want = oracle.attend_seq(work.qf[rows], np.array(rows) + P0, kf, vf, 0, 1e7, work.vscale, SCALE, 0, None)
+    compare_rows(work.out_f[rows], want, "prefill full")
+    # windowed layer: ring positions P0-127 .. P0-1 then the chunk
+    lo = P0 - 127
+    ks = torch.cat([ss.k(127, work.hkv_swa, seq=0, start=lo), work.ks])
+    vs = torch.cat([ss.v(127, work.hkv_swa, seq=0, start=lo), work.vs])
+    want = oracle.attend_seq(work.qs[rows], np.array(rows) + P0, ks, vs, lo, 1e4, work.vscale, SCALE, 128,
+                             work.sinks.double().cpu().numpy())
+    compare_rows(work.out_s[rows], want, "prefill swa")
+    del work
+    torch.cuda.empty_cache()
+
+
+def test_zero_length_calls_are_no_ops(kvr):
+    import sinks_kv_ring_gb300 as k
+    t = k.rope_table(1e7, 64)
+    pool = k.PagedLayout.contiguous(1, 4, 64)
+    out = torch.full((0, 64, 128), 7, dtype=torch.bfloat16, device="cuda")
+    k.full_attn_prefill_chunk(torch.empty(0, 64, 192, dtype=torch.bfloat16, device="cuda"), 10, 0, pool, t, SCALE,
+                              out=out)
+    ring = k.RingLayout.empty(1, 8)
+    stage = k.LinearLayout.empty(1, 8)
+    k.swa_sink_prefill_chunk(torch.empty(0, 64, 192, dtype=torch.bfloat16, device="cuda"), 10, 0, stage, ring,
+                             torch.zeros(64, device="cuda"), k.rope_table(1e4, 64), SCALE, out=out)
+    k.full_attn_decode(torch.empty(0, 64, 192, dtype=torch.bfloat16, device="cuda"),
+                       torch.empty(0, dtype=torch.int64, device="cuda"), torch.empty(0, dtype=torch.int32, device="cuda"),
+                       pool, t, SCALE, 64, out=torch.empty(0, 64, 128, dtype=torch.bfloat16, device="cuda"))
+    torch.cuda.synchronize()
+    assert k.device_status() == 0
