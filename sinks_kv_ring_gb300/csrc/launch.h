@@ -14,6 +14,12 @@ namespace kvr {
 // elements x box_rows rows, 128-byte swizzle.  False if encoding fails.
 bool make_tma_map_2d(CUtensorMap *m, const void *ptr, long long rows, int width, int box_rows);
 
+// 3-D tensor map over [rows][width] bf16 viewed as [rows][width/64][64]: one
+// box brings box_rows whole rows (every 64-element part), so a row is read
+// in one pass; in shared memory the box is [row][part][64] with the 128-byte
+// swizzle applied per 128-byte segment (segment index = row * parts + part).
+bool make_tma_map_rows3d(CUtensorMap *m, const void *ptr, long long rows, int width, int box_rows);
+
 // Raise a kernel's dynamic shared-memory limit once per (kernel slot, device);
 // later launches make no attribute call (so they can sit in a stream capture).
 // `slot` is a small distinct integer per kernel.

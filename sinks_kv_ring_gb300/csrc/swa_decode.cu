@@ -5,19 +5,25 @@
 // the softmax denominator and nothing else; "System One mode and prompt
 // reuse": position p sits in slot p mod 128 and the ring records the position
 // each slot holds.  gaudi-cookbook "MiMo-V2.6-Flash on Gaudi 2", "What was
-// built": the window is exactly the last 128 positions.
+// built": the window is exactly the last 128 positions.  Decode is
+// memory-bound (Xiaomi "Full-Pipeline Inference Optimization", section 1.2).
 //
-// A unit is one (sequence, KV head): 128 ring slots = 48 KB of K + 32 KB of V,
-// contiguous in the ring.  The kernel is persistent (two CTAs per SM, each
-// with one K/V stage, so one CTA's products and merge overlap the other's
-// loads): 8 warps compute unit n (16 slots each; the G query heads are the 16
-// rows of an m16n8k16 bf16 MMA) from five 128-byte-swizzled TMA boxes, while
-// the threads already hold unit n+1's rotated query rows and slot tags in
-// registers.  Each warp keeps
-// its own softmax state; the 8 states and the sink are merged once at the
-// end of the unit.  Decode is memory-bound (Xiaomi "Full-Pipeline Inference
-// Optimization", section 1.2): the point of the design is to keep the ring
-// bytes streaming while the small products run.
+// A unit is one (sequence, KV head): 128 ring slots, 48 KB of K and 32 KB of
+// V, contiguous in the ring, brought into shared memory by two 3-D TMA boxes
+// that read whole K and V rows.  The kernel is persistent with two CTAs per
+// SM (one 80 KB stage each), so one CTA's products overlap the other's loads;
+// the ring rows of all of a CTA's units are staged first, and the next unit's
+// query rows and slot tags are prefetched into registers.  Per unit (the code
+// can also stream a unit in parts with online rescaling; one part measured
+// fastest), with 8 warps:
+//   1. warp w: S = Q K^T for slots 16w..16w+15 (m16n8k16, the G query heads
+//      are the 16 MMA rows), masked by the slot tags; row maxima;
+//   2. the row maximum over all slots and the sink, P = e^{s-M} as bf16 in
+//      shared memory, row sums;
+//   3. warp w: O[:, 16w..16w+15] = P V over all 128 slots -- the value
+//      columns are split across warps, so no warp merges another warp's
+//      numerators -- normalised by the full denominator, in which the sink
+//      is counted once.
 #include <cuda.h>
 
 #include "launch.h"
@@ -31,24 +37,35 @@ using namespace tc;
 
 constexpr int SD_WARPS = 8;
 constexpr int SD_THREADS = SD_WARPS * 32;
-constexpr int SD_BOX = 16384;                        // 128 rows x 128 bytes
-constexpr int SD_STAGE = 5 * SD_BOX;                 // K: 3 boxes, V: 2 boxes (80 KB)
-constexpr int SD_NSTAGE = 1;                        // K/V stages per CTA (2 CTAs share an SM)
-constexpr int SD_OFF_Q = SD_NSTAGE * SD_STAGE;       // two [16][192] query tiles
+constexpr int SD_PARTS = 1;                              // parts (stages) per unit
+constexpr int SD_CTAS = 2;                               // CTAs per SM
+constexpr int SD_NSTAGE = 1;                             // stages per CTA
+constexpr int SD_HALF = WIN / SD_PARTS;                  // slots per part
+constexpr int SD_SPW = SD_HALF / SD_WARPS;               // slots per warp in phase 1 (8 or 16)
+constexpr int SD_NT = SD_SPW / 8;                        // 8-key MMA tiles per warp
+constexpr int SD_HK = SD_HALF * DQK * 2;                 // K bytes per part
+constexpr int SD_HSTAGE = SD_HK + SD_HALF * DV * 2;      // + V bytes
+constexpr int SD_OFF_Q = SD_NSTAGE * SD_HSTAGE;          // two [16][192] query tiles
 constexpr int SD_QTILE = 16 * DQK * 2;
-constexpr int SD_OFF_TAG = SD_OFF_Q + 2 * SD_QTILE;  // two [128] int32 tag arrays
-constexpr int SD_OFF_SINK = SD_OFF_TAG + 2 * WIN * 4;  // [hq] sinks * log2(e)
+constexpr int SD_OFF_TAG = SD_OFF_Q + 2 * SD_QTILE;      // two [128] int32 tag arrays
+constexpr int SD_OFF_SINK = SD_OFF_TAG + 2 * WIN * 4;    // [hq] sinks * log2(e)
 constexpr int SD_MAX_HQ = 1024;
-constexpr int SD_OFF_FAC = SD_OFF_SINK + SD_MAX_HQ * 4;  // [16][8] merge factors, [16] 1/L
-constexpr int SD_OFF_BAR = SD_OFF_FAC + 16 * (SD_WARPS + 1) * 4;
-constexpr int SD_SMEM = SD_OFF_BAR + 64 + 1024;
+constexpr int SD_OFF_P = SD_OFF_SINK + SD_MAX_HQ * 4;    // [16][part slots] bf16 probabilities
+constexpr int SD_OFF_RED = SD_OFF_P + 16 * SD_HALF * 2;  // [8 warps][16] row max, then row sums
+constexpr int SD_MAX_UNITS = 256;                        // units per CTA whose ring rows are staged
+constexpr int SD_OFF_ROW = SD_OFF_RED + 2 * SD_WARPS * 16 * 4;
+constexpr int SD_OFF_BAR = SD_OFF_ROW + SD_MAX_UNITS * 4;
+constexpr int SD_SMEM = SD_OFF_BAR + 8 * SD_NSTAGE + 32 + 1024;
 constexpr unsigned ST_TIMEOUT = 8u;
-static_assert(SD_WARPS * 16 * (MO_STRIDE + 2) * 4 <= SD_STAGE, "merge area fits in a stage");
 
-// Byte offset of 16-byte chunk ch of row r in a [boxes][128 rows][128 B] tile
-// written by TMA with the 128-byte swizzle (chunk bits 4..6 ^ row bits 0..2).
-__device__ __forceinline__ uint32_t sw128(int r, int ch) {
-  return (uint32_t)((ch >> 3) * SD_BOX + r * 128 + (((ch & 7) ^ (r & 7)) << 4));
+// Byte offset of 16-byte chunk ch of row r in a [rows][PARTS][128 B] tile
+// written by a 3-D TMA box with the 128-byte swizzle: segment
+// seg = r * PARTS + ch / 8, chunk (ch % 8) ^ (seg % 8).  For PARTS = 3 the 8
+// rows an ldmatrix reads at one chunk land on 8 different bank groups.
+template <int PARTS>
+__device__ __forceinline__ uint32_t swrow(int r, int ch) {
+  const int seg = r * PARTS + (ch >> 3);
+  return (uint32_t)(seg * 128 + (((ch & 7) ^ (seg & 7)) << 4));
 }
 
 struct SdArgs {
@@ -107,7 +124,7 @@ __device__ __forceinline__ void prefetch_unit(const SdArgs &a, int u, int tid, U
   if (tid < WIN && ok) pf.tag = a.slot_pos[(long long)s * WIN + tid];
 }
 
-// Rotate (threads 0..63) and store a prefetched unit into Q tile / tag buffer.
+// Rotate (threads 0..63) and store a prefetched unit into a Q tile / tag buffer.
 __device__ __forceinline__ void store_unit(const UnitPrefetch &pf, int tid, uint8_t *sQ, int32_t *sTag) {
   const int r = tid >> 4, ch = 8 + (tid & 15);
   *reinterpret_cast<uint4 *>(sQ + swz<DQK>(r, ch)) = pf.pass;
@@ -126,7 +143,7 @@ __device__ __forceinline__ void store_unit(const UnitPrefetch &pf, int tid, uint
   if (tid < WIN) sTag[tid] = pf.tag;
 }
 
-__global__ void __launch_bounds__(SD_THREADS, 2)
+__global__ void __launch_bounds__(SD_THREADS, SD_CTAS)
     swa_decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                       const SdArgs a) {
   extern __shared__ uint8_t smem_raw[];
@@ -134,49 +151,62 @@ __global__ void __launch_bounds__(SD_THREADS, 2)
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t *g = smem_raw + (base - raw);
   const uint32_t sBar = base + SD_OFF_BAR;
-  volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(g + SD_OFF_BAR + 32);
+  volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(g + SD_OFF_BAR + 8 * SD_NSTAGE);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int units = a.B * a.hkv;
   const int nmine = units > (int)blockIdx.x ? (units - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x : 0;
   const int G = a.G;
   auto unit_id = [&](int n) { return (int)blockIdx.x + n * (int)gridDim.x; };
-
-  if (tid == 0) {
-    mbar_init(sBar, 1);
-    mbar_init(sBar + 8, 1);
-    *abort_flag = 0;
-    fence_mbar_init();
-  }
-  float *sSink = reinterpret_cast<float *>(g + SD_OFF_SINK);
-  float *sFac = reinterpret_cast<float *>(g + SD_OFF_FAC);  // [16][8] per-warp factors / L, then [16] 1/L
-  for (int h = tid; h < a.hq; h += SD_THREADS) sSink[h] = a.sinks[h] * LOG2E;
-  __syncthreads();
   if (nmine == 0) return;
+  const int nhalves = SD_PARTS * nmine;
 
-  // Thread 0: the five boxes of unit u into stage st.  An invalid unit still
-  // completes its barrier phase (no bytes).
-  auto issue = [&](int u, int st) {
+  float *sSink = reinterpret_cast<float *>(g + SD_OFF_SINK);
+  uint8_t *sP = g + SD_OFF_P;
+  float *sMax = reinterpret_cast<float *>(g + SD_OFF_RED);  // [8][16]
+  float *sSum = sMax + SD_WARPS * 16;                       // [8][16]
+  int32_t *sRow = reinterpret_cast<int32_t *>(g + SD_OFF_ROW);
+
+  // Ring row of this CTA's n-th unit (-1: invalid unit).
+  auto ring_row = [&](int n) {
     long long p;
     int s;
+    const int u = unit_id(n);
+    return unit_valid(a, u, p, s) ? (s * a.hkv + u % a.hkv) * WIN : -1;
+  };
+  // Thread 0: part H % PARTS of unit H / PARTS into stage H % NSTAGE.  An
+  // invalid unit still completes the stage's barrier phase (no bytes).
+  auto issue = [&](int H, int row) {
+    const int st = H % SD_NSTAGE;
     const uint32_t bar = sBar + 8 * st;
-    if (unit_valid(a, u, p, s)) {
-      const int row = (s * a.hkv + u % a.hkv) * WIN;
-      const uint32_t dst = base + st * SD_STAGE;
-      mbar_expect_tx(bar, SD_STAGE);
-      for (int kb = 0; kb < 3; ++kb) tma_load_2d(dst + kb * SD_BOX, &tmk, 64 * kb, row, bar);
-      for (int db = 0; db < 2; ++db) tma_load_2d(dst + (3 + db) * SD_BOX, &tmv, 64 * db, row, bar);
+    if (row >= 0) {
+      const uint32_t dst = base + st * SD_HSTAGE;
+      const int r = row + SD_HALF * (H % SD_PARTS);
+      mbar_expect_tx(bar, SD_HSTAGE);
+      tma_load_3d(dst, &tmk, 0, 0, r, bar);           // whole 384-byte K rows, one pass
+      tma_load_3d(dst + SD_HK, &tmv, 0, 0, r, bar);   // whole 256-byte V rows
     } else {
       mbar_arrive(bar);
     }
   };
 
-  int issued = -1;  // highest unit index whose stage load was issued (thread 0)
+  // The first loads go out before anything else.
+  int issued = -1;  // highest half whose load was issued (thread 0)
   if (tid == 0) {
-    for (int n = 0; n < SD_NSTAGE && n < nmine; ++n) {
-      issue(unit_id(n), n);
-      issued = n;
+    for (int i = 0; i < SD_NSTAGE; ++i) mbar_init(sBar + 8 * i, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    int row = -1, row_n = -1;
+    for (int H = 0; H < SD_NSTAGE && H < nhalves; ++H) {
+      if (H / SD_PARTS != row_n) {
+        row_n = H / SD_PARTS;
+        row = ring_row(row_n);
+      }
+      issue(H, row);
+      issued = H;
     }
   }
+  for (int n = tid; n < nmine && n < SD_MAX_UNITS; n += SD_THREADS) sRow[n] = ring_row(n);
+  for (int h = tid; h < a.hq; h += SD_THREADS) sSink[h] = a.sinks[h] * LOG2E;
   {
     UnitPrefetch pf;
     prefetch_unit(a, unit_id(0), tid, pf);
@@ -184,8 +214,9 @@ __global__ void __launch_bounds__(SD_THREADS, 2)
   }
   __syncthreads();
 
-  for (int n = 0; n < nmine; ++n) {
-    const int st = n % SD_NSTAGE;
+  const int qr = lane >> 2;  // this thread's MMA rows: qr and qr + 8
+  bool alive = true;
+  for (int n = 0; n < nmine && alive; ++n) {
     const int u = unit_id(n);
     const int b = u / a.hkv, kv = u % a.hkv;
     long long p;
@@ -194,137 +225,206 @@ __global__ void __launch_bounds__(SD_THREADS, 2)
     const bool has_next = n + 1 < nmine;
     UnitPrefetch nx;
     if (has_next) prefetch_unit(a, unit_id(n + 1), tid, nx);
-
-    const bool landed =
-        __syncthreads_and(mbar_wait(sBar + 8 * st, (uint32_t)(n / SD_NSTAGE) & 1u, abort_flag));
-    if (!landed) break;
     uint16_t *orow = a.out + ((long long)b * a.hq + (long long)kv * G) * DV;
-    uint8_t *sK = g + st * SD_STAGE;
-    uint8_t *sV = sK + 3 * SD_BOX;
     const uint8_t *sQ = g + SD_OFF_Q + (n & 1) * SD_QTILE;
     const int32_t *sTag = reinterpret_cast<const int32_t *>(g + SD_OFF_TAG) + (n & 1) * WIN;
 
-    if (ok) {
-      // A slot is in the window iff it holds a position in (p - 128, p].
-      // Zero the V rows of slots outside it so that stale bytes cannot
-      // reach the product (their P is 0, but 0 * NaN is not).
-      const int r0 = 16 * warp;
+    // Running softmax state of this thread's two rows and its O columns.  The
+    // sink starts the running maximum and contributes e^{sink - M} = 1.
+    const float sk0 = qr < G ? sSink[kv * G + qr] : NEG_INF;
+    const float sk1 = qr + 8 < G ? sSink[kv * G + qr + 8] : NEG_INF;
+    float M0 = sk0, M1 = sk1;
+    float L0 = qr < G ? 1.f : 0.f, L1 = qr + 8 < G ? 1.f : 0.f;
+    float O[2][4];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) O[j][0] = O[j][1] = O[j][2] = O[j][3] = 0.f;
+    uint32_t qf[12][4];
+    if (ok) load_q_frags(sQ, lane, qf);
+
+    for (int h = 0; h < SD_PARTS; ++h) {
+      const int H = SD_PARTS * n + h;
+      const int st = H % SD_NSTAGE;
+      const bool landed =
+          __syncthreads_and(mbar_wait(sBar + 8 * st, (uint32_t)(H / SD_NSTAGE) & 1u, abort_flag));
+      if (!landed) {
+        alive = false;
+        break;
+      }
+      // Every half before H is finished: refill the stage of half H - 1.
+      if (tid == 0 && issued + 1 < nhalves && issued + 1 < H + SD_NSTAGE) {
+        const int H2 = issued + 1;
+        const int n2 = H2 / SD_PARTS;
+        fence_proxy_async_smem();  // generic writes to that stage (zeroed rows) before the TMA writes
+        issue(H2, n2 < SD_MAX_UNITS ? sRow[n2] : ring_row(n2));
+        issued = H2;
+      }
+      if (!ok) continue;
+      uint8_t *sK = g + st * SD_HSTAGE;
+      uint8_t *sV = sK + SD_HK;
+      const int slot0 = SD_HALF * h;  // first ring slot of this half
+
+      // Phase 1: warp w takes slots slot0 + SPW*w .. +SPW-1.  Stale slots (tag
+      // outside (p - 128, p]) are masked, and their V rows zeroed so that
+      // stale bytes cannot reach the product (0 * NaN is not 0).
+      const int r0 = SD_SPW * warp;  // row within the part
       bool valid = false;
-      if (lane < 16) {
-        const int sp = sTag[r0 + lane];
+      if (lane < SD_SPW) {
+        const int sp = sTag[slot0 + r0 + lane];
         valid = sp >= 0 && sp <= p && sp > p - WIN;
       }
-      unsigned bad = __ballot_sync(0xffffffffu, !valid) & 0xffffu;
+      unsigned bad = __ballot_sync(0xffffffffu, !valid) & ((1u << SD_SPW) - 1u);
       while (bad) {
         const int r = r0 + __ffs(bad) - 1;
         bad &= bad - 1;
-        if (lane < 16) *reinterpret_cast<uint4 *>(sV + sw128(r, lane)) = make_uint4(0, 0, 0, 0);
+        if (lane < 16) *reinterpret_cast<uint4 *>(sV + swrow<2>(r, lane)) = make_uint4(0, 0, 0, 0);
       }
-      __syncwarp();
-
-      uint32_t qf[12][4];
-      load_q_frags(sQ, lane, qf);
-      float S[2][4];
+      float S[SD_NT][4];
 #pragma unroll
-      for (int j = 0; j < 2; ++j) S[j][0] = S[j][1] = S[j][2] = S[j][3] = 0.f;
-      const uint32_t kb = smem_u32(sK), vb = smem_u32(sV);
+      for (int j = 0; j < SD_NT; ++j) S[j][0] = S[j][1] = S[j][2] = S[j][3] = 0.f;
       {
-        const int row = r0 + (lane & 7) + ((lane >> 4) << 3);
-        const int csel = (lane >> 3) & 1;
+        const uint32_t kb = smem_u32(sK);
 #pragma unroll
-        for (int kk = 0; kk < 12; ++kk) {
-          uint32_t b0, b1, b2, b3;
-          ldsm_x4(kb + sw128(row, 2 * kk + csel), b0, b1, b2, b3);
-          mma_bf16(S[0], qf[kk], b0, b1);
-          mma_bf16(S[1], qf[kk], b2, b3);
+        for (int j = 0; j < SD_NT; ++j) {
+          const int row = r0 + 8 * j + (lane & 7);
+          const int csel = lane >> 3;  // an x4 load covers chunks 2kk .. 2kk+3 (two k-steps)
+#pragma unroll
+          for (int kk = 0; kk < 12; kk += 2) {
+            uint32_t b0, b1, b2, b3;
+            ldsm_x4(kb + swrow<3>(row, 2 * kk + csel), b0, b1, b2, b3);
+            mma_bf16(S[j], qf[kk], b0, b1);
+            mma_bf16(S[j], qf[kk + 1], b2, b3);
+          }
         }
       }
 #pragma unroll
-      for (int j = 0; j < 2; ++j)
+      for (int j = 0; j < SD_NT; ++j)
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const int slot = r0 + 8 * j + 2 * (lane & 3) + (e & 1);
+          const int slot = slot0 + r0 + 8 * j + 2 * (lane & 3) + (e & 1);
           const int sp = sTag[slot];
           const bool in = sp >= 0 && sp <= p && sp > p - WIN;
           S[j][e] = in ? S[j][e] * a.scale_log2 : NEG_INF;
         }
-      float O[16][4];
-#pragma unroll
-      for (int nt = 0; nt < 16; ++nt) O[nt][0] = O[nt][1] = O[nt][2] = O[nt][3] = 0.f;
-      float m0 = NEG_INF, m1 = NEG_INF, l0 = 0.f, l1 = 0.f;
-      softmax_update(S, m0, m1, l0, l1, O);
       {
-        uint32_t pa[4];
-        pa[0] = pack_bf16(S[0][0], S[0][1]);
-        pa[1] = pack_bf16(S[0][2], S[0][3]);
-        pa[2] = pack_bf16(S[1][0], S[1][1]);
-        pa[3] = pack_bf16(S[1][2], S[1][3]);
-        const int row = r0 + (lane & 7) + (((lane >> 3) & 1) << 3);
-        const int csel = lane >> 4;
+        float x0 = NEG_INF, x1 = NEG_INF;
 #pragma unroll
-        for (int dp = 0; dp < 8; ++dp) {
-          uint32_t b0, b1, b2, b3;
-          ldsm_x4_t(vb + sw128(row, 2 * dp + csel), b0, b1, b2, b3);
-          mma_bf16(O[2 * dp], pa, b0, b1);
-          mma_bf16(O[2 * dp + 1], pa, b2, b3);
+        for (int j = 0; j < SD_NT; ++j) {
+          x0 = fmaxf(x0, fmaxf(S[j][0], S[j][1]));
+          x1 = fmaxf(x1, fmaxf(S[j][2], S[j][3]));
+        }
+        x0 = fmaxf(x0, __shfl_xor_sync(0xffffffffu, x0, 1));
+        x0 = fmaxf(x0, __shfl_xor_sync(0xffffffffu, x0, 2));
+        x1 = fmaxf(x1, __shfl_xor_sync(0xffffffffu, x1, 1));
+        x1 = fmaxf(x1, __shfl_xor_sync(0xffffffffu, x1, 2));
+        if ((lane & 3) == 0) {
+          sMax[warp * 16 + qr] = x0;
+          sMax[warp * 16 + qr + 8] = x1;
         }
       }
-      __syncthreads();  // every warp is done with the stage: reuse it as the merge area
-      float *mml = reinterpret_cast<float *>(sK);   // [8][16][2]
-      float *mo = mml + SD_WARPS * 32;              // [8][16][MO_STRIDE]
-      stash_warp_state(mml + warp * 32, mo + warp * 16 * MO_STRIDE, lane, m0, m1, l0, l1, O);
       __syncthreads();
-      // Per query row: the merged max M (sink included), denominator L, and
-      // each warp's weight e^{m_w - M} / L.
-      if (tid < G) {
-        const float sk = sSink[kv * G + tid];
-        float M = sk;
+      // Phase 2: new running maximum, P = e^{s - M} (bf16) and row sums.
+      float N0 = M0, N1 = M1;
 #pragma unroll
-        for (int w = 0; w < SD_WARPS; ++w) M = fmaxf(M, mml[w * 32 + tid * 2]);
-        float f[SD_WARPS];
-        float L = ex2(sk - M);
+      for (int w = 0; w < SD_WARPS; ++w) {
+        N0 = fmaxf(N0, sMax[w * 16 + qr]);
+        N1 = fmaxf(N1, sMax[w * 16 + qr + 8]);
+      }
+      const float c0 = N0 == NEG_INF ? 0.f : N0, c1 = N1 == NEG_INF ? 0.f : N1;
+      const float f0 = ex2(M0 - c0), f1 = ex2(M1 - c1);  // rescale of the old state (M = -inf gives 0)
+      {
+        float s0 = 0.f, s1 = 0.f;
 #pragma unroll
-        for (int w = 0; w < SD_WARPS; ++w) {
-          const float mw = mml[w * 32 + tid * 2];
-          f[w] = mw == NEG_INF ? 0.f : ex2(mw - M);
-          L += mml[w * 32 + tid * 2 + 1] * f[w];
+        for (int j = 0; j < SD_NT; ++j) {
+          const float p0 = ex2(S[j][0] - c0), p1 = ex2(S[j][1] - c0);
+          const float p2 = ex2(S[j][2] - c1), p3 = ex2(S[j][3] - c1);
+          s0 += p0 + p1;
+          s1 += p2 + p3;
+          const int k0 = r0 + 8 * j + 2 * (lane & 3);  // P tile [16 rows][part slots], chunks swizzled by row
+          *reinterpret_cast<uint32_t *>(sP + swz<SD_HALF>(qr, k0 >> 3) + (k0 & 7) * 2) = pack_bf16(p0, p1);
+          *reinterpret_cast<uint32_t *>(sP + swz<SD_HALF>(qr + 8, k0 >> 3) + (k0 & 7) * 2) = pack_bf16(p2, p3);
         }
-        const float inv = 1.f / L;
-#pragma unroll
-        for (int w = 0; w < SD_WARPS; ++w) sFac[tid * SD_WARPS + w] = f[w] * inv;
+        s0 += __shfl_xor_sync(0xffffffffu, s0, 1);
+        s0 += __shfl_xor_sync(0xffffffffu, s0, 2);
+        s1 += __shfl_xor_sync(0xffffffffu, s1, 1);
+        s1 += __shfl_xor_sync(0xffffffffu, s1, 2);
+        if ((lane & 3) == 0) {
+          sSum[warp * 16 + qr] = s0;
+          sSum[warp * 16 + qr + 8] = s1;
+        }
       }
       __syncthreads();
-      for (int idx = tid; idx < G * DV; idx += SD_THREADS) {
-        const int gq = idx >> 7, d = idx & (DV - 1);
-        float acc = 0.f;
+      // Phase 3: warp w's value columns 16w..16w+15 over the half's 64 slots.
+      L0 *= f0;
+      L1 *= f1;
 #pragma unroll
-        for (int w = 0; w < SD_WARPS; ++w) acc += mo[(w * 16 + gq) * MO_STRIDE + d] * sFac[gq * SD_WARPS + w];
-        orow[idx] = f2bf(acc);
+      for (int w = 0; w < SD_WARPS; ++w) {
+        L0 += sSum[w * 16 + qr];
+        L1 += sSum[w * 16 + qr + 8];
+      }
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        O[j][0] *= f0;
+        O[j][1] *= f0;
+        O[j][2] *= f1;
+        O[j][3] *= f1;
+      }
+      M0 = N0;
+      M1 = N1;
+      {
+        const uint32_t pb = smem_u32(sP), vb = smem_u32(sV);
+        const int vrow = (lane & 7) + (((lane >> 3) & 1) << 3);
+        const int vch = 2 * warp + (lane >> 4);
+#pragma unroll
+        for (int ks = 0; ks < SD_HALF / 16; ++ks) {
+          uint32_t af[4], b0, b1, b2, b3;
+          ldsm_x4(pb + swz<SD_HALF>(lane & 15, 2 * ks + (lane >> 4)), af[0], af[1], af[2], af[3]);
+          ldsm_x4_t(vb + swrow<2>(16 * ks + vrow, vch), b0, b1, b2, b3);
+          mma_bf16(O[0], af, b0, b1);
+          mma_bf16(O[1], af, b2, b3);
+        }
+      }
+    }
+    if (!alive) break;
+    if (ok) {
+      const float i0 = L0 > 0.f ? 1.f / L0 : 0.f, i1 = L1 > 0.f ? 1.f / L1 : 0.f;
+      const int dcol = 16 * warp + 2 * (lane & 3);
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        if (qr < G)
+          *reinterpret_cast<uint32_t *>(orow + qr * DV + dcol + 8 * j) = pack_bf16(O[j][0] * i0, O[j][1] * i0);
+        if (qr + 8 < G)
+          *reinterpret_cast<uint32_t *>(orow + (qr + 8) * DV + dcol + 8 * j) =
+              pack_bf16(O[j][2] * i1, O[j][3] * i1);
       }
     } else {
       for (int idx = tid; idx < G * DV; idx += SD_THREADS) orow[idx] = 0;
       if (tid == 0) flag(a.status, (p < 0 || p >= a.max_pos) ? ST_BAD_POS : ST_BAD_SEQ);
     }
-    __syncthreads();  // stage st, query tile st and tags st are free again
     if (has_next) {
-      const int nb = (n + 1) & 1;
+      const int nb = (n + 1) & 1;  // that query tile / tag buffer served unit n - 1
       store_unit(nx, tid, g + SD_OFF_Q + nb * SD_QTILE, reinterpret_cast<int32_t *>(g + SD_OFF_TAG) + nb * WIN);
     }
-    if (tid == 0 && n + SD_NSTAGE < nmine) {
-      fence_proxy_async_smem();  // the merge area's generic accesses before the TMA writes
-      issue(unit_id(n + SD_NSTAGE), st);
-      issued = n + SD_NSTAGE;
-    }
     __syncthreads();
+    // Every part of unit n is consumed: refill what that frees.
+    if (tid == 0) {
+      const int done = SD_PARTS * (n + 1);  // parts 0 .. done-1 are finished
+      while (issued + 1 < nhalves && issued + 1 < done + SD_NSTAGE) {
+        const int H2 = issued + 1;
+        const int n2 = H2 / SD_PARTS;
+        fence_proxy_async_smem();
+        issue(H2, n2 < SD_MAX_UNITS ? sRow[n2] : ring_row(n2));
+        issued = H2;
+      }
+    }
   }
 
   if (*abort_flag) {
     if (tid == 0) {
       flag(a.status, ST_TIMEOUT);
       // Let the loads already issued land before the CTA exits (time bound only).
-      for (int m = issued; m >= 0 && m > issued - SD_NSTAGE; --m) {
+      for (int H = issued; H >= 0 && H > issued - SD_NSTAGE; --H) {
         volatile uint32_t local = 0;
-        mbar_wait(sBar + 8 * (m % SD_NSTAGE), (uint32_t)(m / SD_NSTAGE) & 1u, &local, 1000000000ull);
+        mbar_wait(sBar + 8 * (H % SD_NSTAGE), (uint32_t)(H / SD_NSTAGE) & 1u, &local, 1000000000ull);
       }
     }
     __syncthreads();
@@ -341,7 +441,7 @@ cudaError_t launch_swa_decode(const uint16_t *q, const int64_t *pos, const int32
   const long long rows = (long long)ring.num_seqs * hkv * WIN;
   if (rows >= (1LL << 31)) return cudaErrorInvalidValue;
   CUtensorMap mk, mv;
-  if (!make_tma_map_2d(&mk, ring.k, rows, DQK, WIN) || !make_tma_map_2d(&mv, ring.v, rows, DV, WIN))
+  if (!make_tma_map_rows3d(&mk, ring.k, rows, DQK, SD_HALF) || !make_tma_map_rows3d(&mv, ring.v, rows, DV, SD_HALF))
     return cudaErrorInvalidValue;
   cudaError_t e = ensure_smem_limit(1, (const void *)swa_decode_kernel, SD_SMEM);
   if (e != cudaSuccess) return e;
@@ -362,7 +462,7 @@ cudaError_t launch_swa_decode(const uint16_t *q, const int64_t *pos, const int32
   a.max_pos = max_pos;
   a.scale_log2 = softmax_scale * LOG2E;
   const int units = B * hkv;
-  int grid = 2 * num_sms();
+  int grid = SD_CTAS * num_sms();
   if (grid > units) grid = units;
   swa_decode_kernel<<<grid, SD_THREADS, SD_SMEM, st>>>(mk, mv, a);
   return cudaGetLastError();
