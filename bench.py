@@ -353,6 +353,44 @@ def timed_run(work, steps, warmup, stream, flush=None, label="timed"):
     return sum(a.elapsed_time(b) for a, b in ev) / len(ev)
 
 
+def graph_time_ms(calls, reps=5):
+    """Per-call GPU time of a list of launches replayed as one CUDA graph
+    (no host launch gaps); each call takes the capture stream."""
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for c in calls[:3]:
+            c(side)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        cs = torch.cuda.current_stream()
+        for c in calls:
+            c(cs)
+    g.replay()
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(reps):
+        g.replay()
+    b.record()
+    b.synchronize()
+    return a.elapsed_time(b) / (reps * len(calls))
+
+
+def decode_kernel_graph_times(work):
+    """The two decode kernels alone, each as a graph of launches (windowed:
+    rotating over the ring copies, so every launch reads from HBM)."""
+    kvr = work.kvr
+    swa = [(lambda st, r=r: kvr.swa_sink_decode(work.q_swa, work.pos, work.seq, r, work.sinks, work.t4, SCALE,
+                                                out=work.out_swa, stream=st)) for r in work.rings] * 4
+    full = [(lambda st: kvr.full_attn_decode(work.q_full, work.pos, work.seq, work.pool, work.t7, SCALE, work.max_ctx,
+                                             workspace=work.ws, out=work.out_full, stream=st))] * 10
+    return graph_time_ms(swa), graph_time_ms(full)
+
+
 def e2e_decode(work, steps, warmup, stream):
     """The same decode step with the per-step inputs copied in from pinned host
     memory and the outputs copied back, all inside the timed region."""
@@ -431,6 +469,7 @@ def run_decode(args, kvr, rank):
     ms_full = work.t_full.mean_ms()
     ms_swa = work.t_swa.mean_ms()
     e2e_ms, h2d, d2h = e2e_decode(work, max(3, args.steps // 2), 2, stream)
+    work.graph_ms = decode_kernel_graph_times(work)
     return work, ms, ms_full, ms_swa, clocks, (e2e_ms, h2d, d2h)
 
 
@@ -509,9 +548,16 @@ def main():
                          f"rotated over {len(work.rings)} copies ({len(work.rings) * work.bytes_swa() / 1e9:.2f} GB)"},
         "kernels": {
             "full_attn_decode": {"ms": round(ms_full, 4), "GB/s": round(gbs_full, 1),
-                                 "hbm_frac": round(gbs_full / hbm, 4), "bytes": work.bytes_full()},
+                                 "hbm_frac": round(gbs_full / hbm, 4), "bytes": work.bytes_full(),
+                                 "graph_ms": round(work.graph_ms[1], 4),
+                                 "graph_GB/s": round(work.bytes_full() / work.graph_ms[1] / 1e6, 1)},
             "swa_sink_decode": {"ms": round(ms_swa, 5), "GB/s": round(gbs_swa, 1),
-                                "hbm_frac": round(gbs_swa / hbm, 4), "bytes": work.bytes_swa()},
+                                "hbm_frac": round(gbs_swa / hbm, 4), "bytes": work.bytes_swa(),
+                                "graph_ms": round(work.graph_ms[0], 5),
+                                "graph_GB/s": round(work.bytes_swa() / work.graph_ms[0] / 1e6, 1),
+                                "graph_hbm_frac": round(work.bytes_swa() / work.graph_ms[0] / 1e6 / hbm, 4),
+                                "note": "ms/GB/s: CUDA events around the call inside the timed step (include "
+                                        "launch gaps); graph_*: the kernel replayed back to back in a CUDA graph"},
         },
         "roofline": {"bound": "hbm", "achieved": round(gbs_full, 1), "peak": hbm, "unit": "GB/s",
                      "frac": round(gbs_full / hbm, 4), "peak_source": peaks_src,

@@ -193,6 +193,25 @@ kvr_status full_attn_decode(const kvr_bf16 *q, const int64_t *pos, const int32_t
                             void *workspace, size_t workspace_bytes, kvr_bf16 *out, void *stream);
 
 /*
+ * Ring snapshot and restore (colibri "MiMo-V2.6 (Xiaomi)", "System One mode
+ * and prompt reuse": a snapshot of a prompt holds the windowed layers' rings,
+ * copied out and later copied back, because the next prompt overwrites the
+ * slots of the snapshot's last positions; the full layers' rows stay in place).
+ *   seqs [n] int32 (device): the ring rows to copy (sequence ids of `ring`);
+ *   k_snap [n][Hkv][128][192], v_snap [n][Hkv][128][128] bf16 and
+ *   tags_snap [n][128] int32: the snapshot buffers (device), entry i for
+ *   seqs[i].
+ * kv_ring_snapshot copies ring -> snapshot; kv_ring_restore copies
+ * snapshot -> ring (slot contents and slot tags, bit for bit).  A sequence
+ * id outside the ring sets KVR_DEV_BAD_SEQ and its entry is skipped.  Two
+ * entries of one restore must not name the same sequence.  n = 0 is a no-op.
+ */
+kvr_status kv_ring_snapshot(const kvr_kv_layout *ring, const int32_t *seqs, int32_t n, kvr_bf16 *k_snap,
+                            kvr_bf16 *v_snap, int32_t *tags_snap, void *stream);
+kvr_status kv_ring_restore(const kvr_kv_layout *ring, const int32_t *seqs, int32_t n, const kvr_bf16 *k_snap,
+                           const kvr_bf16 *v_snap, const int32_t *tags_snap, void *stream);
+
+/*
  * Size of the fixed device scratch array used by full_attn_decode_noalloc:
  * 32 MiB, held on every device that loads this library until the process
  * exits.

@@ -26,6 +26,7 @@ __all__ = [
     "KvrError", "RingLayout", "PagedLayout", "LinearLayout", "lib", "rope_table",
     "kv_ring_append_rope", "swa_sink_decode", "full_attn_decode", "full_attn_decode_workspace_size",
     "swa_sink_prefill_chunk", "full_attn_prefill_chunk", "device_status", "full_attn_decode_noalloc",
+    "kv_ring_snapshot", "kv_ring_restore", "ring_snapshot_alloc",
     "DQK", "DV", "DROT", "WINDOW",
 ]
 
@@ -85,6 +86,10 @@ def lib():
                 L.full_attn_decode_workspace_size.argtypes = [i32, i32, i32, i64]
                 L.full_attn_decode.restype = ctypes.c_int
                 L.full_attn_decode.argtypes = [p, p, p, i32, i32, p, p, i64, f32, i64, p, ctypes.c_size_t, p, p]
+                L.kv_ring_snapshot.restype = ctypes.c_int
+                L.kv_ring_snapshot.argtypes = [p, p, i32, p, p, p, p]
+                L.kv_ring_restore.restype = ctypes.c_int
+                L.kv_ring_restore.argtypes = [p, p, i32, p, p, p, p]
                 L.full_attn_decode_noalloc.restype = ctypes.c_int
                 L.full_attn_decode_noalloc.argtypes = [p, p, p, i32, i32, p, p, i64, f32, i64, p, p]
                 L.swa_sink_prefill_chunk.restype = ctypes.c_int
@@ -328,6 +333,36 @@ def full_attn_prefill_chunk(q, P0, seq, pool, table, softmax_scale, out=None, st
     _check(lib().full_attn_prefill_chunk(_ptr(q), int(P0), C, int(seq), Hq, ctypes.byref(c), _ptr(table),
                                          table.shape[0], float(softmax_scale), _ptr(out), _stream(stream)))
     return out
+
+
+def ring_snapshot_alloc(n, num_kv_heads, device="cuda"):
+    """Snapshot buffers for n rings: (k [n, Hkv, 128, 192], v [n, Hkv, 128, 128], tags [n, 128])."""
+    return (torch.empty(n, num_kv_heads, WINDOW, DQK, dtype=torch.bfloat16, device=device),
+            torch.empty(n, num_kv_heads, WINDOW, DV, dtype=torch.bfloat16, device=device),
+            torch.empty(n, WINDOW, dtype=torch.int32, device=device))
+
+
+def _ring_copy(fn, ring, seqs, snap, stream):
+    _want(seqs, "seqs", torch.int32, 1)
+    k, v, t = snap
+    n = seqs.shape[0]
+    _want(k, "k_snap", torch.bfloat16, 4)
+    _want(v, "v_snap", torch.bfloat16, 4)
+    _want(t, "tags_snap", torch.int32, 2)
+    if k.shape[0] < n or v.shape[0] < n or t.shape[0] < n or k.shape[1] != ring.num_kv_heads:
+        raise ValueError("snapshot buffers too small for the ring / sequence list")
+    c = ring.c()
+    _check(fn(ctypes.byref(c), _ptr(seqs), n, _ptr(k), _ptr(v), _ptr(t), _stream(stream)))
+
+
+def kv_ring_snapshot(ring, seqs, snap, stream=None):
+    """Copy the rings (slots + tags) of sequences `seqs` into snapshot buffers."""
+    _ring_copy(lib().kv_ring_snapshot, ring, seqs, snap, stream)
+
+
+def kv_ring_restore(ring, seqs, snap, stream=None):
+    """Copy snapshot buffers back into the rings of sequences `seqs`."""
+    _ring_copy(lib().kv_ring_restore, ring, seqs, snap, stream)
 
 
 def device_status(reset: bool = True) -> int:

@@ -314,6 +314,35 @@ kvr_status full_attn_prefill_chunk(const kvr_bf16 *q, int64_t P0, int32_t C, int
   return ok();
 }
 
+static kvr_status ring_copy(const char *name, const kvr_kv_layout *ring, const int32_t *seqs, int32_t n,
+                            const kvr_bf16 *k_snap, const kvr_bf16 *v_snap, const int32_t *tags_snap, bool to_ring,
+                            void *stream) {
+  if (n < 0) return fail(KVR_EINVAL, "%s: n %d", name, n);
+  kvr_status s = check_layout(ring, KVR_LAYOUT_RING, "ring");
+  if (s) return s;
+  if (n == 0) return ok();
+  if (!seqs || !k_snap || !v_snap || !tags_snap) return fail(KVR_EINVAL, "%s: a pointer is NULL", name);
+  if (!aligned16(k_snap) || !aligned16(v_snap)) return fail(KVR_EINVAL, "%s: snapshot k/v not 16-byte aligned", name);
+  if (n > 65535) return fail(KVR_EUNSUPPORTED, "%s: n %d > 65535", name, n);
+  unsigned *st = nullptr;
+  cudaError_t e = status_ptr(&st);
+  if (e != cudaSuccess) return cuda_fail(e, name);
+  e = kvr::launch_ring_copy(view(*ring), seqs, n, const_cast<uint16_t *>(k_snap), const_cast<uint16_t *>(v_snap),
+                            const_cast<int32_t *>(tags_snap), to_ring, st, as_stream(stream));
+  if (e != cudaSuccess) return cuda_fail(e, name);
+  return ok();
+}
+
+kvr_status kv_ring_snapshot(const kvr_kv_layout *ring, const int32_t *seqs, int32_t n, kvr_bf16 *k_snap,
+                            kvr_bf16 *v_snap, int32_t *tags_snap, void *stream) {
+  return ring_copy("kv_ring_snapshot", ring, seqs, n, k_snap, v_snap, tags_snap, false, stream);
+}
+
+kvr_status kv_ring_restore(const kvr_kv_layout *ring, const int32_t *seqs, int32_t n, const kvr_bf16 *k_snap,
+                           const kvr_bf16 *v_snap, const int32_t *tags_snap, void *stream) {
+  return ring_copy("kv_ring_restore", ring, seqs, n, k_snap, v_snap, tags_snap, true, stream);
+}
+
 }  // extern "C"
 
 // ---------------------------------------------------------------------------

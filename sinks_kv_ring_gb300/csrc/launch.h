@@ -57,6 +57,9 @@ cudaError_t launch_swa_prefill(const uint16_t *q, int64_t P0, int C, int seq, in
                                int64_t max_pos, float softmax_scale, uint16_t *out, unsigned *status,
                                cudaStream_t st);
 
+cudaError_t launch_ring_copy(const KvView &ring, const int32_t *seqs, int n, uint16_t *k_snap, uint16_t *v_snap,
+                             int32_t *tags_snap, bool to_ring, unsigned *status, cudaStream_t st);
+
 int num_sms();
 
 }  // namespace kvr

@@ -387,3 +387,80 @@ def test_full_prefill_many_tiles_all_rows(tables):
     want = oracle.attend_seq(q, np.arange(P0, P0 + C), k, v, 0, 1e7, 0.612, SCALE, 0, None)
     compare(out, want, "full prefill many tiles")
     compare_rows(out, want, "full prefill many tiles")
+
+
+# --------------------------------------------------------------------------- Pro-true head shapes
+
+def test_pro_true_heads_decode_both_kinds(tables):
+    # The pages' MiMo-V2.6-Pro: 128 query heads and 8 KV heads on both layer
+    # kinds (gaudi-cookbook "MiMo-V2.6-Pro"); value scale 0.612.
+    hq, hkv = 128, 8
+    positions = [5, 127, 128, 3000]
+    out, want = _swa_decode_case(len(positions), hq, hkv, positions, "shifted", 3101, tables, vscale=0.612)
+    compare_rows(out, want, "pro swa decode")
+    syn = Synth(3102, dist="plain", device=DEV)
+    ctx = [1, 130, 2049]
+    pool = kvr.PagedLayout.contiguous(len(ctx), hkv, 4096, block_size=64)
+    fill_paged(pool, syn, list(range(len(ctx))), ctx, tables[1e7], 0.612)
+    q = syn.q(len(ctx), hq, hkv, seq=9)
+    out = kvr.full_attn_decode(q, torch.tensor([c - 1 for c in ctx], device=DEV),
+                               torch.arange(len(ctx), dtype=torch.int32, device=DEV), pool, tables[1e7], SCALE, 4096)
+    want = np.stack([oracle.attend_seq(q[b:b + 1], [c - 1], *raw_kv(syn, hkv, b, 0, c), 0, 1e7, 0.612, SCALE, 0,
+                                       None)[0] for b, c in enumerate(ctx)])
+    compare_rows(out, want, "pro full decode")
+
+
+def test_pro_true_heads_prefill_both_kinds(tables):
+    hq, hkv, P0, C = 128, 8, 700, 200
+    syn = Synth(3103, dist="shifted", device=DEV)
+    sinks = syn.sinks(hq).to(DEV)
+    pool = kvr.PagedLayout.contiguous(1, hkv, P0 + C, block_size=64)
+    fill_paged(pool, syn, [0], [P0 + C], tables[1e7], 0.612)
+    q = syn.q(C, hq, hkv, seq=0, start=P0)
+    out = kvr.full_attn_prefill_chunk(q, P0, 0, pool, tables[1e7], SCALE)
+    rows = [0, 1, 100, 199]
+    k, v = raw_kv(syn, hkv, 0, 0, P0 + C)
+    want = oracle.attend_seq(q[rows], np.array(rows) + P0, k, v, 0, 1e7, 0.612, SCALE, 0, None)
+    compare_rows(out[rows], want, "pro full prefill")
+    ring = kvr.RingLayout.empty(1, hkv)
+    fill_ring(ring, syn, [0], [P0 - 1], tables[1e4], 0.612)
+    stage = kvr.LinearLayout.empty(C, hkv)
+    kc, vc = raw_kv(syn, hkv, 0, P0, P0 + C)
+    kvr.kv_ring_append_rope(kc, vc, torch.arange(P0, P0 + C, device=DEV), None, tables[1e4], 0.612, stage)
+    out = kvr.swa_sink_prefill_chunk(q, P0, 0, stage, ring, sinks, tables[1e4], SCALE)
+    lo = P0 - 127
+    k, v = raw_kv(syn, hkv, 0, lo, P0 + C)
+    want = oracle.attend_seq(q[rows], np.array(rows) + P0, k, v, lo, 1e4, 0.612, SCALE, 128,
+                             sinks.double().cpu().numpy())
+    compare_rows(out[rows], want, "pro swa prefill")
+
+
+# --------------------------------------------------------------------------- ring snapshot / restore
+
+def test_ring_snapshot_restore_roundtrip_and_decode(tables):
+    # colibri "System One mode and prompt reuse": the rings are copied into a
+    # snapshot and back; a decode after the restore equals the decode the
+    # snapshot's state gives, bit for bit.
+    syn = Synth(3201, dist="plain", device=DEV)
+    hq, hkv = 64, 8
+    ring = kvr.RingLayout.empty(4, hkv)
+    fill_ring(ring, syn, [0, 1, 2, 3], [300, 90, 500, 127], tables[1e4], 0.707)
+    seqs = torch.tensor([2, 0], dtype=torch.int32, device=DEV)
+    snap = kvr.ring_snapshot_alloc(2, hkv)
+    kvr.kv_ring_snapshot(ring, seqs, snap)
+    q = syn.q(2, hq, hkv, seq=4)
+    sinks = syn.sinks(hq).to(DEV)
+    pos = torch.tensor([500, 300], device=DEV)
+    before = kvr.swa_sink_decode(q, pos, seqs, ring, sinks, tables[1e4], SCALE).clone()
+    ref = (ring.k.clone(), ring.v.clone(), ring.slot_pos.clone())
+    # a later prompt overwrites the rings (here: 200 more positions on each)
+    fill_ring(ring, syn, [0, 2], [700, 900], tables[1e4], 0.707)
+    assert not torch.equal(ring.slot_pos, ref[2])
+    kvr.kv_ring_restore(ring, seqs, snap)
+    torch.cuda.synchronize()
+    assert torch.equal(ring.k, ref[0]) and torch.equal(ring.v, ref[1]) and torch.equal(ring.slot_pos, ref[2])
+    after = kvr.swa_sink_decode(q, pos, seqs, ring, sinks, tables[1e4], SCALE)
+    assert torch.equal(after, before)
+    bad = torch.tensor([9], dtype=torch.int32, device=DEV)
+    kvr.kv_ring_snapshot(ring, bad, snap)
+    assert kvr.device_status() == kvr.DEV_BAD_SEQ
