@@ -64,6 +64,8 @@ enum {
 #define KVR_DEV_BAD_POS 1u    /* a position < 0 or >= the RoPE table length */
 #define KVR_DEV_BAD_SEQ 2u    /* a sequence id outside the layout */
 #define KVR_DEV_BAD_BLOCK 4u  /* a block-table entry outside the pool, or a context past the table */
+#define KVR_DEV_TIMEOUT 8u    /* a kernel gave up waiting on its own pipeline (bounded wait) and returned */
+#define KVR_DEV_BAD_ROWS 16u  /* varlen: cu_rows not non-decreasing within [0, T]; that chunk is skipped */
 
 /* KV storage kinds. */
 enum {
@@ -279,6 +281,71 @@ kvr_status full_attn_prefill_chunk(const kvr_bf16 *q, int64_t P0, int32_t C, int
                                    const kvr_kv_layout *pool, const float *rope_cos_sin,
                                    int64_t max_pos, float softmax_scale, kvr_bf16 *out,
                                    void *stream);
+
+/*
+ * Batches of chunks of different lengths ("varlen"), for both layer kinds.
+ * Chunk s (s < n) is C_s = cu_rows[s+1] - cu_rows[s] query rows at positions
+ * P0[s] .. P0[s] + C_s - 1 of sequence seq[s]; its q rows are rows
+ * cu_rows[s] .. cu_rows[s+1]-1 of q, and its outputs the same rows of out.
+ * Each row attends exactly as in the single-chunk calls above.  Uses:
+ *  - multi-token-prediction verification (the Chinese Xiaomi article,
+ *    section "Decode加速与多模态优化": the model proposes several tokens per
+ *    step and they are checked in one pass): C_s = 2..4 draft tokens per
+ *    sequence, causal within the draft, each sequence's K/V read once;
+ *  - batched prefill of requests of different lengths (section
+ *    "调度与Prefill优化": length buckets 0-64K / 64K-256K / 256K-1M);
+ *  - mixed batches of prefill chunks and single decode tokens (C_s = 1).
+ * cu_rows [n+1] int32, P0 [n] int64, seq [n] int32 are DEVICE arrays, read
+ * by the kernels (the work plan is built on the device, so the call can be
+ * captured in a CUDA graph and the lengths can change between replays).
+ * T (host) is the number of rows of q/out; cu_rows must be non-decreasing
+ * within [0, T] (else that chunk is skipped and KVR_DEV_BAD_ROWS set).  A
+ * chunk whose sequence id is outside the layout (KVR_DEV_BAD_SEQ) or whose
+ * P0 < 0 or P0 + C_s exceeds the bound (KVR_DEV_BAD_POS) has its rows written
+ * as zeros.  Rows of q/out outside every chunk are neither read nor written.
+ * q [T][Hq][192] bf16 un-rotated; out [T][Hq][128] bf16.
+ * workspace: device scratch (16-byte aligned, no initialisation needed) of
+ * the size the matching *_workspace_size call returns; it holds the plan
+ * (and for full layers the key-split partials).  n = 0 or T = 0 is a no-op.
+ */
+
+/* Workspace bytes for full_attn_prefill_varlen (0 on bad arguments). */
+size_t full_attn_prefill_varlen_workspace_size(int32_t n, int64_t T, int32_t Hq, int32_t Hkv, int64_t max_ctx);
+
+/*
+ * Full-attention layer, varlen: chunk s attends positions 0..P0[s] + i of
+ * the paged pool, into which its K/V were already appended.  Every
+ * P0[s] + C_s must be <= max_ctx; max_ctx <= max_pos and
+ * <= max_blocks*block_size.  Runs on the tensor cores; a chunk of at most
+ * 256 / (Hq/Hkv) rows (a decode or draft-verification chunk) is also cut
+ * along its keys into splits that run in parallel and are merged by
+ * log-sum-exp, like full_attn_decode.
+ */
+kvr_status full_attn_prefill_varlen(const kvr_bf16 *q, const int32_t *cu_rows, const int64_t *P0,
+                                    const int32_t *seq, int32_t n, int64_t T, int32_t Hq,
+                                    const kvr_kv_layout *pool, const float *rope_cos_sin, int64_t max_pos,
+                                    float softmax_scale, int64_t max_ctx, void *workspace,
+                                    size_t workspace_bytes, kvr_bf16 *out, void *stream);
+
+/* Workspace bytes for swa_sink_prefill_varlen (0 on bad arguments). */
+size_t swa_sink_prefill_varlen_workspace_size(int32_t n);
+
+/*
+ * Windowed layer, varlen: row i of chunk s attends positions
+ * (P0[s] + i - 128, P0[s] + i]: those below P0[s] from sequence seq[s]'s ring
+ * (its state before the chunk, slot tags checked), those from P0[s] on from
+ * chunk_kv row cu_rows[s] + (pos - P0[s]).  Sink as in swa_sink_prefill_chunk.
+ * chunk_kv: LINEAR with num_rows >= T, the batch's K/V as written by
+ * kv_ring_append_rope; P0[s] + C_s must be <= max_pos.  For a draft
+ * verification, the draft's K/V go to chunk_kv and the ring is left as it was
+ * before the draft; the accepted tokens are appended to the ring afterwards.
+ */
+kvr_status swa_sink_prefill_varlen(const kvr_bf16 *q, const int32_t *cu_rows, const int64_t *P0,
+                                   const int32_t *seq, int32_t n, int64_t T, int32_t Hq,
+                                   const kvr_kv_layout *chunk_kv, const kvr_kv_layout *ring,
+                                   const float *sinks, const float *rope_cos_sin, int64_t max_pos,
+                                   float softmax_scale, void *workspace, size_t workspace_bytes,
+                                   kvr_bf16 *out, void *stream);
 
 #ifdef __cplusplus
 }

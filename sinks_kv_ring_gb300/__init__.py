@@ -13,6 +13,10 @@ gaudi-cookbook "MiMo-V2.6-Flash on Gaudi 2", "What was built"):
   full_attn_decode        one token over a paged pool, split-K + LSE combine
   swa_sink_prefill_chunk  a chunk over ring + chunk rows, sink in the softmax
   full_attn_prefill_chunk a chunk over a paged pool, causal
+
+and the batched forms of the two prefill calls, ``swa_sink_prefill_varlen``
+and ``full_attn_prefill_varlen``: n chunks of different lengths in one call
+(multi-token-prediction draft verification, mixed prefill/decode batches).
 """
 from __future__ import annotations
 
@@ -27,12 +31,14 @@ __all__ = [
     "kv_ring_append_rope", "swa_sink_decode", "full_attn_decode", "full_attn_decode_workspace_size",
     "swa_sink_prefill_chunk", "full_attn_prefill_chunk", "device_status", "full_attn_decode_noalloc",
     "kv_ring_snapshot", "kv_ring_restore", "ring_snapshot_alloc",
+    "full_attn_prefill_varlen", "swa_sink_prefill_varlen", "full_attn_prefill_varlen_workspace_size",
+    "swa_sink_prefill_varlen_workspace_size",
     "DQK", "DV", "DROT", "WINDOW",
 ]
 
 DQK, DV, DROT, WINDOW = 192, 128, 64, 128
 LAYOUT_RING, LAYOUT_PAGED, LAYOUT_LINEAR = 1, 2, 3
-DEV_BAD_POS, DEV_BAD_SEQ, DEV_BAD_BLOCK = 1, 2, 4
+DEV_BAD_POS, DEV_BAD_SEQ, DEV_BAD_BLOCK, DEV_TIMEOUT, DEV_BAD_ROWS = 1, 2, 4, 8, 16
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libkvring.so")
@@ -96,6 +102,16 @@ def lib():
                 L.swa_sink_prefill_chunk.argtypes = [p, i64, i32, i32, i32, p, p, p, p, i64, f32, p, p]
                 L.full_attn_prefill_chunk.restype = ctypes.c_int
                 L.full_attn_prefill_chunk.argtypes = [p, i64, i32, i32, i32, p, p, i64, f32, p, p]
+                L.full_attn_prefill_varlen_workspace_size.restype = ctypes.c_size_t
+                L.full_attn_prefill_varlen_workspace_size.argtypes = [i32, i64, i32, i32, i64]
+                L.full_attn_prefill_varlen.restype = ctypes.c_int
+                L.full_attn_prefill_varlen.argtypes = [p, p, p, p, i32, i64, i32, p, p, i64, f32, i64, p,
+                                                       ctypes.c_size_t, p, p]
+                L.swa_sink_prefill_varlen_workspace_size.restype = ctypes.c_size_t
+                L.swa_sink_prefill_varlen_workspace_size.argtypes = [i32]
+                L.swa_sink_prefill_varlen.restype = ctypes.c_int
+                L.swa_sink_prefill_varlen.argtypes = [p, p, p, p, i32, i64, i32, p, p, p, p, i64, f32, p,
+                                                      ctypes.c_size_t, p, p]
                 _lib = L
     return _lib
 
@@ -332,6 +348,70 @@ def full_attn_prefill_chunk(q, P0, seq, pool, table, softmax_scale, out=None, st
     c = pool.c()
     _check(lib().full_attn_prefill_chunk(_ptr(q), int(P0), C, int(seq), Hq, ctypes.byref(c), _ptr(table),
                                          table.shape[0], float(softmax_scale), _ptr(out), _stream(stream)))
+    return out
+
+
+def full_attn_prefill_varlen_workspace_size(n, T, Hq, Hkv, max_ctx) -> int:
+    return int(lib().full_attn_prefill_varlen_workspace_size(int(n), int(T), int(Hq), int(Hkv), int(max_ctx)))
+
+
+def swa_sink_prefill_varlen_workspace_size(n) -> int:
+    return int(lib().swa_sink_prefill_varlen_workspace_size(int(n)))
+
+
+def _varlen_args(q, cu_rows, P0, seq):
+    _want(q, "q", torch.bfloat16, 3)
+    _want(cu_rows, "cu_rows", torch.int32, 1)
+    _want(P0, "P0", torch.int64, 1)
+    _want(seq, "seq", torch.int32, 1)
+    n = seq.numel()
+    if cu_rows.numel() != n + 1 or P0.numel() != n:
+        raise ValueError(f"cu_rows must have n+1 = {n + 1} entries and P0 n = {n}")
+    return n
+
+
+def full_attn_prefill_varlen(q, cu_rows, P0, seq, pool, table, softmax_scale, max_ctx, workspace=None, out=None,
+                             stream=None):
+    """n chunks over a full layer's paged pool: chunk s is q rows
+    cu_rows[s]..cu_rows[s+1]-1 at positions P0[s].. of sequence seq[s]
+    (device int32 / int64 / int32 tensors)."""
+    n = _varlen_args(q, cu_rows, P0, seq)
+    _want(table, "table", torch.float32, 3)
+    T, Hq, _ = q.shape
+    if workspace is None:
+        nb = full_attn_prefill_varlen_workspace_size(n, T, Hq, pool.num_kv_heads, max_ctx)
+        workspace = torch.empty(max(nb, 1), dtype=torch.uint8, device=q.device)
+    _want(workspace, "workspace", torch.uint8, 1)
+    if out is None:
+        out = torch.empty(T, Hq, DV, dtype=torch.bfloat16, device=q.device)
+    _want(out, "out", torch.bfloat16, 3)
+    c = pool.c()
+    _check(lib().full_attn_prefill_varlen(_ptr(q), _ptr(cu_rows), _ptr(P0), _ptr(seq), n, T, Hq, ctypes.byref(c),
+                                          _ptr(table), table.shape[0], float(softmax_scale), int(max_ctx),
+                                          _ptr(workspace), workspace.numel(), _ptr(out), _stream(stream)))
+    return out
+
+
+def swa_sink_prefill_varlen(q, cu_rows, P0, seq, chunk_kv, ring, sinks, table, softmax_scale, workspace=None,
+                            out=None, stream=None):
+    """n chunks over a windowed layer: ring state before each chunk plus the
+    batch's own rows in chunk_kv (row cu_rows[s] + i for chunk s)."""
+    n = _varlen_args(q, cu_rows, P0, seq)
+    _want(sinks, "sinks", torch.float32, 1)
+    _want(table, "table", torch.float32, 3)
+    T, Hq, _ = q.shape
+    if workspace is None:
+        nb = swa_sink_prefill_varlen_workspace_size(n)
+        workspace = torch.empty(max(nb, 1), dtype=torch.uint8, device=q.device)
+    _want(workspace, "workspace", torch.uint8, 1)
+    if out is None:
+        out = torch.empty(T, Hq, DV, dtype=torch.bfloat16, device=q.device)
+    _want(out, "out", torch.bfloat16, 3)
+    cc, rc = chunk_kv.c(), ring.c()
+    _check(lib().swa_sink_prefill_varlen(_ptr(q), _ptr(cu_rows), _ptr(P0), _ptr(seq), n, T, Hq, ctypes.byref(cc),
+                                         ctypes.byref(rc), _ptr(sinks), _ptr(table), table.shape[0],
+                                         float(softmax_scale), _ptr(workspace), workspace.numel(), _ptr(out),
+                                         _stream(stream)))
     return out
 
 

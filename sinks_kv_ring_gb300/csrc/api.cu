@@ -338,6 +338,93 @@ kvr_status kv_ring_snapshot(const kvr_kv_layout *ring, const int32_t *seqs, int3
   return ring_copy("kv_ring_snapshot", ring, seqs, n, k_snap, v_snap, tags_snap, false, stream);
 }
 
+namespace {
+
+kvr_status check_varlen(const char *who, const kvr_bf16 *q, const int32_t *cu_rows, const int64_t *P0,
+                        const int32_t *seq, int32_t n, int64_t T, const kvr_bf16 *out) {
+  if (n < 0 || T < 0 || T > INT32_MAX) return fail(KVR_EINVAL, "%s: n %d, T %lld", who, n, (long long)T);
+  if (n == 0 || T == 0) return KVR_OK;
+  if (!q || !cu_rows || !P0 || !seq || !out) return fail(KVR_EINVAL, "%s: q/cu_rows/P0/seq/out is NULL", who);
+  if (!aligned16(q) || !aligned16(out)) return fail(KVR_EINVAL, "%s: q/out not 16-byte aligned", who);
+  return KVR_OK;
+}
+
+}  // namespace
+
+size_t full_attn_prefill_varlen_workspace_size(int32_t n, int64_t T, int32_t Hq, int32_t Hkv, int64_t max_ctx) {
+  if (n < 1 || T < 0 || Hq < 1 || Hkv < 1 || Hq % Hkv || max_ctx < 1) return 0;
+  return kvr::varlen_sizes(n, T, Hq, Hkv, max_ctx, 256, true).bytes;
+}
+
+size_t swa_sink_prefill_varlen_workspace_size(int32_t n) {
+  if (n < 1) return 0;
+  return kvr::varlen_sizes(n, 0, 1, 1, 1, 64, false).bytes;
+}
+
+kvr_status full_attn_prefill_varlen(const kvr_bf16 *q, const int32_t *cu_rows, const int64_t *P0, const int32_t *seq,
+                                    int32_t n, int64_t T, int32_t Hq, const kvr_kv_layout *pool,
+                                    const float *rope_cos_sin, int64_t max_pos, float softmax_scale, int64_t max_ctx,
+                                    void *workspace, size_t workspace_bytes, kvr_bf16 *out, void *stream) {
+  const char *who = "full_attn_prefill_varlen";
+  kvr_status s = check_layout(pool, KVR_LAYOUT_PAGED, "pool");
+  if (s) return s;
+  if ((s = check_heads(Hq, pool->num_kv_heads, 0))) return s;
+  if ((s = check_table(rope_cos_sin, max_pos))) return s;
+  if (max_ctx < 1 || max_ctx > max_pos)
+    return fail(KVR_ERANGE, "max_ctx %lld outside [1, max_pos=%lld]", (long long)max_ctx, (long long)max_pos);
+  if (max_ctx > (int64_t)pool->max_blocks * pool->block_size)
+    return fail(KVR_ERANGE, "max_ctx %lld exceeds max_blocks*block_size = %lld", (long long)max_ctx,
+                (long long)pool->max_blocks * pool->block_size);
+  if ((s = check_varlen(who, q, cu_rows, P0, seq, n, T, out))) return s;
+  if (n == 0 || T == 0) return ok();
+  const kvr::VarlenSizes z = kvr::varlen_sizes(n, T, Hq, pool->num_kv_heads, max_ctx, 256, true);
+  if (z.items_max >= INT32_MAX || z.prows_max * z.nsp_max >= INT32_MAX)
+    return fail(KVR_EUNSUPPORTED, "%s: batch too large for one call (n %d, T %lld)", who, n, (long long)T);
+  if (!workspace || workspace_bytes < z.bytes)
+    return fail(KVR_EWORKSPACE, "workspace %zu bytes, need %zu", workspace ? workspace_bytes : (size_t)0, z.bytes);
+  if (!aligned16(workspace)) return fail(KVR_EINVAL, "workspace not 16-byte aligned");
+  unsigned *st = nullptr;
+  cudaError_t e = status_ptr(&st);
+  if (e != cudaSuccess) return cuda_fail(e, who);
+  e = kvr::launch_full_varlen(q, cu_rows, P0, seq, n, T, Hq, view(*pool), rope_cos_sin, softmax_scale, max_ctx,
+                              workspace, out, st, as_stream(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "full_attn_prefill_varlen launch");
+  return ok();
+}
+
+kvr_status swa_sink_prefill_varlen(const kvr_bf16 *q, const int32_t *cu_rows, const int64_t *P0, const int32_t *seq,
+                                   int32_t n, int64_t T, int32_t Hq, const kvr_kv_layout *chunk_kv,
+                                   const kvr_kv_layout *ring, const float *sinks, const float *rope_cos_sin,
+                                   int64_t max_pos, float softmax_scale, void *workspace, size_t workspace_bytes,
+                                   kvr_bf16 *out, void *stream) {
+  const char *who = "swa_sink_prefill_varlen";
+  kvr_status s = check_layout(ring, KVR_LAYOUT_RING, "ring");
+  if (s) return s;
+  if ((s = check_layout(chunk_kv, KVR_LAYOUT_LINEAR, "chunk_kv"))) return s;
+  if (chunk_kv->num_kv_heads != ring->num_kv_heads)
+    return fail(KVR_EINVAL, "chunk_kv has %d KV heads, ring %d", chunk_kv->num_kv_heads, ring->num_kv_heads);
+  if ((s = check_heads(Hq, ring->num_kv_heads, 0))) return s;
+  if ((s = check_table(rope_cos_sin, max_pos))) return s;
+  if ((s = check_varlen(who, q, cu_rows, P0, seq, n, T, out))) return s;
+  if (chunk_kv->num_rows < T)
+    return fail(KVR_EINVAL, "chunk_kv has %lld rows, T = %lld", (long long)chunk_kv->num_rows, (long long)T);
+  if (n == 0 || T == 0) return ok();
+  if (!sinks) return fail(KVR_EINVAL, "sinks is NULL");
+  const kvr::VarlenSizes z = kvr::varlen_sizes(n, T, Hq, ring->num_kv_heads, max_pos, 64, false);
+  if (z.items_max >= INT32_MAX)
+    return fail(KVR_EUNSUPPORTED, "%s: batch too large for one call (n %d, T %lld)", who, n, (long long)T);
+  if (!workspace || workspace_bytes < z.bytes)
+    return fail(KVR_EWORKSPACE, "workspace %zu bytes, need %zu", workspace ? workspace_bytes : (size_t)0, z.bytes);
+  if (!aligned16(workspace)) return fail(KVR_EINVAL, "workspace not 16-byte aligned");
+  unsigned *st = nullptr;
+  cudaError_t e = status_ptr(&st);
+  if (e != cudaSuccess) return cuda_fail(e, who);
+  e = kvr::launch_swa_varlen(q, cu_rows, P0, seq, n, T, Hq, view(*chunk_kv), view(*ring), sinks, rope_cos_sin,
+                             max_pos, softmax_scale, workspace, out, st, as_stream(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "swa_sink_prefill_varlen launch");
+  return ok();
+}
+
 kvr_status kv_ring_restore(const kvr_kv_layout *ring, const int32_t *seqs, int32_t n, const kvr_bf16 *k_snap,
                            const kvr_bf16 *v_snap, const int32_t *tags_snap, void *stream) {
   return ring_copy("kv_ring_restore", ring, seqs, n, k_snap, v_snap, tags_snap, true, stream);

@@ -21,6 +21,7 @@ constexpr float LOG2E = 1.4426950408889634f;
 constexpr unsigned ST_BAD_POS = 1u;
 constexpr unsigned ST_BAD_SEQ = 2u;
 constexpr unsigned ST_BAD_BLOCK = 4u;
+constexpr unsigned ST_BAD_ROWS = 16u;
 
 __device__ __forceinline__ void flag(unsigned *status, unsigned bits) {
   if (status) atomicOr(status, bits);
@@ -113,6 +114,39 @@ __device__ __forceinline__ void rope_pair8(const uint4 &x1v, const uint4 &x2v, c
   }
   o1 = make_uint4(r1[0], r1[1], r1[2], r1[3]);
   o2 = make_uint4(r2[0], r2[1], r2[2], r2[3]);
+}
+
+// Work plan of a batch of chunks of different lengths (written on the device
+// by varlen_plan_kernel into the caller's workspace).  Chunk s holds rows
+// cu_rows[s] .. cu_rows[s+1]-1 of the batch; its CTA work items are
+// item_prefix[s] .. item_prefix[s+1]-1; mode[s] is -1 (rows not addressable:
+// nothing is written), 0 (a position or sequence id out of range: its rows
+// are written as zeros), or k >= 1 (the keys are cut into k splits).
+// Split chunks own partial rows prow_prefix[s] .. prow_prefix[s+1]-1, one per
+// (row, q head), each with nsp_max records (m, l) + o[128].
+struct VarlenPlan {
+  const int32_t *cu_rows;
+  const int64_t *P0;
+  const int32_t *seq;
+  int32_t *item_prefix;  // [n+1]
+  int32_t *prow_prefix;  // [n+1]
+  int32_t *mode;         // [n]
+  float2 *pml;           // [prows][nsp_max]: (max in log2 units, sum of exponentials)
+  float *po;             // [prows][nsp_max][128]: unnormalised numerators
+  int n;
+  int nsp_max;
+  long long split_len;   // keys per split (a multiple of 128); 0 = no splits
+};
+
+// Chunk s of work item b: the last s with item_prefix[s] <= b (the caller
+// has checked b < item_prefix[n]).
+__device__ __forceinline__ int plan_find(const int32_t *prefix, int n, long long b) {
+  int lo = 0, hi = n;  // prefix[lo] <= b < prefix[hi]
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (prefix[mid] <= b) lo = mid; else hi = mid;
+  }
+  return lo;
 }
 
 // Device view of a KV layout (see kvr_kv_layout).

@@ -57,6 +57,35 @@ cudaError_t launch_swa_prefill(const uint16_t *q, int64_t P0, int C, int seq, in
                                int64_t max_pos, float softmax_scale, uint16_t *out, unsigned *status,
                                cudaStream_t st);
 
+// Sizes of the workspace of a varlen call (see VarlenPlan): n chunks, T rows,
+// contexts up to max_ctx, CTA items of tile_rows query rows; with `splits`,
+// chunks of one item are cut along the keys.
+struct VarlenSizes {
+  int tile_rows;
+  long long split_len;
+  int nsp_max;
+  long long prows_max;   // partial rows the workspace holds
+  long long items_max;   // bound on the CTA items of any plan (the grid size)
+  size_t off_prow, off_mode, off_pml, off_po, bytes;
+};
+VarlenSizes varlen_sizes(int n, long long T, int hq, int hkv, long long max_ctx, int tile_rows, bool splits);
+VarlenPlan varlen_plan_view(const VarlenSizes &z, void *ws, const int32_t *cu_rows, const int64_t *P0,
+                            const int32_t *seq, int n);
+cudaError_t launch_varlen_plan(const VarlenPlan &p, long long T, int hq, int hkv, int tile_rows, long long max_ctx,
+                               int num_seqs, unsigned *status, cudaStream_t st);
+cudaError_t launch_varlen_combine(const VarlenPlan &p, long long prows_max, int hq, uint16_t *out, cudaStream_t st);
+
+// Varlen attention: rows of chunk s are q/out rows cu_rows[s] ..; the plan
+// in `ws` is built by the launcher.
+cudaError_t launch_full_varlen(const uint16_t *q, const int32_t *cu_rows, const int64_t *P0, const int32_t *seq,
+                               int n, long long T, int hq, const KvView &pool, const float *table,
+                               float softmax_scale, long long max_ctx, void *ws, uint16_t *out, unsigned *status,
+                               cudaStream_t st);
+cudaError_t launch_swa_varlen(const uint16_t *q, const int32_t *cu_rows, const int64_t *P0, const int32_t *seq,
+                              int n, long long T, int hq, const KvView &chunk, const KvView &ring,
+                              const float *sinks, const float *table, int64_t max_pos, float softmax_scale,
+                              void *ws, uint16_t *out, unsigned *status, cudaStream_t st);
+
 cudaError_t launch_ring_copy(const KvView &ring, const int32_t *seqs, int n, uint16_t *k_snap, uint16_t *v_snap,
                              int32_t *tags_snap, bool to_ring, unsigned *status, cudaStream_t st);
 

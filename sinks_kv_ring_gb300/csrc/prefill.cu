@@ -34,6 +34,15 @@ struct SwaSrc {
   const uint16_t *ck, *cv;   // chunk rows: [C][hkv][192], [C][hkv][128]
   int hkv, kv;
   long long P0;
+  // Point at sequence sq's rings and at the chunk rows from batch row c0.
+  __device__ __forceinline__ void rebase(int sq, long long c0, long long p0) {
+    rk += (long long)sq * hkv * WIN * DQK;
+    rv += (long long)sq * hkv * WIN * DV;
+    slot_pos += (long long)sq * WIN;
+    ck += c0 * hkv * DQK;
+    cv += c0 * hkv * DV;
+    P0 = p0;
+  }
   __device__ __forceinline__ bool locate(long long j, const uint16_t *&kp, const uint16_t *&vp) const {
     if (j >= P0) {
       const long long row = (j - P0) * hkv + kv;
@@ -91,19 +100,47 @@ __device__ __forceinline__ void softmax_update_n(float (&S)[NT][4], float &m0, f
 
 // One CTA: 64 (position, head) rows of KV head kv, flat rows
 // f0 .. f0+63 of the [C x G] row space (position f / G, head f % G).
-template <class Src, bool SINK>
+// VARLEN: the chunk, row tile and KV head come from the plan, and src0, q
+// and out point at sequence 0 / row 0 of the batch.
+template <class Src, bool SINK, bool VARLEN>
 __global__ void __launch_bounds__(PF_WARPS * 32, 2)
     prefill_kernel(const uint16_t *__restrict__ q, long long P0, int C, int hq, int G, int hkv, Src src0,
                    const float *__restrict__ sinks, const float *__restrict__ table, float scale_log2,
-                   uint16_t *__restrict__ out, unsigned *status) {
+                   uint16_t *__restrict__ out, unsigned *status, const VarlenPlan plan) {
   extern __shared__ __align__(128) uint8_t smem[];
   uint8_t *sQ = smem;
   uint8_t *sStage = smem + PF_ROWS * DQK * 2;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int kv = blockIdx.x % hkv;
-  const long long f0 = (long long)(blockIdx.x / hkv) * PF_ROWS;
-  const long long nrows = (long long)C * G;
+  int kv;
+  long long f0;
   Src src = src0;
+  if constexpr (VARLEN) {
+    const long long b = blockIdx.x;
+    if (b >= plan.item_prefix[plan.n]) return;
+    const int s = plan_find(plan.item_prefix, plan.n, b);
+    const int local = (int)(b - plan.item_prefix[s]);
+    kv = local % hkv;
+    f0 = (long long)(local / hkv) * PF_ROWS;
+    const long long c0 = plan.cu_rows[s];
+    C = (int)(plan.cu_rows[s + 1] - c0);
+    q += c0 * hq * DQK;
+    out += c0 * hq * DV;
+    if (plan.mode[s] <= 0) {  // a position or the sequence id is out of range
+      for (int it = tid; it < PF_ROWS * 16; it += blockDim.x) {
+        const long long f = f0 + it / 16;
+        if (f < (long long)C * G)
+          reinterpret_cast<uint4 *>(out + ((f / G) * hq + (long long)kv * G + f % G) * DV)[it % 16] =
+              make_uint4(0, 0, 0, 0);
+      }
+      return;
+    }
+    P0 = plan.P0[s];
+    src.rebase(plan.seq[s], c0, P0);
+  } else {
+    kv = blockIdx.x % hkv;
+    f0 = (long long)(blockIdx.x / hkv) * PF_ROWS;
+  }
+  const long long nrows = (long long)C * G;
   src.kv = kv;
   if constexpr (SINK) {
     src.rk += (long long)kv * WIN * DQK;
@@ -288,14 +325,32 @@ cudaError_t launch_swa_prefill(const uint16_t *q, int64_t P0, int C, int seq, in
                                cudaStream_t st) {
   (void)max_pos;
   const int hkv = ring.hkv, G = hq / hkv;
-  auto kern = prefill_kernel<SwaSrc, true>;
+  auto kern = prefill_kernel<SwaSrc, true, false>;
   cudaError_t e = ensure_smem_limit(3, (const void *)kern, PF_SMEM);
   if (e != cudaSuccess) return e;
   SwaSrc src{ring.k + (long long)seq * hkv * WIN * DQK, ring.v + (long long)seq * hkv * WIN * DV,
              ring.slot_pos + (long long)seq * WIN, chunk.k, chunk.v, hkv, 0, P0};
   const long long tiles = ((long long)C * G + PF_ROWS - 1) / PF_ROWS;
   kern<<<(unsigned)(tiles * hkv), PF_WARPS * 32, PF_SMEM, st>>>(q, P0, C, hq, G, hkv, src, sinks, table,
-                                                                 softmax_scale * LOG2E, out, status);
+                                                                 softmax_scale * LOG2E, out, status, VarlenPlan{});
+  return cudaGetLastError();
+}
+
+cudaError_t launch_swa_varlen(const uint16_t *q, const int32_t *cu_rows, const int64_t *P0, const int32_t *seq,
+                              int n, long long T, int hq, const KvView &chunk, const KvView &ring,
+                              const float *sinks, const float *table, int64_t max_pos, float softmax_scale,
+                              void *ws, uint16_t *out, unsigned *status, cudaStream_t st) {
+  const int hkv = ring.hkv, G = hq / hkv;
+  auto kern = prefill_kernel<SwaSrc, true, true>;
+  cudaError_t e = ensure_smem_limit(5, (const void *)kern, PF_SMEM);
+  if (e != cudaSuccess) return e;
+  const VarlenSizes z = varlen_sizes(n, T, hq, hkv, max_pos, PF_ROWS, false);
+  const VarlenPlan plan = varlen_plan_view(z, ws, cu_rows, P0, seq, n);
+  e = launch_varlen_plan(plan, T, hq, hkv, PF_ROWS, max_pos, ring.num_seqs, status, st);
+  if (e != cudaSuccess) return e;
+  SwaSrc src{ring.k, ring.v, ring.slot_pos, chunk.k, chunk.v, hkv, 0, 0};
+  kern<<<(unsigned)z.items_max, PF_WARPS * 32, PF_SMEM, st>>>(q, 0, 0, hq, G, hkv, src, sinks, table,
+                                                              softmax_scale * LOG2E, out, status, plan);
   return cudaGetLastError();
 }
 

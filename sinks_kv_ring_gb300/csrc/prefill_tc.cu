@@ -71,16 +71,29 @@ struct TcArgs {
   const uint16_t *q;
   long long P0;
   int C, hq, G, hkv;
-  const int32_t *bt;  // block-table row of the sequence
-  int bsz, num_blocks;
+  const int32_t *bt;  // block-table row of the sequence (one chunk) or the whole table (varlen)
+  int bsz, num_blocks, max_blocks;
   long long total_rows;  // rows of the pool tensors (num_blocks * hkv * bsz)
   const float *table;
   float scale_log2;
   uint16_t *out;
   unsigned *status;
+  VarlenPlan plan;       // varlen only
 };
 
+// Rows f0 .. f0+255 (those below nrows) of KV head kv's group, written as zeros.
+__device__ void zero_rows(uint16_t *oc, long long f0, long long nrows, int kv, int G, int hq) {
+  for (int it = threadIdx.x; it < 256 * 16; it += blockDim.x) {
+    const long long f = f0 + it / 16;
+    if (f < nrows)
+      reinterpret_cast<uint4 *>(oc + ((f / G) * hq + (long long)kv * G + f % G) * DV)[it % 16] = make_uint4(0, 0, 0, 0);
+  }
+}
+
 // 10 warps share 4 schedulers (3 warps on some), which caps registers at 168.
+// VARLEN: the CTA's work item comes from the plan (chunk, row tile, KV head,
+// key split); otherwise from blockIdx over one chunk.
+template <bool VARLEN>
 __global__ void __launch_bounds__(TC_THREADS, 1)
     full_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                            const TcArgs a) {
@@ -92,13 +105,49 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(gbase + TC_OFF_BAR + B_ABORT);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-  const int kv = blockIdx.x % a.hkv;
-  const long long f0 = (long long)(blockIdx.x / a.hkv) * 256;
-  const long long nrows = (long long)a.C * a.G;
+  // ---- the work item: flat rows f0 .. f0+255 of KV head kv's group (row f is
+  // position P0 + f / G, head f % G), keys k_lo .. k_hi-1
+  int kv, split = 0, nsp = 1;
+  long long f0, nrows, P0, prow = 0;
+  const uint16_t *qc = a.q;  // row 0 of the chunk
+  uint16_t *oc = a.out;
+  const int32_t *bt = a.bt;
+  if constexpr (VARLEN) {
+    const long long b = blockIdx.x;
+    if (b >= a.plan.item_prefix[a.plan.n]) return;
+    const int s = plan_find(a.plan.item_prefix, a.plan.n, b);
+    const int local = (int)(b - a.plan.item_prefix[s]);
+    const int mode = a.plan.mode[s];
+    const long long c0 = a.plan.cu_rows[s];
+    nrows = (a.plan.cu_rows[s + 1] - c0) * a.G;
+    qc += c0 * a.hq * DQK;
+    oc += c0 * a.hq * DV;
+    kv = local % a.hkv;
+    if (mode <= 0) {  // a position or the sequence id is out of range
+      zero_rows(oc, (long long)(local / a.hkv) * 256, nrows, kv, a.G, a.hq);
+      return;
+    }
+    nsp = mode;
+    split = (local / a.hkv) % nsp;
+    f0 = (long long)(local / a.hkv / nsp) * 256;
+    P0 = a.plan.P0[s];
+    bt += (long long)a.plan.seq[s] * a.max_blocks;
+    prow = a.plan.prow_prefix[s];
+  } else {
+    kv = blockIdx.x % a.hkv;
+    f0 = (long long)(blockIdx.x / a.hkv) * 256;
+    nrows = (long long)a.C * a.G;
+    P0 = a.P0;
+  }
   const long long i_last = min(nrows - 1, f0 + 255) / a.G;
-  const long long key_hi = a.P0 + i_last + 1;         // keys 0 .. key_hi-1
-  const int ntiles = (int)((key_hi + 127) / 128);
-  const long long pmin = a.P0 + f0 / a.G;            // smallest row position in the CTA
+  long long k_lo = 0, k_hi = P0 + i_last + 1;
+  if (nsp > 1) {
+    k_lo = split * a.plan.split_len;
+    k_hi = min(k_hi, k_lo + a.plan.split_len);
+  }
+  const int ntiles = (int)((k_hi - k_lo + 127) / 128);
+  const long long pmin = P0 + f0 / a.G;  // smallest row position in the CTA
+  const int nq = f0 + 128 < nrows ? 2 : 1;  // query tiles with live rows
 
   // ---- set-up: barriers, TMEM, rotated Q tiles
   if (tid == 0) {
@@ -121,13 +170,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   }
   // Q rows: CTA row r -> tile r / 128, TMEM lane r % 128; flat row f0 + r is
   // position (f0 + r) / G, head (f0 + r) % G of this KV head's group.
-  for (int it = tid; it < 256 * 20; it += TC_THREADS) {
+  for (int it = tid; it < nq * 128 * 20; it += TC_THREADS) {
     const int r = it / 20, c = it % 20;
     const long long f = f0 + r;
     const bool live = f < nrows;
     const long long i = live ? f / a.G : 0;
     const int g = live ? (int)(f % a.G) : 0;
-    const uint16_t *qh = a.q + (i * a.hq + (long long)kv * a.G + g) * DQK;
+    const uint16_t *qh = qc + (i * a.hq + (long long)kv * a.G + g) * DQK;
     const int t = r & 127;
     uint8_t *qt = gbase + (r >> 7) * TC_QTILE;
     auto chunk_ptr = [&](int ch) {  // 16-byte chunk ch (0..23) of row t, 128-byte swizzle
@@ -137,7 +186,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     if (c < 4) {
       uint4 o1 = zero, o2 = zero;
       if (live) {
-        const float4 *tr = reinterpret_cast<const float4 *>(a.table + (a.P0 + i) * 64 + 16 * c);
+        const float4 *tr = reinterpret_cast<const float4 *>(a.table + (P0 + i) * 64 + 16 * c);
         float cs[16];
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
@@ -169,13 +218,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     const int rb = low < 128 ? low : 128;      // rows per box: divides the page size and 128
     const int nb = 128 / rb;
     const int total = (int)a.total_rows;       // < 2^31, checked by the launcher
-    const int khi = (int)key_hi;
+    const int khi = (int)k_hi, klo = (int)k_lo;
     auto box_row = [&](int t) {
       int y = total;                           // past the end: the TMA unit fills zeros
       if (lane < nb) {
-        const int key = 128 * t + lane * rb;
+        const int key = klo + 128 * t + lane * rb;
         if (key < khi) {
-          const int blk = a.bt[key / a.bsz];
+          const int blk = bt[key / a.bsz];
           if (blk >= 0 && blk < a.num_blocks)
             y = (blk * a.hkv + kv) * a.bsz + key % a.bsz;
           else
@@ -252,10 +301,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       const long long L0 = 5LL * t + 3;
       for (int db = 0; db < 2; ++db) {
         if (!wait_full(L0 + db)) { ok = false; return; }
-        if (i == 0 && t == ntiles - 1 && 128LL * t + 128 > key_hi) {
+        if (i == 0 && t == ntiles - 1 && k_lo + 128LL * t + 128 > k_hi) {
           // Rows past the last key may hold stale bytes of the page; P is 0
           // there, but 0 * NaN is not, so zero them before the product.
-          const int first = (int)(key_hi - 128LL * t);
+          const int first = (int)(k_hi - k_lo - 128LL * t);
           uint4 *g = reinterpret_cast<uint4 *>(gbase + TC_OFF_RING + slot_of(L0 + db) * TC_SLOT);
           for (int e = first * 8 + lane; e < 128 * 8; e += 32) g[e] = make_uint4(0, 0, 0, 0);
           fence_proxy_async_smem();
@@ -285,18 +334,20 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         mma_commit_elect(sBar + B_EMPTY + 8 * s1);
       }
     };
-    issue_S(0, 0, false);
-    if (ok) issue_S(1, 0, true);
+    // With one live query tile, tile 0's products release the ring slots.
+    const bool one = nq == 1;
+    issue_S(0, 0, one);
+    if (ok && !one) issue_S(1, 0, true);
     for (int t = 1; t < ntiles && ok; ++t) {
-      issue_PV(0, t - 1, false);
-      if (ok) issue_S(0, t, false);
-      if (ok) issue_PV(1, t - 1, true);
-      if (ok) issue_S(1, t, true);
+      issue_PV(0, t - 1, one);
+      if (ok) issue_S(0, t, one);
+      if (ok && !one) issue_PV(1, t - 1, true);
+      if (ok && !one) issue_S(1, t, true);
     }
-    if (ok) issue_PV(0, ntiles - 1, false);
+    if (ok) issue_PV(0, ntiles - 1, one);
     if (ok) mma_commit_elect(sBar + B_OFINAL);
-    if (ok) issue_PV(1, ntiles - 1, true);
-    if (ok) mma_commit_elect(sBar + B_OFINAL + 8);
+    if (ok && !one) issue_PV(1, ntiles - 1, true);
+    if (ok && !one) mma_commit_elect(sBar + B_OFINAL + 8);
     // Every MMA issued must be finished before TMEM is released (bounded by
     // time only, even after an abort).
     mma_commit_elect(sBar + B_DRAIN);
@@ -315,19 +366,19 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     const long long f = f0 + 128 * wg + row;
     const bool live = f < nrows;
     const long long fc = live ? f : nrows - 1;
-    const long long pr = a.P0 + fc / a.G;
+    const long long pr = P0 + fc / a.G;
     const int g = (int)(fc % a.G);
     const float sl2 = a.scale_log2;
     float m_ref = NEG_INF, l = 0.f;
-    bool ok = true;
-    for (int t = 0; t < ntiles; ++t) {
+    bool ok = wg < nq;
+    for (int t = 0; t < ntiles && ok; ++t) {
       if (!warp_wait(sBar + B_SFULL + 8 * wg, (uint32_t)t & 1u, abort_flag)) { ok = false; break; }
       tc_fence_after();
       uint32_t s[4][32];
 #pragma unroll
       for (int c = 0; c < 4; ++c) tmem_ld32(tS + 32 * c, s[c]);
       tmem_wait_ld();
-      const long long j0 = 128LL * t;
+      const long long j0 = k_lo + 128LL * t;
       if (j0 + 127 > pmin) {  // the diagonal (and the end of the keys) is in this tile
 #pragma unroll
         for (int c = 0; c < 4; ++c)
@@ -387,10 +438,30 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       tc_fence_before();
       mbar_arrive(sBar + B_PREADY + 8 * wg);
     }
-    if (ok && warp_wait(sBar + B_OFINAL + 8 * wg, 0, abort_flag)) {
+    if (ok) ok = warp_wait(sBar + B_OFINAL + 8 * wg, 0, abort_flag);
+    if (ok && nsp > 1) {
+      // One split of the keys: the unnormalised numerator, the max (log2
+      // units) and the sum, merged later by varlen_combine_kernel.
+      tc_fence_after();
+      const long long rec = (prow + (pr - P0) * a.hq + (long long)kv * a.G + g) * a.plan.nsp_max + split;
+      if (live) a.plan.pml[rec] = make_float2(m_ref, l);
+      float4 *dst = reinterpret_cast<float4 *>(a.plan.po + rec * DV);
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t o[32];
+        tmem_ld32(tO + 32 * c, o);
+        tmem_wait_ld();
+        if (live) {
+#pragma unroll
+          for (int u = 0; u < 8; ++u)
+            dst[8 * c + u] = make_float4(__uint_as_float(o[4 * u]), __uint_as_float(o[4 * u + 1]),
+                                         __uint_as_float(o[4 * u + 2]), __uint_as_float(o[4 * u + 3]));
+        }
+      }
+    } else if (ok) {
       tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
-      uint16_t *orow = a.out + ((pr - a.P0) * a.hq + (long long)kv * a.G + g) * DV;
+      uint16_t *orow = oc + ((pr - P0) * a.hq + (long long)kv * a.G + g) * DV;
 #pragma unroll 1
       for (int c = 0; c < 4; ++c) {
         uint32_t o[32];
@@ -423,38 +494,74 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 
 }  // namespace
 
-cudaError_t launch_full_prefill(const uint16_t *q, int64_t P0, int C, int seq, int hq, const KvView &pool,
-                                const float *table, int64_t max_pos, float softmax_scale, uint16_t *out,
-                                unsigned *status, cudaStream_t st) {
-  (void)max_pos;
-  const int hkv = pool.hkv, G = hq / hkv;
+namespace {
+
+// Tensor maps of the pool and the common kernel arguments.
+cudaError_t tc_setup(const KvView &pool, int hq, const float *table, float softmax_scale, uint16_t *out,
+                     unsigned *status, CUtensorMap *mk, CUtensorMap *mv, TcArgs *a) {
+  const int hkv = pool.hkv;
   const long long rows = (long long)pool.num_blocks * hkv * pool.block_size;
   if (rows >= (1LL << 31)) return cudaErrorInvalidValue;
   const int low = pool.block_size & -pool.block_size;
   const int box_rows = low < 128 ? low : 128;
-  CUtensorMap mk, mv;
-  if (!make_tma_map_2d(&mk, pool.k, rows, DQK, box_rows) || !make_tma_map_2d(&mv, pool.v, rows, DV, box_rows))
+  if (!make_tma_map_2d(mk, pool.k, rows, DQK, box_rows) || !make_tma_map_2d(mv, pool.v, rows, DV, box_rows))
     return cudaErrorInvalidValue;
-  cudaError_t e = ensure_smem_limit(2, (const void *)full_prefill_tc_kernel, TC_SMEM);
-  if (e != cudaSuccess) return e;
+  *a = TcArgs{};
+  a->hq = hq;
+  a->G = hq / hkv;
+  a->hkv = hkv;
+  a->bt = pool.block_table;
+  a->bsz = pool.block_size;
+  a->num_blocks = pool.num_blocks;
+  a->max_blocks = pool.max_blocks;
+  a->total_rows = rows;
+  a->table = table;
+  a->scale_log2 = softmax_scale * LOG2E;
+  a->out = out;
+  a->status = status;
+  return cudaSuccess;
+}
+
+}  // namespace
+
+cudaError_t launch_full_prefill(const uint16_t *q, int64_t P0, int C, int seq, int hq, const KvView &pool,
+                                const float *table, int64_t max_pos, float softmax_scale, uint16_t *out,
+                                unsigned *status, cudaStream_t st) {
+  (void)max_pos;
+  CUtensorMap mk, mv;
   TcArgs a;
+  cudaError_t e = tc_setup(pool, hq, table, softmax_scale, out, status, &mk, &mv, &a);
+  if (e != cudaSuccess) return e;
+  e = ensure_smem_limit(2, (const void *)full_prefill_tc_kernel<false>, TC_SMEM);
+  if (e != cudaSuccess) return e;
   a.q = q;
   a.P0 = P0;
   a.C = C;
-  a.hq = hq;
-  a.G = G;
-  a.hkv = hkv;
   a.bt = pool.block_table + (long long)seq * pool.max_blocks;
-  a.bsz = pool.block_size;
-  a.num_blocks = pool.num_blocks;
-  a.total_rows = rows;
-  a.table = table;
-  a.scale_log2 = softmax_scale * LOG2E;
-  a.out = out;
-  a.status = status;
-  const long long ctas = ((long long)C * G + 255) / 256 * hkv;
-  full_prefill_tc_kernel<<<(unsigned)ctas, TC_THREADS, TC_SMEM, st>>>(mk, mv, a);
+  const long long ctas = ((long long)C * a.G + 255) / 256 * a.hkv;
+  full_prefill_tc_kernel<false><<<(unsigned)ctas, TC_THREADS, TC_SMEM, st>>>(mk, mv, a);
   return cudaGetLastError();
+}
+
+cudaError_t launch_full_varlen(const uint16_t *q, const int32_t *cu_rows, const int64_t *P0, const int32_t *seq,
+                               int n, long long T, int hq, const KvView &pool, const float *table,
+                               float softmax_scale, long long max_ctx, void *ws, uint16_t *out, unsigned *status,
+                               cudaStream_t st) {
+  CUtensorMap mk, mv;
+  TcArgs a;
+  cudaError_t e = tc_setup(pool, hq, table, softmax_scale, out, status, &mk, &mv, &a);
+  if (e != cudaSuccess) return e;
+  e = ensure_smem_limit(4, (const void *)full_prefill_tc_kernel<true>, TC_SMEM);
+  if (e != cudaSuccess) return e;
+  const VarlenSizes z = varlen_sizes(n, T, hq, pool.hkv, max_ctx, 256, true);
+  a.q = q;
+  a.plan = varlen_plan_view(z, ws, cu_rows, P0, seq, n);
+  e = launch_varlen_plan(a.plan, T, hq, pool.hkv, 256, max_ctx, pool.num_seqs, status, st);
+  if (e != cudaSuccess) return e;
+  full_prefill_tc_kernel<true><<<(unsigned)z.items_max, TC_THREADS, TC_SMEM, st>>>(mk, mv, a);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  return launch_varlen_combine(a.plan, z.prows_max, hq, out, st);
 }
 
 }  // namespace kvr

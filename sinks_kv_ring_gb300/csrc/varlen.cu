@@ -1,0 +1,228 @@
+// varlen.cu -- batches of chunks of different lengths: the device-side work
+// plan, and the merge of key-split partials.
+//
+// A batch holds n chunks; chunk s is C_s rows at positions P0_s .. P0_s+C_s-1
+// of sequence seq_s.  With C_s = 1 this is a decode step, with C_s = 2..4 the
+// verification of a multi-token-prediction draft (the Chinese Xiaomi article,
+// section "Decode加速与多模态优化": the model proposes several tokens per step
+// and checks them together), and with large C_s a prefill chunk (section
+// "调度与Prefill优化": requests of very different lengths batched by length
+// bucket).  The plan is built on the device, so a batch can be launched from
+// device-resident lengths and captured in a CUDA graph.
+#include <algorithm>
+
+#include "launch.h"
+
+namespace kvr {
+namespace {
+
+constexpr int PLAN_THREADS = 1024;
+
+struct PlanArgs {
+  VarlenPlan p;
+  long long T;          // rows of the batch
+  int hq, hkv, G;
+  int tile_rows;        // query rows of one CTA item
+  long long max_ctx;    // P0 + C must not exceed it
+  int num_seqs;
+  unsigned *status;
+};
+
+// One CTA: per chunk its mode and item / partial-row counts, then exclusive
+// prefix sums, 1024 chunks at a time.
+__global__ void __launch_bounds__(PLAN_THREADS) varlen_plan_kernel(const PlanArgs a) {
+  __shared__ int wsum[32][2];
+  __shared__ int carry[2];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) carry[0] = carry[1] = 0;
+  __syncthreads();
+  for (int base = 0; base < a.p.n; base += PLAN_THREADS) {
+    const int s = base + tid;
+    int items = 0, prows = 0;
+    if (s < a.p.n) {
+      int mode = 1;
+      const long long c0 = a.p.cu_rows[s], c1 = a.p.cu_rows[s + 1];
+      if (c0 < 0 || c1 < c0 || c1 > a.T) {
+        flag(a.status, ST_BAD_ROWS);
+        mode = -1;
+      } else if (c1 > c0) {
+        const long long C = c1 - c0, P0 = a.p.P0[s];
+        const int sq = a.p.seq[s];
+        const long long tiles = (C * a.G + a.tile_rows - 1) / a.tile_rows;
+        bool bad = false;
+        if (sq < 0 || sq >= a.num_seqs) { flag(a.status, ST_BAD_SEQ); bad = true; }
+        if (P0 < 0 || P0 + C > a.max_ctx) { flag(a.status, ST_BAD_POS); bad = true; }
+        if (bad) {
+          mode = 0;
+          items = (int)(tiles * a.hkv);
+        } else if (a.p.split_len > 0 && tiles == 1) {
+          const int nsp = (int)((P0 + C + a.p.split_len - 1) / a.p.split_len);
+          mode = nsp;
+          items = nsp * a.hkv;
+          prows = nsp > 1 ? (int)(C * a.hq) : 0;
+        } else {
+          items = (int)(tiles * a.hkv);
+        }
+      }
+      a.p.mode[s] = mode;
+    }
+    // block-wide exclusive scan of (items, prows)
+    int vi = items, vp = prows;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int ti = __shfl_up_sync(0xffffffffu, vi, d), tp = __shfl_up_sync(0xffffffffu, vp, d);
+      if (lane >= d) { vi += ti; vp += tp; }
+    }
+    if (lane == 31) { wsum[warp][0] = vi; wsum[warp][1] = vp; }
+    __syncthreads();
+    if (warp == 0) {
+      int wi = wsum[lane][0], wp = wsum[lane][1];
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const int ti = __shfl_up_sync(0xffffffffu, wi, d), tp = __shfl_up_sync(0xffffffffu, wp, d);
+        if (lane >= d) { wi += ti; wp += tp; }
+      }
+      wsum[lane][0] = wi;  // inclusive over warps
+      wsum[lane][1] = wp;
+    }
+    __syncthreads();
+    const int off_i = carry[0] + (warp ? wsum[warp - 1][0] : 0);
+    const int off_p = carry[1] + (warp ? wsum[warp - 1][1] : 0);
+    if (s < a.p.n) {
+      a.p.item_prefix[s] = off_i + vi - items;
+      a.p.prow_prefix[s] = off_p + vp - prows;
+    }
+    __syncthreads();
+    if (tid == 0) {
+      carry[0] += wsum[31][0];
+      carry[1] += wsum[31][1];
+    }
+    __syncthreads();
+  }
+  if (tid == 0) {
+    a.p.item_prefix[a.p.n] = carry[0];
+    a.p.prow_prefix[a.p.n] = carry[1];
+  }
+}
+
+struct CombineArgs {
+  VarlenPlan p;
+  int hq;
+  uint16_t *out;
+};
+
+// One warp per partial row (row, q head) of a split chunk: merge its splits
+// by log-sum-exp (Xiaomi "Full-Pipeline Inference Optimization", section 1.2,
+// split decode) and write the normalised bf16 row.  Lane = 4 value dims.
+__global__ void __launch_bounds__(256) varlen_combine_kernel(const CombineArgs a) {
+  const long long r = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  const int total = a.p.prow_prefix[a.p.n];
+  if (r >= total) return;
+  const int s = plan_find(a.p.prow_prefix, a.p.n, r);
+  const long long local = r - a.p.prow_prefix[s];
+  const long long i = local / a.hq;
+  const int h = (int)(local % a.hq);
+  const int nsp = a.p.mode[s];
+  const long long rec0 = r * a.p.nsp_max;
+  float M = -INFINITY;
+  for (int k = 0; k < nsp; ++k) M = fmaxf(M, a.p.pml[rec0 + k].x);
+  float l = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (M != -INFINITY) {
+    for (int k = 0; k < nsp; ++k) {
+      const float2 ml = a.p.pml[rec0 + k];
+      const float w = ml.x == -INFINITY ? 0.f : ex2(ml.x - M);
+      const float4 o = reinterpret_cast<const float4 *>(a.p.po + (rec0 + k) * DV)[lane];
+      l += w * ml.y;
+      acc.x += w * o.x;
+      acc.y += w * o.y;
+      acc.z += w * o.z;
+      acc.w += w * o.w;
+    }
+  }
+  const float inv = l > 0.f ? 1.f / l : 0.f;
+  uint2 v;
+  v.x = pack_bf16(acc.x * inv, acc.y * inv);
+  v.y = pack_bf16(acc.z * inv, acc.w * inv);
+  reinterpret_cast<uint2 *>(a.out + ((a.p.cu_rows[s] + i) * a.hq + h) * DV)[lane] = v;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+}  // namespace
+
+VarlenSizes varlen_sizes(int n, long long T, int hq, int hkv, long long max_ctx, int tile_rows, bool splits) {
+  VarlenSizes z{};
+  const int G = hq / hkv;
+  z.tile_rows = tile_rows;
+  z.split_len = 0;
+  z.nsp_max = 1;
+  if (splits) {
+    // Aim for about eight waves of one-CTA-per-SM items when every chunk is a
+    // single query tile; splits are multiples of 128 keys, at least 1024.
+    const long long target = 8LL * num_sms();
+    long long L = ((long long)n * hkv * max_ctx + target - 1) / target;
+    L = (L + 127) / 128 * 128;
+    if (L < 1024) L = 1024;
+    z.split_len = L;
+    z.nsp_max = (int)((max_ctx + L - 1) / L);
+  }
+  const long long small_rows = std::min(T, (long long)n * (tile_rows / G));
+  z.prows_max = z.nsp_max > 1 ? small_rows * hq : 0;
+  const long long tiles = (T * G + tile_rows - 1) / tile_rows;
+  z.items_max = (long long)hkv * (tiles + n + (long long)n * z.nsp_max);
+  z.off_prow = align256(((size_t)n + 1) * 4);
+  z.off_mode = z.off_prow + align256(((size_t)n + 1) * 4);
+  z.off_pml = z.off_mode + align256((size_t)n * 4);
+  const size_t recs = (size_t)z.prows_max * z.nsp_max;
+  z.off_po = z.off_pml + align256(recs * 8);
+  z.bytes = z.off_po + recs * DV * 4;
+  return z;
+}
+
+VarlenPlan varlen_plan_view(const VarlenSizes &z, void *ws, const int32_t *cu_rows, const int64_t *P0,
+                            const int32_t *seq, int n) {
+  uint8_t *b = static_cast<uint8_t *>(ws);
+  VarlenPlan p;
+  p.cu_rows = cu_rows;
+  p.P0 = P0;
+  p.seq = seq;
+  p.item_prefix = reinterpret_cast<int32_t *>(b);
+  p.prow_prefix = reinterpret_cast<int32_t *>(b + z.off_prow);
+  p.mode = reinterpret_cast<int32_t *>(b + z.off_mode);
+  p.pml = reinterpret_cast<float2 *>(b + z.off_pml);
+  p.po = reinterpret_cast<float *>(b + z.off_po);
+  p.n = n;
+  p.nsp_max = z.nsp_max;
+  p.split_len = z.split_len;
+  return p;
+}
+
+cudaError_t launch_varlen_plan(const VarlenPlan &p, long long T, int hq, int hkv, int tile_rows, long long max_ctx,
+                               int num_seqs, unsigned *status, cudaStream_t st) {
+  PlanArgs a;
+  a.p = p;
+  a.T = T;
+  a.hq = hq;
+  a.hkv = hkv;
+  a.G = hq / hkv;
+  a.tile_rows = tile_rows;
+  a.max_ctx = max_ctx;
+  a.num_seqs = num_seqs;
+  a.status = status;
+  varlen_plan_kernel<<<1, PLAN_THREADS, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_varlen_combine(const VarlenPlan &p, long long prows_max, int hq, uint16_t *out, cudaStream_t st) {
+  if (prows_max <= 0) return cudaSuccess;
+  CombineArgs a;
+  a.p = p;
+  a.hq = hq;
+  a.out = out;
+  varlen_combine_kernel<<<(unsigned)((prows_max + 7) / 8), 256, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace kvr

@@ -101,6 +101,39 @@ def test_host_validation_codes(L):
     assert L.swa_sink_decode(P, P, P, 0, 64, ctypes.byref(ring), P, P, 1000, 0.1, P, None) == 0
 
 
+def test_varlen_host_validation_codes(L):
+    P = ctypes.c_void_p(FAKE)
+    ring, pool = _ring(), _paged()
+    lin = kvr._Layout(kind=3, num_kv_heads=8, k=FAKE, v=FAKE, slot_pos=None, block_table=None, num_seqs=0,
+                      max_blocks=0, block_size=0, num_blocks=0, num_rows=100)
+    need = L.full_attn_prefill_varlen_workspace_size(4, 16, 64, 4, 1000)
+    assert need > 0
+    assert L.full_attn_prefill_varlen_workspace_size(4, 16, 62, 4, 1000) == 0  # Hq % Hkv
+    # workspace too small; max_ctx past the table; null cu_rows; wrong layout kind
+    assert L.full_attn_prefill_varlen(P, P, P, P, 4, 16, 64, ctypes.byref(pool), P, 1000, 0.1, 1000, P, need - 1,
+                                      P, None) == -3
+    assert L.full_attn_prefill_varlen(P, P, P, P, 4, 16, 64, ctypes.byref(pool), P, 1000, 0.1, 1001, P, 1 << 40,
+                                      P, None) == -2
+    assert L.full_attn_prefill_varlen(P, None, P, P, 4, 16, 64, ctypes.byref(pool), P, 1000, 0.1, 1000, P,
+                                      1 << 40, P, None) == -1
+    assert L.full_attn_prefill_varlen(P, P, P, P, 4, 16, 64, ctypes.byref(ring), P, 1000, 0.1, 1000, P, 1 << 40,
+                                      P, None) == -1
+    # empty batches succeed without a GPU
+    assert L.full_attn_prefill_varlen(P, P, P, P, 0, 16, 64, ctypes.byref(pool), P, 1000, 0.1, 1000, None, 0, P,
+                                      None) == 0
+    wsn = L.swa_sink_prefill_varlen_workspace_size(4)
+    assert wsn >= 4 * 3 * 4
+    # chunk rows < T; workspace too small; unaligned out
+    assert L.swa_sink_prefill_varlen(P, P, P, P, 4, 200, 64, ctypes.byref(lin), ctypes.byref(ring), P, P, 1000, 0.1,
+                                     P, 1 << 30, P, None) == -1
+    assert L.swa_sink_prefill_varlen(P, P, P, P, 4, 16, 64, ctypes.byref(lin), ctypes.byref(ring), P, P, 1000, 0.1,
+                                     P, wsn - 1, P, None) == -3
+    assert L.swa_sink_prefill_varlen(P, P, P, P, 4, 16, 64, ctypes.byref(lin), ctypes.byref(ring), P, P, 1000, 0.1,
+                                     P, 1 << 30, ctypes.c_void_p(FAKE + 2), None) == -1
+    assert L.swa_sink_prefill_varlen(P, P, P, P, 4, 0, 64, ctypes.byref(lin), ctypes.byref(ring), P, P, 1000, 0.1,
+                                     None, 0, P, None) == 0
+
+
 def test_workspace_size_grows_with_context(L):
     a = L.full_attn_decode_workspace_size(64, 64, 4, 32769)
     b = L.full_attn_decode_workspace_size(64, 64, 4, 2 * 32769)

@@ -1,0 +1,284 @@
+"""GPU parity of the varlen calls (batches of chunks of different lengths)
+against the fp64 oracle: multi-token-prediction draft verification (C = 1..4
+per sequence), mixed prefill + decode batches, key-split boundaries, bad
+device-side inputs, and replay in a CUDA graph with new lengths."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import sinks_kv_ring_gb300 as kvr
+from sinks_kv_ring_gb300.synth import Synth
+
+from kvr_cases import SCALE, compare_rows, fill_paged, fill_ring, raw_kv
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+VS = 0.707
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from sinks_kv_ring_gb300 import build
+    build.build()
+    kvr.device_status(reset=True)
+    yield
+
+
+@pytest.fixture(scope="module")
+def tables():
+    return {1e4: kvr.rope_table(1e4, 1 << 16), 1e7: kvr.rope_table(1e7, 1 << 16)}
+
+
+def _batch(syn, hq, hkv, seqs, P0s, Cs):
+    """q rows of the batch in chunk order, plus the device plan arrays."""
+    qs = [syn.q(C, hq, hkv, seq=s, start=P0) for s, P0, C in zip(seqs, P0s, Cs)]
+    q = torch.cat(qs) if qs else torch.empty(0, hq, 192, dtype=torch.bfloat16, device=DEV)
+    cu = torch.tensor(np.concatenate([[0], np.cumsum(Cs)]), dtype=torch.int32, device=DEV)
+    return (q.contiguous(), cu, torch.tensor(P0s, dtype=torch.int64, device=DEV),
+            torch.tensor(seqs, dtype=torch.int32, device=DEV))
+
+
+def _full_case(syn, hq, hkv, seqs, P0s, Cs, tables, bsz=64, num_seqs=None):
+    """Pool holding positions 0..P0+C-1 of every chunk's sequence (the drafts
+    appended), the batch, and the oracle rows."""
+    ns = num_seqs or (max(seqs) + 1)
+    max_ctx = max(P0 + C for P0, C in zip(P0s, Cs))
+    pool = kvr.PagedLayout.contiguous(ns, hkv, max_ctx, block_size=bsz)
+    fill_paged(pool, syn, seqs, [P0 + C for P0, C in zip(P0s, Cs)], tables[1e7], VS)
+    q, cu, P0, sq = _batch(syn, hq, hkv, seqs, P0s, Cs)
+    return pool, q, cu, P0, sq, max_ctx
+
+
+def _full_want(syn, hkv, q, seqs, P0s, Cs):
+    rows, r = [], 0
+    for s, P0, C in zip(seqs, P0s, Cs):
+        if C:
+            k, v = raw_kv(syn, hkv, s, 0, P0 + C)
+            rows.append(oracle.attend_seq(q[r:r + C], np.arange(P0, P0 + C), k, v, 0, 1e7, VS, SCALE, 0, None))
+        r += C
+    return np.concatenate(rows)
+
+
+@pytest.mark.parametrize("hq,hkv", [(64, 4), (64, 8), (16, 4)])
+def test_full_varlen_draft_verification(hq, hkv, tables):
+    # Draft lengths 1..4; contexts around the 1024-key split boundaries,
+    # including a row whose last split holds no key it may see (P0 = 2047,
+    # C = 2: the split from 2048 on holds only the draft's second token).
+    syn = Synth(3101 + hq + hkv, dist="shifted", device=DEV)
+    seqs = [0, 1, 2, 3, 4, 5, 6]
+    P0s = [0, 129, 1021, 2047, 2044, 4999, 300]
+    Cs = [1, 2, 3, 2, 4, 4, 3]
+    pool, q, cu, P0, sq, max_ctx = _full_case(syn, hq, hkv, seqs, P0s, Cs, tables)
+    out = kvr.full_attn_prefill_varlen(q, cu, P0, sq, pool, tables[1e7], SCALE, max_ctx)
+    torch.cuda.synchronize()
+    assert kvr.device_status() == 0
+    compare_rows(out, _full_want(syn, hkv, q, seqs, P0s, Cs), "full varlen draft")
+
+
+def test_full_varlen_mixed_prefill_and_decode(tables):
+    # One prefill chunk (several 256-row tiles, no key split) beside single
+    # decode tokens and an empty chunk, in one call; the ragged chunk order
+    # puts sequences out of order.
+    syn = Synth(3201, dist="plain", device=DEV)
+    hq, hkv = 32, 4
+    seqs = [3, 0, 2, 1, 4]
+    P0s = [700, 5000, 33, 2500, 0]
+    Cs = [300, 1, 1, 0, 1]
+    pool, q, cu, P0, sq, max_ctx = _full_case(syn, hq, hkv, seqs, P0s, Cs, tables, bsz=128)
+    out = kvr.full_attn_prefill_varlen(q, cu, P0, sq, pool, tables[1e7], SCALE, max_ctx)
+    torch.cuda.synchronize()
+    assert kvr.device_status() == 0
+    want = _full_want(syn, hkv, q, seqs, P0s, Cs)
+    rows = list(range(0, 300, 37)) + [299, 300, 301, 302]
+    compare_rows(out[rows], want[rows], "full varlen mixed")
+
+
+def test_full_varlen_one_chunk_equals_prefill_chunk(tables):
+    # A chunk too long to be split runs the same arithmetic as the single-chunk
+    # call: bit-identical outputs.
+    syn = Synth(3301, dist="plain", device=DEV)
+    hq, hkv = 64, 4
+    pool, q, cu, P0, sq, max_ctx = _full_case(syn, hq, hkv, [0], [3000], [333], tables)
+    a = kvr.full_attn_prefill_varlen(q, cu, P0, sq, pool, tables[1e7], SCALE, max_ctx)
+    b = kvr.full_attn_prefill_chunk(q, 3000, 0, pool, tables[1e7], SCALE)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
+
+
+def test_full_varlen_many_splits_large_batch(tables):
+    # 64 draft chunks of 3 tokens with contexts up to ~20K: several splits per
+    # chunk at the plan's split length; sampled chunks, all rows and heads.
+    syn = Synth(3401, dist="shifted", device=DEV)
+    hq, hkv = 64, 4
+    rng = np.random.default_rng(3401)
+    n = 64
+    P0s = [int(x) for x in rng.integers(1, 20000, size=n)]
+    seqs = list(range(n))
+    Cs = [3] * n
+    pool, q, cu, P0, sq, max_ctx = _full_case(syn, hq, hkv, seqs, P0s, Cs, tables, bsz=256)
+    out = kvr.full_attn_prefill_varlen(q, cu, P0, sq, pool, tables[1e7], SCALE, max_ctx)
+    torch.cuda.synchronize()
+    assert kvr.device_status() == 0
+    for s in (0, 17, 40, 63):
+        k, v = raw_kv(syn, hkv, s, 0, P0s[s] + 3)
+        want = oracle.attend_seq(q[3 * s:3 * s + 3], np.arange(P0s[s], P0s[s] + 3), k, v, 0, 1e7, VS, SCALE, 0, None)
+        compare_rows(out[3 * s:3 * s + 3], want, f"full varlen chunk {s}")
+
+
+# --------------------------------------------------------------------------- windowed
+
+def _swa_case(syn, hq, hkv, seqs, P0s, Cs, tables, num_seqs=None):
+    """Rings holding each sequence's window before its chunk, the chunk rows
+    in a LINEAR staging layout (batch order), and the batch."""
+    ns = num_seqs or (max(seqs) + 1)
+    ring = kvr.RingLayout.empty(ns, hkv)
+    fill_ring(ring, syn, [s for s, P0 in zip(seqs, P0s) if P0 > 0], [P0 - 1 for P0 in P0s if P0 > 0], tables[1e4], VS)
+    ks, vs, ps = [], [], []
+    for s, P0, C in zip(seqs, P0s, Cs):
+        k, v = raw_kv(syn, hkv, s, P0, P0 + C)
+        ks.append(k)
+        vs.append(v)
+        ps.append(torch.arange(P0, P0 + C, dtype=torch.int64, device=DEV))
+    T = sum(Cs)
+    stage = kvr.LinearLayout.empty(max(T, 1), hkv)
+    if T:
+        kvr.kv_ring_append_rope(torch.cat(ks).contiguous(), torch.cat(vs).contiguous(), torch.cat(ps), None,
+                                tables[1e4], VS, stage)
+    q, cu, P0, sq = _batch(syn, hq, hkv, seqs, P0s, Cs)
+    return ring, stage, q, cu, P0, sq
+
+
+def _swa_want(syn, hkv, q, seqs, P0s, Cs, sinks):
+    rows, r = [], 0
+    for s, P0, C in zip(seqs, P0s, Cs):
+        if C:
+            lo = max(0, P0 - 127)
+            k, v = raw_kv(syn, hkv, s, lo, P0 + C)
+            rows.append(oracle.attend_seq(q[r:r + C], np.arange(P0, P0 + C), k, v, lo, 1e4, VS, SCALE, 128,
+                                          sinks.double().cpu().numpy()))
+        r += C
+    return np.concatenate(rows)
+
+
+@pytest.mark.parametrize("dist", ["shifted", "plain"])
+@pytest.mark.parametrize("hq,hkv", [(64, 8), (16, 8), (32, 2)])
+def test_swa_varlen_draft_verification(dist, hq, hkv, tables):
+    # Draft lengths 1..4 with the ring before the draft: empty ring, partly
+    # filled, exactly full, wrapped several times.
+    syn = Synth(3501 + hq + hkv, dist=dist, device=DEV)
+    sinks = syn.sinks(hq).to(DEV)
+    seqs = [0, 1, 2, 3, 4, 5]
+    P0s = [0, 5, 127, 128, 1000, 4093]
+    Cs = [4, 1, 2, 3, 4, 2]
+    ring, stage, q, cu, P0, sq = _swa_case(syn, hq, hkv, seqs, P0s, Cs, tables)
+    out = kvr.swa_sink_prefill_varlen(q, cu, P0, sq, stage, ring, sinks, tables[1e4], SCALE)
+    torch.cuda.synchronize()
+    assert kvr.device_status() == 0
+    compare_rows(out, _swa_want(syn, hkv, q, seqs, P0s, Cs, sinks), "swa varlen draft")
+
+
+def test_swa_varlen_mixed_and_equal_to_single_chunks(tables):
+    # A long chunk beside decode tokens; every chunk's rows equal the
+    # single-chunk call on the same ring and rows, bit for bit.
+    syn = Synth(3601, dist="shifted", device=DEV)
+    hq, hkv = 64, 8
+    sinks = syn.sinks(hq).to(DEV)
+    seqs = [2, 0, 1]
+    P0s = [900, 77, 3000]
+    Cs = [513, 1, 1]
+    ring, stage, q, cu, P0, sq = _swa_case(syn, hq, hkv, seqs, P0s, Cs, tables)
+    out = kvr.swa_sink_prefill_varlen(q, cu, P0, sq, stage, ring, sinks, tables[1e4], SCALE)
+    r = 0
+    for s, p0, C in zip(seqs, P0s, Cs):
+        st = kvr.LinearLayout(stage.k[r:r + C].contiguous(), stage.v[r:r + C].contiguous())
+        one = kvr.swa_sink_prefill_chunk(q[r:r + C].contiguous(), p0, s, st, ring, sinks, tables[1e4], SCALE)
+        torch.cuda.synchronize()
+        assert torch.equal(out[r:r + C], one), f"chunk of sequence {s}"
+        r += C
+    want = _swa_want(syn, hkv, q, seqs, P0s, Cs, sinks)
+    rows = list(range(0, 513, 41)) + [512, 513, 514]
+    compare_rows(out[rows], want[rows], "swa varlen mixed")
+    assert kvr.device_status() == 0
+
+
+# --------------------------------------------------------------------------- bad inputs, graphs
+
+def test_varlen_bad_device_inputs_are_flagged(tables):
+    syn = Synth(3701, dist="plain", device=DEV)
+    hq, hkv = 16, 4
+    seqs, P0s, Cs = [0, 1, 0, 1], [100, 200, 50, 60], [2, 3, 1, 2]
+    pool, q, cu, P0, sq, max_ctx = _full_case(syn, hq, hkv, seqs, P0s, Cs, tables)
+    good = kvr.full_attn_prefill_varlen(q, cu, P0, sq, pool, tables[1e7], SCALE, max_ctx)
+    torch.cuda.synchronize()
+    assert kvr.device_status() == 0
+    # chunk 1: sequence id outside the pool -> zeros, BAD_SEQ
+    sq_bad = sq.clone()
+    sq_bad[1] = 9
+    out = kvr.full_attn_prefill_varlen(q, cu, P0, sq_bad, pool, tables[1e7], SCALE, max_ctx)
+    torch.cuda.synchronize()
+    assert kvr.device_status() == kvr.DEV_BAD_SEQ
+    assert torch.count_nonzero(out[2:5]) == 0
+    assert torch.equal(out[:2], good[:2]) and torch.equal(out[5:], good[5:])
+    # chunk 2: P0 + C past max_ctx -> zeros, BAD_POS
+    P0_bad = P0.clone()
+    P0_bad[2] = max_ctx
+    out = kvr.full_attn_prefill_varlen(q, cu, P0_bad, sq, pool, tables[1e7], SCALE, max_ctx)
+    torch.cuda.synchronize()
+    assert kvr.device_status() == kvr.DEV_BAD_POS
+    assert torch.count_nonzero(out[5:6]) == 0
+    assert torch.equal(out[:5], good[:5]) and torch.equal(out[6:], good[6:])
+    # chunk 1's rows end past T -> skipped (rows untouched), BAD_ROWS
+    cu_bad = cu.clone()
+    cu_bad[2] = 100
+    out = torch.full_like(good, 3.0)
+    kvr.full_attn_prefill_varlen(q, cu_bad, P0, sq, pool, tables[1e7], SCALE, max_ctx, out=out)
+    torch.cuda.synchronize()
+    assert kvr.device_status() & kvr.DEV_BAD_ROWS
+    assert torch.equal(out[:2], good[:2]) and torch.equal(out[6:], good[6:])
+    assert torch.all(out[2:6] == 3.0)
+    # the windowed call: bad sequence id -> zeros, BAD_SEQ
+    sinks = syn.sinks(hq).to(DEV)
+    ring, stage, q2, cu2, P02, sq2 = _swa_case(syn, hq, hkv, seqs, P0s, Cs, tables)
+    sq2[0] = -1
+    out = kvr.swa_sink_prefill_varlen(q2, cu2, P02, sq2, stage, ring, sinks, tables[1e4], SCALE)
+    torch.cuda.synchronize()
+    assert kvr.device_status() == kvr.DEV_BAD_SEQ
+    assert torch.count_nonzero(out[:2]) == 0 and torch.count_nonzero(out[2:]) > 0
+
+
+def test_varlen_calls_replay_in_a_cuda_graph_with_new_lengths(tables):
+    # The plan is built on the device: a captured call replays with other
+    # positions / lengths written into the same device arrays.
+    syn = Synth(3801, dist="plain", device=DEV)
+    hq, hkv = 64, 4
+    seqs, P0s, Cs = [0, 1, 2], [1500, 40, 3000], [3, 3, 3]
+    pool, q, cu, P0, sq, max_ctx = _full_case(syn, hq, hkv, seqs, P0s, Cs, tables)
+    ws = torch.empty(kvr.full_attn_prefill_varlen_workspace_size(3, 9, hq, hkv, max_ctx), dtype=torch.uint8,
+                     device=DEV)
+    out = torch.empty(9, hq, 128, dtype=torch.bfloat16, device=DEV)
+    kvr.full_attn_prefill_varlen(q, cu, P0, sq, pool, tables[1e7], SCALE, max_ctx, workspace=ws, out=out)
+    torch.cuda.synchronize()
+    first = out.clone()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            kvr.full_attn_prefill_varlen(q, cu, P0, sq, pool, tables[1e7], SCALE, max_ctx, workspace=ws, out=out,
+                                         stream=s)
+    out.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out, first)
+    # new lengths: chunk 0 verifies 2 tokens at 1000, chunk 1 one token, chunk 2 six
+    P0.copy_(torch.tensor([1000, 40, 2990], device=DEV))
+    cu.copy_(torch.tensor([0, 2, 3, 9], dtype=torch.int32, device=DEV))
+    g.replay()
+    torch.cuda.synchronize()
+    assert kvr.device_status() == 0
+    want = _full_want(syn, hkv, q, seqs, [1000, 40, 2990], [2, 1, 6])
+    compare_rows(out, want, "graph replay, new lengths")
