@@ -8,7 +8,10 @@ step = the KV write of the new token into both layers (RoPE + value scale)
 also carries a chunked-prefill measurement (8192-token chunk on 122880
 cached tokens, one full + one windowed layer) under "prefill".
 
-Other workloads: prefill, long_decode (batch 16 at 524288 tokens),
+The line also carries "mtp": the same batch verifying a 4-token draft per
+sequence (multi-token prediction) through the varlen calls.
+
+Other workloads: prefill, long_decode (batch 16 at 524288 tokens), mtp_decode,
 pro_mixed (128 ragged sequences through a 70-layer stack, 10 full : 60
 windowed), tiny (1 sequence, 512 tokens).
 
@@ -39,6 +42,7 @@ import torch  # noqa: E402
 
 SCALE = 1.0 / math.sqrt(192.0)
 METRIC = "decode attn tokens/s + HBM GB/s; prefill attn TFLOP/s; % of GB300 roofline"
+MTP_MAX = 4
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -206,10 +210,11 @@ class DecodeWorkload:
         self.p = ctx                      # the new token's position; context = ctx + 1
         self.max_ctx = ctx + 1
         dev = device
-        self.t4 = kvr.rope_table(1e4, ctx + 1, device=dev)
-        self.t7 = kvr.rope_table(1e7, ctx + 1, device=dev)
+        # tables (and pool capacity) also cover a draft of up to MTP_MAX tokens at p
+        self.t4 = kvr.rope_table(1e4, ctx + MTP_MAX, device=dev)
+        self.t7 = kvr.rope_table(1e7, ctx + MTP_MAX, device=dev)
         syn = Synth(seed, dist="shifted", device=dev)
-        self.pool = kvr.PagedLayout.contiguous(B, hkv_full, self.max_ctx, block_size=64, device=dev, zero=False)
+        self.pool = kvr.PagedLayout.contiguous(B, hkv_full, ctx + MTP_MAX, block_size=64, device=dev, zero=False)
         _fill_pool(kvr, self.pool, Synth(seed, layer=1, device=dev), range(B), [ctx] * B, self.t7, vscale)
         ring_bytes = kvr.RingLayout.bytes_per_layer(B, hkv_swa)
         if swa_copies is None:
@@ -268,6 +273,91 @@ class DecodeWorkload:
         ins = [self.q_swa, self.q_full, self.k_swa, self.v_swa, self.k_full, self.v_full, self.pos]
         outs = [self.out_swa, self.out_full]
         return [(pin(t), t) for t in ins], [(torch.empty(t.shape, dtype=t.dtype, pin_memory=True), t) for t in outs]
+
+
+class MtpStep:
+    """Draft verification (multi-token prediction) on a decode workload's
+    pool and rings: each of the B sequences checks q_len tokens at positions
+    p .. p+q_len-1 in one pass per layer.  Step = KV write of the draft into
+    the full pool and into the windowed staging rows + full_attn_prefill_varlen
+    + swa_sink_prefill_varlen.  (Committing the accepted tokens to the ring is
+    the decode step's ring append.)"""
+
+    def __init__(self, work, q_len=4, seed=1005):
+        from sinks_kv_ring_gb300.synth import Synth
+        kvr, B, dev = work.kvr, work.B, work.pool.k.device
+        assert 1 <= q_len <= MTP_MAX
+        self.work, self.kvr, self.B, self.q_len = work, kvr, B, q_len
+        T = B * q_len
+        sf, ss = Synth(seed, layer=1, device=dev), Synth(seed, layer=0, device=dev)
+        self.qf, self.qs = sf.q(T, work.hq, work.hkv_full, seq=30_000), ss.q(T, work.hq, work.hkv_swa, seq=30_000)
+        self.kf, self.vf = sf.k(T, work.hkv_full, seq=40_000), sf.v(T, work.hkv_full, seq=40_000)
+        self.ks, self.vs = ss.k(T, work.hkv_swa, seq=40_000), ss.v(T, work.hkv_swa, seq=40_000)
+        self.pos = (work.p + torch.arange(q_len, device=dev)).repeat(B)
+        self.seq_rows = torch.arange(B, dtype=torch.int32, device=dev).repeat_interleave(q_len)
+        self.cu = torch.arange(0, T + 1, q_len, dtype=torch.int32, device=dev)
+        self.P0 = torch.full((B,), work.p, dtype=torch.int64, device=dev)
+        self.seq = torch.arange(B, dtype=torch.int32, device=dev)
+        self.max_ctx = work.p + q_len
+        self.stage = kvr.LinearLayout.empty(T, work.hkv_swa, device=dev)
+        self.ws_f = torch.empty(kvr.full_attn_prefill_varlen_workspace_size(B, T, work.hq, work.hkv_full, self.max_ctx),
+                                dtype=torch.uint8, device=dev)
+        self.ws_s = torch.empty(kvr.swa_sink_prefill_varlen_workspace_size(B), dtype=torch.uint8, device=dev)
+        self.out_f = torch.empty(T, work.hq, 128, dtype=torch.bfloat16, device=dev)
+        self.out_s = torch.empty(T, work.hq, 128, dtype=torch.bfloat16, device=dev)
+        self.t_full, self.t_swa = EventTimer(), EventTimer()
+        self.step_i = 0
+        self.launches_per_step = 2 + 3 + 2   # two appends, varlen full (plan, attention, merge), varlen windowed
+
+    def bytes_full(self):
+        w = self.work
+        return self.B * w.hkv_full * self.max_ctx * (192 + 128) * 2
+
+    def bytes_swa(self):
+        w = self.work
+        return self.B * w.hkv_swa * (min(128, w.p) + self.q_len) * (192 + 128) * 2
+
+    def step(self, stream, timed=False):
+        kvr, w = self.kvr, self.work
+        ring = w.rings[self.step_i % len(w.rings)]
+        self.step_i += 1
+        kvr.kv_ring_append_rope(self.kf, self.vf, self.pos, self.seq_rows, w.t7, w.vscale, w.pool, stream=stream)
+        kvr.kv_ring_append_rope(self.ks, self.vs, self.pos, None, w.t4, w.vscale, self.stage, stream=stream)
+        a = self.t_full.start(stream) if timed else None
+        kvr.full_attn_prefill_varlen(self.qf, self.cu, self.P0, self.seq, w.pool, w.t7, SCALE, self.max_ctx,
+                                     workspace=self.ws_f, out=self.out_f, stream=stream)
+        if timed:
+            self.t_full.stop(a, stream)
+            a = self.t_swa.start(stream)
+        kvr.swa_sink_prefill_varlen(self.qs, self.cu, self.P0, self.seq, self.stage, ring, w.sinks, w.t4, SCALE,
+                                    workspace=self.ws_s, out=self.out_s, stream=stream)
+        if timed:
+            self.t_swa.stop(a, stream)
+
+
+def run_mtp(work, steps, warmup, q_len=4):
+    stream = torch.cuda.current_stream()
+    m = MtpStep(work, q_len=q_len)
+    with Clocks(torch.cuda.current_device()) as ck:
+        ms = timed_run(m, steps, warmup, stream, label="mtp")
+    full = [(lambda st: m.kvr.full_attn_prefill_varlen(m.qf, m.cu, m.P0, m.seq, work.pool, work.t7, SCALE, m.max_ctx,
+                                                       workspace=m.ws_f, out=m.out_f, stream=st))] * 10
+    return m, ms, ck.summary(), graph_time_ms(full)
+
+
+def mtp_result(m, ms, clocks, graph_full, hbm, world):
+    ms_f, ms_s = m.t_full.mean_ms(), m.t_swa.mean_ms()
+    gbs = m.bytes_full() / (ms_f / 1e3) / 1e9
+    ggbs = m.bytes_full() / (graph_full / 1e3) / 1e9
+    return {"workload": f"draft verification: batch {m.B}, {m.q_len} tokens per sequence at positions "
+                        f"{m.work.p}..{m.work.p + m.q_len - 1}; same layers and pools as the decode step",
+            "ms_per_step": round(ms, 4), "verified_tokens_per_s": round(job_throughput(m.B * m.q_len, world, ms), 1),
+            "full_attn_prefill_varlen": {"ms": round(ms_f, 4), "GB/s": round(gbs, 1), "hbm_frac": round(gbs / hbm, 4),
+                                         "bytes": m.bytes_full(), "graph_ms": round(graph_full, 4),
+                                         "graph_GB/s": round(ggbs, 1), "graph_hbm_frac": round(ggbs / hbm, 4)},
+            "swa_sink_prefill_varlen": {"ms": round(ms_s, 5), "bytes": m.bytes_swa(),
+                                        "GB/s": round(m.bytes_swa() / (ms_s / 1e3) / 1e9, 1)},
+            "clocks": clocks}
 
 
 class PrefillWorkload:
@@ -488,7 +578,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="flash_decode",
-                    choices=["flash_decode", "long_decode", "prefill", "pro_mixed"])
+                    choices=["flash_decode", "long_decode", "prefill", "pro_mixed", "mtp_decode"])
+    ap.add_argument("--mtp-len", type=int, default=4, help="draft tokens verified per sequence (mtp_decode)")
     ap.add_argument("--no-prefill", action="store_true", help="skip the prefill sub-measurement")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--batch", type=int, default=None, help="decode batch per GPU (default: the workload's)")
@@ -529,6 +620,8 @@ def main():
         return prefill_only(args, kvr, peaks_d, peaks_src, rank, world)
     if args.workload == "pro_mixed":
         return pro_mixed(args, kvr, peaks_d, peaks_src, rank, world)
+    if args.workload == "mtp_decode":
+        return mtp_only(args, kvr, peaks_d, peaks_src, rank, world)
 
     work, ms, ms_full, ms_swa, clocks, (e2e_ms, h2d, d2h) = run_decode(args, kvr, rank)
     ms, e2e_ms = max_over_ranks([ms, e2e_ms], world, "cuda")
@@ -570,6 +663,11 @@ def main():
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline_decode(work, max_seqs=16 if args.workload == "flash_decode" else 2)
+    if args.workload == "flash_decode":
+        m, mms, mck, mg = run_mtp(work, min(20, args.steps), 3)
+        res["mtp"] = mtp_result(m, mms, mck, mg, hbm, world)
+        res["gpu_launches"] += m.launches_per_step * min(20, args.steps)
+        del m
     if not args.no_prefill and args.workload == "flash_decode":
         del work
         torch.cuda.empty_cache()
@@ -600,6 +698,33 @@ def main():
         import torch.distributed as dist
         dist.barrier()
         dist.destroy_process_group()
+
+
+def mtp_only(args, kvr, peaks_d, peaks_src, rank, world):
+    """Draft verification as the step (see MtpStep)."""
+    work = DecodeWorkload(kvr, B=args.batch, ctx=args.ctx, seed=rank_seed(1001, rank), swa_copies=None)
+    torch.cuda.synchronize()
+    steps = args.steps if "--steps" in sys.argv else 200
+    m, ms, ck, g = run_mtp(work, steps, args.warmup, q_len=args.mtp_len)
+    ms = max_over_ranks([ms], world, "cuda")[0]
+    hbm = peaks_d["hbm_gbs"]
+    r = mtp_result(m, ms, ck, g, hbm, world)
+    kf = r["full_attn_prefill_varlen"]
+    res = {"metric": METRIC, "value": r["verified_tokens_per_s"], "unit": "tokens/s", "n_gpus": world,
+           "steps": steps, "warmup": args.warmup, "ms_per_step": r["ms_per_step"], "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+           "config": {"workload": "mtp_decode: " + r["workload"] + f"; full layer 4 KV heads at context {m.max_ctx}, "
+                                  "windowed layer 8 KV heads ring 128 + sink; 64 q heads",
+                      "global_batch": m.B * world, "seq_len": m.max_ctx, "parallelism": f"dp{world}",
+                      "l2": f"inputs > L2: full pool {m.bytes_full() / 1e9:.2f} GB read per step; rings rotated over "
+                            f"{len(work.rings)} copies"},
+           "kernels": {k: v for k, v in r.items() if k.endswith("varlen")},
+           "roofline": {"bound": "hbm", "achieved": kf["GB/s"], "peak": hbm, "unit": "GB/s", "frac": kf["hbm_frac"],
+                        "peak_source": peaks_src, "kernel": "full_attn_prefill_varlen (plan + tensor-core kernel + merge)",
+                        "traffic": None},
+           "gpu_launches": m.launches_per_step * steps, "clocks": r["clocks"]}
+    if rank == 0:
+        print(json.dumps(res), flush=True)
 
 
 def prefill_only(args, kvr, peaks_d, peaks_src, rank, world):

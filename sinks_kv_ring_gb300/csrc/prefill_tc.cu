@@ -147,7 +147,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   }
   const int ntiles = (int)((k_hi - k_lo + 127) / 128);
   const long long pmin = P0 + f0 / a.G;  // smallest row position in the CTA
-  const int nq = f0 + 128 < nrows ? 2 : 1;  // query tiles with live rows
+  // query tiles with live rows (a single chunk always runs both)
+  const int nq = (!VARLEN || f0 + 128 < nrows) ? 2 : 1;
 
   // ---- set-up: barriers, TMEM, rotated Q tiles
   if (tid == 0) {

@@ -6,6 +6,8 @@ times: sampled outputs against the fp64 oracle.
 * Chunked prefill: 8192-token chunk on 122880 cached tokens -- sampled rows
   (first, last, window and tile boundaries), all heads, both layer kinds.
 * Long-context decode: batch 16 at context 524289 -- sampled sequences.
+* Draft verification: the decode batch checking 4 tokens per sequence
+  through the varlen calls -- sampled sequences, all rows and heads.
 
 Raw K/V are regenerated from the same seeded draws the bench used (never read
 back from the CUDA path).
@@ -80,6 +82,36 @@ def test_flash_decode_full_size_sampled(kvr):
     torch.cuda.synchronize()
     assert torch.equal(out2, work.out_full)
     del work
+    torch.cuda.empty_cache()
+
+
+def test_draft_verification_full_size_sampled(kvr):
+    # The bench's draft-verification step: batch 64, 4 tokens per sequence at
+    # positions 32768..32771, both layer kinds, through the varlen calls.
+    import bench
+    from sinks_kv_ring_gb300.synth import Synth
+    work = bench.DecodeWorkload(kvr, B=64, ctx=32768, seed=1001, swa_copies=1)
+    m = bench.MtpStep(work, q_len=4)
+    m.step(torch.cuda.current_stream())
+    torch.cuda.synchronize()
+    assert kvr.device_status() == 0
+    p = work.p
+    syn_f = Synth(1001, layer=1, device="cuda")
+    syn_s = Synth(1001, layer=0, device="cuda")
+    sk = work.sinks.double().cpu().numpy()
+    lo = p - 127
+    pos = np.arange(p, p + 4)
+    for b in [0, 33, 63]:
+        r = slice(4 * b, 4 * b + 4)
+        kf, vf = _pool_raw(syn_f, work.hkv_full, b, p)
+        kf, vf = torch.cat([kf, m.kf[r]]), torch.cat([vf, m.vf[r]])
+        want = oracle.attend_seq(m.qf[r], pos, kf, vf, 0, 1e7, work.vscale, SCALE, 0, None)
+        compare_rows(m.out_f[r], want, f"draft full b={b}")
+        ks = torch.cat([syn_s.k(p - lo, work.hkv_swa, seq=b, start=lo), m.ks[r]])
+        vs = torch.cat([syn_s.v(p - lo, work.hkv_swa, seq=b, start=lo), m.vs[r]])
+        want = oracle.attend_seq(m.qs[r], pos, ks, vs, lo, 1e4, work.vscale, SCALE, 128, sk)
+        compare_rows(m.out_s[r], want, f"draft swa b={b}")
+    del m, work
     torch.cuda.empty_cache()
 
 
