@@ -91,6 +91,16 @@ __device__ __forceinline__ uint32_t swz(int row, int chunk) {
   return (uint32_t)(row * ROW_ELEMS * 2 + ((chunk ^ (row & 7)) << 4));
 }
 
+// Byte offset of 16-byte chunk ch of row r in a [rows][PARTS][128 B] tile
+// written by a 3-D (or 4-D) TMA box with the 128-byte swizzle: segment
+// seg = r * PARTS + ch / 8, chunk (ch % 8) ^ (seg % 8).  For PARTS = 3 the 8
+// rows an ldmatrix reads at one chunk land on 8 different bank groups.
+template <int PARTS>
+__device__ __forceinline__ uint32_t swrow(int r, int ch) {
+  const int seg = r * PARTS + (ch >> 3);
+  return (uint32_t)(seg * 128 + (((ch & 7) ^ (seg & 7)) << 4));
+}
+
 // Rotate-half RoPE of 8 + 8 elements (dims 8c..8c+7 and 32+8c..32+8c+7 of a
 // head).  cs16 holds (cos, sin) of frequencies 8c..8c+7, interleaved; results
 // are rounded to bf16 and packed.
@@ -123,7 +133,8 @@ __device__ __forceinline__ void rope_pair8(const uint4 &x1v, const uint4 &x2v, c
 // nothing is written), 0 (a position or sequence id out of range: its rows
 // are written as zeros), or k >= 1 (the keys are cut into k splits).
 // Split chunks own partial rows prow_prefix[s] .. prow_prefix[s+1]-1, one per
-// (row, q head), each with nsp_max records (m, l) + o[128].
+// (row, q head), each with nsp_max records (m, l) + o[128].  Chunks listed in
+// short_list have no items: a kernel for short chunks takes them whole.
 struct VarlenPlan {
   const int32_t *cu_rows;
   const int64_t *P0;
@@ -131,6 +142,7 @@ struct VarlenPlan {
   int32_t *item_prefix;  // [n+1]
   int32_t *prow_prefix;  // [n+1]
   int32_t *mode;         // [n]
+  int32_t *short_list;   // [n+1]: ids of the chunks taken by the short-chunk kernel; count at [n]
   float2 *pml;           // [prows][nsp_max]: (max in log2 units, sum of exponentials)
   float *po;             // [prows][nsp_max][128]: unnormalised numerators
   int n;

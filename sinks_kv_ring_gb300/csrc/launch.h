@@ -66,13 +66,15 @@ struct VarlenSizes {
   int nsp_max;
   long long prows_max;   // partial rows the workspace holds
   long long items_max;   // bound on the CTA items of any plan (the grid size)
-  size_t off_prow, off_mode, off_pml, off_po, bytes;
+  size_t off_prow, off_mode, off_short, off_pml, off_po, bytes;
 };
 VarlenSizes varlen_sizes(int n, long long T, int hq, int hkv, long long max_ctx, int tile_rows, bool splits);
 VarlenPlan varlen_plan_view(const VarlenSizes &z, void *ws, const int32_t *cu_rows, const int64_t *P0,
                             const int32_t *seq, int n);
+// short_rows > 0: chunks of at most short_rows query rows (C * G) and at most
+// short_max_c rows go to short_list instead of getting items.
 cudaError_t launch_varlen_plan(const VarlenPlan &p, long long T, int hq, int hkv, int tile_rows, long long max_ctx,
-                               int num_seqs, unsigned *status, cudaStream_t st);
+                               int num_seqs, int short_rows, int short_max_c, unsigned *status, cudaStream_t st);
 cudaError_t launch_varlen_combine(const VarlenPlan &p, long long prows_max, int hq, uint16_t *out, cudaStream_t st);
 
 // Varlen attention: rows of chunk s are q/out rows cu_rows[s] ..; the plan
@@ -85,6 +87,18 @@ cudaError_t launch_swa_varlen(const uint16_t *q, const int32_t *cu_rows, const i
                               int n, long long T, int hq, const KvView &chunk, const KvView &ring,
                               const float *sinks, const float *table, int64_t max_pos, float softmax_scale,
                               void *ws, uint16_t *out, unsigned *status, cudaStream_t st);
+
+// Windowed attention of the short chunks of a varlen plan (short_list).
+cudaError_t launch_swa_short(const uint16_t *q, const VarlenPlan &plan, int n, long long T, int hq,
+                             const KvView &chunk, const KvView &ring, const float *sinks, const float *table,
+                             float softmax_scale, uint16_t *out, unsigned *status, cudaStream_t st);
+constexpr int SWA_SHORT_ROWS = 32;   // C * G of a short chunk
+constexpr int SWA_SHORT_MAX_C = 16;  // C of a short chunk
+
+// 4-D tensor map over LINEAR rows [T][hkv][width] bf16 viewed as
+// [T][hkv][width/64][64]: one box brings box_rows consecutive tokens of one
+// KV head, every 64-element part (smem [token][part][64], 128-byte swizzle).
+bool make_tma_map_tokens4d(CUtensorMap *m, const void *ptr, long long T, int hkv, int width, int box_rows);
 
 cudaError_t launch_ring_copy(const KvView &ring, const int32_t *seqs, int n, uint16_t *k_snap, uint16_t *v_snap,
                              int32_t *tags_snap, bool to_ring, unsigned *status, cudaStream_t st);

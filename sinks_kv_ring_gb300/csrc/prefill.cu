@@ -346,12 +346,17 @@ cudaError_t launch_swa_varlen(const uint16_t *q, const int32_t *cu_rows, const i
   if (e != cudaSuccess) return e;
   const VarlenSizes z = varlen_sizes(n, T, hq, hkv, max_pos, PF_ROWS, false);
   const VarlenPlan plan = varlen_plan_view(z, ws, cu_rows, P0, seq, n);
-  e = launch_varlen_plan(plan, T, hq, hkv, PF_ROWS, max_pos, ring.num_seqs, status, st);
+  e = launch_varlen_plan(plan, T, hq, hkv, PF_ROWS, max_pos, ring.num_seqs, SWA_SHORT_ROWS, SWA_SHORT_MAX_C, status,
+                         st);
   if (e != cudaSuccess) return e;
+  // Short chunks (a few tokens per sequence) go to the short-chunk kernel;
+  // the rest are tiled here.
   SwaSrc src{ring.k, ring.v, ring.slot_pos, chunk.k, chunk.v, hkv, 0, 0};
   kern<<<(unsigned)z.items_max, PF_WARPS * 32, PF_SMEM, st>>>(q, 0, 0, hq, G, hkv, src, sinks, table,
                                                               softmax_scale * LOG2E, out, status, plan);
-  return cudaGetLastError();
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  return launch_swa_short(q, plan, n, T, hq, chunk, ring, sinks, table, softmax_scale, out, status, st);
 }
 
 }  // namespace kvr

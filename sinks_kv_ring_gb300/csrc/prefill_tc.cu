@@ -557,7 +557,7 @@ cudaError_t launch_full_varlen(const uint16_t *q, const int32_t *cu_rows, const 
   const VarlenSizes z = varlen_sizes(n, T, hq, pool.hkv, max_ctx, 256, true);
   a.q = q;
   a.plan = varlen_plan_view(z, ws, cu_rows, P0, seq, n);
-  e = launch_varlen_plan(a.plan, T, hq, pool.hkv, 256, max_ctx, pool.num_seqs, status, st);
+  e = launch_varlen_plan(a.plan, T, hq, pool.hkv, 256, max_ctx, pool.num_seqs, 0, 0, status, st);
   if (e != cudaSuccess) return e;
   full_prefill_tc_kernel<true><<<(unsigned)z.items_max, TC_THREADS, TC_SMEM, st>>>(mk, mv, a);
   e = cudaGetLastError();

@@ -58,16 +58,6 @@ constexpr int SD_OFF_BAR = SD_OFF_ROW + SD_MAX_UNITS * 4;
 constexpr int SD_SMEM = SD_OFF_BAR + 8 * SD_NSTAGE + 32 + 1024;
 constexpr unsigned ST_TIMEOUT = 8u;
 
-// Byte offset of 16-byte chunk ch of row r in a [rows][PARTS][128 B] tile
-// written by a 3-D TMA box with the 128-byte swizzle: segment
-// seg = r * PARTS + ch / 8, chunk (ch % 8) ^ (seg % 8).  For PARTS = 3 the 8
-// rows an ldmatrix reads at one chunk land on 8 different bank groups.
-template <int PARTS>
-__device__ __forceinline__ uint32_t swrow(int r, int ch) {
-  const int seg = r * PARTS + (ch >> 3);
-  return (uint32_t)(seg * 128 + (((ch & 7) ^ (seg & 7)) << 4));
-}
-
 struct SdArgs {
   const uint16_t *q;
   const int64_t *pos;

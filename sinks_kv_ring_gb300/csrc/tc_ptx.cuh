@@ -99,6 +99,13 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *map, int x
       : "memory");
 }
 
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const void *map, int x, int y, int z, int w, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], [%6];"
+      ::"r"(dst), "l"(map), "r"(x), "r"(y), "r"(z), "r"(w), "r"(bar)
+      : "memory");
+}
+
 // Warp-converged variants: every lane executes the instruction with the same
 // operands and elect.sync lets exactly one of them issue it.  This keeps the
 // operands warp-uniform, which is what the tensor-core and TMA issue paths

@@ -25,20 +25,21 @@ struct PlanArgs {
   int tile_rows;        // query rows of one CTA item
   long long max_ctx;    // P0 + C must not exceed it
   int num_seqs;
+  int short_rows, short_max_c;  // 0: no short-chunk kernel
   unsigned *status;
 };
 
-// One CTA: per chunk its mode and item / partial-row counts, then exclusive
-// prefix sums, 1024 chunks at a time.
+// One CTA: per chunk its mode, item / partial-row counts and short flag,
+// then exclusive prefix sums, 1024 chunks at a time.
 __global__ void __launch_bounds__(PLAN_THREADS) varlen_plan_kernel(const PlanArgs a) {
-  __shared__ int wsum[32][2];
-  __shared__ int carry[2];
+  __shared__ int wsum[32][3];
+  __shared__ int carry[3];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  if (tid == 0) carry[0] = carry[1] = 0;
+  if (tid == 0) carry[0] = carry[1] = carry[2] = 0;
   __syncthreads();
   for (int base = 0; base < a.p.n; base += PLAN_THREADS) {
     const int s = base + tid;
-    int items = 0, prows = 0;
+    int items = 0, prows = 0, shrt = 0;
     if (s < a.p.n) {
       int mode = 1;
       const long long c0 = a.p.cu_rows[s], c1 = a.p.cu_rows[s + 1];
@@ -55,6 +56,8 @@ __global__ void __launch_bounds__(PLAN_THREADS) varlen_plan_kernel(const PlanArg
         if (bad) {
           mode = 0;
           items = (int)(tiles * a.hkv);
+        } else if (a.short_rows > 0 && C * a.G <= a.short_rows && C <= a.short_max_c) {
+          shrt = 1;
         } else if (a.p.split_len > 0 && tiles == 1) {
           const int nsp = (int)((P0 + C + a.p.split_len - 1) / a.p.split_len);
           mode = nsp;
@@ -66,42 +69,46 @@ __global__ void __launch_bounds__(PLAN_THREADS) varlen_plan_kernel(const PlanArg
       }
       a.p.mode[s] = mode;
     }
-    // block-wide exclusive scan of (items, prows)
-    int vi = items, vp = prows;
+    // block-wide exclusive scan of (items, prows, short)
+    int v[3] = {items, prows, shrt};
 #pragma unroll
     for (int d = 1; d < 32; d <<= 1) {
-      const int ti = __shfl_up_sync(0xffffffffu, vi, d), tp = __shfl_up_sync(0xffffffffu, vp, d);
-      if (lane >= d) { vi += ti; vp += tp; }
+#pragma unroll
+      for (int k = 0; k < 3; ++k) {
+        const int t = __shfl_up_sync(0xffffffffu, v[k], d);
+        if (lane >= d) v[k] += t;
+      }
     }
-    if (lane == 31) { wsum[warp][0] = vi; wsum[warp][1] = vp; }
+    if (lane == 31)
+      for (int k = 0; k < 3; ++k) wsum[warp][k] = v[k];
     __syncthreads();
     if (warp == 0) {
-      int wi = wsum[lane][0], wp = wsum[lane][1];
+      int w[3] = {wsum[lane][0], wsum[lane][1], wsum[lane][2]};
 #pragma unroll
       for (int d = 1; d < 32; d <<= 1) {
-        const int ti = __shfl_up_sync(0xffffffffu, wi, d), tp = __shfl_up_sync(0xffffffffu, wp, d);
-        if (lane >= d) { wi += ti; wp += tp; }
+#pragma unroll
+        for (int k = 0; k < 3; ++k) {
+          const int t = __shfl_up_sync(0xffffffffu, w[k], d);
+          if (lane >= d) w[k] += t;
+        }
       }
-      wsum[lane][0] = wi;  // inclusive over warps
-      wsum[lane][1] = wp;
+      for (int k = 0; k < 3; ++k) wsum[lane][k] = w[k];  // inclusive over warps
     }
     __syncthreads();
-    const int off_i = carry[0] + (warp ? wsum[warp - 1][0] : 0);
-    const int off_p = carry[1] + (warp ? wsum[warp - 1][1] : 0);
     if (s < a.p.n) {
-      a.p.item_prefix[s] = off_i + vi - items;
-      a.p.prow_prefix[s] = off_p + vp - prows;
+      a.p.item_prefix[s] = carry[0] + (warp ? wsum[warp - 1][0] : 0) + v[0] - items;
+      a.p.prow_prefix[s] = carry[1] + (warp ? wsum[warp - 1][1] : 0) + v[1] - prows;
+      if (shrt) a.p.short_list[carry[2] + (warp ? wsum[warp - 1][2] : 0) + v[2] - 1] = s;
     }
     __syncthreads();
-    if (tid == 0) {
-      carry[0] += wsum[31][0];
-      carry[1] += wsum[31][1];
-    }
+    if (tid == 0)
+      for (int k = 0; k < 3; ++k) carry[k] += wsum[31][k];
     __syncthreads();
   }
   if (tid == 0) {
     a.p.item_prefix[a.p.n] = carry[0];
     a.p.prow_prefix[a.p.n] = carry[1];
+    a.p.short_list[a.p.n] = carry[2];
   }
 }
 
@@ -174,7 +181,8 @@ VarlenSizes varlen_sizes(int n, long long T, int hq, int hkv, long long max_ctx,
   z.items_max = (long long)hkv * (tiles + n + (long long)n * z.nsp_max);
   z.off_prow = align256(((size_t)n + 1) * 4);
   z.off_mode = z.off_prow + align256(((size_t)n + 1) * 4);
-  z.off_pml = z.off_mode + align256((size_t)n * 4);
+  z.off_short = z.off_mode + align256((size_t)n * 4);
+  z.off_pml = z.off_short + align256(((size_t)n + 1) * 4);
   const size_t recs = (size_t)z.prows_max * z.nsp_max;
   z.off_po = z.off_pml + align256(recs * 8);
   z.bytes = z.off_po + recs * DV * 4;
@@ -191,6 +199,7 @@ VarlenPlan varlen_plan_view(const VarlenSizes &z, void *ws, const int32_t *cu_ro
   p.item_prefix = reinterpret_cast<int32_t *>(b);
   p.prow_prefix = reinterpret_cast<int32_t *>(b + z.off_prow);
   p.mode = reinterpret_cast<int32_t *>(b + z.off_mode);
+  p.short_list = reinterpret_cast<int32_t *>(b + z.off_short);
   p.pml = reinterpret_cast<float2 *>(b + z.off_pml);
   p.po = reinterpret_cast<float *>(b + z.off_po);
   p.n = n;
@@ -200,7 +209,7 @@ VarlenPlan varlen_plan_view(const VarlenSizes &z, void *ws, const int32_t *cu_ro
 }
 
 cudaError_t launch_varlen_plan(const VarlenPlan &p, long long T, int hq, int hkv, int tile_rows, long long max_ctx,
-                               int num_seqs, unsigned *status, cudaStream_t st) {
+                               int num_seqs, int short_rows, int short_max_c, unsigned *status, cudaStream_t st) {
   PlanArgs a;
   a.p = p;
   a.T = T;
@@ -210,6 +219,8 @@ cudaError_t launch_varlen_plan(const VarlenPlan &p, long long T, int hq, int hkv
   a.tile_rows = tile_rows;
   a.max_ctx = max_ctx;
   a.num_seqs = num_seqs;
+  a.short_rows = short_rows;
+  a.short_max_c = short_max_c;
   a.status = status;
   varlen_plan_kernel<<<1, PLAN_THREADS, 0, st>>>(a);
   return cudaGetLastError();

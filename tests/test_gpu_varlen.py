@@ -182,8 +182,9 @@ def test_swa_varlen_draft_verification(dist, hq, hkv, tables):
 
 
 def test_swa_varlen_mixed_and_equal_to_single_chunks(tables):
-    # A long chunk beside decode tokens; every chunk's rows equal the
-    # single-chunk call on the same ring and rows, bit for bit.
+    # A long chunk beside decode tokens: the long chunk's rows equal the
+    # single-chunk call on the same ring and rows, bit for bit (same tiled
+    # kernel); the single tokens (short-chunk kernel) match the oracle.
     syn = Synth(3601, dist="shifted", device=DEV)
     hq, hkv = 64, 8
     sinks = syn.sinks(hq).to(DEV)
@@ -192,17 +193,32 @@ def test_swa_varlen_mixed_and_equal_to_single_chunks(tables):
     Cs = [513, 1, 1]
     ring, stage, q, cu, P0, sq = _swa_case(syn, hq, hkv, seqs, P0s, Cs, tables)
     out = kvr.swa_sink_prefill_varlen(q, cu, P0, sq, stage, ring, sinks, tables[1e4], SCALE)
-    r = 0
-    for s, p0, C in zip(seqs, P0s, Cs):
-        st = kvr.LinearLayout(stage.k[r:r + C].contiguous(), stage.v[r:r + C].contiguous())
-        one = kvr.swa_sink_prefill_chunk(q[r:r + C].contiguous(), p0, s, st, ring, sinks, tables[1e4], SCALE)
-        torch.cuda.synchronize()
-        assert torch.equal(out[r:r + C], one), f"chunk of sequence {s}"
-        r += C
+    st = kvr.LinearLayout(stage.k[:513].contiguous(), stage.v[:513].contiguous())
+    one = kvr.swa_sink_prefill_chunk(q[:513].contiguous(), 900, 2, st, ring, sinks, tables[1e4], SCALE)
+    torch.cuda.synchronize()
+    assert torch.equal(out[:513], one)
     want = _swa_want(syn, hkv, q, seqs, P0s, Cs, sinks)
     rows = list(range(0, 513, 41)) + [512, 513, 514]
     compare_rows(out[rows], want[rows], "swa varlen mixed")
     assert kvr.device_status() == 0
+
+
+@pytest.mark.parametrize("hq,hkv,Cs", [(16, 4, [8, 3, 9, 16]), (8, 8, [16, 17, 1]), (64, 8, [2, 1]),
+                                       (128, 8, [2, 3, 1])])
+def test_swa_varlen_short_chunk_limits(hq, hkv, Cs, tables):
+    # Short chunks up to 32 query rows and 16 tokens (4 heads x 8 tokens;
+    # 1 head x 16; 16 heads x 2), chunks just past either limit (4 x 9,
+    # 1 x 17, 16 x 3) that fall to the tiled kernel, and a batch of fewer
+    # than 16 rows.
+    syn = Synth(3551 + hq + len(Cs), dist="plain", device=DEV)
+    sinks = syn.sinks(hq).to(DEV)
+    seqs = list(range(len(Cs)))
+    P0s = [3000 + 77 * s for s in seqs]
+    ring, stage, q, cu, P0, sq = _swa_case(syn, hq, hkv, seqs, P0s, Cs, tables)
+    out = kvr.swa_sink_prefill_varlen(q, cu, P0, sq, stage, ring, sinks, tables[1e4], SCALE)
+    torch.cuda.synchronize()
+    assert kvr.device_status() == 0
+    compare_rows(out, _swa_want(syn, hkv, q, seqs, P0s, Cs, sinks), "swa varlen short chunks")
 
 
 # --------------------------------------------------------------------------- bad inputs, graphs
