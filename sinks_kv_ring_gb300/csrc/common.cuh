@@ -143,6 +143,7 @@ struct VarlenPlan {
   int32_t *prow_prefix;  // [n+1]
   int32_t *mode;         // [n]
   int32_t *short_list;   // [n+1]: ids of the chunks taken by the short-chunk kernel; count at [n]
+  int32_t *slen;         // [n]: keys per split of chunk s (a multiple of 128; mode[s] >= 2 only)
   float2 *pml;           // [prows][nsp_max]: (max in log2 units, sum of exponentials)
   float *po;             // [prows][nsp_max][128]: unnormalised numerators
   int n;

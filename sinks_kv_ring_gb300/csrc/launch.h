@@ -66,7 +66,7 @@ struct VarlenSizes {
   int nsp_max;
   long long prows_max;   // partial rows the workspace holds
   long long items_max;   // bound on the CTA items of any plan (the grid size)
-  size_t off_prow, off_mode, off_short, off_pml, off_po, bytes;
+  size_t off_prow, off_mode, off_short, off_slen, off_pml, off_po, bytes;
 };
 VarlenSizes varlen_sizes(int n, long long T, int hq, int hkv, long long max_ctx, int tile_rows, bool splits);
 VarlenPlan varlen_plan_view(const VarlenSizes &z, void *ws, const int32_t *cu_rows, const int64_t *P0,

@@ -107,7 +107,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 
   // ---- the work item: flat rows f0 .. f0+255 of KV head kv's group (row f is
   // position P0 + f / G, head f % G), keys k_lo .. k_hi-1
-  int kv, split = 0, nsp = 1;
+  int kv, split = 0, nsp = 1, plan_chunk = 0;
   long long f0, nrows, P0, prow = 0;
   const uint16_t *qc = a.q;  // row 0 of the chunk
   uint16_t *oc = a.out;
@@ -116,6 +116,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     const long long b = blockIdx.x;
     if (b >= a.plan.item_prefix[a.plan.n]) return;
     const int s = plan_find(a.plan.item_prefix, a.plan.n, b);
+    plan_chunk = s;
     const int local = (int)(b - a.plan.item_prefix[s]);
     const int mode = a.plan.mode[s];
     const long long c0 = a.plan.cu_rows[s];
@@ -141,9 +142,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   }
   const long long i_last = min(nrows - 1, f0 + 255) / a.G;
   long long k_lo = 0, k_hi = P0 + i_last + 1;
-  if (nsp > 1) {
-    k_lo = split * a.plan.split_len;
-    k_hi = min(k_hi, k_lo + a.plan.split_len);
+  if constexpr (VARLEN) {
+    if (nsp > 1) {
+      const long long L = a.plan.slen[plan_chunk];
+      k_lo = split * L;
+      k_hi = min(k_hi, k_lo + L);
+    }
   }
   const int ntiles = (int)((k_hi - k_lo + 127) / 128);
   const long long pmin = P0 + f0 / a.G;  // smallest row position in the CTA

@@ -59,8 +59,13 @@ __global__ void __launch_bounds__(PLAN_THREADS) varlen_plan_kernel(const PlanArg
         } else if (a.short_rows > 0 && C * a.G <= a.short_rows && C <= a.short_max_c) {
           shrt = 1;
         } else if (a.p.split_len > 0 && tiles == 1) {
-          const int nsp = (int)((P0 + C + a.p.split_len - 1) / a.p.split_len);
+          // splits of equal length (a multiple of 128) covering the P0 + C keys
+          const long long ctx = P0 + C;
+          const long long n0 = (ctx + a.p.split_len - 1) / a.p.split_len;
+          const long long L = ((ctx + n0 - 1) / n0 + 127) / 128 * 128;
+          const int nsp = (int)((ctx + L - 1) / L);
           mode = nsp;
+          a.p.slen[s] = (int)L;
           items = nsp * a.hkv;
           prows = nsp > 1 ? (int)(C * a.hq) : 0;
         } else {
@@ -165,24 +170,39 @@ VarlenSizes varlen_sizes(int n, long long T, int hq, int hkv, long long max_ctx,
   z.tile_rows = tile_rows;
   z.split_len = 0;
   z.nsp_max = 1;
+  const long long small_rows = std::min(T, (long long)n * (tile_rows / G));
   if (splits) {
-    // Aim for about eight waves of one-CTA-per-SM items when every chunk is a
-    // single query tile; splits are multiples of 128 keys, at least 1024.
-    const long long target = 8LL * num_sms();
-    long long L = ((long long)n * hkv * max_ctx + target - 1) / target;
-    L = (L + 127) / 128 * 128;
-    if (L < 1024) L = 1024;
+    // Number of key splits for chunks of one query tile, from a cost model in
+    // units of one 128-key tile on one SM (one CTA per SM): items run in
+    // waves of `sms`; an item costs a set-up of about 1.6 tiles plus its
+    // tiles; each split adds partial records (520 B written and read per row
+    // and head) spread over all SMs.  Splits are at least 512 keys.
+    const long long sms = num_sms();
+    const long long units = (long long)n * hkv;
+    const long long tiles = (max_ctx + 127) / 128;
+    const double rec_cost = (double)small_rows * hq * 1040.0 / (80.0 * 1024.0 * (double)sms);
+    int best = 1;
+    double best_cost = 1e300;
+    for (int nsp = 1; nsp <= 64 && (nsp == 1 || tiles / nsp >= 4); ++nsp) {
+      const double waves = (double)((units * nsp + sms - 1) / sms);
+      const double cost = waves * (1.6 + (double)((tiles + nsp - 1) / nsp)) + (nsp > 1 ? nsp * rec_cost : 0.0);
+      if (cost < best_cost - 1e-9) {
+        best_cost = cost;
+        best = nsp;
+      }
+    }
+    long long L = ((max_ctx + best - 1) / best + 127) / 128 * 128;
     z.split_len = L;
     z.nsp_max = (int)((max_ctx + L - 1) / L);
   }
-  const long long small_rows = std::min(T, (long long)n * (tile_rows / G));
   z.prows_max = z.nsp_max > 1 ? small_rows * hq : 0;
   const long long tiles = (T * G + tile_rows - 1) / tile_rows;
   z.items_max = (long long)hkv * (tiles + n + (long long)n * z.nsp_max);
   z.off_prow = align256(((size_t)n + 1) * 4);
   z.off_mode = z.off_prow + align256(((size_t)n + 1) * 4);
   z.off_short = z.off_mode + align256((size_t)n * 4);
-  z.off_pml = z.off_short + align256(((size_t)n + 1) * 4);
+  z.off_slen = z.off_short + align256(((size_t)n + 1) * 4);
+  z.off_pml = z.off_slen + align256((size_t)n * 4);
   const size_t recs = (size_t)z.prows_max * z.nsp_max;
   z.off_po = z.off_pml + align256(recs * 8);
   z.bytes = z.off_po + recs * DV * 4;
@@ -200,6 +220,7 @@ VarlenPlan varlen_plan_view(const VarlenSizes &z, void *ws, const int32_t *cu_ro
   p.prow_prefix = reinterpret_cast<int32_t *>(b + z.off_prow);
   p.mode = reinterpret_cast<int32_t *>(b + z.off_mode);
   p.short_list = reinterpret_cast<int32_t *>(b + z.off_short);
+  p.slen = reinterpret_cast<int32_t *>(b + z.off_slen);
   p.pml = reinterpret_cast<float2 *>(b + z.off_pml);
   p.po = reinterpret_cast<float *>(b + z.off_po);
   p.n = n;

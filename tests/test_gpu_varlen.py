@@ -65,9 +65,8 @@ def _full_want(syn, hkv, q, seqs, P0s, Cs):
 
 @pytest.mark.parametrize("hq,hkv", [(64, 4), (64, 8), (16, 4)])
 def test_full_varlen_draft_verification(hq, hkv, tables):
-    # Draft lengths 1..4; contexts around the 1024-key split boundaries,
-    # including a row whose last split holds no key it may see (P0 = 2047,
-    # C = 2: the split from 2048 on holds only the draft's second token).
+    # Draft lengths 1..4; contexts around split boundaries (about 1024 keys
+    # per split at this batch size), from a single key to ~5000.
     syn = Synth(3101 + hq + hkv, dist="shifted", device=DEV)
     seqs = [0, 1, 2, 3, 4, 5, 6]
     P0s = [0, 129, 1021, 2047, 2044, 4999, 300]
