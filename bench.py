@@ -354,7 +354,8 @@ def mtp_result(m, ms, clocks, graph_full, hbm, world):
             "ms_per_step": round(ms, 4), "verified_tokens_per_s": round(job_throughput(m.B * m.q_len, world, ms), 1),
             "full_attn_prefill_varlen": {"ms": round(ms_f, 4), "GB/s": round(gbs, 1), "hbm_frac": round(gbs / hbm, 4),
                                          "bytes": m.bytes_full(), "graph_ms": round(graph_full, 4),
-                                         "graph_GB/s": round(ggbs, 1), "graph_hbm_frac": round(ggbs / hbm, 4)},
+                                         "graph_GB/s": round(ggbs, 1), "graph_hbm_frac": round(ggbs / hbm, 4),
+                                         "traffic": kernel_traffic("full_prefill_tc_kernel_varlen")},
             "swa_sink_prefill_varlen": {"ms": round(ms_s, 5), "bytes": m.bytes_swa(),
                                         "GB/s": round(m.bytes_swa() / (ms_s / 1e3) / 1e9, 1)},
             "clocks": clocks}
@@ -721,7 +722,7 @@ def mtp_only(args, kvr, peaks_d, peaks_src, rank, world):
            "kernels": {k: v for k, v in r.items() if k.endswith("varlen")},
            "roofline": {"bound": "hbm", "achieved": kf["GB/s"], "peak": hbm, "unit": "GB/s", "frac": kf["hbm_frac"],
                         "peak_source": peaks_src, "kernel": "full_attn_prefill_varlen (plan + tensor-core kernel + merge)",
-                        "traffic": None},
+                        "traffic": kernel_traffic("full_prefill_tc_kernel_varlen")},
            "gpu_launches": m.launches_per_step * steps, "clocks": r["clocks"]}
     if rank == 0:
         print(json.dumps(res), flush=True)
