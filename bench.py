@@ -688,7 +688,7 @@ def main():
                                        "flop": pw.flops_swa()},
             "roofline": {"bound": "tensor", "achieved": round(tf_full, 1), "peak": pk, "unit": "TFLOP/s",
                          "frac": round(tf_full / pk, 4), "peak_source": peaks_src + " (sustained)",
-                         "traffic": kernel_traffic("prefill_kernel_full")},
+                         "traffic": kernel_traffic("full_prefill_tc_kernel")},
         }
         res["prefill"]["steps"] = psteps
         res["prefill"]["clocks"] = pck.summary()

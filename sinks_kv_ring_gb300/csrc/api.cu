@@ -284,8 +284,8 @@ kvr_status swa_sink_prefill_chunk(const kvr_bf16 *q, int64_t P0, int32_t C, int3
   unsigned *st = nullptr;
   cudaError_t e = status_ptr(&st);
   if (e != cudaSuccess) return cuda_fail(e, "swa_sink_prefill_chunk");
-  e = kvr::launch_swa_prefill(q, P0, C, seq, Hq, view(*chunk_kv), view(*ring), sinks, rope_cos_sin, max_pos,
-                              softmax_scale, out, st, as_stream(stream));
+  e = kvr::launch_swa_prefill_tc(q, P0, C, seq, Hq, view(*chunk_kv), view(*ring), sinks, rope_cos_sin, softmax_scale,
+                                 out, st, as_stream(stream));
   if (e != cudaSuccess) return cuda_fail(e, "swa_sink_prefill_chunk launch");
   return ok();
 }
@@ -358,7 +358,7 @@ size_t full_attn_prefill_varlen_workspace_size(int32_t n, int64_t T, int32_t Hq,
 
 size_t swa_sink_prefill_varlen_workspace_size(int32_t n) {
   if (n < 1) return 0;
-  return kvr::varlen_sizes(n, 0, 1, 1, 1, 64, false).bytes;
+  return kvr::varlen_sizes(n, 0, 1, 1, 1, 256, false).bytes;
 }
 
 kvr_status full_attn_prefill_varlen(const kvr_bf16 *q, const int32_t *cu_rows, const int64_t *P0, const int32_t *seq,
@@ -410,7 +410,7 @@ kvr_status swa_sink_prefill_varlen(const kvr_bf16 *q, const int32_t *cu_rows, co
     return fail(KVR_EINVAL, "chunk_kv has %lld rows, T = %lld", (long long)chunk_kv->num_rows, (long long)T);
   if (n == 0 || T == 0) return ok();
   if (!sinks) return fail(KVR_EINVAL, "sinks is NULL");
-  const kvr::VarlenSizes z = kvr::varlen_sizes(n, T, Hq, ring->num_kv_heads, max_pos, 64, false);
+  const kvr::VarlenSizes z = kvr::varlen_sizes(n, T, Hq, ring->num_kv_heads, max_pos, 256, false);
   if (z.items_max >= INT32_MAX)
     return fail(KVR_EUNSUPPORTED, "%s: batch too large for one call (n %d, T %lld)", who, n, (long long)T);
   if (!workspace || workspace_bytes < z.bytes)

@@ -52,11 +52,10 @@ cudaError_t launch_full_prefill(const uint16_t *q, int64_t P0, int C, int seq, i
                                 const float *table, int64_t max_pos, float softmax_scale, uint16_t *out,
                                 unsigned *status, cudaStream_t st);
 
-cudaError_t launch_swa_prefill(const uint16_t *q, int64_t P0, int C, int seq, int hq, const KvView &chunk,
-                               const KvView &ring, const float *sinks, const float *table,
-                               int64_t max_pos, float softmax_scale, uint16_t *out, unsigned *status,
-                               cudaStream_t st);
-
+// Windowed chunked prefill on the tensor cores (prefill_tc.cu).
+cudaError_t launch_swa_prefill_tc(const uint16_t *q, int64_t P0, int C, int seq, int hq, const KvView &chunk,
+                                  const KvView &ring, const float *sinks, const float *table, float softmax_scale,
+                                  uint16_t *out, unsigned *status, cudaStream_t st);
 // Sizes of the workspace of a varlen call (see VarlenPlan): n chunks, T rows,
 // contexts up to max_ctx, CTA items of tile_rows query rows; with `splits`,
 // chunks of one item are cut along the keys.
@@ -97,8 +96,10 @@ constexpr int SWA_SHORT_MAX_C = 16;  // C of a short chunk
 
 // 4-D tensor map over LINEAR rows [T][hkv][width] bf16 viewed as
 // [T][hkv][width/64][64]: one box brings box_rows consecutive tokens of one
-// KV head, every 64-element part (smem [token][part][64], 128-byte swizzle).
-bool make_tma_map_tokens4d(CUtensorMap *m, const void *ptr, long long T, int hkv, int width, int box_rows);
+// KV head, every 64-element part (smem [token][part][64], 128-byte swizzle),
+// or with one_part a single 64-element part (smem [token][64]).
+bool make_tma_map_tokens4d(CUtensorMap *m, const void *ptr, long long T, int hkv, int width, int box_rows,
+                           bool one_part = false);
 
 cudaError_t launch_ring_copy(const KvView &ring, const int32_t *seqs, int n, uint16_t *k_snap, uint16_t *v_snap,
                              int32_t *tags_snap, bool to_ring, unsigned *status, cudaStream_t st);

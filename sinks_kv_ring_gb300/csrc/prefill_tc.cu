@@ -43,7 +43,8 @@ constexpr int TC_NSLOT = 8;
 constexpr int TC_QTILE = 3 * TC_SLOT;          // 128 rows x 192 dims
 constexpr int TC_OFF_RING = 2 * TC_QTILE;      // 96 KB
 constexpr int TC_OFF_BAR = TC_OFF_RING + TC_NSLOT * TC_SLOT;  // 224 KB
-constexpr int TC_SMEM = TC_OFF_BAR + 256 + 1024;              // + barriers + alignment slack
+constexpr int TC_OFF_TAG = TC_OFF_BAR + 256;                  // windowed: the ring's 128 slot tags
+constexpr int TC_SMEM = TC_OFF_TAG + 512 + 1024;              // + alignment slack
 constexpr unsigned ST_TIMEOUT = 8u;
 constexpr float NEG_INF = -INFINITY;
 constexpr float RESCALE_THRESHOLD = 8.0f;      // log2 units
@@ -79,6 +80,10 @@ struct TcArgs {
   uint16_t *out;
   unsigned *status;
   VarlenPlan plan;       // varlen only
+  // windowed layers: ring tags, sinks, the ring row (sequence) of a single chunk
+  const int32_t *slot_pos;
+  const float *sinks;
+  int ring_seq;
 };
 
 // Rows f0 .. f0+255 (those below nrows) of KV head kv's group, written as zeros.
@@ -93,9 +98,18 @@ __device__ void zero_rows(uint16_t *oc, long long f0, long long nrows, int kv, i
 // 10 warps share 4 schedulers (3 warps on some), which caps registers at 168.
 // VARLEN: the CTA's work item comes from the plan (chunk, row tile, KV head,
 // key split); otherwise from blockIdx over one chunk.
-template <bool VARLEN>
+// WINDOW: a windowed layer.  Row i attends positions (P0 + i - 128, P0 + i]
+// with the sink in the denominator (its softmax state starts at (m, l) =
+// (sink, 1)).  Key tiles are aligned at P0: tile u >= 0 holds the chunk's
+// own rows P0 + 128u .. (tmk2 / tmv2: 4-D boxes of 128 staged tokens of one
+// KV head); tile u = -1 is the sequence's whole ring in slot order (tmk / tmv:
+// 128 ring rows), slot c holding position P0 - 128 + ((c - P0) mod 128) when
+// its tag says so.  Otherwise tmk / tmv are the paged pool and tmk2 / tmv2
+// are unused.
+template <bool VARLEN, bool WINDOW>
 __global__ void __launch_bounds__(TC_THREADS, 1)
     full_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
+                           const __grid_constant__ CUtensorMap tmk2, const __grid_constant__ CUtensorMap tmv2,
                            const TcArgs a) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -107,8 +121,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 
   // ---- the work item: flat rows f0 .. f0+255 of KV head kv's group (row f is
   // position P0 + f / G, head f % G), keys k_lo .. k_hi-1
-  int kv, split = 0, nsp = 1, plan_chunk = 0;
-  long long f0, nrows, P0, prow = 0;
+  int kv, split = 0, nsp = 1, plan_chunk = 0, rseq = a.ring_seq;
+  long long f0, nrows, P0, prow = 0, crow0 = 0;
   const uint16_t *qc = a.q;  // row 0 of the chunk
   uint16_t *oc = a.out;
   const int32_t *bt = a.bt;
@@ -132,7 +146,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     split = (local / a.hkv) % nsp;
     f0 = (long long)(local / a.hkv / nsp) * 256;
     P0 = a.plan.P0[s];
-    bt += (long long)a.plan.seq[s] * a.max_blocks;
+    crow0 = c0;
+    rseq = a.plan.seq[s];
+    if (!WINDOW) bt += (long long)rseq * a.max_blocks;
     prow = a.plan.prow_prefix[s];
   } else {
     kv = blockIdx.x % a.hkv;
@@ -149,12 +165,21 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       k_hi = min(k_hi, k_lo + L);
     }
   }
-  const int ntiles = (int)((k_hi - k_lo + 127) / 128);
   const long long pmin = P0 + f0 / a.G;  // smallest row position in the CTA
+  // Windowed: key tiles u_lo .. u_hi, aligned at P0 (u = -1: the ring).
+  int u_lo = 0;
+  if constexpr (WINDOW) {
+    u_lo = pmin - P0 >= WIN - 1 ? (int)((pmin - P0 - (WIN - 1)) / 128) : (P0 > 0 ? -1 : 0);
+    k_lo = P0 + 128LL * u_lo;  // first key of tile 0 (for the ring tile: nominal)
+  }
+  const int ntiles = WINDOW ? (int)(i_last / 128) - u_lo + 1 : (int)((k_hi - k_lo + 127) / 128);
   // query tiles with live rows (a single chunk always runs both)
   const int nq = (!VARLEN || f0 + 128 < nrows) ? 2 : 1;
 
   // ---- set-up: barriers, TMEM, rotated Q tiles
+  if constexpr (WINDOW) {
+    if (tid < WIN) reinterpret_cast<int32_t *>(gbase + TC_OFF_TAG)[tid] = a.slot_pos[(long long)rseq * WIN + tid];
+  }
   if (tid == 0) {
     for (int i = 0; i < TC_NSLOT; ++i) {
       mbar_init(sBar + B_FULL + 8 * i, 1);
@@ -175,39 +200,69 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   }
   // Q rows: CTA row r -> tile r / 128, TMEM lane r % 128; flat row f0 + r is
   // position (f0 + r) / G, head (f0 + r) % G of this KV head's group.
-  for (int it = tid; it < nq * 128 * 20; it += TC_THREADS) {
-    const int r = it / 20, c = it % 20;
+  // Byte offset of 16-byte chunk ch (0..23) of CTA row r (128-byte swizzle).
+  auto q_chunk = [&](int r, int ch) {
+    const int t = r & 127;
+    return (uint32_t)((r >> 7) * TC_QTILE + (ch >> 3) * TC_SLOT + t * 128 + (((ch & 7) ^ (t & 7)) << 4));
+  };
+  auto q_row = [&](int r, bool &live) {
     const long long f = f0 + r;
-    const bool live = f < nrows;
+    live = f < nrows;
     const long long i = live ? f / a.G : 0;
     const int g = live ? (int)(f % a.G) : 0;
-    const uint16_t *qh = qc + (i * a.hq + (long long)kv * a.G + g) * DQK;
-    const int t = r & 127;
-    uint8_t *qt = gbase + (r >> 7) * TC_QTILE;
-    auto chunk_ptr = [&](int ch) {  // 16-byte chunk ch (0..23) of row t, 128-byte swizzle
-      return reinterpret_cast<uint4 *>(qt + (ch >> 3) * TC_SLOT + t * 128 + (((ch & 7) ^ (t & 7)) << 4));
-    };
-    const uint4 zero = make_uint4(0, 0, 0, 0);
-    if (c < 4) {
-      uint4 o1 = zero, o2 = zero;
+    return qc + (i * a.hq + (long long)kv * a.G + g) * DQK;
+  };
+  // Dims 64..191 pass through: asynchronous 16-byte copies (zero-filled
+  // past the chunk), all in flight at once.
+  for (int it = tid; it < nq * 128 * 16; it += TC_THREADS) {
+    const int r = it >> 4, ch = 8 + (it & 15);
+    bool live;
+    const uint16_t *qh = q_row(r, live);
+    cp_async16(base + q_chunk(r, ch), live ? qh + ch * 8 : qc, live ? 16 : 0);
+  }
+  cp_async_commit();
+  // Dims 0..63: rotate-half with the table row of the position, four
+  // (row, chunk pair) items per thread, loads issued before any use.
+  {
+    constexpr int NB = (256 * 4 + TC_THREADS - 1) / TC_THREADS;
+    uint4 x1[NB], x2[NB];
+    float4 tv[NB][4];
+#pragma unroll
+    for (int k = 0; k < NB; ++k) {
+      const int it = tid + k * TC_THREADS;
+      const int r = it >> 2, c = it & 3;
+      bool live = false;
+      const uint16_t *qh = q_row(r < nq * 128 ? r : 0, live);
+      live = live && it < nq * 128 * 4;
+      x1[k] = x2[k] = make_uint4(0, 0, 0, 0);
+      tv[k][0] = tv[k][1] = tv[k][2] = tv[k][3] = make_float4(0.f, 0.f, 0.f, 0.f);
       if (live) {
-        const float4 *tr = reinterpret_cast<const float4 *>(a.table + (P0 + i) * 64 + 16 * c);
+        const uint4 *s4 = reinterpret_cast<const uint4 *>(qh);
+        x1[k] = s4[c];
+        x2[k] = s4[c + 4];
+        const float4 *tr = reinterpret_cast<const float4 *>(a.table + (P0 + (f0 + r) / a.G) * 64 + 16 * c);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) tv[k][u] = tr[u];
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < NB; ++k) {
+      const int it = tid + k * TC_THREADS;
+      if (it < nq * 128 * 4) {
+        const int r = it >> 2, c = it & 3;
         float cs[16];
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-          const float4 fv = tr[u];
-          cs[4 * u] = fv.x; cs[4 * u + 1] = fv.y; cs[4 * u + 2] = fv.z; cs[4 * u + 3] = fv.w;
+          cs[4 * u] = tv[k][u].x; cs[4 * u + 1] = tv[k][u].y; cs[4 * u + 2] = tv[k][u].z; cs[4 * u + 3] = tv[k][u].w;
         }
-        const uint4 *s4 = reinterpret_cast<const uint4 *>(qh);
-        rope_pair8(s4[c], s4[c + 4], cs, o1, o2);
+        uint4 o1, o2;
+        rope_pair8(x1[k], x2[k], cs, o1, o2);  // zero in, zero out for rows past the chunk
+        *reinterpret_cast<uint4 *>(gbase + q_chunk(r, c)) = o1;
+        *reinterpret_cast<uint4 *>(gbase + q_chunk(r, c + 4)) = o2;
       }
-      *chunk_ptr(c) = o1;
-      *chunk_ptr(c + 4) = o2;
-    } else {
-      const int ch = c + 4;
-      *chunk_ptr(ch) = live ? reinterpret_cast<const uint4 *>(qh)[ch] : zero;
     }
   }
+  cp_async_wait<0>();
   fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
@@ -238,22 +293,33 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       }
       return y;
     };
-    int y_next = box_row(0);
+    int y_next = WINDOW ? 0 : box_row(0);
     long long L = 0;
     bool ok = true;
+    const int ring_row = (rseq * a.hkv + kv) * WIN;  // windowed: the (sequence, KV head) ring
     for (int t = 0; t < ntiles && ok; ++t) {
       const int y_cur = y_next;
-      if (t + 1 < ntiles) y_next = box_row(t + 1);
+      if (!WINDOW && t + 1 < ntiles) y_next = box_row(t + 1);
+      const int u = u_lo + t;
       for (int part = 0; part < 5; ++part, ++L) {
         const int slot = (int)(L % TC_NSLOT);
         const uint32_t round = (uint32_t)(L / TC_NSLOT);
         if (!warp_wait(sBar + B_EMPTY + 8 * slot, (round & 1u) ^ 1u, abort_flag)) { ok = false; break; }
         const uint32_t full = sBar + B_FULL + 8 * slot;
         mbar_expect_tx_elect(full, TC_SLOT);
-        const void *map = part < 3 ? (const void *)&tmk : (const void *)&tmv;
-        const int x = 64 * (part < 3 ? part : part - 3);
-        for (int b = 0; b < nb; ++b)
-          tma_load_2d_elect(sRing + slot * TC_SLOT + b * rb * 128, map, x, __shfl_sync(0xffffffffu, y_cur, b), full);
+        const int pi = part < 3 ? part : part - 3;
+        if (WINDOW && u >= 0) {
+          const void *map = part < 3 ? (const void *)&tmk2 : (const void *)&tmv2;
+          tma_load_4d_elect(sRing + slot * TC_SLOT, map, 0, pi, kv, (int)(crow0 + 128LL * u), full);
+        } else if (WINDOW) {
+          const void *map = part < 3 ? (const void *)&tmk : (const void *)&tmv;
+          tma_load_2d_elect(sRing + slot * TC_SLOT, map, 64 * pi, ring_row, full);
+        } else {
+          const void *map = part < 3 ? (const void *)&tmk : (const void *)&tmv;
+          for (int b = 0; b < nb; ++b)
+            tma_load_2d_elect(sRing + slot * TC_SLOT + b * rb * 128, map, 64 * pi, __shfl_sync(0xffffffffu, y_cur, b),
+                              full);
+        }
       }
     }
     // On an abort, let the loads already issued land before the CTA exits
@@ -306,6 +372,20 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       const long long L0 = 5LL * t + 3;
       for (int db = 0; db < 2; ++db) {
         if (!wait_full(L0 + db)) { ok = false; return; }
+        if (WINDOW && i == 0 && u_lo + t < 0) {
+          // The ring tile: V rows of slots that hold no position of the
+          // window may be stale or never written; zero them before the product.
+          const int32_t *tg = reinterpret_cast<const int32_t *>(gbase + TC_OFF_TAG);
+          uint4 *g = reinterpret_cast<uint4 *>(gbase + TC_OFF_RING + slot_of(L0 + db) * TC_SLOT);
+          const int pm = (int)(P0 & (WIN - 1));
+          for (int e = lane; e < 128 * 8; e += 32) {
+            const int c = e >> 3;
+            const long long pos = P0 - WIN + ((c - pm) & (WIN - 1));
+            if (pos < 0 || tg[c] != (int32_t)pos) g[e] = make_uint4(0, 0, 0, 0);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+        }
         if (i == 0 && t == ntiles - 1 && k_lo + 128LL * t + 128 > k_hi) {
           // Rows past the last key may hold stale bytes of the page; P is 0
           // there, but 0 * NaN is not, so zero them before the product.
@@ -375,6 +455,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     const int g = (int)(fc % a.G);
     const float sl2 = a.scale_log2;
     float m_ref = NEG_INF, l = 0.f;
+    if constexpr (WINDOW) {  // the sink starts the softmax: e^{sink - m} = 1 in the denominator
+      m_ref = a.sinks[kv * a.G + g] * LOG2E;
+      l = 1.f;
+    }
     bool ok = wg < nq;
     for (int t = 0; t < ntiles && ok; ++t) {
       if (!warp_wait(sBar + B_SFULL + 8 * wg, (uint32_t)t & 1u, abort_flag)) { ok = false; break; }
@@ -384,7 +468,28 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       for (int c = 0; c < 4; ++c) tmem_ld32(tS + 32 * c, s[c]);
       tmem_wait_ld();
       const long long j0 = k_lo + 128LL * t;
-      if (j0 + 127 > pmin) {  // the diagonal (and the end of the keys) is in this tile
+      if constexpr (WINDOW) {
+        if (u_lo + t < 0) {  // the ring: slot c holds position P0 - 128 + ((c - P0) mod 128) if its tag agrees
+          const int32_t *tg = reinterpret_cast<const int32_t *>(gbase + TC_OFF_TAG);
+          const int pm = (int)(P0 & (WIN - 1));
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+              const int col = 32 * c + e;
+              const long long pos = P0 - WIN + ((col - pm) & (WIN - 1));
+              if (pos < 0 || tg[col] != (int32_t)pos || pos <= pr - WIN || pos > pr) s[c][e] = __float_as_uint(NEG_INF);
+            }
+        } else {
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+              const long long pos = j0 + 32 * c + e;
+              if (pos <= pr - WIN || pos > pr) s[c][e] = __float_as_uint(NEG_INF);
+            }
+        }
+      } else if (j0 + 127 > pmin) {  // the diagonal (and the end of the keys) is in this tile
 #pragma unroll
         for (int c = 0; c < 4; ++c)
 #pragma unroll
@@ -537,14 +642,14 @@ cudaError_t launch_full_prefill(const uint16_t *q, int64_t P0, int C, int seq, i
   TcArgs a;
   cudaError_t e = tc_setup(pool, hq, table, softmax_scale, out, status, &mk, &mv, &a);
   if (e != cudaSuccess) return e;
-  e = ensure_smem_limit(2, (const void *)full_prefill_tc_kernel<false>, TC_SMEM);
+  e = ensure_smem_limit(2, (const void *)full_prefill_tc_kernel<false, false>, TC_SMEM);
   if (e != cudaSuccess) return e;
   a.q = q;
   a.P0 = P0;
   a.C = C;
   a.bt = pool.block_table + (long long)seq * pool.max_blocks;
   const long long ctas = ((long long)C * a.G + 255) / 256 * a.hkv;
-  full_prefill_tc_kernel<false><<<(unsigned)ctas, TC_THREADS, TC_SMEM, st>>>(mk, mv, a);
+  full_prefill_tc_kernel<false, false><<<(unsigned)ctas, TC_THREADS, TC_SMEM, st>>>(mk, mv, mk, mv, a);
   return cudaGetLastError();
 }
 
@@ -556,17 +661,90 @@ cudaError_t launch_full_varlen(const uint16_t *q, const int32_t *cu_rows, const 
   TcArgs a;
   cudaError_t e = tc_setup(pool, hq, table, softmax_scale, out, status, &mk, &mv, &a);
   if (e != cudaSuccess) return e;
-  e = ensure_smem_limit(4, (const void *)full_prefill_tc_kernel<true>, TC_SMEM);
+  e = ensure_smem_limit(4, (const void *)full_prefill_tc_kernel<true, false>, TC_SMEM);
   if (e != cudaSuccess) return e;
   const VarlenSizes z = varlen_sizes(n, T, hq, pool.hkv, max_ctx, 256, true);
   a.q = q;
   a.plan = varlen_plan_view(z, ws, cu_rows, P0, seq, n);
   e = launch_varlen_plan(a.plan, T, hq, pool.hkv, 256, max_ctx, pool.num_seqs, 0, 0, status, st);
   if (e != cudaSuccess) return e;
-  full_prefill_tc_kernel<true><<<(unsigned)z.items_max, TC_THREADS, TC_SMEM, st>>>(mk, mv, a);
+  full_prefill_tc_kernel<true, false><<<(unsigned)z.items_max, TC_THREADS, TC_SMEM, st>>>(mk, mv, mk, mv, a);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   return launch_varlen_combine(a.plan, z.prows_max, hq, out, st);
+}
+
+namespace {
+
+// Tensor maps of a windowed layer: the ring (128-row boxes of one 64-dim
+// part) and the staged chunk rows (4-D boxes of 128 tokens of one KV head,
+// one part), and the common arguments.
+cudaError_t tc_window_setup(const KvView &chunk, long long T, const KvView &ring, int hq, const float *sinks,
+                            const float *table, float softmax_scale, uint16_t *out, unsigned *status, CUtensorMap *m,
+                            TcArgs *a) {
+  const int hkv = ring.hkv;
+  const long long rows = (long long)ring.num_seqs * hkv * WIN;
+  if (rows >= (1LL << 31) || T >= (1LL << 31)) return cudaErrorInvalidValue;
+  if (!make_tma_map_2d(&m[0], ring.k, rows, DQK, 128) || !make_tma_map_2d(&m[1], ring.v, rows, DV, 128) ||
+      !make_tma_map_tokens4d(&m[2], chunk.k, T, hkv, DQK, 128, true) ||
+      !make_tma_map_tokens4d(&m[3], chunk.v, T, hkv, DV, 128, true))
+    return cudaErrorInvalidValue;
+  *a = TcArgs{};
+  a->hq = hq;
+  a->G = hq / hkv;
+  a->hkv = hkv;
+  a->table = table;
+  a->scale_log2 = softmax_scale * LOG2E;
+  a->out = out;
+  a->status = status;
+  a->slot_pos = ring.slot_pos;
+  a->sinks = sinks;
+  return cudaSuccess;
+}
+
+}  // namespace
+
+cudaError_t launch_swa_prefill_tc(const uint16_t *q, int64_t P0, int C, int seq, int hq, const KvView &chunk,
+                                  const KvView &ring, const float *sinks, const float *table, float softmax_scale,
+                                  uint16_t *out, unsigned *status, cudaStream_t st) {
+  CUtensorMap m[4];
+  TcArgs a;
+  cudaError_t e = tc_window_setup(chunk, C, ring, hq, sinks, table, softmax_scale, out, status, m, &a);
+  if (e != cudaSuccess) return e;
+  e = ensure_smem_limit(7, (const void *)full_prefill_tc_kernel<false, true>, TC_SMEM);
+  if (e != cudaSuccess) return e;
+  a.q = q;
+  a.P0 = P0;
+  a.C = C;
+  a.ring_seq = seq;
+  const long long ctas = ((long long)C * a.G + 255) / 256 * a.hkv;
+  full_prefill_tc_kernel<false, true><<<(unsigned)ctas, TC_THREADS, TC_SMEM, st>>>(m[0], m[1], m[2], m[3], a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_swa_varlen(const uint16_t *q, const int32_t *cu_rows, const int64_t *P0, const int32_t *seq,
+                              int n, long long T, int hq, const KvView &chunk, const KvView &ring,
+                              const float *sinks, const float *table, int64_t max_pos, float softmax_scale,
+                              void *ws, uint16_t *out, unsigned *status, cudaStream_t st) {
+  const int hkv = ring.hkv;
+  CUtensorMap m[4];
+  TcArgs a;
+  cudaError_t e = tc_window_setup(chunk, T, ring, hq, sinks, table, softmax_scale, out, status, m, &a);
+  if (e != cudaSuccess) return e;
+  e = ensure_smem_limit(8, (const void *)full_prefill_tc_kernel<true, true>, TC_SMEM);
+  if (e != cudaSuccess) return e;
+  const VarlenSizes z = varlen_sizes(n, T, hq, hkv, max_pos, 256, false);
+  a.q = q;
+  a.plan = varlen_plan_view(z, ws, cu_rows, P0, seq, n);
+  e = launch_varlen_plan(a.plan, T, hq, hkv, 256, max_pos, ring.num_seqs, SWA_SHORT_ROWS, SWA_SHORT_MAX_C, status,
+                         st);
+  if (e != cudaSuccess) return e;
+  // Chunks of more than 32 query rows are tiled here; the short ones go to
+  // the short-chunk kernel.
+  full_prefill_tc_kernel<true, true><<<(unsigned)z.items_max, TC_THREADS, TC_SMEM, st>>>(m[0], m[1], m[2], m[3], a);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  return launch_swa_short(q, a.plan, n, T, hq, chunk, ring, sinks, table, softmax_scale, out, status, st);
 }
 
 }  // namespace kvr

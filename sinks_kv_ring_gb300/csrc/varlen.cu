@@ -197,7 +197,8 @@ VarlenSizes varlen_sizes(int n, long long T, int hq, int hkv, long long max_ctx,
   }
   z.prows_max = z.nsp_max > 1 ? small_rows * hq : 0;
   const long long tiles = (T * G + tile_rows - 1) / tile_rows;
-  z.items_max = (long long)hkv * (tiles + n + (long long)n * z.nsp_max);
+  // tiles: at most one partial tile per chunk; splits: only chunks of one tile
+  z.items_max = (long long)hkv * (tiles + n + (splits ? (long long)n * z.nsp_max : 0));
   z.off_prow = align256(((size_t)n + 1) * 4);
   z.off_mode = z.off_prow + align256(((size_t)n + 1) * 4);
   z.off_short = z.off_mode + align256((size_t)n * 4);
