@@ -12,6 +12,7 @@ The line also carries "mtp": the same batch verifying a 4-token draft per
 sequence (multi-token prediction) through the varlen calls.
 
 Other workloads: prefill, long_decode (batch 16 at 524288 tokens), mtp_decode,
+pro_true (pro_mixed with the Pro's own head counts: 128 q heads, 8 KV heads on both kinds),
 pro_mixed (128 ragged sequences through a 70-layer stack, 10 full : 60
 windowed), tiny (1 sequence, 512 tokens).
 
@@ -579,7 +580,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="flash_decode",
-                    choices=["flash_decode", "long_decode", "prefill", "pro_mixed", "mtp_decode"])
+                    choices=["flash_decode", "long_decode", "prefill", "pro_mixed", "pro_true", "mtp_decode"])
     ap.add_argument("--mtp-len", type=int, default=4, help="draft tokens verified per sequence (mtp_decode)")
     ap.add_argument("--no-prefill", action="store_true", help="skip the prefill sub-measurement")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -619,7 +620,7 @@ def main():
     peaks_d, peaks_src = peaks()
     if args.workload == "prefill":
         return prefill_only(args, kvr, peaks_d, peaks_src, rank, world)
-    if args.workload == "pro_mixed":
+    if args.workload in ("pro_mixed", "pro_true"):
         return pro_mixed(args, kvr, peaks_d, peaks_src, rank, world)
     if args.workload == "mtp_decode":
         return mtp_only(args, kvr, peaks_d, peaks_src, rank, world)
@@ -766,10 +767,11 @@ class ProMixedWorkload:
     (layer l -> pool l mod n_pools; every pool is far larger than L2, so each
     layer still streams its full bytes from HBM)."""
 
-    def __init__(self, kvr, B=128, hq=64, layers=70, vscale=0.612, seed=1004, n_pools=None, device="cuda"):
+    def __init__(self, kvr, B=128, hq=64, layers=70, vscale=0.612, seed=1004, n_pools=None, device="cuda",
+                 hkv_full=4, hkv_swa=8):
         from sinks_kv_ring_gb300.synth import Synth, ragged_contexts
         self.kvr, self.B, self.hq, self.vscale = kvr, B, hq, vscale
-        self.hkv_full, self.hkv_swa = 4, 8
+        self.hkv_full, self.hkv_swa = hkv_full, hkv_swa
         dev = device
         self.ctx = ragged_contexts(B, 1024, 1 << 20, seed)        # cached tokens per sequence
         self.max_ctx = max(self.ctx) + 1
@@ -809,8 +811,8 @@ class ProMixedWorkload:
         self.pos = torch.tensor(self.ctx, dtype=torch.int64, device=dev)   # the new token's position
         self.seq = torch.arange(B, dtype=torch.int32, device=dev)
         self.q = syn_s.q(B, hq, self.hkv_swa, seq=50_000)
-        self.k_new = {h: syn_s.k(B, h, seq=60_000) for h in (4, 8)}
-        self.v_new = {h: syn_s.v(B, h, seq=60_000) for h in (4, 8)}
+        self.k_new = {h: syn_s.k(B, h, seq=60_000) for h in {hkv_full, hkv_swa}}
+        self.v_new = {h: syn_s.v(B, h, seq=60_000) for h in {hkv_full, hkv_swa}}
         self.sinks = syn_s.sinks(hq).to(dev)
         self.ws = torch.empty(kvr.full_attn_decode_workspace_size(B, hq, self.hkv_full, self.max_ctx),
                               dtype=torch.uint8, device=dev)
@@ -838,15 +840,15 @@ class ProMixedWorkload:
             if kind == "full":
                 pool = self.pools[fi % self.n_pools]
                 fi += 1
-                kvr.kv_ring_append_rope(self.k_new[4], self.v_new[4], self.pos, self.seq, self.t7, self.vscale, pool,
-                                        stream=stream)
+                kvr.kv_ring_append_rope(self.k_new[self.hkv_full], self.v_new[self.hkv_full], self.pos, self.seq,
+                                        self.t7, self.vscale, pool, stream=stream)
                 kvr.full_attn_decode(self.q, self.pos, self.seq, pool, self.t7, SCALE, self.max_ctx,
                                      workspace=self.ws, out=self.out, stream=stream)
             else:
                 ring = self.rings[si]
                 si += 1
-                kvr.kv_ring_append_rope(self.k_new[8], self.v_new[8], self.pos, self.seq, self.t4, self.vscale, ring,
-                                        stream=stream)
+                kvr.kv_ring_append_rope(self.k_new[self.hkv_swa], self.v_new[self.hkv_swa], self.pos, self.seq,
+                                        self.t4, self.vscale, ring, stream=stream)
                 kvr.swa_sink_decode(self.q, self.pos, self.seq, ring, self.sinks, self.t4, SCALE, out=self.out,
                                     stream=stream)
 
@@ -867,7 +869,11 @@ class ProMixedWorkload:
 
 
 def pro_mixed(args, kvr, peaks_d, peaks_src, rank, world):
-    work = ProMixedWorkload(kvr, seed=rank_seed(1004, rank))
+    true_heads = args.workload == "pro_true"
+    if true_heads:   # the head counts the pages imply for the real Pro: 128 q heads, 8 KV heads on both kinds
+        work = ProMixedWorkload(kvr, hq=128, hkv_full=8, hkv_swa=8, seed=rank_seed(1004, rank))
+    else:
+        work = ProMixedWorkload(kvr, seed=rank_seed(1004, rank))
     work.capture()
     stream = torch.cuda.current_stream()
     steps = args.steps if "--steps" in sys.argv else 20
@@ -879,9 +885,10 @@ def pro_mixed(args, kvr, peaks_d, peaks_src, rank, world):
     res = {"metric": METRIC, "value": round(job_throughput(work.B, world, ms), 1), "unit": "tokens/s",
            "n_gpus": world, "steps": steps, "warmup": args.warmup, "ms_per_step": round(ms, 3),
            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-           "config": {"workload": "pro_mixed: 128 sequences, contexts log-uniform 1K-1M (seed 1004); 70 layers "
-                                  "(i % 7 == 6 full: 10 full, 60 windowed); 64 q heads, windowed 8 KV heads, full 4 "
-                                  "KV heads; value scale 0.612; one decode step as one CUDA graph",
+           "config": {"workload": f"{args.workload}: 128 sequences, contexts log-uniform 1K-1M (seed 1004); 70 layers "
+                                  f"(i % 7 == 6 full: 10 full, 60 windowed); {work.hq} q heads, windowed "
+                                  f"{work.hkv_swa} KV heads, full {work.hkv_full} KV heads; value scale 0.612; one "
+                                  "decode step as one CUDA graph",
                       "global_batch": work.B * world, "seq_len": work.max_ctx, "parallelism": f"dp{world}",
                       "buckets": work.buckets(), "distinct_full_pools": work.n_pools,
                       "total_context_tokens": int(sum(work.ctx)),
