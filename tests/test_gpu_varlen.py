@@ -220,6 +220,61 @@ def test_swa_varlen_short_chunk_limits(hq, hkv, Cs, tables):
     compare_rows(out, _swa_want(syn, hkv, q, seqs, P0s, Cs, sinks), "swa varlen short chunks")
 
 
+def test_varlen_plan_more_than_1024_chunks(tables):
+    # 2500 chunks (the plan scans 1024 at a time with a carried prefix): a
+    # mix of single tokens, drafts of 2-3 tokens and empty chunks over 40
+    # sequences; every 97th chunk and the last ones checked, both kinds.
+    syn = Synth(3901, dist="plain", device=DEV)
+    hq, hkv_f, hkv_s = 16, 4, 8
+    rng = np.random.default_rng(3901)
+    n, ns = 2500, 40
+    Cs = [int(c) for c in rng.choice([0, 1, 1, 2, 3], size=n)]
+    seqs = [int(x) for x in rng.integers(0, ns, size=n)]
+    P0s = [int(x) for x in rng.integers(0, 3000, size=n)]
+    T = sum(Cs)
+    # full layer: every sequence's pool holds positions 0..2999 + 3 (drafts
+    # of different chunks of one sequence read the same pool rows)
+    pool = kvr.PagedLayout.contiguous(ns, hkv_f, 3003, block_size=128)
+    fill_paged(pool, syn, list(range(ns)), [3003] * ns, tables[1e7], VS)
+    q, cu, P0, sq = _batch(syn, hq, hkv_f, seqs, P0s, Cs)
+    out = kvr.full_attn_prefill_varlen(q, cu, P0, sq, pool, tables[1e7], SCALE, 3003)
+    torch.cuda.synchronize()
+    assert kvr.device_status() == 0
+    starts = np.concatenate([[0], np.cumsum(Cs)])
+    pick = [i for i in range(0, n, 97) if Cs[i]] + [i for i in range(n - 5, n) if Cs[i]]
+    for i in pick:
+        k, v = raw_kv(syn, hkv_f, seqs[i], 0, P0s[i] + Cs[i])
+        r = slice(int(starts[i]), int(starts[i + 1]))
+        want = oracle.attend_seq(q[r], np.arange(P0s[i], P0s[i] + Cs[i]), k, v, 0, 1e7, VS, SCALE, 0, None)
+        compare_rows(out[r], want, f"full chunk {i}")
+    # windowed layer: one ring per sequence holding positions 2872..2999;
+    # every chunk verifies its tokens at 3000.. (chunks of one sequence share
+    # that ring state and read their own staged rows)
+    sinks = syn.sinks(hq).to(DEV)
+    P0w = [3000] * n
+    ring = kvr.RingLayout.empty(ns, hkv_s)
+    fill_ring(ring, syn, list(range(ns)), [2999] * ns, tables[1e4], VS)
+    ks, vs, ps = [], [], []
+    for s_, C in zip(seqs, Cs):
+        k, v = raw_kv(syn, hkv_s, s_, 3000, 3000 + C)
+        ks.append(k)
+        vs.append(v)
+        ps.append(torch.arange(3000, 3000 + C, dtype=torch.int64, device=DEV))
+    stage = kvr.LinearLayout.empty(T, hkv_s)
+    kvr.kv_ring_append_rope(torch.cat(ks).contiguous(), torch.cat(vs).contiguous(), torch.cat(ps), None, tables[1e4],
+                            VS, stage)
+    qw, cuw, P0wt, sqw = _batch(syn, hq, hkv_s, seqs, P0w, Cs)
+    outw = kvr.swa_sink_prefill_varlen(qw, cuw, P0wt, sqw, stage, ring, sinks, tables[1e4], SCALE)
+    torch.cuda.synchronize()
+    assert kvr.device_status() == 0
+    for i in pick:
+        k, v = raw_kv(syn, hkv_s, seqs[i], 2873, 3000 + Cs[i])
+        r = slice(int(starts[i]), int(starts[i + 1]))
+        want = oracle.attend_seq(qw[r], np.arange(3000, 3000 + Cs[i]), k, v, 2873, 1e4, VS, SCALE, 128,
+                                 sinks.double().cpu().numpy())
+        compare_rows(outw[r], want, f"swa chunk {i}")
+
+
 # --------------------------------------------------------------------------- bad inputs, graphs
 
 def test_varlen_bad_device_inputs_are_flagged(tables):
