@@ -667,6 +667,7 @@ def main():
         res["cpu_baseline"] = cpu_baseline_decode(work, max_seqs=16 if args.workload == "flash_decode" else 2)
     if args.workload == "flash_decode":
         m, mms, mck, mg = run_mtp(work, min(20, args.steps), 3)
+        mms = max_over_ranks([mms], world, "cuda")[0]
         res["mtp"] = mtp_result(m, mms, mck, mg, hbm, world)
         res["gpu_launches"] += m.launches_per_step * min(20, args.steps)
         del m
@@ -676,6 +677,7 @@ def main():
         psteps = min(5, args.steps)
         with Clocks(torch.cuda.current_device()) as pck:
             pw, pms = run_prefill(kvr, psteps, 3)
+        pms = max_over_ranks([pms], world, "cuda")[0]
         tf_full = pw.flops_full() / (pw.t_full.mean_ms() / 1e3) / 1e12
         tf_swa = pw.flops_swa() / (pw.t_swa.mean_ms() / 1e3) / 1e12
         pk = peaks_d.get("bf16_tflops_sustained", peaks_d["bf16_tflops"])
