@@ -355,8 +355,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       const uint32_t d = tmem + 128 * i;
       for (int kb = 0; kb < 3; ++kb) {
         const long long L = 5LL * t + kb;
-        if (!wait_full(L)) { ok = false; return; }
-        tc_fence_after();
+        if (i == 0) {  // query tile 1 reads the same slots right after tile 0
+          if (!wait_full(L)) { ok = false; return; }
+          tc_fence_after();
+        }
         const uint64_t a0 = dq + (uint64_t)((kb * TC_SLOT) >> 4);
         const uint64_t b0 = dring_k + (uint64_t)((slot_of(L) * TC_SLOT) >> 4);
 #pragma unroll
@@ -370,7 +372,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     auto issue_PV = [&](int i, int t, bool release) {
       if (!warp_wait(sBar + B_PREADY + 8 * i, (uint32_t)t & 1u, abort_flag)) { ok = false; return; }
       const long long L0 = 5LL * t + 3;
-      for (int db = 0; db < 2; ++db) {
+      for (int db = 0; db < 2 && i == 0; ++db) {  // tile 1: waited for by tile 0
         if (!wait_full(L0 + db)) { ok = false; return; }
         if (WINDOW && i == 0 && u_lo + t < 0) {
           // The ring tile: V rows of slots that hold no position of the
@@ -503,7 +505,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 #pragma unroll
       for (int c = 0; c < 4; ++c)
 #pragma unroll
-        for (int e = 0; e < 32; ++e) mxv[e & 7] = fmaxf(mxv[e & 7], __uint_as_float(s[c][e]));
+        for (int e = 0; e < 32; e += 2)
+          mxv[(e >> 1) & 7] = fmax3(mxv[(e >> 1) & 7], __uint_as_float(s[c][e]), __uint_as_float(s[c][e + 1]));
       const float mx = fmaxf(fmaxf(fmaxf(mxv[0], mxv[1]), fmaxf(mxv[2], mxv[3])),
                              fmaxf(fmaxf(mxv[4], mxv[5]), fmaxf(mxv[6], mxv[7])));
       const float m_new = fmaxf(m_ref, mx * sl2);
@@ -517,18 +520,25 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         resc = true;
       }
       const float b = m_ref == NEG_INF ? 0.f : m_ref;
-      float sumv[4] = {0.f, 0.f, 0.f, 0.f};
+      // p = 2^(s * scale - b), two elements per packed FMA; row sums in
+      // four packed accumulators
+      uint64_t sumv[4] = {0, 0, 0, 0};  // (+0.0f, +0.0f) pairs
       uint32_t pk[2][32];
+      const uint64_t sl2v = f32x2(sl2, sl2), nbv = f32x2(-b, -b);
 #pragma unroll
       for (int c = 0; c < 4; ++c)
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
-          const float p0 = ex2(fmaf(__uint_as_float(s[c][e]), sl2, -b));
-          const float p1 = ex2(fmaf(__uint_as_float(s[c][e + 1]), sl2, -b));
-          sumv[(e >> 1) & 3] += p0 + p1;
+          float a0, a1;
+          f32x2_split(fma_f32x2(f32x2(__uint_as_float(s[c][e]), __uint_as_float(s[c][e + 1])), sl2v, nbv), a0, a1);
+          const float p0 = ex2(a0), p1 = ex2(a1);
+          sumv[(e >> 1) & 3] = add_f32x2(sumv[(e >> 1) & 3], f32x2(p0, p1));
           pk[c >> 1][(c & 1) * 16 + e / 2] = pack_bf16(p0, p1);
         }
-      l = l * factor + ((sumv[0] + sumv[1]) + (sumv[2] + sumv[3]));
+      float su[8];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) f32x2_split(sumv[u], su[2 * u], su[2 * u + 1]);
+      l = l * factor + (((su[0] + su[1]) + (su[2] + su[3])) + ((su[4] + su[5]) + (su[6] + su[7])));
       tmem_st32(tS, pk[0]);
       tmem_st32(tS + 32, pk[1]);
       if (__any_sync(0xffffffffu, resc)) {
