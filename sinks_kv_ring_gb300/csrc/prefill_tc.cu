@@ -50,7 +50,7 @@ constexpr float NEG_INF = -INFINITY;
 constexpr float RESCALE_THRESHOLD = 8.0f;      // log2 units
 
 // barrier area layout (byte offsets)
-constexpr int B_FULL = 0;       // [8]
+constexpr int B_FULL = 0;       // [4]: K loads (0, 1) / V loads (2, 3) of key tile t landed, t % 2
 constexpr int B_EMPTY = 64;     // [8]
 constexpr int B_SFULL = 128;    // [2]
 constexpr int B_PREADY = 144;   // [2]
@@ -181,10 +181,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     if (tid < WIN) reinterpret_cast<int32_t *>(gbase + TC_OFF_TAG)[tid] = a.slot_pos[(long long)rseq * WIN + tid];
   }
   if (tid == 0) {
-    for (int i = 0; i < TC_NSLOT; ++i) {
-      mbar_init(sBar + B_FULL + 8 * i, 1);
-      mbar_init(sBar + B_EMPTY + 8 * i, 1);
-    }
+    for (int i = 0; i < TC_NSLOT; ++i) mbar_init(sBar + B_EMPTY + 8 * i, 1);
+    for (int i = 0; i < 4; ++i) mbar_init(sBar + B_FULL + 8 * i, 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(sBar + B_SFULL + 8 * i, 1);
       mbar_init(sBar + B_PREADY + 8 * i, 128);
@@ -301,12 +299,18 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       const int y_cur = y_next;
       if (!WINDOW && t + 1 < ntiles) y_next = box_row(t + 1);
       const int u = u_lo + t;
+      // Two transaction barriers per key tile (each double-buffered): its
+      // three K loads and its two V loads.  A barrier's arrive + byte count
+      // goes out once the first slot of its part is free; that slot was freed
+      // by products issued after the wait on the same barrier for tile t-2,
+      // so that phase is over.
       for (int part = 0; part < 5; ++part, ++L) {
         const int slot = (int)(L % TC_NSLOT);
         const uint32_t round = (uint32_t)(L / TC_NSLOT);
         if (!warp_wait(sBar + B_EMPTY + 8 * slot, (round & 1u) ^ 1u, abort_flag)) { ok = false; break; }
-        const uint32_t full = sBar + B_FULL + 8 * slot;
-        mbar_expect_tx_elect(full, TC_SLOT);
+        const uint32_t full = sBar + B_FULL + 8 * ((part < 3 ? 0 : 2) + (t & 1));
+        if (part == 0) mbar_expect_tx_elect(full, 3 * TC_SLOT);
+        if (part == 3) mbar_expect_tx_elect(full, 2 * TC_SLOT);
         const int pi = part < 3 ? part : part - 3;
         if (WINDOW && u >= 0) {
           const void *map = part < 3 ? (const void *)&tmk2 : (const void *)&tmv2;
@@ -324,12 +328,15 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     }
     // On an abort, let the loads already issued land before the CTA exits
     // (bounded by time only: the abort flag is already set).
-    if (lane == 0) {
+    if (lane == 0 && L > 0) {
       volatile uint32_t local = 0;
-      for (long long M = L - 1; M >= 0 && M >= L - TC_NSLOT; --M) {
-        const int slot = (int)(M % TC_NSLOT);
-        local = 0;
-        mbar_wait(sBar + B_FULL + 8 * slot, (uint32_t)(M / TC_NSLOT) & 1u, &local, 1000000000ull);
+      const long long tl = (L - 1) / 5;  // the last tile with a load issued, and the one before
+      for (long long t = tl; t >= 0 && t >= tl - 1; --t) {
+        for (int h = 0; h < 2; ++h) {
+          if (h == 1 && 5 * t + 3 >= L) continue;  // its V loads were never issued
+          local = 0;
+          mbar_wait(sBar + B_FULL + 8 * (2 * h + (t & 1)), (uint32_t)(t >> 1) & 1u, &local, 1000000000ull);
+        }
       }
     }
     __syncwarp();
@@ -346,19 +353,22 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     const uint64_t dring_v = sdesc_sw128(sRing, TC_SLOT, 1024);  // LBO = next slot (the other value half)
     bool ok = true;
     auto slot_of = [](long long L) { return (uint32_t)(L % TC_NSLOT); };
-    auto wait_full = [&](long long L) {
-      return warp_wait(sBar + B_FULL + 8 * slot_of(L), (uint32_t)(L / TC_NSLOT) & 1u, abort_flag);
+    auto wait_k = [&](int t) {  // the three K loads of key tile t
+      return warp_wait(sBar + B_FULL + 8 * (t & 1), (uint32_t)(t >> 1) & 1u, abort_flag);
+    };
+    auto wait_v = [&](int t) {  // the two V loads of key tile t
+      return warp_wait(sBar + B_FULL + 8 * (2 + (t & 1)), (uint32_t)(t >> 1) & 1u, abort_flag);
     };
     // S_i = Q_i K(t)^T : 12 MMAs of K = 16 over three 64-dim slots.
     auto issue_S = [&](int i, int t, bool release) {
       const uint64_t dq = i ? dq1 : dq0;
       const uint32_t d = tmem + 128 * i;
+      if (i == 0) {  // query tile 1 reads the same slots right after tile 0
+        if (!wait_k(t)) { ok = false; return; }
+        tc_fence_after();
+      }
       for (int kb = 0; kb < 3; ++kb) {
         const long long L = 5LL * t + kb;
-        if (i == 0) {  // query tile 1 reads the same slots right after tile 0
-          if (!wait_full(L)) { ok = false; return; }
-          tc_fence_after();
-        }
         const uint64_t a0 = dq + (uint64_t)((kb * TC_SLOT) >> 4);
         const uint64_t b0 = dring_k + (uint64_t)((slot_of(L) * TC_SLOT) >> 4);
 #pragma unroll
@@ -372,8 +382,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     auto issue_PV = [&](int i, int t, bool release) {
       if (!warp_wait(sBar + B_PREADY + 8 * i, (uint32_t)t & 1u, abort_flag)) { ok = false; return; }
       const long long L0 = 5LL * t + 3;
-      for (int db = 0; db < 2 && i == 0; ++db) {  // tile 1: waited for by tile 0
-        if (!wait_full(L0 + db)) { ok = false; return; }
+      if (i == 0 && !wait_v(t)) { ok = false; return; }  // tile 1 reads them right after tile 0
+      for (int db = 0; db < 2 && i == 0; ++db) {
         if (WINDOW && i == 0 && u_lo + t < 0) {
           // The ring tile: V rows of slots that hold no position of the
           // window may be stale or never written; zero them before the product.
