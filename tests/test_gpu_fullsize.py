@@ -6,6 +6,8 @@ times: sampled outputs against the fp64 oracle.
 * Chunked prefill: 8192-token chunk on 122880 cached tokens -- sampled rows
   (first, last, window and tile boundaries), all heads, both layer kinds.
 * Long-context decode: batch 16 at context 524289 -- sampled sequences.
+* Pro-shaped decode: 128 sequences with contexts log-uniform up to ~1M, both
+  head configurations -- the shortest, a median and the longest sequence.
 * Draft verification: the decode batch checking 4 tokens per sequence
   through the varlen calls -- sampled sequences, all rows and heads.
 
@@ -146,6 +148,64 @@ def test_chunked_prefill_full_size_sampled(kvr):
                              work.sinks.double().cpu().numpy())
     compare_rows(work.out_s[rows], want, "prefill swa")
     del work
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("hq,hkv_full", [(64, 4), (128, 8)])
+def test_pro_shaped_contexts_decode_sampled(kvr, hq, hkv_full):
+    # The Pro-shaped decode step's batch: 128 sequences with contexts
+    # log-uniform over [1K, 1M] (seed 1004), one full layer (paged pool of all
+    # 19.6M cached tokens) and one windowed layer (8 KV heads, ring 128 +
+    # sink); 64 q / 4 KV heads as the workload states, and the Pro's own 128 q
+    # / 8 KV heads.  Sampled: the shortest, a median and the longest sequence.
+    from sinks_kv_ring_gb300.synth import Synth, ragged_contexts
+    B, vs_, bsz = 128, 0.612, 64
+    ctx = ragged_contexts(B, 1024, 1 << 20, 1004)
+    max_ctx = max(ctx) + 1
+    t4, t7 = kvr.rope_table(1e4, max_ctx), kvr.rope_table(1e7, max_ctx)
+    mb = [(c + 1 + bsz - 1) // bsz for c in ctx]
+    bt = torch.zeros(B, max(mb), dtype=torch.int32)
+    off = 0
+    for b, m in enumerate(mb):
+        bt[b, :m] = torch.arange(off, off + m, dtype=torch.int32)
+        off += m
+    pool = kvr.PagedLayout(torch.empty(off, hkv_full, bsz, 192, dtype=torch.bfloat16, device="cuda"),
+                           torch.empty(off, hkv_full, bsz, 128, dtype=torch.bfloat16, device="cuda"), bt.cuda())
+    syn_f, syn_s = Synth(1004, layer=1, device="cuda"), Synth(1004, layer=0, device="cuda")
+    import bench
+    bench._fill_pool(kvr, pool, syn_f, range(B), ctx, t7, vs_)
+    ring = kvr.RingLayout.empty(B, 8)
+    for b, c in enumerate(ctx):
+        lo = c - 127
+        kvr.kv_ring_append_rope(syn_s.k(127, 8, seq=b, start=lo), syn_s.v(127, 8, seq=b, start=lo),
+                                torch.arange(lo, c, device="cuda"), torch.full((127,), b, dtype=torch.int32,
+                                                                              device="cuda"), t4, vs_, ring)
+    pos = torch.tensor(ctx, dtype=torch.int64, device="cuda")
+    seq = torch.arange(B, dtype=torch.int32, device="cuda")
+    kn_f, vn_f = syn_f.k(B, hkv_full, seq=60_000), syn_f.v(B, hkv_full, seq=60_000)
+    kn_s, vn_s = syn_s.k(B, 8, seq=60_000), syn_s.v(B, 8, seq=60_000)
+    kvr.kv_ring_append_rope(kn_f, vn_f, pos, seq, t7, vs_, pool)
+    kvr.kv_ring_append_rope(kn_s, vn_s, pos, seq, t4, vs_, ring)
+    qf, qs = syn_f.q(B, hq, hkv_full, seq=50_000), syn_s.q(B, hq, 8, seq=50_000)
+    sinks = syn_s.sinks(hq).cuda()
+    scale = 1.0 / math.sqrt(192.0)
+    of = kvr.full_attn_decode(qf, pos, seq, pool, t7, scale, max_ctx)
+    osw = kvr.swa_sink_decode(qs, pos, seq, ring, sinks, t4, scale)
+    torch.cuda.synchronize()
+    assert kvr.device_status() == 0
+    order = np.argsort(ctx)
+    for b in (int(order[0]), int(order[B // 2]), int(order[-1])):
+        p = ctx[b]
+        kf, vf = _pool_raw(syn_f, hkv_full, b, p)
+        kf, vf = torch.cat([kf, kn_f[b:b + 1]]), torch.cat([vf, vn_f[b:b + 1]])
+        want = oracle.attend_seq(qf[b:b + 1], [p], kf, vf, 0, 1e7, vs_, scale, 0, None)
+        compare_rows(of[b:b + 1], want, f"pro full b={b} ctx={p}")
+        lo = p - 127
+        ks = torch.cat([syn_s.k(127, 8, seq=b, start=lo), kn_s[b:b + 1]])
+        vs = torch.cat([syn_s.v(127, 8, seq=b, start=lo), vn_s[b:b + 1]])
+        want = oracle.attend_seq(qs[b:b + 1], [p], ks, vs, lo, 1e4, vs_, scale, 128, sinks.double().cpu().numpy())
+        compare_rows(osw[b:b + 1], want, f"pro swa b={b}")
+    del pool, ring
     torch.cuda.empty_cache()
 
 
