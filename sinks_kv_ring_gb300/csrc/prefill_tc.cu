@@ -1,6 +1,9 @@
-// prefill_tc.cu -- chunked prefill over a full-attention layer on the
-// Blackwell tensor cores: TMA tile loads, tcgen05.mma with accumulators in
-// TMEM, fp32 online softmax in registers.
+// prefill_tc.cu -- chunked prefill on the Blackwell tensor cores: TMA tile
+// loads, tcgen05.mma with accumulators in TMEM, fp32 online softmax in
+// registers.  One kernel serves full-attention layers (paged pool) and, in
+// window mode, windowed layers (ring + staged chunk rows, sink); one chunk
+// or a batch of chunks of different lengths (varlen plan, with key splits
+// for short chunks).
 //
 // gaudi-cookbook "MiMo-V2.6-Flash on Gaudi 2", "Tiled global-attention
 // prefill": softmax is per query row, so independent tiles of query rows
@@ -13,15 +16,17 @@
 // (position, head) pairs of one KV head's GQA group), one SM, 320 threads:
 //   warps 0-3  softmax of tile 0 (thread = row = TMEM lane)
 //   warps 4-7  softmax of tile 1
-//   warp  8    TMEM owner and MMA issuer (lane 0)
-//   warp  9    TMA producer (lane 0)
+//   warp  8    TMEM owner and MMA issuer (converged; elect.sync issues)
+//   warp  9    TMA producer (converged; elect.sync issues)
 // TMEM (512 columns): S0 | S1 | O0 | O1, 128 fp32 columns each.  The bf16
 // probabilities P of a tile are written over the first 64 columns of its S
 // and feed the P.V product straight from TMEM.
 // Shared memory: Q0, Q1 (3 x 16 KB each, 128-byte swizzled K-major) and a
 // ring of eight 16 KB slots.  Every K/V tile of 128 keys is five slot loads:
 // K dims 0-63, 64-127, 128-191 (K-major, for S = Q K^T) and V dims 0-63,
-// 64-127 (MN-major, for O += P V).
+// 64-127 (MN-major, for O += P V).  The three K loads and the two V loads of
+// a key tile each complete on one transaction barrier (double-buffered);
+// query tile 1 relies on tile 0's waits.
 // MMA order per key tile j (the two tiles ping-pong, so one tile's softmax
 // overlaps the other tile's products):
 //   O0 += P0(j-1) V(j-1);  S0 = Q0 K(j)^T;  O1 += P1(j-1) V(j-1);  S1 = Q1 K(j)^T

@@ -1,5 +1,5 @@
 // tc_ptx.cuh -- inline-PTX wrappers for the Blackwell (sm_100 family) tensor
-// path: mbarriers with bounded waits, TMA 2-D tile loads, tcgen05 TMEM
+// path: mbarriers with bounded waits, TMA 2-D / 3-D / 4-D tile loads, tcgen05 TMEM
 // allocation / MMA / commit / loads / stores, and the shared-memory and
 // instruction descriptors of tcgen05.mma kind::f16.
 #pragma once
@@ -83,15 +83,9 @@ __device__ __forceinline__ void tc_fence_after() {
 }
 
 // ----------------------------------------------------------------- TMA
-// 2-D tiled load of box {x.., y..} of `map` into shared memory, completing
-// `bytes` on mbarrier `bar`.  x * element size must be a multiple of 16.
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *map, int x, int y, uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
-      ::"r"(dst), "l"(map), "r"(x), "r"(y), "r"(bar)
-      : "memory");
-}
-
+// Tiled loads of the box at coordinates {x, y, ...} of `map` into shared
+// memory, completing their bytes on mbarrier `bar`.  x * element size must be
+// a multiple of 16.
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *map, int x, int y, int z, uint32_t bar) {
   asm volatile(
       "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];"
@@ -146,22 +140,8 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
   asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
 }
 
-// D[tmem] (+)= A[smem desc] * B[smem desc]
-__device__ __forceinline__ void mma_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
-  asm volatile(
-      "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d),
-      "l"(a), "l"(b), "r"(idesc), "r"(acc)
-      : "memory");
-}
-// D[tmem] (+)= A[tmem] * B[smem desc]
-__device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
-  asm volatile(
-      "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d),
-      "r"(a), "l"(b), "r"(idesc), "r"(acc)
-      : "memory");
-}
+// D[tmem] (+)= A[smem desc] * B[smem desc] (ss) or A[tmem] * B[smem desc]
+// (ts); acc = 0 overwrites D.  Issued by one elected lane of a converged warp.
 __device__ __forceinline__ void mma_ss_elect(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
   asm volatile(
       "{\n.reg .pred p, e;\nsetp.ne.b32 p, %4, 0;\nelect.sync _|e, 0xffffffff;\n"
@@ -176,18 +156,13 @@ __device__ __forceinline__ void mma_ts_elect(uint32_t d, uint32_t a, uint64_t b,
       "r"(a), "l"(b), "r"(idesc), "r"(acc)
       : "memory");
 }
+// Arrive on `bar` once every tcgen05 op issued so far by this thread is done.
 __device__ __forceinline__ void mma_commit_elect(uint32_t bar) {
   asm volatile(
       "{\n.reg .pred e;\nelect.sync _|e, 0xffffffff;\n"
       "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n}\n" ::"r"(bar)
       : "memory");
 }
-// Arrive on `bar` once every tcgen05 op issued so far by this thread is done.
-__device__ __forceinline__ void mma_commit(uint32_t bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-               : "memory");
-}
-
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
