@@ -48,7 +48,7 @@ constexpr int TC_NSLOT = 8;
 constexpr int TC_QTILE = 3 * TC_SLOT;          // 128 rows x 192 dims
 constexpr int TC_OFF_RING = 2 * TC_QTILE;      // 96 KB
 constexpr int TC_OFF_BAR = TC_OFF_RING + TC_NSLOT * TC_SLOT;  // 224 KB
-constexpr int TC_OFF_TAG = TC_OFF_BAR + 256;                  // windowed: the ring's 128 slot tags
+constexpr int TC_OFF_TAG = TC_OFF_BAR + 256;                  // windowed: 128 bits, slot c holds its window position
 constexpr int TC_SMEM = TC_OFF_TAG + 512 + 1024;              // + alignment slack
 constexpr unsigned ST_TIMEOUT = 8u;
 constexpr float NEG_INF = -INFINITY;
@@ -183,7 +183,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 
   // ---- set-up: barriers, TMEM, rotated Q tiles
   if constexpr (WINDOW) {
-    if (tid < WIN) reinterpret_cast<int32_t *>(gbase + TC_OFF_TAG)[tid] = a.slot_pos[(long long)rseq * WIN + tid];
+    // Slot c of the ring tile stands for position P0 - 128 + ((c - P0) mod
+    // 128); one bit per slot says whether its tag agrees (warps 0-3).
+    if (tid < WIN) {
+      const long long pos = P0 - WIN + ((tid - (int)(P0 & (WIN - 1))) & (WIN - 1));
+      const bool held = pos >= 0 && a.slot_pos[(long long)rseq * WIN + tid] == (int32_t)pos;
+      const unsigned bits = __ballot_sync(0xffffffffu, held);
+      if (lane == 0) reinterpret_cast<uint32_t *>(gbase + TC_OFF_TAG)[warp] = bits;
+    }
   }
   if (tid == 0) {
     for (int i = 0; i < TC_NSLOT; ++i) mbar_init(sBar + B_EMPTY + 8 * i, 1);
@@ -392,14 +399,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         if (WINDOW && i == 0 && u_lo + t < 0) {
           // The ring tile: V rows of slots that hold no position of the
           // window may be stale or never written; zero them before the product.
-          const int32_t *tg = reinterpret_cast<const int32_t *>(gbase + TC_OFF_TAG);
+          const uint32_t *held = reinterpret_cast<const uint32_t *>(gbase + TC_OFF_TAG);
           uint4 *g = reinterpret_cast<uint4 *>(gbase + TC_OFF_RING + slot_of(L0 + db) * TC_SLOT);
-          const int pm = (int)(P0 & (WIN - 1));
-          for (int e = lane; e < 128 * 8; e += 32) {
-            const int c = e >> 3;
-            const long long pos = P0 - WIN + ((c - pm) & (WIN - 1));
-            if (pos < 0 || tg[c] != (int32_t)pos) g[e] = make_uint4(0, 0, 0, 0);
-          }
+#pragma unroll 4
+          for (int e = lane; e < 128 * 8; e += 32)
+            if (!((held[e >> 8] >> ((e >> 3) & 31)) & 1u)) g[e] = make_uint4(0, 0, 0, 0);
           fence_proxy_async_smem();
           __syncwarp();
         }
@@ -486,25 +490,27 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       tmem_wait_ld();
       const long long j0 = k_lo + 128LL * t;
       if constexpr (WINDOW) {
-        if (u_lo + t < 0) {  // the ring: slot c holds position P0 - 128 + ((c - P0) mod 128) if its tag agrees
-          const int32_t *tg = reinterpret_cast<const int32_t *>(gbase + TC_OFF_TAG);
+        const int ii = (int)(pr - P0);  // this row's offset in the chunk
+        if (u_lo + t < 0) {
+          // The ring: slot c is position P0 - 128 + k, k = (c - P0) mod 128,
+          // inside this row's window iff k > ii, and present iff its bit is set.
+          const uint32_t *held = reinterpret_cast<const uint32_t *>(gbase + TC_OFF_TAG);
           const int pm = (int)(P0 & (WIN - 1));
 #pragma unroll
-          for (int c = 0; c < 4; ++c)
+          for (int c = 0; c < 4; ++c) {
+            const uint32_t hb = held[c];
 #pragma unroll
-            for (int e = 0; e < 32; ++e) {
-              const int col = 32 * c + e;
-              const long long pos = P0 - WIN + ((col - pm) & (WIN - 1));
-              if (pos < 0 || tg[col] != (int32_t)pos || pos <= pr - WIN || pos > pr) s[c][e] = __float_as_uint(NEG_INF);
-            }
+            for (int e = 0; e < 32; ++e)
+              if (!((hb >> e) & 1u) || ((32 * c + e - pm) & (WIN - 1)) <= ii) s[c][e] = __float_as_uint(NEG_INF);
+          }
         } else {
+          // Chunk rows 128u + col: inside the window iff ii - 128 < 128u + col <= ii.
+          const int d = ii - 128 * (u_lo + t);
 #pragma unroll
           for (int c = 0; c < 4; ++c)
 #pragma unroll
-            for (int e = 0; e < 32; ++e) {
-              const long long pos = j0 + 32 * c + e;
-              if (pos <= pr - WIN || pos > pr) s[c][e] = __float_as_uint(NEG_INF);
-            }
+            for (int e = 0; e < 32; ++e)
+              if (32 * c + e > d || 32 * c + e <= d - WIN) s[c][e] = __float_as_uint(NEG_INF);
         }
       } else if (j0 + 127 > pmin) {  // the diagonal (and the end of the keys) is in this tile
 #pragma unroll
