@@ -215,12 +215,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     const int t = r & 127;
     return (uint32_t)((r >> 7) * TC_QTILE + (ch >> 3) * TC_SLOT + t * 128 + (((ch & 7) ^ (t & 7)) << 4));
   };
+  // (f0 + r < nrows < 2^31: 32-bit index math)
   auto q_row = [&](int r, bool &live) {
-    const long long f = f0 + r;
-    live = f < nrows;
-    const long long i = live ? f / a.G : 0;
-    const int g = live ? (int)(f % a.G) : 0;
-    return qc + (i * a.hq + (long long)kv * a.G + g) * DQK;
+    const int f = (int)f0 + r;
+    live = f < (int)nrows;
+    const int i = live ? f / a.G : 0;
+    const int g = live ? f - i * a.G : 0;
+    return qc + ((long long)i * a.hq + kv * a.G + g) * DQK;
   };
   // Dims 64..191 pass through: asynchronous 16-byte copies (zero-filled
   // past the chunk), all in flight at once.
@@ -250,7 +251,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         const uint4 *s4 = reinterpret_cast<const uint4 *>(qh);
         x1[k] = s4[c];
         x2[k] = s4[c + 4];
-        const float4 *tr = reinterpret_cast<const float4 *>(a.table + (P0 + (f0 + r) / a.G) * 64 + 16 * c);
+        const float4 *tr = reinterpret_cast<const float4 *>(a.table + (P0 + ((int)f0 + r) / a.G) * 64 + 16 * c);
 #pragma unroll
         for (int u = 0; u < 4; ++u) tv[k][u] = tr[u];
       }
@@ -277,6 +278,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  bool all_held = false;  // windowed: every ring slot holds its window position
+  if constexpr (WINDOW) {
+    const uint32_t *held = reinterpret_cast<const uint32_t *>(gbase + TC_OFF_TAG);
+    all_held = (held[0] & held[1] & held[2] & held[3]) == 0xffffffffu;
+  }
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(gbase + TC_OFF_BAR + B_TMEM);
 
   if (warp == 9) {
@@ -396,7 +402,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       const long long L0 = 5LL * t + 3;
       if (i == 0 && !wait_v(t)) { ok = false; return; }  // tile 1 reads them right after tile 0
       for (int db = 0; db < 2 && i == 0; ++db) {
-        if (WINDOW && i == 0 && u_lo + t < 0) {
+        if (WINDOW && i == 0 && u_lo + t < 0 && !all_held) {
           // The ring tile: V rows of slots that hold no position of the
           // window may be stale or never written; zero them before the product.
           const uint32_t *held = reinterpret_cast<const uint32_t *>(gbase + TC_OFF_TAG);
@@ -496,12 +502,20 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           // inside this row's window iff k > ii, and present iff its bit is set.
           const uint32_t *held = reinterpret_cast<const uint32_t *>(gbase + TC_OFF_TAG);
           const int pm = (int)(P0 & (WIN - 1));
+          if (all_held) {
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            const uint32_t hb = held[c];
+            for (int c = 0; c < 4; ++c)
 #pragma unroll
-            for (int e = 0; e < 32; ++e)
-              if (!((hb >> e) & 1u) || ((32 * c + e - pm) & (WIN - 1)) <= ii) s[c][e] = __float_as_uint(NEG_INF);
+              for (int e = 0; e < 32; ++e)
+                if (((32 * c + e - pm) & (WIN - 1)) <= ii) s[c][e] = __float_as_uint(NEG_INF);
+          } else {
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              const uint32_t hb = held[c];
+#pragma unroll
+              for (int e = 0; e < 32; ++e)
+                if (!((hb >> e) & 1u) || ((32 * c + e - pm) & (WIN - 1)) <= ii) s[c][e] = __float_as_uint(NEG_INF);
+            }
           }
         } else {
           // Chunk rows 128u + col: inside the window iff ii - 128 < 128u + col <= ii.
