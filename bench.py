@@ -13,6 +13,7 @@ sequence (multi-token prediction) through the varlen calls.
 
 Other workloads: prefill, long_decode (batch 16 at 524288 tokens), mtp_decode,
 pro_true (pro_mixed with the Pro's own head counts: 128 q heads, 8 KV heads on both kinds),
+long_stack (batch 16 at 524288 tokens through a 48-layer stack, 9 full : 39 windowed),
 pro_mixed (128 ragged sequences through a 70-layer stack, 10 full : 60
 windowed), tiny (1 sequence, 512 tokens).
 
@@ -580,7 +581,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="flash_decode",
-                    choices=["flash_decode", "long_decode", "prefill", "pro_mixed", "pro_true", "mtp_decode"])
+                    choices=["flash_decode", "long_decode", "prefill", "pro_mixed", "pro_true", "long_stack",
+                             "mtp_decode"])
     ap.add_argument("--mtp-len", type=int, default=4, help="draft tokens verified per sequence (mtp_decode)")
     ap.add_argument("--no-prefill", action="store_true", help="skip the prefill sub-measurement")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -620,7 +622,7 @@ def main():
     peaks_d, peaks_src = peaks()
     if args.workload == "prefill":
         return prefill_only(args, kvr, peaks_d, peaks_src, rank, world)
-    if args.workload in ("pro_mixed", "pro_true"):
+    if args.workload in ("pro_mixed", "pro_true", "long_stack"):
         return pro_mixed(args, kvr, peaks_d, peaks_src, rank, world)
     if args.workload == "mtp_decode":
         return mtp_only(args, kvr, peaks_d, peaks_src, rank, world)
@@ -770,14 +772,15 @@ class ProMixedWorkload:
     layer still streams its full bytes from HBM)."""
 
     def __init__(self, kvr, B=128, hq=64, layers=70, vscale=0.612, seed=1004, n_pools=None, device="cuda",
-                 hkv_full=4, hkv_swa=8):
+                 hkv_full=4, hkv_swa=8, contexts=None, full_period=7):
         from sinks_kv_ring_gb300.synth import Synth, ragged_contexts
         self.kvr, self.B, self.hq, self.vscale = kvr, B, hq, vscale
         self.hkv_full, self.hkv_swa = hkv_full, hkv_swa
         dev = device
-        self.ctx = ragged_contexts(B, 1024, 1 << 20, seed)        # cached tokens per sequence
+        # cached tokens per sequence
+        self.ctx = list(contexts) if contexts is not None else ragged_contexts(B, 1024, 1 << 20, seed)
         self.max_ctx = max(self.ctx) + 1
-        self.kinds = ["full" if i % 7 == 6 else "swa" for i in range(layers)]
+        self.kinds = ["full" if i % full_period == full_period - 1 else "swa" for i in range(layers)]
         self.t4 = kvr.rope_table(1e4, self.max_ctx, device=dev)
         self.t7 = kvr.rope_table(1e7, self.max_ctx, device=dev)
         bsz = 64
@@ -786,7 +789,7 @@ class ProMixedWorkload:
         pool_bytes = nblk * self.hkv_full * bsz * 640
         free = torch.cuda.mem_get_info()[0]
         if n_pools is None:
-            n_pools = max(1, min(10, int((free - 16e9) * 0.85 // pool_bytes)))
+            n_pools = max(1, min(self.kinds.count("full"), int((free - 16e9) * 0.85 // pool_bytes)))
         self.n_pools = n_pools
         bt = torch.zeros(B, max(mb), dtype=torch.int32)
         off = 0
@@ -871,11 +874,16 @@ class ProMixedWorkload:
 
 
 def pro_mixed(args, kvr, peaks_d, peaks_src, rank, world):
-    true_heads = args.workload == "pro_true"
-    if true_heads:   # the head counts the pages imply for the real Pro: 128 q heads, 8 KV heads on both kinds
+    if args.workload == "pro_true":   # the head counts the pages imply for the real Pro: 128 q / 8 KV heads
         work = ProMixedWorkload(kvr, hq=128, hkv_full=8, hkv_swa=8, seed=rank_seed(1004, rank))
+        shape = "128 sequences, contexts log-uniform 1K-1M (seed 1004); 70 layers (i % 7 == 6 full: 10 full, 60 windowed)"
+    elif args.workload == "long_stack":   # long-context decode through a Flash-shaped 48-layer stack
+        work = ProMixedWorkload(kvr, B=16, hq=64, layers=48, vscale=0.707, seed=rank_seed(1003, rank),
+                                contexts=[524288] * 16, full_period=5)
+        shape = "16 sequences at 524288 cached tokens; 48 layers (i % 5 == 4 full: 9 full, 39 windowed)"
     else:
         work = ProMixedWorkload(kvr, seed=rank_seed(1004, rank))
+        shape = "128 sequences, contexts log-uniform 1K-1M (seed 1004); 70 layers (i % 7 == 6 full: 10 full, 60 windowed)"
     work.capture()
     stream = torch.cuda.current_stream()
     steps = args.steps if "--steps" in sys.argv else 20
@@ -887,17 +895,18 @@ def pro_mixed(args, kvr, peaks_d, peaks_src, rank, world):
     res = {"metric": METRIC, "value": round(job_throughput(work.B, world, ms), 1), "unit": "tokens/s",
            "n_gpus": world, "steps": steps, "warmup": args.warmup, "ms_per_step": round(ms, 3),
            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-           "config": {"workload": f"{args.workload}: 128 sequences, contexts log-uniform 1K-1M (seed 1004); 70 layers "
-                                  f"(i % 7 == 6 full: 10 full, 60 windowed); {work.hq} q heads, windowed "
-                                  f"{work.hkv_swa} KV heads, full {work.hkv_full} KV heads; value scale 0.612; one "
-                                  "decode step as one CUDA graph",
+           "config": {"workload": f"{args.workload}: {shape}; {work.hq} q heads, windowed "
+                                  f"{work.hkv_swa} KV heads, full {work.hkv_full} KV heads; value scale {work.vscale}; "
+                                  "one decode step as one CUDA graph",
                       "global_batch": work.B * world, "seq_len": work.max_ctx, "parallelism": f"dp{world}",
                       "buckets": work.buckets(), "distinct_full_pools": work.n_pools,
                       "total_context_tokens": int(sum(work.ctx)),
-                      "l2": "inputs > L2: each full layer streams its pool (tens of GB); 60 distinct rings"},
+                      "l2": f"inputs > L2: each full layer streams its pool (tens of GB); "
+                            f"{work.kinds.count('swa')} distinct rings"},
            "hbm_gbs": round(gbs, 1),
            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s",
-                        "frac": round(gbs / hbm, 4), "peak_source": peaks_src, "kernel": "whole 70-layer step",
+                        "frac": round(gbs / hbm, 4), "peak_source": peaks_src,
+                        "kernel": f"whole {len(work.kinds)}-layer step",
                         "traffic": None},
            "gpu_launches": work.launches_per_step * steps, "clocks": ck.summary()}
     if rank == 0:
