@@ -59,6 +59,16 @@ def peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
+NOMINAL = {"hbm": 7900.0, "tensor": 2250.0}  # GB300 data-sheet HBM3e GB/s and dense bf16 TFLOP/s
+
+
+def with_nominal(roof: dict) -> dict:
+    """Add the fraction of the nominal (data-sheet) peak beside the measured one."""
+    roof["nominal_peak"] = NOMINAL[roof["bound"]]
+    roof["frac_of_nominal"] = round(roof["achieved"] / NOMINAL[roof["bound"]], 4)
+    return roof
+
+
 def kernel_traffic(kernel: str):
     """DRAM bytes per launch of `kernel` from the committed ncu summary, if the
     kernel's source has not changed since the counters were taken."""
@@ -656,10 +666,10 @@ def main():
                                 "note": "ms/GB/s: CUDA events around the call inside the timed step (include "
                                         "launch gaps); graph_*: the kernel replayed back to back in a CUDA graph"},
         },
-        "roofline": {"bound": "hbm", "achieved": round(gbs_full, 1), "peak": hbm, "unit": "GB/s",
+        "roofline": with_nominal({"bound": "hbm", "achieved": round(gbs_full, 1), "peak": hbm, "unit": "GB/s",
                      "frac": round(gbs_full / hbm, 4), "peak_source": peaks_src,
                      "kernel": "full_attn_decode (split kernel + combine)",
-                     "traffic": kernel_traffic("full_decode_kernel")},
+                     "traffic": kernel_traffic("full_decode_kernel")}),
         "e2e": {"value": round(job_throughput(B, world, e2e_ms), 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": work.launches_per_step * args.steps,
@@ -691,9 +701,9 @@ def main():
                                         "flop": pw.flops_full()},
             "swa_sink_prefill_chunk": {"ms": round(pw.t_swa.mean_ms(), 4), "TFLOP/s": round(tf_swa, 1),
                                        "flop": pw.flops_swa()},
-            "roofline": {"bound": "tensor", "achieved": round(tf_full, 1), "peak": pk, "unit": "TFLOP/s",
+            "roofline": with_nominal({"bound": "tensor", "achieved": round(tf_full, 1), "peak": pk, "unit": "TFLOP/s",
                          "frac": round(tf_full / pk, 4), "peak_source": peaks_src + " (sustained)",
-                         "traffic": kernel_traffic("full_prefill_tc_kernel")},
+                         "traffic": kernel_traffic("full_prefill_tc_kernel")}),
         }
         res["prefill"]["steps"] = psteps
         res["prefill"]["clocks"] = pck.summary()
@@ -725,9 +735,9 @@ def mtp_only(args, kvr, peaks_d, peaks_src, rank, world):
                       "l2": f"inputs > L2: full pool {m.bytes_full() / 1e9:.2f} GB read per step; rings rotated over "
                             f"{len(work.rings)} copies"},
            "kernels": {k: v for k, v in r.items() if k.endswith("varlen")},
-           "roofline": {"bound": "hbm", "achieved": kf["GB/s"], "peak": hbm, "unit": "GB/s", "frac": kf["hbm_frac"],
+           "roofline": with_nominal({"bound": "hbm", "achieved": kf["GB/s"], "peak": hbm, "unit": "GB/s", "frac": kf["hbm_frac"],
                         "peak_source": peaks_src, "kernel": "full_attn_prefill_varlen (plan + tensor-core kernel + merge)",
-                        "traffic": kernel_traffic("full_prefill_tc_kernel_varlen")},
+                        "traffic": kernel_traffic("full_prefill_tc_kernel_varlen")}),
            "gpu_launches": m.launches_per_step * steps, "clocks": r["clocks"]}
     if rank == 0:
         print(json.dumps(res), flush=True)
@@ -755,9 +765,9 @@ def prefill_only(args, kvr, peaks_d, peaks_src, rank, world):
                        "swa_sink_prefill_chunk": {"ms": round(ms_s, 4),
                                                   "TFLOP/s": round(pw.flops_swa() / (ms_s / 1e3) / 1e12, 1),
                                                   "flop": pw.flops_swa()}},
-           "roofline": {"bound": "tensor", "achieved": round(tf_full, 1), "peak": pk, "unit": "TFLOP/s",
+           "roofline": with_nominal({"bound": "tensor", "achieved": round(tf_full, 1), "peak": pk, "unit": "TFLOP/s",
                         "frac": round(tf_full / pk, 4), "peak_source": peaks_src + " (sustained)",
-                        "kernel": "full_prefill_tc_kernel", "traffic": kernel_traffic("full_prefill_tc_kernel")},
+                        "kernel": "full_prefill_tc_kernel", "traffic": kernel_traffic("full_prefill_tc_kernel")}),
            "gpu_launches": pw.launches_per_step * steps, "clocks": ck.summary()}
     if rank == 0:
         print(json.dumps(res), flush=True)
@@ -904,10 +914,10 @@ def pro_mixed(args, kvr, peaks_d, peaks_src, rank, world):
                       "l2": f"inputs > L2: each full layer streams its pool (tens of GB); "
                             f"{work.kinds.count('swa')} distinct rings"},
            "hbm_gbs": round(gbs, 1),
-           "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s",
+           "roofline": with_nominal({"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s",
                         "frac": round(gbs / hbm, 4), "peak_source": peaks_src,
                         "kernel": f"whole {len(work.kinds)}-layer step",
-                        "traffic": None},
+                        "traffic": None}),
            "gpu_launches": work.launches_per_step * steps, "clocks": ck.summary()}
     if rank == 0:
         print(json.dumps(res), flush=True)
