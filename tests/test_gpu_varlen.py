@@ -275,6 +275,27 @@ def test_varlen_plan_more_than_1024_chunks(tables):
         compare_rows(outw[r], want, f"swa chunk {i}")
 
 
+@pytest.mark.parametrize("hq,hkv", [(6, 2), (24, 2)])
+def test_swa_prefill_odd_group_sizes(hq, hkv, tables):
+    # Group sizes that do not divide the 256-row tiles (3 and 12 query heads
+    # per KV head): a single long chunk on a wrapped ring, and a varlen batch
+    # of short and long chunks.
+    syn = Synth(3951 + hq, dist="plain", device=DEV)
+    sinks = syn.sinks(hq).to(DEV)
+    P0, C = 1000, 300
+    ring, stage, q, cu, P0t, sq = _swa_case(syn, hq, hkv, [0], [P0], [C], tables)
+    out = kvr.swa_sink_prefill_chunk(q, P0, 0, stage, ring, sinks, tables[1e4], SCALE)
+    torch.cuda.synchronize()
+    assert kvr.device_status() == 0
+    compare_rows(out, _swa_want(syn, hkv, q, [0], [P0], [C], sinks), f"swa chunk G={hq // hkv}")
+    seqs, P0s, Cs = [0, 1, 2, 3], [500, 77, 2000, 129], [3, 1, 150, 10]
+    ring, stage, q, cu, P0t, sq = _swa_case(syn, hq, hkv, seqs, P0s, Cs, tables)
+    out = kvr.swa_sink_prefill_varlen(q, cu, P0t, sq, stage, ring, sinks, tables[1e4], SCALE)
+    torch.cuda.synchronize()
+    assert kvr.device_status() == 0
+    compare_rows(out, _swa_want(syn, hkv, q, seqs, P0s, Cs, sinks), f"swa varlen G={hq // hkv}")
+
+
 # --------------------------------------------------------------------------- bad inputs, graphs
 
 def test_varlen_bad_device_inputs_are_flagged(tables):
