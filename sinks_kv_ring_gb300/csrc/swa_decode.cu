@@ -40,6 +40,9 @@ constexpr int SD_THREADS = SD_WARPS * 32;
 constexpr int SD_PARTS = 1;                              // parts (stages) per unit
 constexpr int SD_CTAS = 2;                               // CTAs per SM
 constexpr int SD_NSTAGE = 1;                             // stages per CTA
+// A unit streamed in parts needs a second stage: the next part is issued
+// when the stage of the part before it frees up.
+static_assert(SD_PARTS == 1 || SD_NSTAGE >= 2, "parts > 1 need at least two stages");
 constexpr int SD_HALF = WIN / SD_PARTS;                  // slots per part
 constexpr int SD_SPW = SD_HALF / SD_WARPS;               // slots per warp in phase 1 (8 or 16)
 constexpr int SD_NT = SD_SPW / 8;                        // 8-key MMA tiles per warp
