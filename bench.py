@@ -182,6 +182,30 @@ class EventTimer:
         return sum(a.elapsed_time(b) for a, b in self.pairs) / len(self.pairs)
 
 
+# --------------------------------------------------------------------------- work counters
+
+KV_BYTES = (192 + 128) * 2   # K and V of one position and KV head, bf16
+
+
+def layer_kv_bytes(contexts, hkv: int, window: int | None = None) -> int:
+    """K/V bytes one decode step must read from one layer: every context
+    position (full layer) or the last `window` ones (windowed layer)."""
+    return sum(min(window, c) if window else c for c in contexts) * hkv * KV_BYTES
+
+
+def prefill_pairs(P0: int, C: int, window: int | None = None) -> int:
+    """(query, key) pairs of a C-row chunk on P0 cached positions (causal; the
+    last `window` keys of each row for a windowed layer)."""
+    if window is None:
+        return C * P0 + C * (C + 1) // 2
+    return sum(min(window, P0 + i + 1) for i in range(C))
+
+
+def attn_flops(pairs: int, hq: int) -> int:
+    """Multiply-adds x 2 of S = QK^T (192) and O = PV (128) over the pairs."""
+    return hq * pairs * 2 * (192 + 128)
+
+
 # --------------------------------------------------------------------------- workloads
 
 def _fill_pool(kvr, pool, syn, seqs, ctx, table, vscale, chunk=65536):
@@ -256,10 +280,10 @@ class DecodeWorkload:
 
     def bytes_full(self):
         # K/V bytes the full layer must read (every cached position, every KV head)
-        return self.B * self.hkv_full * (self.p + 1) * (192 + 128) * 2
+        return layer_kv_bytes([self.p + 1] * self.B, self.hkv_full)
 
     def bytes_swa(self):
-        return self.B * self.hkv_swa * min(128, self.p + 1) * (192 + 128) * 2
+        return layer_kv_bytes([self.p + 1] * self.B, self.hkv_swa, window=128)
 
     def step(self, stream, timed=False):
         kvr = self.kvr
@@ -406,13 +430,10 @@ class PrefillWorkload:
         self.launches_per_step = 5
 
     def flops_full(self):
-        C, P0 = self.C, self.P0
-        pairs = C * P0 + C * (C + 1) // 2
-        return self.hq * pairs * 2 * (192 + 128)
+        return attn_flops(prefill_pairs(self.P0, self.C), self.hq)
 
     def flops_swa(self):
-        pairs = sum(min(128, self.P0 + i + 1) for i in range(self.C))
-        return self.hq * pairs * 2 * (192 + 128)
+        return attn_flops(prefill_pairs(self.P0, self.C, window=128), self.hq)
 
     def step(self, stream, timed=False):
         kvr = self.kvr
@@ -836,8 +857,9 @@ class ProMixedWorkload:
         self.graph = None
 
     def bytes_per_step(self):
-        full = sum(c + 1 for c in self.ctx) * self.hkv_full * 640
-        swa = sum(min(128, c + 1) for c in self.ctx) * self.hkv_swa * 640
+        ctx = [c + 1 for c in self.ctx]
+        full = layer_kv_bytes(ctx, self.hkv_full)
+        swa = layer_kv_bytes(ctx, self.hkv_swa, window=128)
         return self.kinds.count("full") * full + self.kinds.count("swa") * swa
 
     def buckets(self):
