@@ -37,28 +37,22 @@ using namespace tc;
 
 constexpr int SD_WARPS = 8;
 constexpr int SD_THREADS = SD_WARPS * 32;
-constexpr int SD_PARTS = 1;                              // parts (stages) per unit
 constexpr int SD_CTAS = 2;                               // CTAs per SM
-constexpr int SD_NSTAGE = 1;                             // stages per CTA
-// A unit streamed in parts needs a second stage: the next part is issued
-// when the stage of the part before it frees up.
-static_assert(SD_PARTS == 1 || SD_NSTAGE >= 2, "parts > 1 need at least two stages");
-constexpr int SD_HALF = WIN / SD_PARTS;                  // slots per part
-constexpr int SD_SPW = SD_HALF / SD_WARPS;               // slots per warp in phase 1 (8 or 16)
+constexpr int SD_SPW = WIN / SD_WARPS;                   // slots per warp in phase 1
 constexpr int SD_NT = SD_SPW / 8;                        // 8-key MMA tiles per warp
-constexpr int SD_HK = SD_HALF * DQK * 2;                 // K bytes per part
-constexpr int SD_HSTAGE = SD_HK + SD_HALF * DV * 2;      // + V bytes
-constexpr int SD_OFF_Q = SD_NSTAGE * SD_HSTAGE;          // two [16][192] query tiles
+constexpr int SD_HK = WIN * DQK * 2;                     // K bytes of a unit (48 KB)
+constexpr int SD_HV = WIN * DV * 2;                      // V bytes of a unit (32 KB)
+constexpr int SD_OFF_Q = SD_HK + SD_HV;                  // two [16][192] query tiles
 constexpr int SD_QTILE = 16 * DQK * 2;
 constexpr int SD_OFF_TAG = SD_OFF_Q + 2 * SD_QTILE;      // two [128] int32 tag arrays
 constexpr int SD_OFF_SINK = SD_OFF_TAG + 2 * WIN * 4;    // [hq] sinks * log2(e)
 constexpr int SD_MAX_HQ = 1024;
-constexpr int SD_OFF_P = SD_OFF_SINK + SD_MAX_HQ * 4;    // [16][part slots] bf16 probabilities
-constexpr int SD_OFF_RED = SD_OFF_P + 16 * SD_HALF * 2;  // [8 warps][16] row max, then row sums
+constexpr int SD_OFF_P = SD_OFF_SINK + SD_MAX_HQ * 4;    // [16][128] bf16 probabilities
+constexpr int SD_OFF_RED = SD_OFF_P + 16 * WIN * 2;      // [8 warps][16] row max, then row sums
 constexpr int SD_MAX_UNITS = 256;                        // units per CTA whose ring rows are staged
 constexpr int SD_OFF_ROW = SD_OFF_RED + 2 * SD_WARPS * 16 * 4;
-constexpr int SD_OFF_BAR = SD_OFF_ROW + SD_MAX_UNITS * 4;
-constexpr int SD_SMEM = SD_OFF_BAR + 8 * SD_NSTAGE + 32 + 1024;
+constexpr int SD_OFF_BAR = SD_OFF_ROW + SD_MAX_UNITS * 4;  // K barrier, V barrier, abort flag
+constexpr int SD_SMEM = SD_OFF_BAR + 16 + 32 + 1024;
 constexpr unsigned ST_TIMEOUT = 8u;
 
 struct SdArgs {
@@ -98,19 +92,23 @@ __device__ __forceinline__ void prefetch_unit(const SdArgs &a, int u, int tid, U
   const int b = u / a.hkv, kv = u % a.hkv;
   const uint16_t *qb = a.q + ((long long)b * a.hq + (long long)kv * a.G) * DQK;
   const int r = tid >> 4, ch = 8 + (tid & 15);
-  pf.pass = (ok && r < a.G) ? reinterpret_cast<const uint4 *>(qb + r * DQK)[ch] : make_uint4(0, 0, 0, 0);
+  // The query rows depend only on the unit, so they are loaded without
+  // waiting for the position / sequence checks (an invalid unit is skipped).
+  pf.pass = r < a.G ? reinterpret_cast<const uint4 *>(qb + r * DQK)[ch] : make_uint4(0, 0, 0, 0);
   pf.r1 = pf.r2 = make_uint4(0, 0, 0, 0);
 #pragma unroll
   for (int k = 0; k < 4; ++k) pf.cs[k] = make_float4(0.f, 0.f, 0.f, 0.f);
   if (tid < 64) {
     const int rr = tid >> 2, c = tid & 3;
-    if (ok && rr < a.G) {
+    if (rr < a.G) {
       const uint4 *s4 = reinterpret_cast<const uint4 *>(qb + rr * DQK);
       pf.r1 = s4[c];
       pf.r2 = s4[c + 4];
-      const float4 *tr = reinterpret_cast<const float4 *>(a.table + p * 64 + 16 * c);
+      if (ok) {
+        const float4 *tr = reinterpret_cast<const float4 *>(a.table + p * 64 + 16 * c);
 #pragma unroll
-      for (int k = 0; k < 4; ++k) pf.cs[k] = tr[k];
+        for (int k = 0; k < 4; ++k) pf.cs[k] = tr[k];
+      }
     }
   }
   pf.tag = -1;
@@ -143,21 +141,21 @@ __global__ void __launch_bounds__(SD_THREADS, SD_CTAS)
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t *g = smem_raw + (base - raw);
-  const uint32_t sBar = base + SD_OFF_BAR;
-  volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(g + SD_OFF_BAR + 8 * SD_NSTAGE);
+  const uint32_t kBar = base + SD_OFF_BAR, vBar = kBar + 8;
+  volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(g + SD_OFF_BAR + 16);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int units = a.B * a.hkv;
   const int nmine = units > (int)blockIdx.x ? (units - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x : 0;
   const int G = a.G;
   auto unit_id = [&](int n) { return (int)blockIdx.x + n * (int)gridDim.x; };
   if (nmine == 0) return;
-  const int nhalves = SD_PARTS * nmine;
 
   float *sSink = reinterpret_cast<float *>(g + SD_OFF_SINK);
   uint8_t *sP = g + SD_OFF_P;
   float *sMax = reinterpret_cast<float *>(g + SD_OFF_RED);  // [8][16]
   float *sSum = sMax + SD_WARPS * 16;                       // [8][16]
   int32_t *sRow = reinterpret_cast<int32_t *>(g + SD_OFF_ROW);
+  uint8_t *sK = g, *sV = g + SD_HK;
 
   // Ring row of this CTA's n-th unit (-1: invalid unit).
   auto ring_row = [&](int n) {
@@ -166,37 +164,38 @@ __global__ void __launch_bounds__(SD_THREADS, SD_CTAS)
     const int u = unit_id(n);
     return unit_valid(a, u, p, s) ? (s * a.hkv + u % a.hkv) * WIN : -1;
   };
-  // Thread 0: part H % PARTS of unit H / PARTS into stage H % NSTAGE.  An
-  // invalid unit still completes the stage's barrier phase (no bytes).
-  auto issue = [&](int H, int row) {
-    const int st = H % SD_NSTAGE;
-    const uint32_t bar = sBar + 8 * st;
+  auto row_of = [&](int n) { return n < SD_MAX_UNITS ? sRow[n] : ring_row(n); };
+  // Thread 0: the K rows / the V rows of unit n, as one 3-D TMA box of whole
+  // rows each, on their own barriers.  An invalid unit still completes the
+  // barrier's phase (no bytes).
+  auto issue_k = [&](int row) {
     if (row >= 0) {
-      const uint32_t dst = base + st * SD_HSTAGE;
-      const int r = row + SD_HALF * (H % SD_PARTS);
-      mbar_expect_tx(bar, SD_HSTAGE);
-      tma_load_3d(dst, &tmk, 0, 0, r, bar);           // whole 384-byte K rows, one pass
-      tma_load_3d(dst + SD_HK, &tmv, 0, 0, r, bar);   // whole 256-byte V rows
+      mbar_expect_tx(kBar, SD_HK);
+      tma_load_3d(base, &tmk, 0, 0, row, kBar);
     } else {
-      mbar_arrive(bar);
+      mbar_arrive(kBar);
+    }
+  };
+  auto issue_v = [&](int row) {
+    if (row >= 0) {
+      mbar_expect_tx(vBar, SD_HV);
+      tma_load_3d(base + SD_HK, &tmv, 0, 0, row, vBar);
+    } else {
+      mbar_arrive(vBar);
     }
   };
 
   // The first loads go out before anything else.
-  int issued = -1;  // highest half whose load was issued (thread 0)
+  int issued_k = -1, issued_v = -1;  // last unit whose K / V load was issued (thread 0)
   if (tid == 0) {
-    for (int i = 0; i < SD_NSTAGE; ++i) mbar_init(sBar + 8 * i, 1);
+    mbar_init(kBar, 1);
+    mbar_init(vBar, 1);
     *abort_flag = 0;
     fence_mbar_init();
-    int row = -1, row_n = -1;
-    for (int H = 0; H < SD_NSTAGE && H < nhalves; ++H) {
-      if (H / SD_PARTS != row_n) {
-        row_n = H / SD_PARTS;
-        row = ring_row(row_n);
-      }
-      issue(H, row);
-      issued = H;
-    }
+    const int row = ring_row(0);
+    issue_k(row);
+    issue_v(row);
+    issued_k = issued_v = 0;
   }
   for (int n = tid; n < nmine && n < SD_MAX_UNITS; n += SD_THREADS) sRow[n] = ring_row(n);
   for (int h = tid; h < a.hq; h += SD_THREADS) sSink[h] = a.sinks[h] * LOG2E;
@@ -208,6 +207,7 @@ __global__ void __launch_bounds__(SD_THREADS, SD_CTAS)
   __syncthreads();
 
   const int qr = lane >> 2;  // this thread's MMA rows: qr and qr + 8
+  const int r0 = SD_SPW * warp;  // this warp's ring slots in phase 1
   bool alive = true;
   for (int n = 0; n < nmine && alive; ++n) {
     const int u = unit_id(n);
@@ -221,48 +221,106 @@ __global__ void __launch_bounds__(SD_THREADS, SD_CTAS)
     uint16_t *orow = a.out + ((long long)b * a.hq + (long long)kv * G) * DV;
     const uint8_t *sQ = g + SD_OFF_Q + (n & 1) * SD_QTILE;
     const int32_t *sTag = reinterpret_cast<const int32_t *>(g + SD_OFF_TAG) + (n & 1) * WIN;
-
-    // Running softmax state of this thread's two rows and its O columns.  The
-    // sink starts the running maximum and contributes e^{sink - M} = 1.
+    // The softmax state of this thread's two rows starts at the sink: it is
+    // the running maximum and contributes e^{sink - M} = 1 to the sum.
     const float sk0 = qr < G ? sSink[kv * G + qr] : NEG_INF;
     const float sk1 = qr + 8 < G ? sSink[kv * G + qr + 8] : NEG_INF;
-    float M0 = sk0, M1 = sk1;
-    float L0 = qr < G ? 1.f : 0.f, L1 = qr + 8 < G ? 1.f : 0.f;
-    float O[2][4];
+    float S[SD_NT][4];
+
+    if (!__syncthreads_and(mbar_wait(kBar, (uint32_t)n & 1u, abort_flag))) {
+      alive = false;
+      break;
+    }
+    if (ok) {
+      // Phase 1: warp w: S = Q K^T for slots 16w .. 16w+15; slots whose tag is
+      // outside (p - 128, p] are masked; row maxima.
+      uint32_t qf[12][4];
+      load_q_frags(sQ, lane, qf);
 #pragma unroll
-    for (int j = 0; j < 2; ++j) O[j][0] = O[j][1] = O[j][2] = O[j][3] = 0.f;
-    uint32_t qf[12][4];
-    if (ok) load_q_frags(sQ, lane, qf);
-
-    for (int h = 0; h < SD_PARTS; ++h) {
-      const int H = SD_PARTS * n + h;
-      const int st = H % SD_NSTAGE;
-      const bool landed =
-          __syncthreads_and(mbar_wait(sBar + 8 * st, (uint32_t)(H / SD_NSTAGE) & 1u, abort_flag));
-      if (!landed) {
-        alive = false;
-        break;
+      for (int j = 0; j < SD_NT; ++j) S[j][0] = S[j][1] = S[j][2] = S[j][3] = 0.f;
+      const uint32_t kb = smem_u32(sK);
+#pragma unroll
+      for (int j = 0; j < SD_NT; ++j) {
+        const int row = r0 + 8 * j + (lane & 7);
+        const int csel = lane >> 3;  // an x4 load covers chunks 2kk .. 2kk+3 (two k-steps)
+#pragma unroll
+        for (int kk = 0; kk < 12; kk += 2) {
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4(kb + swrow<3>(row, 2 * kk + csel), b0, b1, b2, b3);
+          mma_bf16(S[j], qf[kk], b0, b1);
+          mma_bf16(S[j], qf[kk + 1], b2, b3);
+        }
       }
-      // Every half before H is finished: refill the stage of half H - 1.
-      if (tid == 0 && issued + 1 < nhalves && issued + 1 < H + SD_NSTAGE) {
-        const int H2 = issued + 1;
-        const int n2 = H2 / SD_PARTS;
-        fence_proxy_async_smem();  // generic writes to that stage (zeroed rows) before the TMA writes
-        issue(H2, n2 < SD_MAX_UNITS ? sRow[n2] : ring_row(n2));
-        issued = H2;
+#pragma unroll
+      for (int j = 0; j < SD_NT; ++j)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int sp = sTag[r0 + 8 * j + 2 * (lane & 3) + (e & 1)];
+          const bool in = sp >= 0 && sp <= p && sp > p - WIN;
+          S[j][e] = in ? S[j][e] * a.scale_log2 : NEG_INF;
+        }
+      float x0 = NEG_INF, x1 = NEG_INF;
+#pragma unroll
+      for (int j = 0; j < SD_NT; ++j) {
+        x0 = fmaxf(x0, fmaxf(S[j][0], S[j][1]));
+        x1 = fmaxf(x1, fmaxf(S[j][2], S[j][3]));
       }
-      if (!ok) continue;
-      uint8_t *sK = g + st * SD_HSTAGE;
-      uint8_t *sV = sK + SD_HK;
-      const int slot0 = SD_HALF * h;  // first ring slot of this half
-
-      // Phase 1: warp w takes slots slot0 + SPW*w .. +SPW-1.  Stale slots (tag
-      // outside (p - 128, p]) are masked, and their V rows zeroed so that
-      // stale bytes cannot reach the product (0 * NaN is not 0).
-      const int r0 = SD_SPW * warp;  // row within the part
+      x0 = fmaxf(x0, __shfl_xor_sync(0xffffffffu, x0, 1));
+      x0 = fmaxf(x0, __shfl_xor_sync(0xffffffffu, x0, 2));
+      x1 = fmaxf(x1, __shfl_xor_sync(0xffffffffu, x1, 1));
+      x1 = fmaxf(x1, __shfl_xor_sync(0xffffffffu, x1, 2));
+      if ((lane & 3) == 0) {
+        sMax[warp * 16 + qr] = x0;
+        sMax[warp * 16 + qr + 8] = x1;
+      }
+    }
+    __syncthreads();
+    // Every warp is done with this unit's K: the next unit's K rows come in
+    // while this unit's P.V runs.
+    if (tid == 0 && has_next) {
+      fence_proxy_async_smem();
+      issue_k(row_of(n + 1));
+      issued_k = n + 1;
+    }
+    float M0 = sk0, M1 = sk1;
+    if (ok) {
+      // Phase 2: the row maximum over all slots and the sink, P = e^{s - M}
+      // (bf16) and row sums.
+#pragma unroll
+      for (int w = 0; w < SD_WARPS; ++w) {
+        M0 = fmaxf(M0, sMax[w * 16 + qr]);
+        M1 = fmaxf(M1, sMax[w * 16 + qr + 8]);
+      }
+      float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+      for (int j = 0; j < SD_NT; ++j) {
+        const float p0 = ex2(S[j][0] - M0), p1 = ex2(S[j][1] - M0);
+        const float p2 = ex2(S[j][2] - M1), p3 = ex2(S[j][3] - M1);
+        s0 += p0 + p1;
+        s1 += p2 + p3;
+        const int k0 = r0 + 8 * j + 2 * (lane & 3);  // P tile [16 rows][128 slots], chunks swizzled by row
+        *reinterpret_cast<uint32_t *>(sP + swz<WIN>(qr, k0 >> 3) + (k0 & 7) * 2) = pack_bf16(p0, p1);
+        *reinterpret_cast<uint32_t *>(sP + swz<WIN>(qr + 8, k0 >> 3) + (k0 & 7) * 2) = pack_bf16(p2, p3);
+      }
+      s0 += __shfl_xor_sync(0xffffffffu, s0, 1);
+      s0 += __shfl_xor_sync(0xffffffffu, s0, 2);
+      s1 += __shfl_xor_sync(0xffffffffu, s1, 1);
+      s1 += __shfl_xor_sync(0xffffffffu, s1, 2);
+      if ((lane & 3) == 0) {
+        sSum[warp * 16 + qr] = s0;
+        sSum[warp * 16 + qr + 8] = s1;
+      }
+    }
+    if (!__syncthreads_and(mbar_wait(vBar, (uint32_t)n & 1u, abort_flag))) {
+      alive = false;
+      break;
+    }
+    if (ok) {
+      // V rows of stale slots are zeroed so that their bytes cannot reach the
+      // product (P is 0 there, but 0 * NaN is not 0).
       bool valid = false;
       if (lane < SD_SPW) {
-        const int sp = sTag[slot0 + r0 + lane];
+        const int sp = sTag[r0 + lane];
         valid = sp >= 0 && sp <= p && sp > p - WIN;
       }
       unsigned bad = __ballot_sync(0xffffffffu, !valid) & ((1u << SD_SPW) - 1u);
@@ -271,115 +329,33 @@ __global__ void __launch_bounds__(SD_THREADS, SD_CTAS)
         bad &= bad - 1;
         if (lane < 16) *reinterpret_cast<uint4 *>(sV + swrow<2>(r, lane)) = make_uint4(0, 0, 0, 0);
       }
-      float S[SD_NT][4];
-#pragma unroll
-      for (int j = 0; j < SD_NT; ++j) S[j][0] = S[j][1] = S[j][2] = S[j][3] = 0.f;
-      {
-        const uint32_t kb = smem_u32(sK);
-#pragma unroll
-        for (int j = 0; j < SD_NT; ++j) {
-          const int row = r0 + 8 * j + (lane & 7);
-          const int csel = lane >> 3;  // an x4 load covers chunks 2kk .. 2kk+3 (two k-steps)
-#pragma unroll
-          for (int kk = 0; kk < 12; kk += 2) {
-            uint32_t b0, b1, b2, b3;
-            ldsm_x4(kb + swrow<3>(row, 2 * kk + csel), b0, b1, b2, b3);
-            mma_bf16(S[j], qf[kk], b0, b1);
-            mma_bf16(S[j], qf[kk + 1], b2, b3);
-          }
-        }
-      }
-#pragma unroll
-      for (int j = 0; j < SD_NT; ++j)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int slot = slot0 + r0 + 8 * j + 2 * (lane & 3) + (e & 1);
-          const int sp = sTag[slot];
-          const bool in = sp >= 0 && sp <= p && sp > p - WIN;
-          S[j][e] = in ? S[j][e] * a.scale_log2 : NEG_INF;
-        }
-      {
-        float x0 = NEG_INF, x1 = NEG_INF;
-#pragma unroll
-        for (int j = 0; j < SD_NT; ++j) {
-          x0 = fmaxf(x0, fmaxf(S[j][0], S[j][1]));
-          x1 = fmaxf(x1, fmaxf(S[j][2], S[j][3]));
-        }
-        x0 = fmaxf(x0, __shfl_xor_sync(0xffffffffu, x0, 1));
-        x0 = fmaxf(x0, __shfl_xor_sync(0xffffffffu, x0, 2));
-        x1 = fmaxf(x1, __shfl_xor_sync(0xffffffffu, x1, 1));
-        x1 = fmaxf(x1, __shfl_xor_sync(0xffffffffu, x1, 2));
-        if ((lane & 3) == 0) {
-          sMax[warp * 16 + qr] = x0;
-          sMax[warp * 16 + qr + 8] = x1;
-        }
-      }
-      __syncthreads();
-      // Phase 2: new running maximum, P = e^{s - M} (bf16) and row sums.
-      float N0 = M0, N1 = M1;
-#pragma unroll
-      for (int w = 0; w < SD_WARPS; ++w) {
-        N0 = fmaxf(N0, sMax[w * 16 + qr]);
-        N1 = fmaxf(N1, sMax[w * 16 + qr + 8]);
-      }
-      const float c0 = N0 == NEG_INF ? 0.f : N0, c1 = N1 == NEG_INF ? 0.f : N1;
-      const float f0 = ex2(M0 - c0), f1 = ex2(M1 - c1);  // rescale of the old state (M = -inf gives 0)
-      {
-        float s0 = 0.f, s1 = 0.f;
-#pragma unroll
-        for (int j = 0; j < SD_NT; ++j) {
-          const float p0 = ex2(S[j][0] - c0), p1 = ex2(S[j][1] - c0);
-          const float p2 = ex2(S[j][2] - c1), p3 = ex2(S[j][3] - c1);
-          s0 += p0 + p1;
-          s1 += p2 + p3;
-          const int k0 = r0 + 8 * j + 2 * (lane & 3);  // P tile [16 rows][part slots], chunks swizzled by row
-          *reinterpret_cast<uint32_t *>(sP + swz<SD_HALF>(qr, k0 >> 3) + (k0 & 7) * 2) = pack_bf16(p0, p1);
-          *reinterpret_cast<uint32_t *>(sP + swz<SD_HALF>(qr + 8, k0 >> 3) + (k0 & 7) * 2) = pack_bf16(p2, p3);
-        }
-        s0 += __shfl_xor_sync(0xffffffffu, s0, 1);
-        s0 += __shfl_xor_sync(0xffffffffu, s0, 2);
-        s1 += __shfl_xor_sync(0xffffffffu, s1, 1);
-        s1 += __shfl_xor_sync(0xffffffffu, s1, 2);
-        if ((lane & 3) == 0) {
-          sSum[warp * 16 + qr] = s0;
-          sSum[warp * 16 + qr + 8] = s1;
-        }
-      }
-      __syncthreads();
-      // Phase 3: warp w's value columns 16w..16w+15 over the half's 64 slots.
-      L0 *= f0;
-      L1 *= f1;
-#pragma unroll
-      for (int w = 0; w < SD_WARPS; ++w) {
-        L0 += sSum[w * 16 + qr];
-        L1 += sSum[w * 16 + qr + 8];
-      }
-#pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        O[j][0] *= f0;
-        O[j][1] *= f0;
-        O[j][2] *= f1;
-        O[j][3] *= f1;
-      }
-      M0 = N0;
-      M1 = N1;
-      {
-        const uint32_t pb = smem_u32(sP), vb = smem_u32(sV);
-        const int vrow = (lane & 7) + (((lane >> 3) & 1) << 3);
-        const int vch = 2 * warp + (lane >> 4);
-#pragma unroll
-        for (int ks = 0; ks < SD_HALF / 16; ++ks) {
-          uint32_t af[4], b0, b1, b2, b3;
-          ldsm_x4(pb + swz<SD_HALF>(lane & 15, 2 * ks + (lane >> 4)), af[0], af[1], af[2], af[3]);
-          ldsm_x4_t(vb + swrow<2>(16 * ks + vrow, vch), b0, b1, b2, b3);
-          mma_bf16(O[0], af, b0, b1);
-          mma_bf16(O[1], af, b2, b3);
-        }
-      }
     }
-    if (!alive) break;
+    __syncthreads();
     if (ok) {
-      const float i0 = L0 > 0.f ? 1.f / L0 : 0.f, i1 = L1 > 0.f ? 1.f / L1 : 0.f;
+      // Phase 3: warp w: O[:, 16w..16w+15] = P V over the 128 slots, divided
+      // by the sum (in which the sink counts once).
+      const float L0 = (qr < G ? ex2(sk0 - M0) : 0.f), L1 = (qr + 8 < G ? ex2(sk1 - M1) : 0.f);
+      float l0 = L0, l1 = L1;
+#pragma unroll
+      for (int w = 0; w < SD_WARPS; ++w) {
+        l0 += sSum[w * 16 + qr];
+        l1 += sSum[w * 16 + qr + 8];
+      }
+      float O[2][4];
+#pragma unroll
+      for (int j = 0; j < 2; ++j) O[j][0] = O[j][1] = O[j][2] = O[j][3] = 0.f;
+      const uint32_t pb = smem_u32(sP), vb = smem_u32(sV);
+      const int vrow = (lane & 7) + (((lane >> 3) & 1) << 3);
+      const int vch = 2 * warp + (lane >> 4);
+#pragma unroll
+      for (int ks = 0; ks < WIN / 16; ++ks) {
+        uint32_t af[4], b0, b1, b2, b3;
+        ldsm_x4(pb + swz<WIN>(lane & 15, 2 * ks + (lane >> 4)), af[0], af[1], af[2], af[3]);
+        ldsm_x4_t(vb + swrow<2>(16 * ks + vrow, vch), b0, b1, b2, b3);
+        mma_bf16(O[0], af, b0, b1);
+        mma_bf16(O[1], af, b2, b3);
+      }
+      const float i0 = l0 > 0.f ? 1.f / l0 : 0.f, i1 = l1 > 0.f ? 1.f / l1 : 0.f;
       const int dcol = 16 * warp + 2 * (lane & 3);
 #pragma unroll
       for (int j = 0; j < 2; ++j) {
@@ -397,17 +373,12 @@ __global__ void __launch_bounds__(SD_THREADS, SD_CTAS)
       const int nb = (n + 1) & 1;  // that query tile / tag buffer served unit n - 1
       store_unit(nx, tid, g + SD_OFF_Q + nb * SD_QTILE, reinterpret_cast<int32_t *>(g + SD_OFF_TAG) + nb * WIN);
     }
+    fence_proxy_async_smem();  // the zeroed V rows (generic writes) before the next TMA writes there
     __syncthreads();
-    // Every part of unit n is consumed: refill what that frees.
-    if (tid == 0) {
-      const int done = SD_PARTS * (n + 1);  // parts 0 .. done-1 are finished
-      while (issued + 1 < nhalves && issued + 1 < done + SD_NSTAGE) {
-        const int H2 = issued + 1;
-        const int n2 = H2 / SD_PARTS;
-        fence_proxy_async_smem();
-        issue(H2, n2 < SD_MAX_UNITS ? sRow[n2] : ring_row(n2));
-        issued = H2;
-      }
+    // Every warp is done with this unit's V: the next unit's V rows.
+    if (tid == 0 && has_next) {
+      issue_v(row_of(n + 1));
+      issued_v = n + 1;
     }
   }
 
@@ -415,10 +386,10 @@ __global__ void __launch_bounds__(SD_THREADS, SD_CTAS)
     if (tid == 0) {
       flag(a.status, ST_TIMEOUT);
       // Let the loads already issued land before the CTA exits (time bound only).
-      for (int H = issued; H >= 0 && H > issued - SD_NSTAGE; --H) {
-        volatile uint32_t local = 0;
-        mbar_wait(sBar + 8 * (H % SD_NSTAGE), (uint32_t)(H / SD_NSTAGE) & 1u, &local, 1000000000ull);
-      }
+      volatile uint32_t local = 0;
+      if (issued_k >= 0) mbar_wait(kBar, (uint32_t)issued_k & 1u, &local, 1000000000ull);
+      local = 0;
+      if (issued_v >= 0) mbar_wait(vBar, (uint32_t)issued_v & 1u, &local, 1000000000ull);
     }
     __syncthreads();
   }
@@ -434,7 +405,7 @@ cudaError_t launch_swa_decode(const uint16_t *q, const int64_t *pos, const int32
   const long long rows = (long long)ring.num_seqs * hkv * WIN;
   if (rows >= (1LL << 31)) return cudaErrorInvalidValue;
   CUtensorMap mk, mv;
-  if (!make_tma_map_rows3d(&mk, ring.k, rows, DQK, SD_HALF) || !make_tma_map_rows3d(&mv, ring.v, rows, DV, SD_HALF))
+  if (!make_tma_map_rows3d(&mk, ring.k, rows, DQK, WIN) || !make_tma_map_rows3d(&mv, ring.v, rows, DV, WIN))
     return cudaErrorInvalidValue;
   cudaError_t e = ensure_smem_limit(1, (const void *)swa_decode_kernel, SD_SMEM);
   if (e != cudaSuccess) return e;
