@@ -700,6 +700,7 @@ def main():
                                 "graph_ms": round(work.graph_ms[0], 5),
                                 "graph_GB/s": round(work.bytes_swa() / work.graph_ms[0] / 1e6, 1),
                                 "graph_hbm_frac": round(work.bytes_swa() / work.graph_ms[0] / 1e6 / hbm, 4),
+                                "traffic": kernel_traffic("swa_decode_kernel"),
                                 "note": "ms/GB/s: CUDA events around the call inside the timed step (include "
                                         "launch gaps); graph_*: the kernel replayed back to back in a CUDA graph"},
         },
@@ -750,7 +751,8 @@ def main():
             "workload": "65536 tokens x 4 KV heads into the paged pool (RoPE + value scale), CUDA graph replay",
             "ms": round(ams, 4), "bytes": abytes, "GB/s": round(agbs, 1),
             "roofline": with_nominal({"bound": "hbm", "achieved": round(agbs, 1), "peak": hbm, "unit": "GB/s",
-                                      "frac": round(agbs / hbm, 4), "peak_source": peaks_src})}
+                                      "frac": round(agbs / hbm, 4), "peak_source": peaks_src,
+                                  "kernel": "append_kernel", "traffic": kernel_traffic("append_kernel")})}
         res["gpu_launches"] += pw.launches_per_step * psteps
     if rank == 0:
         print(json.dumps(res), flush=True)
@@ -820,7 +822,8 @@ def prefill_only(args, kvr, peaks_d, peaks_src, rank, world):
         "workload": "65536 tokens x 4 KV heads into the paged pool (RoPE + value scale), CUDA graph replay",
         "ms": round(ams, 4), "bytes": abytes, "GB/s": round(agbs, 1),
         "roofline": with_nominal({"bound": "hbm", "achieved": round(agbs, 1), "peak": hbm, "unit": "GB/s",
-                                  "frac": round(agbs / hbm, 4), "peak_source": peaks_src})}
+                                  "frac": round(agbs / hbm, 4), "peak_source": peaks_src,
+                                  "kernel": "append_kernel", "traffic": kernel_traffic("append_kernel")})}
     if rank == 0:
         print(json.dumps(res), flush=True)
 
