@@ -301,3 +301,108 @@ def test_shifted_inputs_have_the_stated_logit_statistics():
     assert abs(logits.mean() + 25.0) < 0.5 and abs(logits.std() - 3.0) < 0.3
     sk = Synth(1000).sinks(20000).numpy()
     assert abs(sk.mean() - 1.0) < 0.02 and abs(sk.std() - 0.5) < 0.02
+
+
+# --------------------------------------------------------------------------- paged windowed pool
+
+def _read_release_example():
+    cfg, table, calls, final = {}, {}, [], {}
+    for line in open(os.path.join(GOLDEN, "pages_release_example.txt")):
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        if line.startswith("table ") or line.startswith("final "):
+            head, vals = line.split(":")
+            (table if line.startswith("table") else final)[int(head.split()[1])] = [int(x) for x in vals.split()]
+        elif line.startswith("call "):
+            f = dict(kv.split("=") for kv in line[5:].split())
+            ints = lambda s: [int(x) for x in s.split(",")] if s else []
+            calls.append((ints(f["seqs"]), ints(f["next_pos"]), ints(f["released"]), ints(f["lo"]), int(f["flags"])))
+        else:
+            k, v = line.split()
+            cfg[k] = int(v)
+    return cfg, [table[s] for s in sorted(table)], calls, [final[s] for s in sorted(final)]
+
+
+def test_release_window_worked_example():
+    from oracle import pages
+    cfg, table, calls, final = _read_release_example()
+    lo, ids, count = [0] * len(table), [], 0
+    for seqs, nxt, want_rel, want_lo, want_flags in calls:
+        table, lo, ids, new_count, flags = pages.release_window(
+            table, cfg["num_blocks"], cfg["block_size"], seqs, nxt, cfg["window"], lo=lo,
+            free_ids=ids, free_count=count, free_cap=cfg["free_cap"])
+        assert ids[count:new_count] == want_rel
+        assert lo == want_lo and flags == want_flags
+        count = new_count
+    assert table == final
+
+
+def _attended_by_later_query(block_index, bs, next_pos, window):
+    """Brute force: does any query at q >= next_pos read a position of the block?"""
+    first, last = block_index * bs, block_index * bs + bs - 1
+    for q in range(next_pos, max(next_pos, last) + 1):
+        for p in range(max(0, q - window + 1), q + 1):
+            if first <= p <= last:
+                return True
+    return False
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_release_window_against_brute_force_windows(seed):
+    # every released block is read by no later query; every kept valid block
+    # at or past lo is read by one (so nothing that could go stays)
+    from oracle import pages
+    rng = np.random.default_rng(seed)
+    S, mb, bs, W = 5, 12, 4, 8
+    nblk = S * mb
+    ids = rng.permutation(nblk)[: S * mb].reshape(S, mb).tolist()
+    for s in range(S):
+        for b in range(mb):
+            if rng.random() < 0.15:
+                ids[s][b] = -1
+    lo = [int(x) for x in rng.integers(0, 3, S)]
+    nxt = [int(x) for x in rng.integers(0, mb * bs + 10, S)]
+    table, lo2, free, cnt, flags = pages.release_window(ids, nblk, bs, list(range(S)), nxt, W, lo=lo)
+    assert flags == 0 and cnt == len(free)
+    freed = set(free)
+    for s in range(S):
+        for b in range(mb):
+            before, after = ids[s][b], table[s][b]
+            if before < 0:
+                assert after == before
+            elif b < lo[s]:
+                assert after == before and before not in freed
+            elif _attended_by_later_query(b, bs, nxt[s], W):
+                assert after == before and before not in freed
+            else:
+                assert after == -1 and before in freed
+        assert lo2[s] >= lo[s]
+    # released ids come in (sequence, block index) order
+    order = [ids[s][b] for s in range(S) for b in range(mb) if ids[s][b] >= 0 and table[s][b] == -1]
+    assert free == order
+
+
+def test_ring_from_pages_equals_appending_in_order():
+    # colibri "System One mode and prompt reuse": the ring after appending
+    # positions 0..E-1 one by one, slot p mod 128 <- row p, tag p
+    from oracle import pages
+    rng = np.random.default_rng(7)
+    hkv, bs, mb = 2, 16, 24
+    nblk = 2 * mb
+    pk = rng.integers(0, 1 << 16, (nblk, hkv, bs, 192), dtype=np.uint16)
+    pv = rng.integers(0, 1 << 16, (nblk, hkv, bs, 128), dtype=np.uint16)
+    table = rng.permutation(nblk).reshape(2, mb).tolist()
+    for end in [0, 1, 77, 128, 129, 300, 383]:
+        k0 = rng.integers(0, 1 << 16, (hkv, 128, 192), dtype=np.uint16)
+        v0 = rng.integers(0, 1 << 16, (hkv, 128, 128), dtype=np.uint16)
+        t0 = np.full(128, -1, dtype=np.int32)
+        wk, wv, wt = k0.copy(), v0.copy(), t0.copy()
+        for p in range(end):
+            b = table[1][p // bs]
+            wk[:, p % 128] = pk[b, :, p % bs]
+            wv[:, p % 128] = pv[b, :, p % bs]
+            wt[p % 128] = p
+        k, v, t, flags = pages.ring_from_pages(pk, pv, table, bs, 1, end, k0, v0, t0)
+        assert flags == 0
+        assert np.array_equal(t, wt) and np.array_equal(k, wk) and np.array_equal(v, wv)
