@@ -66,11 +66,12 @@ enum {
 #define KVR_DEV_BAD_BLOCK 4u  /* a block-table entry outside the pool, or a context past the table */
 #define KVR_DEV_TIMEOUT 8u    /* a kernel gave up waiting on its own pipeline (bounded wait) and returned */
 #define KVR_DEV_BAD_ROWS 16u  /* varlen: cu_rows not non-decreasing within [0, T]; that chunk is skipped */
+#define KVR_DEV_FREE_FULL 32u /* kv_pages_release_window: the free list could not take the released ids */
 
 /* KV storage kinds. */
 enum {
   KVR_LAYOUT_RING = 1,   /* SWA pool: one ring of 128 slots per (sequence, KV head) */
-  KVR_LAYOUT_PAGED = 2,  /* Full pool: pages of block_size positions per KV head */
+  KVR_LAYOUT_PAGED = 2,  /* Full pool (or a windowed layer kept in pages): pages of block_size positions */
   KVR_LAYOUT_LINEAR = 3  /* staging: rows in call order (a prefill chunk) */
 };
 
@@ -82,7 +83,9 @@ enum {
  *        k [num_seqs][Hkv][128][192], v [num_seqs][Hkv][128][128],
  *        slot_pos [num_seqs][128] int32, -1 = empty.  slot_pos is shared by
  *        the KV heads of a sequence and is written by kv_ring_append_rope.
- * PAGED  (the Full KV pool of Xiaomi section 2.1, grown on demand):
+ * PAGED  (the Full KV pool of Xiaomi section 2.1, grown on demand; a
+ *        windowed layer may be kept this way too, its out-of-window pages
+ *        released by kv_pages_release_window):
  *        k [num_blocks][Hkv][block_size][192], v [num_blocks][Hkv][block_size][128],
  *        block_table [num_seqs][max_blocks] int32: position p of sequence s is
  *        row p % block_size of block block_table[s][p / block_size].
@@ -163,6 +166,14 @@ kvr_status kv_ring_append_rope(const kvr_bf16 *k, const kvr_bf16 *v, const int64
  * rounded to bf16); ring: a RING layout; sinks [Hq] fp32 (raw logits, not
  * multiplied by softmax_scale); out [B][Hq][128] bf16.  Hq/Hkv <= 16.
  * The sink is counted once, in the final normalisation.
+ *
+ * `ring` may also be a PAGED layout holding the windowed layer in pages
+ * (gaudi-cookbook "Windowed KV groups": vLLM's paged sliding-window groups):
+ * the keys are positions max(0, p-127)..p of sequence seq[b], read through
+ * its block table; no entry for a position below p-127 rounded down to a
+ * multiple of 16 is read, so pages released by kv_pages_release_window with
+ * next_pos <= p are never touched.  p must be < max_blocks*block_size (else
+ * the row is zeroed and KVR_DEV_BAD_POS set).
  */
 kvr_status swa_sink_decode(const kvr_bf16 *q, const int64_t *pos, const int32_t *seq, int32_t B,
                            int32_t Hq, const kvr_kv_layout *ring, const float *sinks,
@@ -212,6 +223,61 @@ kvr_status kv_ring_snapshot(const kvr_kv_layout *ring, const int32_t *seqs, int3
                             kvr_bf16 *v_snap, int32_t *tags_snap, void *stream);
 kvr_status kv_ring_restore(const kvr_kv_layout *ring, const int32_t *seqs, int32_t n, const kvr_bf16 *k_snap,
                            const kvr_bf16 *v_snap, const int32_t *tags_snap, void *stream);
+
+/*
+ * Out-of-window release of a windowed layer kept in pages (Xiaomi
+ * "Full-Pipeline Inference Optimization", section 2.1: the SWA pool is kept
+ * at window size -- the end of each prefill chunk, the end of a request and
+ * every N decoded tokens release the SWA KV that has left the window;
+ * gaudi-cookbook "Windowed KV groups": the out-of-window blocks are freed).
+ * A query at q reads positions q-window+1..q, so once the next query of a
+ * sequence is at P, table entries bi with (bi+1)*block_size <= P-window+1
+ * hold only positions no later query reads.
+ *   block_table [num_seqs][max_blocks] int32 (device, read and written);
+ *   seqs [n] int32, next_pos [n] int64 (device): entry i names sequence
+ *     seqs[i] and the position of its next query; no two entries of one call
+ *     may name the same sequence; next_pos must not decrease from one call
+ *     to the next for a sequence (release with the committed position, not
+ *     one a rejected draft could roll back);
+ *   lo [num_seqs] int32 (device, read and written) or NULL: entries below
+ *     lo[s] were handled by earlier calls and are not looked at again; the
+ *     call sets lo[s] = max(lo[s], bound) (keep it 0 for a new sequence);
+ *   free_ids [free_cap] int32, free_count [1] int32 (device): the free list.
+ * Every entry in [max(lo[s], 0), bound) holding a block id in
+ * [0, num_blocks) is released: the id is written at free_ids[*free_count +
+ * k] and the entry set to -1; *free_count grows by the number released.
+ * Ids are appended in the order (call entry i, block index).  Entries
+ * holding -1 are skipped; ids >= num_blocks are left in place and set
+ * KVR_DEV_BAD_BLOCK; a sequence id outside [0, num_seqs) sets
+ * KVR_DEV_BAD_SEQ.  If the ids the whole call would release do not fit in
+ * free_cap, the call changes nothing and sets KVR_DEV_FREE_FULL.  One CTA;
+ * the work per call is the entries between lo and the bound.  n = 0 is a
+ * no-op.
+ */
+kvr_status kv_pages_release_window(int32_t *block_table, int32_t num_seqs, int32_t max_blocks,
+                                   int32_t block_size, int32_t num_blocks, const int32_t *seqs,
+                                   const int64_t *next_pos, int32_t *lo, int32_t n, int32_t window,
+                                   int32_t *free_ids, int32_t *free_count, int32_t free_cap, void *stream);
+
+/*
+ * Ring from pages (colibri "System One mode and prompt reuse": position p
+ * lives in ring slot p mod 128, and the ring records the position each slot
+ * holds).  For entry i, ring sequence dst_seqs[i] receives the window of
+ * paged sequence src_seqs[i] that ends before position end[i]: slot c gets
+ * the row of the largest position p < end[i] with p mod 128 == c (K and V,
+ * bit for bit) and slot_pos = p; a slot with no such position (end[i] <= c)
+ * gets slot_pos -1 and keeps its rows.  The result equals the ring that
+ * appending positions 0..end[i]-1 in order would leave, so the ring-based
+ * calls (swa_sink_prefill_chunk, swa_sink_prefill_varlen) can continue a
+ * sequence kept in pages.  A needed position whose block entry is not a
+ * block id of the pool gets slot_pos -1 and sets KVR_DEV_BAD_BLOCK; a
+ * sequence id outside either layout sets KVR_DEV_BAD_SEQ and the entry is
+ * skipped.  pages: PAGED; ring: RING with the same num_kv_heads; src_seqs,
+ * dst_seqs [n] int32 and end [n] int64 are device arrays; no two entries
+ * may name the same dst sequence.  n = 0 is a no-op.
+ */
+kvr_status kv_ring_gather_pages(const kvr_kv_layout *pages, const kvr_kv_layout *ring, const int32_t *src_seqs,
+                                const int32_t *dst_seqs, const int64_t *end, int32_t n, void *stream);
 
 /*
  * Size of the fixed device scratch array used by full_attn_decode_noalloc:

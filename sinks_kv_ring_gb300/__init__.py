@@ -38,7 +38,7 @@ __all__ = [
 
 DQK, DV, DROT, WINDOW = 192, 128, 64, 128
 LAYOUT_RING, LAYOUT_PAGED, LAYOUT_LINEAR = 1, 2, 3
-DEV_BAD_POS, DEV_BAD_SEQ, DEV_BAD_BLOCK, DEV_TIMEOUT, DEV_BAD_ROWS = 1, 2, 4, 8, 16
+DEV_BAD_POS, DEV_BAD_SEQ, DEV_BAD_BLOCK, DEV_TIMEOUT, DEV_BAD_ROWS, DEV_FREE_FULL = 1, 2, 4, 8, 16, 32
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libkvring.so")
@@ -112,6 +112,10 @@ def lib():
                 L.swa_sink_prefill_varlen.restype = ctypes.c_int
                 L.swa_sink_prefill_varlen.argtypes = [p, p, p, p, i32, i64, i32, p, p, p, p, i64, f32, p,
                                                       ctypes.c_size_t, p, p]
+                L.kv_pages_release_window.restype = ctypes.c_int
+                L.kv_pages_release_window.argtypes = [p, i32, i32, i32, i32, p, p, p, i32, i32, p, p, i32, p]
+                L.kv_ring_gather_pages.restype = ctypes.c_int
+                L.kv_ring_gather_pages.argtypes = [p, p, p, p, p, i32, p]
                 _lib = L
     return _lib
 
@@ -443,6 +447,42 @@ def kv_ring_snapshot(ring, seqs, snap, stream=None):
 def kv_ring_restore(ring, seqs, snap, stream=None):
     """Copy snapshot buffers back into the rings of sequences `seqs`."""
     _ring_copy(lib().kv_ring_restore, ring, seqs, snap, stream)
+
+
+def kv_pages_release_window(pool, seqs, next_pos, free_ids, free_count, lo=None, window=WINDOW, stream=None):
+    """Release the pages of a windowed layer kept in `pool` (a PagedLayout)
+    that no query at or after next_pos[i] reads: their ids are appended to
+    free_ids (int32 [cap]) at free_count (int32 [1], advanced), their
+    block-table entries set to -1, and lo (int32 [num_seqs], optional)
+    advanced.  Everything stays on the device."""
+    _want(seqs, "seqs", torch.int32, 1)
+    _want(next_pos, "next_pos", torch.int64, 1)
+    _want(free_ids, "free_ids", torch.int32, 1)
+    _want(free_count, "free_count", torch.int32, 1)
+    if lo is not None:
+        _want(lo, "lo", torch.int32, 1)
+        if lo.shape[0] != pool.num_seqs:
+            raise ValueError("lo must have one entry per sequence of the pool")
+    n = seqs.shape[0]
+    if next_pos.shape[0] != n or free_count.shape[0] != 1:
+        raise ValueError("seqs/next_pos/free_count shapes disagree")
+    _check(lib().kv_pages_release_window(_ptr(pool.block_table), pool.num_seqs, pool.max_blocks, pool.block_size,
+                                         pool.num_blocks, _ptr(seqs), _ptr(next_pos), _ptr(lo), n, int(window),
+                                         _ptr(free_ids), _ptr(free_count), free_ids.shape[0], _stream(stream)))
+
+
+def kv_ring_gather_pages(pages, ring, src_seqs, dst_seqs, end, stream=None):
+    """Fill ring rows dst_seqs[i] with the window of paged sequence
+    src_seqs[i] that ends before position end[i] (slot p mod 128 <- row p)."""
+    _want(src_seqs, "src_seqs", torch.int32, 1)
+    _want(dst_seqs, "dst_seqs", torch.int32, 1)
+    _want(end, "end", torch.int64, 1)
+    n = src_seqs.shape[0]
+    if dst_seqs.shape[0] != n or end.shape[0] != n:
+        raise ValueError("src_seqs/dst_seqs/end shapes disagree")
+    pc, rc = pages.c(), ring.c()
+    _check(lib().kv_ring_gather_pages(ctypes.byref(pc), ctypes.byref(rc), _ptr(src_seqs), _ptr(dst_seqs), _ptr(end),
+                                      n, _stream(stream)))
 
 
 def device_status(reset: bool = True) -> int:

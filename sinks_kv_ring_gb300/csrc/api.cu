@@ -211,8 +211,10 @@ kvr_status swa_sink_decode(const kvr_bf16 *q, const int64_t *pos, const int32_t 
                            const kvr_kv_layout *ring, const float *sinks, const float *rope_cos_sin,
                            int64_t max_pos, float softmax_scale, kvr_bf16 *out, void *stream) {
   if (B < 0) return fail(KVR_EINVAL, "B %d", B);
-  kvr_status s = check_layout(ring, KVR_LAYOUT_RING, "ring");
+  kvr_status s = check_layout(ring, 0, "ring");
   if (s) return s;
+  if (ring->kind != KVR_LAYOUT_RING && ring->kind != KVR_LAYOUT_PAGED)
+    return fail(KVR_EINVAL, "ring: layout kind %d, expected RING or PAGED", ring->kind);
   if ((s = check_heads(Hq, ring->num_kv_heads, 16))) return s;
   if (Hq > 1024) return fail(KVR_EUNSUPPORTED, "Hq %d > 1024", Hq);
   if ((s = check_table(rope_cos_sin, max_pos))) return s;
@@ -222,8 +224,12 @@ kvr_status swa_sink_decode(const kvr_bf16 *q, const int64_t *pos, const int32_t 
   unsigned *st = nullptr;
   cudaError_t e = status_ptr(&st);
   if (e != cudaSuccess) return cuda_fail(e, "swa_sink_decode");
-  e = kvr::launch_swa_decode(q, pos, seq, B, Hq, view(*ring), sinks, rope_cos_sin, max_pos, softmax_scale, out,
-                             st, as_stream(stream));
+  if (ring->kind == KVR_LAYOUT_PAGED)
+    e = kvr::launch_swa_decode_paged(q, pos, seq, B, Hq, view(*ring), sinks, rope_cos_sin, max_pos, softmax_scale,
+                                     out, st, as_stream(stream));
+  else
+    e = kvr::launch_swa_decode(q, pos, seq, B, Hq, view(*ring), sinks, rope_cos_sin, max_pos, softmax_scale, out,
+                               st, as_stream(stream));
   if (e != cudaSuccess) return cuda_fail(e, "swa_sink_decode launch");
   return ok();
 }
@@ -428,6 +434,46 @@ kvr_status swa_sink_prefill_varlen(const kvr_bf16 *q, const int32_t *cu_rows, co
 kvr_status kv_ring_restore(const kvr_kv_layout *ring, const int32_t *seqs, int32_t n, const kvr_bf16 *k_snap,
                            const kvr_bf16 *v_snap, const int32_t *tags_snap, void *stream) {
   return ring_copy("kv_ring_restore", ring, seqs, n, k_snap, v_snap, tags_snap, true, stream);
+}
+
+kvr_status kv_pages_release_window(int32_t *block_table, int32_t num_seqs, int32_t max_blocks, int32_t block_size,
+                                   int32_t num_blocks, const int32_t *seqs, const int64_t *next_pos, int32_t *lo,
+                                   int32_t n, int32_t window, int32_t *free_ids, int32_t *free_count,
+                                   int32_t free_cap, void *stream) {
+  if (n < 0) return fail(KVR_EINVAL, "kv_pages_release_window: n %d", n);
+  if (num_seqs < 1 || max_blocks < 1 || num_blocks < 1 || block_size < 1)
+    return fail(KVR_EINVAL, "kv_pages_release_window: num_seqs/max_blocks/num_blocks/block_size must be >= 1");
+  if (window < 1) return fail(KVR_EINVAL, "kv_pages_release_window: window %d", window);
+  if (free_cap < 0) return fail(KVR_EINVAL, "kv_pages_release_window: free_cap %d", free_cap);
+  if (!block_table || !free_count) return fail(KVR_EINVAL, "kv_pages_release_window: block_table/free_count is NULL");
+  if (n == 0) return ok();
+  if (!seqs || !next_pos) return fail(KVR_EINVAL, "kv_pages_release_window: seqs/next_pos is NULL");
+  if (free_cap > 0 && !free_ids) return fail(KVR_EINVAL, "kv_pages_release_window: free_ids is NULL");
+  unsigned *st = nullptr;
+  cudaError_t e = status_ptr(&st);
+  if (e != cudaSuccess) return cuda_fail(e, "kv_pages_release_window");
+  e = kvr::launch_pages_release(block_table, num_seqs, max_blocks, block_size, num_blocks, seqs, next_pos, lo, n,
+                                window, free_ids, free_count, free_cap, st, as_stream(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "kv_pages_release_window launch");
+  return ok();
+}
+
+kvr_status kv_ring_gather_pages(const kvr_kv_layout *pages, const kvr_kv_layout *ring, const int32_t *src_seqs,
+                                const int32_t *dst_seqs, const int64_t *end, int32_t n, void *stream) {
+  kvr_status s = check_layout(pages, KVR_LAYOUT_PAGED, "pages");
+  if (s) return s;
+  if ((s = check_layout(ring, KVR_LAYOUT_RING, "ring"))) return s;
+  if (pages->num_kv_heads != ring->num_kv_heads)
+    return fail(KVR_EINVAL, "pages have %d KV heads, ring %d", pages->num_kv_heads, ring->num_kv_heads);
+  if (n < 0) return fail(KVR_EINVAL, "kv_ring_gather_pages: n %d", n);
+  if (n == 0) return ok();
+  if (!src_seqs || !dst_seqs || !end) return fail(KVR_EINVAL, "kv_ring_gather_pages: src_seqs/dst_seqs/end is NULL");
+  unsigned *st = nullptr;
+  cudaError_t e = status_ptr(&st);
+  if (e != cudaSuccess) return cuda_fail(e, "kv_ring_gather_pages");
+  e = kvr::launch_ring_gather(view(*pages), view(*ring), src_seqs, dst_seqs, end, n, st, as_stream(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "kv_ring_gather_pages launch");
+  return ok();
 }
 
 }  // extern "C"

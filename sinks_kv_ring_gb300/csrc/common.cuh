@@ -22,6 +22,7 @@ constexpr unsigned ST_BAD_POS = 1u;
 constexpr unsigned ST_BAD_SEQ = 2u;
 constexpr unsigned ST_BAD_BLOCK = 4u;
 constexpr unsigned ST_BAD_ROWS = 16u;
+constexpr unsigned ST_FREE_FULL = 32u;
 
 __device__ __forceinline__ void flag(unsigned *status, unsigned bits) {
   if (status) atomicOr(status, bits);

@@ -10,6 +10,12 @@
 // into swizzled shared memory, and the two small products per key tile run
 // on the bf16 tensor cores (mma.sync m16n8k16, fp32 accumulate) with the G
 // query heads of one KV head as the 16 rows of the MMA.
+//
+// The same split kernel serves a windowed layer kept in pages (the paged SWA
+// pool of Xiaomi section 2.1; gaudi-cookbook "Windowed KV groups"): the key
+// range starts at p - 127 (rounded down to a 16-key subtile, the extra keys
+// masked), one split covers it, and the kernel normalises directly with the
+// sink in the denominator (colibri "What the engine implements").
 #include "launch.h"
 #include "warp_attn.cuh"
 
@@ -35,7 +41,8 @@ __global__ void __launch_bounds__(FD_WARPS * 32, 2)
                        const int32_t *__restrict__ seq, int B, int hq, int G, KvView pool,
                        const float *__restrict__ table, int64_t max_pos, float scale_log2,
                        long long max_ctx, int splits, int split_len, float *__restrict__ part_ml,
-                       float *__restrict__ part_o, unsigned *status) {
+                       float *__restrict__ part_o, unsigned *status, int window,
+                       const float *__restrict__ sinks, uint16_t *__restrict__ out_direct) {
   extern __shared__ __align__(128) uint8_t smem[];
   uint8_t *sQ = smem;
   uint8_t *sStage = smem + 16 * DQK * 2;
@@ -54,9 +61,17 @@ __global__ void __launch_bounds__(FD_WARPS * 32, 2)
     if (bad_pos || bad_seq) {
       if (split == 0 && kv == 0 && tid == 0)
         flag(status, (bad_pos ? ST_BAD_POS : 0u) | (bad_seq ? ST_BAD_SEQ : 0u));
-      continue;  // the combine writes zeros for this sequence
+      if (out_direct && split == 0) {  // direct mode writes the zero rows itself
+        uint16_t *o = out_direct + ((long long)b * hq + (long long)kv * G) * DV;
+        for (int e = tid; e < G * DV; e += blockDim.x) o[e] = 0;
+      }
+      continue;  // otherwise the combine writes zeros for this sequence
     }
-    const long long key_lo = (long long)split * split_len;
+    // window: keys p-window+1..p; the range starts on a 16-key subtile boundary
+    // (a subtile never straddles a block); rows below key_min are zero-filled
+    // instead of read and their scores masked
+    const long long key_min = window > 0 ? max(0LL, p - window + 1) : 0;
+    const long long key_lo = (key_min & ~15LL) + (long long)split * split_len;
     if (key_lo > p) continue;
     const long long key_hi = min(key_lo + split_len, p + 1);
 
@@ -90,13 +105,13 @@ __global__ void __launch_bounds__(FD_WARPS * 32, 2)
 #pragma unroll
       for (int u = 0; u < 12; ++u) {
         const int c = lane + 32 * u, r = c / 24, ch = c % 24;
-        const int nb = (blk_ok && key0 + r < key_hi) ? 16 : 0;
+        const int nb = (blk_ok && key0 + r < key_hi && key0 + r >= key_min) ? 16 : 0;
         cp_async16(kb + swz<DQK>(r, ch), kg + r * DQK + ch * 8, nb);
       }
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
         const int c = lane + 32 * u, r = c >> 4, ch = c & 15;
-        const int nb = (blk_ok && key0 + r < key_hi) ? 16 : 0;
+        const int nb = (blk_ok && key0 + r < key_hi && key0 + r >= key_min) ? 16 : 0;
         cp_async16(vb + swz<DV>(r, ch), vg + r * DV + ch * 8, nb);
       }
     };
@@ -122,7 +137,7 @@ __global__ void __launch_bounds__(FD_WARPS * 32, 2)
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const long long key = key0 + 8 * j + 2 * (lane & 3) + (e & 1);
-          S[j][e] = (blk_ok && key < key_hi) ? S[j][e] * scale_log2 : NEG_INF;
+          S[j][e] = (blk_ok && key < key_hi && key >= key_min) ? S[j][e] * scale_log2 : NEG_INF;
         }
       softmax_update(S, m0, m1, l0, l1, O);
       pv_16keys(S, kb + FD_SUB_K, 0, lane, O);
@@ -136,6 +151,34 @@ __global__ void __launch_bounds__(FD_WARPS * 32, 2)
     stash_warp_state(mml + warp * 32, mo + warp * 16 * MO_STRIDE, lane, m0, m1, l0, l1, O);
     __syncthreads();
 
+    if (out_direct) {
+      // one split holds the whole window: normalise here, the sink joining
+      // the denominator only (its numerator is zero)
+      uint16_t *o = out_direct + ((long long)b * hq + (long long)kv * G) * DV;
+      for (int g = 0; g < G; ++g) {
+        const float sl = sinks[kv * G + g] * LOG2E;
+        float M = sl;
+#pragma unroll
+        for (int ww = 0; ww < FD_WARPS; ++ww) M = fmaxf(M, mml[ww * 32 + g * 2]);
+        float L = ex2(sl - M);
+#pragma unroll
+        for (int ww = 0; ww < FD_WARPS; ++ww) {
+          const float mw = mml[ww * 32 + g * 2];
+          L += mml[ww * 32 + g * 2 + 1] * (mw == NEG_INF ? 0.f : ex2(mw - M));
+        }
+        const float inv = 1.f / L;
+        for (int d = tid; d < DV; d += blockDim.x) {
+          float acc = 0.f;
+#pragma unroll
+          for (int ww = 0; ww < FD_WARPS; ++ww) {
+            const float mw = mml[ww * 32 + g * 2];
+            acc += mo[(ww * 16 + g) * MO_STRIDE + d] * (mw == NEG_INF ? 0.f : ex2(mw - M));
+          }
+          o[g * DV + d] = f2bf(acc * inv);
+        }
+      }
+      continue;
+    }
     float *pml = part_ml + w * G * 2;
     float *po = part_o + w * G * DV;
     for (int g = 0; g < G; ++g) {
@@ -252,11 +295,29 @@ cudaError_t launch_full_decode(const uint16_t *q, const int64_t *pos, const int3
   if (grid > (long long)items) grid = (long long)items;
   full_decode_kernel<<<(unsigned)grid, FD_WARPS * 32, FD_SMEM, st>>>(
       q, pos, seq, B, hq, G, pool, table, max_pos, softmax_scale * LOG2E, max_ctx, pl.splits, pl.split_len,
-      part_ml, part_o, status);
+      part_ml, part_o, status, 0, nullptr, nullptr);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   full_combine_kernel<<<B * hkv, 256, 0, st>>>(pos, seq, hq, G, hkv, pool.num_seqs, max_pos, max_ctx, pl.splits,
                                                pl.split_len, part_ml, part_o, out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_swa_decode_paged(const uint16_t *q, const int64_t *pos, const int32_t *seq, int B, int hq,
+                                    const KvView &pool, const float *sinks, const float *table, int64_t max_pos,
+                                    float softmax_scale, uint16_t *out, unsigned *status, cudaStream_t st) {
+  cudaError_t e = ensure_smem_limit(0, (const void *)full_decode_kernel, FD_SMEM);
+  if (e != cudaSuccess) return e;
+  const int hkv = pool.hkv, G = hq / hkv;
+  // positions past the pool are flagged as bad positions, like full_attn_decode's max_ctx
+  const long long cap = (long long)pool.max_blocks * pool.block_size;
+  const long long max_ctx = cap < max_pos ? cap : max_pos;
+  const long long items = (long long)B * hkv;
+  long long grid = (long long)num_sms() * 2;
+  if (grid > items) grid = items;
+  full_decode_kernel<<<(unsigned)grid, FD_WARPS * 32, FD_SMEM, st>>>(
+      q, pos, seq, B, hq, G, pool, table, max_pos, softmax_scale * LOG2E, max_ctx, 1, WIN + 16, nullptr, nullptr,
+      status, WIN, sinks, out);
   return cudaGetLastError();
 }
 

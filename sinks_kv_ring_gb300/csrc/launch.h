@@ -34,6 +34,12 @@ cudaError_t launch_swa_decode(const uint16_t *q, const int64_t *pos, const int32
                               int64_t max_pos, float softmax_scale, uint16_t *out, unsigned *status,
                               cudaStream_t st);
 
+// Windowed decode over a PAGED layout: the split decode kernel with the key
+// range p-127..p, one split, the sink in the final normalisation.
+cudaError_t launch_swa_decode_paged(const uint16_t *q, const int64_t *pos, const int32_t *seq, int B, int hq,
+                                    const KvView &pool, const float *sinks, const float *table, int64_t max_pos,
+                                    float softmax_scale, uint16_t *out, unsigned *status, cudaStream_t st);
+
 // Split plan of the full-attention decode: contexts up to max_ctx are cut
 // into at most `splits` pieces of `split_len` keys (a multiple of 64).
 struct DecodePlan {
@@ -103,6 +109,15 @@ bool make_tma_map_tokens4d(CUtensorMap *m, const void *ptr, long long T, int hkv
 
 cudaError_t launch_ring_copy(const KvView &ring, const int32_t *seqs, int n, uint16_t *k_snap, uint16_t *v_snap,
                              int32_t *tags_snap, bool to_ring, unsigned *status, cudaStream_t st);
+
+cudaError_t launch_pages_release(int32_t *table, int num_seqs, int max_blocks, int block_size, int num_blocks,
+                                 const int32_t *seqs, const int64_t *next_pos, int32_t *lo, int n, int window,
+                                 int32_t *free_ids, int32_t *free_count, int free_cap, unsigned *status,
+                                 cudaStream_t st);
+
+cudaError_t launch_ring_gather(const KvView &pages, const KvView &ring, const int32_t *src_seqs,
+                               const int32_t *dst_seqs, const int64_t *end, int n, unsigned *status,
+                               cudaStream_t st);
 
 int num_sms();
 

@@ -1,0 +1,210 @@
+// pages.cu -- pool management of a windowed layer kept in pages.
+//
+// release: Xiaomi "Full-Pipeline Inference Optimization for MiMo-V2.5
+// Series", section 2.1 ("SWA KVCache Management": the SWA pool is bounded by
+// the window; "SWA-Aware Prefix Cache Tree": the end of a prefill chunk, the
+// end of a request and every N decoded tokens release the SWA KV that has
+// left the window) and gaudi-cookbook "Windowed KV groups" (the sliding
+// layers' out-of-window blocks are freed).  A query at q reads q-W+1..q, so
+// with the next query of a sequence at P, the blocks whose positions all lie
+// below P-W+1 are read by no later query.
+//
+// gather: colibri "System One mode and prompt reuse": position p sits in ring
+// slot p mod 128 and the ring records which position each slot holds; the
+// ring of a sequence whose positions 0..E-1 were appended in order holds, in
+// slot c, the last of them congruent to c.
+#include "launch.h"
+
+namespace kvr {
+namespace {
+
+constexpr int RL_THREADS = 1024;
+constexpr int RL_WARPS = RL_THREADS / 32;
+constexpr unsigned FULLW = 0xffffffffu;
+
+struct ReleaseArgs {
+  int32_t *table;
+  int num_seqs, max_blocks, block_size, num_blocks;
+  const int32_t *seqs;
+  const int64_t *next_pos;
+  int32_t *lo;  // [num_seqs] or null
+  int n, window;
+  int32_t *free_ids;
+  int32_t *free_count;
+  int free_cap;
+};
+
+// Table range [a, b) that entry i looks at; false for a bad sequence id.
+__device__ __forceinline__ bool release_range(const ReleaseArgs &A, int i, int &s, int &a, int &b) {
+  s = A.seqs[i];
+  if (s < 0 || s >= A.num_seqs) return false;
+  const long long first_kept = A.next_pos[i] - A.window + 1;  // earliest position a later query reads
+  long long hi = first_kept > 0 ? first_kept / A.block_size : 0;
+  if (hi > A.max_blocks) hi = A.max_blocks;
+  int lo = A.lo ? A.lo[s] : 0;
+  if (lo < 0) lo = 0;
+  if (lo > A.max_blocks) lo = A.max_blocks;
+  a = lo;
+  b = (int)hi;
+  return true;
+}
+
+// Live (releasable) entries of one range, counted by a warp.
+__device__ __forceinline__ int warp_count_live(const ReleaseArgs &A, const int32_t *row, int a, int b, int lane,
+                                               bool &bad) {
+  int cnt = 0;
+  for (int c0 = a; c0 < b; c0 += 32) {
+    const int bi = c0 + lane;
+    const int id = bi < b ? row[bi] : -1;
+    if (id >= A.num_blocks) bad = true;
+    cnt += __popc(__ballot_sync(FULLW, id >= 0 && id < A.num_blocks));
+  }
+  return cnt;
+}
+
+// One CTA: pass 1 counts what the whole call releases (all or nothing
+// against the free list's capacity); pass 2 walks the entries in rounds of
+// 32 (one per warp), takes each entry's offset from a scan of the round's
+// counts, and writes the ids in (entry, block index) order.
+__global__ void __launch_bounds__(RL_THREADS) pages_release_kernel(ReleaseArgs A, unsigned *status) {
+  __shared__ int s_cnt[RL_WARPS];
+  __shared__ int s_off[RL_WARPS];
+  __shared__ int s_total, s_base;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+
+  // pass 1
+  int mine = 0;
+  bool bad_seq = false, bad_blk = false;
+  for (int i = warp; i < A.n; i += RL_WARPS) {
+    int s, a, b;
+    if (!release_range(A, i, s, a, b)) {
+      bad_seq = true;
+      continue;
+    }
+    mine += warp_count_live(A, A.table + (long long)s * A.max_blocks, a, b, lane, bad_blk);
+  }
+  if (lane == 0) s_cnt[warp] = mine;
+  if (threadIdx.x == 0) s_base = *A.free_count;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int t = 0;
+    for (int w = 0; w < RL_WARPS; ++w) t += s_cnt[w];
+    s_total = t;
+  }
+  if (bad_seq && lane == 0) flag(status, ST_BAD_SEQ);
+  if (__any_sync(FULLW, bad_blk) && lane == 0) flag(status, ST_BAD_BLOCK);
+  __syncthreads();
+  const int base0 = s_base, total = s_total;
+  if (base0 < 0 || (long long)base0 + total > A.free_cap) {
+    if (threadIdx.x == 0) flag(status, ST_FREE_FULL);
+    return;  // nothing released, nothing changed
+  }
+
+  // pass 2
+  int base = base0;
+  for (int r0 = 0; r0 < A.n; r0 += RL_WARPS) {
+    const int i = r0 + warp;
+    int s = -1, a = 0, b = 0;
+    const bool ok = i < A.n && release_range(A, i, s, a, b);
+    bool dummy = false;
+    const int cnt = ok ? warp_count_live(A, A.table + (long long)s * A.max_blocks, a, b, lane, dummy) : 0;
+    if (lane == 0) s_cnt[warp] = cnt;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      int t = 0;
+      for (int w = 0; w < RL_WARPS; ++w) {
+        s_off[w] = t;
+        t += s_cnt[w];
+      }
+      s_total = t;
+    }
+    __syncthreads();
+    if (ok) {
+      int32_t *row = A.table + (long long)s * A.max_blocks;
+      int at = base + s_off[warp];
+      for (int c0 = a; c0 < b; c0 += 32) {
+        const int bi = c0 + lane;
+        const int id = bi < b ? row[bi] : -1;
+        const bool live = id >= 0 && id < A.num_blocks;
+        const unsigned m = __ballot_sync(FULLW, live);
+        if (live) {
+          A.free_ids[at + __popc(m & ((1u << lane) - 1u))] = id;
+          row[bi] = -1;
+        }
+        at += __popc(m);
+      }
+      if (A.lo && lane == 0 && A.lo[s] < b) A.lo[s] = b;
+    }
+    base += s_total;
+    __syncthreads();  // s_cnt / s_off / s_total are rewritten by the next round
+  }
+  if (threadIdx.x == 0) *A.free_count = base;
+}
+
+// One CTA per (entry, KV head): the 128 slots' K and V rows with 16-byte
+// accesses; the KV-head-0 CTA also writes the slot tags.
+__global__ void __launch_bounds__(256)
+    ring_gather_kernel(KvView pages, KvView ring, const int32_t *__restrict__ src_seqs,
+                       const int32_t *__restrict__ dst_seqs, const int64_t *__restrict__ end, unsigned *status) {
+  const int i = blockIdx.x, kv = blockIdx.y, hkv = ring.hkv;
+  const int ss = src_seqs[i], ds = dst_seqs[i];
+  if (ss < 0 || ss >= pages.num_seqs || ds < 0 || ds >= ring.num_seqs) {
+    if (kv == 0 && threadIdx.x == 0) flag(status, ST_BAD_SEQ);
+    return;
+  }
+  const long long e = end[i];
+  const int32_t *bt = pages.block_table + (long long)ss * pages.max_blocks;
+  uint4 *rk = reinterpret_cast<uint4 *>(ring.k + ((long long)ds * hkv + kv) * WIN * DQK);
+  uint4 *rv = reinterpret_cast<uint4 *>(ring.v + ((long long)ds * hkv + kv) * WIN * DV);
+  constexpr int CK = DQK / 8, CV = DV / 8, CR = CK + CV;  // 16-byte chunks per slot
+  for (int x = threadIdx.x; x < WIN * CR; x += blockDim.x) {
+    const int c = x / CR, ch = x % CR;
+    // the position slot c holds: the largest p < e with p mod 128 == c
+    const long long p = e - 1 - (long long)(((e - 1 - c) % WIN + WIN) % WIN);
+    if (e <= 0 || p < 0) continue;
+    const long long bi = p / pages.block_size;
+    const int blk = bi < pages.max_blocks ? bt[bi] : -1;
+    if (blk < 0 || blk >= pages.num_blocks) continue;
+    const long long row = ((long long)blk * pages.hkv + kv) * pages.block_size + (p - bi * pages.block_size);
+    if (ch < CK)
+      rk[c * CK + ch] = reinterpret_cast<const uint4 *>(pages.k + row * DQK)[ch];
+    else
+      rv[c * CV + ch - CK] = reinterpret_cast<const uint4 *>(pages.v + row * DV)[ch - CK];
+  }
+  if (kv == 0 && threadIdx.x < WIN) {
+    const int c = threadIdx.x;
+    const long long p = e - 1 - (long long)(((e - 1 - c) % WIN + WIN) % WIN);
+    int32_t tag = -1;
+    if (e > 0 && p >= 0) {
+      const long long bi = p / pages.block_size;
+      const int blk = bi < pages.max_blocks ? bt[bi] : -1;
+      if (blk >= 0 && blk < pages.num_blocks)
+        tag = (int32_t)p;
+      else
+        flag(status, ST_BAD_BLOCK);
+    }
+    ring.slot_pos[(long long)ds * WIN + c] = tag;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_pages_release(int32_t *table, int num_seqs, int max_blocks, int block_size, int num_blocks,
+                                 const int32_t *seqs, const int64_t *next_pos, int32_t *lo, int n, int window,
+                                 int32_t *free_ids, int32_t *free_count, int free_cap, unsigned *status,
+                                 cudaStream_t st) {
+  ReleaseArgs A{table, num_seqs, max_blocks, block_size, num_blocks, seqs, next_pos, lo, n, window,
+                free_ids, free_count, free_cap};
+  pages_release_kernel<<<1, RL_THREADS, 0, st>>>(A, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_ring_gather(const KvView &pages, const KvView &ring, const int32_t *src_seqs,
+                               const int32_t *dst_seqs, const int64_t *end, int n, unsigned *status,
+                               cudaStream_t st) {
+  dim3 grid((unsigned)n, (unsigned)ring.hkv);
+  ring_gather_kernel<<<grid, 256, 0, st>>>(pages, ring, src_seqs, dst_seqs, end, status);
+  return cudaGetLastError();
+}
+
+}  // namespace kvr

@@ -63,8 +63,11 @@ def _paged(**kw):
 def test_host_validation_codes(L):
     P = ctypes.c_void_p(FAKE)
     ring = _ring()
-    # wrong layout kind
-    assert L.swa_sink_decode(P, P, P, 2, 64, ctypes.byref(_paged()), P, P, 1000, 0.1, P, None) == -1
+    # wrong layout kind (RING or PAGED are taken)
+    lin = _paged(kind=3, num_rows=16)
+    assert L.swa_sink_decode(P, P, P, 2, 64, ctypes.byref(lin), P, P, 1000, 0.1, P, None) == -1
+    # a PAGED windowed layer: still at most 16 query heads per KV head
+    assert L.swa_sink_decode(P, P, P, 2, 128, ctypes.byref(_paged()), P, P, 1000, 0.1, P, None) == -4
     # Hq not a multiple of Hkv
     assert L.swa_sink_decode(P, P, P, 2, 60, ctypes.byref(ring), P, P, 1000, 0.1, P, None) == -1
     # more than 16 query heads per KV head
@@ -166,3 +169,30 @@ def test_layout_byte_counts_match_the_pages():
     # (8 KV heads there) -- same per-token arithmetic.
     gib = 10 * 8192 * kvr.PagedLayout.bytes_per_token(8, elem_bytes=4) / 2 ** 30
     assert abs(gib - 0.78) < 0.01
+
+
+def test_pages_management_host_validation(L):
+    P = ctypes.c_void_p(FAKE)
+    rel = L.kv_pages_release_window
+    # n < 0, empty pool shapes, window < 1, negative capacity, NULL table / counter
+    assert rel(P, 4, 16, 64, 64, P, P, None, -1, 128, P, P, 8, None) == -1
+    assert rel(P, 0, 16, 64, 64, P, P, None, 1, 128, P, P, 8, None) == -1
+    assert rel(P, 4, 16, 64, 64, P, P, None, 1, 0, P, P, 8, None) == -1
+    assert rel(P, 4, 16, 64, 64, P, P, None, 1, 128, P, P, -1, None) == -1
+    assert rel(None, 4, 16, 64, 64, P, P, None, 1, 128, P, P, 8, None) == -1
+    assert rel(P, 4, 16, 64, 64, P, P, None, 1, 128, P, None, 8, None) == -1
+    # NULL seqs / next_pos / free_ids (with a capacity)
+    assert rel(P, 4, 16, 64, 64, None, P, None, 1, 128, P, P, 8, None) == -1
+    assert rel(P, 4, 16, 64, 64, P, P, None, 1, 128, None, P, 8, None) == -1
+    # n = 0 launches nothing
+    assert rel(P, 4, 16, 64, 64, None, None, None, 0, 128, None, P, 0, None) == 0
+    gat = L.kv_ring_gather_pages
+    ring8 = _ring()
+    # pages must be PAGED, ring must be RING, and their KV head counts agree
+    assert gat(ctypes.byref(ring8), ctypes.byref(ring8), P, P, P, 1, None) == -1
+    assert gat(ctypes.byref(_paged(num_kv_heads=8)), ctypes.byref(_paged(num_kv_heads=8)), P, P, P, 1, None) == -1
+    assert gat(ctypes.byref(_paged()), ctypes.byref(ring8), P, P, P, 1, None) == -1
+    pg8 = _paged(num_kv_heads=8)
+    assert gat(ctypes.byref(pg8), ctypes.byref(ring8), P, P, P, -1, None) == -1
+    assert gat(ctypes.byref(pg8), ctypes.byref(ring8), None, P, P, 1, None) == -1
+    assert gat(ctypes.byref(pg8), ctypes.byref(ring8), None, None, None, 0, None) == 0
