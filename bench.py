@@ -515,6 +515,76 @@ def decode_kernel_graph_times(work):
     return graph_time_ms(swa), graph_time_ms(full)
 
 
+def pages_times(work, hbm, peaks_src, copies=None):
+    """The decode workload's windowed layer kept in pages (block size 64; the
+    block table holds only the blocks of each sequence's window): windowed
+    decode over the pages and the ring-from-pages gather, each a graph of
+    launches rotating over copies larger than L2 together; and the
+    out-of-window release at decode cadence (one block per sequence)."""
+    kvr = work.kvr
+    from sinks_kv_ring_gb300.synth import Synth
+    dev = work.pos.device
+    B, hkv, p, bs = work.B, work.hkv_swa, work.p, 64
+    lo = max(0, p - 127)
+    b0, b1 = lo // bs, p // bs
+    nper = b1 - b0 + 1
+    tab = torch.full((B, b1 + 1), -1, dtype=torch.int32, device=dev)
+    tab[:, b0:] = torch.arange(B * nper, dtype=torch.int32, device=dev).reshape(B, nper)
+    base = kvr.PagedLayout(torch.zeros(B * nper, hkv, bs, 192, dtype=torch.bfloat16, device=dev),
+                           torch.zeros(B * nper, hkv, bs, 128, dtype=torch.bfloat16, device=dev), tab)
+    syn = Synth(1001, dist="shifted", device=dev)
+    for s in range(B):
+        kvr.kv_ring_append_rope(syn.k(p + 1 - lo, hkv, seq=s, start=lo), syn.v(p + 1 - lo, hkv, seq=s, start=lo),
+                                torch.arange(lo, p + 1, device=dev), torch.full((p + 1 - lo,), s, dtype=torch.int32,
+                                                                                 device=dev), work.t4, work.vscale, base)
+    one = (base.k.numel() + base.v.numel()) * 2
+    if copies is None:
+        copies = max(1, min(64, math.ceil(4 * 129e6 / one)))
+    pools = [base] + [kvr.PagedLayout(base.k.clone(), base.v.clone(), tab) for _ in range(copies - 1)]
+    dec = [(lambda st, pl=pl: kvr.swa_sink_decode(work.q_swa, work.pos, work.seq, pl, work.sinks, work.t4, SCALE,
+                                                  out=work.out_swa, stream=st)) for pl in pools] * 4
+    ms_dec = graph_time_ms(dec)
+    ring = kvr.RingLayout.empty(B, hkv, device=dev)
+    end = torch.full((B,), p + 1, dtype=torch.int64, device=dev)
+    gat = [(lambda st, pl=pl: kvr.kv_ring_gather_pages(pl, ring, work.seq, work.seq, end, stream=st))
+           for pl in pools] * 4
+    ms_gat = graph_time_ms(gat)
+    gat_bytes = 2 * layer_kv_bytes([p + 1] * B, hkv, window=128) + B * 128 * 4
+    # release: every sequence has a full table (ids 0..B*mb-1); each call frees
+    # the one block that the next query's window has just left
+    mb = b1 + 1
+    rtab0 = torch.arange(B * mb, dtype=torch.int32, device=dev).reshape(B, mb)
+    rtab, rlo0 = rtab0.clone(), torch.full((B,), max(0, b0 - 1), dtype=torch.int32, device=dev)
+    rlo = rlo0.clone()
+    free = torch.empty(B * mb, dtype=torch.int32, device=dev)
+    cnt = torch.zeros(1, dtype=torch.int32, device=dev)
+    nxt = torch.full((B,), b0 * bs + 127, dtype=torch.int64, device=dev)
+    reset = lambda st: (rtab.copy_(rtab0), rlo.copy_(rlo0), cnt.zero_())
+    rel = lambda st: kvr.kv_pages_release_window(rtab, B * mb, bs, work.seq, nxt, free, cnt, lo=rlo, stream=st)
+    ms_reset = graph_time_ms([reset] * 20)
+    ms_both = graph_time_ms([lambda st: (reset(st), rel(st))] * 20)
+    released = int(cnt.item())
+    dec_gbs = work.bytes_swa() / (ms_dec / 1e3) / 1e9
+    gat_gbs = gat_bytes / (ms_gat / 1e3) / 1e9
+    return {
+        "swa_sink_decode_paged": {
+            "workload": f"batch {B}, windowed layer kept in pages of {bs} (block table holds the window's {nper} "
+                        f"blocks per sequence), graph rotating over {copies} copies", "graph_ms": round(ms_dec, 5),
+            "bytes": work.bytes_swa(), "GB/s": round(dec_gbs, 1),
+            "roofline": with_nominal({"bound": "hbm", "achieved": round(dec_gbs, 1), "peak": hbm, "unit": "GB/s",
+                                      "frac": round(dec_gbs / hbm, 4), "peak_source": peaks_src})},
+        "kv_ring_gather_pages": {
+            "workload": f"{B} sequences x {hkv} KV heads: the 128-position window from pages into rings",
+            "graph_ms": round(ms_gat, 5), "bytes": gat_bytes, "GB/s": round(gat_gbs, 1),
+            "roofline": with_nominal({"bound": "hbm", "achieved": round(gat_gbs, 1), "peak": hbm, "unit": "GB/s",
+                                      "frac": round(gat_gbs / hbm, 4), "peak_source": peaks_src})},
+        "kv_pages_release_window": {
+            "workload": f"{B} sequences, one out-of-window block each (decode cadence)",
+            "us_per_call": round((ms_both - ms_reset) * 1e3, 2), "released_per_call": released,
+            "note": "one-CTA bookkeeping kernel; latency, no roofline"},
+    }
+
+
 def e2e_decode(work, steps, warmup, stream):
     """The same decode step with the per-step inputs copied in from pinned host
     memory and the outputs copied back, all inside the timed region."""
@@ -721,6 +791,7 @@ def main():
         res["mtp"] = mtp_result(m, mms, mck, mg, hbm, world)
         res["gpu_launches"] += m.launches_per_step * min(20, args.steps)
         del m
+        res["pages"] = pages_times(work, hbm, peaks_src)
     if not args.no_prefill and args.workload == "flash_decode":
         del work
         torch.cuda.empty_cache()

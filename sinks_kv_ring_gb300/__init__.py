@@ -449,26 +449,30 @@ def kv_ring_restore(ring, seqs, snap, stream=None):
     _ring_copy(lib().kv_ring_restore, ring, seqs, snap, stream)
 
 
-def kv_pages_release_window(pool, seqs, next_pos, free_ids, free_count, lo=None, window=WINDOW, stream=None):
-    """Release the pages of a windowed layer kept in `pool` (a PagedLayout)
-    that no query at or after next_pos[i] reads: their ids are appended to
-    free_ids (int32 [cap]) at free_count (int32 [1], advanced), their
-    block-table entries set to -1, and lo (int32 [num_seqs], optional)
-    advanced.  Everything stays on the device."""
+def kv_pages_release_window(block_table, num_blocks, block_size, seqs, next_pos, free_ids, free_count, lo=None,
+                            window=WINDOW, stream=None):
+    """Release the pages of a windowed layer kept in pages that no query at or
+    after next_pos[i] reads: their ids (entries of block_table, int32
+    [num_seqs, max_blocks], ids < num_blocks) are appended to free_ids (int32
+    [cap]) at free_count (int32 [1], advanced), their entries set to -1, and
+    lo (int32 [num_seqs], optional) advanced.  Everything stays on the
+    device."""
+    _want(block_table, "block_table", torch.int32, 2)
     _want(seqs, "seqs", torch.int32, 1)
     _want(next_pos, "next_pos", torch.int64, 1)
     _want(free_ids, "free_ids", torch.int32, 1)
     _want(free_count, "free_count", torch.int32, 1)
+    S, mb = block_table.shape
     if lo is not None:
         _want(lo, "lo", torch.int32, 1)
-        if lo.shape[0] != pool.num_seqs:
-            raise ValueError("lo must have one entry per sequence of the pool")
+        if lo.shape[0] != S:
+            raise ValueError("lo must have one entry per sequence of the block table")
     n = seqs.shape[0]
     if next_pos.shape[0] != n or free_count.shape[0] != 1:
         raise ValueError("seqs/next_pos/free_count shapes disagree")
-    _check(lib().kv_pages_release_window(_ptr(pool.block_table), pool.num_seqs, pool.max_blocks, pool.block_size,
-                                         pool.num_blocks, _ptr(seqs), _ptr(next_pos), _ptr(lo), n, int(window),
-                                         _ptr(free_ids), _ptr(free_count), free_ids.shape[0], _stream(stream)))
+    _check(lib().kv_pages_release_window(_ptr(block_table), S, mb, int(block_size), int(num_blocks), _ptr(seqs),
+                                         _ptr(next_pos), _ptr(lo), n, int(window), _ptr(free_ids),
+                                         _ptr(free_count), free_ids.shape[0], _stream(stream)))
 
 
 def kv_ring_gather_pages(pages, ring, src_seqs, dst_seqs, end, stream=None):

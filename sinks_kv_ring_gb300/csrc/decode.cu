@@ -36,6 +36,11 @@ constexpr int FD_SMEM = 16 * DQK * 2 + FD_WARPS * FD_STAGES * FD_STAGE;
 constexpr int FD_TARGET_ITEMS = 152 * 8;
 static_assert(FD_WARPS * FD_STAGES * FD_STAGE >= FD_WARPS * 16 * (MO_STRIDE + 2) * 4, "merge area");
 
+// WINDOW = false: a full layer (keys 0..p, split partials to the workspace);
+// true: a windowed layer kept in pages (keys p-127..p, one split, direct
+// normalised output with the sink).  Separate instantiations keep the full
+// layer's issue path free of the window's per-row checks.
+template <bool WINDOW>
 __global__ void __launch_bounds__(FD_WARPS * 32, 2)
     full_decode_kernel(const uint16_t *__restrict__ q, const int64_t *__restrict__ pos,
                        const int32_t *__restrict__ seq, int B, int hq, int G, KvView pool,
@@ -61,7 +66,7 @@ __global__ void __launch_bounds__(FD_WARPS * 32, 2)
     if (bad_pos || bad_seq) {
       if (split == 0 && kv == 0 && tid == 0)
         flag(status, (bad_pos ? ST_BAD_POS : 0u) | (bad_seq ? ST_BAD_SEQ : 0u));
-      if (out_direct && split == 0) {  // direct mode writes the zero rows itself
+      if (WINDOW && split == 0) {  // direct mode writes the zero rows itself
         uint16_t *o = out_direct + ((long long)b * hq + (long long)kv * G) * DV;
         for (int e = tid; e < G * DV; e += blockDim.x) o[e] = 0;
       }
@@ -70,7 +75,7 @@ __global__ void __launch_bounds__(FD_WARPS * 32, 2)
     // window: keys p-window+1..p; the range starts on a 16-key subtile boundary
     // (a subtile never straddles a block); rows below key_min are zero-filled
     // instead of read and their scores masked
-    const long long key_min = window > 0 ? max(0LL, p - window + 1) : 0;
+    const long long key_min = WINDOW ? max(0LL, p - window + 1) : 0;
     const long long key_lo = (key_min & ~15LL) + (long long)split * split_len;
     if (key_lo > p) continue;
     const long long key_hi = min(key_lo + split_len, p + 1);
@@ -105,13 +110,13 @@ __global__ void __launch_bounds__(FD_WARPS * 32, 2)
 #pragma unroll
       for (int u = 0; u < 12; ++u) {
         const int c = lane + 32 * u, r = c / 24, ch = c % 24;
-        const int nb = (blk_ok && key0 + r < key_hi && key0 + r >= key_min) ? 16 : 0;
+        const int nb = (blk_ok && key0 + r < key_hi && (!WINDOW || key0 + r >= key_min)) ? 16 : 0;
         cp_async16(kb + swz<DQK>(r, ch), kg + r * DQK + ch * 8, nb);
       }
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
         const int c = lane + 32 * u, r = c >> 4, ch = c & 15;
-        const int nb = (blk_ok && key0 + r < key_hi && key0 + r >= key_min) ? 16 : 0;
+        const int nb = (blk_ok && key0 + r < key_hi && (!WINDOW || key0 + r >= key_min)) ? 16 : 0;
         cp_async16(vb + swz<DV>(r, ch), vg + r * DV + ch * 8, nb);
       }
     };
@@ -137,7 +142,7 @@ __global__ void __launch_bounds__(FD_WARPS * 32, 2)
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const long long key = key0 + 8 * j + 2 * (lane & 3) + (e & 1);
-          S[j][e] = (blk_ok && key < key_hi && key >= key_min) ? S[j][e] * scale_log2 : NEG_INF;
+          S[j][e] = (blk_ok && key < key_hi && (!WINDOW || key >= key_min)) ? S[j][e] * scale_log2 : NEG_INF;
         }
       softmax_update(S, m0, m1, l0, l1, O);
       pv_16keys(S, kb + FD_SUB_K, 0, lane, O);
@@ -151,7 +156,7 @@ __global__ void __launch_bounds__(FD_WARPS * 32, 2)
     stash_warp_state(mml + warp * 32, mo + warp * 16 * MO_STRIDE, lane, m0, m1, l0, l1, O);
     __syncthreads();
 
-    if (out_direct) {
+    if (WINDOW) {
       // one split holds the whole window: normalise here, the sink joining
       // the denominator only (its numerator is zero)
       uint16_t *o = out_direct + ((long long)b * hq + (long long)kv * G) * DV;
@@ -283,7 +288,7 @@ cudaError_t launch_full_decode(const uint16_t *q, const int64_t *pos, const int3
                                const KvView &pool, const float *table, int64_t max_pos,
                                float softmax_scale, long long max_ctx, void *ws, uint16_t *out,
                                unsigned *status, cudaStream_t st) {
-  cudaError_t e = ensure_smem_limit(0, (const void *)full_decode_kernel, FD_SMEM);
+  cudaError_t e = ensure_smem_limit(0, (const void *)full_decode_kernel<false>, FD_SMEM);
   if (e != cudaSuccess) return e;
   const int hkv = pool.hkv, G = hq / hkv;
   const DecodePlan pl = full_decode_plan(B, hkv, max_ctx);
@@ -293,7 +298,7 @@ cudaError_t launch_full_decode(const uint16_t *q, const int64_t *pos, const int3
                                             align256(items * G * 2 * sizeof(float)));
   long long grid = (long long)num_sms() * 2;
   if (grid > (long long)items) grid = (long long)items;
-  full_decode_kernel<<<(unsigned)grid, FD_WARPS * 32, FD_SMEM, st>>>(
+  full_decode_kernel<false><<<(unsigned)grid, FD_WARPS * 32, FD_SMEM, st>>>(
       q, pos, seq, B, hq, G, pool, table, max_pos, softmax_scale * LOG2E, max_ctx, pl.splits, pl.split_len,
       part_ml, part_o, status, 0, nullptr, nullptr);
   e = cudaGetLastError();
@@ -306,7 +311,7 @@ cudaError_t launch_full_decode(const uint16_t *q, const int64_t *pos, const int3
 cudaError_t launch_swa_decode_paged(const uint16_t *q, const int64_t *pos, const int32_t *seq, int B, int hq,
                                     const KvView &pool, const float *sinks, const float *table, int64_t max_pos,
                                     float softmax_scale, uint16_t *out, unsigned *status, cudaStream_t st) {
-  cudaError_t e = ensure_smem_limit(0, (const void *)full_decode_kernel, FD_SMEM);
+  cudaError_t e = ensure_smem_limit(9, (const void *)full_decode_kernel<true>, FD_SMEM);
   if (e != cudaSuccess) return e;
   const int hkv = pool.hkv, G = hq / hkv;
   // positions past the pool are flagged as bad positions, like full_attn_decode's max_ctx
@@ -315,7 +320,7 @@ cudaError_t launch_swa_decode_paged(const uint16_t *q, const int64_t *pos, const
   const long long items = (long long)B * hkv;
   long long grid = (long long)num_sms() * 2;
   if (grid > items) grid = items;
-  full_decode_kernel<<<(unsigned)grid, FD_WARPS * 32, FD_SMEM, st>>>(
+  full_decode_kernel<true><<<(unsigned)grid, FD_WARPS * 32, FD_SMEM, st>>>(
       q, pos, seq, B, hq, G, pool, table, max_pos, softmax_scale * LOG2E, max_ctx, 1, WIN + 16, nullptr, nullptr,
       status, WIN, sinks, out);
   return cudaGetLastError();

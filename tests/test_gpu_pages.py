@@ -142,20 +142,16 @@ def test_swa_decode_paged_bad_inputs_are_zeroed_and_flagged(tables):
 # --------------------------------------------------------------------------- out-of-window release
 
 def _release_gpu(table_np, nblk, bsz, seqs, nxt, window, lo, free_np, count, cap_override=None):
-    S, mb = table_np.shape
-    k = torch.zeros(1, 1, bsz, 192, dtype=torch.bfloat16, device=DEV)   # rows are not touched
-    v = torch.zeros(1, 1, bsz, 128, dtype=torch.bfloat16, device=DEV)
-    pool = kvr.PagedLayout(k, v, torch.from_numpy(table_np.copy()).to(DEV))
-    pool.num_blocks = nblk
+    tab = torch.from_numpy(table_np.copy()).to(DEV)
     free = torch.from_numpy(free_np.copy()).to(DEV)
     if cap_override is not None:
         free = free[:cap_override]
     cnt = torch.tensor([count], dtype=torch.int32, device=DEV)
     lo_t = None if lo is None else torch.tensor(lo, dtype=torch.int32, device=DEV)
-    kvr.kv_pages_release_window(pool, torch.tensor(seqs, dtype=torch.int32, device=DEV),
+    kvr.kv_pages_release_window(tab, nblk, bsz, torch.tensor(seqs, dtype=torch.int32, device=DEV),
                                 torch.tensor(nxt, dtype=torch.int64, device=DEV), free, cnt, lo=lo_t, window=window)
     st = kvr.device_status()
-    return (pool.block_table.cpu().numpy(), None if lo_t is None else lo_t.cpu().tolist(), free.cpu().numpy(),
+    return (tab.cpu().numpy(), None if lo_t is None else lo_t.cpu().tolist(), free.cpu().numpy(),
             int(cnt.item()), st)
 
 
@@ -240,7 +236,7 @@ def test_paged_decode_unchanged_by_release(tables):
     free = torch.full((nblk,), -1, dtype=torch.int32, device=DEV)
     cnt = torch.zeros(1, dtype=torch.int32, device=DEV)
     lo = torch.zeros(B, dtype=torch.int32, device=DEV)
-    kvr.kv_pages_release_window(pool, seq, pos, free, cnt, lo=lo)
+    kvr.kv_pages_release_window(pool.block_table, pool.num_blocks, bsz, seq, pos, free, cnt, lo=lo)
     # poison every released block: a read of one would show
     freed = free[: int(cnt.item())].long()
     pool.k.view(torch.int16)[freed] = NAN_BITS
