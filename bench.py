@@ -515,8 +515,8 @@ def decode_kernel_graph_times(work):
     return graph_time_ms(swa), graph_time_ms(full)
 
 
-def pages_times(work, hbm, peaks_src, copies=None):
-    """The decode workload's windowed layer kept in pages (block size 64; the
+def pool_ops_times(work, hbm, peaks_src, copies=None):
+    """Ring snapshot and restore of the decode batch; and the decode workload's windowed layer kept in pages (block size 64; the
     block table holds only the blocks of each sequence's window): windowed
     decode over the pages and the ring-from-pages gather, each a graph of
     launches rotating over copies larger than L2 together; and the
@@ -566,7 +566,22 @@ def pages_times(work, hbm, peaks_src, copies=None):
     released = int(cnt.item())
     dec_gbs = work.bytes_swa() / (ms_dec / 1e3) / 1e9
     gat_gbs = gat_bytes / (ms_gat / 1e3) / 1e9
+    # ring snapshot / restore of the whole batch, rotating over the decode workload's ring copies
+    snap = kvr.ring_snapshot_alloc(B, hkv, device=dev)
+    sn = [(lambda st, r=r: kvr.kv_ring_snapshot(r, work.seq, snap, stream=st)) for r in work.rings] * 4
+    rs = [(lambda st, r=r: kvr.kv_ring_restore(r, work.seq, snap, stream=st)) for r in work.rings] * 4
+    ms_sn, ms_rs = graph_time_ms(sn), graph_time_ms(rs)
+    copy_bytes = 2 * (kvr.RingLayout.bytes_per_layer(B, hkv) + B * 128 * 4)
+    copy = lambda ms: {"graph_ms": round(ms, 5), "bytes": copy_bytes, "GB/s": round(copy_bytes / ms / 1e6, 1),
+                       "roofline": with_nominal({"bound": "hbm", "achieved": round(copy_bytes / ms / 1e6, 1),
+                                                 "peak": hbm, "unit": "GB/s",
+                                                 "frac": round(copy_bytes / ms / 1e6 / hbm, 4),
+                                                 "peak_source": peaks_src})}
     return {
+        "kv_ring_snapshot": dict(workload=f"{B} sequences x {hkv} KV heads: rings (slots + tags) to a snapshot, "
+                                          f"rotating over {len(work.rings)} ring copies", **copy(ms_sn)),
+        "kv_ring_restore": dict(workload=f"{B} sequences x {hkv} KV heads: snapshot back into the rings",
+                                **copy(ms_rs)),
         "swa_sink_decode_paged": {
             "workload": f"batch {B}, windowed layer kept in pages of {bs} (block table holds the window's {nper} "
                         f"blocks per sequence), graph rotating over {copies} copies", "graph_ms": round(ms_dec, 5),
@@ -791,7 +806,7 @@ def main():
         res["mtp"] = mtp_result(m, mms, mck, mg, hbm, world)
         res["gpu_launches"] += m.launches_per_step * min(20, args.steps)
         del m
-        res["pages"] = pages_times(work, hbm, peaks_src)
+        res["pool_ops"] = pool_ops_times(work, hbm, peaks_src)
     if not args.no_prefill and args.workload == "flash_decode":
         del work
         torch.cuda.empty_cache()

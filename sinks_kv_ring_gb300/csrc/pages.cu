@@ -141,49 +141,70 @@ __global__ void __launch_bounds__(RL_THREADS) pages_release_kernel(ReleaseArgs A
   if (threadIdx.x == 0) *A.free_count = base;
 }
 
-// One CTA per (entry, KV head): the 128 slots' K and V rows with 16-byte
-// accesses; the KV-head-0 CTA also writes the slot tags.
-__global__ void __launch_bounds__(256)
+// One CTA per (entry, KV head).  The first 128 threads resolve slot c to its
+// source row (-1 when the slot gets no position) into shared memory; then
+// every thread moves 16-byte chunks, GATHER_BATCH loads in flight before
+// their stores.  The KV-head-0 CTA also writes the slot tags.
+constexpr int GATHER_THREADS = 256;
+constexpr int GATHER_BATCH = 4;
+
+__global__ void __launch_bounds__(GATHER_THREADS)
     ring_gather_kernel(KvView pages, KvView ring, const int32_t *__restrict__ src_seqs,
                        const int32_t *__restrict__ dst_seqs, const int64_t *__restrict__ end, unsigned *status) {
+  __shared__ long long s_row[WIN];
   const int i = blockIdx.x, kv = blockIdx.y, hkv = ring.hkv;
   const int ss = src_seqs[i], ds = dst_seqs[i];
   if (ss < 0 || ss >= pages.num_seqs || ds < 0 || ds >= ring.num_seqs) {
     if (kv == 0 && threadIdx.x == 0) flag(status, ST_BAD_SEQ);
     return;
   }
-  const long long e = end[i];
-  const int32_t *bt = pages.block_table + (long long)ss * pages.max_blocks;
-  uint4 *rk = reinterpret_cast<uint4 *>(ring.k + ((long long)ds * hkv + kv) * WIN * DQK);
-  uint4 *rv = reinterpret_cast<uint4 *>(ring.v + ((long long)ds * hkv + kv) * WIN * DV);
-  constexpr int CK = DQK / 8, CV = DV / 8, CR = CK + CV;  // 16-byte chunks per slot
-  for (int x = threadIdx.x; x < WIN * CR; x += blockDim.x) {
-    const int c = x / CR, ch = x % CR;
+  if (threadIdx.x < WIN) {
+    const int c = threadIdx.x;
+    const long long e = end[i];
     // the position slot c holds: the largest p < e with p mod 128 == c
     const long long p = e - 1 - (long long)(((e - 1 - c) % WIN + WIN) % WIN);
-    if (e <= 0 || p < 0) continue;
-    const long long bi = p / pages.block_size;
-    const int blk = bi < pages.max_blocks ? bt[bi] : -1;
-    if (blk < 0 || blk >= pages.num_blocks) continue;
-    const long long row = ((long long)blk * pages.hkv + kv) * pages.block_size + (p - bi * pages.block_size);
-    if (ch < CK)
-      rk[c * CK + ch] = reinterpret_cast<const uint4 *>(pages.k + row * DQK)[ch];
-    else
-      rv[c * CV + ch - CK] = reinterpret_cast<const uint4 *>(pages.v + row * DV)[ch - CK];
-  }
-  if (kv == 0 && threadIdx.x < WIN) {
-    const int c = threadIdx.x;
-    const long long p = e - 1 - (long long)(((e - 1 - c) % WIN + WIN) % WIN);
+    long long row = -1;
     int32_t tag = -1;
     if (e > 0 && p >= 0) {
       const long long bi = p / pages.block_size;
-      const int blk = bi < pages.max_blocks ? bt[bi] : -1;
-      if (blk >= 0 && blk < pages.num_blocks)
+      const int blk = bi < pages.max_blocks ? pages.block_table[(long long)ss * pages.max_blocks + bi] : -1;
+      if (blk >= 0 && blk < pages.num_blocks) {
+        row = ((long long)blk * pages.hkv + kv) * pages.block_size + (p - bi * pages.block_size);
         tag = (int32_t)p;
-      else
+      } else if (kv == 0) {
         flag(status, ST_BAD_BLOCK);
+      }
     }
-    ring.slot_pos[(long long)ds * WIN + c] = tag;
+    s_row[c] = row;
+    if (kv == 0) ring.slot_pos[(long long)ds * WIN + c] = tag;
+  }
+  __syncthreads();
+  uint4 *rk = reinterpret_cast<uint4 *>(ring.k + ((long long)ds * hkv + kv) * WIN * DQK);
+  uint4 *rv = reinterpret_cast<uint4 *>(ring.v + ((long long)ds * hkv + kv) * WIN * DV);
+  constexpr int CK = DQK / 8, CV = DV / 8, CR = CK + CV;  // 16-byte chunks per slot
+  constexpr int TOTAL = WIN * CR;
+  static_assert(TOTAL % (GATHER_THREADS * GATHER_BATCH) == 0, "whole batches");
+  for (int x0 = threadIdx.x; x0 < TOTAL; x0 += GATHER_THREADS * GATHER_BATCH) {
+    uint4 val[GATHER_BATCH];
+    uint4 *dst[GATHER_BATCH];
+#pragma unroll
+    for (int u = 0; u < GATHER_BATCH; ++u) {
+      const int x = x0 + u * GATHER_THREADS, c = x / CR, ch = x % CR;
+      const long long row = s_row[c];
+      dst[u] = nullptr;
+      if (row >= 0) {
+        if (ch < CK) {
+          val[u] = reinterpret_cast<const uint4 *>(pages.k + row * DQK)[ch];
+          dst[u] = rk + c * CK + ch;
+        } else {
+          val[u] = reinterpret_cast<const uint4 *>(pages.v + row * DV)[ch - CK];
+          dst[u] = rv + c * CV + ch - CK;
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < GATHER_BATCH; ++u)
+      if (dst[u]) *dst[u] = val[u];
   }
 }
 
@@ -203,7 +224,7 @@ cudaError_t launch_ring_gather(const KvView &pages, const KvView &ring, const in
                                const int32_t *dst_seqs, const int64_t *end, int n, unsigned *status,
                                cudaStream_t st) {
   dim3 grid((unsigned)n, (unsigned)ring.hkv);
-  ring_gather_kernel<<<grid, 256, 0, st>>>(pages, ring, src_seqs, dst_seqs, end, status);
+  ring_gather_kernel<<<grid, GATHER_THREADS, 0, st>>>(pages, ring, src_seqs, dst_seqs, end, status);
   return cudaGetLastError();
 }
 
