@@ -303,13 +303,6 @@ class DecodeWorkload:
         if timed:
             self.t_full.stop(a, stream)
 
-    def e2e_buffers(self):
-        """Pinned host copies of the per-step inputs and outputs."""
-        pin = lambda t: torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t)
-        ins = [self.q_swa, self.q_full, self.k_swa, self.v_swa, self.k_full, self.v_full, self.pos]
-        outs = [self.out_swa, self.out_full]
-        return [(pin(t), t) for t in ins], [(torch.empty(t.shape, dtype=t.dtype, pin_memory=True), t) for t in outs]
-
 
 class MtpStep:
     """Draft verification (multi-token prediction) on a decode workload's
@@ -601,30 +594,80 @@ def pool_ops_times(work, hbm, peaks_src, copies=None):
 
 
 def e2e_decode(work, steps, warmup, stream):
-    """The same decode step with the per-step inputs copied in from pinned host
-    memory and the outputs copied back, all inside the timed region."""
-    ins, outs = work.e2e_buffers()
-    h2d = sum(h.numel() * h.element_size() for h, _ in ins)
-    d2h = sum(h.numel() * h.element_size() for h, _ in outs)
+    """The same decode step with each step's inputs copied in from pinned host
+    memory and its outputs copied back, all inside the timed region.  As in a
+    serving loop the copies run on their own streams with two device buffer
+    sets: step i+1's inputs upload while step i computes, and step i's outputs
+    download while step i+1 computes.  The region runs from the first upload
+    to the end of the last download."""
+    names_in = ["q_swa", "q_full", "k_swa", "v_swa", "k_full", "v_full", "pos"]
+    names_out = ["out_swa", "out_full"]
+    orig = {n: getattr(work, n) for n in names_in + names_out}
+    pin = lambda t: torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+    host_in = {n: pin(orig[n]).copy_(orig[n]) for n in names_in}
+    host_out = [{n: pin(orig[n]) for n in names_out} for _ in range(2)]
+    sets = [orig, {n: torch.empty_like(orig[n]) for n in names_in + names_out}]
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = sum(t.numel() * t.element_size() for t in host_out[0].values())
+    up, down = torch.cuda.Stream(), torch.cuda.Stream()
+    ready = [torch.cuda.Event() for _ in range(2)]
+    done = [torch.cuda.Event() for _ in range(2)]
+    fetched = [torch.cuda.Event() for _ in range(2)]
 
-    def one():
+    def upload(i):
+        k = i % 2
+        up.wait_event(done[k])         # step i-2 (same buffer set) has finished computing
+        with torch.cuda.stream(up):
+            for n in names_in:
+                sets[k][n].copy_(host_in[n], non_blocking=True)
+        ready[k].record(up)
+
+    def compute(i):
+        k = i % 2
+        stream.wait_event(ready[k])
+        stream.wait_event(fetched[k])  # step i-2's outputs (same buffer set) are on the host
+        for n in names_in + names_out:
+            setattr(work, n, sets[k][n])
         with torch.cuda.stream(stream):
-            for h, d in ins:
-                d.copy_(h, non_blocking=True)
             work.step(stream)
-            for h, d in outs:
-                h.copy_(d, non_blocking=True)
+        done[k].record(stream)
 
-    for _ in range(warmup):
-        one()
-    torch.cuda.synchronize()
+    def download(i):
+        k = i % 2
+        down.wait_event(done[k])
+        with torch.cuda.stream(down):
+            for n in names_out:
+                host_out[k][n].copy_(sets[k][n], non_blocking=True)
+        fetched[k].record(down)
+
+    def run(n, a=None, b=None):
+        torch.cuda.synchronize()
+        for k in range(2):                 # events start out "already happened"
+            done[k].record(stream)
+            fetched[k].record(down)
+        if a is not None:
+            a.record(up)
+            down.wait_event(a)
+            stream.wait_event(a)
+        upload(0)
+        for i in range(n):
+            if i + 1 < n:
+                upload(i + 1)
+            compute(i)
+            download(i)
+        if b is not None:
+            b.record(down)
+        torch.cuda.synchronize()
+
+    run(warmup)
     a = torch.cuda.Event(enable_timing=True)
     b = torch.cuda.Event(enable_timing=True)
-    a.record(stream)
-    for _ in range(steps):
-        one()
-    b.record(stream)
-    b.synchronize()
+    run(steps, a, b)
+    for n, t in orig.items():
+        setattr(work, n, t)
+    # the last step's outputs came back intact
+    last = host_out[(steps - 1) % 2]
+    assert all(torch.equal(last[n], sets[(steps - 1) % 2][n].cpu()) for n in names_out)
     return a.elapsed_time(b) / steps, h2d, d2h
 
 
@@ -794,7 +837,10 @@ def main():
                      "kernel": "full_attn_decode (split kernel + combine)",
                      "traffic": kernel_traffic("full_decode_kernel")}),
         "e2e": {"value": round(job_throughput(B, world, e2e_ms), 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
+                "d2h_bytes_per_step": d2h,
+                "copies": "every step's inputs uploaded from pinned host memory and outputs read back, on their own "
+                          "streams with two device buffer sets: step i+1's upload and step i-1's download overlap "
+                          "step i; timed from the first upload to the end of the last download"},
         "gpu_launches": work.launches_per_step * args.steps,
         "clocks": clocks,
     }
