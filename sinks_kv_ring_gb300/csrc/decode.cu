@@ -33,7 +33,6 @@ constexpr int FD_SUB_K = 16 * DQK * 2;                 // 6144 B
 constexpr int FD_SUB_V = 16 * DV * 2;                  // 4096 B
 constexpr int FD_STAGE = FD_SUB_K + FD_SUB_V;          // 10240 B
 constexpr int FD_SMEM = 16 * DQK * 2 + FD_WARPS * FD_STAGES * FD_STAGE;
-constexpr int FD_TARGET_ITEMS = 152 * 8;
 static_assert(FD_WARPS * FD_STAGES * FD_STAGE >= FD_WARPS * 16 * (MO_STRIDE + 2) * 4, "merge area");
 
 // WINDOW = false: a full layer (keys 0..p, split partials to the workspace);
@@ -214,65 +213,124 @@ __global__ void __launch_bounds__(FD_WARPS * 32, 2)
   }
 }
 
-// Full layer, phase 2: merge the splits of each (sequence, KV head) by
-// log-sum-exp and normalise.  One CTA per (sequence, KV head); thread t owns
-// query head t / 16 of the group and value dims 8 * (t % 16) .. +7, and folds
-// the splits in one pass with a running maximum.
-__global__ void __launch_bounds__(256)
-    full_combine_kernel(const int64_t *__restrict__ pos, const int32_t *__restrict__ seq, int hq, int G,
-                        int hkv, int num_seqs, int64_t max_pos, long long max_ctx, int splits, int split_len,
+// Full layer, phase 2: merge the splits of each (sequence, KV head, q head)
+// row by log-sum-exp and normalise.  NW warps per row (NW in {1, 2, 4, 8},
+// from the split count) fold interleaved subsets of the splits with a
+// running maximum -- lane l owns value dims 4l..4l+3 -- and the row's first
+// warp merges their partial states from shared memory.  Eight warps per CTA,
+// 8 / NW rows per CTA, so short contexts with many sequences and one long
+// sequence with hundreds of splits both keep the GPU busy.
+constexpr int FC_WARPS = 8;
+
+__global__ void __launch_bounds__(FC_WARPS * 32)
+    full_combine_kernel(const int64_t *__restrict__ pos, const int32_t *__restrict__ seq, int B, int hq, int G,
+                        int hkv, int num_seqs, int64_t max_pos, long long max_ctx, int splits, int split_len, int nw,
                         const float *__restrict__ part_ml, const float *__restrict__ part_o,
                         uint16_t *__restrict__ out) {
-  const int b = blockIdx.x / hkv, kv = blockIdx.x % hkv;
-  const int g = threadIdx.x >> 4, d0 = 8 * (threadIdx.x & 15);
-  if (g >= G) return;
-  const long long p = pos[b];
-  const int s = seq[b];
-  const bool ok = p >= 0 && p < max_pos && p + 1 <= max_ctx && s >= 0 && s < num_seqs;
-  const int n = ok ? (int)(p / split_len) + 1 : 0;
-  float M = NEG_INF, L = 0.f, acc[8];
-#pragma unroll
-  for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+  __shared__ float s_ml[FC_WARPS][2];
+  __shared__ float4 s_acc[FC_WARPS][32];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int rows_per_cta = FC_WARPS / nw;
+  const long long row = (long long)blockIdx.x * rows_per_cta + warp / nw;  // ((b * hkv) + kv) * G + g
+  const int sub = warp % nw;
+  const bool have = row < (long long)B * hkv * G;
+  const int g = have ? (int)(row % G) : 0;
+  const int kv = have ? (int)((row / G) % hkv) : 0;
+  const int b = have ? (int)(row / ((long long)G * hkv)) : 0;
+  int n = 0;
+  if (have) {
+    const long long p = pos[b];
+    const int s = seq[b];
+    const bool ok = p >= 0 && p < max_pos && p + 1 <= max_ctx && s >= 0 && s < num_seqs;
+    n = ok ? (int)(p / split_len) + 1 : 0;
+  }
+  float M = NEG_INF, L = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 4
-  for (int i = 0; i < n; ++i) {
+  for (int i = sub; i < n; i += nw) {
     const long long w = ((long long)b * splits + i) * hkv + kv;
     const float2 ml = *reinterpret_cast<const float2 *>(part_ml + (w * G + g) * 2);
-    const float4 o0 = *reinterpret_cast<const float4 *>(part_o + (w * G + g) * DV + d0);
-    const float4 o1 = *reinterpret_cast<const float4 *>(part_o + (w * G + g) * DV + d0 + 4);
+    const float4 o = *reinterpret_cast<const float4 *>(part_o + (w * G + g) * DV + 4 * lane);
     if (ml.x == NEG_INF) continue;
     const float Mn = fmaxf(M, ml.x);
     const float c = ex2(M - Mn), f = ex2(ml.x - Mn);  // M = -inf gives c = 0
     L = L * c + ml.y * f;
-    acc[0] = acc[0] * c + o0.x * f; acc[1] = acc[1] * c + o0.y * f;
-    acc[2] = acc[2] * c + o0.z * f; acc[3] = acc[3] * c + o0.w * f;
-    acc[4] = acc[4] * c + o1.x * f; acc[5] = acc[5] * c + o1.y * f;
-    acc[6] = acc[6] * c + o1.z * f; acc[7] = acc[7] * c + o1.w * f;
+    acc.x = acc.x * c + o.x * f;
+    acc.y = acc.y * c + o.y * f;
+    acc.z = acc.z * c + o.z * f;
+    acc.w = acc.w * c + o.w * f;
     M = Mn;
   }
+  if (nw > 1) {
+    if (lane == 0) {
+      s_ml[warp][0] = M;
+      s_ml[warp][1] = L;
+    }
+    s_acc[warp][lane] = acc;
+    __syncthreads();
+    if (sub == 0) {
+      float Mt = NEG_INF;
+      for (int u = 0; u < nw; ++u) Mt = fmaxf(Mt, s_ml[warp + u][0]);
+      L = 0.f;
+      acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (Mt != NEG_INF) {
+        for (int u = 0; u < nw; ++u) {
+          const float mu = s_ml[warp + u][0];
+          if (mu == NEG_INF) continue;
+          const float f = ex2(mu - Mt);
+          const float4 o = s_acc[warp + u][lane];
+          L += s_ml[warp + u][1] * f;
+          acc.x += o.x * f;
+          acc.y += o.y * f;
+          acc.z += o.z * f;
+          acc.w += o.w * f;
+        }
+      }
+    }
+  }
+  if (!have || sub != 0) return;
   const float inv = L > 0.f ? 1.f / L : 0.f;
-  uint4 w4;
-  w4.x = pack_bf16(acc[0] * inv, acc[1] * inv);
-  w4.y = pack_bf16(acc[2] * inv, acc[3] * inv);
-  w4.z = pack_bf16(acc[4] * inv, acc[5] * inv);
-  w4.w = pack_bf16(acc[6] * inv, acc[7] * inv);
-  *reinterpret_cast<uint4 *>(out + ((long long)b * hq + (long long)kv * G + g) * DV + d0) = w4;
+  uint2 w2;
+  w2.x = pack_bf16(acc.x * inv, acc.y * inv);
+  w2.y = pack_bf16(acc.z * inv, acc.w * inv);
+  *reinterpret_cast<uint2 *>(out + ((long long)b * hq + (long long)kv * G + g) * DV + 4 * lane) = w2;
 }
 
 }  // namespace
 
 // ---------------------------------------------------------------------------
 
+// Split plan.  The split kernel is persistent with R = 2 CTAs per SM taking
+// the items (sequence, split, KV head) round-robin, so a CTA does
+// ceil(items / R) items of `len` keys, each with a fixed cost (query tile,
+// pipeline fill, partial-state store) worth about FD_ITEM_KEYS keys.  The
+// plan takes the split count n minimising ceil(items / R) * (len + that
+// cost) among the counts that give about k items per resident CTA,
+// k = 1..8; ties go to fewer splits.  Measured at batch 1 and 4: one item
+// per CTA beats eight short ones by 1.5x; at batch 16, four per CTA beat an
+// uneven 1.05.
+constexpr long long FD_ITEM_KEYS = 300;
+
 DecodePlan full_decode_plan(int B, int hkv, long long max_ctx) {
-  long long len0 = ((long long)B * hkv * max_ctx + FD_TARGET_ITEMS - 1) / FD_TARGET_ITEMS;
-  if (len0 < 512) len0 = 512;
-  if (len0 > 8192) len0 = 8192;
-  long long n = (max_ctx + len0 - 1) / len0;
-  long long len = ((max_ctx + n - 1) / n + 63) / 64 * 64;
-  n = (max_ctx + len - 1) / len;
-  DecodePlan pl;
-  pl.splits = (int)n;
-  pl.split_len = (int)len;
-  return pl;
+  const long long R = 2LL * num_sms();
+  const long long units = (long long)B * hkv;  // (sequence, KV head) pairs
+  long long best_cost = -1;
+  DecodePlan best{1, 64};
+  for (int k = 1; k <= 8; ++k) {
+    long long n = k * R / units;
+    if (n < 1) n = 1;
+    long long len = ((max_ctx + n - 1) / n + 63) / 64 * 64;
+    if (len > (1LL << 20)) len = 1LL << 20;  // keeps split_len * splits in range
+    n = (max_ctx + len - 1) / len;
+    const long long rounds = (units * n + R - 1) / R;
+    const long long cost = rounds * (len + FD_ITEM_KEYS);
+    if (best_cost < 0 || cost < best_cost || (cost == best_cost && n < best.splits)) {
+      best_cost = cost;
+      best.splits = (int)n;
+      best.split_len = (int)len;
+    }
+  }
+  return best;
 }
 
 static size_t align256(size_t x) { return (x + 255) / 256 * 256; }
@@ -303,8 +361,14 @@ cudaError_t launch_full_decode(const uint16_t *q, const int64_t *pos, const int3
       part_ml, part_o, status, 0, nullptr, nullptr);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  full_combine_kernel<<<B * hkv, 256, 0, st>>>(pos, seq, hq, G, hkv, pool.num_seqs, max_pos, max_ctx, pl.splits,
-                                               pl.split_len, part_ml, part_o, out);
+  // warps per merged row: about eight splits each, at most eight
+  int nw = 1;
+  while (nw < FC_WARPS && nw * 8 < pl.splits) nw *= 2;
+  const long long rows = (long long)B * hkv * G;
+  const long long ctas = (rows + FC_WARPS / nw - 1) / (FC_WARPS / nw);
+  full_combine_kernel<<<(unsigned)ctas, FC_WARPS * 32, 0, st>>>(pos, seq, B, hq, G, hkv, pool.num_seqs, max_pos,
+                                                               max_ctx, pl.splits, pl.split_len, nw, part_ml, part_o,
+                                                               out);
   return cudaGetLastError();
 }
 

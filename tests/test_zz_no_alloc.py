@@ -48,7 +48,8 @@ def test_noalloc_decode_matches_workspace_decode_on_two_calls(setup):
 
 
 def test_noalloc_decode_rejects_batches_past_the_scratch_size(setup):
-    B, max_ctx = 128, 131072
+    # partials of 2048 sequences x 4 KV heads x 16 q heads at one split each: 68 MB
+    B, max_ctx = 2048, 131072
     need = kvr.full_attn_decode_workspace_size(B, 64, 4, max_ctx)
     assert need > kvr.NOALLOC_SCRATCH_BYTES
     table = torch.zeros(max_ctx, 32, 2, dtype=torch.float32, device=DEV)
