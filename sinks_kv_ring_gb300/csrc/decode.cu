@@ -306,10 +306,17 @@ __global__ void __launch_bounds__(FC_WARPS * 32)
 // pipeline fill, partial-state store) worth about FD_ITEM_KEYS keys.  The
 // plan takes the split count n minimising ceil(items / R) * (len + that
 // cost) among the counts that give about k items per resident CTA,
-// k = 1..8; ties go to fewer splits.  Measured at batch 1 and 4: one item
-// per CTA beats eight short ones by 1.5x; at batch 16, four per CTA beat an
-// uneven 1.05.
+// k = 1..8, and whose splits are at most FD_MAX_LEN keys; ties go to fewer
+// splits.  The model sees only the longest context: the cap keeps a batch
+// of ragged contexts (a few at 1M among many short ones) in items small
+// enough to spread over the CTAs.  Measured: at batch 1 and 4 one item per
+// CTA beats eight short ones by 1.5x; at batch 16, four per CTA beat an
+// uneven 1.05; a cap of 8192 keys against 16K / 32K: the 128-sequence
+// ragged step 73.9 ms against 80.3 / 83.8, uniform batch 16 at 524K 3.01 ms
+// against 2.94 / 2.92.  The cap has 256 keys of headroom so that an 8K
+// context (8193 keys, 8256 rounded) is still one split.
 constexpr long long FD_ITEM_KEYS = 300;
+constexpr long long FD_MAX_LEN = 8192 + 256;
 
 DecodePlan full_decode_plan(int B, int hkv, long long max_ctx) {
   const long long R = 2LL * num_sms();
@@ -320,7 +327,7 @@ DecodePlan full_decode_plan(int B, int hkv, long long max_ctx) {
     long long n = k * R / units;
     if (n < 1) n = 1;
     long long len = ((max_ctx + n - 1) / n + 63) / 64 * 64;
-    if (len > (1LL << 20)) len = 1LL << 20;  // keeps split_len * splits in range
+    if (len > FD_MAX_LEN) continue;
     n = (max_ctx + len - 1) / len;
     const long long rounds = (units * n + R - 1) / R;
     const long long cost = rounds * (len + FD_ITEM_KEYS);
@@ -329,6 +336,10 @@ DecodePlan full_decode_plan(int B, int hkv, long long max_ctx) {
       best.splits = (int)n;
       best.split_len = (int)len;
     }
+  }
+  if (best_cost < 0) {  // even eight items per CTA would be longer than the cap
+    best.split_len = (int)FD_MAX_LEN;
+    best.splits = (int)((max_ctx + FD_MAX_LEN - 1) / FD_MAX_LEN);
   }
   return best;
 }
