@@ -185,6 +185,56 @@ def test_full_decode_split_boundaries(bsz, tables):
     assert kvr.device_status() == 0
 
 
+def _ragged_pool(syn, ctx, max_ctx, hkv, bsz, table, vs, seed):
+    """A paged pool with blocks for each sequence's own context only (shuffled
+    ids; entries past a context are -1), filled through the library."""
+    mb = (max_ctx + bsz - 1) // bsz
+    need = [(b, i) for b, c in enumerate(ctx) for i in range((c + bsz - 1) // bsz)]
+    ids = np.random.default_rng(seed).permutation(len(need))
+    tab = np.full((len(ctx), mb), -1, dtype=np.int32)
+    for (b, i), blk in zip(need, ids):
+        tab[b, i] = blk
+    pool = kvr.PagedLayout(torch.zeros(len(need), hkv, bsz, 192, dtype=torch.bfloat16, device=DEV),
+                           torch.zeros(len(need), hkv, bsz, 128, dtype=torch.bfloat16, device=DEV),
+                           torch.from_numpy(tab).to(DEV))
+    fill_paged(pool, syn, list(range(len(ctx))), ctx, table, vs)
+    return pool
+
+
+@pytest.mark.parametrize("case", ["one_long_sequence", "many_short_sequences", "ragged_past_the_split_cap"])
+def test_full_decode_split_plans(case, tables):
+    # The split count follows the batch size and the longest context: one
+    # sequence at 131072 (dozens of splits, the merge folds them over eight
+    # warps), 400 short sequences (one split each), 128 sequences of which four
+    # are far longer than the rest (splits at the length cap).
+    hq, hkv, bsz, vs = 64, 4, 64, 0.707
+    rng = np.random.default_rng({"one_long_sequence": 1, "many_short_sequences": 2,
+                                 "ragged_past_the_split_cap": 3}[case])
+    if case == "one_long_sequence":
+        ctx, max_ctx = [131072], 131072
+    elif case == "many_short_sequences":
+        ctx, max_ctx = [int(c) for c in rng.integers(1, 1025, 400)], 1024
+    else:
+        ctx = [int(c) for c in rng.integers(1, 2001, 128)]
+        for b in (5, 60, 61, 127):
+            ctx[b] = int(rng.integers(33000, 40001))
+        max_ctx = 40000
+    syn = Synth(2601 + len(ctx), dist="shifted", device=DEV)
+    pool = _ragged_pool(syn, ctx, max_ctx, hkv, bsz, tables[1e7], vs, len(ctx))
+    B = len(ctx)
+    q = syn.q(B, hq, hkv, seq=88)
+    pos = torch.tensor([c - 1 for c in ctx], dtype=torch.int64, device=DEV)
+    seq = torch.arange(B, dtype=torch.int32, device=DEV)
+    out = kvr.full_attn_decode(q, pos, seq, pool, tables[1e7], SCALE, max_ctx)
+    torch.cuda.synchronize()
+    assert kvr.device_status() == 0
+    longest = sorted(range(B), key=lambda b: -ctx[b])[:4]
+    sample = sorted(set(longest + [0, B - 1, B // 2]))
+    want = np.stack([oracle.attend_seq(q[b:b + 1], [ctx[b] - 1], *raw_kv(syn, hkv, b, 0, ctx[b]), 0, 1e7, vs,
+                                       SCALE, 0, None)[0] for b in sample])
+    compare_rows(out[sample], want, f"full decode, {case}")
+
+
 def test_full_decode_small_groups_and_reuse_of_workspace(tables):
     syn = Synth(2501, dist="plain", device=DEV)
     for hq, hkv in [(8, 2), (4, 4)]:
