@@ -51,7 +51,7 @@ enum {
   KVR_EINVAL = -1,       /* null pointer, bad size, Hq not a multiple of Hkv, wrong layout kind */
   KVR_ERANGE = -2,       /* a host-known position or length past the RoPE table or the pool */
   KVR_EWORKSPACE = -3,   /* workspace missing or smaller than the size query returned */
-  KVR_EUNSUPPORTED = -4, /* a shape this build does not handle (e.g. Hq/Hkv > 16) */
+  KVR_EUNSUPPORTED = -4, /* a shape the library does not handle (e.g. Hq/Hkv > 16) */
   KVR_ECUDA = -5         /* a CUDA runtime call or launch failed */
 };
 

@@ -19,7 +19,7 @@ from sinks_kv_ring_gb300.synth import Synth
 BLK = 4096
 SCALE = 1.0 / math.sqrt(192.0)
 
-# spec bar for bf16 outputs with fp32 accumulation
+# the parity bar for bf16 outputs with fp32 accumulation
 MAX_ABS = 2e-2
 REL_RMS = 1e-2
 
