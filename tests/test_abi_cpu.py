@@ -196,3 +196,35 @@ def test_pages_management_host_validation(L):
     assert gat(ctypes.byref(pg8), ctypes.byref(ring8), P, P, P, -1, None) == -1
     assert gat(ctypes.byref(pg8), ctypes.byref(ring8), None, P, P, 1, None) == -1
     assert gat(ctypes.byref(pg8), ctypes.byref(ring8), None, None, None, 0, None) == 0
+
+
+def _plan_items(B, hkv, max_ctx, sms=152):
+    """The decode split rule restated: among split counts giving about k items
+    per resident CTA (two per SM), k = 1..8, with splits of at most 8448 keys,
+    the one minimising rounds x (keys per split + 300); else 8448-key splits."""
+    R, units = 2 * sms, B * hkv
+    best = None
+    for k in range(1, 9):
+        n = max(1, k * R // units)
+        length = -(-(-(-max_ctx // n)) // 64) * 64
+        if length > 8448:
+            continue
+        n = -(-max_ctx // length)
+        cost = -(-(units * n) // R) * (length + 300)
+        if best is None or cost < best[0] or (cost == best[0] and n < best[1]):
+            best = (cost, n)
+    n = best[1] if best else -(-max_ctx // 8448)
+    return units * n
+
+
+@pytest.mark.parametrize("B,max_ctx", [(64, 32769), (1, 131073), (4, 32769), (16, 524289), (128, 1 << 20),
+                                        (700, 2048), (64, 8193)])
+def test_decode_workspace_follows_the_split_plan(L, B, max_ctx):
+    # workspace = fp32 (m, l) and 128 numerators per (item, q head of the
+    # group), each part rounded up to 256 bytes; no GPU here, so the library
+    # plans for 152 SMs
+    hq, hkv = 64, 4
+    items = _plan_items(B, hkv, max_ctx)
+    G = hq // hkv
+    want = -(-(items * G * 2 * 4) // 256) * 256 + -(-(items * G * 128 * 4) // 256) * 256
+    assert L.full_attn_decode_workspace_size(B, hq, hkv, max_ctx) == want
