@@ -63,6 +63,7 @@ constexpr int B_OFINAL = 160;   // [2]
 constexpr int B_TMEM = 176;     // u32: TMEM base address
 constexpr int B_ABORT = 180;    // u32: set when a wait timed out
 constexpr int B_DRAIN = 192;    // all MMAs of the CTA done (before TMEM is freed)
+constexpr int B_QFULL = 200;    // the query tiles' TMA boxes landed
 
 // Every lane waits on the barrier; the warp agrees on the outcome so that it
 // stays converged for the warp-collective (.sync.aligned / elect.sync)
@@ -89,6 +90,7 @@ struct TcArgs {
   const int32_t *slot_pos;
   const float *sinks;
   int ring_seq;
+  int q_tma;  // query tiles come in as TMA boxes (tmq); else 16-byte copies
 };
 
 // Rows f0 .. f0+255 (those below nrows) of KV head kv's group, written as zeros.
@@ -115,7 +117,7 @@ template <bool VARLEN, bool WINDOW>
 __global__ void __launch_bounds__(TC_THREADS, 1)
     full_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                            const __grid_constant__ CUtensorMap tmk2, const __grid_constant__ CUtensorMap tmv2,
-                           const TcArgs a) {
+                           const __grid_constant__ CUtensorMap tmq, const TcArgs a) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -201,8 +203,18 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       mbar_init(sBar + B_OFINAL + 8 * i, 1);
     }
     mbar_init(sBar + B_DRAIN, 1);
+    mbar_init(sBar + B_QFULL, 1);
     *abort_flag = 0;
     fence_mbar_init();
+    if (a.q_tma) {
+      // Query tile r is rows f0 + 128r .. of the group: 128 / G positions
+      // starting at chunk position (f0 + 128r) / G, G heads, three 64-dim parts.
+      mbar_expect_tx(sBar + B_QFULL, nq * 3 * TC_SLOT);
+      for (int r = 0; r < nq; ++r)
+        for (int part = 0; part < 3; ++part)
+          tma_load_3d(base + r * TC_QTILE + part * TC_SLOT, &tmq, 64 * part, kv * a.G,
+                      (int)(crow0 + ((int)f0 + 128 * r) / a.G), sBar + B_QFULL);
+    }
   }
   if (warp == 8) {
     tmem_alloc(sBar + B_TMEM, 512);
@@ -223,19 +235,56 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     const int g = live ? f - i * a.G : 0;
     return qc + ((long long)i * a.hq + kv * a.G + g) * DQK;
   };
-  // Dims 64..191 pass through: asynchronous 16-byte copies (zero-filled
-  // past the chunk), all in flight at once.
-  for (int it = tid; it < nq * 128 * 16; it += TC_THREADS) {
-    const int r = it >> 4, ch = 8 + (it & 15);
-    bool live;
-    const uint16_t *qh = q_row(r, live);
-    cp_async16(base + q_chunk(r, ch), live ? qh + ch * 8 : qc, live ? 16 : 0);
-  }
-  cp_async_commit();
-  // Dims 0..63: rotate-half with the table row of the position, four
-  // (row, chunk pair) items per thread, loads issued before any use.
-  {
-    constexpr int NB = (256 * 4 + TC_THREADS - 1) / TC_THREADS;
+  constexpr int NB = (256 * 4 + TC_THREADS - 1) / TC_THREADS;  // (row, chunk pair) items per thread
+  if (a.q_tma) {
+    // The boxes bring every dim; dims 0..63 are then rotated in place, the
+    // table rows fetched while the boxes land.  Rows past the chunk keep what
+    // the boxes brought (finite values; their outputs are never stored).
+    float4 tv[NB][4];
+    bool liv[NB];
+#pragma unroll
+    for (int k = 0; k < NB; ++k) {
+      const int it = tid + k * TC_THREADS;
+      const int r = it >> 2, c = it & 3;
+      liv[k] = it < nq * 128 * 4 && (int)f0 + r < (int)nrows;
+      if (liv[k]) {
+        const float4 *tr = reinterpret_cast<const float4 *>(a.table + (P0 + ((int)f0 + r) / a.G) * 64 + 16 * c);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) tv[k][u] = tr[u];
+      }
+    }
+    __syncthreads();  // the barrier's initialisation is visible
+    if (mbar_wait(sBar + B_QFULL, 0, abort_flag)) {
+#pragma unroll
+      for (int k = 0; k < NB; ++k) {
+        if (!liv[k]) continue;
+        const int it = tid + k * TC_THREADS;
+        const int r = it >> 2, c = it & 3;
+        float cs[16];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          cs[4 * u] = tv[k][u].x; cs[4 * u + 1] = tv[k][u].y; cs[4 * u + 2] = tv[k][u].z; cs[4 * u + 3] = tv[k][u].w;
+        }
+        uint4 *p1 = reinterpret_cast<uint4 *>(gbase + q_chunk(r, c));
+        uint4 *p2 = reinterpret_cast<uint4 *>(gbase + q_chunk(r, c + 4));
+        uint4 o1, o2;
+        rope_pair8(*p1, *p2, cs, o1, o2);
+        *p1 = o1;
+        *p2 = o2;
+      }
+    }
+  } else {
+    // Dims 64..191 pass through: asynchronous 16-byte copies (zero-filled
+    // past the chunk), all in flight at once.
+    for (int it = tid; it < nq * 128 * 16; it += TC_THREADS) {
+      const int r = it >> 4, ch = 8 + (it & 15);
+      bool live;
+      const uint16_t *qh = q_row(r, live);
+      cp_async16(base + q_chunk(r, ch), live ? qh + ch * 8 : qc, live ? 16 : 0);
+    }
+    cp_async_commit();
+    // Dims 0..63: rotate-half with the table row of the position, four
+    // (row, chunk pair) items per thread, loads issued before any use.
     uint4 x1[NB], x2[NB];
     float4 tv[NB][4];
 #pragma unroll
@@ -640,7 +689,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (*abort_flag && tid == 0) flag(a.status, ST_TIMEOUT);
+  if (*abort_flag && tid == 0) {
+    flag(a.status, ST_TIMEOUT);
+    if (a.q_tma) {  // the query boxes must have landed before the CTA leaves (time bound only)
+      volatile uint32_t local = 0;
+      mbar_wait(sBar + B_QFULL, 0, &local, 1000000000ull);
+    }
+  }
   if (warp == 8) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
@@ -693,8 +748,11 @@ cudaError_t launch_full_prefill(const uint16_t *q, int64_t P0, int C, int seq, i
   a.P0 = P0;
   a.C = C;
   a.bt = pool.block_table + (long long)seq * pool.max_blocks;
+  CUtensorMap mq;
+  a.q_tma = make_tma_map_q3d(&mq, q, C, hq, a.G) ? 1 : 0;
   const long long ctas = ((long long)C * a.G + 255) / 256 * a.hkv;
-  full_prefill_tc_kernel<false, false><<<(unsigned)ctas, TC_THREADS, TC_SMEM, st>>>(mk, mv, mk, mv, a);
+  full_prefill_tc_kernel<false, false><<<(unsigned)ctas, TC_THREADS, TC_SMEM, st>>>(mk, mv, mk, mv,
+                                                                                    a.q_tma ? mq : mk, a);
   return cudaGetLastError();
 }
 
@@ -711,9 +769,12 @@ cudaError_t launch_full_varlen(const uint16_t *q, const int32_t *cu_rows, const 
   const VarlenSizes z = varlen_sizes(n, T, hq, pool.hkv, max_ctx, 256, true);
   a.q = q;
   a.plan = varlen_plan_view(z, ws, cu_rows, P0, seq, n);
+  CUtensorMap mq;
+  a.q_tma = make_tma_map_q3d(&mq, q, T, hq, a.G) ? 1 : 0;
   e = launch_varlen_plan(a.plan, T, hq, pool.hkv, 256, max_ctx, pool.num_seqs, 0, 0, status, st);
   if (e != cudaSuccess) return e;
-  full_prefill_tc_kernel<true, false><<<(unsigned)z.items_max, TC_THREADS, TC_SMEM, st>>>(mk, mv, mk, mv, a);
+  full_prefill_tc_kernel<true, false><<<(unsigned)z.items_max, TC_THREADS, TC_SMEM, st>>>(mk, mv, mk, mv,
+                                                                                          a.q_tma ? mq : mk, a);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   return launch_varlen_combine(a.plan, z.prows_max, hq, out, st);
@@ -762,8 +823,11 @@ cudaError_t launch_swa_prefill_tc(const uint16_t *q, int64_t P0, int C, int seq,
   a.P0 = P0;
   a.C = C;
   a.ring_seq = seq;
+  CUtensorMap mq;
+  a.q_tma = make_tma_map_q3d(&mq, q, C, hq, a.G) ? 1 : 0;
   const long long ctas = ((long long)C * a.G + 255) / 256 * a.hkv;
-  full_prefill_tc_kernel<false, true><<<(unsigned)ctas, TC_THREADS, TC_SMEM, st>>>(m[0], m[1], m[2], m[3], a);
+  full_prefill_tc_kernel<false, true><<<(unsigned)ctas, TC_THREADS, TC_SMEM, st>>>(m[0], m[1], m[2], m[3],
+                                                                                   a.q_tma ? mq : m[0], a);
   return cudaGetLastError();
 }
 
@@ -781,12 +845,15 @@ cudaError_t launch_swa_varlen(const uint16_t *q, const int32_t *cu_rows, const i
   const VarlenSizes z = varlen_sizes(n, T, hq, hkv, max_pos, 256, false);
   a.q = q;
   a.plan = varlen_plan_view(z, ws, cu_rows, P0, seq, n);
+  CUtensorMap mq;
+  a.q_tma = make_tma_map_q3d(&mq, q, T, hq, a.G) ? 1 : 0;
   e = launch_varlen_plan(a.plan, T, hq, hkv, 256, max_pos, ring.num_seqs, SWA_SHORT_ROWS, SWA_SHORT_MAX_C, status,
                          st);
   if (e != cudaSuccess) return e;
   // Chunks of more than 32 query rows are tiled here; the short ones go to
   // the short-chunk kernel.
-  full_prefill_tc_kernel<true, true><<<(unsigned)z.items_max, TC_THREADS, TC_SMEM, st>>>(m[0], m[1], m[2], m[3], a);
+  full_prefill_tc_kernel<true, true><<<(unsigned)z.items_max, TC_THREADS, TC_SMEM, st>>>(m[0], m[1], m[2], m[3],
+                                                                                         a.q_tma ? mq : m[0], a);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   return launch_swa_short(q, a.plan, n, T, hq, chunk, ring, sinks, table, softmax_scale, out, status, st);
