@@ -107,11 +107,12 @@ constexpr int SWA_SHORT_MAX_C = 16;  // C of a short chunk
 bool make_tma_map_tokens4d(CUtensorMap *m, const void *ptr, long long T, int hkv, int width, int box_rows,
                            bool one_part = false);
 
-// 3-D tensor map over q [rows][hq][192] bf16 for the tensor-core kernel's
-// query tiles: a box of 64 dims x G heads x 128/G rows lands as 128 tile rows
-// (row = position * G + head) of 128 bytes, 128-byte swizzled.  False when G
-// does not divide 128 (those group sizes stage q with plain copies).
-bool make_tma_map_q3d(CUtensorMap *m, const void *ptr, long long rows, int hq, int G);
+// 3-D tensor map over [rows][hq][width] bf16 (q: width 192, out: width 128)
+// for the tensor-core kernel's query tiles: a box of 64 dims x G heads x
+// 128/G rows is 128 tile rows (row = position * G + head) of 128 bytes,
+// 128-byte swizzled.  False when G does not divide 128 (those group sizes
+// move q and out with plain copies).
+bool make_tma_map_heads3d(CUtensorMap *m, const void *ptr, long long rows, int hq, int width, int G);
 
 cudaError_t launch_ring_copy(const KvView &ring, const int32_t *seqs, int n, uint16_t *k_snap, uint16_t *v_snap,
                              int32_t *tags_snap, bool to_ring, unsigned *status, cudaStream_t st);

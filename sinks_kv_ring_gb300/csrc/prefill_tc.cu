@@ -91,6 +91,7 @@ struct TcArgs {
   const float *sinks;
   int ring_seq;
   int q_tma;  // query tiles come in as TMA boxes (tmq); else 16-byte copies
+  int o_tma;  // one chunk: output tiles leave as TMA boxes (tmo); else per-row stores
 };
 
 // Rows f0 .. f0+255 (those below nrows) of KV head kv's group, written as zeros.
@@ -117,7 +118,8 @@ template <bool VARLEN, bool WINDOW>
 __global__ void __launch_bounds__(TC_THREADS, 1)
     full_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                            const __grid_constant__ CUtensorMap tmk2, const __grid_constant__ CUtensorMap tmv2,
-                           const __grid_constant__ CUtensorMap tmq, const TcArgs a) {
+                           const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmo,
+                           const TcArgs a) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -643,6 +645,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       mbar_arrive(sBar + B_PREADY + 8 * wg);
     }
     if (ok) ok = warp_wait(sBar + B_OFINAL + 8 * wg, 0, abort_flag);
+    // The TMA epilogue needs all four warps of the group: they agree first
+    // (every warp reaches this barrier, whatever its own outcome).
+    bool box_store = false;
+    if constexpr (!VARLEN) {
+      if (a.o_tma) box_store = named_bar_and(1 + wg, 128, ok);
+    }
     if (ok && nsp > 1) {
       // One split of the keys: the unnormalised numerator, the max (log2
       // units) and the sum, merged later by varlen_combine_kernel.
@@ -661,6 +669,38 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             dst[8 * c + u] = make_float4(__uint_as_float(o[4 * u]), __uint_as_float(o[4 * u + 1]),
                                          __uint_as_float(o[4 * u + 2]), __uint_as_float(o[4 * u + 3]));
         }
+      }
+    } else if (box_store) {
+      // One chunk: every row of the tile inside the output tensor is live, so
+      // the tile goes out as two TMA boxes (dims 0-63, 64-127) staged in its
+      // query region, which no product reads once O is final.
+      tc_fence_after();
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const uint32_t stage = base + wg * TC_QTILE;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t o[32];
+        tmem_ld32(tO + 32 * c, o);
+        tmem_wait_ld();
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const uint32_t w0 = pack_bf16(__uint_as_float(o[8 * u + 0]) * inv, __uint_as_float(o[8 * u + 1]) * inv);
+          const uint32_t w1 = pack_bf16(__uint_as_float(o[8 * u + 2]) * inv, __uint_as_float(o[8 * u + 3]) * inv);
+          const uint32_t w2 = pack_bf16(__uint_as_float(o[8 * u + 4]) * inv, __uint_as_float(o[8 * u + 5]) * inv);
+          const uint32_t w3 = pack_bf16(__uint_as_float(o[8 * u + 6]) * inv, __uint_as_float(o[8 * u + 7]) * inv);
+          const int ch = 4 * (c & 1) + u;  // 16-byte chunk of dims 8 * ch .. within the part
+          *reinterpret_cast<uint4 *>(gbase + wg * TC_QTILE + (c >> 1) * TC_SLOT + row * 128 +
+                                     ((ch ^ (row & 7)) << 4)) = make_uint4(w0, w1, w2, w3);
+        }
+      }
+      fence_proxy_async_smem();
+      named_bar_sync(1 + wg, 128);
+      if (row == 0) {
+        const int pos0 = (int)(crow0 + ((int)f0 + 128 * wg) / a.G);
+        tma_store_3d(&tmo, 0, kv * a.G, pos0, stage);
+        tma_store_3d(&tmo, 64, kv * a.G, pos0, stage + TC_SLOT);
+        bulk_commit();
+        bulk_wait_read_all();  // the staging area stays valid until read
       }
     } else if (ok) {
       tc_fence_after();
@@ -748,11 +788,12 @@ cudaError_t launch_full_prefill(const uint16_t *q, int64_t P0, int C, int seq, i
   a.P0 = P0;
   a.C = C;
   a.bt = pool.block_table + (long long)seq * pool.max_blocks;
-  CUtensorMap mq;
-  a.q_tma = make_tma_map_q3d(&mq, q, C, hq, a.G) ? 1 : 0;
+  CUtensorMap mq, mo;
+  a.q_tma = make_tma_map_heads3d(&mq, q, C, hq, DQK, a.G) ? 1 : 0;
+  a.o_tma = make_tma_map_heads3d(&mo, out, C, hq, DV, a.G) ? 1 : 0;
   const long long ctas = ((long long)C * a.G + 255) / 256 * a.hkv;
-  full_prefill_tc_kernel<false, false><<<(unsigned)ctas, TC_THREADS, TC_SMEM, st>>>(mk, mv, mk, mv,
-                                                                                    a.q_tma ? mq : mk, a);
+  full_prefill_tc_kernel<false, false><<<(unsigned)ctas, TC_THREADS, TC_SMEM, st>>>(
+      mk, mv, mk, mv, a.q_tma ? mq : mk, a.o_tma ? mo : mk, a);
   return cudaGetLastError();
 }
 
@@ -770,11 +811,11 @@ cudaError_t launch_full_varlen(const uint16_t *q, const int32_t *cu_rows, const 
   a.q = q;
   a.plan = varlen_plan_view(z, ws, cu_rows, P0, seq, n);
   CUtensorMap mq;
-  a.q_tma = make_tma_map_q3d(&mq, q, T, hq, a.G) ? 1 : 0;
+  a.q_tma = make_tma_map_heads3d(&mq, q, T, hq, DQK, a.G) ? 1 : 0;
   e = launch_varlen_plan(a.plan, T, hq, pool.hkv, 256, max_ctx, pool.num_seqs, 0, 0, status, st);
   if (e != cudaSuccess) return e;
-  full_prefill_tc_kernel<true, false><<<(unsigned)z.items_max, TC_THREADS, TC_SMEM, st>>>(mk, mv, mk, mv,
-                                                                                          a.q_tma ? mq : mk, a);
+  full_prefill_tc_kernel<true, false><<<(unsigned)z.items_max, TC_THREADS, TC_SMEM, st>>>(
+      mk, mv, mk, mv, a.q_tma ? mq : mk, mk, a);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   return launch_varlen_combine(a.plan, z.prows_max, hq, out, st);
@@ -823,11 +864,12 @@ cudaError_t launch_swa_prefill_tc(const uint16_t *q, int64_t P0, int C, int seq,
   a.P0 = P0;
   a.C = C;
   a.ring_seq = seq;
-  CUtensorMap mq;
-  a.q_tma = make_tma_map_q3d(&mq, q, C, hq, a.G) ? 1 : 0;
+  CUtensorMap mq, mo;
+  a.q_tma = make_tma_map_heads3d(&mq, q, C, hq, DQK, a.G) ? 1 : 0;
+  a.o_tma = make_tma_map_heads3d(&mo, out, C, hq, DV, a.G) ? 1 : 0;
   const long long ctas = ((long long)C * a.G + 255) / 256 * a.hkv;
-  full_prefill_tc_kernel<false, true><<<(unsigned)ctas, TC_THREADS, TC_SMEM, st>>>(m[0], m[1], m[2], m[3],
-                                                                                   a.q_tma ? mq : m[0], a);
+  full_prefill_tc_kernel<false, true><<<(unsigned)ctas, TC_THREADS, TC_SMEM, st>>>(
+      m[0], m[1], m[2], m[3], a.q_tma ? mq : m[0], a.o_tma ? mo : m[0], a);
   return cudaGetLastError();
 }
 
@@ -846,14 +888,14 @@ cudaError_t launch_swa_varlen(const uint16_t *q, const int32_t *cu_rows, const i
   a.q = q;
   a.plan = varlen_plan_view(z, ws, cu_rows, P0, seq, n);
   CUtensorMap mq;
-  a.q_tma = make_tma_map_q3d(&mq, q, T, hq, a.G) ? 1 : 0;
+  a.q_tma = make_tma_map_heads3d(&mq, q, T, hq, DQK, a.G) ? 1 : 0;
   e = launch_varlen_plan(a.plan, T, hq, hkv, 256, max_pos, ring.num_seqs, SWA_SHORT_ROWS, SWA_SHORT_MAX_C, status,
                          st);
   if (e != cudaSuccess) return e;
   // Chunks of more than 32 query rows are tiled here; the short ones go to
   // the short-chunk kernel.
-  full_prefill_tc_kernel<true, true><<<(unsigned)z.items_max, TC_THREADS, TC_SMEM, st>>>(m[0], m[1], m[2], m[3],
-                                                                                         a.q_tma ? mq : m[0], a);
+  full_prefill_tc_kernel<true, true><<<(unsigned)z.items_max, TC_THREADS, TC_SMEM, st>>>(
+      m[0], m[1], m[2], m[3], a.q_tma ? mq : m[0], m[0], a);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   return launch_swa_short(q, a.plan, n, T, hq, chunk, ring, sinks, table, softmax_scale, out, status, st);

@@ -93,6 +93,33 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *map, int x
       : "memory");
 }
 
+// Tiled store of a box from shared memory to global memory at non-negative
+// coordinates {x, y, z} (elements past the tensor's bounds are not written),
+// tracked by the bulk-async group of the issuing thread.
+__device__ __forceinline__ void tma_store_3d(const void *map, int x, int y, int z, uint32_t src) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(map), "r"(x),
+               "r"(y), "r"(z), "r"(src)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Wait until every committed bulk store has read its shared-memory source.
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// Barrier among `count` threads (a multiple of 32) on hardware barrier `id`
+// (1..15).  Every one of them must reach it: it has no time limit.
+__device__ __forceinline__ void named_bar_sync(int id, int count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+// The same barrier, returning the AND of `pred` over the participating threads.
+__device__ __forceinline__ bool named_bar_and(int id, int count, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n.reg .pred p, q;\nsetp.ne.u32 q, %1, 0;\nbar.red.and.pred p, %2, %3, q;\nselp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(r)
+      : "r"((uint32_t)pred), "r"(id), "r"(count)
+      : "memory");
+  return r != 0;
+}
+
 __device__ __forceinline__ void tma_load_4d_elect(uint32_t dst, const void *map, int x, int y, int z, int w,
                                                   uint32_t bar) {
   asm volatile(

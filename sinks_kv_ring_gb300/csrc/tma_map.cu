@@ -66,11 +66,11 @@ bool make_tma_map_tokens4d(CUtensorMap *m, const void *ptr, long long T, int hkv
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-bool make_tma_map_q3d(CUtensorMap *m, const void *ptr, long long rows, int hq, int G) {
+bool make_tma_map_heads3d(CUtensorMap *m, const void *ptr, long long rows, int hq, int width, int G) {
   EncodeTiledFn fn = encode_fn();
-  if (!fn || G < 1 || 128 % G || hq % G) return false;
-  cuuint64_t dims[3] = {192, (cuuint64_t)hq, (cuuint64_t)rows};
-  cuuint64_t strides[2] = {192 * 2, (cuuint64_t)hq * 192 * 2};
+  if (!fn || G < 1 || 128 % G || hq % G || width % 64) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)width, (cuuint64_t)hq, (cuuint64_t)rows};
+  cuuint64_t strides[2] = {(cuuint64_t)width * 2, (cuuint64_t)hq * width * 2};
   cuuint32_t box[3] = {64, (cuuint32_t)G, (cuuint32_t)(128 / G)};
   cuuint32_t estr[3] = {1, 1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box, estr,
