@@ -22,7 +22,10 @@
 // probabilities P of a tile are written over the first 64 columns of its S
 // and feed the P.V product straight from TMEM.
 // Shared memory: Q0, Q1 (3 x 16 KB each, 128-byte swizzled K-major) and a
-// ring of eight 16 KB slots.  Every K/V tile of 128 keys is five slot loads:
+// ring of eight 16 KB slots.  A query tile is three TMA boxes of q (128 / G
+// positions x G heads x 64 dims) when G divides 128, its dims 0-63 then
+// rotated in place; a single chunk's output tile leaves through its query
+// region as two TMA boxes.  Every K/V tile of 128 keys is five slot loads:
 // K dims 0-63, 64-127, 128-191 (K-major, for S = Q K^T) and V dims 0-63,
 // 64-127 (MN-major, for O += P V).  The three K loads and the two V loads of
 // a key tile each complete on one transaction barrier (double-buffered);
