@@ -1028,12 +1028,38 @@ class ProMixedWorkload:
         swa = layer_kv_bytes(ctx, self.hkv_swa, window=128)
         return self.kinds.count("full") * full + self.kinds.count("swa") * swa
 
+    BUCKETS = [(0, 65536, "0-64K"), (65536, 262144, "64K-256K"), (262144, 1 << 21, "256K-1M")]
+
     def buckets(self):
-        edges = [(0, 65536, "0-64K"), (65536, 262144, "64K-256K"), (262144, 1 << 21, "256K-1M")]
         out = {}
-        for lo, hi, name in edges:
+        for lo, hi, name in self.BUCKETS:
             sel = [c for c in self.ctx if lo <= c + 1 < hi]
             out[name] = {"sequences": len(sel), "tokens": int(sum(sel))}
+        return out
+
+    def bucket_times(self, hbm):
+        """One full layer's decode for each length bucket's sequences alone
+        (the batch a scheduler that groups requests by these buckets would
+        form; its own split plan), replayed over the distinct pools."""
+        kvr, dev = self.kvr, self.pos.device
+        out = {}
+        for lo, hi, name in self.BUCKETS:
+            idx = [b for b, c in enumerate(self.ctx) if lo <= c + 1 < hi]
+            if not idx:
+                continue
+            sel = torch.tensor(idx, dtype=torch.int64, device=dev)
+            seq, pos, q = sel.to(torch.int32), self.pos[sel].contiguous(), self.q[sel].contiguous()
+            mx = max(self.ctx[b] for b in idx) + 1
+            ws = torch.empty(kvr.full_attn_decode_workspace_size(len(idx), self.hq, self.hkv_full, mx),
+                             dtype=torch.uint8, device=dev)
+            o = torch.empty(len(idx), self.hq, 128, dtype=torch.bfloat16, device=dev)
+            calls = [(lambda st, pl=pl: kvr.full_attn_decode(q, pos, seq, pl, self.t7, SCALE, mx, workspace=ws, out=o,
+                                                             stream=st)) for pl in self.pools] * max(1, 8 // self.n_pools)
+            ms = graph_time_ms(calls)
+            nbytes = layer_kv_bytes([self.ctx[b] + 1 for b in idx], self.hkv_full)
+            gbs = nbytes / (ms / 1e3) / 1e9
+            out[name] = {"sequences": len(idx), "full_layer_ms": round(ms, 4), "bytes": nbytes, "GB/s": round(gbs, 1),
+                         "hbm_frac": round(gbs / hbm, 4)}
         return out
 
     def _eager_step(self, stream):
@@ -1107,6 +1133,8 @@ def pro_mixed(args, kvr, peaks_d, peaks_src, rank, world):
                         "kernel": f"whole {len(work.kinds)}-layer step",
                         "traffic": None}),
            "gpu_launches": work.launches_per_step * steps, "clocks": ck.summary()}
+    if len(set(work.ctx)) > 1:
+        res["buckets"] = work.bucket_times(hbm)
     if rank == 0:
         print(json.dumps(res), flush=True)
 

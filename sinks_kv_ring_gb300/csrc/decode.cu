@@ -23,9 +23,9 @@ namespace kvr {
 namespace {
 
 // ---------------------------------------------------------------------------
-// Full layer, phase 1: persistent CTAs walk the virtual items
-// (sequence, split, KV head); each real item streams its key range through
-// per-warp cp.async pipelines of 16-key subtiles and writes fp32 partials.
+// Full layer, phase 1: persistent CTAs walk the plan's items (sequence,
+// split, KV head) round-robin; each streams its key range through per-warp
+// cp.async pipelines of 16-key subtiles and writes fp32 partials.
 
 constexpr int FD_WARPS = 4;
 constexpr int FD_STAGES = 2;
@@ -33,6 +33,165 @@ constexpr int FD_SUB_K = 16 * DQK * 2;                 // 6144 B
 constexpr int FD_SUB_V = 16 * DV * 2;                  // 4096 B
 constexpr int FD_STAGE = FD_SUB_K + FD_SUB_V;          // 10240 B
 constexpr int FD_SMEM = 16 * DQK * 2 + FD_WARPS * FD_STAGES * FD_STAGE;
+// split plan (see full_decode_plan_kernel): the fixed cost of an item in keys,
+// the longest split, and where the per-sequence item prefix starts in the
+// plan (after L and the item count, 256-byte aligned)
+constexpr long long FD_ITEM_KEYS = 300;
+constexpr long long FD_MAX_LEN = 8192 + 256;
+constexpr int DPLAN_PREFIX = 64;
+
+// Full layer, phase 0: the split plan, from the batch's own contexts (one
+// CTA).  The split kernel is persistent with R = 2 CTAs per SM taking items
+// round-robin, so a CTA does ceil(items / R) items of up to L keys, each with
+// a fixed cost (query tile, pipeline fill, partial-state store) worth about
+// FD_ITEM_KEYS keys.  Candidate split lengths: those giving about k items per
+// resident CTA (k = 1..8) for the longest context alone, and for the batch's
+// total keys; capped at FD_MAX_LEN keys, at least 64.  The plan takes the
+// candidate minimising ceil(items / R) * (L + that cost) with the batch's
+// real item count (ties: fewer items), then writes L, the item count and the
+// per-sequence item prefix.  Sequences with a bad position or id get no items
+// (flagged here; the merge zeroes their rows).
+constexpr int DP_CANDS = 16;
+constexpr int DP_INLINE_MAX = 4096;  // batches the split kernel plans itself (prefix in shared memory)
+
+// The plan by one CTA of NT threads: the split length (returned), the item
+// count (*nitems) and the per-sequence item prefix (prefix[0..B]).  Flags bad
+// entries when `status` is not null.
+template <int NT>
+__device__ int decode_plan_block(const int64_t *__restrict__ pos, const int32_t *__restrict__ seq, int B, int hkv,
+                                 int num_seqs, int64_t max_pos, long long max_ctx, int R, int32_t *prefix,
+                                 int *nitems, unsigned *status) {
+  constexpr int NW = NT / 32;
+  __shared__ long long s_tot[NW], s_mx[NW];
+  __shared__ int s_cnt[NW][DP_CANDS];
+  __shared__ int s_scan[NW];
+  __shared__ int s_L;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  auto ctx_of = [&](int b) -> long long {
+    const long long p = pos[b];
+    const int s = seq[b];
+    return (p >= 0 && p < max_pos && p + 1 <= max_ctx && s >= 0 && s < num_seqs) ? p + 1 : 0;
+  };
+  // 1. total keys, longest context, bad entries
+  long long tot = 0, mx = 0;
+  unsigned bad = 0;
+  for (int b = tid; b < B; b += NT) {
+    const long long p = pos[b];
+    const int s = seq[b];
+    const bool bp = p < 0 || p >= max_pos || p + 1 > max_ctx, bs = s < 0 || s >= num_seqs;
+    if (bp || bs) {
+      bad |= (bp ? ST_BAD_POS : 0u) | (bs ? ST_BAD_SEQ : 0u);
+    } else {
+      tot += p + 1;
+      mx = p + 1 > mx ? p + 1 : mx;
+    }
+  }
+  if (bad && status) flag(status, bad);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    tot += __shfl_xor_sync(0xffffffffu, tot, o);
+    const long long y = __shfl_xor_sync(0xffffffffu, mx, o);
+    mx = y > mx ? y : mx;
+  }
+  if (lane == 0) {
+    s_tot[warp] = tot;
+    s_mx[warp] = mx;
+  }
+  __syncthreads();
+  tot = 0;
+  mx = 0;
+#pragma unroll
+  for (int i = 0; i < NW; ++i) {
+    tot += s_tot[i];
+    mx = s_mx[i] > mx ? s_mx[i] : mx;
+  }
+  // 2. candidate split lengths: lane c of every warp derives candidate c and
+  // the warp shares them by shuffles (GB300's FP64 rate is a small fraction of
+  // its integer rate, so no double arithmetic here; one 64-bit division per
+  // lane, the rest in 32 bits as contexts and split lengths fit)
+  unsigned mine_L;
+  {
+    const unsigned k = lane % 8 + 1;
+    unsigned L;
+    if (lane < 8) {  // about k items per resident CTA for the longest context
+      unsigned n = k * (unsigned)R / ((unsigned)B * (unsigned)hkv);
+      if (n < 1) n = 1;
+      L = ((unsigned)mx + n - 1) / n;
+    } else {         // ... for the batch's total keys
+      const unsigned long long d = (unsigned long long)k * (unsigned)R;
+      const unsigned long long l = ((unsigned long long)tot * (unsigned)hkv + d - 1) / d;
+      L = l > (unsigned long long)FD_MAX_LEN ? (unsigned)FD_MAX_LEN : (unsigned)l;
+    }
+    L = (L + 63) / 64 * 64;
+    mine_L = L < 64 ? 64u : (L > (unsigned)FD_MAX_LEN ? (unsigned)FD_MAX_LEN : L);
+  }
+  unsigned cand[DP_CANDS];
+#pragma unroll
+  for (int c = 0; c < DP_CANDS; ++c) cand[c] = __shfl_sync(0xffffffffu, mine_L, c);
+  // 3. items of every candidate, one combined reduction
+  int cnt[DP_CANDS];
+#pragma unroll
+  for (int c = 0; c < DP_CANDS; ++c) cnt[c] = 0;
+  for (int b = tid; b < B; b += NT) {
+    const unsigned ctx = (unsigned)ctx_of(b);
+#pragma unroll
+    for (int c = 0; c < DP_CANDS; ++c) cnt[c] += (int)((ctx + cand[c] - 1) / cand[c]);
+  }
+#pragma unroll
+  for (int c = 0; c < DP_CANDS; ++c) cnt[c] = __reduce_add_sync(0xffffffffu, cnt[c]);
+  if (lane == 0) {
+#pragma unroll
+    for (int c = 0; c < DP_CANDS; ++c) s_cnt[warp][c] = cnt[c];
+  }
+  __syncthreads();
+  // 4. choose: the least cost, ties to fewer items (one thread: measured
+  // quicker here than a warp-wide argmin)
+  if (tid == 0) {
+    unsigned best_L = (unsigned)FD_MAX_LEN, best_items = 0;
+    long long best_cost = -1;
+    for (int c = 0; c < DP_CANDS; ++c) {
+      unsigned items = 0;
+      for (int i = 0; i < NW; ++i) items += (unsigned)s_cnt[i][c];
+      items *= (unsigned)hkv;
+      const long long cost = (long long)((items + (unsigned)R - 1) / (unsigned)R) * (cand[c] + FD_ITEM_KEYS);
+      if (best_cost < 0 || cost < best_cost || (cost == best_cost && items < best_items)) {
+        best_cost = cost;
+        best_L = cand[c];
+        best_items = items;
+      }
+    }
+    s_L = (int)best_L;
+  }
+  __syncthreads();
+  const unsigned L = (unsigned)s_L;
+  // 5. per-sequence item prefix (exclusive scan, NT sequences at a time)
+  int running = 0;
+  for (int b0 = 0; b0 < B; b0 += NT) {
+    const int b = b0 + tid;
+    const int mine = b < B ? (int)(((unsigned)ctx_of(b) + L - 1) / L) * hkv : 0;
+    int x = mine;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    if (lane == 31) s_scan[warp] = x;
+    __syncthreads();
+    int before = 0, all = 0;
+#pragma unroll
+    for (int i = 0; i < NW; ++i) {
+      before += i < warp ? s_scan[i] : 0;
+      all += s_scan[i];
+    }
+    if (b < B) prefix[b] = running + before + x - mine;
+    running += all;
+    __syncthreads();  // s_scan is rewritten by the next round
+  }
+  if (tid == 0) prefix[B] = running;
+  *nitems = running;
+  return (int)L;
+}
+
 static_assert(FD_WARPS * FD_STAGES * FD_STAGE >= FD_WARPS * 16 * (MO_STRIDE + 2) * 4, "merge area");
 
 // WINDOW = false: a full layer (keys 0..p, split partials to the workspace);
@@ -44,29 +203,64 @@ __global__ void __launch_bounds__(FD_WARPS * 32, 2)
     full_decode_kernel(const uint16_t *__restrict__ q, const int64_t *__restrict__ pos,
                        const int32_t *__restrict__ seq, int B, int hq, int G, KvView pool,
                        const float *__restrict__ table, int64_t max_pos, float scale_log2,
-                       long long max_ctx, int splits, int split_len, float *__restrict__ part_ml,
-                       float *__restrict__ part_o, unsigned *status, int window,
+                       long long max_ctx, const int32_t *__restrict__ plan, int split_len,
+                       float *__restrict__ part_ml, float *__restrict__ part_o, unsigned *status, int window,
                        const float *__restrict__ sinks, uint16_t *__restrict__ out_direct) {
   extern __shared__ __align__(128) uint8_t smem[];
   uint8_t *sQ = smem;
   uint8_t *sStage = smem + 16 * DQK * 2;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int hkv = pool.hkv;
-  const long long nvirt = (long long)B * splits * hkv;
+  // Full layer: the items (sequence, split, KV head) of the device plan, in
+  // sequence order, sequence b owning items prefix[b] .. prefix[b+1]-1.
+  // Windowed layer: one item per (sequence, KV head).
+  // A batch of up to DP_INLINE_MAX sequences is planned by every CTA itself
+  // (the same inputs give every CTA the same plan; CTA 0 stores it for the
+  // merge); a larger one by full_decode_plan_kernel before this kernel.
+  const int32_t *prefix = plan + DPLAN_PREFIX;
+  long long nitems = (long long)B * hkv;
+  if (!WINDOW) {
+    if (B <= DP_INLINE_MAX) {
+      int32_t *sPrefix = reinterpret_cast<int32_t *>(smem + FD_SMEM);
+      int n;
+      split_len = decode_plan_block<FD_WARPS * 32>(pos, seq, B, hkv, pool.num_seqs, max_pos, max_ctx, gridDim.x,
+                                                   sPrefix, &n, blockIdx.x == 0 ? status : nullptr);
+      nitems = n;
+      if (blockIdx.x == 0) {
+        int32_t *gp = const_cast<int32_t *>(plan);
+        for (int b = tid; b <= B; b += blockDim.x) gp[DPLAN_PREFIX + b] = sPrefix[b];
+        if (tid == 0) {
+          gp[0] = split_len;
+          gp[1] = n;
+        }
+      }
+      prefix = sPrefix;
+    } else {
+      split_len = plan[0];
+      nitems = plan[1];
+    }
+  }
 
-  for (long long w = blockIdx.x; w < nvirt; w += gridDim.x) {
-    const int kv = (int)(w % hkv);
-    const int split = (int)((w / hkv) % splits);
-    const int b = (int)(w / ((long long)hkv * splits));
+  for (long long w = blockIdx.x; w < nitems; w += gridDim.x) {
+    int b, split, kv;
+    if (WINDOW) {
+      b = (int)(w / hkv);
+      kv = (int)(w % hkv);
+      split = 0;
+    } else {
+      b = plan_find(prefix, B, w);
+      const int local = (int)(w - prefix[b]);
+      split = local / hkv;
+      kv = local - split * hkv;
+    }
     const long long p = pos[b];
     const int s = seq[b];
     const bool bad_pos = p < 0 || p >= max_pos || p + 1 > max_ctx;
     const bool bad_seq = s < 0 || s >= pool.num_seqs;
-    if (bad_pos || bad_seq) {
-      if (split == 0 && kv == 0 && tid == 0)
-        flag(status, (bad_pos ? ST_BAD_POS : 0u) | (bad_seq ? ST_BAD_SEQ : 0u));
-      if (WINDOW && split == 0) {  // direct mode writes the zero rows itself
-        uint16_t *o = out_direct + ((long long)b * hq + (long long)kv * G) * DV;
+    if (bad_pos || bad_seq) {  // (the plan gives such a sequence no items; flagged there)
+      if (WINDOW) {
+        if (kv == 0 && tid == 0) flag(status, (bad_pos ? ST_BAD_POS : 0u) | (bad_seq ? ST_BAD_SEQ : 0u));
+        uint16_t *o = out_direct + ((long long)b * hq + (long long)kv * G) * DV;  // direct mode: zero rows
         for (int e = tid; e < G * DV; e += blockDim.x) o[e] = 0;
       }
       continue;  // otherwise the combine writes zeros for this sequence
@@ -213,10 +407,27 @@ __global__ void __launch_bounds__(FD_WARPS * 32, 2)
   }
 }
 
+// Batches past DP_INLINE_MAX sequences: the plan by a kernel of its own,
+// written to the workspace for the split and merge kernels.
+constexpr int DP_THREADS = 256;
+
+__global__ void __launch_bounds__(DP_THREADS)
+    full_decode_plan_kernel(const int64_t *__restrict__ pos, const int32_t *__restrict__ seq, int B, int hkv,
+                            int num_seqs, int64_t max_pos, long long max_ctx, int R, int32_t *__restrict__ plan,
+                            unsigned *status) {
+  int nitems;
+  const int L = decode_plan_block<DP_THREADS>(pos, seq, B, hkv, num_seqs, max_pos, max_ctx, R,
+                                              plan + DPLAN_PREFIX, &nitems, status);
+  if (threadIdx.x == 0) {
+    plan[0] = L;
+    plan[1] = nitems;
+  }
+}
+
 // Full layer, phase 2: merge the splits of each (sequence, KV head, q head)
 // row by log-sum-exp and normalise.  NW warps per row (NW in {1, 2, 4, 8},
-// from the split count) fold interleaved subsets of the splits with a
-// running maximum -- lane l owns value dims 4l..4l+3 -- and the row's first
+// from the expected split count) fold interleaved subsets of the splits with
+// a running maximum -- lane l owns value dims 4l..4l+3 -- and the row's first
 // warp merges their partial states from shared memory.  Eight warps per CTA,
 // 8 / NW rows per CTA, so short contexts with many sequences and one long
 // sequence with hundreds of splits both keep the GPU busy.
@@ -224,8 +435,8 @@ constexpr int FC_WARPS = 8;
 
 __global__ void __launch_bounds__(FC_WARPS * 32)
     full_combine_kernel(const int64_t *__restrict__ pos, const int32_t *__restrict__ seq, int B, int hq, int G,
-                        int hkv, int num_seqs, int64_t max_pos, long long max_ctx, int splits, int split_len, int nw,
-                        const float *__restrict__ part_ml, const float *__restrict__ part_o,
+                        int hkv, int num_seqs, int64_t max_pos, long long max_ctx, const int32_t *__restrict__ plan,
+                        int nw, const float *__restrict__ part_ml, const float *__restrict__ part_o,
                         uint16_t *__restrict__ out) {
   __shared__ float s_ml[FC_WARPS][2];
   __shared__ float4 s_acc[FC_WARPS][32];
@@ -237,18 +448,21 @@ __global__ void __launch_bounds__(FC_WARPS * 32)
   const int g = have ? (int)(row % G) : 0;
   const int kv = have ? (int)((row / G) % hkv) : 0;
   const int b = have ? (int)(row / ((long long)G * hkv)) : 0;
+  const int split_len = plan[0];
   int n = 0;
+  long long base = 0;
   if (have) {
     const long long p = pos[b];
     const int s = seq[b];
     const bool ok = p >= 0 && p < max_pos && p + 1 <= max_ctx && s >= 0 && s < num_seqs;
     n = ok ? (int)(p / split_len) + 1 : 0;
+    base = plan[DPLAN_PREFIX + b];
   }
   float M = NEG_INF, L = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 4
   for (int i = sub; i < n; i += nw) {
-    const long long w = ((long long)b * splits + i) * hkv + kv;
+    const long long w = base + (long long)i * hkv + kv;
     const float2 ml = *reinterpret_cast<const float2 *>(part_ml + (w * G + g) * 2);
     const float4 o = *reinterpret_cast<const float4 *>(part_o + (w * G + g) * DV + 4 * lane);
     if (ml.x == NEG_INF) continue;
@@ -300,24 +514,14 @@ __global__ void __launch_bounds__(FC_WARPS * 32)
 
 // ---------------------------------------------------------------------------
 
-// Split plan.  The split kernel is persistent with R = 2 CTAs per SM taking
-// the items (sequence, split, KV head) round-robin, so a CTA does
-// ceil(items / R) items of `len` keys, each with a fixed cost (query tile,
-// pipeline fill, partial-state store) worth about FD_ITEM_KEYS keys.  The
-// plan takes the split count n minimising ceil(items / R) * (len + that
-// cost) among the counts that give about k items per resident CTA,
-// k = 1..8, and whose splits are at most FD_MAX_LEN keys; ties go to fewer
-// splits.  The model sees only the longest context: the cap keeps a batch
-// of ragged contexts (a few at 1M among many short ones) in items small
-// enough to spread over the CTAs.  Measured: at batch 1 and 4 one item per
-// CTA beats eight short ones by 1.5x; at batch 16, four per CTA beat an
-// uneven 1.05; a cap of 8192 keys against 16K / 32K: the 128-sequence
-// ragged step 73.9 ms against 80.3 / 83.8, uniform batch 16 at 524K 3.01 ms
-// against 2.94 / 2.92.  The cap has 256 keys of headroom so that an 8K
-// context (8193 keys, 8256 rounded) is still one split.
-constexpr long long FD_ITEM_KEYS = 300;
-constexpr long long FD_MAX_LEN = 8192 + 256;
-
+// Uniform-batch estimate of the split plan (every sequence at max_ctx): the
+// first eight candidates of full_decode_plan_kernel.  The merge kernel sizes
+// its warps per row from it.  Measured with the plan taken this way: at batch
+// 1 and 4 one item per CTA beats eight short ones by 1.5x; at batch 16, four
+// per CTA beat an uneven 1.05; a cap of 8192 keys against 16K / 32K: the
+// 128-sequence ragged step 73.9 ms against 80.3 / 83.8, uniform batch 16 at
+// 524K 3.01 ms against 2.94 / 2.92.  The cap has 256 keys of headroom so that
+// an 8K context (8193 keys, 8256 rounded) is still one split.
 DecodePlan full_decode_plan(int B, int hkv, long long max_ctx) {
   const long long R = 2LL * num_sms();
   const long long units = (long long)B * hkv;  // (sequence, KV head) pairs
@@ -327,7 +531,7 @@ DecodePlan full_decode_plan(int B, int hkv, long long max_ctx) {
     long long n = k * R / units;
     if (n < 1) n = 1;
     long long len = ((max_ctx + n - 1) / n + 63) / 64 * 64;
-    if (len > FD_MAX_LEN) continue;
+    if (len > FD_MAX_LEN) len = FD_MAX_LEN;
     n = (max_ctx + len - 1) / len;
     const long long rounds = (units * n + R - 1) / R;
     const long long cost = rounds * (len + FD_ITEM_KEYS);
@@ -337,49 +541,67 @@ DecodePlan full_decode_plan(int B, int hkv, long long max_ctx) {
       best.split_len = (int)len;
     }
   }
-  if (best_cost < 0) {  // even eight items per CTA would be longer than the cap
-    best.split_len = (int)FD_MAX_LEN;
-    best.splits = (int)((max_ctx + FD_MAX_LEN - 1) / FD_MAX_LEN);
-  }
   return best;
 }
 
 static size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
+// Most items a device plan can give: a candidate of about k items per
+// resident CTA gives at most k * R plus one partial split per (sequence, KV
+// head); a capped one at most ceil(max_ctx / FD_MAX_LEN) splits per sequence.
+static long long decode_items_cap(int B, int hkv, long long max_ctx) {
+  const long long R = 2LL * num_sms(), units = (long long)B * hkv;
+  const long long a = 8 * R + units, c = units * ((max_ctx + FD_MAX_LEN - 1) / FD_MAX_LEN);
+  return a > c ? a : c;
+}
+
+// Workspace: the plan (L, item count, item prefix), then fp32 (m, l) and
+// numerators per (item, q head of the group).
+static size_t plan_bytes(int B) { return align256(((size_t)DPLAN_PREFIX + B + 1) * 4); }
+
 size_t full_decode_workspace(int B, int hq, int hkv, long long max_ctx) {
-  const DecodePlan pl = full_decode_plan(B, hkv, max_ctx);
-  const size_t items = (size_t)B * pl.splits * hkv;
+  const size_t items = (size_t)decode_items_cap(B, hkv, max_ctx);
   const size_t G = (size_t)(hq / hkv);
-  return align256(items * G * 2 * sizeof(float)) + align256(items * G * DV * sizeof(float));
+  return plan_bytes(B) + align256(items * G * 2 * sizeof(float)) + align256(items * G * DV * sizeof(float));
 }
 
 cudaError_t launch_full_decode(const uint16_t *q, const int64_t *pos, const int32_t *seq, int B, int hq,
                                const KvView &pool, const float *table, int64_t max_pos,
                                float softmax_scale, long long max_ctx, void *ws, uint16_t *out,
                                unsigned *status, cudaStream_t st) {
-  cudaError_t e = ensure_smem_limit(0, (const void *)full_decode_kernel<false>, FD_SMEM);
+  // shared memory: the stages, plus the plan's item prefix when the kernel plans itself
+  constexpr int FD_SMEM_MAX = FD_SMEM + (DP_INLINE_MAX + 1) * 4;
+  cudaError_t e = ensure_smem_limit(0, (const void *)full_decode_kernel<false>, FD_SMEM_MAX);
   if (e != cudaSuccess) return e;
   const int hkv = pool.hkv, G = hq / hkv;
-  const DecodePlan pl = full_decode_plan(B, hkv, max_ctx);
-  const size_t items = (size_t)B * pl.splits * hkv;
-  float *part_ml = reinterpret_cast<float *>(ws);
-  float *part_o = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(ws) +
-                                            align256(items * G * 2 * sizeof(float)));
-  long long grid = (long long)num_sms() * 2;
-  if (grid > (long long)items) grid = (long long)items;
-  full_decode_kernel<false><<<(unsigned)grid, FD_WARPS * 32, FD_SMEM, st>>>(
-      q, pos, seq, B, hq, G, pool, table, max_pos, softmax_scale * LOG2E, max_ctx, pl.splits, pl.split_len,
-      part_ml, part_o, status, 0, nullptr, nullptr);
+  const size_t items = (size_t)decode_items_cap(B, hkv, max_ctx);
+  int32_t *plan = reinterpret_cast<int32_t *>(ws);
+  uint8_t *w8 = reinterpret_cast<uint8_t *>(ws) + plan_bytes(B);
+  float *part_ml = reinterpret_cast<float *>(w8);
+  float *part_o = reinterpret_cast<float *>(w8 + align256(items * G * 2 * sizeof(float)));
+  const int R = 2 * num_sms();
+  int smem = FD_SMEM;
+  if (B <= DP_INLINE_MAX) {
+    smem += ((B + 1) * 4 + 15) / 16 * 16;
+  } else {
+    full_decode_plan_kernel<<<1, DP_THREADS, 0, st>>>(pos, seq, B, hkv, pool.num_seqs, max_pos, max_ctx, R, plan,
+                                                      status);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  full_decode_kernel<false><<<(unsigned)R, FD_WARPS * 32, smem, st>>>(
+      q, pos, seq, B, hq, G, pool, table, max_pos, softmax_scale * LOG2E, max_ctx, plan, 0, part_ml, part_o, status,
+      0, nullptr, nullptr);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   // warps per merged row: about eight splits each, at most eight
+  const DecodePlan est = full_decode_plan(B, hkv, max_ctx);
   int nw = 1;
-  while (nw < FC_WARPS && nw * 8 < pl.splits) nw *= 2;
+  while (nw < FC_WARPS && nw * 8 < est.splits) nw *= 2;
   const long long rows = (long long)B * hkv * G;
   const long long ctas = (rows + FC_WARPS / nw - 1) / (FC_WARPS / nw);
   full_combine_kernel<<<(unsigned)ctas, FC_WARPS * 32, 0, st>>>(pos, seq, B, hq, G, hkv, pool.num_seqs, max_pos,
-                                                               max_ctx, pl.splits, pl.split_len, nw, part_ml, part_o,
-                                                               out);
+                                                               max_ctx, plan, nw, part_ml, part_o, out);
   return cudaGetLastError();
 }
 
@@ -396,8 +618,8 @@ cudaError_t launch_swa_decode_paged(const uint16_t *q, const int64_t *pos, const
   long long grid = (long long)num_sms() * 2;
   if (grid > items) grid = items;
   full_decode_kernel<true><<<(unsigned)grid, FD_WARPS * 32, FD_SMEM, st>>>(
-      q, pos, seq, B, hq, G, pool, table, max_pos, softmax_scale * LOG2E, max_ctx, 1, WIN + 16, nullptr, nullptr,
-      status, WIN, sinks, out);
+      q, pos, seq, B, hq, G, pool, table, max_pos, softmax_scale * LOG2E, max_ctx, nullptr, WIN + 16, nullptr,
+      nullptr, status, WIN, sinks, out);
   return cudaGetLastError();
 }
 

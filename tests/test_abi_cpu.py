@@ -198,33 +198,25 @@ def test_pages_management_host_validation(L):
     assert gat(ctypes.byref(pg8), ctypes.byref(ring8), None, None, None, 0, None) == 0
 
 
-def _plan_items(B, hkv, max_ctx, sms=152):
-    """The decode split rule restated: among split counts giving about k items
-    per resident CTA (two per SM), k = 1..8, with splits of at most 8448 keys,
-    the one minimising rounds x (keys per split + 300); else 8448-key splits."""
-    R, units = 2 * sms, B * hkv
-    best = None
-    for k in range(1, 9):
-        n = max(1, k * R // units)
-        length = -(-(-(-max_ctx // n)) // 64) * 64
-        if length > 8448:
-            continue
-        n = -(-max_ctx // length)
-        cost = -(-(units * n) // R) * (length + 300)
-        if best is None or cost < best[0] or (cost == best[0] and n < best[1]):
-            best = (cost, n)
-    n = best[1] if best else -(-max_ctx // 8448)
-    return units * n
+def _items_cap(B, hkv, max_ctx, sms=152):
+    """The most items the decode split plan can give: a candidate of about k
+    items per resident CTA (two per SM, k <= 8) gives at most 8 x 2 x SMs plus
+    one partial split per (sequence, KV head); a split length capped at 8448
+    keys at most ceil(max_ctx / 8448) splits per sequence."""
+    units = B * hkv
+    return max(8 * 2 * sms + units, units * -(-max_ctx // 8448))
 
 
 @pytest.mark.parametrize("B,max_ctx", [(64, 32769), (1, 131073), (4, 32769), (16, 524289), (128, 1 << 20),
                                         (700, 2048), (64, 8193)])
 def test_decode_workspace_follows_the_split_plan(L, B, max_ctx):
-    # workspace = fp32 (m, l) and 128 numerators per (item, q head of the
-    # group), each part rounded up to 256 bytes; no GPU here, so the library
-    # plans for 152 SMs
+    # workspace = the plan (split length, item count, per-sequence item prefix
+    # after 64 header words), then fp32 (m, l) and 128 numerators per (item, q
+    # head of the group), each part rounded up to 256 bytes; no GPU here, so
+    # the library plans for 152 SMs
     hq, hkv = 64, 4
-    items = _plan_items(B, hkv, max_ctx)
+    items = _items_cap(B, hkv, max_ctx)
     G = hq // hkv
-    want = -(-(items * G * 2 * 4) // 256) * 256 + -(-(items * G * 128 * 4) // 256) * 256
+    up = lambda x: -(-x // 256) * 256
+    want = up((64 + B + 1) * 4) + up(items * G * 2 * 4) + up(items * G * 128 * 4)
     assert L.full_attn_decode_workspace_size(B, hq, hkv, max_ctx) == want
