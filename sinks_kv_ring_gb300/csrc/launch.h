@@ -62,6 +62,11 @@ cudaError_t launch_full_prefill(const uint16_t *q, int64_t P0, int C, int seq, i
 cudaError_t launch_swa_prefill_tc(const uint16_t *q, int64_t P0, int C, int seq, int hq, const KvView &chunk,
                                   const KvView &ring, const float *sinks, const float *table, float softmax_scale,
                                   uint16_t *out, unsigned *status, cudaStream_t st);
+// Windowed chunked prefill for group sizes G >= 8 dividing 128 (swa_band.cu):
+// *taken is false when the call does not fit it (nothing launched).
+cudaError_t launch_swa_band(const uint16_t *q, int64_t P0, int C, int seq, int hq, const KvView &chunk,
+                            const KvView &ring, const float *sinks, const float *table, float softmax_scale,
+                            uint16_t *out, unsigned *status, cudaStream_t st, bool *taken);
 // Sizes of the workspace of a varlen call (see VarlenPlan): n chunks, T rows,
 // contexts up to max_ctx, CTA items of tile_rows query rows; with `splits`,
 // chunks of one item are cut along the keys.

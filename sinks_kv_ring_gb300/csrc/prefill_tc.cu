@@ -857,9 +857,13 @@ cudaError_t tc_window_setup(const KvView &chunk, long long T, const KvView &ring
 cudaError_t launch_swa_prefill_tc(const uint16_t *q, int64_t P0, int C, int seq, int hq, const KvView &chunk,
                                   const KvView &ring, const float *sinks, const float *table, float softmax_scale,
                                   uint16_t *out, unsigned *status, cudaStream_t st) {
+  bool taken = false;
+  cudaError_t e = launch_swa_band(q, P0, C, seq, hq, chunk, ring, sinks, table, softmax_scale, out, status, st,
+                                  &taken);
+  if (e != cudaSuccess || taken) return e;
   CUtensorMap m[4];
   TcArgs a;
-  cudaError_t e = tc_window_setup(chunk, C, ring, hq, sinks, table, softmax_scale, out, status, m, &a);
+  e = tc_window_setup(chunk, C, ring, hq, sinks, table, softmax_scale, out, status, m, &a);
   if (e != cudaSuccess) return e;
   e = ensure_smem_limit(7, (const void *)full_prefill_tc_kernel<false, true>, TC_SMEM);
   if (e != cudaSuccess) return e;

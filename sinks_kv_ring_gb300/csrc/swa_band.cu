@@ -1,0 +1,560 @@
+// swa_band.cu -- chunked prefill of a windowed layer on the tensor cores, one
+// 144-key band per tile of query rows, persistent CTAs.
+//
+// colibri "MiMo-V2.6 (Xiaomi)", "What the engine implements": the sink joins
+// the softmax denominator and nothing else; gaudi-cookbook "MiMo-V2.6-Flash on
+// Gaudi 2", "What was built": the window is exactly the last 128 positions, so
+// row i of a chunk at P0 (position P0 + i) attends positions P0+i-127..P0+i;
+// colibri "System One mode and prompt reuse": a position before the chunk
+// sits in ring slot p mod 128, whose tag records the position it holds.
+//
+// A work item is 128 query rows of one KV head's GQA group: np = 128 / G
+// consecutive chunk rows r0 .. r0+np-1 (np <= 16) times the G heads, row
+// d * G + g.  Every key such a row can attend lies in chunk rows r0-128 ..
+// r0+15, one band of 144 keys, so an item is one S = Q K^T (N = 144) and one
+// O = P V, and its softmax is a single pass with no rescaling: the window
+// and the sink are all there.  In band column t (chunk row r0-128+t) row d
+// attends columns d+1 .. d+128.  Band rows before the chunk come back from
+// the TMA unit as zeros (a negative coordinate); for the first items the
+// rows whose ring slot holds their position are then copied in.
+//
+// One CTA per SM, 320 threads:
+//   warps 0-3  softmax of item i, then the epilogue of item i-1 (thread =
+//              row = TMEM lane)
+//   warps 4-7  RoPE of each query tile in shared memory; the ring rows of
+//              the items that reach before the chunk
+//   warp  8    TMEM owner and MMA issuer (converged; elect.sync issues)
+//   warp  9    TMA producer (converged; elect.sync issues)
+// Shared memory: two query tiles (3 x 16 KB each, 128-byte swizzled,
+// K-major), the band's K (3 x 18 KB, K-major) and V (2 x 18 KB, MN-major),
+// one output tile (2 x 16 KB) that leaves as two TMA boxes.  The next
+// item's query tile loads while the current one is computed; the band's K
+// reloads once S = Q K^T is done, its V once P V is done.
+// TMEM (512 columns): S0 at 0, S1 at 160 (144 fp32 columns each; the bf16
+// probabilities P overwrite the first 72 and feed P V from TMEM), O at 320.
+#include <cuda.h>
+
+#include "launch.h"
+#include "tc_ptx.cuh"
+
+namespace kvr {
+namespace {
+
+using namespace tc;
+
+constexpr int SB_THREADS = 320;
+constexpr int SB_N = 144;                          // keys of a band
+constexpr int SB_QPART = 128 * 128;                // 128 rows x 64 dims
+constexpr int SB_QTILE = 3 * SB_QPART;
+constexpr int SB_KPART = SB_N * 128;               // 144 keys x 64 dims
+constexpr int SB_OFF_K = 2 * SB_QTILE;
+constexpr int SB_OFF_V = SB_OFF_K + 3 * SB_KPART;
+constexpr int SB_OFF_O = SB_OFF_V + 2 * SB_KPART;
+constexpr int SB_OFF_BAR = SB_OFF_O + 2 * SB_QPART;
+constexpr int SB_OFF_TAG = SB_OFF_BAR + 256;       // 128 bits: ring slot c holds its pre-chunk position
+constexpr int SB_SMEM = SB_OFF_TAG + 16 + 1024;    // + alignment slack
+static_assert(SB_OFF_K % 1024 == 0 && SB_KPART % 1024 == 0 && SB_OFF_V % 1024 == 0 && SB_OFF_O % 1024 == 0,
+              "swizzled tiles start on 1024-byte boundaries");
+static_assert(SB_SMEM <= 227 * 1024, "one CTA per SM");
+constexpr uint32_t SB_COL_S1 = 160, SB_COL_O = 320;
+constexpr unsigned ST_TIMEOUT = 8u;
+
+// barrier area (byte offsets): [2] = one per query tile / S buffer
+constexpr int SBB_QFULL = 0;    // [2] query tile landed (TMA bytes)
+constexpr int SBB_QROPE = 16;   // [2] query tile rotated (128 arrivals)
+constexpr int SBB_QFREE = 32;   // [2] S = Q K^T of the tile done
+constexpr int SBB_SFULL = 48;   // [2] S in TMEM
+constexpr int SBB_PREADY = 64;  // [2] P in TMEM (128 arrivals)
+constexpr int SBB_KFULL = 80;   // band K landed
+constexpr int SBB_VFULL = 88;   // band V landed
+constexpr int SBB_KFREE = 96;   // band K read by S = Q K^T
+constexpr int SBB_VFREE = 104;  // band V read by P V
+constexpr int SBB_KPATCH = 112; // ring rows copied into K (128 arrivals)
+constexpr int SBB_VPATCH = 120; // ring rows copied into V (128 arrivals)
+constexpr int SBB_OFULL = 128;  // O in TMEM
+constexpr int SBB_OFREE = 136;  // O read out of TMEM (128 arrivals)
+constexpr int SBB_DRAIN = 144;  // every MMA of the CTA done
+constexpr int SBB_TMEM = 152;   // u32: TMEM base
+constexpr int SBB_ABORT = 156;  // u32: a wait timed out
+
+struct SbArgs {
+  long long P0;
+  int C, hq, G, hkv, np, nitems;
+  int ring_seq;
+  const int32_t *slot_pos;  // [ring sequences][128]
+  const uint16_t *ring_k;   // [ring sequences][hkv][128][192]
+  const uint16_t *ring_v;   // [ring sequences][hkv][128][128]
+  const float *sinks;
+  const float *table;
+  float scale_log2;
+  unsigned *status;
+};
+
+__device__ __forceinline__ bool sb_wait(uint32_t bar, uint32_t parity, volatile uint32_t *abort) {
+  const bool ok = mbar_wait(bar, parity, abort);
+  return __all_sync(0xffffffffu, ok);
+}
+
+// Item i of this CTA: KV head and first chunk row.
+__device__ __forceinline__ void sb_item(const SbArgs &a, int i, int &kv, int &r0) {
+  const int w = (int)blockIdx.x + i * (int)gridDim.x;
+  kv = w % a.hkv;
+  r0 = (w / a.hkv) * a.np;
+}
+// Bits lo .. hi (clamped to 0 .. 31) of a word.
+__device__ __forceinline__ uint32_t span_bits(int lo, int hi) {
+  lo = lo < 0 ? 0 : lo;
+  hi = hi > 31 ? 31 : hi;
+  return lo > hi ? 0u : (0xffffffffu >> (31 - hi)) & (0xffffffffu << lo);
+}
+// An item whose rows reach before the chunk: those band columns are
+// attended only where the position exists and its ring slot holds it.
+__device__ __forceinline__ bool sb_boundary(int r0) { return r0 < WIN - 1; }
+
+__global__ void __launch_bounds__(SB_THREADS, 1)
+    swa_band_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmo,
+                    const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
+                    const SbArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t *gbase = smem_raw + (base - raw);
+  const uint32_t sK = base + SB_OFF_K, sV = base + SB_OFF_V, sO = base + SB_OFF_O, sBar = base + SB_OFF_BAR;
+  volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(gbase + SB_OFF_BAR + SBB_ABORT);
+  const uint32_t *held = reinterpret_cast<const uint32_t *>(gbase + SB_OFF_TAG);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int n_my = (int)blockIdx.x < a.nitems ? (a.nitems - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+
+  if (tid == 0) {
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(sBar + SBB_QFULL + 8 * i, 1);
+      mbar_init(sBar + SBB_QROPE + 8 * i, 128);
+      mbar_init(sBar + SBB_QFREE + 8 * i, 1);
+      mbar_init(sBar + SBB_SFULL + 8 * i, 1);
+      mbar_init(sBar + SBB_PREADY + 8 * i, 128);
+    }
+    mbar_init(sBar + SBB_KFULL, 1);
+    mbar_init(sBar + SBB_VFULL, 1);
+    mbar_init(sBar + SBB_KFREE, 1);
+    mbar_init(sBar + SBB_VFREE, 1);
+    mbar_init(sBar + SBB_KPATCH, 128);
+    mbar_init(sBar + SBB_VPATCH, 128);
+    mbar_init(sBar + SBB_OFULL, 1);
+    mbar_init(sBar + SBB_OFREE, 128);
+    mbar_init(sBar + SBB_DRAIN, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (tid < WIN) {
+    // Ring slot c stands for position P0 - 128 + ((c - P0) mod 128).
+    const long long pos = a.P0 - WIN + ((tid - (int)(a.P0 & (WIN - 1))) & (WIN - 1));
+    const bool h = pos >= 0 && a.slot_pos[(long long)a.ring_seq * WIN + tid] == (int32_t)pos;
+    const unsigned bits = __ballot_sync(0xffffffffu, h);
+    if (lane == 0) reinterpret_cast<uint32_t *>(gbase + SB_OFF_TAG)[warp] = bits;
+  }
+  if (warp == 8) {
+    tmem_alloc(sBar + SBB_TMEM, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(gbase + SB_OFF_BAR + SBB_TMEM);
+
+  if (warp == 9) {
+    // ------------------------------------------------------------ TMA producer
+    // Order of the loads follows the order in which their buffers come free:
+    // S(i-1) frees the band's K and the query tile of item i+1, P V(i-1) the
+    // band's V.
+    int last_q0 = -1, last_q1 = -1, last_k = -1, last_v = -1;
+    auto load_q = [&](int i) {
+      int kv, r0;
+      sb_item(a, i, kv, r0);
+      const uint32_t bar = sBar + SBB_QFULL + 8 * (i & 1);
+      mbar_expect_tx_elect(bar, SB_QTILE);
+      for (int part = 0; part < 3; ++part)
+        tma_load_3d_elect(base + (i & 1) * SB_QTILE + part * SB_QPART, &tmq, 64 * part, kv * a.G, r0, bar);
+      (i & 1 ? last_q1 : last_q0) = i;
+    };
+    auto load_band = [&](int i, bool v) {
+      int kv, r0;
+      sb_item(a, i, kv, r0);
+      const uint32_t bar = sBar + (v ? SBB_VFULL : SBB_KFULL);
+      const int parts = v ? 2 : 3;
+      mbar_expect_tx_elect(bar, parts * SB_KPART);
+      for (int part = 0; part < parts; ++part)
+        tma_load_4d_elect((v ? sV : sK) + part * SB_KPART, v ? (const void *)&tmv : (const void *)&tmk, 0, part, kv,
+                          r0 - 128, bar);
+      (v ? last_v : last_k) = i;
+    };
+    if (n_my > 0) {
+      load_q(0);
+      load_band(0, false);
+      load_band(0, true);
+      if (n_my > 1) load_q(1);
+    }
+    for (int i = 1; i < n_my; ++i) {
+      if (!sb_wait(sBar + SBB_KFREE, (uint32_t)(i - 1) & 1u, abort_flag)) break;
+      load_band(i, false);
+      if (i + 1 < n_my) {
+        if (!sb_wait(sBar + SBB_QFREE + 8 * ((i + 1) & 1), (uint32_t)((i - 1) >> 1) & 1u, abort_flag)) break;
+        load_q(i + 1);
+      }
+      if (!sb_wait(sBar + SBB_VFREE, (uint32_t)(i - 1) & 1u, abort_flag)) break;
+      load_band(i, true);
+    }
+    // On an abort, the loads already issued land before the CTA leaves
+    // (bounded by time only: the abort flag is already set).
+    if (*abort_flag && lane == 0) {
+      volatile uint32_t local = 0;
+      for (int s = 0; s < 2; ++s) {
+        const int lq = s ? last_q1 : last_q0;
+        if (lq >= 0) {
+          local = 0;
+          mbar_wait(sBar + SBB_QFULL + 8 * s, (uint32_t)(lq >> 1) & 1u, &local, 1000000000ull);
+        }
+      }
+      if (last_k >= 0) {
+        local = 0;
+        mbar_wait(sBar + SBB_KFULL, (uint32_t)last_k & 1u, &local, 1000000000ull);
+      }
+      if (last_v >= 0) {
+        local = 0;
+        mbar_wait(sBar + SBB_VFULL, (uint32_t)last_v & 1u, &local, 1000000000ull);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 8) {
+    // ------------------------------------------------------------ MMA issuer
+    // Order: S(0), then S(i), P V(i-1) for i = 1.. (the tensor core computes
+    // the next tile's scores while the softmax warps work on the last ones),
+    // then P V of the last item.
+    const uint32_t id_s = idesc_bf16(128, SB_N, 0, 0);
+    const uint32_t id_pv = idesc_bf16(128, 128, 0, 1);
+    const uint64_t dk = sdesc_sw128(sK, 16, 1024);
+    const uint64_t dv = sdesc_sw128(sV, SB_KPART, 1024);  // LBO = the other 64-dim half of V
+    int nbk = 0, nbv = 0;  // boundary items met (their patch barriers' phases)
+    auto issue_S = [&](int i) -> bool {
+      int kv, r0;
+      sb_item(a, i, kv, r0);
+      const int q = i & 1;
+      if (!sb_wait(sBar + SBB_QROPE + 8 * q, (uint32_t)(i >> 1) & 1u, abort_flag)) return false;
+      if (!sb_wait(sBar + SBB_KFULL, (uint32_t)i & 1u, abort_flag)) return false;
+      if (sb_boundary(r0)) {
+        if (!sb_wait(sBar + SBB_KPATCH, (uint32_t)nbk & 1u, abort_flag)) return false;
+        ++nbk;
+      }
+      tc_fence_after();
+      const uint64_t dq = sdesc_sw128(base + q * SB_QTILE, 16, 1024);
+      const uint32_t d = tmem + (q ? SB_COL_S1 : 0u);
+      for (int kb = 0; kb < 3; ++kb) {
+        const uint64_t a0 = dq + (uint64_t)((kb * SB_QPART) >> 4);
+        const uint64_t b0 = dk + (uint64_t)((kb * SB_KPART) >> 4);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) mma_ss_elect(d, a0 + 2 * kk, b0 + 2 * kk, id_s, (kb | kk) != 0);
+      }
+      mma_commit_elect(sBar + SBB_SFULL + 8 * q);
+      mma_commit_elect(sBar + SBB_KFREE);
+      mma_commit_elect(sBar + SBB_QFREE + 8 * q);
+      return true;
+    };
+    auto issue_PV = [&](int i) -> bool {
+      int kv, r0;
+      sb_item(a, i, kv, r0);
+      const int s = i & 1;
+      if (!sb_wait(sBar + SBB_PREADY + 8 * s, (uint32_t)(i >> 1) & 1u, abort_flag)) return false;
+      if (!sb_wait(sBar + SBB_VFULL, (uint32_t)i & 1u, abort_flag)) return false;
+      if (sb_boundary(r0)) {
+        if (!sb_wait(sBar + SBB_VPATCH, (uint32_t)nbv & 1u, abort_flag)) return false;
+        ++nbv;
+      }
+      if (i > 0 && !sb_wait(sBar + SBB_OFREE, (uint32_t)(i - 1) & 1u, abort_flag)) return false;
+      tc_fence_after();
+      const uint32_t ap = tmem + (s ? SB_COL_S1 : 0u);
+      const uint32_t d = tmem + SB_COL_O;
+#pragma unroll
+      for (int kk = 0; kk < SB_N / 16; ++kk) mma_ts_elect(d, ap + 8 * kk, dv + 128 * kk, id_pv, kk > 0 ? 1u : 0u);
+      mma_commit_elect(sBar + SBB_OFULL);
+      mma_commit_elect(sBar + SBB_VFREE);
+      return true;
+    };
+    bool ok = true;
+    for (int i = 0; i < n_my && ok; ++i) {
+      ok = issue_S(i);
+      if (ok && i > 0) ok = issue_PV(i - 1);
+    }
+    if (ok && n_my > 0) issue_PV(n_my - 1);
+    // Every MMA issued must be finished before TMEM is released (bounded by
+    // time only, even after an abort).
+    mma_commit_elect(sBar + SBB_DRAIN);
+    if (lane == 0) {
+      volatile uint32_t local = 0;
+      mbar_wait(sBar + SBB_DRAIN, 0, &local, 1000000000ull);
+    }
+    __syncwarp();
+  }
+  else if (warp >= 4) {
+    // ------------------------------------------------------------ RoPE + ring rows (warps 4-7)
+    const int t = tid - 128;
+    for (int i = 0; i < n_my; ++i) {
+      int kv, r0;
+      sb_item(a, i, kv, r0);
+      const int q = i & 1;
+      // (row, chunk pair) tasks: row r = it / 4 (position r0 + r / G), dims
+      // 8c..8c+7 with 32+8c..; table rows fetched before the wait
+      float4 tv[4][4];
+      bool liv[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int it = t + 128 * k, r = it >> 2, c = it & 3;
+        const int ii = r0 + r / a.G;
+        liv[k] = ii < a.C;
+        if (liv[k]) {
+          const float4 *tr = reinterpret_cast<const float4 *>(a.table + (a.P0 + ii) * 64 + 16 * c);
+#pragma unroll
+          for (int u = 0; u < 4; ++u) tv[k][u] = tr[u];
+        }
+      }
+      if (!mbar_wait(sBar + SBB_QFULL + 8 * q, (uint32_t)(i >> 1) & 1u, abort_flag)) break;
+      uint8_t *qt = gbase + q * SB_QTILE;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        if (!liv[k]) continue;  // rows past the chunk keep the zeros of the box
+        const int it = t + 128 * k, r = it >> 2, c = it & 3;
+        float cs[16];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          cs[4 * u] = tv[k][u].x; cs[4 * u + 1] = tv[k][u].y; cs[4 * u + 2] = tv[k][u].z; cs[4 * u + 3] = tv[k][u].w;
+        }
+        uint4 *p1 = reinterpret_cast<uint4 *>(qt + r * 128 + ((c ^ (r & 7)) << 4));
+        uint4 *p2 = reinterpret_cast<uint4 *>(qt + r * 128 + (((c + 4) ^ (r & 7)) << 4));
+        uint4 o1, o2;
+        rope_pair8(*p1, *p2, cs, o1, o2);
+        *p1 = o1;
+        *p2 = o2;
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(sBar + SBB_QROPE + 8 * q);
+      if (!sb_boundary(r0)) continue;
+      // Band rows 1 .. 127-r0 are chunk rows r0-127 .. -1, positions
+      // P0+r0-127 .. P0-1: copied from the ring where the slot holds the
+      // position (the box left zeros everywhere else).
+      const int t_hi = WIN - 1 - r0;
+      const uint16_t *rk = a.ring_k + ((long long)a.ring_seq * a.hkv + kv) * WIN * DQK;
+      const uint16_t *rv = a.ring_v + ((long long)a.ring_seq * a.hkv + kv) * WIN * DV;
+      for (int h = 0; h < 2; ++h) {
+        const bool v = h == 1;
+        if (!mbar_wait(sBar + (v ? SBB_VFULL : SBB_KFULL), (uint32_t)i & 1u, abort_flag)) break;
+        const int nch = v ? DV / 8 : DQK / 8;  // 16-byte chunks of a row
+        for (int e = t; e < t_hi * nch; e += 128) {
+          const int tr = 1 + e / nch, cc = e % nch;
+          const long long p = a.P0 + r0 - 128 + tr;
+          if (p < 0) continue;
+          const int slot = (int)(p & (WIN - 1));
+          if (!((held[slot >> 5] >> (slot & 31)) & 1u)) continue;
+          const uint4 x = v ? reinterpret_cast<const uint4 *>(rv + (long long)slot * DV)[cc]
+                            : reinterpret_cast<const uint4 *>(rk + (long long)slot * DQK)[cc];
+          const uint32_t dst = (v ? SB_OFF_V : SB_OFF_K) + (cc >> 3) * SB_KPART + tr * 128 + (((cc & 7) ^ (tr & 7)) << 4);
+          *reinterpret_cast<uint4 *>(gbase + dst) = x;
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(sBar + (v ? SBB_VPATCH : SBB_KPATCH));
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ softmax + epilogue (warps 0-3)
+    const int row = tid;  // TMEM lane = tile row d * G + g
+    const int d = row / a.G, g = row - d * a.G;
+    const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
+    const float sl2 = a.scale_log2;
+    // The output of item j: O / l as bf16 into the staging tile, then two
+    // TMA boxes.  The four warps agree on `good` first (every warp reaches
+    // the barrier, whatever its own outcome) and return it.
+    auto epilogue = [&](int j, float l, bool good) -> bool {
+      int kv, r0;
+      sb_item(a, j, kv, r0);
+      if (good) good = sb_wait(sBar + SBB_OFULL, (uint32_t)j & 1u, abort_flag);
+      if (tid == 0) bulk_wait_read_all();  // the last store has read the staging tile
+      good = named_bar_and(1, 128, good);
+      if (!good) return false;
+      tc_fence_after();
+      const float inv = 1.f / l;  // l >= e^(sink - m) > 0
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t o[32];
+        tmem_ld32(tmem + lane_base + SB_COL_O + 32 * c, o);
+        tmem_wait_ld();
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const uint32_t w0 = pack_bf16(__uint_as_float(o[8 * u + 0]) * inv, __uint_as_float(o[8 * u + 1]) * inv);
+          const uint32_t w1 = pack_bf16(__uint_as_float(o[8 * u + 2]) * inv, __uint_as_float(o[8 * u + 3]) * inv);
+          const uint32_t w2 = pack_bf16(__uint_as_float(o[8 * u + 4]) * inv, __uint_as_float(o[8 * u + 5]) * inv);
+          const uint32_t w3 = pack_bf16(__uint_as_float(o[8 * u + 6]) * inv, __uint_as_float(o[8 * u + 7]) * inv);
+          const int ch = 4 * (c & 1) + u;  // 16-byte chunk of dims 8 ch .. within the part
+          *reinterpret_cast<uint4 *>(gbase + SB_OFF_O + (c >> 1) * SB_QPART + row * 128 + ((ch ^ (row & 7)) << 4)) =
+              make_uint4(w0, w1, w2, w3);
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(sBar + SBB_OFREE);
+      fence_proxy_async_smem();
+      named_bar_sync(1, 128);
+      if (tid == 0) {  // rows past the chunk are clipped by the store
+        tma_store_3d(&tmo, 0, kv * a.G, r0, sO);
+        tma_store_3d(&tmo, 64, kv * a.G, r0, sO + SB_QPART);
+        bulk_commit();
+      }
+      return true;
+    };
+    bool ok = true;
+    float l_prev = 1.f;
+    for (int i = 0; i <= n_my; ++i) {
+      float l_cur = 1.f;
+      if (i < n_my && ok) {
+        int kv, r0;
+        sb_item(a, i, kv, r0);
+        const int s = i & 1;
+        const float sink2 = a.sinks[kv * a.G + g] * LOG2E;
+        ok = sb_wait(sBar + SBB_SFULL + 8 * s, (uint32_t)(i >> 1) & 1u, abort_flag);
+        if (ok) {
+          tc_fence_after();
+          const uint32_t tS = tmem + lane_base + (s ? SB_COL_S1 : 0u);
+          // Attended columns as a bitmask (column t = bit t % 32 of word t / 32):
+          // d+1 <= t <= d+128 and, before the chunk, the position exists and
+          // its ring slot holds it.  Pass 1 writes the masked scores, in log2
+          // units, back over S and takes the row maximum; pass 2 turns them
+          // into probabilities.  P of columns c0 .. c0+63 goes to columns
+          // c0/2 .., which pass 2 has already read.  Blocks of 64 columns
+          // keep the live registers low.
+          uint32_t msk[5];
+#pragma unroll
+          for (int k = 0; k < 5; ++k) msk[k] = span_bits(d + 1 - 32 * k, d + WIN - 32 * k);
+          if (sb_boundary(r0)) {
+            const long long pfirst = a.P0 + r0 - 128;   // position of column 0
+            const int tneg = WIN - r0;                   // columns before the chunk
+            const int t0 = pfirst < 0 ? (int)-pfirst : 0;  // first column with a position
+            const int off = (int)(pfirst & (WIN - 1));   // ring slot of column 0
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const int sb = 32 * k + off, w0 = (sb >> 5) & 3, sh = sb & 31;
+              const uint32_t hk = __funnelshift_r(held[w0], held[(w0 + 1) & 3], sh);  // bit e: slot (sb + e) % 128
+              const uint32_t before = span_bits(-32 * k, tneg - 1 - 32 * k);
+              const uint32_t exists = span_bits(t0 - 32 * k, 31);
+              msk[k] &= ~before | (hk & exists);
+            }
+          }
+          float mx = sink2;
+#pragma unroll
+          for (int c0 = 0; c0 < SB_N; c0 += 64) {
+            uint32_t v[64];
+            const bool full = c0 + 64 <= SB_N;
+            if (full) {
+              tmem_ld32(tS + c0, *reinterpret_cast<uint32_t(*)[32]>(v));
+              tmem_ld32(tS + c0 + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
+            } else {
+              tmem_ld16(tS + c0, *reinterpret_cast<uint32_t(*)[16]>(v));
+            }
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 64 && c0 + e < SB_N; ++e) {
+              const int c = c0 + e;
+              const float x = (msk[c >> 5] >> (c & 31)) & 1u ? __uint_as_float(v[e]) * sl2 : -INFINITY;
+              mx = fmaxf(mx, x);
+              v[e] = __float_as_uint(x);
+            }
+            if (full) {
+              tmem_st32(tS + c0, *reinterpret_cast<const uint32_t(*)[32]>(v));
+              tmem_st32(tS + c0 + 32, *reinterpret_cast<const uint32_t(*)[32]>(v + 32));
+            } else {
+              tmem_st16(tS + c0, *reinterpret_cast<const uint32_t(*)[16]>(v));
+            }
+          }
+          tmem_wait_st();
+          float su[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int c0 = 0; c0 < SB_N; c0 += 64) {
+            uint32_t v[64];
+            const bool full = c0 + 64 <= SB_N;
+            if (full) {
+              tmem_ld32(tS + c0, *reinterpret_cast<uint32_t(*)[32]>(v));
+              tmem_ld32(tS + c0 + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
+            } else {
+              tmem_ld16(tS + c0, *reinterpret_cast<uint32_t(*)[16]>(v));
+            }
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 64 && c0 + e < SB_N; e += 2) {
+              const float p0 = ex2(__uint_as_float(v[e]) - mx), p1 = ex2(__uint_as_float(v[e + 1]) - mx);
+              su[(e >> 1) & 3] += p0 + p1;
+              v[e >> 1] = pack_bf16(p0, p1);
+            }
+            if (full)
+              tmem_st32(tS + c0 / 2, *reinterpret_cast<const uint32_t(*)[32]>(v));
+            else
+              tmem_st8(tS + c0 / 2, *reinterpret_cast<const uint32_t(*)[8]>(v));
+          }
+          l_cur = ex2(sink2 - mx) + ((su[0] + su[1]) + (su[2] + su[3]));
+          tmem_wait_st();
+          tc_fence_before();
+          mbar_arrive(sBar + SBB_PREADY + 8 * s);
+        }
+      }
+      if (i > 0) {
+        ok = epilogue(i - 1, l_prev, ok);
+        if (!ok) break;
+      }
+      l_prev = l_cur;
+    }
+    if (tid == 0) bulk_wait_all();  // the stores are done before the CTA leaves
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (*abort_flag && tid == 0) flag(a.status, ST_TIMEOUT);
+  if (warp == 8) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_swa_band(const uint16_t *q, int64_t P0, int C, int seq, int hq, const KvView &chunk,
+                            const KvView &ring, const float *sinks, const float *table, float softmax_scale,
+                            uint16_t *out, unsigned *status, cudaStream_t st, bool *taken) {
+  *taken = false;
+  const int hkv = ring.hkv, G = hq / hkv;
+  if (G < 8 || 128 % G) return cudaSuccess;
+  const int np = 128 / G;
+  const long long nitems = ((long long)C + np - 1) / np * hkv;
+  if (C <= 0 || nitems >= (1LL << 31)) return cudaSuccess;
+  CUtensorMap mq, mo, mk, mv;
+  if (!make_tma_map_heads3d(&mq, q, C, hq, DQK, G) || !make_tma_map_heads3d(&mo, out, C, hq, DV, G) ||
+      !make_tma_map_tokens4d(&mk, chunk.k, C, hkv, DQK, SB_N, true) ||
+      !make_tma_map_tokens4d(&mv, chunk.v, C, hkv, DV, SB_N, true))
+    return cudaSuccess;
+  cudaError_t e = ensure_smem_limit(10, (const void *)swa_band_kernel, SB_SMEM);
+  if (e != cudaSuccess) return e;
+  SbArgs a{};
+  a.P0 = P0;
+  a.C = C;
+  a.hq = hq;
+  a.G = G;
+  a.hkv = hkv;
+  a.np = np;
+  a.nitems = (int)nitems;
+  a.ring_seq = seq;
+  a.slot_pos = ring.slot_pos;
+  a.ring_k = ring.k;
+  a.ring_v = ring.v;
+  a.sinks = sinks;
+  a.table = table;
+  a.scale_log2 = softmax_scale * LOG2E;
+  a.status = status;
+  const long long grid = nitems < num_sms() ? nitems : num_sms();
+  swa_band_kernel<<<(unsigned)grid, SB_THREADS, SB_SMEM, st>>>(mq, mo, mk, mv, a);
+  *taken = true;
+  return cudaGetLastError();
+}
+
+}  // namespace kvr

@@ -181,9 +181,11 @@ def test_swa_varlen_draft_verification(dist, hq, hkv, tables):
 
 
 def test_swa_varlen_mixed_and_equal_to_single_chunks(tables):
-    # A long chunk beside decode tokens: the long chunk's rows equal the
-    # single-chunk call on the same ring and rows, bit for bit (same tiled
-    # kernel); the single tokens (short-chunk kernel) match the oracle.
+    # A long chunk beside decode tokens: the long chunk's rows agree with the
+    # single-chunk call on the same ring and rows (a different kernel for
+    # this group size: the band kernel, single-pass softmax) within the bar,
+    # and both with the oracle; the single tokens (short-chunk kernel) match
+    # the oracle.
     syn = Synth(3601, dist="shifted", device=DEV)
     hq, hkv = 64, 8
     sinks = syn.sinks(hq).to(DEV)
@@ -195,10 +197,11 @@ def test_swa_varlen_mixed_and_equal_to_single_chunks(tables):
     st = kvr.LinearLayout(stage.k[:513].contiguous(), stage.v[:513].contiguous())
     one = kvr.swa_sink_prefill_chunk(q[:513].contiguous(), 900, 2, st, ring, sinks, tables[1e4], SCALE)
     torch.cuda.synchronize()
-    assert torch.equal(out[:513], one)
+    compare_rows(out[:513], one.double().cpu().numpy(), "swa varlen vs single chunk")
     want = _swa_want(syn, hkv, q, seqs, P0s, Cs, sinks)
     rows = list(range(0, 513, 41)) + [512, 513, 514]
     compare_rows(out[rows], want[rows], "swa varlen mixed")
+    compare_rows(one[rows[:-2]], want[rows[:-2]], "swa single chunk")
     assert kvr.device_status() == 0
 
 
