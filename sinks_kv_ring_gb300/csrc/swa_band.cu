@@ -18,18 +18,21 @@
 // the TMA unit as zeros (a negative coordinate); for the first items the
 // rows whose ring slot holds their position are then copied in.
 //
-// One CTA per SM, 320 threads:
-//   warps 0-3  softmax of item i, then the epilogue of item i-1 (thread =
-//              row = TMEM lane)
-//   warps 4-7  RoPE of each query tile in shared memory; the ring rows of
-//              the items that reach before the chunk
-//   warp  8    TMEM owner and MMA issuer (converged; elect.sync issues)
-//   warp  9    TMA producer (converged; elect.sync issues)
+// One CTA per SM, 480 threads:
+//   warps 0-7   softmax of item i, then the epilogue of item i-1; warp w
+//               takes TMEM lanes 32 (w % 4) .. (one tile row each) and half
+//               w / 4 of the band's columns and of O's columns
+//   warps 8-11  RoPE of each query tile in shared memory; the ring rows of
+//               the items that reach before the chunk
+//   warp  12    TMEM owner and MMA issuer (converged; elect.sync issues)
+//   warp  13    TMA producer of the bands, warp 14 of the query tiles
+//               (converged; elect.sync issues)
 // Shared memory: two query tiles (3 x 16 KB each, 128-byte swizzled,
 // K-major), the band's K (3 x 18 KB, K-major) and V (2 x 18 KB, MN-major),
-// one output tile (2 x 16 KB) that leaves as two TMA boxes.  The next
-// item's query tile loads while the current one is computed; the band's K
-// reloads once S = Q K^T is done, its V once P V is done.
+// one output tile (2 x 16 KB) that leaves as two TMA boxes.  The producer
+// issues each load as soon as its buffer is free: the query tile of item
+// i+2 once S(i) is done, the band's K of item i+1 once S(i) is done, its V
+// once P V(i) is done.
 // TMEM (512 columns): S0 at 0, S1 at 160 (144 fp32 columns each; the bf16
 // probabilities P overwrite the first 72 and feed P V from TMEM), O at 320.
 #include <cuda.h>
@@ -42,7 +45,8 @@ namespace {
 
 using namespace tc;
 
-constexpr int SB_THREADS = 320;
+constexpr int SB_THREADS = 480;
+constexpr int SB_WARP_ROPE = 8, SB_WARP_MMA = 12, SB_WARP_TMA = 13, SB_WARP_TMAQ = 14;
 constexpr int SB_N = 144;                          // keys of a band
 constexpr int SB_QPART = 128 * 128;                // 128 rows x 64 dims
 constexpr int SB_QTILE = 3 * SB_QPART;
@@ -52,7 +56,8 @@ constexpr int SB_OFF_V = SB_OFF_K + 3 * SB_KPART;
 constexpr int SB_OFF_O = SB_OFF_V + 2 * SB_KPART;
 constexpr int SB_OFF_BAR = SB_OFF_O + 2 * SB_QPART;
 constexpr int SB_OFF_TAG = SB_OFF_BAR + 256;       // 128 bits: ring slot c holds its pre-chunk position
-constexpr int SB_SMEM = SB_OFF_TAG + 16 + 1024;    // + alignment slack
+constexpr int SB_OFF_RED = SB_OFF_TAG + 16;        // half-row maxima [2][128], sums [2][2][128] (fp32)
+constexpr int SB_SMEM = SB_OFF_RED + 768 * 4 + 1024;  // + alignment slack
 static_assert(SB_OFF_K % 1024 == 0 && SB_KPART % 1024 == 0 && SB_OFF_V % 1024 == 0 && SB_OFF_O % 1024 == 0,
               "swizzled tiles start on 1024-byte boundaries");
 static_assert(SB_SMEM <= 227 * 1024, "one CTA per SM");
@@ -131,7 +136,7 @@ __global__ void __launch_bounds__(SB_THREADS, 1)
       mbar_init(sBar + SBB_QROPE + 8 * i, 128);
       mbar_init(sBar + SBB_QFREE + 8 * i, 1);
       mbar_init(sBar + SBB_SFULL + 8 * i, 1);
-      mbar_init(sBar + SBB_PREADY + 8 * i, 128);
+      mbar_init(sBar + SBB_PREADY + 8 * i, 256);
     }
     mbar_init(sBar + SBB_KFULL, 1);
     mbar_init(sBar + SBB_VFULL, 1);
@@ -140,7 +145,7 @@ __global__ void __launch_bounds__(SB_THREADS, 1)
     mbar_init(sBar + SBB_KPATCH, 128);
     mbar_init(sBar + SBB_VPATCH, 128);
     mbar_init(sBar + SBB_OFULL, 1);
-    mbar_init(sBar + SBB_OFREE, 128);
+    mbar_init(sBar + SBB_OFREE, 256);
     mbar_init(sBar + SBB_DRAIN, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -152,7 +157,7 @@ __global__ void __launch_bounds__(SB_THREADS, 1)
     const unsigned bits = __ballot_sync(0xffffffffu, h);
     if (lane == 0) reinterpret_cast<uint32_t *>(gbase + SB_OFF_TAG)[warp] = bits;
   }
-  if (warp == 8) {
+  if (warp == SB_WARP_MMA) {
     tmem_alloc(sBar + SBB_TMEM, 512);
     tmem_relinquish();
   }
@@ -161,12 +166,15 @@ __global__ void __launch_bounds__(SB_THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(gbase + SB_OFF_BAR + SBB_TMEM);
 
-  if (warp == 9) {
-    // ------------------------------------------------------------ TMA producer
-    // Order of the loads follows the order in which their buffers come free:
-    // S(i-1) frees the band's K and the query tile of item i+1, P V(i-1) the
-    // band's V.
-    int last_q0 = -1, last_q1 = -1, last_k = -1, last_v = -1;
+  if (warp == SB_WARP_TMA || warp == SB_WARP_TMAQ) {
+    // ------------------------------------------------------------ TMA producers
+    // Warp 13 loads the bands, warp 14 the query tiles (a load from HBM
+    // that waits for the TMA unit does not hold up the other stream).  Each
+    // load goes out as soon as its buffer is free: K(k) after S(k-1), V(v)
+    // after P V(v-1), Q(q) after S(q-2).  Lane 0's view of a barrier decides
+    // for the warp.
+    const bool qw = warp == SB_WARP_TMAQ;
+    int last_a = -1, last_b = -1;  // last loads issued: K, V (warp 13); even, odd query tile (warp 14)
     auto load_q = [&](int i) {
       int kv, r0;
       sb_item(a, i, kv, r0);
@@ -174,7 +182,7 @@ __global__ void __launch_bounds__(SB_THREADS, 1)
       mbar_expect_tx_elect(bar, SB_QTILE);
       for (int part = 0; part < 3; ++part)
         tma_load_3d_elect(base + (i & 1) * SB_QTILE + part * SB_QPART, &tmq, 64 * part, kv * a.G, r0, bar);
-      (i & 1 ? last_q1 : last_q0) = i;
+      (i & 1 ? last_b : last_a) = i;
     };
     auto load_band = [&](int i, bool v) {
       int kv, r0;
@@ -185,46 +193,68 @@ __global__ void __launch_bounds__(SB_THREADS, 1)
       for (int part = 0; part < parts; ++part)
         tma_load_4d_elect((v ? sV : sK) + part * SB_KPART, v ? (const void *)&tmv : (const void *)&tmk, 0, part, kv,
                           r0 - 128, bar);
-      (v ? last_v : last_k) = i;
+      (v ? last_b : last_a) = i;
     };
+    auto ready = [&](uint32_t bar, uint32_t parity) {
+      return __shfl_sync(0xffffffffu, (int)mbar_test(bar, parity), 0) != 0;
+    };
+    int n1 = 1, n2 = 1;  // next K and V (warp 13); next query tile: n1 (warp 14)
     if (n_my > 0) {
-      load_q(0);
-      load_band(0, false);
-      load_band(0, true);
-      if (n_my > 1) load_q(1);
-    }
-    for (int i = 1; i < n_my; ++i) {
-      if (!sb_wait(sBar + SBB_KFREE, (uint32_t)(i - 1) & 1u, abort_flag)) break;
-      load_band(i, false);
-      if (i + 1 < n_my) {
-        if (!sb_wait(sBar + SBB_QFREE + 8 * ((i + 1) & 1), (uint32_t)((i - 1) >> 1) & 1u, abort_flag)) break;
-        load_q(i + 1);
+      if (qw) {
+        load_q(0);
+        if (n_my > 1) load_q(1);
+        n1 = 2;
+      } else {
+        load_band(0, false);
+        load_band(0, true);
       }
-      if (!sb_wait(sBar + SBB_VFREE, (uint32_t)(i - 1) & 1u, abort_flag)) break;
-      load_band(i, true);
+    }
+    uint64_t t_last = global_ns();
+    while (qw ? n1 < n_my : (n1 < n_my || n2 < n_my)) {
+      bool prog = false;
+      if (qw) {
+        if (ready(sBar + SBB_QFREE + 8 * (n1 & 1), (uint32_t)((n1 - 2) >> 1) & 1u)) {
+          load_q(n1++);
+          prog = true;
+        }
+      } else {
+        if (n1 < n_my && ready(sBar + SBB_KFREE, (uint32_t)(n1 - 1) & 1u)) {
+          load_band(n1++, false);
+          prog = true;
+        }
+        if (n2 < n_my && ready(sBar + SBB_VFREE, (uint32_t)(n2 - 1) & 1u)) {
+          load_band(n2++, true);
+          prog = true;
+        }
+      }
+      if (prog) {
+        t_last = global_ns();
+      } else {
+        // warp-uniform: lane 0 decides whether to give up (aborted elsewhere,
+        // or no buffer came free for 2 s)
+        const bool stop =
+            __shfl_sync(0xffffffffu, (int)(*abort_flag != 0 || global_ns() - t_last > 2000000000ull), 0) != 0;
+        if (stop) {
+          if (lane == 0) *abort_flag = 1;
+          break;
+        }
+        __nanosleep(32);
+      }
     }
     // On an abort, the loads already issued land before the CTA leaves
     // (bounded by time only: the abort flag is already set).
     if (*abort_flag && lane == 0) {
       volatile uint32_t local = 0;
       for (int s = 0; s < 2; ++s) {
-        const int lq = s ? last_q1 : last_q0;
-        if (lq >= 0) {
-          local = 0;
-          mbar_wait(sBar + SBB_QFULL + 8 * s, (uint32_t)(lq >> 1) & 1u, &local, 1000000000ull);
-        }
-      }
-      if (last_k >= 0) {
+        const int li = s ? last_b : last_a;
+        if (li < 0) continue;
         local = 0;
-        mbar_wait(sBar + SBB_KFULL, (uint32_t)last_k & 1u, &local, 1000000000ull);
-      }
-      if (last_v >= 0) {
-        local = 0;
-        mbar_wait(sBar + SBB_VFULL, (uint32_t)last_v & 1u, &local, 1000000000ull);
+        const uint32_t bar = qw ? sBar + SBB_QFULL + 8 * s : sBar + (s ? SBB_VFULL : SBB_KFULL);
+        mbar_wait(bar, qw ? (uint32_t)(li >> 1) & 1u : (uint32_t)li & 1u, &local, 1000000000ull);
       }
     }
     __syncwarp();
-  } else if (warp == 8) {
+  } else if (warp == SB_WARP_MMA) {
     // ------------------------------------------------------------ MMA issuer
     // Order: S(0), then S(i), P V(i-1) for i = 1.. (the tensor core computes
     // the next tile's scores while the softmax warps work on the last ones),
@@ -293,9 +323,9 @@ __global__ void __launch_bounds__(SB_THREADS, 1)
     }
     __syncwarp();
   }
-  else if (warp >= 4) {
-    // ------------------------------------------------------------ RoPE + ring rows (warps 4-7)
-    const int t = tid - 128;
+  else if (warp >= SB_WARP_ROPE) {
+    // ------------------------------------------------------------ RoPE + ring rows (warps 8-11)
+    const int t = tid - 32 * SB_WARP_ROPE;
     for (int i = 0; i < n_my; ++i) {
       int kv, r0;
       sb_item(a, i, kv, r0);
@@ -346,43 +376,52 @@ __global__ void __launch_bounds__(SB_THREADS, 1)
         const bool v = h == 1;
         if (!mbar_wait(sBar + (v ? SBB_VFULL : SBB_KFULL), (uint32_t)i & 1u, abort_flag)) break;
         const int nch = v ? DV / 8 : DQK / 8;  // 16-byte chunks of a row
+        // asynchronous 16-byte copies, all in flight before the one wait
         for (int e = t; e < t_hi * nch; e += 128) {
           const int tr = 1 + e / nch, cc = e % nch;
           const long long p = a.P0 + r0 - 128 + tr;
           if (p < 0) continue;
           const int slot = (int)(p & (WIN - 1));
           if (!((held[slot >> 5] >> (slot & 31)) & 1u)) continue;
-          const uint4 x = v ? reinterpret_cast<const uint4 *>(rv + (long long)slot * DV)[cc]
-                            : reinterpret_cast<const uint4 *>(rk + (long long)slot * DQK)[cc];
-          const uint32_t dst = (v ? SB_OFF_V : SB_OFF_K) + (cc >> 3) * SB_KPART + tr * 128 + (((cc & 7) ^ (tr & 7)) << 4);
-          *reinterpret_cast<uint4 *>(gbase + dst) = x;
+          const uint16_t *src = v ? rv + (long long)slot * DV + 8 * cc : rk + (long long)slot * DQK + 8 * cc;
+          cp_async16(base + (v ? SB_OFF_V : SB_OFF_K) + (cc >> 3) * SB_KPART + tr * 128 + (((cc & 7) ^ (tr & 7)) << 4),
+                     src);
         }
+        cp_async_commit();
+        cp_async_wait<0>();
         fence_proxy_async_smem();
         mbar_arrive(sBar + (v ? SBB_VPATCH : SBB_KPATCH));
       }
     }
   } else {
-    // ------------------------------------------------------------ softmax + epilogue (warps 0-3)
-    const int row = tid;  // TMEM lane = tile row d * G + g
+    // ------------------------------------------------------------ softmax + epilogue (warps 0-7)
+    // Warp w reads TMEM lanes 32 (w % 4) .. (tile rows d * G + g) and half
+    // h = w / 4 of the columns: band columns 72h .. 72h+71, O columns
+    // 64h .. 64h+63.  The halves of a row exchange their maxima and partial
+    // sums through shared memory.  Named barriers 1 and 2 span the eight
+    // warps; before each, the warps agree on their outcome, so all of them
+    // always reach it.
+    const int row = tid & 127, h = tid >> 7;
     const int d = row / a.G, g = row - d * a.G;
-    const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
+    const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
     const float sl2 = a.scale_log2;
+    float *red_m = reinterpret_cast<float *>(gbase + SB_OFF_RED);  // [2 halves][128] maxima
+    float *red_l = red_m + 256;                                      // [2 items][2 halves][128] sums
     // The output of item j: O / l as bf16 into the staging tile, then two
-    // TMA boxes.  The four warps agree on `good` first (every warp reaches
-    // the barrier, whatever its own outcome) and return it.
-    auto epilogue = [&](int j, float l, bool good) -> bool {
+    // TMA boxes.
+    auto epilogue = [&](int j, bool good) -> bool {
       int kv, r0;
       sb_item(a, j, kv, r0);
       if (good) good = sb_wait(sBar + SBB_OFULL, (uint32_t)j & 1u, abort_flag);
       if (tid == 0) bulk_wait_read_all();  // the last store has read the staging tile
-      good = named_bar_and(1, 128, good);
+      good = named_bar_and(1, 256, good);
       if (!good) return false;
       tc_fence_after();
-      const float inv = 1.f / l;  // l >= e^(sink - m) > 0
-#pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
+      const float inv = 1.f / (red_l[(j & 1) * 256 + row] + red_l[(j & 1) * 256 + 128 + row]);  // l >= e^(sink-m) > 0
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
         uint32_t o[32];
-        tmem_ld32(tmem + lane_base + SB_COL_O + 32 * c, o);
+        tmem_ld32(tmem + lane_base + SB_COL_O + 64 * h + 32 * c, o);
         tmem_wait_ld();
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
@@ -390,15 +429,15 @@ __global__ void __launch_bounds__(SB_THREADS, 1)
           const uint32_t w1 = pack_bf16(__uint_as_float(o[8 * u + 2]) * inv, __uint_as_float(o[8 * u + 3]) * inv);
           const uint32_t w2 = pack_bf16(__uint_as_float(o[8 * u + 4]) * inv, __uint_as_float(o[8 * u + 5]) * inv);
           const uint32_t w3 = pack_bf16(__uint_as_float(o[8 * u + 6]) * inv, __uint_as_float(o[8 * u + 7]) * inv);
-          const int ch = 4 * (c & 1) + u;  // 16-byte chunk of dims 8 ch .. within the part
-          *reinterpret_cast<uint4 *>(gbase + SB_OFF_O + (c >> 1) * SB_QPART + row * 128 + ((ch ^ (row & 7)) << 4)) =
+          const int ch = 4 * c + u;  // 16-byte chunk of dims 64h + 8 ch .. within part h
+          *reinterpret_cast<uint4 *>(gbase + SB_OFF_O + h * SB_QPART + row * 128 + ((ch ^ (row & 7)) << 4)) =
               make_uint4(w0, w1, w2, w3);
         }
       }
       tc_fence_before();
       mbar_arrive(sBar + SBB_OFREE);
       fence_proxy_async_smem();
-      named_bar_sync(1, 128);
+      named_bar_sync(1, 256);
       if (tid == 0) {  // rows past the chunk are clipped by the store
         tma_store_3d(&tmo, 0, kv * a.G, r0, sO);
         tma_store_3d(&tmo, 64, kv * a.G, r0, sO + SB_QPART);
@@ -407,103 +446,74 @@ __global__ void __launch_bounds__(SB_THREADS, 1)
       return true;
     };
     bool ok = true;
-    float l_prev = 1.f;
     for (int i = 0; i <= n_my; ++i) {
-      float l_cur = 1.f;
       if (i < n_my && ok) {
         int kv, r0;
         sb_item(a, i, kv, r0);
         const int s = i & 1;
         const float sink2 = a.sinks[kv * a.G + g] * LOG2E;
         ok = sb_wait(sBar + SBB_SFULL + 8 * s, (uint32_t)(i >> 1) & 1u, abort_flag);
+        ok = named_bar_and(2, 256, ok);
         if (ok) {
           tc_fence_after();
           const uint32_t tS = tmem + lane_base + (s ? SB_COL_S1 : 0u);
-          // Attended columns as a bitmask (column t = bit t % 32 of word t / 32):
-          // d+1 <= t <= d+128 and, before the chunk, the position exists and
-          // its ring slot holds it.  Pass 1 writes the masked scores, in log2
-          // units, back over S and takes the row maximum; pass 2 turns them
-          // into probabilities.  P of columns c0 .. c0+63 goes to columns
-          // c0/2 .., which pass 2 has already read.  Blocks of 64 columns
-          // keep the live registers low.
-          uint32_t msk[5];
+          const int cb = 72 * h;  // first band column of this half
+          uint32_t v[72];
+          tmem_ld32(tS + cb, *reinterpret_cast<uint32_t(*)[32]>(v));
+          tmem_ld32(tS + cb + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
+          tmem_ld8(tS + cb + 64, *reinterpret_cast<uint32_t(*)[8]>(v + 64));
+          // Attended columns (bit e of word k = column cb + 32k + e): d+1 <=
+          // t <= d+128 and, before the chunk, the position exists and its ring
+          // slot holds it.
+          uint32_t msk[3];
 #pragma unroll
-          for (int k = 0; k < 5; ++k) msk[k] = span_bits(d + 1 - 32 * k, d + WIN - 32 * k);
+          for (int k = 0; k < 3; ++k) msk[k] = span_bits(d + 1 - cb - 32 * k, d + WIN - cb - 32 * k);
           if (sb_boundary(r0)) {
-            const long long pfirst = a.P0 + r0 - 128;   // position of column 0
-            const int tneg = WIN - r0;                   // columns before the chunk
+            const long long pfirst = a.P0 + r0 - 128;     // position of column 0
+            const int tneg = WIN - r0;                     // columns before the chunk
             const int t0 = pfirst < 0 ? (int)-pfirst : 0;  // first column with a position
-            const int off = (int)(pfirst & (WIN - 1));   // ring slot of column 0
+            const int off = (int)(pfirst & (WIN - 1));     // ring slot of column 0
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const int sb = 32 * k + off, w0 = (sb >> 5) & 3, sh = sb & 31;
+            for (int k = 0; k < 3; ++k) {
+              const int ck = cb + 32 * k;
+              const int sb = ck + off, w0 = (sb >> 5) & 3, sh = sb & 31;
               const uint32_t hk = __funnelshift_r(held[w0], held[(w0 + 1) & 3], sh);  // bit e: slot (sb + e) % 128
-              const uint32_t before = span_bits(-32 * k, tneg - 1 - 32 * k);
-              const uint32_t exists = span_bits(t0 - 32 * k, 31);
+              const uint32_t before = span_bits(-ck, tneg - 1 - ck);
+              const uint32_t exists = span_bits(t0 - ck, 31);
               msk[k] &= ~before | (hk & exists);
             }
           }
-          float mx = sink2;
+          tmem_wait_ld();
+          float mx = -INFINITY;
 #pragma unroll
-          for (int c0 = 0; c0 < SB_N; c0 += 64) {
-            uint32_t v[64];
-            const bool full = c0 + 64 <= SB_N;
-            if (full) {
-              tmem_ld32(tS + c0, *reinterpret_cast<uint32_t(*)[32]>(v));
-              tmem_ld32(tS + c0 + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
-            } else {
-              tmem_ld16(tS + c0, *reinterpret_cast<uint32_t(*)[16]>(v));
-            }
-            tmem_wait_ld();
-#pragma unroll
-            for (int e = 0; e < 64 && c0 + e < SB_N; ++e) {
-              const int c = c0 + e;
-              const float x = (msk[c >> 5] >> (c & 31)) & 1u ? __uint_as_float(v[e]) * sl2 : -INFINITY;
-              mx = fmaxf(mx, x);
-              v[e] = __float_as_uint(x);
-            }
-            if (full) {
-              tmem_st32(tS + c0, *reinterpret_cast<const uint32_t(*)[32]>(v));
-              tmem_st32(tS + c0 + 32, *reinterpret_cast<const uint32_t(*)[32]>(v + 32));
-            } else {
-              tmem_st16(tS + c0, *reinterpret_cast<const uint32_t(*)[16]>(v));
-            }
+          for (int e = 0; e < 72; ++e) {
+            const float x = (msk[e >> 5] >> (e & 31)) & 1u ? __uint_as_float(v[e]) * sl2 : -INFINITY;
+            v[e] = __float_as_uint(x);
+            mx = fmaxf(mx, x);
           }
-          tmem_wait_st();
-          float su[4] = {0.f, 0.f, 0.f, 0.f};
+          red_m[h * 128 + row] = mx;
+          named_bar_sync(2, 256);  // both maxima; both halves' S loads done before any P store
+          mx = fmaxf(fmaxf(red_m[row], red_m[128 + row]), sink2);
+          // p = 2^(x - m) as bf16 pairs, packed into the registers already read
+          float su[4] = {h == 0 ? ex2(sink2 - mx) : 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-          for (int c0 = 0; c0 < SB_N; c0 += 64) {
-            uint32_t v[64];
-            const bool full = c0 + 64 <= SB_N;
-            if (full) {
-              tmem_ld32(tS + c0, *reinterpret_cast<uint32_t(*)[32]>(v));
-              tmem_ld32(tS + c0 + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
-            } else {
-              tmem_ld16(tS + c0, *reinterpret_cast<uint32_t(*)[16]>(v));
-            }
-            tmem_wait_ld();
-#pragma unroll
-            for (int e = 0; e < 64 && c0 + e < SB_N; e += 2) {
-              const float p0 = ex2(__uint_as_float(v[e]) - mx), p1 = ex2(__uint_as_float(v[e + 1]) - mx);
-              su[(e >> 1) & 3] += p0 + p1;
-              v[e >> 1] = pack_bf16(p0, p1);
-            }
-            if (full)
-              tmem_st32(tS + c0 / 2, *reinterpret_cast<const uint32_t(*)[32]>(v));
-            else
-              tmem_st8(tS + c0 / 2, *reinterpret_cast<const uint32_t(*)[8]>(v));
+          for (int e = 0; e < 72; e += 2) {
+            const float p0 = ex2(__uint_as_float(v[e]) - mx), p1 = ex2(__uint_as_float(v[e + 1]) - mx);
+            su[(e >> 1) & 3] += p0 + p1;
+            v[e >> 1] = pack_bf16(p0, p1);
           }
-          l_cur = ex2(sink2 - mx) + ((su[0] + su[1]) + (su[2] + su[3]));
+          red_l[(i & 1) * 256 + h * 128 + row] = (su[0] + su[1]) + (su[2] + su[3]);
+          tmem_st32(tS + 36 * h, *reinterpret_cast<const uint32_t(*)[32]>(v));
+          tmem_st4(tS + 36 * h + 32, *reinterpret_cast<const uint32_t(*)[4]>(v + 32));
           tmem_wait_st();
           tc_fence_before();
           mbar_arrive(sBar + SBB_PREADY + 8 * s);
         }
       }
       if (i > 0) {
-        ok = epilogue(i - 1, l_prev, ok);
+        ok = epilogue(i - 1, ok);
         if (!ok) break;
       }
-      l_prev = l_cur;
     }
     if (tid == 0) bulk_wait_all();  // the stores are done before the CTA leaves
   }
@@ -511,7 +521,7 @@ __global__ void __launch_bounds__(SB_THREADS, 1)
   tc_fence_before();
   __syncthreads();
   if (*abort_flag && tid == 0) flag(a.status, ST_TIMEOUT);
-  if (warp == 8) {
+  if (warp == SB_WARP_MMA) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
