@@ -418,17 +418,22 @@ __global__ void __launch_bounds__(SB_THREADS, 1)
       if (!good) return false;
       tc_fence_after();
       const float inv = 1.f / (red_l[(j & 1) * 256 + row] + red_l[(j & 1) * 256 + 128 + row]);  // l >= e^(sink-m) > 0
+      const uint64_t invv = f32x2(inv, inv), zero2 = f32x2(0.f, 0.f);
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
         uint32_t o[32];
         tmem_ld32(tmem + lane_base + SB_COL_O + 64 * h + 32 * c, o);
         tmem_wait_ld();
+        uint32_t w[16];
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {  // O / l, one packed multiply per pair
+          float y0, y1;
+          f32x2_split(fma_f32x2(f32x2(__uint_as_float(o[e]), __uint_as_float(o[e + 1])), invv, zero2), y0, y1);
+          w[e >> 1] = pack_bf16(y0, y1);
+        }
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-          const uint32_t w0 = pack_bf16(__uint_as_float(o[8 * u + 0]) * inv, __uint_as_float(o[8 * u + 1]) * inv);
-          const uint32_t w1 = pack_bf16(__uint_as_float(o[8 * u + 2]) * inv, __uint_as_float(o[8 * u + 3]) * inv);
-          const uint32_t w2 = pack_bf16(__uint_as_float(o[8 * u + 4]) * inv, __uint_as_float(o[8 * u + 5]) * inv);
-          const uint32_t w3 = pack_bf16(__uint_as_float(o[8 * u + 6]) * inv, __uint_as_float(o[8 * u + 7]) * inv);
+          const uint32_t w0 = w[4 * u], w1 = w[4 * u + 1], w2 = w[4 * u + 2], w3 = w[4 * u + 3];
           const int ch = 4 * c + u;  // 16-byte chunk of dims 64h + 8 ch .. within part h
           *reinterpret_cast<uint4 *>(gbase + SB_OFF_O + h * SB_QPART + row * 128 + ((ch ^ (row & 7)) << 4)) =
               make_uint4(w0, w1, w2, w3);
@@ -484,25 +489,41 @@ __global__ void __launch_bounds__(SB_THREADS, 1)
             }
           }
           tmem_wait_ld();
+          // Masked raw scores: outside the first items only columns 0 .. 15
+          // (before a row's window) and 128 .. 143 (after it) can be masked,
+          // i.e. the first 16 and the last 16 of either half.
+          const uint32_t NINF = __float_as_uint(-INFINITY);
+          if (sb_boundary(r0)) {
+#pragma unroll
+            for (int e = 0; e < 72; ++e) v[e] = (msk[e >> 5] >> (e & 31)) & 1u ? v[e] : NINF;
+          } else {
+#pragma unroll
+            for (int e = 0; e < 72; ++e)
+              if (e < 16 || e >= 56) v[e] = (msk[e >> 5] >> (e & 31)) & 1u ? v[e] : NINF;
+          }
           float mx = -INFINITY;
 #pragma unroll
-          for (int e = 0; e < 72; ++e) {
-            const float x = (msk[e >> 5] >> (e & 31)) & 1u ? __uint_as_float(v[e]) * sl2 : -INFINITY;
-            v[e] = __float_as_uint(x);
-            mx = fmaxf(mx, x);
-          }
+          for (int e = 0; e < 72; e += 2) mx = fmax3(mx, __uint_as_float(v[e]), __uint_as_float(v[e + 1]));
           red_m[h * 128 + row] = mx;
           named_bar_sync(2, 256);  // both maxima; both halves' S loads done before any P store
-          mx = fmaxf(fmaxf(red_m[row], red_m[128 + row]), sink2);
-          // p = 2^(x - m) as bf16 pairs, packed into the registers already read
-          float su[4] = {h == 0 ? ex2(sink2 - mx) : 0.f, 0.f, 0.f, 0.f};
+          // row maximum in log2 units (the scale is positive), with the sink
+          mx = fmaxf(fmaxf(red_m[row], red_m[128 + row]) * sl2, sink2);
+          // p = 2^(s * scale - m) (one packed FMA per pair) as bf16 pairs,
+          // packed into the registers already read; sums in packed pairs
+          const uint64_t sl2v = f32x2(sl2, sl2), nmv = f32x2(-mx, -mx);
+          uint64_t sumv[4] = {f32x2(h == 0 ? ex2(sink2 - mx) : 0.f, 0.f), 0, 0, 0};
 #pragma unroll
           for (int e = 0; e < 72; e += 2) {
-            const float p0 = ex2(__uint_as_float(v[e]) - mx), p1 = ex2(__uint_as_float(v[e + 1]) - mx);
-            su[(e >> 1) & 3] += p0 + p1;
+            float a0, a1;
+            f32x2_split(fma_f32x2(f32x2(__uint_as_float(v[e]), __uint_as_float(v[e + 1])), sl2v, nmv), a0, a1);
+            const float p0 = ex2(a0), p1 = ex2(a1);
+            sumv[(e >> 1) & 3] = add_f32x2(sumv[(e >> 1) & 3], f32x2(p0, p1));
             v[e >> 1] = pack_bf16(p0, p1);
           }
-          red_l[(i & 1) * 256 + h * 128 + row] = (su[0] + su[1]) + (su[2] + su[3]);
+          float su[8];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) f32x2_split(sumv[u], su[2 * u], su[2 * u + 1]);
+          red_l[(i & 1) * 256 + h * 128 + row] = ((su[0] + su[1]) + (su[2] + su[3])) + ((su[4] + su[5]) + (su[6] + su[7]));
           tmem_st32(tS + 36 * h, *reinterpret_cast<const uint32_t(*)[32]>(v));
           tmem_st4(tS + 36 * h + 32, *reinterpret_cast<const uint32_t(*)[4]>(v + 32));
           tmem_wait_st();
