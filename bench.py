@@ -428,6 +428,16 @@ class PrefillWorkload:
     def flops_swa(self):
         return attn_flops(prefill_pairs(self.P0, self.C, window=128), self.hq)
 
+    def bytes_swa(self):
+        """Bytes the windowed prefill must move at least: q read, out written,
+        the staged chunk K/V and the ring rows before the chunk read once,
+        the ring tags and the fp32 RoPE rows of the chunk's positions."""
+        C, hq, hkv = self.C, self.hq, self.hkv_swa
+        ring_rows = min(self.P0, 127)
+        return (C * hq * (192 + 128) * 2 + C * hkv * (192 + 128) * 2 + ring_rows * hkv * (192 + 128) * 2
+                + 128 * 4 + C * 64 * 4)
+
+
     def step(self, stream, timed=False):
         kvr = self.kvr
         # restore the ring's pre-chunk state (the previous step committed the chunk's tail)
@@ -740,6 +750,17 @@ def append_bulk_time(pw, ntok=65536):
     ms = graph_time_ms(calls)
     return ms, ntok * (pw.hkv_full * KV_BYTES * 2 + 256)
 
+def swa_prefill_entry(pw, ms, hbm, peaks_src):
+    """The windowed chunked prefill: TFLOP/s and, as it is bound by memory
+    (few flops per byte of q and out), its HBM roofline."""
+    gbs = pw.bytes_swa() / (ms / 1e3) / 1e9
+    return {"ms": round(ms, 4), "TFLOP/s": round(pw.flops_swa() / (ms / 1e3) / 1e12, 1), "flop": pw.flops_swa(),
+            "bytes": pw.bytes_swa(), "GB/s": round(gbs, 1),
+            "roofline": with_nominal({"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s",
+                                      "frac": round(gbs / hbm, 4), "peak_source": peaks_src,
+                                      "kernel": "swa_band_kernel", "traffic": kernel_traffic("swa_band_kernel")})}
+
+
 
 def run_prefill(kvr, steps, warmup, P0=122880, C=8192):
     stream = torch.cuda.current_stream()
@@ -861,7 +882,6 @@ def main():
             pw, pms = run_prefill(kvr, psteps, 3)
         pms = max_over_ranks([pms], world, "cuda")[0]
         tf_full = pw.flops_full() / (pw.t_full.mean_ms() / 1e3) / 1e12
-        tf_swa = pw.flops_swa() / (pw.t_swa.mean_ms() / 1e3) / 1e12
         pk = peaks_d.get("bf16_tflops_sustained", peaks_d["bf16_tflops"])
         res["prefill"] = {
             "workload": "1 sequence, 8192-token chunk on 122880 cached tokens; 64 q heads; full layer 4 KV heads "
@@ -869,8 +889,7 @@ def main():
             "ms_per_step": round(pms, 3),
             "full_attn_prefill_chunk": {"ms": round(pw.t_full.mean_ms(), 3), "TFLOP/s": round(tf_full, 1),
                                         "flop": pw.flops_full()},
-            "swa_sink_prefill_chunk": {"ms": round(pw.t_swa.mean_ms(), 4), "TFLOP/s": round(tf_swa, 1),
-                                       "flop": pw.flops_swa()},
+            "swa_sink_prefill_chunk": swa_prefill_entry(pw, pw.t_swa.mean_ms(), hbm, peaks_src),
             "roofline": with_nominal({"bound": "tensor", "achieved": round(tf_full, 1), "peak": pk, "unit": "TFLOP/s",
                          "frac": round(tf_full / pk, 4), "peak_source": peaks_src + " (sustained)",
                          "traffic": kernel_traffic("full_prefill_tc_kernel")}),
@@ -940,9 +959,7 @@ def prefill_only(args, kvr, peaks_d, peaks_src, rank, world):
                       "parallelism": f"dp{world}", "l2": "K/V of the full layer re-read from L2 by every query tile"},
            "kernels": {"full_attn_prefill_chunk": {"ms": round(ms_f, 3), "TFLOP/s": round(tf_full, 1),
                                                    "flop": pw.flops_full()},
-                       "swa_sink_prefill_chunk": {"ms": round(ms_s, 4),
-                                                  "TFLOP/s": round(pw.flops_swa() / (ms_s / 1e3) / 1e12, 1),
-                                                  "flop": pw.flops_swa()}},
+                       "swa_sink_prefill_chunk": swa_prefill_entry(pw, ms_s, peaks_d["hbm_gbs"], peaks_src)},
            "roofline": with_nominal({"bound": "tensor", "achieved": round(tf_full, 1), "peak": pk, "unit": "TFLOP/s",
                         "frac": round(tf_full / pk, 4), "peak_source": peaks_src + " (sustained)",
                         "kernel": "full_prefill_tc_kernel", "traffic": kernel_traffic("full_prefill_tc_kernel")}),
