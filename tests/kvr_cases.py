@@ -64,7 +64,7 @@ def fill_ring(ring, syn: Synth, seqs, last_pos, table, vscale):
 
 
 def compare(got, want, what=""):
-    """Assert the spec bar: max |err| <= 2e-2 and relative RMS <= 1e-2."""
+    """Assert the accuracy bar: max |err| <= 2e-2 and relative RMS <= 1e-2."""
     g = got.float().cpu().double().numpy() if isinstance(got, torch.Tensor) else np.asarray(got, dtype=np.float64)
     w = np.asarray(want, dtype=np.float64)
     assert g.shape == w.shape, (g.shape, w.shape)
