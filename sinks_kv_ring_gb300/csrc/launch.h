@@ -67,6 +67,12 @@ cudaError_t launch_swa_prefill_tc(const uint16_t *q, int64_t P0, int C, int seq,
 cudaError_t launch_swa_band(const uint16_t *q, int64_t P0, int C, int seq, int hq, const KvView &chunk,
                             const KvView &ring, const float *sinks, const float *table, float softmax_scale,
                             uint16_t *out, unsigned *status, cudaStream_t st, bool *taken);
+// The same for a batch of chunks (builds the plan in `ws`, then the band
+// kernel for the long chunks and the short-chunk kernel for the others).
+cudaError_t launch_swa_band_varlen(const uint16_t *q, const int32_t *cu_rows, const int64_t *P0, const int32_t *seq,
+                                   int n, long long T, int hq, const KvView &chunk, const KvView &ring,
+                                   const float *sinks, const float *table, int64_t max_pos, float softmax_scale,
+                                   void *ws, uint16_t *out, unsigned *status, cudaStream_t st, bool *taken);
 // Sizes of the workspace of a varlen call (see VarlenPlan): n chunks, T rows,
 // contexts up to max_ctx, CTA items of tile_rows query rows; with `splits`,
 // chunks of one item are cut along the keys.

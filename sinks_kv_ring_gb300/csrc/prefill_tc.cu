@@ -885,9 +885,13 @@ cudaError_t launch_swa_varlen(const uint16_t *q, const int32_t *cu_rows, const i
                               const float *sinks, const float *table, int64_t max_pos, float softmax_scale,
                               void *ws, uint16_t *out, unsigned *status, cudaStream_t st) {
   const int hkv = ring.hkv;
+  bool taken = false;
+  cudaError_t e = launch_swa_band_varlen(q, cu_rows, P0, seq, n, T, hq, chunk, ring, sinks, table, max_pos,
+                                         softmax_scale, ws, out, status, st, &taken);
+  if (e != cudaSuccess || taken) return e;
   CUtensorMap m[4];
   TcArgs a;
-  cudaError_t e = tc_window_setup(chunk, T, ring, hq, sinks, table, softmax_scale, out, status, m, &a);
+  e = tc_window_setup(chunk, T, ring, hq, sinks, table, softmax_scale, out, status, m, &a);
   if (e != cudaSuccess) return e;
   e = ensure_smem_limit(8, (const void *)full_prefill_tc_kernel<true, true>, TC_SMEM);
   if (e != cudaSuccess) return e;

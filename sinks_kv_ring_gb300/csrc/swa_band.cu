@@ -55,9 +55,10 @@ constexpr int SB_OFF_K = 2 * SB_QTILE;
 constexpr int SB_OFF_V = SB_OFF_K + 3 * SB_KPART;
 constexpr int SB_OFF_O = SB_OFF_V + 2 * SB_KPART;
 constexpr int SB_OFF_BAR = SB_OFF_O + 2 * SB_QPART;
-constexpr int SB_OFF_TAG = SB_OFF_BAR + 256;       // 128 bits: ring slot c holds its pre-chunk position
-constexpr int SB_OFF_RED = SB_OFF_TAG + 16;        // half-row maxima [2][128], sums [2][2][128] (fp32)
-constexpr int SB_SMEM = SB_OFF_RED + 768 * 4 + 1024;  // + alignment slack
+constexpr int SB_OFF_RED = SB_OFF_BAR + 256;       // half-row maxima [2][128], sums [2][2][128] (fp32)
+constexpr int SB_OFF_INFO = SB_OFF_RED + 768 * 4;  // records of the work items in flight [8] (SbInfo)
+constexpr int SB_NINFO = 8;
+constexpr int SB_SMEM = SB_OFF_INFO + SB_NINFO * 64 + 1024;  // + alignment slack
 static_assert(SB_OFF_K % 1024 == 0 && SB_KPART % 1024 == 0 && SB_OFF_V % 1024 == 0 && SB_OFF_O % 1024 == 0,
               "swizzled tiles start on 1024-byte boundaries");
 static_assert(SB_SMEM <= 227 * 1024, "one CTA per SM");
@@ -81,11 +82,16 @@ constexpr int SBB_OFREE = 136;  // O read out of TMEM (128 arrivals)
 constexpr int SBB_DRAIN = 144;  // every MMA of the CTA done
 constexpr int SBB_TMEM = 152;   // u32: TMEM base
 constexpr int SBB_ABORT = 156;  // u32: a wait timed out
+constexpr int SBB_KLAND = 160;  // a band reaching before the chunk landed (K): fill its rows before the chunk
+constexpr int SBB_VLAND = 168;  // the same for V
+constexpr int SBB_INFO = 192;   // [8] the record of work item i is in slot i % 8
 
 struct SbArgs {
-  long long P0;
+  long long P0;              // one chunk: its first position, rows, ring row
   int C, hq, G, hkv, np, nitems;
   int ring_seq;
+  VarlenPlan plan;           // a batch of chunks: the plan (items of 128 query rows)
+  uint16_t *out;             // [rows][hq][128] (row-by-row stores)
   const int32_t *slot_pos;  // [ring sequences][128]
   const uint16_t *ring_k;   // [ring sequences][hkv][128][192]
   const uint16_t *ring_v;   // [ring sequences][hkv][128][128]
@@ -100,12 +106,20 @@ __device__ __forceinline__ bool sb_wait(uint32_t bar, uint32_t parity, volatile 
   return __all_sync(0xffffffffu, ok);
 }
 
-// Item i of this CTA: KV head and first chunk row.
-__device__ __forceinline__ void sb_item(const SbArgs &a, int i, int &kv, int &r0) {
-  const int w = (int)blockIdx.x + i * (int)gridDim.x;
-  kv = w % a.hkv;
-  r0 = (w / a.hkv) * a.np;
-}
+// The record of a work item: 128 query rows (rows r0 .. r0 + 128/G - 1 of a
+// chunk, times the G heads of KV head kv) and the chunk they belong to.
+struct SbInfo {
+  int c0;            // the chunk's first row in q, out and the staged rows
+  int C;             // its rows
+  int P0;            // position of its first row
+  int seq;           // its ring
+  int kv, r0;
+  int mode;          // > 0: attend; 0: a bad position or sequence (rows written as zeros)
+  int pad;
+  uint32_t held[4];  // bit c: ring slot c holds position P0 - 128 + ((c - P0) mod 128)
+  uint32_t pad2[4];
+};
+static_assert(sizeof(SbInfo) == 64, "64-byte records");
 // Bits lo .. hi (clamped to 0 .. 31) of a word.
 __device__ __forceinline__ uint32_t span_bits(int lo, int hi) {
   lo = lo < 0 ? 0 : lo;
@@ -114,8 +128,10 @@ __device__ __forceinline__ uint32_t span_bits(int lo, int hi) {
 }
 // An item whose rows reach before the chunk: those band columns are
 // attended only where the position exists and its ring slot holds it.
-__device__ __forceinline__ bool sb_boundary(int r0) { return r0 < WIN - 1; }
+__device__ __forceinline__ bool sb_boundary(const SbInfo &t) { return t.mode > 0 && t.r0 < WIN - 1; }
 
+// VARLEN: the items of the long chunks of a batch (plan); else one chunk.
+template <bool VARLEN>
 __global__ void __launch_bounds__(SB_THREADS, 1)
     swa_band_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmo,
                     const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
@@ -126,9 +142,15 @@ __global__ void __launch_bounds__(SB_THREADS, 1)
   uint8_t *gbase = smem_raw + (base - raw);
   const uint32_t sK = base + SB_OFF_K, sV = base + SB_OFF_V, sO = base + SB_OFF_O, sBar = base + SB_OFF_BAR;
   volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(gbase + SB_OFF_BAR + SBB_ABORT);
-  const uint32_t *held = reinterpret_cast<const uint32_t *>(gbase + SB_OFF_TAG);
+  SbInfo *infos = reinterpret_cast<SbInfo *>(gbase + SB_OFF_INFO);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int n_my = (int)blockIdx.x < a.nitems ? (a.nitems - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+  const int nitems = VARLEN ? a.plan.item_prefix[a.plan.n] : a.nitems;
+  const int n_my = (int)blockIdx.x < nitems ? (nitems - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+  // record of item i (written by the query producer, two items ahead)
+  auto info = [&](int i) -> const SbInfo & { return infos[i % SB_NINFO]; };
+  auto info_ready = [&](int i) {  // one thread
+    return mbar_wait(sBar + SBB_INFO + 8 * (i % SB_NINFO), (uint32_t)(i / SB_NINFO) & 1u, abort_flag);
+  };
 
   if (tid == 0) {
     for (int i = 0; i < 2; ++i) {
@@ -147,15 +169,11 @@ __global__ void __launch_bounds__(SB_THREADS, 1)
     mbar_init(sBar + SBB_OFULL, 1);
     mbar_init(sBar + SBB_OFREE, 256);
     mbar_init(sBar + SBB_DRAIN, 1);
+    mbar_init(sBar + SBB_KLAND, 1);
+    mbar_init(sBar + SBB_VLAND, 1);
+    for (int k = 0; k < SB_NINFO; ++k) mbar_init(sBar + SBB_INFO + 8 * k, 1);
     *abort_flag = 0;
     fence_mbar_init();
-  }
-  if (tid < WIN) {
-    // Ring slot c stands for position P0 - 128 + ((c - P0) mod 128).
-    const long long pos = a.P0 - WIN + ((tid - (int)(a.P0 & (WIN - 1))) & (WIN - 1));
-    const bool h = pos >= 0 && a.slot_pos[(long long)a.ring_seq * WIN + tid] == (int32_t)pos;
-    const unsigned bits = __ballot_sync(0xffffffffu, h);
-    if (lane == 0) reinterpret_cast<uint32_t *>(gbase + SB_OFF_TAG)[warp] = bits;
   }
   if (warp == SB_WARP_MMA) {
     tmem_alloc(sBar + SBB_TMEM, 512);
@@ -175,25 +193,74 @@ __global__ void __launch_bounds__(SB_THREADS, 1)
     // for the warp.
     const bool qw = warp == SB_WARP_TMAQ;
     int last_a = -1, last_b = -1;  // last loads issued: K, V (warp 13); even, odd query tile (warp 14)
+    // Warp 14 writes the record of item i (slot i % 8) before loading its
+    // query tile; the slot last served item i-8, whose epilogue is done once
+    // S(i-2) is (the query tile waits for that).  A batch's items come in
+    // chunk order, so the chunk search starts at the previous item's chunk.
+    int s_cur = 0;
+    auto make_info = [&](int i) {
+      const int w = (int)blockIdx.x + i * (int)gridDim.x;
+      SbInfo t{};
+      if (VARLEN) {
+        int lo = s_cur, hi = a.plan.n;  // item_prefix[lo] <= w < item_prefix[hi]
+        while (hi - lo > 1) {
+          const int mid = (lo + hi) >> 1;
+          if (a.plan.item_prefix[mid] <= w) lo = mid; else hi = mid;
+        }
+        s_cur = lo;
+        const int local = w - a.plan.item_prefix[lo];
+        t.kv = local % a.hkv;
+        t.r0 = (local / a.hkv) * a.np;
+        t.c0 = a.plan.cu_rows[lo];
+        t.C = a.plan.cu_rows[lo + 1] - t.c0;
+        t.P0 = (int)a.plan.P0[lo];
+        t.seq = a.plan.seq[lo];
+        t.mode = a.plan.mode[lo];
+      } else {
+        t.kv = w % a.hkv;
+        t.r0 = (w / a.hkv) * a.np;
+        t.c0 = 0;
+        t.C = a.C;
+        t.P0 = (int)a.P0;
+        t.seq = a.ring_seq;
+        t.mode = 1;
+      }
+      for (int k = 0; k < 4; ++k) {  // ring slot c = 32k + lane: holds its pre-chunk position?
+        bool h = false;
+        if (sb_boundary(t)) {
+          const int c = 32 * k + lane;
+          const long long pos = (long long)t.P0 - WIN + ((c - (t.P0 & (WIN - 1))) & (WIN - 1));
+          h = pos >= 0 && a.slot_pos[(long long)t.seq * WIN + c] == (int32_t)pos;
+        }
+        t.held[k] = __ballot_sync(0xffffffffu, h);
+      }
+      if (lane == 0) {
+        infos[i % SB_NINFO] = t;
+        mbar_arrive(sBar + SBB_INFO + 8 * (i % SB_NINFO));
+      }
+      __syncwarp();
+    };
     auto load_q = [&](int i) {
-      int kv, r0;
-      sb_item(a, i, kv, r0);
+      make_info(i);
+      const SbInfo &t = info(i);
       const uint32_t bar = sBar + SBB_QFULL + 8 * (i & 1);
       mbar_expect_tx_elect(bar, SB_QTILE);
       for (int part = 0; part < 3; ++part)
-        tma_load_3d_elect(base + (i & 1) * SB_QTILE + part * SB_QPART, &tmq, 64 * part, kv * a.G, r0, bar);
+        tma_load_3d_elect(base + (i & 1) * SB_QTILE + part * SB_QPART, &tmq, 64 * part, t.kv * a.G, t.c0 + t.r0, bar);
       (i & 1 ? last_b : last_a) = i;
     };
-    auto load_band = [&](int i, bool v) {
-      int kv, r0;
-      sb_item(a, i, kv, r0);
+    // (warp 13) false when the record did not come (abort)
+    auto load_band = [&](int i, bool v) -> bool {
+      if (!sb_wait(sBar + SBB_INFO + 8 * (i % SB_NINFO), (uint32_t)(i / SB_NINFO) & 1u, abort_flag)) return false;
+      const SbInfo &t = info(i);
       const uint32_t bar = sBar + (v ? SBB_VFULL : SBB_KFULL);
       const int parts = v ? 2 : 3;
       mbar_expect_tx_elect(bar, parts * SB_KPART);
       for (int part = 0; part < parts; ++part)
-        tma_load_4d_elect((v ? sV : sK) + part * SB_KPART, v ? (const void *)&tmv : (const void *)&tmk, 0, part, kv,
-                          r0 - 128, bar);
+        tma_load_4d_elect((v ? sV : sK) + part * SB_KPART, v ? (const void *)&tmv : (const void *)&tmk, 0, part, t.kv,
+                          t.c0 + t.r0 - 128, bar);
       (v ? last_b : last_a) = i;
+      return true;
     };
     auto ready = [&](uint32_t bar, uint32_t parity) {
       return __shfl_sync(0xffffffffu, (int)mbar_test(bar, parity), 0) != 0;
@@ -204,13 +271,20 @@ __global__ void __launch_bounds__(SB_THREADS, 1)
         load_q(0);
         if (n_my > 1) load_q(1);
         n1 = 2;
-      } else {
-        load_band(0, false);
-        load_band(0, true);
+      } else if (!load_band(0, false) || !load_band(0, true)) {
+        n1 = n2 = n_my;  // aborted: nothing more to load
       }
     }
+    // Warp 13 also watches each band's K and V land, in item order, and
+    // tells the RoPE warps when a band that reaches before the chunk is in
+    // (they then fill its rows before the chunk).  A waiter on a barrier that
+    // may be two phases behind would mistake an old phase for the one it
+    // wants, so the next load of a stream goes out only once the previous
+    // one was seen to land, and the RoPE warps wait on barriers that move
+    // once per such band.
+    int lk = 0, lv = 0;  // next items whose K / V landing is still to be seen
     uint64_t t_last = global_ns();
-    while (qw ? n1 < n_my : (n1 < n_my || n2 < n_my)) {
+    while (qw ? n1 < n_my : (n1 < n_my || n2 < n_my || lk < n_my || lv < n_my)) {
       bool prog = false;
       if (qw) {
         if (ready(sBar + SBB_QFREE + 8 * (n1 & 1), (uint32_t)((n1 - 2) >> 1) & 1u)) {
@@ -218,12 +292,22 @@ __global__ void __launch_bounds__(SB_THREADS, 1)
           prog = true;
         }
       } else {
-        if (n1 < n_my && ready(sBar + SBB_KFREE, (uint32_t)(n1 - 1) & 1u)) {
-          load_band(n1++, false);
+        if (lk < n1 && ready(sBar + SBB_KFULL, (uint32_t)lk & 1u)) {
+          if (lane == 0 && sb_boundary(info(lk))) mbar_arrive(sBar + SBB_KLAND);
+          ++lk;
           prog = true;
         }
-        if (n2 < n_my && ready(sBar + SBB_VFREE, (uint32_t)(n2 - 1) & 1u)) {
-          load_band(n2++, true);
+        if (lv < n2 && ready(sBar + SBB_VFULL, (uint32_t)lv & 1u)) {
+          if (lane == 0 && sb_boundary(info(lv))) mbar_arrive(sBar + SBB_VLAND);
+          ++lv;
+          prog = true;
+        }
+        if (n1 < n_my && lk == n1 && ready(sBar + SBB_KFREE, (uint32_t)(n1 - 1) & 1u)) {
+          if (!load_band(n1++, false)) break;
+          prog = true;
+        }
+        if (n2 < n_my && lv == n2 && ready(sBar + SBB_VFREE, (uint32_t)(n2 - 1) & 1u)) {
+          if (!load_band(n2++, true)) break;
           prog = true;
         }
       }
@@ -265,12 +349,12 @@ __global__ void __launch_bounds__(SB_THREADS, 1)
     const uint64_t dv = sdesc_sw128(sV, SB_KPART, 1024);  // LBO = the other 64-dim half of V
     int nbk = 0, nbv = 0;  // boundary items met (their patch barriers' phases)
     auto issue_S = [&](int i) -> bool {
-      int kv, r0;
-      sb_item(a, i, kv, r0);
       const int q = i & 1;
+      if (!sb_wait(sBar + SBB_INFO + 8 * (i % SB_NINFO), (uint32_t)(i / SB_NINFO) & 1u, abort_flag)) return false;
+      const bool bnd = sb_boundary(info(i));
       if (!sb_wait(sBar + SBB_QROPE + 8 * q, (uint32_t)(i >> 1) & 1u, abort_flag)) return false;
       if (!sb_wait(sBar + SBB_KFULL, (uint32_t)i & 1u, abort_flag)) return false;
-      if (sb_boundary(r0)) {
+      if (bnd) {
         if (!sb_wait(sBar + SBB_KPATCH, (uint32_t)nbk & 1u, abort_flag)) return false;
         ++nbk;
       }
@@ -288,13 +372,12 @@ __global__ void __launch_bounds__(SB_THREADS, 1)
       mma_commit_elect(sBar + SBB_QFREE + 8 * q);
       return true;
     };
-    auto issue_PV = [&](int i) -> bool {
-      int kv, r0;
-      sb_item(a, i, kv, r0);
+    auto issue_PV = [&](int i) -> bool {  // (S(i) came first: the record of item i is in)
+      const bool bnd = sb_boundary(info(i));
       const int s = i & 1;
       if (!sb_wait(sBar + SBB_PREADY + 8 * s, (uint32_t)(i >> 1) & 1u, abort_flag)) return false;
       if (!sb_wait(sBar + SBB_VFULL, (uint32_t)i & 1u, abort_flag)) return false;
-      if (sb_boundary(r0)) {
+      if (bnd) {
         if (!sb_wait(sBar + SBB_VPATCH, (uint32_t)nbv & 1u, abort_flag)) return false;
         ++nbv;
       }
@@ -326,21 +409,24 @@ __global__ void __launch_bounds__(SB_THREADS, 1)
   else if (warp >= SB_WARP_ROPE) {
     // ------------------------------------------------------------ RoPE + ring rows (warps 8-11)
     const int t = tid - 32 * SB_WARP_ROPE;
+    int nb = 0;  // boundary items met (phases of the land / fill barriers)
     for (int i = 0; i < n_my; ++i) {
-      int kv, r0;
-      sb_item(a, i, kv, r0);
+      if (!info_ready(i)) break;
+      const SbInfo &it0 = info(i);
+      const int kv = it0.kv, r0 = it0.r0;
       const int q = i & 1;
-      // (row, chunk pair) tasks: row r = it / 4 (position r0 + r / G), dims
-      // 8c..8c+7 with 32+8c..; table rows fetched before the wait
+      // (row, chunk pair) tasks: row r = it / 4 (chunk row r0 + r / G), dims
+      // 8c..8c+7 with 32+8c..; table rows fetched before the wait.  Rows past
+      // the chunk, and every row of an item of a bad chunk, are not rotated.
       float4 tv[4][4];
       bool liv[4];
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         const int it = t + 128 * k, r = it >> 2, c = it & 3;
         const int ii = r0 + r / a.G;
-        liv[k] = ii < a.C;
+        liv[k] = it0.mode > 0 && ii < it0.C;
         if (liv[k]) {
-          const float4 *tr = reinterpret_cast<const float4 *>(a.table + (a.P0 + ii) * 64 + 16 * c);
+          const float4 *tr = reinterpret_cast<const float4 *>(a.table + ((long long)it0.P0 + ii) * 64 + 16 * c);
 #pragma unroll
           for (int u = 0; u < 4; ++u) tv[k][u] = tr[u];
         }
@@ -349,7 +435,7 @@ __global__ void __launch_bounds__(SB_THREADS, 1)
       uint8_t *qt = gbase + q * SB_QTILE;
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        if (!liv[k]) continue;  // rows past the chunk keep the zeros of the box
+        if (!liv[k]) continue;
         const int it = t + 128 * k, r = it >> 2, c = it & 3;
         float cs[16];
 #pragma unroll
@@ -365,33 +451,38 @@ __global__ void __launch_bounds__(SB_THREADS, 1)
       }
       fence_proxy_async_smem();
       mbar_arrive(sBar + SBB_QROPE + 8 * q);
-      if (!sb_boundary(r0)) continue;
-      // Band rows 1 .. 127-r0 are chunk rows r0-127 .. -1, positions
-      // P0+r0-127 .. P0-1: copied from the ring where the slot holds the
-      // position (the box left zeros everywhere else).
-      const int t_hi = WIN - 1 - r0;
-      const uint16_t *rk = a.ring_k + ((long long)a.ring_seq * a.hkv + kv) * WIN * DQK;
-      const uint16_t *rv = a.ring_v + ((long long)a.ring_seq * a.hkv + kv) * WIN * DV;
+      if (!sb_boundary(it0)) continue;
+      // Band rows 0 .. 127-r0 are chunk rows r0-128 .. -1, positions
+      // P0+r0-128 .. P0-1: the ring row where the slot holds the position,
+      // else zeros (in a batch these rows of the box belong to the previous
+      // chunk; before row 0 of the batch the box brought zeros).
+      const int t_hi = WIN - r0;
+      const uint16_t *rk = a.ring_k + ((long long)it0.seq * a.hkv + kv) * WIN * DQK;
+      const uint16_t *rv = a.ring_v + ((long long)it0.seq * a.hkv + kv) * WIN * DV;
       for (int h = 0; h < 2; ++h) {
         const bool v = h == 1;
-        if (!mbar_wait(sBar + (v ? SBB_VFULL : SBB_KFULL), (uint32_t)i & 1u, abort_flag)) break;
+        if (!mbar_wait(sBar + (v ? SBB_VLAND : SBB_KLAND), (uint32_t)nb & 1u, abort_flag)) break;
         const int nch = v ? DV / 8 : DQK / 8;  // 16-byte chunks of a row
         // asynchronous 16-byte copies, all in flight before the one wait
         for (int e = t; e < t_hi * nch; e += 128) {
-          const int tr = 1 + e / nch, cc = e % nch;
-          const long long p = a.P0 + r0 - 128 + tr;
-          if (p < 0) continue;
+          const int tr = e / nch, cc = e % nch;
+          const long long p = (long long)it0.P0 + r0 - 128 + tr;
           const int slot = (int)(p & (WIN - 1));
-          if (!((held[slot >> 5] >> (slot & 31)) & 1u)) continue;
-          const uint16_t *src = v ? rv + (long long)slot * DV + 8 * cc : rk + (long long)slot * DQK + 8 * cc;
-          cp_async16(base + (v ? SB_OFF_V : SB_OFF_K) + (cc >> 3) * SB_KPART + tr * 128 + (((cc & 7) ^ (tr & 7)) << 4),
-                     src);
+          const uint32_t dst =
+              (v ? SB_OFF_V : SB_OFF_K) + (cc >> 3) * SB_KPART + tr * 128 + (((cc & 7) ^ (tr & 7)) << 4);
+          if (p >= 0 && ((it0.held[slot >> 5] >> (slot & 31)) & 1u)) {
+            const uint16_t *src = v ? rv + (long long)slot * DV + 8 * cc : rk + (long long)slot * DQK + 8 * cc;
+            cp_async16(base + dst, src);
+          } else {
+            *reinterpret_cast<uint4 *>(gbase + dst) = make_uint4(0, 0, 0, 0);
+          }
         }
         cp_async_commit();
         cp_async_wait<0>();
         fence_proxy_async_smem();
         mbar_arrive(sBar + (v ? SBB_VPATCH : SBB_KPATCH));
       }
+      ++nb;
     }
   } else {
     // ------------------------------------------------------------ softmax + epilogue (warps 0-7)
@@ -408,10 +499,12 @@ __global__ void __launch_bounds__(SB_THREADS, 1)
     float *red_m = reinterpret_cast<float *>(gbase + SB_OFF_RED);  // [2 halves][128] maxima
     float *red_l = red_m + 256;                                      // [2 items][2 halves][128] sums
     // The output of item j: O / l as bf16 into the staging tile, then two
-    // TMA boxes.
+    // TMA boxes; the last block of a chunk in a batch, whose box would reach
+    // into the next chunk's rows, is stored row by row instead.
     auto epilogue = [&](int j, bool good) -> bool {
-      int kv, r0;
-      sb_item(a, j, kv, r0);
+      const SbInfo &t = info(j);  // (its softmax waited for the record)
+      const int kv = t.kv;
+      const bool by_rows = VARLEN && t.r0 + a.np > t.C;
       if (good) good = sb_wait(sBar + SBB_OFULL, (uint32_t)j & 1u, abort_flag);
       if (tid == 0) bulk_wait_read_all();  // the last store has read the staging tile
       good = named_bar_and(1, 256, good);
@@ -435,17 +528,23 @@ __global__ void __launch_bounds__(SB_THREADS, 1)
         for (int u = 0; u < 4; ++u) {
           const uint32_t w0 = w[4 * u], w1 = w[4 * u + 1], w2 = w[4 * u + 2], w3 = w[4 * u + 3];
           const int ch = 4 * c + u;  // 16-byte chunk of dims 64h + 8 ch .. within part h
-          *reinterpret_cast<uint4 *>(gbase + SB_OFF_O + h * SB_QPART + row * 128 + ((ch ^ (row & 7)) << 4)) =
-              make_uint4(w0, w1, w2, w3);
+          if (by_rows) {
+            if (t.r0 + d < t.C)
+              reinterpret_cast<uint4 *>(a.out + ((long long)(t.c0 + t.r0 + d) * a.hq + kv * a.G + g) * DV + 64 * h)[ch] =
+                  make_uint4(w0, w1, w2, w3);
+          } else {
+            *reinterpret_cast<uint4 *>(gbase + SB_OFF_O + h * SB_QPART + row * 128 + ((ch ^ (row & 7)) << 4)) =
+                make_uint4(w0, w1, w2, w3);
+          }
         }
       }
       tc_fence_before();
       mbar_arrive(sBar + SBB_OFREE);
       fence_proxy_async_smem();
       named_bar_sync(1, 256);
-      if (tid == 0) {  // rows past the chunk are clipped by the store
-        tma_store_3d(&tmo, 0, kv * a.G, r0, sO);
-        tma_store_3d(&tmo, 64, kv * a.G, r0, sO + SB_QPART);
+      if (tid == 0 && !by_rows) {  // rows past the last one of the output are clipped by the store
+        tma_store_3d(&tmo, 0, kv * a.G, t.c0 + t.r0, sO);
+        tma_store_3d(&tmo, 64, kv * a.G, t.c0 + t.r0, sO + SB_QPART);
         bulk_commit();
       }
       return true;
@@ -453,11 +552,12 @@ __global__ void __launch_bounds__(SB_THREADS, 1)
     bool ok = true;
     for (int i = 0; i <= n_my; ++i) {
       if (i < n_my && ok) {
-        int kv, r0;
-        sb_item(a, i, kv, r0);
         const int s = i & 1;
-        const float sink2 = a.sinks[kv * a.G + g] * LOG2E;
-        ok = sb_wait(sBar + SBB_SFULL + 8 * s, (uint32_t)(i >> 1) & 1u, abort_flag);
+        ok = sb_wait(sBar + SBB_INFO + 8 * (i % SB_NINFO), (uint32_t)(i / SB_NINFO) & 1u, abort_flag);
+        const SbInfo &t = info(i);
+        const float sink2 = ok ? a.sinks[t.kv * a.G + g] * LOG2E : 0.f;
+        const int r0 = t.r0;
+        if (ok) ok = sb_wait(sBar + SBB_SFULL + 8 * s, (uint32_t)(i >> 1) & 1u, abort_flag);
         ok = named_bar_and(2, 256, ok);
         if (ok) {
           tc_fence_after();
@@ -473,8 +573,11 @@ __global__ void __launch_bounds__(SB_THREADS, 1)
           uint32_t msk[3];
 #pragma unroll
           for (int k = 0; k < 3; ++k) msk[k] = span_bits(d + 1 - cb - 32 * k, d + WIN - cb - 32 * k);
-          if (sb_boundary(r0)) {
-            const long long pfirst = a.P0 + r0 - 128;     // position of column 0
+          if (t.mode <= 0) {  // a bad chunk: nothing attended, its rows come out as zeros
+#pragma unroll
+            for (int k = 0; k < 3; ++k) msk[k] = 0u;
+          } else if (sb_boundary(t)) {
+            const long long pfirst = (long long)t.P0 + r0 - 128;  // position of column 0
             const int tneg = WIN - r0;                     // columns before the chunk
             const int t0 = pfirst < 0 ? (int)-pfirst : 0;  // first column with a position
             const int off = (int)(pfirst & (WIN - 1));     // ring slot of column 0
@@ -482,7 +585,7 @@ __global__ void __launch_bounds__(SB_THREADS, 1)
             for (int k = 0; k < 3; ++k) {
               const int ck = cb + 32 * k;
               const int sb = ck + off, w0 = (sb >> 5) & 3, sh = sb & 31;
-              const uint32_t hk = __funnelshift_r(held[w0], held[(w0 + 1) & 3], sh);  // bit e: slot (sb + e) % 128
+              const uint32_t hk = __funnelshift_r(t.held[w0], t.held[(w0 + 1) & 3], sh);  // bit e: slot (sb + e) % 128
               const uint32_t before = span_bits(-ck, tneg - 1 - ck);
               const uint32_t exists = span_bits(t0 - ck, 31);
               msk[k] &= ~before | (hk & exists);
@@ -493,7 +596,7 @@ __global__ void __launch_bounds__(SB_THREADS, 1)
           // (before a row's window) and 128 .. 143 (after it) can be masked,
           // i.e. the first 16 and the last 16 of either half.
           const uint32_t NINF = __float_as_uint(-INFINITY);
-          if (sb_boundary(r0)) {
+          if (sb_boundary(t) || t.mode <= 0) {
 #pragma unroll
             for (int e = 0; e < 72; ++e) v[e] = (msk[e >> 5] >> (e & 31)) & 1u ? v[e] : NINF;
           } else {
@@ -550,42 +653,82 @@ __global__ void __launch_bounds__(SB_THREADS, 1)
 
 }  // namespace
 
+namespace {
+
+// Tensor maps (q and out as 128-row tiles of (position, head) rows; the
+// staged rows as 144-token boxes of one KV head) and the common arguments.
+bool band_setup(const uint16_t *q, long long T, int hq, const KvView &chunk, const KvView &ring, const float *sinks,
+                const float *table, float softmax_scale, uint16_t *out, unsigned *status, CUtensorMap *m,
+                SbArgs *a) {
+  const int hkv = ring.hkv, G = hq / hkv;
+  if (G < 8 || 128 % G || T <= 0 || T >= (1LL << 31)) return false;
+  if (!make_tma_map_heads3d(&m[0], q, T, hq, DQK, G) || !make_tma_map_heads3d(&m[1], out, T, hq, DV, G) ||
+      !make_tma_map_tokens4d(&m[2], chunk.k, T, hkv, DQK, SB_N, true) ||
+      !make_tma_map_tokens4d(&m[3], chunk.v, T, hkv, DV, SB_N, true))
+    return false;
+  *a = SbArgs{};
+  a->hq = hq;
+  a->G = G;
+  a->hkv = hkv;
+  a->np = 128 / G;
+  a->slot_pos = ring.slot_pos;
+  a->ring_k = ring.k;
+  a->ring_v = ring.v;
+  a->sinks = sinks;
+  a->table = table;
+  a->scale_log2 = softmax_scale * LOG2E;
+  a->out = out;
+  a->status = status;
+  return true;
+}
+
+}  // namespace
+
 cudaError_t launch_swa_band(const uint16_t *q, int64_t P0, int C, int seq, int hq, const KvView &chunk,
                             const KvView &ring, const float *sinks, const float *table, float softmax_scale,
                             uint16_t *out, unsigned *status, cudaStream_t st, bool *taken) {
   *taken = false;
-  const int hkv = ring.hkv, G = hq / hkv;
-  if (G < 8 || 128 % G) return cudaSuccess;
-  const int np = 128 / G;
-  const long long nitems = ((long long)C + np - 1) / np * hkv;
-  if (C <= 0 || nitems >= (1LL << 31)) return cudaSuccess;
-  CUtensorMap mq, mo, mk, mv;
-  if (!make_tma_map_heads3d(&mq, q, C, hq, DQK, G) || !make_tma_map_heads3d(&mo, out, C, hq, DV, G) ||
-      !make_tma_map_tokens4d(&mk, chunk.k, C, hkv, DQK, SB_N, true) ||
-      !make_tma_map_tokens4d(&mv, chunk.v, C, hkv, DV, SB_N, true))
-    return cudaSuccess;
-  cudaError_t e = ensure_smem_limit(10, (const void *)swa_band_kernel, SB_SMEM);
+  CUtensorMap m[4];
+  SbArgs a;
+  if (!band_setup(q, C, hq, chunk, ring, sinks, table, softmax_scale, out, status, m, &a)) return cudaSuccess;
+  const long long nitems = ((long long)C + a.np - 1) / a.np * a.hkv;
+  if (nitems >= (1LL << 31)) return cudaSuccess;
+  cudaError_t e = ensure_smem_limit(10, (const void *)swa_band_kernel<false>, SB_SMEM);
   if (e != cudaSuccess) return e;
-  SbArgs a{};
   a.P0 = P0;
   a.C = C;
-  a.hq = hq;
-  a.G = G;
-  a.hkv = hkv;
-  a.np = np;
   a.nitems = (int)nitems;
   a.ring_seq = seq;
-  a.slot_pos = ring.slot_pos;
-  a.ring_k = ring.k;
-  a.ring_v = ring.v;
-  a.sinks = sinks;
-  a.table = table;
-  a.scale_log2 = softmax_scale * LOG2E;
-  a.status = status;
   const long long grid = nitems < num_sms() ? nitems : num_sms();
-  swa_band_kernel<<<(unsigned)grid, SB_THREADS, SB_SMEM, st>>>(mq, mo, mk, mv, a);
+  swa_band_kernel<false><<<(unsigned)grid, SB_THREADS, SB_SMEM, st>>>(m[0], m[1], m[2], m[3], a);
   *taken = true;
   return cudaGetLastError();
+}
+
+cudaError_t launch_swa_band_varlen(const uint16_t *q, const int32_t *cu_rows, const int64_t *P0, const int32_t *seq,
+                                   int n, long long T, int hq, const KvView &chunk, const KvView &ring,
+                                   const float *sinks, const float *table, int64_t max_pos, float softmax_scale,
+                                   void *ws, uint16_t *out, unsigned *status, cudaStream_t st, bool *taken) {
+  *taken = false;
+  CUtensorMap m[4];
+  SbArgs a;
+  if (!band_setup(q, T, hq, chunk, ring, sinks, table, softmax_scale, out, status, m, &a)) return cudaSuccess;
+  // the plan in items of 128 query rows; chunks of at most 32 query rows and
+  // 16 tokens go to the short-chunk kernel
+  const VarlenSizes z = varlen_sizes(n, T, hq, a.hkv, max_pos, 128, false);
+  if (z.items_max >= (1LL << 31)) return cudaSuccess;
+  cudaError_t e = ensure_smem_limit(11, (const void *)swa_band_kernel<true>, SB_SMEM);
+  if (e != cudaSuccess) return e;
+  a.plan = varlen_plan_view(z, ws, cu_rows, P0, seq, n);
+  e = launch_varlen_plan(a.plan, T, hq, a.hkv, 128, max_pos, ring.num_seqs, SWA_SHORT_ROWS, SWA_SHORT_MAX_C, status,
+                         st);
+  if (e != cudaSuccess) return e;
+  const long long grid = z.items_max < num_sms() ? z.items_max : num_sms();
+  if (grid > 0) swa_band_kernel<true><<<(unsigned)grid, SB_THREADS, SB_SMEM, st>>>(m[0], m[1], m[2], m[3], a);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  *taken = true;
+  return launch_swa_short(q, a.plan, n, T, hq, chunk, ring, sinks, table, softmax_scale, out, status, st);
 }
 
 }  // namespace kvr

@@ -78,6 +78,22 @@ def compare(got, want, what=""):
     return mx, rel
 
 
+def compare_rows_vec(got, want, what=""):
+    """The bar of compare_rows (max |err| and relative RMS of every (token,
+    head) output vector on its own), vectorised for large cases."""
+    g = got.float().cpu().double().numpy().reshape(-1, got.shape[-1])
+    w = np.asarray(want, dtype=np.float64).reshape(-1, g.shape[-1])
+    assert np.all(np.isfinite(g)), f"{what}: non-finite output"
+    err = np.abs(g - w)
+    assert err.max() <= MAX_ABS, f"{what}: max|err| {err.max():.3e}"
+    rms_w = np.sqrt(np.mean(w * w, axis=1))
+    rms_e = np.sqrt(np.mean(err * err, axis=1))
+    rel = np.where(rms_w > 0, rms_e / np.where(rms_w > 0, rms_w, 1.0), rms_e)
+    worst = int(np.argmax(rel))
+    assert rel[worst] <= REL_RMS, f"{what}: row {worst} rel RMS {rel[worst]:.3e}"
+    return float(rel[worst])
+
+
 def compare_rows(got, want, what=""):
     """The bar row by row (each (token, head) output vector on its own), so a
     tiny-valued row (the sink taking the mass) is still held to 1e-2."""

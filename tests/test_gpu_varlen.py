@@ -10,7 +10,7 @@ import oracle
 import sinks_kv_ring_gb300 as kvr
 from sinks_kv_ring_gb300.synth import Synth
 
-from kvr_cases import SCALE, compare_rows, fill_paged, fill_ring, raw_kv
+from kvr_cases import SCALE, compare, compare_rows, compare_rows_vec, fill_paged, fill_ring, raw_kv
 
 pytestmark = pytest.mark.gpu
 
@@ -276,6 +276,40 @@ def test_varlen_plan_more_than_1024_chunks(tables):
         want = oracle.attend_seq(qw[r], np.arange(3000, 3000 + Cs[i]), k, v, 2873, 1e4, VS, SCALE, 128,
                                  sinks.double().cpu().numpy())
         compare_rows(outw[r], want, f"swa chunk {i}")
+
+
+@pytest.mark.parametrize("hq,hkv", [(64, 8), (128, 8), (64, 4)])
+def test_swa_varlen_long_chunks(hq, hkv, tables):
+    # Long windowed chunks beside decode tokens and drafts with 8 or 16 q
+    # heads per KV head (tiles of 128 query rows, one key band each): chunk
+    # lengths that are not whole tiles, chunks near position 0 and deep in
+    # their sequence, a chunk of 2048 rows; every row against the oracle.
+    syn = Synth(3801 + hq + hkv, dist="plain", device=DEV)
+    sinks = syn.sinks(hq).to(DEV)
+    seqs = [0, 1, 2, 3, 4, 5, 6]
+    P0s = [0, 1000, 300, 60, 4000, 129, 2000]
+    Cs = [300, 1, 517, 130, 3, 2048, 64]
+    ring, stage, q, cu, P0, sq = _swa_case(syn, hq, hkv, seqs, P0s, Cs, tables)
+    out = kvr.swa_sink_prefill_varlen(q, cu, P0, sq, stage, ring, sinks, tables[1e4], SCALE)
+    torch.cuda.synchronize()
+    assert kvr.device_status() == 0
+    want = _swa_want(syn, hkv, q, seqs, P0s, Cs, sinks)
+    compare(out, want, "swa varlen long chunks")
+    compare_rows_vec(out, want, "swa varlen long chunks")
+    # the same call again gives the same bits (tiles of different chunks in
+    # one CTA, tiles that reach before their chunk among others)
+    again = kvr.swa_sink_prefill_varlen(q, cu, P0, sq, stage, ring, sinks, tables[1e4], SCALE)
+    assert torch.equal(again, out)
+    # a long chunk with a bad sequence id: its rows are zeros, BAD_SEQ, the
+    # others unchanged
+    sq_bad = sq.clone()
+    sq_bad[2] = ring.num_seqs
+    bad = kvr.swa_sink_prefill_varlen(q, cu, P0, sq_bad, stage, ring, sinks, tables[1e4], SCALE)
+    torch.cuda.synchronize()
+    assert kvr.device_status() == kvr.DEV_BAD_SEQ
+    r0, r1 = sum(Cs[:2]), sum(Cs[:3])
+    assert torch.count_nonzero(bad[r0:r1]) == 0
+    assert torch.equal(bad[:r0], out[:r0]) and torch.equal(bad[r1:], out[r1:])
 
 
 @pytest.mark.parametrize("hq,hkv", [(6, 2), (24, 2)])
