@@ -762,6 +762,48 @@ def swa_prefill_entry(pw, ms, hbm, peaks_src):
 
 
 
+def mixed_window_batch(kvr, hbm, peaks_src, device="cuda"):
+    """A mixed prefill / decode batch on a windowed layer through the varlen
+    call: 8 chunks of 2048 rows beside 64 decode tokens (64 q / 8 KV heads,
+    every sequence 32768 tokens in), two such batches alternated in one CUDA
+    graph.  Bytes: q and out, the staged rows, each chunk's 127 ring rows
+    and slot tags, the fp32 RoPE rows."""
+    from sinks_kv_ring_gb300.synth import Synth
+    hq, hkv, vs, P = 64, 8, 0.707, 32768
+    Cs = [2048] * 8 + [1] * 64
+    n, T = len(Cs), sum(Cs)
+    t4 = kvr.rope_table(1e4, P + max(Cs), device=device)
+    syn = Synth(1005, device=device)
+    ring = kvr.RingLayout.empty(n, hkv, device=device)
+    _fill_rings(kvr, ring, syn, n, P, t4, vs)
+    cu = torch.zeros(n + 1, dtype=torch.int32, device=device)
+    cu[1:] = torch.cumsum(torch.tensor(Cs, dtype=torch.int32, device=device), 0)
+    P0 = torch.full((n,), P, dtype=torch.int64, device=device)
+    seq = torch.arange(n, dtype=torch.int32, device=device)
+    pos = torch.cat([torch.arange(P, P + C, device=device) for C in Cs])
+    sinks = syn.sinks(hq).to(device)
+    ws = torch.empty(kvr.swa_sink_prefill_varlen_workspace_size(n), dtype=torch.uint8, device=device)
+    batches = []
+    for b in range(2):
+        stage = kvr.LinearLayout.empty(T, hkv, device=device)
+        kvr.kv_ring_append_rope(syn.k(T, hkv, seq=100 + b, start=P), syn.v(T, hkv, seq=100 + b, start=P), pos, None, t4,
+                                vs, stage)
+        batches.append((syn.q(T, hq, hkv, seq=200 + b, start=P), stage,
+                        torch.empty(T, hq, 128, dtype=torch.bfloat16, device=device)))
+    calls = [(lambda st, bt=bt: kvr.swa_sink_prefill_varlen(bt[0], cu, P0, seq, bt[1], ring, sinks, t4, SCALE,
+                                                             workspace=ws, out=bt[2], stream=st)) for bt in batches] * 2
+    ms = graph_time_ms(calls)
+    nbytes = T * hq * (192 + 128) * 2 + T * hkv * (192 + 128) * 2 + n * (127 * hkv * (192 + 128) * 2 + 128 * 4) + T * 256
+    gbs = nbytes / (ms / 1e3) / 1e9
+    return {"workload": "mixed batch on a windowed layer: 8 chunks of 2048 rows + 64 decode tokens, 64 q / 8 KV heads, "
+                        "32768 tokens in; varlen call, CUDA graph over 2 batches",
+            "graph_ms": round(ms, 4), "bytes": nbytes, "GB/s": round(gbs, 1),
+            "roofline": with_nominal({"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s",
+                                      "frac": round(gbs / hbm, 4), "peak_source": peaks_src,
+                                      "kernel": "swa_band_kernel (+ varlen_plan_kernel, swa_short_kernel)",
+                                      "traffic": None})}
+
+
 def run_prefill(kvr, steps, warmup, P0=122880, C=8192):
     stream = torch.cuda.current_stream()
     work = PrefillWorkload(kvr, P0=P0, C=C)
@@ -905,6 +947,7 @@ def main():
                                       "frac": round(agbs / hbm, 4), "peak_source": peaks_src,
                                   "kernel": "append_kernel", "traffic": kernel_traffic("append_kernel")})}
         res["gpu_launches"] += pw.launches_per_step * psteps
+        res["prefill"]["swa_sink_prefill_varlen"] = mixed_window_batch(kvr, hbm, peaks_src)
     if rank == 0:
         print(json.dumps(res), flush=True)
     if world > 1:
@@ -973,6 +1016,7 @@ def prefill_only(args, kvr, peaks_d, peaks_src, rank, world):
         "roofline": with_nominal({"bound": "hbm", "achieved": round(agbs, 1), "peak": hbm, "unit": "GB/s",
                                   "frac": round(agbs / hbm, 4), "peak_source": peaks_src,
                                   "kernel": "append_kernel", "traffic": kernel_traffic("append_kernel")})}
+    res["kernels"]["swa_sink_prefill_varlen"] = mixed_window_batch(kvr, hbm, peaks_src)
     if rank == 0:
         print(json.dumps(res), flush=True)
 
