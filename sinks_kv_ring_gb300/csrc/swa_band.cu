@@ -151,6 +151,7 @@ __global__ void __launch_bounds__(SB_THREADS, 1)
   auto info_ready = [&](int i) {  // one thread
     return mbar_wait(sBar + SBB_INFO + 8 * (i % SB_NINFO), (uint32_t)(i / SB_NINFO) & 1u, abort_flag);
   };
+  if (n_my == 0) return;  // (a batch of short chunks only: nothing set up yet, nothing to do)
 
   if (tid == 0) {
     for (int i = 0; i < 2; ++i) {
