@@ -76,6 +76,8 @@ def _stage_for(syn, hkv, P0, C, table, vscale, extra=64):
     (64, 8, 777, 129, 127),   # only the newest ring slot is live
     (128, 8, 700, 200, 0),    # G = 16: 8 positions per tile
     (64, 4, 333, 129, 0),     # G = 16 with 4 KV heads
+    (64, 2, 500, 300, 0),     # G = 32: four positions per tile
+    (128, 2, 700, 77, 3),     # G = 64: two positions per tile, stale slots
     (256, 2, 300, 40, 0),     # G = 128: one position per tile
     (8, 1, 400, 90, 0),       # one KV head
     # many items per CTA: bands slide along the ring, ranges cross KV heads
