@@ -192,10 +192,8 @@ __global__ void __launch_bounds__(SD_THREADS, SD_CTAS)
     mbar_init(vBar, 1);
     *abort_flag = 0;
     fence_mbar_init();
-    const int row = ring_row(0);
-    issue_k(row);
-    issue_v(row);
-    issued_k = issued_v = 0;
+    issue_k(ring_row(0));  // V(0) goes out once K(0) is in (below)
+    issued_k = 0;
   }
   for (int n = tid; n < nmine && n < SD_MAX_UNITS; n += SD_THREADS) sRow[n] = ring_row(n);
   for (int h = tid; h < a.hq; h += SD_THREADS) sSink[h] = a.sinks[h] * LOG2E;
@@ -230,6 +228,12 @@ __global__ void __launch_bounds__(SD_THREADS, SD_CTAS)
     if (!__syncthreads_and(mbar_wait(kBar, (uint32_t)n & 1u, abort_flag))) {
       alive = false;
       break;
+    }
+    // All CTAs start at once: their first K rows alone come in sooner than K
+    // and V together would, and V(0) then loads during this unit's S = Q K^T.
+    if (n == 0 && tid == 0) {
+      issue_v(row_of(0));
+      issued_v = 0;
     }
     if (ok) {
       // Phase 1: warp w: S = Q K^T for slots 16w .. 16w+15; slots whose tag is
