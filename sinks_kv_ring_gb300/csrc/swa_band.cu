@@ -14,9 +14,17 @@
 // r0+15, one band of 144 keys, so an item is one S = Q K^T (N = 144) and one
 // O = P V, and its softmax is a single pass with no rescaling: the window
 // and the sink are all there.  In band column t (chunk row r0-128+t) row d
-// attends columns d+1 .. d+128.  Band rows before the chunk come back from
-// the TMA unit as zeros (a negative coordinate); for the first items the
-// rows whose ring slot holds their position are then copied in.
+// attends columns d+1 .. d+128.  The RoPE warps fill a band's rows before
+// the chunk: the ring row where its slot holds the position, zeros otherwise
+// (for one chunk the box brought zeros there already, a negative coordinate;
+// in a batch those rows of the box belong to the previous chunk).
+//
+// A batch of chunks (VARLEN): the long chunks' items come from the device
+// plan (tiles of 128 query rows).  The query producer writes each item's
+// record (chunk rows, length, position, ring, KV head, tile, ring-slot bits)
+// into one of eight shared-memory slots before loading its query tile, and
+// every other role reads it from there.  A chunk's partial last tile is
+// stored row by row, as its box would reach into the next chunk's rows.
 //
 // One CTA per SM, 480 threads:
 //   warps 0-7   softmax of item i, then the epilogue of item i-1; warp w
@@ -29,10 +37,11 @@
 //               (converged; elect.sync issues)
 // Shared memory: two query tiles (3 x 16 KB each, 128-byte swizzled,
 // K-major), the band's K (3 x 18 KB, K-major) and V (2 x 18 KB, MN-major),
-// one output tile (2 x 16 KB) that leaves as two TMA boxes.  The producer
-// issues each load as soon as its buffer is free: the query tile of item
+// one output tile (2 x 16 KB) that leaves as two TMA boxes.  The producers
+// issue each load as soon as its buffer is free: the query tile of item
 // i+2 once S(i) is done, the band's K of item i+1 once S(i) is done, its V
-// once P V(i) is done.
+// once P V(i) is done; the band producer also tells the RoPE warps when a
+// band that reaches before its chunk has landed.
 // TMEM (512 columns): S0 at 0, S1 at 160 (144 fp32 columns each; the bf16
 // probabilities P overwrite the first 72 and feed P V from TMEM), O at 320.
 #include <cuda.h>
