@@ -192,6 +192,76 @@ __device__ int decode_plan_block(const int64_t *__restrict__ pos, const int32_t 
   return (int)L;
 }
 
+// The same plan made by one warp for a batch of at most 32 sequences (lane b
+// is sequence b): warp reductions and shuffles only, no block barrier.  Ties
+// between candidates of equal cost go to the lower candidate index.  The
+// split length and the item count go to prefix[B + 1] and prefix[B + 2].
+__device__ void decode_plan_warp(const int64_t *__restrict__ pos, const int32_t *__restrict__ seq, int B, int hkv,
+                                 int num_seqs, int64_t max_pos, long long max_ctx, int R, int32_t *prefix,
+                                 unsigned *status) {
+  constexpr unsigned FULL = 0xffffffffu;
+  const int lane = threadIdx.x & 31;
+  unsigned ctx = 0, bad = 0;
+  if (lane < B) {
+    const long long p = pos[lane];
+    const int s = seq[lane];
+    const bool bp = p < 0 || p >= max_pos || p + 1 > max_ctx, bs = s < 0 || s >= num_seqs;
+    if (bp || bs)
+      bad = (bp ? ST_BAD_POS : 0u) | (bs ? ST_BAD_SEQ : 0u);
+    else
+      ctx = (unsigned)(p + 1);
+  }
+  if (bad && status) flag(status, bad);
+  const unsigned mx = __reduce_max_sync(FULL, ctx);
+  const unsigned long long tot = ((unsigned long long)__reduce_add_sync(FULL, ctx >> 16) << 16) +
+                                 __reduce_add_sync(FULL, ctx & 0xffffu);
+  // candidate `lane` (lanes 0 .. 15), as in decode_plan_block
+  unsigned mine_L;
+  {
+    const unsigned k = lane % 8 + 1;
+    unsigned L;
+    if (lane < 8) {
+      unsigned n = k * (unsigned)R / ((unsigned)B * (unsigned)hkv);
+      if (n < 1) n = 1;
+      L = (mx + n - 1) / n;
+    } else {
+      const unsigned long long d = (unsigned long long)k * (unsigned)R;
+      const unsigned long long l = (tot * (unsigned)hkv + d - 1) / d;
+      L = l > (unsigned long long)FD_MAX_LEN ? (unsigned)FD_MAX_LEN : (unsigned)l;
+    }
+    L = (L + 63) / 64 * 64;
+    mine_L = L < 64 ? 64u : (L > (unsigned)FD_MAX_LEN ? (unsigned)FD_MAX_LEN : L);
+  }
+  unsigned items_mine = 0;  // items of candidate `lane`
+#pragma unroll
+  for (int c = 0; c < DP_CANDS; ++c) {
+    const unsigned L = __shfl_sync(FULL, mine_L, c);
+    const unsigned n = __reduce_add_sync(FULL, (ctx + L - 1) / L);
+    if (lane == c) items_mine = n * (unsigned)hkv;
+  }
+  unsigned key = FULL;
+  if (lane < DP_CANDS) {
+    unsigned cost = (items_mine + (unsigned)R - 1) / (unsigned)R * (mine_L + FD_ITEM_KEYS);
+    cost = cost > 0x7ffffffu ? 0x7ffffffu : cost;
+    key = (cost << 4) | (unsigned)lane;
+  }
+  const unsigned L = __shfl_sync(FULL, mine_L, (int)(__reduce_min_sync(FULL, key) & 15u));
+  // per-sequence item prefix
+  const int mine = lane < B ? (int)((ctx + L - 1) / L) * hkv : 0;
+  int x = mine;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(FULL, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane < B) prefix[lane] = x - mine;
+  if (lane == 31) {
+    prefix[B] = x;
+    prefix[B + 1] = (int)L;
+    prefix[B + 2] = x;
+  }
+}
+
 static_assert(FD_WARPS * FD_STAGES * FD_STAGE >= FD_WARPS * 16 * (MO_STRIDE + 2) * 4, "merge area");
 
 // WINDOW = false: a full layer (keys 0..p, split partials to the workspace);
@@ -223,8 +293,17 @@ __global__ void __launch_bounds__(FD_WARPS * 32, 2)
     if (B <= DP_INLINE_MAX) {
       int32_t *sPrefix = reinterpret_cast<int32_t *>(smem + FD_SMEM);
       int n;
-      split_len = decode_plan_block<FD_WARPS * 32>(pos, seq, B, hkv, pool.num_seqs, max_pos, max_ctx, gridDim.x,
-                                                   sPrefix, &n, blockIdx.x == 0 ? status : nullptr);
+      if (B <= 32) {  // one warp plans, the others wait at the barrier
+        if (warp == 0)
+          decode_plan_warp(pos, seq, B, hkv, pool.num_seqs, max_pos, max_ctx, gridDim.x, sPrefix,
+                           blockIdx.x == 0 ? status : nullptr);
+        __syncthreads();
+        split_len = sPrefix[B + 1];
+        n = sPrefix[B + 2];
+      } else {
+        split_len = decode_plan_block<FD_WARPS * 32>(pos, seq, B, hkv, pool.num_seqs, max_pos, max_ctx, gridDim.x,
+                                                     sPrefix, &n, blockIdx.x == 0 ? status : nullptr);
+      }
       nitems = n;
       if (blockIdx.x == 0) {
         int32_t *gp = const_cast<int32_t *>(plan);
@@ -570,7 +649,7 @@ cudaError_t launch_full_decode(const uint16_t *q, const int64_t *pos, const int3
                                float softmax_scale, long long max_ctx, void *ws, uint16_t *out,
                                unsigned *status, cudaStream_t st) {
   // shared memory: the stages, plus the plan's item prefix when the kernel plans itself
-  constexpr int FD_SMEM_MAX = FD_SMEM + (DP_INLINE_MAX + 1) * 4;
+  constexpr int FD_SMEM_MAX = FD_SMEM + (DP_INLINE_MAX + 3) * 4;
   cudaError_t e = ensure_smem_limit(0, (const void *)full_decode_kernel<false>, FD_SMEM_MAX);
   if (e != cudaSuccess) return e;
   const int hkv = pool.hkv, G = hq / hkv;
@@ -582,7 +661,7 @@ cudaError_t launch_full_decode(const uint16_t *q, const int64_t *pos, const int3
   const int R = 2 * num_sms();
   int smem = FD_SMEM;
   if (B <= DP_INLINE_MAX) {
-    smem += ((B + 1) * 4 + 15) / 16 * 16;
+    smem += ((B + 3) * 4 + 15) / 16 * 16;  // prefix[B + 1] and a split length and item count
   } else {
     full_decode_plan_kernel<<<1, DP_THREADS, 0, st>>>(pos, seq, B, hkv, pool.num_seqs, max_pos, max_ctx, R, plan,
                                                       status);
