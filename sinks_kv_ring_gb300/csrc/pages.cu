@@ -146,7 +146,7 @@ __global__ void __launch_bounds__(RL_THREADS) pages_release_kernel(ReleaseArgs A
 // every thread moves 16-byte chunks, GATHER_BATCH loads in flight before
 // their stores.  The KV-head-0 CTA also writes the slot tags.
 constexpr int GATHER_THREADS = 256;
-constexpr int GATHER_BATCH = 4;
+constexpr int GATHER_BATCH = 5;
 
 __global__ void __launch_bounds__(GATHER_THREADS)
     ring_gather_kernel(KvView pages, KvView ring, const int32_t *__restrict__ src_seqs,
