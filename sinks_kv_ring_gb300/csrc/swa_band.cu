@@ -79,7 +79,7 @@ constexpr int SBB_QFULL = 0;    // [2] query tile landed (TMA bytes)
 constexpr int SBB_QROPE = 16;   // [2] query tile rotated (128 arrivals)
 constexpr int SBB_QFREE = 32;   // [2] S = Q K^T of the tile done
 constexpr int SBB_SFULL = 48;   // [2] S in TMEM
-constexpr int SBB_PREADY = 64;  // [2] P in TMEM (128 arrivals)
+constexpr int SBB_PREADY = 64;  // [2] P in TMEM (256 arrivals: the eight softmax warps)
 constexpr int SBB_KFULL = 80;   // band K landed
 constexpr int SBB_VFULL = 88;   // band V landed
 constexpr int SBB_KFREE = 96;   // band K read by S = Q K^T
@@ -87,7 +87,7 @@ constexpr int SBB_VFREE = 104;  // band V read by P V
 constexpr int SBB_KPATCH = 112; // ring rows copied into K (128 arrivals)
 constexpr int SBB_VPATCH = 120; // ring rows copied into V (128 arrivals)
 constexpr int SBB_OFULL = 128;  // O in TMEM
-constexpr int SBB_OFREE = 136;  // O read out of TMEM (128 arrivals)
+constexpr int SBB_OFREE = 136;  // O read out of TMEM (256 arrivals)
 constexpr int SBB_DRAIN = 144;  // every MMA of the CTA done
 constexpr int SBB_TMEM = 152;   // u32: TMEM base
 constexpr int SBB_ABORT = 156;  // u32: a wait timed out
