@@ -312,6 +312,44 @@ def test_swa_varlen_long_chunks(hq, hkv, tables):
     assert torch.equal(bad[:r0], out[:r0]) and torch.equal(bad[r1:], out[r1:])
 
 
+def test_swa_varlen_many_long_chunks(tables):
+    # 300 chunks of 5..80 rows (none short enough for the short-chunk kernel
+    # at 8 q heads per KV head) over 40 sequences, all at 3000 on rings that
+    # hold 2872..2999: the tile records come from a long chunk search, most
+    # chunks end in a partial tile; every 13th chunk and the last ones
+    # checked row by row.
+    syn = Synth(3991, dist="plain", device=DEV)
+    hq, hkv = 64, 8
+    rng = np.random.default_rng(3991)
+    n, ns = 300, 40
+    Cs = [int(c) for c in rng.integers(5, 81, size=n)]
+    seqs = [int(x) for x in rng.integers(0, ns, size=n)]
+    T = sum(Cs)
+    sinks = syn.sinks(hq).to(DEV)
+    ring = kvr.RingLayout.empty(ns, hkv)
+    fill_ring(ring, syn, list(range(ns)), [2999] * ns, tables[1e4], VS)
+    ks, vs, ps = [], [], []
+    for s_, C in zip(seqs, Cs):
+        k, v = raw_kv(syn, hkv, s_, 3000, 3000 + C)
+        ks.append(k)
+        vs.append(v)
+        ps.append(torch.arange(3000, 3000 + C, dtype=torch.int64, device=DEV))
+    stage = kvr.LinearLayout.empty(T, hkv)
+    kvr.kv_ring_append_rope(torch.cat(ks).contiguous(), torch.cat(vs).contiguous(), torch.cat(ps), None, tables[1e4],
+                            VS, stage)
+    q, cu, P0, sq = _batch(syn, hq, hkv, seqs, [3000] * n, Cs)
+    out = kvr.swa_sink_prefill_varlen(q, cu, P0, sq, stage, ring, sinks, tables[1e4], SCALE)
+    torch.cuda.synchronize()
+    assert kvr.device_status() == 0
+    starts = np.concatenate([[0], np.cumsum(Cs)])
+    for i in list(range(0, n, 13)) + [n - 2, n - 1]:
+        k, v = raw_kv(syn, hkv, seqs[i], 2873, 3000 + Cs[i])
+        r = slice(int(starts[i]), int(starts[i + 1]))
+        want = oracle.attend_seq(q[r], np.arange(3000, 3000 + Cs[i]), k, v, 2873, 1e4, VS, SCALE, 128,
+                                 sinks.double().cpu().numpy())
+        compare_rows_vec(out[r], want, f"swa chunk {i}")
+
+
 @pytest.mark.parametrize("hq,hkv", [(6, 2), (24, 2)])
 def test_swa_prefill_odd_group_sizes(hq, hkv, tables):
     # Group sizes that do not divide the 256-row tiles (3 and 12 query heads
