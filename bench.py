@@ -1205,7 +1205,6 @@ def run_reference(args, rank, world):
     workload (one sequence per step, both layers, all heads)."""
     if rank != 0:
         return
-    import numpy as np
     import oracle
     oracle.build()
     from sinks_kv_ring_gb300.synth import Synth
