@@ -148,6 +148,48 @@ def _want(t, name, dtype, dim=None, cuda=True):
         raise ValueError(f"{name} must be contiguous")
 
 
+# The C ABI takes bare pointers, so the sizes the kernels index by are
+# checked here, before any launch.
+
+def _want_q(q):
+    _want(q, "q", torch.bfloat16, 3)
+    if q.shape[2] != DQK:
+        raise ValueError(f"q must be [rows, Hq, {DQK}], got shape {tuple(q.shape)}")
+
+
+def _want_table(table):
+    _want(table, "table", torch.float32, 3)
+    if tuple(table.shape[1:]) != (DROT // 2, 2):
+        raise ValueError(f"table must be [max_pos, {DROT // 2}, 2] (cos, sin), got shape {tuple(table.shape)}")
+
+
+def _want_len(t, name, n):
+    if t.shape[0] != n:
+        raise ValueError(f"{name} must have {n} entries, got {t.shape[0]}")
+
+
+def _out(out, rows, hq, like):
+    if out is None:
+        return torch.empty(rows, hq, DV, dtype=torch.bfloat16, device=like.device)
+    _want(out, "out", torch.bfloat16, 3)
+    if tuple(out.shape) != (rows, hq, DV):
+        raise ValueError(f"out must be [{rows}, {hq}, {DV}], got shape {tuple(out.shape)}")
+    return out
+
+
+def _same_device(first, *rest):
+    """The library launches on the current CUDA device and reads every pointer
+    of a call there, so all of the call's tensors must live on that device."""
+    dev = first.device
+    cur = torch.cuda.current_device()
+    if dev.index != cur:
+        raise ValueError(f"the call's tensors are on {dev} but the current device is cuda:{cur} "
+                         "(make it current with torch.cuda.device)")
+    for t in rest:
+        if t is not None and t.device != dev:
+            raise ValueError(f"a tensor of the call is on {t.device}, the others on {dev}")
+
+
 class RingLayout:
     """SWA pool of one layer: k [S, Hkv, 128, 192], v [S, Hkv, 128, 128] bf16,
     slot_pos [S, 128] int32 (-1 = empty)."""
@@ -161,6 +203,9 @@ class RingLayout:
             raise ValueError("ring tensors have inconsistent shapes")
         self.k, self.v, self.slot_pos = k, v, slot_pos
         self.num_seqs, self.num_kv_heads = S, H
+
+    def tensors(self):
+        return self.k, self.v, self.slot_pos
 
     @classmethod
     def empty(cls, num_seqs, num_kv_heads, device="cuda"):
@@ -193,6 +238,9 @@ class PagedLayout:
         self.k, self.v, self.block_table = k, v, block_table
         self.num_blocks, self.num_kv_heads, self.block_size = nb, H, bsz
         self.num_seqs, self.max_blocks = block_table.shape
+
+    def tensors(self):
+        return self.k, self.v, self.block_table
 
     @classmethod
     def contiguous(cls, num_seqs, num_kv_heads, max_ctx, block_size=64, device="cuda", zero=True):
@@ -228,6 +276,9 @@ class LinearLayout:
         self.k, self.v = k, v
         self.num_rows, self.num_kv_heads = T, H
 
+    def tensors(self):
+        return self.k, self.v
+
     @classmethod
     def empty(cls, rows, num_kv_heads, device="cuda"):
         return cls(torch.empty(rows, num_kv_heads, DQK, dtype=torch.bfloat16, device=device),
@@ -252,27 +303,30 @@ def kv_ring_append_rope(k, v, pos, seq, table, value_scale, dst, stream=None):
     _want(pos, "pos", torch.int64, 1)
     if seq is not None:
         _want(seq, "seq", torch.int32, 1)
-    _want(table, "table", torch.float32, 3)
+    _want_table(table)
     T, H = k.shape[0], k.shape[1]
     if tuple(k.shape) != (T, H, DQK) or tuple(v.shape) != (T, H, DV) or pos.shape[0] != T:
         raise ValueError("k/v/pos shapes disagree")
     if seq is not None and seq.shape[0] != T:
         raise ValueError("seq shape disagrees")
+    _same_device(k, v, pos, seq, table, *dst.tensors())
     c = dst.c()
     _check(lib().kv_ring_append_rope(_ptr(k), _ptr(v), _ptr(pos), _ptr(seq), T, H, _ptr(table),
                                      table.shape[0], float(value_scale), ctypes.byref(c), _stream(stream)))
 
 
 def swa_sink_decode(q, pos, seq, ring, sinks, table, softmax_scale, out=None, stream=None):
-    _want(q, "q", torch.bfloat16, 3)
+    _want_q(q)
     _want(pos, "pos", torch.int64, 1)
     _want(seq, "seq", torch.int32, 1)
     _want(sinks, "sinks", torch.float32, 1)
-    _want(table, "table", torch.float32, 3)
+    _want_table(table)
     B, Hq, _ = q.shape
-    if out is None:
-        out = torch.empty(B, Hq, DV, dtype=torch.bfloat16, device=q.device)
-    _want(out, "out", torch.bfloat16, 3)
+    _want_len(pos, "pos", B)
+    _want_len(seq, "seq", B)
+    _want_len(sinks, "sinks", Hq)
+    out = _out(out, B, Hq, q)
+    _same_device(q, pos, seq, sinks, table, out, *ring.tensors())
     c = ring.c()
     _check(lib().swa_sink_decode(_ptr(q), _ptr(pos), _ptr(seq), B, Hq, ctypes.byref(c), _ptr(sinks),
                                  _ptr(table), table.shape[0], float(softmax_scale), _ptr(out), _stream(stream)))
@@ -284,18 +338,19 @@ def full_attn_decode_workspace_size(B, Hq, Hkv, max_ctx) -> int:
 
 
 def full_attn_decode(q, pos, seq, pool, table, softmax_scale, max_ctx, workspace=None, out=None, stream=None):
-    _want(q, "q", torch.bfloat16, 3)
+    _want_q(q)
     _want(pos, "pos", torch.int64, 1)
     _want(seq, "seq", torch.int32, 1)
-    _want(table, "table", torch.float32, 3)
+    _want_table(table)
     B, Hq, _ = q.shape
+    _want_len(pos, "pos", B)
+    _want_len(seq, "seq", B)
     if workspace is None:
         n = full_attn_decode_workspace_size(B, Hq, pool.num_kv_heads, max_ctx)
         workspace = torch.empty(max(n, 1), dtype=torch.uint8, device=q.device)
     _want(workspace, "workspace", torch.uint8, 1)
-    if out is None:
-        out = torch.empty(B, Hq, DV, dtype=torch.bfloat16, device=q.device)
-    _want(out, "out", torch.bfloat16, 3)
+    out = _out(out, B, Hq, q)
+    _same_device(q, pos, seq, table, workspace, out, *pool.tensors())
     c = pool.c()
     _check(lib().full_attn_decode(_ptr(q), _ptr(pos), _ptr(seq), B, Hq, ctypes.byref(c), _ptr(table),
                                   table.shape[0], float(softmax_scale), int(max_ctx), _ptr(workspace),
@@ -312,14 +367,15 @@ def full_attn_decode_noalloc(q, pos, seq, pool, table, softmax_scale, max_ctx, o
     workspace.  Calls that may run at the same time on the GPU share that
     array and must be ordered (e.g. one stream).  The first call on a device
     looks the array up; make it before any stream capture."""
-    _want(q, "q", torch.bfloat16, 3)
+    _want_q(q)
     _want(pos, "pos", torch.int64, 1)
     _want(seq, "seq", torch.int32, 1)
-    _want(table, "table", torch.float32, 3)
+    _want_table(table)
     B, Hq, _ = q.shape
-    if out is None:
-        out = torch.empty(B, Hq, DV, dtype=torch.bfloat16, device=q.device)
-    _want(out, "out", torch.bfloat16, 3)
+    _want_len(pos, "pos", B)
+    _want_len(seq, "seq", B)
+    out = _out(out, B, Hq, q)
+    _same_device(q, pos, seq, table, out, *pool.tensors())
     c = pool.c()
     _check(lib().full_attn_decode_noalloc(_ptr(q), _ptr(pos), _ptr(seq), B, Hq, ctypes.byref(c), _ptr(table),
                                           table.shape[0], float(softmax_scale), int(max_ctx), _ptr(out),
@@ -328,13 +384,13 @@ def full_attn_decode_noalloc(q, pos, seq, pool, table, softmax_scale, max_ctx, o
 
 
 def swa_sink_prefill_chunk(q, P0, seq, chunk_kv, ring, sinks, table, softmax_scale, out=None, stream=None):
-    _want(q, "q", torch.bfloat16, 3)
+    _want_q(q)
     _want(sinks, "sinks", torch.float32, 1)
-    _want(table, "table", torch.float32, 3)
+    _want_table(table)
     C, Hq, _ = q.shape
-    if out is None:
-        out = torch.empty(C, Hq, DV, dtype=torch.bfloat16, device=q.device)
-    _want(out, "out", torch.bfloat16, 3)
+    _want_len(sinks, "sinks", Hq)
+    out = _out(out, C, Hq, q)
+    _same_device(q, sinks, table, out, *chunk_kv.tensors(), *ring.tensors())
     cc, rc = chunk_kv.c(), ring.c()
     _check(lib().swa_sink_prefill_chunk(_ptr(q), int(P0), C, int(seq), Hq, ctypes.byref(cc), ctypes.byref(rc),
                                         _ptr(sinks), _ptr(table), table.shape[0], float(softmax_scale), _ptr(out),
@@ -343,12 +399,11 @@ def swa_sink_prefill_chunk(q, P0, seq, chunk_kv, ring, sinks, table, softmax_sca
 
 
 def full_attn_prefill_chunk(q, P0, seq, pool, table, softmax_scale, out=None, stream=None):
-    _want(q, "q", torch.bfloat16, 3)
-    _want(table, "table", torch.float32, 3)
+    _want_q(q)
+    _want_table(table)
     C, Hq, _ = q.shape
-    if out is None:
-        out = torch.empty(C, Hq, DV, dtype=torch.bfloat16, device=q.device)
-    _want(out, "out", torch.bfloat16, 3)
+    out = _out(out, C, Hq, q)
+    _same_device(q, table, out, *pool.tensors())
     c = pool.c()
     _check(lib().full_attn_prefill_chunk(_ptr(q), int(P0), C, int(seq), Hq, ctypes.byref(c), _ptr(table),
                                          table.shape[0], float(softmax_scale), _ptr(out), _stream(stream)))
@@ -364,7 +419,7 @@ def swa_sink_prefill_varlen_workspace_size(n) -> int:
 
 
 def _varlen_args(q, cu_rows, P0, seq):
-    _want(q, "q", torch.bfloat16, 3)
+    _want_q(q)
     _want(cu_rows, "cu_rows", torch.int32, 1)
     _want(P0, "P0", torch.int64, 1)
     _want(seq, "seq", torch.int32, 1)
@@ -380,15 +435,14 @@ def full_attn_prefill_varlen(q, cu_rows, P0, seq, pool, table, softmax_scale, ma
     cu_rows[s]..cu_rows[s+1]-1 at positions P0[s].. of sequence seq[s]
     (device int32 / int64 / int32 tensors)."""
     n = _varlen_args(q, cu_rows, P0, seq)
-    _want(table, "table", torch.float32, 3)
+    _want_table(table)
     T, Hq, _ = q.shape
     if workspace is None:
         nb = full_attn_prefill_varlen_workspace_size(n, T, Hq, pool.num_kv_heads, max_ctx)
         workspace = torch.empty(max(nb, 1), dtype=torch.uint8, device=q.device)
     _want(workspace, "workspace", torch.uint8, 1)
-    if out is None:
-        out = torch.empty(T, Hq, DV, dtype=torch.bfloat16, device=q.device)
-    _want(out, "out", torch.bfloat16, 3)
+    out = _out(out, T, Hq, q)
+    _same_device(q, cu_rows, P0, seq, table, workspace, out, *pool.tensors())
     c = pool.c()
     _check(lib().full_attn_prefill_varlen(_ptr(q), _ptr(cu_rows), _ptr(P0), _ptr(seq), n, T, Hq, ctypes.byref(c),
                                           _ptr(table), table.shape[0], float(softmax_scale), int(max_ctx),
@@ -402,15 +456,15 @@ def swa_sink_prefill_varlen(q, cu_rows, P0, seq, chunk_kv, ring, sinks, table, s
     batch's own rows in chunk_kv (row cu_rows[s] + i for chunk s)."""
     n = _varlen_args(q, cu_rows, P0, seq)
     _want(sinks, "sinks", torch.float32, 1)
-    _want(table, "table", torch.float32, 3)
+    _want_table(table)
     T, Hq, _ = q.shape
+    _want_len(sinks, "sinks", Hq)
     if workspace is None:
         nb = swa_sink_prefill_varlen_workspace_size(n)
         workspace = torch.empty(max(nb, 1), dtype=torch.uint8, device=q.device)
     _want(workspace, "workspace", torch.uint8, 1)
-    if out is None:
-        out = torch.empty(T, Hq, DV, dtype=torch.bfloat16, device=q.device)
-    _want(out, "out", torch.bfloat16, 3)
+    out = _out(out, T, Hq, q)
+    _same_device(q, cu_rows, P0, seq, sinks, table, workspace, out, *chunk_kv.tensors(), *ring.tensors())
     cc, rc = chunk_kv.c(), ring.c()
     _check(lib().swa_sink_prefill_varlen(_ptr(q), _ptr(cu_rows), _ptr(P0), _ptr(seq), n, T, Hq, ctypes.byref(cc),
                                          ctypes.byref(rc), _ptr(sinks), _ptr(table), table.shape[0],
@@ -435,6 +489,7 @@ def _ring_copy(fn, ring, seqs, snap, stream):
     _want(t, "tags_snap", torch.int32, 2)
     if k.shape[0] < n or v.shape[0] < n or t.shape[0] < n or k.shape[1] != ring.num_kv_heads:
         raise ValueError("snapshot buffers too small for the ring / sequence list")
+    _same_device(seqs, k, v, t, *ring.tensors())
     c = ring.c()
     _check(fn(ctypes.byref(c), _ptr(seqs), n, _ptr(k), _ptr(v), _ptr(t), _stream(stream)))
 
@@ -470,6 +525,7 @@ def kv_pages_release_window(block_table, num_blocks, block_size, seqs, next_pos,
     n = seqs.shape[0]
     if next_pos.shape[0] != n or free_count.shape[0] != 1:
         raise ValueError("seqs/next_pos/free_count shapes disagree")
+    _same_device(block_table, seqs, next_pos, free_ids, free_count, lo)
     _check(lib().kv_pages_release_window(_ptr(block_table), S, mb, int(block_size), int(num_blocks), _ptr(seqs),
                                          _ptr(next_pos), _ptr(lo), n, int(window), _ptr(free_ids),
                                          _ptr(free_count), free_ids.shape[0], _stream(stream)))
@@ -484,6 +540,7 @@ def kv_ring_gather_pages(pages, ring, src_seqs, dst_seqs, end, stream=None):
     n = src_seqs.shape[0]
     if dst_seqs.shape[0] != n or end.shape[0] != n:
         raise ValueError("src_seqs/dst_seqs/end shapes disagree")
+    _same_device(src_seqs, dst_seqs, end, *pages.tensors(), *ring.tensors())
     pc, rc = pages.c(), ring.c()
     _check(lib().kv_ring_gather_pages(ctypes.byref(pc), ctypes.byref(rc), _ptr(src_seqs), _ptr(dst_seqs), _ptr(end),
                                       n, _stream(stream)))
