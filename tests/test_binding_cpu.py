@@ -138,3 +138,27 @@ def test_other_calls_refuse_mismatched_sizes(rec):
         with pytest.raises(ValueError):
             case()
         assert [n for n, _ in rec.calls if not n.endswith("workspace_size")] == [], i
+
+
+def test_pool_calls_check_devices_and_reach_the_library(rec):
+    ring, pool, _ = _layouts()
+    seqs, end = _i32(2), _i64(2)
+    snap = kvr.ring_snapshot_alloc(2, HKV, device="cpu")
+    kvr.kv_ring_snapshot(ring, seqs, snap)
+    kvr.kv_ring_restore(ring, seqs, snap)
+    kvr.kv_ring_gather_pages(pool, ring, seqs, seqs, end)
+    kvr.kv_pages_release_window(pool.block_table, pool.num_blocks, 64, seqs, end, _i32(16), _i32(1))
+    assert [n for n, _ in rec.calls] == ["kv_ring_snapshot", "kv_ring_restore", "kv_ring_gather_pages",
+                                         "kv_pages_release_window"]
+    rec.calls.clear()
+    meta = lambda t: torch.empty(t.shape, dtype=t.dtype, device="meta")
+    cases = [
+        lambda: kvr.kv_ring_snapshot(ring, seqs, (snap[0], meta(snap[1]), snap[2])),
+        lambda: kvr.kv_ring_gather_pages(pool, ring, seqs, seqs, meta(end)),
+        lambda: kvr.kv_pages_release_window(pool.block_table, pool.num_blocks, 64, seqs, end, _i32(16), _i32(1),
+                                            lo=meta(_i32(4))),
+    ]
+    for i, case in enumerate(cases):
+        with pytest.raises(ValueError):
+            case()
+        assert rec.calls == [], i
