@@ -83,6 +83,7 @@ enum {
  *        k [num_seqs][Hkv][128][192], v [num_seqs][Hkv][128][128],
  *        slot_pos [num_seqs][128] int32, -1 = empty.  slot_pos is shared by
  *        the KV heads of a sequence and is written by kv_ring_append_rope.
+ *        k, v and slot_pos must be 16-byte aligned.
  * PAGED  (the Full KV pool of Xiaomi section 2.1, grown on demand; a
  *        windowed layer may be kept this way too, its out-of-window pages
  *        released by kv_pages_release_window):

@@ -90,6 +90,7 @@ kvr_status check_layout(const kvr_kv_layout *L, int want_kind, const char *name)
   switch (L->kind) {
     case KVR_LAYOUT_RING:
       if (!L->slot_pos) return fail(KVR_EINVAL, "%s: ring slot_pos is NULL", name);
+      if (!aligned16(L->slot_pos)) return fail(KVR_EINVAL, "%s: ring slot_pos not 16-byte aligned", name);
       if (L->num_seqs < 1) return fail(KVR_EINVAL, "%s: num_seqs %d", name, L->num_seqs);
       break;
     case KVR_LAYOUT_PAGED:

@@ -18,7 +18,10 @@ bool make_tma_map_2d(CUtensorMap *m, const void *ptr, long long rows, int width,
 // box brings box_rows whole rows (every 64-element part), so a row is read
 // in one pass; in shared memory the box is [row][part][64] with the 128-byte
 // swizzle applied per 128-byte segment (segment index = row * parts + part).
-bool make_tma_map_rows3d(CUtensorMap *m, const void *ptr, long long rows, int width, int box_rows);
+// With one_part a box brings a single 64-element part of box_rows rows
+// ([row][64], segment index = row); the part is the box's y coordinate.
+bool make_tma_map_rows3d(CUtensorMap *m, const void *ptr, long long rows, int width, int box_rows,
+                         bool one_part = false);
 
 // Raise a kernel's dynamic shared-memory limit once per (kernel slot, device);
 // later launches make no attribute call (so they can sit in a stream capture).

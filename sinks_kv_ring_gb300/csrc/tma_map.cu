@@ -39,13 +39,13 @@ bool make_tma_map_2d(CUtensorMap *m, const void *ptr, long long rows, int width,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-bool make_tma_map_rows3d(CUtensorMap *m, const void *ptr, long long rows, int width, int box_rows) {
+bool make_tma_map_rows3d(CUtensorMap *m, const void *ptr, long long rows, int width, int box_rows, bool one_part) {
   EncodeTiledFn fn = encode_fn();
   if (!fn || width % 64) return false;
   const int parts = width / 64;
   cuuint64_t dims[3] = {64, (cuuint64_t)parts, (cuuint64_t)rows};
   cuuint64_t strides[2] = {128, (cuuint64_t)width * 2};
-  cuuint32_t box[3] = {64, (cuuint32_t)parts, (cuuint32_t)box_rows};
+  cuuint32_t box[3] = {64, one_part ? 1u : (cuuint32_t)parts, (cuuint32_t)box_rows};
   cuuint32_t estr[3] = {1, 1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,

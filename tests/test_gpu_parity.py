@@ -11,7 +11,7 @@ import oracle
 import sinks_kv_ring_gb300 as kvr
 from sinks_kv_ring_gb300.synth import Synth
 
-from kvr_cases import SCALE, compare, compare_rows, fill_paged, fill_ring, raw_kv
+from kvr_cases import SCALE, compare, compare_rows, compare_rows_vec, fill_paged, fill_ring, raw_kv
 
 pytestmark = pytest.mark.gpu
 
@@ -139,6 +139,34 @@ def test_swa_decode_ragged_ring_fill(dist, tables):
     compare(out, want, "swa decode")
     compare_rows(out, want, "swa decode")
     assert kvr.device_status() == 0
+
+
+@pytest.mark.parametrize("hq", [64, 128])
+def test_swa_decode_many_units_per_cta(hq, tables):
+    """A batch of 240 sequences puts 12-13 (sequence, KV head) units on every
+    CTA, so the kernel's two consumer groups run many units each and can
+    drift apart: every row against the oracle, and three calls bit-equal."""
+    B, hkv = 240, 8
+    positions = [(b * 977) % 5000 for b in range(B)]  # includes p < 127 (partly filled rings)
+    syn = Synth(2111 + hq, dist="plain", device=DEV)
+    ring = kvr.RingLayout.empty(B, hkv)
+    seqs = list(range(B))
+    fill_ring(ring, syn, seqs, positions, tables[1e4], 0.707)
+    q = syn.q(B, hq, hkv, seq=999)
+    sinks = syn.sinks(hq).to(DEV)
+    pos = torch.tensor(positions, dtype=torch.int64, device=DEV)
+    seq = torch.tensor(seqs, dtype=torch.int32, device=DEV)
+    outs = [kvr.swa_sink_decode(q, pos, seq, ring, sinks, tables[1e4], SCALE) for _ in range(3)]
+    torch.cuda.synchronize()
+    assert kvr.device_status() == 0
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2])
+    want = np.zeros((B, hq, 128))
+    sk = sinks.double().cpu().numpy()
+    for b, p in enumerate(positions):
+        lo = max(0, p - 127)
+        k, v = raw_kv(syn, hkv, b, lo, p + 1)
+        want[b] = oracle.attend_seq(q[b:b + 1], [p], k, v, lo, 1e4, 0.707, SCALE, 128, sk)[0]
+    compare_rows_vec(outs[0], want, f"swa decode B={B} hq={hq}")
 
 
 def test_swa_decode_group_sizes(tables):
