@@ -122,6 +122,21 @@ const char *kvr_last_error(void);
 kvr_status kvr_device_status(uint32_t *flags, int reset);
 
 /*
+ * Test hook for the bounded waits (no counterpart on the pages).  The next
+ * `launches` kernels started by swa_sink_decode over a RING layout or by
+ * full_attn_prefill_chunk, in this process, stall on purpose: once their
+ * loads are in flight (and, for the prefill, with its tensor memory held),
+ * one warp group waits on an internal barrier that nothing completes, with a
+ * time limit of limit_ns nanoseconds.  When the limit passes the kernel takes
+ * the exit a real stall would take -- the other warps see the abort, the
+ * loads and products already issued finish, tensor memory is freed -- and
+ * sets KVR_DEV_TIMEOUT; that call's output is unspecified.  launches = 0
+ * turns the hook off.  KVR_EINVAL unless 0 <= launches and
+ * 1000 <= limit_ns <= 1e9.  For tests of that exit path only.
+ */
+kvr_status kvr_debug_stall_next(int32_t launches, int64_t limit_ns);
+
+/*
  * RoPE cos/sin table, computed on the host in fp64 and stored as fp32
  * (gaudi-cookbook "The RoPE fix for large positions": a table built with
  * fp32 cos/sin goes wrong past about 1.5e5 radians, so it is built on the CPU

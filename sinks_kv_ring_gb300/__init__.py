@@ -82,6 +82,8 @@ def lib():
                 L.kvr_last_error.argtypes = []
                 L.kvr_device_status.restype = ctypes.c_int
                 L.kvr_device_status.argtypes = [p, ctypes.c_int]
+                L.kvr_debug_stall_next.restype = ctypes.c_int
+                L.kvr_debug_stall_next.argtypes = [i32, i64]
                 L.kvr_rope_table_build.restype = ctypes.c_int
                 L.kvr_rope_table_build.argtypes = [f64, i64, p, ctypes.c_int]
                 L.kv_ring_append_rope.restype = ctypes.c_int
@@ -544,6 +546,13 @@ def kv_ring_gather_pages(pages, ring, src_seqs, dst_seqs, end, stream=None):
     pc, rc = pages.c(), ring.c()
     _check(lib().kv_ring_gather_pages(ctypes.byref(pc), ctypes.byref(rc), _ptr(src_seqs), _ptr(dst_seqs), _ptr(end),
                                       n, _stream(stream)))
+
+
+def debug_stall_next(launches: int, limit_ns: int) -> None:
+    """Test hook: the next `launches` windowed decodes (ring layout) or
+    single-chunk full-attention prefills stall on purpose and leave by their
+    bounded-wait exit after limit_ns, setting DEV_TIMEOUT (kvr_debug_stall_next)."""
+    _check(lib().kvr_debug_stall_next(int(launches), int(limit_ns)))
 
 
 def device_status(reset: bool = True) -> int:

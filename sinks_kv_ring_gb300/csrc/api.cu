@@ -1,6 +1,7 @@
 // api.cu -- the C ABI declared in include/kvring.h: host-side validation of
 // every argument the host can see, then the kernel launches.  Nothing here
 // allocates device memory.
+#include <atomic>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -129,6 +130,23 @@ cudaStream_t as_stream(void *s) { return static_cast<cudaStream_t>(s); }
 
 namespace kvr {
 namespace {
+std::atomic<int> g_stall_left{0};
+std::atomic<unsigned long long> g_stall_ns{0};
+}  // namespace
+
+void set_stall(int launches, unsigned long long ns) {
+  g_stall_ns.store(ns);
+  g_stall_left.store(launches);
+}
+
+unsigned long long take_stall() {
+  int left = g_stall_left.load();
+  while (left > 0 && !g_stall_left.compare_exchange_weak(left, left - 1)) {
+  }
+  return left > 0 ? g_stall_ns.load() : 0ull;
+}
+
+namespace {
 constexpr int MAX_KSLOT = 16;
 unsigned char g_smem_done[MAX_DEV][MAX_KSLOT];
 }  // namespace
@@ -174,6 +192,13 @@ kvr_status kvr_device_status(uint32_t *flags, int reset) {
     e = cudaMemcpyToSymbol(g_status_word, &zero, sizeof zero);
     if (e != cudaSuccess) return cuda_fail(e, "kvr_device_status");
   }
+  return ok();
+}
+
+kvr_status kvr_debug_stall_next(int32_t launches, int64_t limit_ns) {
+  if (launches < 0 || limit_ns < 1000 || limit_ns > 1000000000LL)
+    return fail(KVR_EINVAL, "launches %d, limit_ns %lld", launches, (long long)limit_ns);
+  kvr::set_stall(launches, (unsigned long long)limit_ns);
   return ok();
 }
 

@@ -28,6 +28,11 @@ bool make_tma_map_rows3d(CUtensorMap *m, const void *ptr, long long rows, int wi
 // `slot` is a small distinct integer per kernel.
 cudaError_t ensure_smem_limit(int slot, const void *func, int bytes);
 
+// The wait limit of a launch that kvr_debug_stall_next asked to stall (one
+// taken per call), or 0 for a normal launch.
+void set_stall(int launches, unsigned long long ns);
+unsigned long long take_stall();
+
 cudaError_t launch_append(const uint16_t *k, const uint16_t *v, const int64_t *pos, const int32_t *seq,
                           int T, int hkv, const float *table, int64_t max_pos, float value_scale,
                           const KvView &dst, unsigned *status, cudaStream_t st);

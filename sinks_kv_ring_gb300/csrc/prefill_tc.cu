@@ -67,6 +67,7 @@ constexpr int B_TMEM = 176;     // u32: TMEM base address
 constexpr int B_ABORT = 180;    // u32: set when a wait timed out
 constexpr int B_DRAIN = 192;    // all MMAs of the CTA done (before TMEM is freed)
 constexpr int B_QFULL = 200;    // the query tiles' TMA boxes landed
+constexpr int B_STALL = 208;    // test hook: a barrier nothing arrives on
 
 // Every lane waits on the barrier; the warp agrees on the outcome so that it
 // stays converged for the warp-collective (.sync.aligned / elect.sync)
@@ -95,6 +96,7 @@ struct TcArgs {
   int ring_seq;
   int q_tma;  // query tiles come in as TMA boxes (tmq); else 16-byte copies
   int o_tma;  // one chunk: output tiles leave as TMA boxes (tmo); else per-row stores
+  unsigned long long stall_ns;  // test hook: the MMA warp stalls before its first product (0 = never)
 };
 
 // Rows f0 .. f0+255 (those below nrows) of KV head kv's group, written as zeros.
@@ -209,6 +211,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     }
     mbar_init(sBar + B_DRAIN, 1);
     mbar_init(sBar + B_QFULL, 1);
+    mbar_init(sBar + B_STALL, 1);
     *abort_flag = 0;
     fence_mbar_init();
     if (a.q_tma) {
@@ -502,7 +505,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     };
     // With one live query tile, tile 0's products release the ring slots.
     const bool one = nq == 1;
-    issue_S(0, 0, one);
+    if (a.stall_ns && !warp_wait(sBar + B_STALL, 0, abort_flag, a.stall_ns)) ok = false;
+    if (ok) issue_S(0, 0, one);
     if (ok && !one) issue_S(1, 0, true);
     for (int t = 1; t < ntiles && ok; ++t) {
       issue_PV(0, t - 1, one);
@@ -770,6 +774,7 @@ cudaError_t tc_setup(const KvView &pool, int hq, const float *table, float softm
   a->total_rows = rows;
   a->table = table;
   a->scale_log2 = softmax_scale * LOG2E;
+  a->stall_ns = 0;
   a->out = out;
   a->status = status;
   return cudaSuccess;
@@ -791,6 +796,7 @@ cudaError_t launch_full_prefill(const uint16_t *q, int64_t P0, int C, int seq, i
   a.P0 = P0;
   a.C = C;
   a.bt = pool.block_table + (long long)seq * pool.max_blocks;
+  a.stall_ns = take_stall();
   CUtensorMap mq, mo;
   a.q_tma = make_tma_map_heads3d(&mq, q, C, hq, DQK, a.G) ? 1 : 0;
   a.o_tma = make_tma_map_heads3d(&mo, out, C, hq, DV, a.G) ? 1 : 0;

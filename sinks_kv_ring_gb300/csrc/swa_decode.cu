@@ -77,7 +77,7 @@ struct SdLayout {
   static constexpr int OFF_ROW = OFF_INFO + NG * 8;     // [SD_MAX_UNITS] (ring row, position)
   static constexpr int OFF_GO = OFF_ROW + SD_MAX_UNITS * 8;  // [NG] int: producer gi has queued its first K parts
   static constexpr int OFF_BAR = OFF_GO + 64;
-  static constexpr int NBAR = NG * (2 * R + 2);         // per group: chunk full/empty, entry full/empty
+  static constexpr int NBAR = NG * (2 * R + 2) + 1;     // per group: chunk full/empty, entry full/empty; stall
   static constexpr int SMEM = OFF_BAR + NBAR * 8 + 8 + 1024;
   static_assert(OFF_M % 1024 == 0 && META % 1024 == 0, "swizzled tiles need 1024-byte alignment");
   static_assert(GRP % 16 == 0 && OFF_BAR % 8 == 0, "alignment");
@@ -96,6 +96,7 @@ struct SdArgs {
   int B, hq, G, hkv, num_seqs;
   long long max_pos;
   float scale_log2;
+  unsigned long long stall_ns;  // test hook: group 0 stalls on its first unit (0 = never)
 };
 
 // Ring row of unit u (its first K/V row) and its position.  Row -1: the
@@ -164,6 +165,7 @@ __global__ void __launch_bounds__(SdLayout<NT>::THREADS, 1)
   auto cEmpty = [&](int pl) { return bar0 + 8u * (NG * R + pl); };
   auto mFull = [&](int gi) { return bar0 + 8u * (2 * NG * R + gi); };
   auto mEmpty = [&](int gi) { return bar0 + 8u * (2 * NG * R + NG + gi); };
+  const uint32_t stallBar = bar0 + 8u * (2 * NG * R + 2 * NG);  // nothing arrives on it
   volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(g + L::OFF_BAR + 8 * L::NBAR);
   int2 *sRow = reinterpret_cast<int2 *>(g + L::OFF_ROW);
   int2 *sInfo = reinterpret_cast<int2 *>(g + L::OFF_INFO);
@@ -179,6 +181,7 @@ __global__ void __launch_bounds__(SdLayout<NT>::THREADS, 1)
       mbar_init(mFull(gi), 1);
       mbar_init(mEmpty(gi), SD_GWARPS);
     }
+    mbar_init(stallBar, 1);
     *abort_flag = 0;
     for (int gi = 0; gi < NG; ++gi) sGo[gi] = 0;
     fence_mbar_init();
@@ -316,7 +319,11 @@ __global__ void __launch_bounds__(SdLayout<NT>::THREADS, 1)
         snk[nt][i] = h < G ? __ldg(a.sinks + kv * G + h) * LOG2E : NEG_INF;
       }
 
-    bool ok = mbar_wait(mFull(grp), (uint32_t)m & 1u, abort_flag);
+    // A warp hands a chunk or entry back only when every lane saw it land:
+    // after an abort, a place whose load may still be landing is kept.
+    const bool got_m = __all_sync(0xffffffffu, mbar_wait(mFull(grp), (uint32_t)m & 1u, abort_flag));
+    bool ok = got_m;
+    if (a.stall_ns && grp == 0 && m == 0) ok = mbar_wait(stallBar, 0, abort_flag, a.stall_ns) && ok;
     const int2 info = sInfo[grp];
     const int p = info.x;
     const bool valid = ok && info.y >= 0;
@@ -359,7 +366,8 @@ __global__ void __launch_bounds__(SdLayout<NT>::THREADS, 1)
 #pragma unroll
       for (int j = 0; j < SD_KPARTS; ++j) {
         const int cg = c0 + j, pl = place(cg);
-        ok = mbar_wait(cFull(pl), (uint32_t)(cg / R) & 1u, abort_flag) && ok;
+        const bool got = __all_sync(0xffffffffu, mbar_wait(cFull(pl), (uint32_t)(cg / R) & 1u, abort_flag));
+        ok = got && ok;
         const uint32_t kb = base + L::OFF_C + pl * SD_CHUNK;
 #pragma unroll
         for (int kl = 0; kl < 4; ++kl) {
@@ -374,16 +382,16 @@ __global__ void __launch_bounds__(SdLayout<NT>::THREADS, 1)
           }
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(cEmpty(pl));
+        if (lane == 0 && got) mbar_arrive(cEmpty(pl));
       }
     } else {
       // nothing to compute: hand the K parts back as they come
 #pragma unroll
       for (int j = 0; j < SD_KPARTS; ++j) {
         const int cg = c0 + j, pl = place(cg);
-        ok = mbar_wait(cFull(pl), (uint32_t)(cg / R) & 1u, abort_flag) && ok;
-        __syncwarp();
-        if (lane == 0) mbar_arrive(cEmpty(pl));
+        const bool got = __all_sync(0xffffffffu, mbar_wait(cFull(pl), (uint32_t)(cg / R) & 1u, abort_flag));
+        ok = got && ok;
+        if (lane == 0 && got) mbar_arrive(cEmpty(pl));
       }
     }
     if (valid) {
@@ -405,7 +413,7 @@ __global__ void __launch_bounds__(SdLayout<NT>::THREADS, 1)
     }
     // This warp is done with the entry (q rows, tags, table row).
     __syncwarp();
-    if (lane == 0) mbar_arrive(mEmpty(grp));
+    if (lane == 0 && got_m) mbar_arrive(mEmpty(grp));
     if (valid) {
       // per-head maxima over this warp's 32 slots
 #pragma unroll
@@ -466,7 +474,8 @@ __global__ void __launch_bounds__(SdLayout<NT>::THREADS, 1)
     // This warp reads value dims 32wg..32wg+31: V part wg/2.
     const int vp = wg >> 1;
     const int cv = c0 + SD_KPARTS + vp, sv = place(cv);
-    ok = mbar_wait(cFull(sv), (uint32_t)(cv / R) & 1u, abort_flag) && ok;
+    const bool got_v = __all_sync(0xffffffffu, mbar_wait(cFull(sv), (uint32_t)(cv / R) & 1u, abort_flag));
+    ok = got_v && ok;
     uint8_t *sV = g + L::OFF_C + sv * SD_CHUNK;
     if (valid && ok) {
       // V rows of stale slots are zeroed so that their bytes cannot reach the
@@ -527,7 +536,7 @@ __global__ void __launch_bounds__(SdLayout<NT>::THREADS, 1)
       // The part's two readers hand it back (two arrivals each: a ring
       // place takes four whatever it holds).
       __syncwarp();
-      if (lane == 0) mbar_arrive_cnt(cEmpty(sv), SD_GWARPS / SD_VPARTS);
+      if (lane == 0 && got_v) mbar_arrive_cnt(cEmpty(sv), SD_GWARPS / SD_VPARTS);
       // Normalise by the denominator (sink once + all slots), transpose each
       // 8x8 block back to [head][value dim] and store.
 #pragma unroll
@@ -554,7 +563,7 @@ __global__ void __launch_bounds__(SdLayout<NT>::THREADS, 1)
       }
     } else {
       __syncwarp();
-      if (lane == 0) mbar_arrive_cnt(cEmpty(sv), SD_GWARPS / SD_VPARTS);
+      if (lane == 0 && got_v) mbar_arrive_cnt(cEmpty(sv), SD_GWARPS / SD_VPARTS);
       for (int i = gtid; i < G * DV / 8; i += SD_GWARPS * 32)
         reinterpret_cast<uint4 *>(orow)[i] = make_uint4(0, 0, 0, 0);
       if (gtid == 0 && ok) flag(a.status, info.y == -1 ? ST_BAD_POS : ST_BAD_SEQ);
@@ -606,6 +615,7 @@ cudaError_t launch_swa_decode(const uint16_t *q, const int64_t *pos, const int32
   a.num_seqs = ring.num_seqs;
   a.max_pos = max_pos;
   a.scale_log2 = softmax_scale * LOG2E;
+  a.stall_ns = take_stall();
   const int units = B * hkv;
   return G <= 8 ? launch_nt<1>(mk, mv, mq, a, units, st) : launch_nt<2>(mk, mv, mq, a, units, st);
 }

@@ -137,6 +137,13 @@ def test_varlen_host_validation_codes(L):
                                      None, 0, P, None) == 0
 
 
+def test_stall_hook_host_validation(L):
+    assert L.kvr_debug_stall_next(-1, 100000) == -1
+    assert L.kvr_debug_stall_next(1, 999) == -1
+    assert L.kvr_debug_stall_next(1, 2_000_000_000) == -1
+    assert L.kvr_debug_stall_next(0, 1000) == 0
+
+
 def test_workspace_size_grows_with_context(L):
     a = L.full_attn_decode_workspace_size(64, 64, 4, 32769)
     b = L.full_attn_decode_workspace_size(64, 64, 4, 2 * 32769)

@@ -1,0 +1,100 @@
+"""The bounded-wait exit of the pipelined kernels, made to run on purpose.
+
+Every wait of the windowed decode and of the tensor-core prefill kernel has a
+time limit; when one runs out the kernel sets an abort flag, its other warps
+leave their loops, the loads and products already issued finish, tensor
+memory is freed and the kernel returns with KVR_DEV_TIMEOUT set.  The test
+hook kvr_debug_stall_next makes one launch wait on a barrier that nothing
+completes, with a short limit, once its loads are in flight: the call must
+return promptly, report the timeout, and leave the device usable -- the next
+normal call on it matches the oracle.  No fault, trap or endless wait is
+involved: the stalled wait ends by its own limit.
+"""
+import math
+import time
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import sinks_kv_ring_gb300 as kvr
+from sinks_kv_ring_gb300.synth import Synth
+
+from kvr_cases import SCALE, compare_rows, fill_paged, fill_ring, raw_kv
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+LIMIT_NS = 200_000  # the stalled wait's limit: 0.2 ms
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from sinks_kv_ring_gb300 import build
+    build.build()
+    kvr.device_status(reset=True)
+    yield
+    kvr.debug_stall_next(0, 1000)
+
+
+def _stalled(call):
+    """Run call() with the next launch stalled; returns the seconds it took."""
+    kvr.device_status(reset=True)
+    kvr.debug_stall_next(1, LIMIT_NS)
+    try:
+        t0 = time.perf_counter()
+        call()
+        torch.cuda.synchronize()
+        return time.perf_counter() - t0
+    finally:
+        kvr.debug_stall_next(0, 1000)
+
+
+def test_windowed_decode_stall_takes_the_bounded_exit():
+    B, hq, hkv = 40, 64, 8
+    positions = [300 + 7 * b for b in range(B)]
+    t4 = kvr.rope_table(1e4, 4096)
+    syn = Synth(2601, dist="plain", device=DEV)
+    ring = kvr.RingLayout.empty(B, hkv)
+    fill_ring(ring, syn, list(range(B)), positions, t4, 0.707)
+    q = syn.q(B, hq, hkv, seq=999)
+    sinks = syn.sinks(hq).to(DEV)
+    pos = torch.tensor(positions, dtype=torch.int64, device=DEV)
+    seq = torch.arange(B, dtype=torch.int32, device=DEV)
+    out = torch.empty(B, hq, 128, dtype=torch.bfloat16, device=DEV)
+    dt = _stalled(lambda: kvr.swa_sink_decode(q, pos, seq, ring, sinks, t4, SCALE, out=out))
+    assert kvr.device_status() & kvr.DEV_TIMEOUT
+    assert dt < 5.0, f"the stalled call took {dt:.2f} s"
+    # the device is still usable: the same call, not stalled
+    out = kvr.swa_sink_decode(q, pos, seq, ring, sinks, t4, SCALE)
+    torch.cuda.synchronize()
+    assert kvr.device_status() == 0
+    want = np.zeros((B, hq, 128))
+    sk = sinks.double().cpu().numpy()
+    for b, p in enumerate(positions):
+        k, v = raw_kv(syn, hkv, b, p - 127, p + 1)
+        want[b] = oracle.attend_seq(q[b:b + 1], [p], k, v, p - 127, 1e4, 0.707, SCALE, 128, sk)[0]
+    compare_rows(out, want, "windowed decode after a stalled launch")
+
+
+def test_prefill_stall_takes_the_bounded_exit():
+    # The tensor-core kernel stalls in its MMA warp with TMEM allocated and
+    # its first K/V loads issued; 20 CTAs (10 tiles of 256 rows x 2 KV heads).
+    hq, hkv, P0, C = 16, 2, 700, 300
+    t7 = kvr.rope_table(1e7, 2048)
+    syn = Synth(2602, dist="plain", device=DEV)
+    pool = kvr.PagedLayout.contiguous(1, hkv, 2048, block_size=64)
+    fill_paged(pool, syn, [0], [P0 + C], t7, 0.707)
+    q = syn.q(C, hq, hkv, seq=5, start=P0)
+    out = torch.empty(C, hq, 128, dtype=torch.bfloat16, device=DEV)
+    dt = _stalled(lambda: kvr.full_attn_prefill_chunk(q, P0, 0, pool, t7, SCALE, out=out))
+    assert kvr.device_status() & kvr.DEV_TIMEOUT
+    assert dt < 5.0, f"the stalled call took {dt:.2f} s"
+    out = kvr.full_attn_prefill_chunk(q, P0, 0, pool, t7, SCALE)
+    torch.cuda.synchronize()
+    assert kvr.device_status() == 0
+    k, v = raw_kv(syn, hkv, 0, 0, P0 + C)
+    want = oracle.attend_seq(q, np.arange(P0, P0 + C), k, v, 0, 1e7, 0.707, SCALE, 0, None)
+    compare_rows(out, want, "prefill after a stalled launch")

@@ -209,6 +209,103 @@ def test_pro_shaped_contexts_decode_sampled(kvr, hq, hkv_full):
     torch.cuda.empty_cache()
 
 
+def test_pro_stack_captured_graph_sampled(kvr):
+    # The Pro-shaped decode step as the bench runs it: a layer stack (layer i
+    # full iff i % 7 == 6) captured as one CUDA graph, each layer a KV write
+    # then its attention, on the seed-1004 batch (128 sequences, contexts
+    # log-uniform over [1K, 1M]).  14 layers: 12 windowed (a ring each) and 2
+    # full that share one paged pool, as the bench's full layers share pools;
+    # every layer has its own q, sinks, new-token K/V and output.  Two
+    # replays are bit-equal, and every layer's shortest, median and longest
+    # sequences match the oracle (all heads).
+    from sinks_kv_ring_gb300.synth import Synth, ragged_contexts
+    import bench
+    B, hq, vs_, bsz, layers = 128, 64, 0.612, 64, 14
+    kinds = ["full" if i % 7 == 6 else "swa" for i in range(layers)]
+    ctx = ragged_contexts(B, 1024, 1 << 20, 1004)
+    max_ctx = max(ctx) + 1
+    t4, t7 = kvr.rope_table(1e4, max_ctx), kvr.rope_table(1e7, max_ctx)
+    mb = [(c + 1 + bsz - 1) // bsz for c in ctx]
+    bt = torch.zeros(B, max(mb), dtype=torch.int32)
+    off = 0
+    for b, m in enumerate(mb):
+        bt[b, :m] = torch.arange(off, off + m, dtype=torch.int32)
+        off += m
+    pool = kvr.PagedLayout(torch.empty(off, 4, bsz, 192, dtype=torch.bfloat16, device="cuda"),
+                           torch.empty(off, 4, bsz, 128, dtype=torch.bfloat16, device="cuda"), bt.cuda())
+    syn_pool = Synth(1004, layer=100, device="cuda")
+    bench._fill_pool(kvr, pool, syn_pool, range(B), ctx, t7, vs_)
+    pos = torch.tensor(ctx, dtype=torch.int64, device="cuda")
+    seq = torch.arange(B, dtype=torch.int32, device="cuda")
+    L = []
+    for i, kind in enumerate(kinds):
+        syn = Synth(1004, layer=i, device="cuda")
+        hkv = 4 if kind == "full" else 8
+        d = {"kind": kind, "syn": syn, "hkv": hkv, "q": syn.q(B, hq, hkv, seq=50_000),
+             "kn": syn.k(B, hkv, seq=60_000), "vn": syn.v(B, hkv, seq=60_000),
+             "out": torch.empty(B, hq, 128, dtype=torch.bfloat16, device="cuda")}
+        if kind == "swa":
+            d["sinks"] = syn.sinks(hq).cuda()
+            ring = kvr.RingLayout.empty(B, 8)
+            for b, c in enumerate(ctx):
+                lo = c - 127
+                kvr.kv_ring_append_rope(syn.k(127, 8, seq=b, start=lo), syn.v(127, 8, seq=b, start=lo),
+                                        torch.arange(lo, c, device="cuda"),
+                                        torch.full((127,), b, dtype=torch.int32, device="cuda"), t4, vs_, ring)
+            d["ring"] = ring
+        L.append(d)
+    ws = torch.empty(kvr.full_attn_decode_workspace_size(B, hq, 4, max_ctx), dtype=torch.uint8, device="cuda")
+
+    def step(st):
+        for d in L:
+            if d["kind"] == "full":
+                kvr.kv_ring_append_rope(d["kn"], d["vn"], pos, seq, t7, vs_, pool, stream=st)
+                kvr.full_attn_decode(d["q"], pos, seq, pool, t7, SCALE, max_ctx, workspace=ws, out=d["out"],
+                                     stream=st)
+            else:
+                kvr.kv_ring_append_rope(d["kn"], d["vn"], pos, seq, t4, vs_, d["ring"], stream=st)
+                kvr.swa_sink_decode(d["q"], pos, seq, d["ring"], d["sinks"], t4, SCALE, out=d["out"], stream=st)
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        step(side)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    for d in L:
+        d["out"].fill_(7.0)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step(torch.cuda.current_stream())
+    g.replay()
+    torch.cuda.synchronize()
+    first = [d["out"].clone() for d in L]
+    g.replay()
+    torch.cuda.synchronize()
+    assert kvr.device_status() == 0
+    for i, d in enumerate(L):
+        assert torch.equal(first[i], d["out"]), f"layer {i}: replays differ"
+    order = np.argsort(ctx)
+    sample = (int(order[0]), int(order[B // 2]), int(order[-1]))
+    raw_pool = {b: _pool_raw(syn_pool, 4, b, ctx[b]) for b in sample}
+    for i, d in enumerate(L):
+        for b in sample:
+            p = ctx[b]
+            if d["kind"] == "full":
+                kf, vf = raw_pool[b]
+                kf, vf = torch.cat([kf, d["kn"][b:b + 1]]), torch.cat([vf, d["vn"][b:b + 1]])
+                want = oracle.attend_seq(d["q"][b:b + 1], [p], kf, vf, 0, 1e7, vs_, SCALE, 0, None)
+            else:
+                lo = p - 127
+                ks = torch.cat([d["syn"].k(127, 8, seq=b, start=lo), d["kn"][b:b + 1]])
+                vv = torch.cat([d["syn"].v(127, 8, seq=b, start=lo), d["vn"][b:b + 1]])
+                want = oracle.attend_seq(d["q"][b:b + 1], [p], ks, vv, lo, 1e4, vs_, SCALE, 128,
+                                         d["sinks"].double().cpu().numpy())
+            compare_rows(d["out"][b:b + 1], want, f"stack layer {i} ({d['kind']}) b={b} ctx={p}")
+    del g, pool, L
+    torch.cuda.empty_cache()
+
+
 def test_zero_length_calls_are_no_ops(kvr):
     import sinks_kv_ring_gb300 as k
     t = k.rope_table(1e7, 64)
