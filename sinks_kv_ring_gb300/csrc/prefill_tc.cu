@@ -165,9 +165,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     if (!WINDOW) bt += (long long)rseq * a.max_blocks;
     prow = a.plan.prow_prefix[s];
   } else {
-    kv = blockIdx.x % a.hkv;
-    f0 = (long long)(blockIdx.x / a.hkv) * 256;
+    // KV-head-major: the CTAs that run together read the same KV head's
+    // K/V (at 122880 cached tokens one head's is 79 MB, all four together
+    // more than L2), so it comes from DRAM about once.
     nrows = (long long)a.C * a.G;
+    const int tiles = (int)((nrows + 255) / 256);
+    kv = blockIdx.x / tiles;
+    f0 = (long long)(blockIdx.x % tiles) * 256;
     P0 = a.P0;
   }
   const long long i_last = min(nrows - 1, f0 + 255) / a.G;
