@@ -111,6 +111,13 @@ typedef struct kvr_kv_layout {
   int64_t num_rows;            /* LINEAR */
 } kvr_kv_layout;
 
+/*
+ * Every call that launches work looks up, on its first use on a device (and
+ * again after cudaDeviceReset), the device address of the library's status
+ * word; that first call must not run while its stream is being captured
+ * into a CUDA graph: it then returns KVR_EINVAL and launches nothing.
+ */
+
 /* Message for the last failing call on this thread ("" if none). */
 const char *kvr_last_error(void);
 
@@ -297,8 +304,9 @@ kvr_status kv_ring_gather_pages(const kvr_kv_layout *pages, const kvr_kv_layout 
 
 /*
  * Size of the fixed device scratch array used by full_attn_decode_noalloc:
- * 32 MiB, held on every device that loads this library until the process
- * exits.
+ * 32 MiB.  It is part of the library's device image, so a device holds it
+ * from the first call of any kind into this library on that device (not only
+ * the first no-allocation call) until the process exits.
  */
 #define KVR_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
 
@@ -326,7 +334,11 @@ kvr_status kv_ring_gather_pages(const kvr_kv_layout *pages, const kvr_kv_layout 
  *
  * The first call on each device looks up the array's device address with
  * cudaGetSymbolAddress (with that device current); make that first call
- * before any stream capture begins.
+ * before any stream capture begins.  A first call made while its stream is
+ * being captured returns KVR_EINVAL (with a message saying so) and launches
+ * nothing.  The looked-up address belongs to the device's current context:
+ * after cudaDeviceReset it is looked up again on the next call (which again
+ * must not be inside a capture).
  */
 kvr_status full_attn_decode_noalloc(const kvr_bf16 *q, const int64_t *pos, const int32_t *seq, int32_t B,
                                     int32_t Hq, const kvr_kv_layout *pool, const float *rope_cos_sin,

@@ -2,6 +2,7 @@
 // every argument the host can see, then the kernel launches.  Nothing here
 // allocates device memory.
 #include <atomic>
+#include <cuda.h>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -43,25 +44,101 @@ __device__ unsigned int g_status_word;
 
 constexpr int MAX_DEV = 64;
 std::mutex g_mu;
-unsigned *g_status_ptr[MAX_DEV];
 int g_sms[MAX_DEV];
 
-// Device address of the status word on the current device (host code may
-// not use the symbol itself as an address).
-cudaError_t status_ptr(unsigned **out) {
+// The calling thread's current CUDA context (the driver's cuCtxGetCurrent,
+// looked up once through the runtime, so the library does not link the
+// driver library).  Device addresses of this library's symbols belong to the
+// context they were looked up in: after cudaDeviceReset, or with another
+// context current, they are looked up again.
+void *current_ctx() {
+  typedef CUresult (*Fn)(CUcontext *);
+  static Fn fn = [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      p = nullptr;
+    return reinterpret_cast<Fn>(p);
+  }();
+  CUcontext c = nullptr;
+  if (fn) fn(&c);
+  return c;
+}
+
+// Per device: the context its cached addresses belong to, the status word's
+// address and the no-allocation scratch array's address (null: not looked up).
+struct DevSyms {
+  void *ctx;
+  void *status;
+  void *scratch;
+};
+DevSyms g_syms[MAX_DEV];
+
+// A lookup that would have run while the caller's stream is captured.
+constexpr cudaError_t ERR_CAPTURE = cudaErrorStreamCaptureUnsupported;
+
+// Under g_mu: the entry of the current device, emptied when the context
+// current now is not the one its addresses were looked up in.
+cudaError_t cur_syms(DevSyms **out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= MAX_DEV) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> lk(g_mu);
-  if (!g_status_ptr[dev]) {
-    void *p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_status_word);
-    if (e != cudaSuccess) return e;
-    g_status_ptr[dev] = static_cast<unsigned *>(p);
-  }
-  *out = g_status_ptr[dev];
+  DevSyms &d = g_syms[dev];
+  const void *ctx = current_ctx();
+  if (d.ctx != ctx) d = DevSyms{nullptr, nullptr, nullptr};
+  *out = &d;
   return cudaSuccess;
+}
+
+// Whether work issued to `stream` is being captured into a graph (for the
+// legacy default stream: whether any global capture is under way).
+bool capturing(void *stream) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(static_cast<cudaStream_t>(stream), &cs) != cudaSuccess) {
+    (void)cudaGetLastError();  // the query's own error must not reach the launch check
+    return true;
+  }
+  return cs != cudaStreamCaptureStatusNone;
+}
+
+// Device address of `sym` for the current device and context, cached in
+// `slot`; the lookup (cudaGetSymbolAddress) never runs inside a capture.
+template <class T>
+cudaError_t symbol_addr(void *DevSyms::*slot, const T &sym, void *stream, void **out) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  DevSyms *d = nullptr;
+  cudaError_t e = cur_syms(&d);
+  if (e != cudaSuccess) return e;
+  if (!(d->*slot)) {
+    if (capturing(stream)) return ERR_CAPTURE;
+    void *p = nullptr;
+    e = cudaGetSymbolAddress(&p, sym);
+    if (e != cudaSuccess) return e;
+    d->ctx = current_ctx();  // the lookup may have made the primary context current
+    d->*slot = p;
+  }
+  *out = d->*slot;
+  return cudaSuccess;
+}
+
+// Device address of the status word on the current device (host code may
+// not use the symbol itself as an address).
+cudaError_t status_ptr(unsigned **out, void *stream) {
+  void *p = nullptr;
+  const cudaError_t e = symbol_addr(&DevSyms::status, g_status_word, stream, &p);
+  *out = static_cast<unsigned *>(p);
+  return e;
+}
+
+kvr_status state_fail(cudaError_t e, const char *what) {
+  if (e == ERR_CAPTURE)
+    return fail(KVR_EINVAL,
+                "%s: the first call on a device (and the first after a device reset) looks up the library's device "
+                "symbols, which cannot happen while its stream is being captured; make one call before capturing",
+                what);
+  return cuda_fail(e, what);
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -149,6 +226,7 @@ unsigned long long take_stall() {
 namespace {
 constexpr int MAX_KSLOT = 16;
 unsigned char g_smem_done[MAX_DEV][MAX_KSLOT];
+void *g_smem_ctx[MAX_DEV];  // the context g_smem_done[dev] is for
 }  // namespace
 
 cudaError_t ensure_smem_limit(int slot, const void *func, int bytes) {
@@ -156,8 +234,13 @@ cudaError_t ensure_smem_limit(int slot, const void *func, int bytes) {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= MAX_DEV || slot < 0 || slot >= MAX_KSLOT) return cudaErrorInvalidValue;
-  if (g_smem_done[dev][slot]) return cudaSuccess;
   std::lock_guard<std::mutex> lk(g_mu);
+  void *ctx = current_ctx();
+  if (g_smem_ctx[dev] != ctx) {  // a new context: its kernels' attributes start from the defaults
+    for (int i = 0; i < MAX_KSLOT; ++i) g_smem_done[dev][i] = 0;
+    g_smem_ctx[dev] = ctx;
+  }
+  if (g_smem_done[dev][slot]) return cudaSuccess;
   e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   if (e == cudaSuccess) g_smem_done[dev][slot] = 1;
   return e;
@@ -225,8 +308,8 @@ kvr_status kv_ring_append_rope(const kvr_bf16 *k, const kvr_bf16 *v, const int64
   if (dst->kind == KVR_LAYOUT_LINEAR && dst->num_rows < T)
     return fail(KVR_EINVAL, "LINEAR dst has %lld rows, T = %d", (long long)dst->num_rows, T);
   unsigned *st = nullptr;
-  cudaError_t e = status_ptr(&st);
-  if (e != cudaSuccess) return cuda_fail(e, "kv_ring_append_rope");
+  cudaError_t e = status_ptr(&st, stream);
+  if (e != cudaSuccess) return state_fail(e, "kv_ring_append_rope");
   e = kvr::launch_append(k, v, pos, seq, T, Hkv, rope_cos_sin, max_pos, value_scale, view(*dst), st,
                          as_stream(stream));
   if (e != cudaSuccess) return cuda_fail(e, "kv_ring_append_rope launch");
@@ -248,8 +331,8 @@ kvr_status swa_sink_decode(const kvr_bf16 *q, const int64_t *pos, const int32_t 
   if (!q || !pos || !seq || !sinks || !out) return fail(KVR_EINVAL, "q/pos/seq/sinks/out is NULL");
   if (!aligned16(q) || !aligned16(out)) return fail(KVR_EINVAL, "q/out not 16-byte aligned");
   unsigned *st = nullptr;
-  cudaError_t e = status_ptr(&st);
-  if (e != cudaSuccess) return cuda_fail(e, "swa_sink_decode");
+  cudaError_t e = status_ptr(&st, stream);
+  if (e != cudaSuccess) return state_fail(e, "swa_sink_decode");
   if (ring->kind == KVR_LAYOUT_PAGED)
     e = kvr::launch_swa_decode_paged(q, pos, seq, B, Hq, view(*ring), sinks, rope_cos_sin, max_pos, softmax_scale,
                                      out, st, as_stream(stream));
@@ -287,8 +370,8 @@ kvr_status full_attn_decode(const kvr_bf16 *q, const int64_t *pos, const int32_t
     return fail(KVR_EWORKSPACE, "workspace %zu bytes, need %zu", workspace ? workspace_bytes : (size_t)0, need);
   if (!aligned16(workspace)) return fail(KVR_EINVAL, "workspace not 16-byte aligned");
   unsigned *st = nullptr;
-  cudaError_t e = status_ptr(&st);
-  if (e != cudaSuccess) return cuda_fail(e, "full_attn_decode");
+  cudaError_t e = status_ptr(&st, stream);
+  if (e != cudaSuccess) return state_fail(e, "full_attn_decode");
   e = kvr::launch_full_decode(q, pos, seq, B, Hq, view(*pool), rope_cos_sin, max_pos, softmax_scale, max_ctx,
                               workspace, out, st, as_stream(stream));
   if (e != cudaSuccess) return cuda_fail(e, "full_attn_decode launch");
@@ -314,8 +397,8 @@ kvr_status swa_sink_prefill_chunk(const kvr_bf16 *q, int64_t P0, int32_t C, int3
   if (!q || !sinks || !out) return fail(KVR_EINVAL, "q/sinks/out is NULL");
   if (!aligned16(q) || !aligned16(out)) return fail(KVR_EINVAL, "q/out not 16-byte aligned");
   unsigned *st = nullptr;
-  cudaError_t e = status_ptr(&st);
-  if (e != cudaSuccess) return cuda_fail(e, "swa_sink_prefill_chunk");
+  cudaError_t e = status_ptr(&st, stream);
+  if (e != cudaSuccess) return state_fail(e, "swa_sink_prefill_chunk");
   e = kvr::launch_swa_prefill_tc(q, P0, C, seq, Hq, view(*chunk_kv), view(*ring), sinks, rope_cos_sin, softmax_scale,
                                  out, st, as_stream(stream));
   if (e != cudaSuccess) return cuda_fail(e, "swa_sink_prefill_chunk launch");
@@ -338,8 +421,8 @@ kvr_status full_attn_prefill_chunk(const kvr_bf16 *q, int64_t P0, int32_t C, int
   if (!q || !out) return fail(KVR_EINVAL, "q/out is NULL");
   if (!aligned16(q) || !aligned16(out)) return fail(KVR_EINVAL, "q/out not 16-byte aligned");
   unsigned *st = nullptr;
-  cudaError_t e = status_ptr(&st);
-  if (e != cudaSuccess) return cuda_fail(e, "full_attn_prefill_chunk");
+  cudaError_t e = status_ptr(&st, stream);
+  if (e != cudaSuccess) return state_fail(e, "full_attn_prefill_chunk");
   e = kvr::launch_full_prefill(q, P0, C, seq, Hq, view(*pool), rope_cos_sin, max_pos, softmax_scale, out, st,
                                as_stream(stream));
   if (e != cudaSuccess) return cuda_fail(e, "full_attn_prefill_chunk launch");
@@ -357,8 +440,8 @@ static kvr_status ring_copy(const char *name, const kvr_kv_layout *ring, const i
   if (!aligned16(k_snap) || !aligned16(v_snap)) return fail(KVR_EINVAL, "%s: snapshot k/v not 16-byte aligned", name);
   if (n > 65535) return fail(KVR_EUNSUPPORTED, "%s: n %d > 65535", name, n);
   unsigned *st = nullptr;
-  cudaError_t e = status_ptr(&st);
-  if (e != cudaSuccess) return cuda_fail(e, name);
+  cudaError_t e = status_ptr(&st, stream);
+  if (e != cudaSuccess) return state_fail(e, name);
   e = kvr::launch_ring_copy(view(*ring), seqs, n, const_cast<uint16_t *>(k_snap), const_cast<uint16_t *>(v_snap),
                             const_cast<int32_t *>(tags_snap), to_ring, st, as_stream(stream));
   if (e != cudaSuccess) return cuda_fail(e, name);
@@ -416,8 +499,8 @@ kvr_status full_attn_prefill_varlen(const kvr_bf16 *q, const int32_t *cu_rows, c
     return fail(KVR_EWORKSPACE, "workspace %zu bytes, need %zu", workspace ? workspace_bytes : (size_t)0, z.bytes);
   if (!aligned16(workspace)) return fail(KVR_EINVAL, "workspace not 16-byte aligned");
   unsigned *st = nullptr;
-  cudaError_t e = status_ptr(&st);
-  if (e != cudaSuccess) return cuda_fail(e, who);
+  cudaError_t e = status_ptr(&st, stream);
+  if (e != cudaSuccess) return state_fail(e, who);
   e = kvr::launch_full_varlen(q, cu_rows, P0, seq, n, T, Hq, view(*pool), rope_cos_sin, softmax_scale, max_ctx,
                               workspace, out, st, as_stream(stream));
   if (e != cudaSuccess) return cuda_fail(e, "full_attn_prefill_varlen launch");
@@ -449,8 +532,8 @@ kvr_status swa_sink_prefill_varlen(const kvr_bf16 *q, const int32_t *cu_rows, co
     return fail(KVR_EWORKSPACE, "workspace %zu bytes, need %zu", workspace ? workspace_bytes : (size_t)0, z.bytes);
   if (!aligned16(workspace)) return fail(KVR_EINVAL, "workspace not 16-byte aligned");
   unsigned *st = nullptr;
-  cudaError_t e = status_ptr(&st);
-  if (e != cudaSuccess) return cuda_fail(e, who);
+  cudaError_t e = status_ptr(&st, stream);
+  if (e != cudaSuccess) return state_fail(e, who);
   e = kvr::launch_swa_varlen(q, cu_rows, P0, seq, n, T, Hq, view(*chunk_kv), view(*ring), sinks, rope_cos_sin,
                              max_pos, softmax_scale, workspace, out, st, as_stream(stream));
   if (e != cudaSuccess) return cuda_fail(e, "swa_sink_prefill_varlen launch");
@@ -476,8 +559,8 @@ kvr_status kv_pages_release_window(int32_t *block_table, int32_t num_seqs, int32
   if (!seqs || !next_pos) return fail(KVR_EINVAL, "kv_pages_release_window: seqs/next_pos is NULL");
   if (free_cap > 0 && !free_ids) return fail(KVR_EINVAL, "kv_pages_release_window: free_ids is NULL");
   unsigned *st = nullptr;
-  cudaError_t e = status_ptr(&st);
-  if (e != cudaSuccess) return cuda_fail(e, "kv_pages_release_window");
+  cudaError_t e = status_ptr(&st, stream);
+  if (e != cudaSuccess) return state_fail(e, "kv_pages_release_window");
   e = kvr::launch_pages_release(block_table, num_seqs, max_blocks, block_size, num_blocks, seqs, next_pos, lo, n,
                                 window, free_ids, free_count, free_cap, st, as_stream(stream));
   if (e != cudaSuccess) return cuda_fail(e, "kv_pages_release_window launch");
@@ -495,8 +578,8 @@ kvr_status kv_ring_gather_pages(const kvr_kv_layout *pages, const kvr_kv_layout 
   if (n == 0) return ok();
   if (!src_seqs || !dst_seqs || !end) return fail(KVR_EINVAL, "kv_ring_gather_pages: src_seqs/dst_seqs/end is NULL");
   unsigned *st = nullptr;
-  cudaError_t e = status_ptr(&st);
-  if (e != cudaSuccess) return cuda_fail(e, "kv_ring_gather_pages");
+  cudaError_t e = status_ptr(&st, stream);
+  if (e != cudaSuccess) return state_fail(e, "kv_ring_gather_pages");
   e = kvr::launch_ring_gather(view(*pages), view(*ring), src_seqs, dst_seqs, end, n, st, as_stream(stream));
   if (e != cudaSuccess) return cuda_fail(e, "kv_ring_gather_pages launch");
   return ok();
@@ -518,25 +601,10 @@ namespace {
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[KVR_NOALLOC_SCRATCH_BYTES];
 
-std::mutex g_noalloc_mu;
-void *g_noalloc_ptr[MAX_DEV];
-
 // Device address of g_noalloc_scratch on the current device; looked up on the
-// first call made on that device.
-cudaError_t noalloc_scratch(void **out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= MAX_DEV) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> lk(g_noalloc_mu);
-  if (!g_noalloc_ptr[dev]) {
-    void *p = nullptr;
-    e = cudaGetSymbolAddress((void **)&p, g_noalloc_scratch);
-    if (e != cudaSuccess) return e;
-    g_noalloc_ptr[dev] = p;
-  }
-  *out = g_noalloc_ptr[dev];
-  return cudaSuccess;
+// first call made on that device (and again after a device reset).
+cudaError_t noalloc_scratch(void **out, void *stream) {
+  return symbol_addr(&DevSyms::scratch, g_noalloc_scratch, stream, out);
 }
 
 }  // namespace
@@ -565,11 +633,11 @@ extern "C" kvr_status full_attn_decode_noalloc(const kvr_bf16 *q, const int64_t 
                 "use full_attn_decode with a workspace, or a smaller batch or max_ctx",
                 need, (size_t)KVR_NOALLOC_SCRATCH_BYTES);
   void *scratch = nullptr;
-  cudaError_t e = noalloc_scratch(&scratch);
-  if (e != cudaSuccess) return cuda_fail(e, "full_attn_decode_noalloc: cudaGetSymbolAddress");
+  cudaError_t e = noalloc_scratch(&scratch, stream);
+  if (e != cudaSuccess) return state_fail(e, "full_attn_decode_noalloc: cudaGetSymbolAddress");
   unsigned *st = nullptr;
-  e = status_ptr(&st);
-  if (e != cudaSuccess) return cuda_fail(e, "full_attn_decode_noalloc");
+  e = status_ptr(&st, stream);
+  if (e != cudaSuccess) return state_fail(e, "full_attn_decode_noalloc");
   e = kvr::launch_full_decode(q, pos, seq, B, Hq, view(*pool), rope_cos_sin, max_pos, softmax_scale, max_ctx,
                               scratch, out, st, as_stream(stream));
   if (e != cudaSuccess) return cuda_fail(e, "full_attn_decode_noalloc launch");
