@@ -32,7 +32,20 @@ constexpr int FD_STAGES = 2;
 constexpr int FD_SUB_K = 16 * DQK * 2;                 // 6144 B
 constexpr int FD_SUB_V = 16 * DV * 2;                  // 4096 B
 constexpr int FD_STAGE = FD_SUB_K + FD_SUB_V;          // 10240 B
-constexpr int FD_SMEM = 16 * DQK * 2 + FD_WARPS * FD_STAGES * FD_STAGE;
+// the query tile, the table row, (windowed layer) the next item's block ids
+constexpr int FDW_NB = 16;
+constexpr int FD_HEAD = 16 * DQK * 2 + 256 + 128;
+constexpr int FD_SMEM = FD_HEAD + FD_WARPS * FD_STAGES * FD_STAGE;
+// Windowed layer in pages: a window of WIN keys starting anywhere covers at
+// most FDW_SUBS 16-key subtiles, each with a stage of its own, so the whole
+// window is requested at once (at most FDW_AHEAD subtiles per warp).
+constexpr int FDW_SUBS = WIN / 16 + 1;
+constexpr int FDW_AHEAD = (FDW_SUBS + FD_WARPS - 1) / FD_WARPS;
+constexpr int FDW_SMEM = FD_HEAD + FDW_SUBS * FD_STAGE;
+static_assert(FDW_AHEAD == 3, "the windowed wait below counts three groups");
+// a window's keys (at most WIN + 15 from its 16-key aligned start) over
+// blocks of at least 16 keys
+static_assert((WIN + 15 + 15) / 16 + 1 <= FDW_NB, "block ids of one window");
 // split plan (see full_decode_plan_kernel): the fixed cost of an item in keys,
 // the longest split, and where the per-sequence item prefix starts in the
 // plan (after L and the item count, 256-byte aligned)
@@ -262,7 +275,8 @@ __device__ void decode_plan_warp(const int64_t *__restrict__ pos, const int32_t 
   }
 }
 
-static_assert(FD_WARPS * FD_STAGES * FD_STAGE >= FD_WARPS * 16 * (MO_STRIDE + 2) * 4, "merge area");
+static_assert(FD_WARPS * FD_STAGES * FD_STAGE >= (FD_WARPS * 16 * (MO_STRIDE + 2) + FD_WARPS * 16) * 4, "merge area");
+static_assert(FDW_SUBS * FD_STAGE >= (FD_WARPS * 16 * (MO_STRIDE + 2) + FD_WARPS * 16) * 4, "merge area");
 
 // WINDOW = false: a full layer (keys 0..p, split partials to the workspace);
 // true: a windowed layer kept in pages (keys p-127..p, one split, direct
@@ -277,8 +291,13 @@ __global__ void __launch_bounds__(FD_WARPS * 32, 2)
                        float *__restrict__ part_ml, float *__restrict__ part_o, unsigned *status, int window,
                        const float *__restrict__ sinks, uint16_t *__restrict__ out_direct) {
   extern __shared__ __align__(128) uint8_t smem[];
+  // the merge kernel (a programmatic dependent) may be scheduled as SMs free
+  // up; it reads nothing of this kernel's before this kernel has completed
+  if (!WINDOW) asm volatile("griddepcontrol.launch_dependents;");
   uint8_t *sQ = smem;
-  uint8_t *sStage = smem + 16 * DQK * 2;
+  uint8_t *sCS = smem + 16 * DQK * 2;
+  int32_t *sNB = reinterpret_cast<int32_t *>(smem + 16 * DQK * 2 + 256);
+  uint8_t *sStage = smem + FD_HEAD;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int hkv = pool.hkv;
   // Full layer: the items (sequence, split, KV head) of the device plan, in
@@ -320,6 +339,15 @@ __global__ void __launch_bounds__(FD_WARPS * 32, 2)
     }
   }
 
+  // Windowed layer, across items: the next item's position and sequence id
+  // are loaded during the current one (carried), its query rows, table row
+  // and window rows prefetched into L2, and its block ids left in sNB
+  // (nb_ok) by the last warp.
+  bool carried = false, nb_ok = false;
+  long long p_next = 0;
+  int s_next = 0;
+  const int bsz = pool.block_size;
+
   for (long long w = blockIdx.x; w < nitems; w += gridDim.x) {
     int b, split, kv;
     if (WINDOW) {
@@ -332,11 +360,35 @@ __global__ void __launch_bounds__(FD_WARPS * 32, 2)
       split = local / hkv;
       kv = local - split * hkv;
     }
-    const long long p = pos[b];
-    const int s = seq[b];
+    // The query rows' copies go out before anything is waited for; they join
+    // the query group closed below (or are drained on the early exits).
+    q_rows_issue<FD_WARPS * 32>(q + ((long long)b * hq + (long long)kv * G) * DQK, G, sQ, tid);
+    long long p;
+    int s;
+    if (WINDOW && carried) {
+      p = p_next;
+      s = s_next;
+    } else {
+      p = pos[b];
+      s = seq[b];
+    }
+    const long long wn = w + gridDim.x;
+    const bool has_next = WINDOW && wn < nitems;
+    int kv_next = 0;
+    if (has_next) {
+      const int bn = (int)(wn / hkv);
+      kv_next = (int)(wn % hkv);
+      p_next = pos[bn];
+      s_next = seq[bn];
+      if (tid == 0) prefetch_l2(q + ((long long)bn * hq + (long long)kv_next * G) * DQK, G * DQK * 2);
+    }
+    carried = has_next;
+    const bool use_nb = WINDOW && nb_ok;  // sNB holds this item's block ids
+    nb_ok = false;
     const bool bad_pos = p < 0 || p >= max_pos || p + 1 > max_ctx;
     const bool bad_seq = s < 0 || s >= pool.num_seqs;
     if (bad_pos || bad_seq) {  // (the plan gives such a sequence no items; flagged there)
+      cp_async_wait_all();
       if (WINDOW) {
         if (kv == 0 && tid == 0) flag(status, (bad_pos ? ST_BAD_POS : 0u) | (bad_seq ? ST_BAD_SEQ : 0u));
         uint16_t *o = out_direct + ((long long)b * hq + (long long)kv * G) * DV;  // direct mode: zero rows
@@ -349,35 +401,35 @@ __global__ void __launch_bounds__(FD_WARPS * 32, 2)
     // instead of read and their scores masked
     const long long key_min = WINDOW ? max(0LL, p - window + 1) : 0;
     const long long key_lo = (key_min & ~15LL) + (long long)split * split_len;
-    if (key_lo > p) continue;
     const long long key_hi = min(key_lo + split_len, p + 1);
+    if (key_lo > p) {
+      cp_async_wait_all();
+      continue;
+    }
 
-    __syncthreads();  // the previous item's merge area is free again
-    load_q_tile(q + ((long long)b * hq + (long long)kv * G) * DQK, G, table + p * 64, sQ, tid, blockDim.x);
-    __syncthreads();
-    uint32_t qf[12][4];
-    load_q_frags(sQ, lane, qf);
-
-    float O[16][4];
-#pragma unroll
-    for (int nt = 0; nt < 16; ++nt) O[nt][0] = O[nt][1] = O[nt][2] = O[nt][3] = 0.f;
-    float m0 = NEG_INF, m1 = NEG_INF, l0 = 0.f, l1 = 0.f;
-
+    __syncthreads();  // the previous item's merge area (over the stages) is free again
+    // The query group closes before the first key subtiles go out; the query
+    // tile is rotated once it has landed.  The subtiles do not depend on it,
+    // and the query's copies do not queue behind theirs.
+    q_table_issue(table + p * 64, sCS, tid);
     const int nsub = (int)((key_hi - key_lo + 15) / 16);
     const int my_n = nsub > warp ? (nsub - warp + FD_WARPS - 1) / FD_WARPS : 0;
-    uint8_t *wst = sStage + warp * FD_STAGES * FD_STAGE;
+    // the warp's i-th subtile (subtile warp + 4i of the item): a ring of
+    // FD_STAGES stages per warp, or (window) the subtile's own stage
+    auto stage = [&](int i) -> uint8_t * {
+      return sStage + (WINDOW ? warp + i * FD_WARPS : warp * FD_STAGES + i % FD_STAGES) * FD_STAGE;
+    };
     const int32_t *bt = pool.block_table + (long long)s * pool.max_blocks;
-    const int bsz = pool.block_size;
 
     auto issue = [&](int i) {
       const long long key0 = key_lo + 16LL * (warp + i * FD_WARPS);
-      const int blk = bt[key0 / bsz];
+      const int blk = use_nb ? sNB[key0 / bsz - key_lo / bsz] : bt[key0 / bsz];
       const bool blk_ok = blk >= 0 && blk < pool.num_blocks;
       if (!blk_ok && lane == 0) flag(status, ST_BAD_BLOCK);
       const long long hrow = ((long long)(blk_ok ? blk : 0) * hkv + kv) * bsz + (key0 % bsz);
       const uint16_t *kg = pool.k + hrow * DQK;
       const uint16_t *vg = pool.v + hrow * DV;
-      const uint32_t kb = smem_u32(wst + (i % FD_STAGES) * FD_STAGE);
+      const uint32_t kb = smem_u32(stage(i));
       const uint32_t vb = kb + FD_SUB_K;
 #pragma unroll
       for (int u = 0; u < 12; ++u) {
@@ -393,17 +445,65 @@ __global__ void __launch_bounds__(FD_WARPS * 32, 2)
       }
     };
 
+    constexpr int AHEAD = WINDOW ? FDW_AHEAD : FD_STAGES - 1;
 #pragma unroll
-    for (int i = 0; i < FD_STAGES - 1; ++i) {
+    for (int i = 0; i < AHEAD; ++i) {
       if (i < my_n) issue(i);
       cp_async_commit();
     }
+    cp_async_wait<AHEAD>();  // the query group (the oldest)
+    __syncthreads();
+    q_tile_rotate(G, sQ, sCS, tid);
+    __syncthreads();
+    uint32_t qf[12][4];
+    load_q_frags(sQ, lane, qf);
+    if (WINDOW && has_next) {
+      // the next item: its window rows and table row into L2, its block ids
+      // into sNB (every issue of this item has read sNB before the barrier
+      // above); the warp's wait for the ids overlaps its first subtile's
+      const bool ok_next = p_next >= 0 && p_next < max_pos && p_next + 1 <= max_ctx && s_next >= 0 &&
+                           s_next < pool.num_seqs;
+      if (ok_next) {
+        const long long kmin = max(0LL, p_next - window + 1), klo = kmin & ~15LL;
+        const long long b0 = klo / bsz, nblk = p_next / bsz - b0 + 1;
+        if (warp == FD_WARPS - 1) {
+          const int32_t *btn = pool.block_table + (long long)s_next * pool.max_blocks;
+          if (lane < nblk) {
+            const int blk = btn[b0 + lane];
+            sNB[lane] = blk;
+            if (blk >= 0 && blk < pool.num_blocks) {
+              const long long first = (b0 + lane) * bsz;
+              const long long r0 = max(kmin, first) - first, r1 = min(p_next, first + bsz - 1) - first;
+              const long long hrow = ((long long)blk * hkv + kv_next) * bsz + r0;
+              prefetch_l2(pool.k + hrow * DQK, (uint32_t)(r1 - r0 + 1) * DQK * 2);
+              prefetch_l2(pool.v + hrow * DV, (uint32_t)(r1 - r0 + 1) * DV * 2);
+            }
+          }
+          if (lane == 0) prefetch_l2(table + p_next * 64, 256);
+        }
+        nb_ok = true;
+      }
+    }
+
+    float O[16][4];
+#pragma unroll
+    for (int nt = 0; nt < 16; ++nt) O[nt][0] = O[nt][1] = O[nt][2] = O[nt][3] = 0.f;
+    float m0 = NEG_INF, m1 = NEG_INF, l0 = 0.f, l1 = 0.f;
     for (int i = 0; i < my_n; ++i) {
-      if (i + FD_STAGES - 1 < my_n) issue(i + FD_STAGES - 1);
-      cp_async_commit();
-      cp_async_wait<FD_STAGES - 1>();
+      if (WINDOW) {  // all of the warp's subtiles are in flight: wait for the i-th group
+        if (i == 0)
+          cp_async_wait<FDW_AHEAD - 1>();
+        else if (i == 1)
+          cp_async_wait<FDW_AHEAD - 2>();
+        else
+          cp_async_wait<0>();
+      } else {
+        if (i + FD_STAGES - 1 < my_n) issue(i + FD_STAGES - 1);
+        cp_async_commit();
+        cp_async_wait<FD_STAGES - 1>();
+      }
       __syncwarp();
-      const uint32_t kb = smem_u32(wst + (i % FD_STAGES) * FD_STAGE);
+      const uint32_t kb = smem_u32(stage(i));
       const long long key0 = key_lo + 16LL * (warp + i * FD_WARPS);
       const int blk = bt[key0 / bsz];
       const bool blk_ok = blk >= 0 && blk < pool.num_blocks;
@@ -428,59 +528,56 @@ __global__ void __launch_bounds__(FD_WARPS * 32, 2)
     stash_warp_state(mml + warp * 32, mo + warp * 16 * MO_STRIDE, lane, m0, m1, l0, l1, O);
     __syncthreads();
 
-    if (WINDOW) {
-      // one split holds the whole window: normalise here, the sink joining
-      // the denominator only (its numerator is zero)
-      uint16_t *o = out_direct + ((long long)b * hq + (long long)kv * G) * DV;
-      for (int g = 0; g < G; ++g) {
-        const float sl = sinks[kv * G + g] * LOG2E;
-        float M = sl;
-#pragma unroll
-        for (int ww = 0; ww < FD_WARPS; ++ww) M = fmaxf(M, mml[ww * 32 + g * 2]);
-        float L = ex2(sl - M);
-#pragma unroll
-        for (int ww = 0; ww < FD_WARPS; ++ww) {
-          const float mw = mml[ww * 32 + g * 2];
-          L += mml[ww * 32 + g * 2 + 1] * (mw == NEG_INF ? 0.f : ex2(mw - M));
-        }
-        const float inv = 1.f / L;
-        for (int d = tid; d < DV; d += blockDim.x) {
-          float acc = 0.f;
-#pragma unroll
-          for (int ww = 0; ww < FD_WARPS; ++ww) {
-            const float mw = mml[ww * 32 + g * 2];
-            acc += mo[(ww * 16 + g) * MO_STRIDE + d] * (mw == NEG_INF ? 0.f : ex2(mw - M));
-          }
-          o[g * DV + d] = f2bf(acc * inv);
-        }
-      }
-      continue;
-    }
-    float *pml = part_ml + w * G * 2;
-    float *po = part_o + w * G * DV;
-    for (int g = 0; g < G; ++g) {
-      float M = NEG_INF;
+    // Per q head (threads 0..G-1): the head's maximum over the four warps
+    // and each warp's scale factor; then every thread takes 4-dim pieces of
+    // the G x 128 outputs.
+    float *fac = mo + FD_WARPS * 16 * MO_STRIDE;  // [4 warps][16 heads]
+    if (tid < G) {
+      const int g = tid;
+      const float sl = WINDOW ? sinks[kv * G + g] * LOG2E : NEG_INF;
+      float M = sl;
 #pragma unroll
       for (int ww = 0; ww < FD_WARPS; ++ww) M = fmaxf(M, mml[ww * 32 + g * 2]);
       const float base = M == NEG_INF ? 0.f : M;
-      float L = 0.f;
-      for (int d = tid; d < DV; d += blockDim.x) {
-        float acc = 0.f;
+      float f[FD_WARPS], L = WINDOW ? ex2(sl - base) : 0.f;
 #pragma unroll
-        for (int ww = 0; ww < FD_WARPS; ++ww) {
-          const float mw = mml[ww * 32 + g * 2];
-          acc += mo[(ww * 16 + g) * MO_STRIDE + d] * (mw == NEG_INF ? 0.f : ex2(mw - base));
-        }
-        po[g * DV + d] = acc;
+      for (int ww = 0; ww < FD_WARPS; ++ww) {
+        const float mw = mml[ww * 32 + g * 2];
+        f[ww] = mw == NEG_INF ? 0.f : ex2(mw - base);
+        L += mml[ww * 32 + g * 2 + 1] * f[ww];
       }
-      if (tid == 0) {
+      if (WINDOW) {
+        // one split holds the whole window: normalise here, the sink joining
+        // the denominator only (its numerator is zero)
+        const float inv = 1.f / L;
 #pragma unroll
-        for (int ww = 0; ww < FD_WARPS; ++ww) {
-          const float mw = mml[ww * 32 + g * 2];
-          L += mml[ww * 32 + g * 2 + 1] * (mw == NEG_INF ? 0.f : ex2(mw - base));
-        }
+        for (int ww = 0; ww < FD_WARPS; ++ww) fac[ww * 16 + g] = f[ww] * inv;
+      } else {
+#pragma unroll
+        for (int ww = 0; ww < FD_WARPS; ++ww) fac[ww * 16 + g] = f[ww];
+        float *pml = part_ml + w * G * 2;
         pml[g * 2] = M;
         pml[g * 2 + 1] = L;
+      }
+    }
+    __syncthreads();
+    for (int idx = tid; idx < G * (DV / 4); idx += blockDim.x) {
+      const int g = idx / (DV / 4), d4 = 4 * (idx % (DV / 4));
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int ww = 0; ww < FD_WARPS; ++ww) {
+        const float f = fac[ww * 16 + g];
+        const float4 x = *reinterpret_cast<const float4 *>(mo + (ww * 16 + g) * MO_STRIDE + d4);
+        acc.x += x.x * f;
+        acc.y += x.y * f;
+        acc.z += x.z * f;
+        acc.w += x.w * f;
+      }
+      if (WINDOW) {
+        uint16_t *o = out_direct + ((long long)b * hq + (long long)kv * G + g) * DV + d4;
+        *reinterpret_cast<uint2 *>(o) = make_uint2(pack_bf16(acc.x, acc.y), pack_bf16(acc.z, acc.w));
+      } else {
+        *reinterpret_cast<float4 *>(part_o + (w * G + g) * DV + d4) = acc;
       }
     }
   }
@@ -504,13 +601,21 @@ __global__ void __launch_bounds__(DP_THREADS)
 }
 
 // Full layer, phase 2: merge the splits of each (sequence, KV head, q head)
-// row by log-sum-exp and normalise.  NW warps per row (NW in {1, 2, 4, 8},
-// from the expected split count) fold interleaved subsets of the splits with
-// a running maximum -- lane l owns value dims 4l..4l+3 -- and the row's first
-// warp merges their partial states from shared memory.  Eight warps per CTA,
-// 8 / NW rows per CTA, so short contexts with many sequences and one long
-// sequence with hundreds of splits both keep the GPU busy.
-constexpr int FC_WARPS = 8;
+// row by log-sum-exp and normalise.  NW warps per row (NW in {1, 2, 4, 8,
+// 16}, from the expected split count) fold interleaved subsets of the splits
+// -- lane l owns value dims 4l..4l+3 -- FC_K splits at a time, all of their
+// loads in flight together, and the row's first warp merges their partial
+// states from shared memory.  Sixteen warps per CTA, 16 / NW rows per CTA, so
+// short contexts with many sequences and one long sequence with hundreds of
+// splits both keep the GPU busy.
+//
+// The kernel is launched as a programmatic dependent of the split kernel: its
+// CTAs may start while the split kernel's last CTAs run, read the inputs the
+// split kernel does not write (positions, sequence ids), and wait at
+// griddepcontrol.wait -- which returns once the split kernel has completed
+// and its writes are visible -- before reading the plan and the partials.
+constexpr int FC_WARPS = 16;
+constexpr int FC_K = 8;
 
 __global__ void __launch_bounds__(FC_WARPS * 32)
     full_combine_kernel(const int64_t *__restrict__ pos, const int32_t *__restrict__ seq, int B, int hq, int G,
@@ -527,31 +632,52 @@ __global__ void __launch_bounds__(FC_WARPS * 32)
   const int g = have ? (int)(row % G) : 0;
   const int kv = have ? (int)((row / G) % hkv) : 0;
   const int b = have ? (int)(row / ((long long)G * hkv)) : 0;
-  const int split_len = plan[0];
-  int n = 0;
-  long long base = 0;
+  bool ok = false;
+  long long p = 0;
   if (have) {
-    const long long p = pos[b];
+    p = pos[b];
     const int s = seq[b];
-    const bool ok = p >= 0 && p < max_pos && p + 1 <= max_ctx && s >= 0 && s < num_seqs;
-    n = ok ? (int)(p / split_len) + 1 : 0;
-    base = plan[DPLAN_PREFIX + b];
+    ok = p >= 0 && p < max_pos && p + 1 <= max_ctx && s >= 0 && s < num_seqs;
   }
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int split_len = plan[0];
+  const int n = ok ? (int)(p / split_len) + 1 : 0;
+  const long long base = have ? plan[DPLAN_PREFIX + b] : 0;
   float M = NEG_INF, L = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-  for (int i = sub; i < n; i += nw) {
-    const long long w = base + (long long)i * hkv + kv;
-    const float2 ml = *reinterpret_cast<const float2 *>(part_ml + (w * G + g) * 2);
-    const float4 o = *reinterpret_cast<const float4 *>(part_o + (w * G + g) * DV + 4 * lane);
-    if (ml.x == NEG_INF) continue;
-    const float Mn = fmaxf(M, ml.x);
-    const float c = ex2(M - Mn), f = ex2(ml.x - Mn);  // M = -inf gives c = 0
-    L = L * c + ml.y * f;
-    acc.x = acc.x * c + o.x * f;
-    acc.y = acc.y * c + o.y * f;
-    acc.z = acc.z * c + o.z * f;
-    acc.w = acc.w * c + o.w * f;
+  for (int i0 = sub; i0 < n; i0 += FC_K * nw) {
+    float2 ml[FC_K];
+    float4 o[FC_K];
+#pragma unroll
+    for (int k = 0; k < FC_K; ++k) {
+      const int i = i0 + k * nw;
+      ml[k] = make_float2(NEG_INF, 0.f);
+      o[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (i < n) {
+        const long long w = base + (long long)i * hkv + kv;
+        ml[k] = *reinterpret_cast<const float2 *>(part_ml + (w * G + g) * 2);
+        o[k] = *reinterpret_cast<const float4 *>(part_o + (w * G + g) * DV + 4 * lane);
+      }
+    }
+    float Mn = M;
+#pragma unroll
+    for (int k = 0; k < FC_K; ++k) Mn = fmaxf(Mn, ml[k].x);
+    if (Mn == NEG_INF) continue;  // nothing yet (empty splits only)
+    const float c = ex2(M - Mn);  // M = -inf gives 0
+    L *= c;
+    acc.x *= c;
+    acc.y *= c;
+    acc.z *= c;
+    acc.w *= c;
+#pragma unroll
+    for (int k = 0; k < FC_K; ++k) {
+      const float f = ex2(ml[k].x - Mn);  // an empty split (-inf) gives 0
+      L += ml[k].y * f;
+      acc.x += o[k].x * f;
+      acc.y += o[k].y * f;
+      acc.z += o[k].z * f;
+      acc.w += o[k].w * f;
+    }
     M = Mn;
   }
   if (nw > 1) {
@@ -673,21 +799,31 @@ cudaError_t launch_full_decode(const uint16_t *q, const int64_t *pos, const int3
       0, nullptr, nullptr);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  // warps per merged row: about eight splits each, at most eight
+  // warps per merged row: about four splits each, at most sixteen
   const DecodePlan est = full_decode_plan(B, hkv, max_ctx);
   int nw = 1;
-  while (nw < FC_WARPS && nw * 8 < est.splits) nw *= 2;
+  while (nw < FC_WARPS && nw * 4 < est.splits) nw *= 2;
   const long long rows = (long long)B * hkv * G;
   const long long ctas = (rows + FC_WARPS / nw - 1) / (FC_WARPS / nw);
-  full_combine_kernel<<<(unsigned)ctas, FC_WARPS * 32, 0, st>>>(pos, seq, B, hq, G, hkv, pool.num_seqs, max_pos,
-                                                               max_ctx, plan, nw, part_ml, part_o, out);
-  return cudaGetLastError();
+  // a programmatic dependent of the split kernel (see full_combine_kernel)
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)ctas);
+  cfg.blockDim = dim3(FC_WARPS * 32);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, full_combine_kernel, pos, seq, B, hq, G, hkv, pool.num_seqs, max_pos, max_ctx,
+                            (const int32_t *)plan, nw, (const float *)part_ml, (const float *)part_o, out);
 }
 
 cudaError_t launch_swa_decode_paged(const uint16_t *q, const int64_t *pos, const int32_t *seq, int B, int hq,
                                     const KvView &pool, const float *sinks, const float *table, int64_t max_pos,
                                     float softmax_scale, uint16_t *out, unsigned *status, cudaStream_t st) {
-  cudaError_t e = ensure_smem_limit(9, (const void *)full_decode_kernel<true>, FD_SMEM);
+  cudaError_t e = ensure_smem_limit(9, (const void *)full_decode_kernel<true>, FDW_SMEM);
   if (e != cudaSuccess) return e;
   const int hkv = pool.hkv, G = hq / hkv;
   // positions past the pool are flagged as bad positions, like full_attn_decode's max_ctx
@@ -696,7 +832,8 @@ cudaError_t launch_swa_decode_paged(const uint16_t *q, const int64_t *pos, const
   const long long items = (long long)B * hkv;
   long long grid = (long long)num_sms() * 2;
   if (grid > items) grid = items;
-  full_decode_kernel<true><<<(unsigned)grid, FD_WARPS * 32, FD_SMEM, st>>>(
+  static_assert((WIN + 16) / 16 == FDW_SUBS, "split length of the window below: at most FDW_SUBS subtiles");
+  full_decode_kernel<true><<<(unsigned)grid, FD_WARPS * 32, FDW_SMEM, st>>>(
       q, pos, seq, B, hq, G, pool, table, max_pos, softmax_scale * LOG2E, max_ctx, nullptr, WIN + 16, nullptr,
       nullptr, status, WIN, sinks, out);
   return cudaGetLastError();

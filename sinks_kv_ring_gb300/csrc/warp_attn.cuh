@@ -11,37 +11,42 @@ namespace {
 
 constexpr float NEG_INF = -INFINITY;
 
-// Rotate the G query heads of one token (q_heads [G][192]) with the table
-// row cs_row ([32][2] fp32), round to bf16 and store them as rows 0..G-1 of
-// the swizzled [16][192] tile sQ; rows G..15 are zero.
-__device__ __forceinline__ void load_q_tile(const uint16_t *__restrict__ q_heads, int G,
-                                            const float *__restrict__ cs_row, uint8_t *sQ, int tid,
-                                            int nthreads) {
-  for (int it = tid; it < 16 * 20; it += nthreads) {
-    const int r = it / 20, c = it % 20;
-    const uint4 zero = make_uint4(0, 0, 0, 0);
-    if (c < 4) {
-      uint4 o1 = zero, o2 = zero;
-      if (r < G) {
-        const uint4 *src = reinterpret_cast<const uint4 *>(q_heads + r * DQK);
-        const float4 *tr = reinterpret_cast<const float4 *>(cs_row + 16 * c);
-        float cs[16];
+// Rotated query tile in steps.  q_rows_issue: cp.async copies of the G query
+// heads of one token (q_heads [G][192]) into rows 0..G-1 of the swizzled
+// [16][192] tile sQ (rows G..15 zero-filled); q_table_issue: of the table row
+// cs_row ([32][2] fp32, 256 B) into sCS, closing the commit group.  Copies
+// issued after that group (the first key subtiles) queue behind it, not in
+// front of it.  q_tile_rotate, once the group has landed and the block has
+// synchronised: rotate dims 0..63 of each row in place and round to bf16
+// (threads 0..63, one (row, chunk pair c, c + 4) each).
+template <int NTH>
+__device__ __forceinline__ void q_rows_issue(const uint16_t *__restrict__ q_heads, int G, uint8_t *sQ, int tid) {
+  const uint32_t qb = smem_u32(sQ);
+  // opaque copy of tid: keeps the compiler from hoisting these per-thread
+  // offsets out of a caller's item loop and holding them in registers
+  asm volatile("" : "+r"(tid));
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const float4 f = tr[u];
-          cs[4 * u] = f.x; cs[4 * u + 1] = f.y; cs[4 * u + 2] = f.z; cs[4 * u + 3] = f.w;
-        }
-        rope_pair8(src[c], src[c + 4], cs, o1, o2);
-      }
-      *reinterpret_cast<uint4 *>(sQ + swz<DQK>(r, c)) = o1;
-      *reinterpret_cast<uint4 *>(sQ + swz<DQK>(r, c + 4)) = o2;
-    } else {
-      const int ch = c + 4;  // chunks 8..23
-      uint4 x = zero;
-      if (r < G) x = reinterpret_cast<const uint4 *>(q_heads + r * DQK)[ch];
-      *reinterpret_cast<uint4 *>(sQ + swz<DQK>(r, ch)) = x;
-    }
+  for (int k = 0; k < (16 * 24 + NTH - 1) / NTH; ++k) {
+    const int it = tid + k * NTH, r = it / 24, c = it % 24;
+    if (it < 16 * 24) cp_async16(qb + swz<DQK>(r, c), q_heads + (r < G ? r : 0) * DQK + c * 8, r < G ? 16 : 0);
   }
+}
+
+__device__ __forceinline__ void q_table_issue(const float *__restrict__ cs_row, uint8_t *sCS, int tid) {
+  if (tid < 16) cp_async16(smem_u32(sCS) + 16 * tid, cs_row + 4 * tid);
+  cp_async_commit();
+}
+
+__device__ __forceinline__ void q_tile_rotate(int G, uint8_t *sQ, const uint8_t *sCS, int tid) {
+  const int r = tid >> 2, c = tid & 3;
+  if (tid >= 64 || r >= G) return;
+  uint4 *p1 = reinterpret_cast<uint4 *>(sQ + swz<DQK>(r, c));
+  uint4 *p2 = reinterpret_cast<uint4 *>(sQ + swz<DQK>(r, c + 4));
+  const float *cs = reinterpret_cast<const float *>(sCS) + 16 * c;
+  uint4 o1, o2;
+  rope_pair8(*p1, *p2, cs, o1, o2);
+  *p1 = o1;
+  *p2 = o2;
 }
 
 // A fragments of the [16][192] Q tile for the 12 k-steps.
