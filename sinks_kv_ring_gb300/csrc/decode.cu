@@ -16,7 +16,10 @@
 // range starts at p - 127 (rounded down to a 16-key subtile, the extra keys
 // masked), one split covers it, and the kernel normalises directly with the
 // sink in the denominator (colibri "What the engine implements").
+#include <cuda.h>
+
 #include "launch.h"
+#include "tc_ptx.cuh"
 #include "warp_attn.cuh"
 
 namespace kvr {
@@ -27,22 +30,28 @@ namespace {
 // split, KV head) round-robin; each streams its key range through per-warp
 // cp.async pipelines of 16-key subtiles and writes fp32 partials.
 
+constexpr unsigned ST_TIMEOUT = 8u;  // KVR_DEV_TIMEOUT
 constexpr int FD_WARPS = 4;
 constexpr int FD_STAGES = 2;
 constexpr int FD_SUB_K = 16 * DQK * 2;                 // 6144 B
 constexpr int FD_SUB_V = 16 * DV * 2;                  // 4096 B
 constexpr int FD_STAGE = FD_SUB_K + FD_SUB_V;          // 10240 B
-// the query tile, the table row, (windowed layer) the next item's block ids
-constexpr int FDW_NB = 16;
-constexpr int FD_HEAD = 16 * DQK * 2 + 256 + 128;
-constexpr int FD_SMEM = FD_HEAD + FD_WARPS * FD_STAGES * FD_STAGE;
 // Windowed layer in pages: a window of WIN keys starting anywhere covers at
 // most FDW_SUBS 16-key subtiles, each with a stage of its own, so the whole
-// window is requested at once (at most FDW_AHEAD subtiles per warp).
+// window is requested at once (at most FDW_AHEAD subtiles per warp), by TMA.
 constexpr int FDW_SUBS = WIN / 16 + 1;
 constexpr int FDW_AHEAD = (FDW_SUBS + FD_WARPS - 1) / FD_WARPS;
-constexpr int FDW_SMEM = FD_HEAD + FDW_SUBS * FD_STAGE;
-static_assert(FDW_AHEAD == 3, "the windowed wait below counts three groups");
+constexpr int FDW_NB = 16;
+// head of the shared memory: the query tile, the table row, then (windowed
+// layer) the next item's block ids, one mbarrier per stage and the abort flag
+constexpr int FD_OFF_CS = 16 * DQK * 2;
+constexpr int FD_OFF_NB = FD_OFF_CS + 256;
+constexpr int FD_OFF_BAR = FD_OFF_NB + FDW_NB * 4;
+constexpr int FD_OFF_ABORT = FD_OFF_BAR + 8 * FDW_SUBS;
+constexpr int FD_HEAD = (FD_OFF_ABORT + 4 + 127) / 128 * 128;
+constexpr int FD_SMEM = FD_HEAD + FD_WARPS * FD_STAGES * FD_STAGE;
+// (the TMA stages start on the next 1024-byte boundary, as the 128-byte swizzle wants)
+constexpr int FDW_SMEM = FD_HEAD + 1024 + FDW_SUBS * FD_STAGE;
 // a window's keys (at most WIN + 15 from its 16-key aligned start) over
 // blocks of at least 16 keys
 static_assert((WIN + 15 + 15) / 16 + 1 <= FDW_NB, "block ids of one window");
@@ -284,7 +293,8 @@ static_assert(FDW_SUBS * FD_STAGE >= (FD_WARPS * 16 * (MO_STRIDE + 2) + FD_WARPS
 // layer's issue path free of the window's per-row checks.
 template <bool WINDOW>
 __global__ void __launch_bounds__(FD_WARPS * 32, 2)
-    full_decode_kernel(const uint16_t *__restrict__ q, const int64_t *__restrict__ pos,
+    full_decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+                       const uint16_t *__restrict__ q, const int64_t *__restrict__ pos,
                        const int32_t *__restrict__ seq, int B, int hq, int G, KvView pool,
                        const float *__restrict__ table, int64_t max_pos, float scale_log2,
                        long long max_ctx, const int32_t *__restrict__ plan, int split_len,
@@ -295,9 +305,12 @@ __global__ void __launch_bounds__(FD_WARPS * 32, 2)
   // up; it reads nothing of this kernel's before this kernel has completed
   if (!WINDOW) asm volatile("griddepcontrol.launch_dependents;");
   uint8_t *sQ = smem;
-  uint8_t *sCS = smem + 16 * DQK * 2;
-  int32_t *sNB = reinterpret_cast<int32_t *>(smem + 16 * DQK * 2 + 256);
-  uint8_t *sStage = smem + FD_HEAD;
+  uint8_t *sCS = smem + FD_OFF_CS;
+  int32_t *sNB = reinterpret_cast<int32_t *>(smem + FD_OFF_NB);
+  const uint32_t sBar = smem_u32(smem + FD_OFF_BAR);
+  volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(smem + FD_OFF_ABORT);
+  uint8_t *sStage = WINDOW ? smem + (((smem_u32(smem) + FD_HEAD + 1023u) & ~1023u) - smem_u32(smem))
+                           : smem + FD_HEAD;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int hkv = pool.hkv;
   // Full layer: the items (sequence, split, KV head) of the device plan, in
@@ -308,6 +321,18 @@ __global__ void __launch_bounds__(FD_WARPS * 32, 2)
   // merge); a larger one by full_decode_plan_kernel before this kernel.
   const int32_t *prefix = plan + DPLAN_PREFIX;
   long long nitems = (long long)B * hkv;
+  // windowed layer: bit j of ph is the parity of stage j's next phase, bit j
+  // of pend marks a load into stage j not yet seen complete (this warp's
+  // stages j = warp + 4i only)
+  uint32_t ph = 0, pend = 0;
+  if (WINDOW) {
+    if (tid == 0) {
+      for (int j = 0; j < FDW_SUBS; ++j) tc::mbar_init(sBar + 8 * j, 1);
+      *abort_flag = 0;
+      tc::fence_mbar_init();
+    }
+    __syncthreads();
+  }
   if (!WINDOW) {
     if (B <= DP_INLINE_MAX) {
       int32_t *sPrefix = reinterpret_cast<int32_t *>(smem + FD_SMEM);
@@ -407,7 +432,17 @@ __global__ void __launch_bounds__(FD_WARPS * 32, 2)
       continue;
     }
 
-    __syncthreads();  // the previous item's merge area (over the stages) is free again
+    // the previous item's merge area (over the stages) is free again; a
+    // windowed layer whose wait gave up stops here
+    if (WINDOW) {
+      if (__syncthreads_or(*abort_flag != 0)) {
+        cp_async_wait_all();
+        break;
+      }
+      tc::fence_proxy_async_smem();  // generic accesses to the stages before the TMA writes
+    } else {
+      __syncthreads();
+    }
     // The query group closes before the first key subtiles go out; the query
     // tile is rotated once it has landed.  The subtiles do not depend on it,
     // and the query's copies do not queue behind theirs.
@@ -445,7 +480,37 @@ __global__ void __launch_bounds__(FD_WARPS * 32, 2)
       }
     };
 
-    constexpr int AHEAD = WINDOW ? FDW_AHEAD : FD_STAGES - 1;
+    // Windowed layer: the warp's subtiles by TMA, one-part boxes of 16 rows
+    // (a 16-key subtile never straddles a block), each completing on its
+    // stage's barrier; rows outside the window arrive too (zeroed or masked
+    // below).  A bad block id: no load, the barrier completes at once and the
+    // subtile counts as masked.
+    auto issue_tma = [&](int i) {
+      const int j = warp + i * FD_WARPS;
+      const long long key0 = key_lo + 16LL * j;
+      const int blk = use_nb ? sNB[key0 / bsz - key_lo / bsz] : bt[key0 / bsz];
+      const uint32_t bar = sBar + 8 * j, dst = smem_u32(stage(i));
+      if (blk >= 0 && blk < pool.num_blocks) {
+        const int hrow = (int)(((long long)blk * hkv + kv) * bsz + key0 % bsz);
+        tc::mbar_expect_tx_elect(bar, FD_STAGE);
+#pragma unroll
+        for (int part = 0; part < 3; ++part) tc::tma_load_3d_elect(dst + part * 2048, &kmap, 0, part, hrow, bar);
+#pragma unroll
+        for (int part = 0; part < 2; ++part)
+          tc::tma_load_3d_elect(dst + FD_SUB_K + part * 2048, &vmap, 0, part, hrow, bar);
+      } else if (lane == 0) {
+        flag(status, ST_BAD_BLOCK);
+        tc::mbar_arrive(bar);
+      }
+      pend |= 1u << j;
+    };
+
+    constexpr int AHEAD = WINDOW ? 0 : FD_STAGES - 1;
+    if (WINDOW) {
+#pragma unroll
+      for (int i = 0; i < FDW_AHEAD; ++i)
+        if (i < my_n) issue_tma(i);
+    }
 #pragma unroll
     for (int i = 0; i < AHEAD; ++i) {
       if (i < my_n) issue(i);
@@ -490,25 +555,35 @@ __global__ void __launch_bounds__(FD_WARPS * 32, 2)
     for (int nt = 0; nt < 16; ++nt) O[nt][0] = O[nt][1] = O[nt][2] = O[nt][3] = 0.f;
     float m0 = NEG_INF, m1 = NEG_INF, l0 = 0.f, l1 = 0.f;
     for (int i = 0; i < my_n; ++i) {
-      if (WINDOW) {  // all of the warp's subtiles are in flight: wait for the i-th group
-        if (i == 0)
-          cp_async_wait<FDW_AHEAD - 1>();
-        else if (i == 1)
-          cp_async_wait<FDW_AHEAD - 2>();
-        else
-          cp_async_wait<0>();
+      const uint32_t kb = smem_u32(stage(i));
+      const long long key0 = key_lo + 16LL * (warp + i * FD_WARPS);
+      const int blk = WINDOW && use_nb ? sNB[key0 / bsz - key_lo / bsz] : bt[key0 / bsz];
+      const bool blk_ok = blk >= 0 && blk < pool.num_blocks;
+      if (WINDOW) {
+        const int j = warp + i * FD_WARPS;
+        const bool got = __all_sync(0xffffffffu, tc::mbar_wait(sBar + 8 * j, (ph >> j) & 1u, abort_flag));
+        if (!got) continue;  // gave up: the subtile counts as masked, and the kernel stops at the next item
+        ph ^= 1u << j;
+        pend &= ~(1u << j);
+        // rows outside the window (or of a bad block) hold other keys' values:
+        // zero them, as their zero weights must not meet a non-finite value
+        if (!blk_ok || key0 < key_min || key0 + 16 > key_hi) {
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const int c = lane + 32 * u, r = c >> 4, ch = c & 15;
+            const long long key = key0 + r;
+            if (!(blk_ok && key < key_hi && key >= key_min))
+              *reinterpret_cast<uint4 *>(stage(i) + FD_SUB_K + sub_off<DV, true>(r, ch)) = make_uint4(0, 0, 0, 0);
+          }
+        }
       } else {
         if (i + FD_STAGES - 1 < my_n) issue(i + FD_STAGES - 1);
         cp_async_commit();
         cp_async_wait<FD_STAGES - 1>();
       }
       __syncwarp();
-      const uint32_t kb = smem_u32(stage(i));
-      const long long key0 = key_lo + 16LL * (warp + i * FD_WARPS);
-      const int blk = bt[key0 / bsz];
-      const bool blk_ok = blk >= 0 && blk < pool.num_blocks;
       float S[2][4];
-      qk_16keys(qf, kb, 0, lane, S);
+      qk_16keys<WINDOW>(qf, kb, 0, lane, S);
 #pragma unroll
       for (int j = 0; j < 2; ++j)
 #pragma unroll
@@ -517,7 +592,7 @@ __global__ void __launch_bounds__(FD_WARPS * 32, 2)
           S[j][e] = (blk_ok && key < key_hi && (!WINDOW || key >= key_min)) ? S[j][e] * scale_log2 : NEG_INF;
         }
       softmax_update(S, m0, m1, l0, l1, O);
-      pv_16keys(S, kb + FD_SUB_K, 0, lane, O);
+      pv_16keys<WINDOW>(S, kb + FD_SUB_K, 0, lane, O);
       __syncwarp();
     }
     cp_async_wait<0>();
@@ -580,6 +655,14 @@ __global__ void __launch_bounds__(FD_WARPS * 32, 2)
         *reinterpret_cast<float4 *>(part_o + (w * G + g) * DV + d4) = acc;
       }
     }
+  }
+  if (WINDOW && pend) {
+    // a wait gave up: report it, and before leaving wait (bounded, whatever
+    // the abort flag says) for this warp's loads still in flight
+    if (lane == 0) flag(status, ST_TIMEOUT);
+    uint32_t never = 0;
+    for (int j = 0; j < FDW_SUBS; ++j)
+      if ((pend >> j) & 1u) tc::mbar_wait(sBar + 8 * j, (ph >> j) & 1u, &never);
   }
 }
 
@@ -794,8 +877,9 @@ cudaError_t launch_full_decode(const uint16_t *q, const int64_t *pos, const int3
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
+  const CUtensorMap unused{};  // (the full layer's subtiles go by cp.async)
   full_decode_kernel<false><<<(unsigned)R, FD_WARPS * 32, smem, st>>>(
-      q, pos, seq, B, hq, G, pool, table, max_pos, softmax_scale * LOG2E, max_ctx, plan, 0, part_ml, part_o, status,
+      unused, unused, q, pos, seq, B, hq, G, pool, table, max_pos, softmax_scale * LOG2E, max_ctx, plan, 0, part_ml, part_o, status,
       0, nullptr, nullptr);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
@@ -832,9 +916,15 @@ cudaError_t launch_swa_decode_paged(const uint16_t *q, const int64_t *pos, const
   const long long items = (long long)B * hkv;
   long long grid = (long long)num_sms() * 2;
   if (grid > items) grid = items;
+  // the pool as rows of 64-element parts, boxes of one part x 16 rows
+  const long long rows = (long long)pool.num_blocks * hkv * pool.block_size;
+  CUtensorMap km, vm;
+  if (rows > 0x7fffffffLL || !make_tma_map_rows3d(&km, pool.k, rows, DQK, 16, true) ||
+      !make_tma_map_rows3d(&vm, pool.v, rows, DV, 16, true))
+    return cudaErrorInvalidValue;
   static_assert((WIN + 16) / 16 == FDW_SUBS, "split length of the window below: at most FDW_SUBS subtiles");
   full_decode_kernel<true><<<(unsigned)grid, FD_WARPS * 32, FDW_SMEM, st>>>(
-      q, pos, seq, B, hq, G, pool, table, max_pos, softmax_scale * LOG2E, max_ctx, nullptr, WIN + 16, nullptr,
+      km, vm, q, pos, seq, B, hq, G, pool, table, max_pos, softmax_scale * LOG2E, max_ctx, nullptr, WIN + 16, nullptr,
       nullptr, status, WIN, sinks, out);
   return cudaGetLastError();
 }

@@ -62,6 +62,17 @@ __device__ __forceinline__ void load_q_frags(const uint8_t *sQ, int lane, uint32
 
 // S[16 x 16 keys] = Q K^T for the 16 K rows starting at row r0 of a swizzled
 // [*][192] tile (chunk swizzle of swz<DQK>).
+// Byte offset of 16-byte chunk ch of row r of a 16-row subtile: the
+// XOR-swizzled [16][ROW_ELEMS] tile of the cp.async path, or (PARTED) the
+// [ROW_ELEMS / 64][16][128 B] tile that one-part TMA boxes of 16 rows write
+// with the 128-byte swizzle, 2048 bytes per 64-element part.
+template <int ROW_ELEMS, bool PARTED>
+__device__ __forceinline__ uint32_t sub_off(int r, int ch) {
+  if (PARTED) return (uint32_t)((ch >> 3) * 2048) + swrow<1>(r, ch & 7);
+  return swz<ROW_ELEMS>(r, ch);
+}
+
+template <bool PARTED = false>
 __device__ __forceinline__ void qk_16keys(const uint32_t (&qf)[12][4], uint32_t kbase, int r0, int lane,
                                           float (&S)[2][4]) {
 #pragma unroll
@@ -73,7 +84,7 @@ __device__ __forceinline__ void qk_16keys(const uint32_t (&qf)[12][4], uint32_t 
 #pragma unroll
   for (int kk = 0; kk < 12; ++kk) {
     uint32_t b0, b1, b2, b3;
-    ldsm_x4(kbase + swz<DQK>(row, 2 * kk + csel), b0, b1, b2, b3);
+    ldsm_x4(kbase + sub_off<DQK, PARTED>(row, 2 * kk + csel), b0, b1, b2, b3);
     mma_bf16(S[0], qf[kk], b0, b1);
     mma_bf16(S[1], qf[kk], b2, b3);
   }
@@ -81,6 +92,7 @@ __device__ __forceinline__ void qk_16keys(const uint32_t (&qf)[12][4], uint32_t 
 
 // O[16 x 128] += P[16 x 16 keys] V[16 keys x 128] for the V rows starting at
 // row r0 of a swizzled [*][128] tile; P comes from the S accumulators.
+template <bool PARTED = false>
 __device__ __forceinline__ void pv_16keys(const float (&P)[2][4], uint32_t vbase, int r0, int lane,
                                           float (&O)[16][4]) {
   uint32_t a[4];
@@ -93,7 +105,7 @@ __device__ __forceinline__ void pv_16keys(const float (&P)[2][4], uint32_t vbase
 #pragma unroll
   for (int dp = 0; dp < 8; ++dp) {
     uint32_t b0, b1, b2, b3;
-    ldsm_x4_t(vbase + swz<DV>(row, 2 * dp + csel), b0, b1, b2, b3);
+    ldsm_x4_t(vbase + sub_off<DV, PARTED>(row, 2 * dp + csel), b0, b1, b2, b3);
     mma_bf16(O[2 * dp], a, b0, b1);
     mma_bf16(O[2 * dp + 1], a, b2, b3);
   }
