@@ -480,7 +480,7 @@ __global__ void __launch_bounds__(FD_WARPS * 32, 2)
       }
     };
 
-    // Windowed layer: the warp's subtiles by TMA, one-part boxes of 16 rows
+    // Windowed layer: the warp's subtiles by TMA, one box of 16 rows each for K and V
     // (a 16-key subtile never straddles a block), each completing on its
     // stage's barrier; rows outside the window arrive too (zeroed or masked
     // below).  A bad block id: no load, the barrier completes at once and the
@@ -493,11 +493,8 @@ __global__ void __launch_bounds__(FD_WARPS * 32, 2)
       if (blk >= 0 && blk < pool.num_blocks) {
         const int hrow = (int)(((long long)blk * hkv + kv) * bsz + key0 % bsz);
         tc::mbar_expect_tx_elect(bar, FD_STAGE);
-#pragma unroll
-        for (int part = 0; part < 3; ++part) tc::tma_load_3d_elect(dst + part * 2048, &kmap, 0, part, hrow, bar);
-#pragma unroll
-        for (int part = 0; part < 2; ++part)
-          tc::tma_load_3d_elect(dst + FD_SUB_K + part * 2048, &vmap, 0, part, hrow, bar);
+        tc::tma_load_3d_elect(dst, &kmap, 0, 0, hrow, bar);
+        tc::tma_load_3d_elect(dst + FD_SUB_K, &vmap, 0, 0, hrow, bar);
       } else if (lane == 0) {
         flag(status, ST_BAD_BLOCK);
         tc::mbar_arrive(bar);
@@ -907,6 +904,8 @@ cudaError_t launch_full_decode(const uint16_t *q, const int64_t *pos, const int3
 cudaError_t launch_swa_decode_paged(const uint16_t *q, const int64_t *pos, const int32_t *seq, int B, int hq,
                                     const KvView &pool, const float *sinks, const float *table, int64_t max_pos,
                                     float softmax_scale, uint16_t *out, unsigned *status, cudaStream_t st) {
+  if (hq / pool.hkv <= 8)  // groups of up to 8 q heads: the keys-as-rows kernel (swa_paged.cu)
+    return launch_swa_paged(q, pos, seq, B, hq, pool, sinks, table, max_pos, softmax_scale, out, status, st);
   cudaError_t e = ensure_smem_limit(9, (const void *)full_decode_kernel<true>, FDW_SMEM);
   if (e != cudaSuccess) return e;
   const int hkv = pool.hkv, G = hq / hkv;
@@ -916,11 +915,11 @@ cudaError_t launch_swa_decode_paged(const uint16_t *q, const int64_t *pos, const
   const long long items = (long long)B * hkv;
   long long grid = (long long)num_sms() * 2;
   if (grid > items) grid = items;
-  // the pool as rows of 64-element parts, boxes of one part x 16 rows
+  // the pool as rows of 64-element parts, boxes of all parts x 16 rows
   const long long rows = (long long)pool.num_blocks * hkv * pool.block_size;
   CUtensorMap km, vm;
-  if (rows > 0x7fffffffLL || !make_tma_map_rows3d(&km, pool.k, rows, DQK, 16, true) ||
-      !make_tma_map_rows3d(&vm, pool.v, rows, DV, 16, true))
+  if (rows > 0x7fffffffLL || !make_tma_map_rows3d(&km, pool.k, rows, DQK, 16) ||
+      !make_tma_map_rows3d(&vm, pool.v, rows, DV, 16))
     return cudaErrorInvalidValue;
   static_assert((WIN + 16) / 16 == FDW_SUBS, "split length of the window below: at most FDW_SUBS subtiles");
   full_decode_kernel<true><<<(unsigned)grid, FD_WARPS * 32, FDW_SMEM, st>>>(

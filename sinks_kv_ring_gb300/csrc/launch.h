@@ -42,11 +42,16 @@ cudaError_t launch_swa_decode(const uint16_t *q, const int64_t *pos, const int32
                               int64_t max_pos, float softmax_scale, uint16_t *out, unsigned *status,
                               cudaStream_t st);
 
-// Windowed decode over a PAGED layout: the split decode kernel with the key
+// Windowed decode over a PAGED layout: groups of up to 8 q heads per KV head
+// go to launch_swa_paged; larger ones run the split decode kernel with the key
 // range p-127..p, one split, the sink in the final normalisation.
 cudaError_t launch_swa_decode_paged(const uint16_t *q, const int64_t *pos, const int32_t *seq, int B, int hq,
                                     const KvView &pool, const float *sinks, const float *table, int64_t max_pos,
                                     float softmax_scale, uint16_t *out, unsigned *status, cudaStream_t st);
+// the same for G <= 8 q heads per KV head (swa_paged.cu: keys as the MMA rows)
+cudaError_t launch_swa_paged(const uint16_t *q, const int64_t *pos, const int32_t *seq, int B, int hq,
+                             const KvView &pool, const float *sinks, const float *table, int64_t max_pos,
+                             float softmax_scale, uint16_t *out, unsigned *status, cudaStream_t st);
 
 // Split plan of the full-attention decode: contexts up to max_ctx are cut
 // into at most `splits` pieces of `split_len` keys (a multiple of 64).

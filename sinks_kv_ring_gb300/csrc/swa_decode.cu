@@ -116,17 +116,6 @@ __device__ __forceinline__ void prefetch_tmap(const void *map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
 }
 
-// Bulk copy of `bytes` (a multiple of 16, both addresses 16-byte aligned)
-// from global to shared memory, completing on `bar`; one elected lane of a
-// converged warp issues it.
-__device__ __forceinline__ void bulk_load_elect(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
-  asm volatile(
-      "{\n.reg .pred e;\nelect.sync _|e, 0xffffffff;\n"
-      "@e cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n}\n" ::"r"(dst),
-      "l"(src), "r"(bytes), "r"(bar)
-      : "memory");
-}
-
 // Transpose of an 8x8 bf16 block held as m16n8 accumulator pairs: thread t
 // holds row t/4, columns 2(t%4), 2(t%4)+1 before and after.
 __device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {

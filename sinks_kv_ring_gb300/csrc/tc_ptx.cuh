@@ -173,6 +173,15 @@ __device__ __forceinline__ void tma_load_2d_elect(uint32_t dst, const void *map,
       ::"r"(dst), "l"(map), "r"(x), "r"(y), "r"(bar)
       : "memory");
 }
+// Untiled bulk copy global -> shared of `bytes` (a multiple of 16, both
+// addresses 16-byte aligned), completing on mbarrier `bar`; one elected lane.
+__device__ __forceinline__ void bulk_load_elect(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
+  asm volatile(
+      "{\n.reg .pred e;\nelect.sync _|e, 0xffffffff;\n"
+      "@e cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n}\n" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
 __device__ __forceinline__ void mbar_expect_tx_elect(uint32_t bar, uint32_t bytes) {
   asm volatile(
       "{\n.reg .pred e;\n.reg .b64 st;\nelect.sync _|e, 0xffffffff;\n"

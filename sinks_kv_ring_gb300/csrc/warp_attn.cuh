@@ -64,11 +64,12 @@ __device__ __forceinline__ void load_q_frags(const uint8_t *sQ, int lane, uint32
 // [*][192] tile (chunk swizzle of swz<DQK>).
 // Byte offset of 16-byte chunk ch of row r of a 16-row subtile: the
 // XOR-swizzled [16][ROW_ELEMS] tile of the cp.async path, or (PARTED) the
-// [ROW_ELEMS / 64][16][128 B] tile that one-part TMA boxes of 16 rows write
-// with the 128-byte swizzle, 2048 bytes per 64-element part.
+// [16][ROW_ELEMS / 64][128 B] tile that a TMA box of all parts x 16 rows
+// writes with the 128-byte swizzle (conflict-free ldmatrix for 3 parts, 2-way
+// for 2).
 template <int ROW_ELEMS, bool PARTED>
 __device__ __forceinline__ uint32_t sub_off(int r, int ch) {
-  if (PARTED) return (uint32_t)((ch >> 3) * 2048) + swrow<1>(r, ch & 7);
+  if (PARTED) return swrow<ROW_ELEMS / 64>(r, ch);
   return swz<ROW_ELEMS>(r, ch);
 }
 
