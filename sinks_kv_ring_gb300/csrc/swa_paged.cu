@@ -98,18 +98,24 @@ __device__ __forceinline__ void load_qt_frags(const uint8_t *sQ, int lane, uint3
     ldsm_x4(base + (2 * kk + (lane >> 3)) * 16, qf[kk][0], qf[kk][1], qf[kk + 1][0], qf[kk + 1][1]);
 }
 
-// Rotate dims 0..63 of rows 0..G-1 of the plain query tile in place and round
-// to bf16: thread i < 4G takes row i/4, chunk pair (i%4, i%4 + 4); cs is the
-// table row ([32][2] fp32).
-__device__ __forceinline__ void rotate_q_rows(uint8_t *sQ, const float *cs, int G, int i) {
-  if (i >= 4 * G) return;
-  const int r = i >> 2, c = i & 3;
-  uint4 *p1 = reinterpret_cast<uint4 *>(sQ + r * DQK * 2 + c * 16);
-  uint4 *p2 = reinterpret_cast<uint4 *>(sQ + r * DQK * 2 + (c + 4) * 16);
-  uint4 o1, o2;
-  rope_pair8(*p1, *p2, cs + 16 * c, o1, o2);
-  *p1 = o1;
-  *p2 = o2;
+// Rotate-half RoPE of dims 0..63 on the Q^T B fragments in registers: dims d
+// and d + 32 (d < 32) sit in k-steps kk and kk + 2 of the same lane; cs is the
+// table row ([32][2] fp32, (cos, sin) per frequency); the results are rounded
+// to bf16, as a rotated query tile would be.
+__device__ __forceinline__ void rope_qt_frags(uint32_t (&qf)[12][2], const float *cs, int lane) {
+  const int t = lane & 3;
+#pragma unroll
+  for (int kk = 0; kk < 2; ++kk)
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      const int d = 16 * kk + 8 * r + 2 * t;
+      const float4 c = *reinterpret_cast<const float4 *>(cs + 2 * d);  // (cos, sin) of d and d + 1
+      const uint32_t x1 = qf[kk][r], x2 = qf[kk + 2][r];
+      const float u0 = bf2f((uint16_t)(x1 & 0xffffu)), u1 = bf2f((uint16_t)(x1 >> 16));
+      const float v0 = bf2f((uint16_t)(x2 & 0xffffu)), v1 = bf2f((uint16_t)(x2 >> 16));
+      qf[kk][r] = pack_bf16(u0 * c.x - v0 * c.y, u1 * c.z - v1 * c.w);
+      qf[kk + 2][r] = pack_bf16(v0 * c.x + u0 * c.y, v1 * c.z + u1 * c.w);
+    }
 }
 
 // S^T[16 keys x 8 heads] = K Q^T for a TMA-written K subtile ([16][3][128 B]).
@@ -182,9 +188,33 @@ __global__ void __launch_bounds__(SP_THREADS, 1)
       asm volatile("prefetch.tensormap [%0];" ::"l"(&kmap) : "memory");
       asm volatile("prefetch.tensormap [%0];" ::"l"(&vmap) : "memory");
     }
+    // an item's metadata is loaded one item ahead: its position and sequence
+    // id at the top of the previous iteration, its block ids (lane i: the
+    // window's i-th block) at that iteration's end, so both are in when the
+    // set frees up
+    long long p_n = 0;
+    int s_n = 0, blk_n = -1;
+    auto load_ps = [&](long long wn) {
+      if (wn < nitems) {
+        p_n = pos[wn / hkv];
+        s_n = seq[wn / hkv];
+      }
+    };
+    auto load_ids = [&]() {
+      blk_n = -1;
+      if (p_n >= 0 && p_n < max_pos && p_n + 1 <= max_ctx && s_n >= 0 && s_n < pool.num_seqs) {
+        const long long b0n = (max(0LL, p_n - WIN + 1) & ~15LL) / bsz;
+        if (lane < p_n / bsz - b0n + 1) blk_n = pool.block_table[(long long)s_n * pool.max_blocks + b0n + lane];
+      }
+    };
+    load_ps(blockIdx.x);
+    load_ids();
     int k = 0;  // items issued
     for (long long w = blockIdx.x; w < nitems; w += gridDim.x, ++k) {
       const int set = k & 1;
+      const long long p = p_n;
+      const int s = s_n, blk_l = blk_n;
+      load_ps(w + gridDim.x);
       // The set is free once every consumer warp is done with item k - 2.
       // The producer warps then agree to go on (or all stop); the barrier
       // also puts every producer's arrivals for earlier items before warp
@@ -194,20 +224,15 @@ __global__ void __launch_bounds__(SP_THREADS, 1)
       if (k >= 2) ok = __all_sync(0xffffffffu, tc::mbar_wait(empty0 + 8 * set, ((k >> 1) - 1) & 1u, abort_flag));
       if (!tc::named_bar_and(9, SP_PWARPS * 32, ok)) break;
       const int b = (int)(w / hkv), kv = (int)(w % hkv);
-      const long long p = pos[b];
-      const int s = seq[b];
       const unsigned bad = (p < 0 || p >= max_pos || p + 1 > max_ctx ? ST_BAD_POS : 0u) |
                            (s < 0 || s >= pool.num_seqs ? ST_BAD_SEQ : 0u);
-      int nsub = 0, blk_l = -1;
+      int nsub = 0;
       long long key_lo = 0, b0 = 0;
       if (!bad) {
         key_lo = max(0LL, p - WIN + 1) & ~15LL;
         nsub = (int)((p + 1 - key_lo + 15) / 16);
         b0 = key_lo / bsz;
-        if (lane < p / bsz - b0 + 1) {
-          blk_l = pool.block_table[(long long)s * pool.max_blocks + b0 + lane];
-          if (pw == 0) sNB[set * SP_NB + lane] = blk_l;
-        }
+        if (pw == 0 && lane < p / bsz - b0 + 1) sNB[set * SP_NB + lane] = blk_l;
       }
       if (pw == 0) {
         if (lane == 0) {
@@ -251,6 +276,7 @@ __global__ void __launch_bounds__(SP_THREADS, 1)
           tc::mbar_arrive(fb);
         }
       }
+      load_ids();
     }
     // before leaving, wait (bounded, whatever the abort flag says) for the
     // loads of the last item issued into each set
@@ -294,11 +320,9 @@ __global__ void __launch_bounds__(SP_THREADS, 1)
     const long long key_min = max(0LL, p - WIN + 1);
     const long long key_lo = key_min & ~15LL, key_hi = p + 1, b0 = key_lo / bsz;
     const int nsub = (int)((key_hi - key_lo + 15) / 16);
-    uint8_t *sQ = smem + SP_OFF_Q + set * SP_QTILE;
-    rotate_q_rows(sQ, reinterpret_cast<const float *>(smem + SP_OFF_CS + set * 256), G, ltid);
-    tc::named_bar_sync(bar0 + 1, SP_GTHREADS);
     uint32_t qf[12][2];
-    load_qt_frags(sQ, lane, qf);
+    load_qt_frags(smem + SP_OFF_Q + set * SP_QTILE, lane, qf);
+    rope_qt_frags(qf, reinterpret_cast<const float *>(smem + SP_OFF_CS + set * 256), lane);
     const int32_t *nb = sNB + set * SP_NB;
 
     // per thread: O^T[dims 16m + g (+8)][heads 2t, 2t+1]; (m, l) of heads 2t, 2t+1
@@ -361,8 +385,8 @@ __global__ void __launch_bounds__(SP_THREADS, 1)
       __syncwarp();
     }
     // this warp is done with the set (stages, query tile): hand it back; its
-    // generic writes there (rotation, zeroed rows) come before the next TMA
-    // writes into it
+    // generic writes there (zeroed rows) come before the next TMA writes
+    // into it
     tc::fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) tc::mbar_arrive(empty0 + 8 * set);
