@@ -590,7 +590,9 @@ def pool_ops_times(work, hbm, peaks_src, copies=None):
                         f"blocks per sequence), graph rotating over {copies} copies", "graph_ms": round(ms_dec, 5),
             "bytes": work.bytes_swa(), "GB/s": round(dec_gbs, 1),
             "roofline": with_nominal({"bound": "hbm", "achieved": round(dec_gbs, 1), "peak": hbm, "unit": "GB/s",
-                                      "frac": round(dec_gbs / hbm, 4), "peak_source": peaks_src})},
+                                      "frac": round(dec_gbs / hbm, 4), "peak_source": peaks_src,
+                                      "kernel": "swa_paged_kernel",
+                                      "traffic": kernel_traffic("swa_paged_kernel")})},
         "kv_ring_gather_pages": {
             "workload": f"{B} sequences x {hkv} KV heads: the 128-position window from pages into rings",
             "graph_ms": round(ms_gat, 5), "bytes": gat_bytes, "GB/s": round(gat_gbs, 1),
