@@ -42,6 +42,8 @@ __global__ void __launch_bounds__(APPEND_WARPS * 32)
                   const int64_t *__restrict__ pos, const int32_t *__restrict__ seq, int T, int hkv,
                   const float *__restrict__ table, int64_t max_pos, float vscale, KvView dst,
                   unsigned *status) {
+  pdl_wait();
+  pdl_trigger();
   const int lane = threadIdx.x & 31;
   const long long total = (long long)T * hkv;
   const long long base = ((long long)blockIdx.x * APPEND_WARPS + (threadIdx.x >> 5)) * APPEND_ITEMS;
@@ -136,9 +138,8 @@ cudaError_t launch_append(const uint16_t *k, const uint16_t *v, const int64_t *p
   const long long items = (long long)T * hkv;
   const long long per_block = (long long)APPEND_WARPS * APPEND_ITEMS;
   const long long blocks = (items + per_block - 1) / per_block;
-  append_kernel<<<(unsigned)blocks, APPEND_WARPS * 32, 0, st>>>(k, v, pos, seq, T, hkv, table, max_pos,
-                                                                 value_scale, dst, status);
-  return cudaGetLastError();
+  return launch_pdl(append_kernel, dim3((unsigned)blocks), dim3(APPEND_WARPS * 32), 0, st, k, v, pos, seq, T, hkv,
+                    table, max_pos, value_scale, dst, status);
 }
 
 }  // namespace kvr

@@ -24,6 +24,16 @@ constexpr unsigned ST_BAD_BLOCK = 4u;
 constexpr unsigned ST_BAD_ROWS = 16u;
 constexpr unsigned ST_FREE_FULL = 32u;
 
+// Programmatic dependent launch (kernels launched through launch_pdl).
+// pdl_wait returns once the kernel before this one on the stream has
+// completed and its writes are visible (at once for a plain launch); a kernel
+// calls it before its first global-memory access.  pdl_trigger lets a kernel
+// launched the same way after this one be scheduled as this one's CTAs leave;
+// it is called only after pdl_wait, so a dependent never runs beside this
+// kernel's own predecessor.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 __device__ __forceinline__ void flag(unsigned *status, unsigned bits) {
   if (status) atomicOr(status, bits);
 }

@@ -301,9 +301,11 @@ __global__ void __launch_bounds__(FD_WARPS * 32, 2)
                        float *__restrict__ part_ml, float *__restrict__ part_o, unsigned *status, int window,
                        const float *__restrict__ sinks, uint16_t *__restrict__ out_direct) {
   extern __shared__ __align__(128) uint8_t smem[];
-  // the merge kernel (a programmatic dependent) may be scheduled as SMs free
-  // up; it reads nothing of this kernel's before this kernel has completed
-  if (!WINDOW) asm volatile("griddepcontrol.launch_dependents;");
+  // launched as a programmatic dependent (launch_pdl); the merge kernel after
+  // it may be scheduled as its CTAs leave and reads nothing of this kernel's
+  // before this kernel has completed
+  pdl_wait();
+  pdl_trigger();
   uint8_t *sQ = smem;
   uint8_t *sCS = smem + FD_OFF_CS;
   int32_t *sNB = reinterpret_cast<int32_t *>(smem + FD_OFF_NB);
@@ -671,6 +673,8 @@ __global__ void __launch_bounds__(DP_THREADS)
     full_decode_plan_kernel(const int64_t *__restrict__ pos, const int32_t *__restrict__ seq, int B, int hkv,
                             int num_seqs, int64_t max_pos, long long max_ctx, int R, int32_t *__restrict__ plan,
                             unsigned *status) {
+  pdl_wait();
+  pdl_trigger();
   int nitems;
   const int L = decode_plan_block<DP_THREADS>(pos, seq, B, hkv, num_seqs, max_pos, max_ctx, R,
                                               plan + DPLAN_PREFIX, &nitems, status);
@@ -719,7 +723,8 @@ __global__ void __launch_bounds__(FC_WARPS * 32)
     const int s = seq[b];
     ok = p >= 0 && p < max_pos && p + 1 <= max_ctx && s >= 0 && s < num_seqs;
   }
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+  pdl_wait();
+  pdl_trigger();
   const int split_len = plan[0];
   const int n = ok ? (int)(p / split_len) + 1 : 0;
   const long long base = have ? plan[DPLAN_PREFIX + b] : 0;
@@ -869,16 +874,14 @@ cudaError_t launch_full_decode(const uint16_t *q, const int64_t *pos, const int3
   if (B <= DP_INLINE_MAX) {
     smem += ((B + 3) * 4 + 15) / 16 * 16;  // prefix[B + 1] and a split length and item count
   } else {
-    full_decode_plan_kernel<<<1, DP_THREADS, 0, st>>>(pos, seq, B, hkv, pool.num_seqs, max_pos, max_ctx, R, plan,
-                                                      status);
-    e = cudaGetLastError();
+    e = launch_pdl(full_decode_plan_kernel, dim3(1), dim3(DP_THREADS), 0, st, pos, seq, B, hkv, pool.num_seqs, max_pos,
+                   max_ctx, R, plan, status);
     if (e != cudaSuccess) return e;
   }
   const CUtensorMap unused{};  // (the full layer's subtiles go by cp.async)
-  full_decode_kernel<false><<<(unsigned)R, FD_WARPS * 32, smem, st>>>(
-      unused, unused, q, pos, seq, B, hq, G, pool, table, max_pos, softmax_scale * LOG2E, max_ctx, plan, 0, part_ml, part_o, status,
-      0, nullptr, nullptr);
-  e = cudaGetLastError();
+  e = launch_pdl(full_decode_kernel<false>, dim3((unsigned)R), dim3(FD_WARPS * 32), (size_t)smem, st, unused, unused, q,
+                 pos, seq, B, hq, G, pool, table, max_pos, softmax_scale * LOG2E, max_ctx, (const int32_t *)plan, 0,
+                 part_ml, part_o, status, 0, (const float *)nullptr, (uint16_t *)nullptr);
   if (e != cudaSuccess) return e;
   // warps per merged row: about four splits each, at most sixteen
   const DecodePlan est = full_decode_plan(B, hkv, max_ctx);
@@ -887,18 +890,9 @@ cudaError_t launch_full_decode(const uint16_t *q, const int64_t *pos, const int3
   const long long rows = (long long)B * hkv * G;
   const long long ctas = (rows + FC_WARPS / nw - 1) / (FC_WARPS / nw);
   // a programmatic dependent of the split kernel (see full_combine_kernel)
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)ctas);
-  cfg.blockDim = dim3(FC_WARPS * 32);
-  cfg.dynamicSmemBytes = 0;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, full_combine_kernel, pos, seq, B, hq, G, hkv, pool.num_seqs, max_pos, max_ctx,
-                            (const int32_t *)plan, nw, (const float *)part_ml, (const float *)part_o, out);
+  return launch_pdl(full_combine_kernel, dim3((unsigned)ctas), dim3(FC_WARPS * 32), 0, st, pos, seq, B, hq, G, hkv,
+                    pool.num_seqs, max_pos, max_ctx, (const int32_t *)plan, nw, (const float *)part_ml,
+                    (const float *)part_o, out);
 }
 
 cudaError_t launch_swa_decode_paged(const uint16_t *q, const int64_t *pos, const int32_t *seq, int B, int hq,
@@ -922,10 +916,9 @@ cudaError_t launch_swa_decode_paged(const uint16_t *q, const int64_t *pos, const
       !make_tma_map_rows3d(&vm, pool.v, rows, DV, 16))
     return cudaErrorInvalidValue;
   static_assert((WIN + 16) / 16 == FDW_SUBS, "split length of the window below: at most FDW_SUBS subtiles");
-  full_decode_kernel<true><<<(unsigned)grid, FD_WARPS * 32, FDW_SMEM, st>>>(
-      km, vm, q, pos, seq, B, hq, G, pool, table, max_pos, softmax_scale * LOG2E, max_ctx, nullptr, WIN + 16, nullptr,
-      nullptr, status, WIN, sinks, out);
-  return cudaGetLastError();
+  return launch_pdl(full_decode_kernel<true>, dim3((unsigned)grid), dim3(FD_WARPS * 32), (size_t)FDW_SMEM, st, km, vm, q,
+                    pos, seq, B, hq, G, pool, table, max_pos, softmax_scale * LOG2E, max_ctx, (const int32_t *)nullptr,
+                    WIN + 16, (float *)nullptr, (float *)nullptr, status, WIN, sinks, out);
 }
 
 }  // namespace kvr

@@ -28,6 +28,26 @@ bool make_tma_map_rows3d(CUtensorMap *m, const void *ptr, long long rows, int wi
 // `slot` is a small distinct integer per kernel.
 cudaError_t ensure_smem_limit(int slot, const void *func, int bytes);
 
+// Launch with programmatic stream serialisation: the kernel may be scheduled
+// before the work ahead of it on the stream has finished, and waits for it on
+// the device (pdl_wait) before touching global memory.  This hides the launch
+// gap between back-to-back kernels.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 // The wait limit of a launch that kvr_debug_stall_next asked to stall (one
 // taken per call), or 0 for a normal launch.
 void set_stall(int launches, unsigned long long ns);

@@ -70,6 +70,8 @@ __global__ void __launch_bounds__(RL_THREADS) pages_release_kernel(ReleaseArgs A
   __shared__ int s_cnt[RL_WARPS];
   __shared__ int s_off[RL_WARPS];
   __shared__ int s_total, s_base;
+  pdl_wait();
+  pdl_trigger();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 
   // pass 1
@@ -152,6 +154,8 @@ __global__ void __launch_bounds__(GATHER_THREADS)
     ring_gather_kernel(KvView pages, KvView ring, const int32_t *__restrict__ src_seqs,
                        const int32_t *__restrict__ dst_seqs, const int64_t *__restrict__ end, unsigned *status) {
   __shared__ long long s_row[WIN];
+  pdl_wait();
+  pdl_trigger();
   const int i = blockIdx.x, kv = blockIdx.y, hkv = ring.hkv;
   const int ss = src_seqs[i], ds = dst_seqs[i];
   if (ss < 0 || ss >= pages.num_seqs || ds < 0 || ds >= ring.num_seqs) {
@@ -216,16 +220,14 @@ cudaError_t launch_pages_release(int32_t *table, int num_seqs, int max_blocks, i
                                  cudaStream_t st) {
   ReleaseArgs A{table, num_seqs, max_blocks, block_size, num_blocks, seqs, next_pos, lo, n, window,
                 free_ids, free_count, free_cap};
-  pages_release_kernel<<<1, RL_THREADS, 0, st>>>(A, status);
-  return cudaGetLastError();
+  return launch_pdl(pages_release_kernel, dim3(1), dim3(RL_THREADS), 0, st, A, status);
 }
 
 cudaError_t launch_ring_gather(const KvView &pages, const KvView &ring, const int32_t *src_seqs,
                                const int32_t *dst_seqs, const int64_t *end, int n, unsigned *status,
                                cudaStream_t st) {
   dim3 grid((unsigned)n, (unsigned)ring.hkv);
-  ring_gather_kernel<<<grid, GATHER_THREADS, 0, st>>>(pages, ring, src_seqs, dst_seqs, end, status);
-  return cudaGetLastError();
+  return launch_pdl(ring_gather_kernel, grid, dim3(GATHER_THREADS), 0, st, pages, ring, src_seqs, dst_seqs, end, status);
 }
 
 }  // namespace kvr

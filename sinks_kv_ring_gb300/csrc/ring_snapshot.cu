@@ -26,6 +26,8 @@ __device__ __forceinline__ void copy_chunks(uint4 *__restrict__ dst, const uint4
 __global__ void __launch_bounds__(COPY_THREADS)
     ring_copy_kernel(KvView ring, const int32_t *__restrict__ seqs, uint16_t *k_snap, uint16_t *v_snap,
                      int32_t *tags_snap, int to_ring, unsigned *status) {
+  pdl_wait();
+  pdl_trigger();
   const int i = blockIdx.x, kv = blockIdx.y, hkv = ring.hkv;
   const int s = seqs[i];
   if (s < 0 || s >= ring.num_seqs) {
@@ -60,8 +62,8 @@ __global__ void __launch_bounds__(COPY_THREADS)
 cudaError_t launch_ring_copy(const KvView &ring, const int32_t *seqs, int n, uint16_t *k_snap, uint16_t *v_snap,
                              int32_t *tags_snap, bool to_ring, unsigned *status, cudaStream_t st) {
   dim3 grid((unsigned)n, (unsigned)ring.hkv);
-  ring_copy_kernel<<<grid, COPY_THREADS, 0, st>>>(ring, seqs, k_snap, v_snap, tags_snap, to_ring ? 1 : 0, status);
-  return cudaGetLastError();
+  return launch_pdl(ring_copy_kernel, grid, dim3(COPY_THREADS), 0, st, ring, seqs, k_snap, v_snap, tags_snap,
+                    to_ring ? 1 : 0, status);
 }
 
 }  // namespace kvr

@@ -160,6 +160,9 @@ __global__ void __launch_bounds__(SdLayout<NT>::THREADS, 1)
   int2 *sInfo = reinterpret_cast<int2 *>(g + L::OFF_INFO);
   volatile int *sGo = reinterpret_cast<volatile int *>(g + L::OFF_GO);
   const bool producer = warp >= NG * SD_GWARPS;
+  // Launched as a programmatic dependent (launch_pdl): the set-up below
+  // overlaps the end of the kernel before it on the stream; no global memory
+  // is touched before pdl_wait.
 
   if (tid == 0) {
     for (int pl = 0; pl < NG * R; ++pl) {
@@ -182,6 +185,7 @@ __global__ void __launch_bounds__(SdLayout<NT>::THREADS, 1)
       prefetch_tmap(&tmv);
       prefetch_tmap(&tmq);
     }
+    pdl_wait();
     // One round of independent loads for the ring rows of the CTA's units.
     for (int n = pw * 32 + lane; n < nmine && n < SD_MAX_UNITS; n += NG * 32) {
       int p;
@@ -189,6 +193,7 @@ __global__ void __launch_bounds__(SdLayout<NT>::THREADS, 1)
       sRow[n] = make_int2(row, p);
     }
   } else {
+    pdl_wait();
     // Query rows G..QROWS-1 of every entry stay zero (the loads bring G rows).
     const int per = (L::QROWS - G) * (DQK / 8);
     for (int i = tid; i < NG * per; i += NG * SD_GWARPS * 32) {
@@ -197,6 +202,7 @@ __global__ void __launch_bounds__(SdLayout<NT>::THREADS, 1)
     }
   }
   __syncthreads();
+  pdl_trigger();  // (every thread has passed pdl_wait)
 
   if (producer) {
     // ------------------------------------------------------------ producer
@@ -570,8 +576,7 @@ cudaError_t launch_nt(const CUtensorMap &mk, const CUtensorMap &mv, const CUtens
   // so that no SM is left with an extra unit at the end.
   const int per = (units + num_sms() - 1) / num_sms();
   const int grid = (units + per - 1) / per;
-  swa_decode_kernel<NT><<<grid, L::THREADS, L::SMEM, st>>>(mk, mv, mq, a);
-  return cudaGetLastError();
+  return launch_pdl(swa_decode_kernel<NT>, dim3((unsigned)grid), dim3(L::THREADS), (size_t)L::SMEM, st, mk, mv, mq, a);
 }
 
 }  // namespace

@@ -177,7 +177,11 @@ __global__ void __launch_bounds__(SP_THREADS, 1)
   for (int e = tid; e < 2 * SP_QTILE / 16; e += SP_THREADS)
     *reinterpret_cast<uint4 *>(smem + SP_OFF_Q + 16 * e) = make_uint4(0, 0, 0, 0);
   tc::fence_proxy_async_smem();  // the zeroing before the bulk copies into the same tiles
+  // launched as a programmatic dependent (launch_pdl): the set-up above
+  // overlaps the end of the kernel before it; nothing global before pdl_wait
+  pdl_wait();
   __syncthreads();
+  pdl_trigger();
 
   if (warp >= SP_CWARPS) {
     // ---------------------------------------------------------- producers
@@ -473,9 +477,8 @@ cudaError_t launch_swa_paged(const uint16_t *q, const int64_t *pos, const int32_
   const long long items = (long long)B * hkv;
   long long grid = (long long)num_sms();
   if (grid > items) grid = items;
-  swa_paged_kernel<<<(unsigned)grid, SP_THREADS, SP_SMEM, st>>>(km, vm, q, pos, seq, B, hq, G, pool, table, max_pos,
-                                                                softmax_scale * LOG2E, max_ctx, status, sinks, out);
-  return cudaGetLastError();
+  return launch_pdl(swa_paged_kernel, dim3((unsigned)grid), dim3(SP_THREADS), (size_t)SP_SMEM, st, km, vm, q, pos, seq, B,
+                    hq, G, pool, table, max_pos, softmax_scale * LOG2E, max_ctx, status, sinks, out);
 }
 
 }  // namespace kvr

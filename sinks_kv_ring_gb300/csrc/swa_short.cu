@@ -140,6 +140,10 @@ __global__ void __launch_bounds__(SS_THREADS, SS_CTAS)
                      const __grid_constant__ CUtensorMap tdk, const __grid_constant__ CUtensorMap tdv,
                      const SsArgs a) {
   extern __shared__ uint8_t smem_raw[];
+  // launched as a programmatic dependent (launch_pdl): the plan it reads is
+  // the kernel before it's output
+  pdl_wait();
+  pdl_trigger();
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t *g = smem_raw + (base - raw);
@@ -430,8 +434,7 @@ cudaError_t launch_swa_short(const uint16_t *q, const VarlenPlan &plan, int n, l
   long long units = (long long)n * hkv;
   int grid = SS_CTAS * num_sms();
   if (grid > units) grid = (int)units;
-  swa_short_kernel<<<grid, SS_THREADS, SS_SMEM, st>>>(mk, mv, dk, dv, a);
-  return cudaGetLastError();
+  return launch_pdl(swa_short_kernel, dim3((unsigned)grid), dim3(SS_THREADS), (size_t)SS_SMEM, st, mk, mv, dk, dv, a);
 }
 
 }  // namespace kvr

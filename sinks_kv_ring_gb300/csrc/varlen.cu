@@ -34,6 +34,8 @@ struct PlanArgs {
 __global__ void __launch_bounds__(PLAN_THREADS) varlen_plan_kernel(const PlanArgs a) {
   __shared__ int wsum[32][3];
   __shared__ int carry[3];
+  pdl_wait();
+  pdl_trigger();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (tid == 0) carry[0] = carry[1] = carry[2] = 0;
   __syncthreads();
@@ -127,6 +129,8 @@ struct CombineArgs {
 // by log-sum-exp (Xiaomi "Full-Pipeline Inference Optimization", section 1.2,
 // split decode) and write the normalised bf16 row.  Lane = 4 value dims.
 __global__ void __launch_bounds__(256) varlen_combine_kernel(const CombineArgs a) {
+  pdl_wait();
+  pdl_trigger();
   const long long r = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   const int total = a.p.prow_prefix[a.p.n];
@@ -244,8 +248,7 @@ cudaError_t launch_varlen_plan(const VarlenPlan &p, long long T, int hq, int hkv
   a.short_rows = short_rows;
   a.short_max_c = short_max_c;
   a.status = status;
-  varlen_plan_kernel<<<1, PLAN_THREADS, 0, st>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(varlen_plan_kernel, dim3(1), dim3(PLAN_THREADS), 0, st, a);
 }
 
 cudaError_t launch_varlen_combine(const VarlenPlan &p, long long prows_max, int hq, uint16_t *out, cudaStream_t st) {
@@ -254,8 +257,7 @@ cudaError_t launch_varlen_combine(const VarlenPlan &p, long long prows_max, int 
   a.p = p;
   a.hq = hq;
   a.out = out;
-  varlen_combine_kernel<<<(unsigned)((prows_max + 7) / 8), 256, 0, st>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(varlen_combine_kernel, dim3((unsigned)((prows_max + 7) / 8)), dim3(256), 0, st, a);
 }
 
 }  // namespace kvr
