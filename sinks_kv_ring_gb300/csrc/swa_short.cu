@@ -55,7 +55,8 @@ constexpr int SS_OFF_TAG = SS_OFF_Q + SS_ROWS * DQK * 2;   // [128] int32
 constexpr int SS_PROW = 192;                               // P row stride (24 chunks: the swizzle stays in the row)
 constexpr int SS_OFF_P = SS_OFF_TAG + WIN * 4;             // [16][192] bf16
 constexpr int SS_OFF_RED = SS_OFF_P + 16 * SS_PROW * 2;    // [8][16] row maxima, then [8][16] row sums
-constexpr int SS_OFF_BAR = SS_OFF_RED + 2 * SS_WARPS * 16 * 4;
+constexpr int SS_OFF_SINK = SS_OFF_RED + 2 * SS_WARPS * 16 * 4;  // [32] the rows' sinks (x log2 e)
+constexpr int SS_OFF_BAR = SS_OFF_SINK + SS_ROWS * 4;
 constexpr int SS_SMEM = SS_OFF_BAR + 8 * SS_NSTAGE + 16 + 1024;
 constexpr unsigned ST_TIMEOUT = 8u;
 
@@ -97,6 +98,7 @@ struct ShortPrefetch {
   uint4 r1, r2;
   float4 cs[4];
   int tag;
+  float sink;  // row tid's sink (x log2 e), threads 0..31
 };
 
 __device__ __forceinline__ void ss_prefetch(const SsArgs &a, const Unit &U, int tid, ShortPrefetch &pf) {
@@ -115,9 +117,11 @@ __device__ __forceinline__ void ss_prefetch(const SsArgs &a, const Unit &U, int 
 #pragma unroll
   for (int k = 0; k < 4; ++k) pf.cs[k] = rot ? tr[k] : make_float4(0.f, 0.f, 0.f, 0.f);
   pf.tag = tid < WIN ? a.slot_pos[(long long)U.seq * WIN + tid] : -1;
+  pf.sink = tid < SS_ROWS && tid < U.C * a.G ? a.sinks[U.kv * a.G + tid % a.G] * LOG2E : 0.f;
 }
 
-__device__ __forceinline__ void ss_store(const ShortPrefetch &pf, int tid, uint8_t *sQ, int32_t *sTag) {
+__device__ __forceinline__ void ss_store(const ShortPrefetch &pf, int tid, uint8_t *sQ, int32_t *sTag,
+                                         float *sSink) {
   const int r = tid >> 3, qd = tid & 7;
   *reinterpret_cast<uint4 *>(sQ + swz<DQK>(r, 8 + 2 * qd)) = pf.pass[0];
   *reinterpret_cast<uint4 *>(sQ + swz<DQK>(r, 9 + 2 * qd)) = pf.pass[1];
@@ -133,6 +137,7 @@ __device__ __forceinline__ void ss_store(const ShortPrefetch &pf, int tid, uint8
     *reinterpret_cast<uint4 *>(sQ + swz<DQK>(r, qd + 4)) = o2;
   }
   if (tid < WIN) sTag[tid] = pf.tag;
+  if (tid < SS_ROWS) sSink[tid] = pf.sink;
 }
 
 __global__ void __launch_bounds__(SS_THREADS, SS_CTAS)
@@ -162,10 +167,10 @@ __global__ void __launch_bounds__(SS_THREADS, SS_CTAS)
   uint8_t *sP = g + SS_OFF_P;
   float *sMax = reinterpret_cast<float *>(g + SS_OFF_RED);  // [8][16]
   float *sSum = sMax + SS_WARPS * 16;                      // [8][16]
+  float *sSink = reinterpret_cast<float *>(g + SS_OFF_SINK);
 
-  // Thread 0: the four boxes of unit k into stage k % 2.
-  auto issue = [&](int k) {
-    const Unit U = get_unit(a, unit_id(k));
+  // Thread 0: the four boxes of unit k (described by U) into its stage.
+  auto issue = [&](int k, const Unit &U) {
     const uint32_t bar = sBar + 8 * (k % SS_NSTAGE);
     const uint32_t dst = base + (k % SS_NSTAGE) * SS_STAGE;
     const int row = (U.seq * a.hkv + U.kv) * WIN;
@@ -175,20 +180,21 @@ __global__ void __launch_bounds__(SS_THREADS, SS_CTAS)
     tma_load_4d(dst + SS_RK + SS_RV, &tdk, 0, 0, U.kv, (int)U.c0, bar);
     tma_load_4d(dst + SS_RK + SS_RV + SS_DK, &tdv, 0, 0, U.kv, (int)U.c0, bar);
   };
+  static_assert(SS_NSTAGE == 1, "the next unit's description is carried one unit ahead");
   int issued = -1;
+  // the unit being computed; the next one's description is loaded during it
+  Unit U = get_unit(a, unit_id(0));
   if (tid == 0) {
     for (int i = 0; i < SS_NSTAGE; ++i) mbar_init(sBar + 8 * i, 1);
     *abort_flag = 0;
     fence_mbar_init();
-    for (int k = 0; k < SS_NSTAGE && k < nmine; ++k) {
-      issue(k);
-      issued = k;
-    }
+    issue(0, U);
+    issued = 0;
   }
   {
     ShortPrefetch pf;
-    ss_prefetch(a, get_unit(a, unit_id(0)), tid, pf);
-    ss_store(pf, tid, sQ, sTag);
+    ss_prefetch(a, U, tid, pf);
+    ss_store(pf, tid, sQ, sTag, sSink);
   }
   __syncthreads();
 
@@ -196,10 +202,12 @@ __global__ void __launch_bounds__(SS_THREADS, SS_CTAS)
   const int r0 = 16 * warp;  // this warp's ring slots in phase 1
   bool alive = true;
   for (int k = 0; k < nmine && alive; ++k) {
-    const Unit U = get_unit(a, unit_id(k));
     const bool has_next = k + 1 < nmine;
     ShortPrefetch nx;
-    if (has_next) ss_prefetch(a, get_unit(a, unit_id(k + 1)), tid, nx);
+    // the next unit's description: its loads go out now, its query rows and
+    // tags are fetched after the first m-tile (the description's latency
+    // hides behind that m-tile, theirs behind the rest of the unit)
+    const Unit Un = has_next ? get_unit(a, unit_id(k + 1)) : U;
     const int st = k % SS_NSTAGE;
     if (!__syncthreads_and(mbar_wait(sBar + 8 * st, (uint32_t)(k / SS_NSTAGE) & 1u, abort_flag))) {
       alive = false;
@@ -295,8 +303,7 @@ __global__ void __launch_bounds__(SS_THREADS, SS_CTAS)
       }
       __syncthreads();
       // Phase 2: M = max(sink, all keys); P = e^{s - M}; row sums.
-      const float ska = a.sinks[U.kv * G + (ra < R ? ra % G : 0)] * LOG2E;
-      const float skb = a.sinks[U.kv * G + (rb < R ? rb % G : 0)] * LOG2E;
+      const float ska = sSink[ra < R ? ra : 0], skb = sSink[rb < R ? rb : 0];
       float M0 = ska, M1 = skb;
 #pragma unroll
       for (int w = 0; w < SS_WARPS; ++w) {
@@ -378,15 +385,17 @@ __global__ void __launch_bounds__(SS_THREADS, SS_CTAS)
         }
       }
       __syncthreads();  // P and the row arrays are reused by the next m-tile
+      if (mt == 0 && has_next) ss_prefetch(a, Un, tid, nx);
     }
     // The unit is done: its query tile, tags and stage are free.
-    if (has_next) ss_store(nx, tid, sQ, sTag);
+    if (has_next) ss_store(nx, tid, sQ, sTag, sSink);
     fence_proxy_async_smem();  // zeroed V rows (generic writes) before the stage is refilled by TMA
     __syncthreads();
     if (tid == 0 && k + SS_NSTAGE < nmine) {
-      issue(k + SS_NSTAGE);
+      issue(k + SS_NSTAGE, Un);
       issued = k + SS_NSTAGE;
     }
+    U = Un;
   }
 
   if (*abort_flag) {
