@@ -21,8 +21,8 @@
 // kernel is persistent with two CTAs per SM (one 90 KB stage each), so one
 // CTA's products overlap the other's loads; the next unit's query rows and
 // slot tags are prefetched into registers.  Per m-tile, with 8 warps:
-//   1. warp w: S = Q K^T for ring slots 16w..16w+15; warp 0 also for the 16
-//      staged rows; masked per row (ring slot: tag in (P0 + i - 128, P0);
+//   1. warp w: S = Q K^T for ring slots 16w..16w+15; warps 0 and 1 also for
+//      the 16 staged rows (8 each); masked per row (ring slot: tag in (P0 + i - 128, P0);
 //      staged row d: d <= i and d < C); row maxima;
 //   2. M = max(sink, row maxima), P = e^{s - M} as bf16 in shared memory
 //      ([16][144] keys), row sums;
@@ -269,7 +269,7 @@ __global__ void __launch_bounds__(SS_THREADS, SS_CTAS)
             ldsm_x4(kb + swrow<3>(r0 + row, 2 * kk + csel), b0, b1, b2, b3);
             mma_bf16(S[j], qa, b0, b1);
             mma_bf16(S[j], qc, b2, b3);
-            if (warp == 0) {
+            if (warp == j) {  // the staged rows' two 8-row halves: warps 0 and 1
               ldsm_x4(db + swrow<3>(row, 2 * kk + csel), b0, b1, b2, b3);
               mma_bf16(D[j], qa, b0, b1);
               mma_bf16(D[j], qc, b2, b3);
@@ -288,7 +288,7 @@ __global__ void __launch_bounds__(SS_THREADS, SS_CTAS)
           const int sp = sTag[r0 + key];
           const bool ok = i >= 0 && sp >= 0 && sp < P0 && sp > pr - WIN;
           S[j][e] = ok ? S[j][e] * a.scale_log2 : NEG_INF;
-          const bool okd = warp == 0 && i >= 0 && key < U.C && key <= i;
+          const bool okd = warp == j && i >= 0 && key < U.C && key <= i;
           D[j][e] = okd ? D[j][e] * a.scale_log2 : NEG_INF;
           const float m = fmaxf(S[j][e], D[j][e]);
           if (e < 2) x0 = fmaxf(x0, m); else x1 = fmaxf(x1, m);
@@ -322,9 +322,10 @@ __global__ void __launch_bounds__(SS_THREADS, SS_CTAS)
           *reinterpret_cast<uint32_t *>(sP + swz<SS_PROW>(qr, k0 >> 3) + (k0 & 7) * 2) = pack_bf16(p0, p1);
           *reinterpret_cast<uint32_t *>(sP + swz<SS_PROW>(qr + 8, k0 >> 3) + (k0 & 7) * 2) = pack_bf16(p2, p3);
         }
-        if (warp == 0) {
+        if (warp < 2) {
 #pragma unroll
           for (int j = 0; j < 2; ++j) {
+            if (j != warp) continue;  // warp j holds the staged rows' half j
             const float p0 = ex2(D[j][0] - M0), p1 = ex2(D[j][1] - M0);
             const float p2 = ex2(D[j][2] - M1), p3 = ex2(D[j][3] - M1);
             s0 += p0 + p1;
