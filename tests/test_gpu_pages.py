@@ -103,6 +103,40 @@ def test_swa_decode_paged_matches_oracle(dist, bsz, tables):
     compare_rows(out, want, "paged swa decode")
 
 
+@pytest.mark.parametrize("bsz", [16, 64])
+@pytest.mark.parametrize("hq", [64, 128])
+def test_swa_decode_paged_many_items_per_cta(bsz, hq, tables):
+    """Many more (sequence, KV head) items than CTAs, so every CTA streams
+    five or more windows in turn: at 8 q heads per KV head through its two
+    stage sets (each reused several times, its barriers' parities
+    alternating), at 16 through the split kernel's window mode (the next
+    item's ids carried, its window prefetched); positions mixed: short
+    sequences, windows on and off 16-key boundaries.  Two calls must agree
+    bit for bit, and every row must match the oracle."""
+    rng = np.random.default_rng(6401 + bsz)
+    B = 200
+    positions = [int(x) for x in rng.integers(0, 5000, size=B)]
+    positions[:6] = [0, 5, 127, 128, 143, 144]
+    hkv, vs = 8, 0.707
+    syn = Synth(6501 + bsz, dist="shifted", device=DEV)
+    pool = _window_pool(positions, hkv, bsz, 71 + bsz)
+    seqs = list(range(1, B + 1))
+    for s, p in zip(seqs, positions):
+        _append_range(pool, syn, s, max(0, p - 127), p + 1, tables[1e4], vs)
+    q = syn.q(B, hq, hkv, seq=77)
+    sinks = syn.sinks(hq).to(DEV)
+    pos = torch.tensor(positions, dtype=torch.int64, device=DEV)
+    sq = torch.tensor(seqs, dtype=torch.int32, device=DEV)
+    out1 = kvr.swa_sink_decode(q, pos, sq, pool, sinks, tables[1e4], SCALE).clone()
+    out2 = kvr.swa_sink_decode(q, pos, sq, pool, sinks, tables[1e4], SCALE)
+    torch.cuda.synchronize()
+    assert kvr.device_status() == 0
+    assert torch.equal(out1, out2)
+    want = _oracle_swa(q, syn, hkv, seqs, positions, sinks, vs)
+    compare(out1, want, "paged swa decode, many items per CTA")
+    compare_rows(out1, want, "paged swa decode, many items per CTA")
+
+
 def test_swa_decode_paged_group_sizes(tables):
     positions = [200, 17, 128, 3000]
     for hq, hkv in [(8, 2), (16, 16), (16, 1), (24, 8), (128, 8)]:
