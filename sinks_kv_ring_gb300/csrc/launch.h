@@ -147,9 +147,11 @@ constexpr int SWA_SHORT_MAX_C = 16;  // C of a short chunk
 // 4-D tensor map over LINEAR rows [T][hkv][width] bf16 viewed as
 // [T][hkv][width/64][64]: one box brings box_rows consecutive tokens of one
 // KV head, every 64-element part (smem [token][part][64], 128-byte swizzle),
-// or with one_part a single 64-element part (smem [token][64]).
+// or with one_part a single 64-element part (smem [token][64]).  With
+// heads_per_box > 1 (rows of [T][heads][width], e.g. q) a box brings that
+// many consecutive heads of each token: smem [token][head][part][64].
 bool make_tma_map_tokens4d(CUtensorMap *m, const void *ptr, long long T, int hkv, int width, int box_rows,
-                           bool one_part = false);
+                           bool one_part = false, int heads_per_box = 1);
 
 // 3-D tensor map over [rows][hq][width] bf16 (q: width 192, out: width 128)
 // for the tensor-core kernel's query tiles: a box of 64 dims x G heads x

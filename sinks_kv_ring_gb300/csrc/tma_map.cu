@@ -53,13 +53,13 @@ bool make_tma_map_rows3d(CUtensorMap *m, const void *ptr, long long rows, int wi
 }
 
 bool make_tma_map_tokens4d(CUtensorMap *m, const void *ptr, long long T, int hkv, int width, int box_rows,
-                           bool one_part) {
+                           bool one_part, int heads_per_box) {
   EncodeTiledFn fn = encode_fn();
-  if (!fn || width % 64) return false;
+  if (!fn || width % 64 || heads_per_box < 1 || heads_per_box > hkv) return false;
   const int parts = width / 64;
   cuuint64_t dims[4] = {64, (cuuint64_t)parts, (cuuint64_t)hkv, (cuuint64_t)T};
   cuuint64_t strides[3] = {128, (cuuint64_t)width * 2, (cuuint64_t)hkv * width * 2};
-  cuuint32_t box[4] = {64, one_part ? 1u : (cuuint32_t)parts, 1, (cuuint32_t)box_rows};
+  cuuint32_t box[4] = {64, one_part ? 1u : (cuuint32_t)parts, (cuuint32_t)heads_per_box, (cuuint32_t)box_rows};
   cuuint32_t estr[4] = {1, 1, 1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(ptr), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
