@@ -19,7 +19,11 @@
  *    workspaces; the library allocates and frees nothing on the device.
  *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
  *    default stream).  Buffers must stay valid until the stream has run the
- *    work.  Calls on one stream execute in order.
+ *    work.  Calls on one stream execute in order.  The decode-path kernels
+ *    are launched with programmatic stream serialisation: one may be
+ *    scheduled while the kernel before it on the stream is still running,
+ *    but touches no global memory until that kernel has completed and its
+ *    writes are visible, so stream order holds as for a plain launch.
  *  - Arguments are validated on the host before anything is launched; a bad
  *    argument returns a negative kvr_status and launches nothing.  A launch
  *    failure returns KVR_ECUDA.  kvr_last_error() gives a message (thread
