@@ -134,8 +134,10 @@ kvr_status kvr_device_status(uint32_t *flags, int reset);
 
 /*
  * Test hook for the bounded waits (no counterpart on the pages).  The next
- * `launches` kernels started by swa_sink_decode over a RING layout or by
- * full_attn_prefill_chunk, in this process, stall on purpose: once their
+ * `launches` kernels started by swa_sink_decode (over a RING layout, or over
+ * a PAGED one with up to 8 q heads per KV head), by the short-chunk part of
+ * swa_sink_prefill_varlen or by full_attn_prefill_chunk, in this process,
+ * stall on purpose: once their
  * loads are in flight (and, for the prefill, with its tensor memory held),
  * one warp group waits on an internal barrier that nothing completes, with a
  * time limit of limit_ns nanoseconds.  When the limit passes the kernel takes

@@ -71,8 +71,9 @@ constexpr int SP_OFF_CS = SP_OFF_Q + 2 * SP_QTILE;
 constexpr int SP_OFF_NB = SP_OFF_CS + 2 * 256;
 constexpr int SP_OFF_REC = SP_OFF_NB + 2 * SP_NB * 4;
 constexpr int SP_OFF_BAR = SP_OFF_REC + 2 * 16;
-// barriers: full[set][j] (one per subtile), qbar[set], empty[set]
-constexpr int SP_NBAR = 2 * SP_SUBS + 4;
+// barriers: full[set][j] (one per subtile), qbar[set], empty[set], and one
+// nothing arrives on (the test hook's stall)
+constexpr int SP_NBAR = 2 * SP_SUBS + 5;
 constexpr int SP_OFF_ABORT = SP_OFF_BAR + 8 * SP_NBAR;
 constexpr int SP_SMEM = SP_OFF_ABORT + 16 + 1024;
 static_assert(SP_SMEM <= 232448, "one CTA per SM");
@@ -151,11 +152,13 @@ __global__ void __launch_bounds__(SP_THREADS, 1)
                      const uint16_t *__restrict__ q, const int64_t *__restrict__ pos,
                      const int32_t *__restrict__ seq, int B, int hq, int G, KvView pool,
                      const float *__restrict__ table, int64_t max_pos, float scale_log2, long long max_ctx,
-                     unsigned *status, const float *__restrict__ sinks, uint16_t *__restrict__ out) {
+                     unsigned *status, const float *__restrict__ sinks, uint16_t *__restrict__ out,
+                     unsigned long long stall_ns) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   uint8_t *smem = smem_raw + (((smem_u32(smem_raw) + 1023u) & ~1023u) - smem_u32(smem_raw));
   const uint32_t sBar = smem_u32(smem + SP_OFF_BAR);
   const uint32_t qbar0 = sBar + 8 * (2 * SP_SUBS), empty0 = qbar0 + 16;  // qbar[set], empty[set]: + 8 * set
+  const uint32_t stallBar = empty0 + 16;
   SpRec *rec = reinterpret_cast<SpRec *>(smem + SP_OFF_REC);
   int32_t *sNB = reinterpret_cast<int32_t *>(smem + SP_OFF_NB);
   volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(smem + SP_OFF_ABORT);
@@ -170,6 +173,7 @@ __global__ void __launch_bounds__(SP_THREADS, 1)
       tc::mbar_init(qbar0 + 8 * set, 1);
       tc::mbar_init(empty0 + 8 * set, SP_GWARPS);
     }
+    tc::mbar_init(stallBar, 1);
     *abort_flag = 0;
     tc::fence_mbar_init();
   }
@@ -309,6 +313,9 @@ __global__ void __launch_bounds__(SP_THREADS, 1)
     // the group's warps: the item's record is in and the previous item's
     // merge area is free; a wait that gave up stops them here
     if (!tc::named_bar_and(bar0, SP_GTHREADS, got_q && *abort_flag == 0)) break;
+    // test hook (stall_ns != 0): group 0 waits on a barrier nothing completes,
+    // with the item's loads in flight; its limit sets the abort flag
+    if (stall_ns && k == 0) tc::mbar_wait(stallBar, 0, abort_flag, stall_ns);
     const int b = (int)(w / hkv), kv = (int)(w % hkv);
     const long long p = rec[set].p;
     const unsigned bad = (unsigned)rec[set].pad;
@@ -478,7 +485,7 @@ cudaError_t launch_swa_paged(const uint16_t *q, const int64_t *pos, const int32_
   long long grid = (long long)num_sms();
   if (grid > items) grid = items;
   return launch_pdl(swa_paged_kernel, dim3((unsigned)grid), dim3(SP_THREADS), (size_t)SP_SMEM, st, km, vm, q, pos, seq, B,
-                    hq, G, pool, table, max_pos, softmax_scale * LOG2E, max_ctx, status, sinks, out);
+                    hq, G, pool, table, max_pos, softmax_scale * LOG2E, max_ctx, status, sinks, out, take_stall());
 }
 
 }  // namespace kvr

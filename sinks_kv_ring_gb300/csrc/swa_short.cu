@@ -66,11 +66,12 @@ constexpr int SS_OFF_CS = SS_OFF_Q + SS_ROWS * DQK * 2;
 constexpr int SS_OFF_TAG = SS_OFF_CS + SS_DRAFT * 256;
 constexpr int SS_SET = (SS_OFF_TAG + WIN * 4 + 1023) / 1024 * 1024;
 // after the two sets: per set the unit record and its rows' sinks (x log2 e),
-// then the barriers (kv[2], q[2], free[2]) and the abort flag
+// then the barriers (kv[2], q[2], free[2], one nothing arrives on: the test
+// hook's stall) and the abort flag
 constexpr int SS_OFF_REC = 2 * SS_SET;
 constexpr int SS_OFF_SINK = SS_OFF_REC + 2 * 32;
 constexpr int SS_OFF_BAR = SS_OFF_SINK + 2 * SS_ROWS * 4;
-constexpr int SS_OFF_ABORT = SS_OFF_BAR + 6 * 8;
+constexpr int SS_OFF_ABORT = SS_OFF_BAR + 7 * 8;
 constexpr int SS_SMEM = SS_OFF_ABORT + 16 + 1024;
 static_assert(SS_SMEM <= 232448, "one CTA per SM");
 static_assert(SS_OFF_RV % 1024 == 0 && SS_OFF_DK % 1024 == 0 && SS_OFF_DV % 1024 == 0 && SS_OFF_Q % 1024 == 0,
@@ -89,6 +90,7 @@ struct SsArgs {
   int draft_rows;     // rows of one staged box (16, or T when T < 16)
   int q_tokens;       // tokens of one query box (SS_ROWS / G, at most 16, at most T)
   float scale_log2;
+  unsigned long long stall_ns;  // test hook: group 0 stalls on its first unit (0 = never)
 };
 
 // one unit as the producers find it in the plan and pass it on
@@ -203,6 +205,7 @@ __global__ void __launch_bounds__(SS_THREADS, 1)
   auto kvbar = [&](int set) -> uint32_t { return bar0 + 8 * set; };         // ring and staged K/V landed
   auto qbar = [&](int set) -> uint32_t { return bar0 + 16 + 8 * set; };     // query rows, RoPE rows, tags landed
   auto freebar = [&](int set) -> uint32_t { return bar0 + 32 + 8 * set; };  // the group has read the set
+  const uint32_t stallBar = bar0 + 48;                                      // nothing arrives on it
   volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(smem + SS_OFF_ABORT);
   SsUnit *rec = reinterpret_cast<SsUnit *>(smem + SS_OFF_REC);
   float *sSink = reinterpret_cast<float *>(smem + SS_OFF_SINK);  // [2][32]
@@ -213,6 +216,7 @@ __global__ void __launch_bounds__(SS_THREADS, 1)
       tc::mbar_init(qbar(set), 1);
       tc::mbar_init(freebar(set), SS_GWARPS);
     }
+    tc::mbar_init(stallBar, 1);
     *abort_flag = 0;
     tc::fence_mbar_init();
   }
@@ -298,6 +302,9 @@ __global__ void __launch_bounds__(SS_THREADS, 1)
     // the group's warps: the unit's record and rows are in, the previous
     // unit's reads of the set are done; a wait that gave up stops them here
     if (!tc::named_bar_and(barA, SS_GTHREADS, got_q && *abort_flag == 0)) break;
+    // test hook (stall_ns != 0): group 0 waits on a barrier nothing completes,
+    // with the unit's loads in flight; its limit sets the abort flag
+    if (a.stall_ns && k == 0) tc::mbar_wait(stallBar, 0, abort_flag, a.stall_ns);
     const SsUnit U = rec[set];
     const int R = U.C * G;
     const long long P0 = U.P0;
@@ -471,6 +478,7 @@ cudaError_t launch_swa_short(const uint16_t *q, const VarlenPlan &plan, int n, l
   a.draft_rows = draft_rows;
   a.q_tokens = q_tokens;
   a.scale_log2 = softmax_scale * LOG2E;
+  a.stall_ns = take_stall();
   const long long units = (long long)n * hkv;
   int grid = num_sms();
   if (grid > units) grid = (int)units;

@@ -1,7 +1,8 @@
 """The bounded-wait exit of the pipelined kernels, made to run on purpose.
 
-Every wait of the windowed decode and of the tensor-core prefill kernel has a
-time limit; when one runs out the kernel sets an abort flag, its other warps
+Every wait of the windowed decode kernels (over rings and over pages), of the
+short-chunk windowed kernel and of the tensor-core prefill kernel has a time
+limit; when one runs out the kernel sets an abort flag, its other warps
 leave their loops, the loads and products already issued finish, tensor
 memory is freed and the kernel returns with KVR_DEV_TIMEOUT set.  The test
 hook kvr_debug_stall_next makes one launch wait on a barrier that nothing
@@ -98,3 +99,70 @@ def test_prefill_stall_takes_the_bounded_exit():
     k, v = raw_kv(syn, hkv, 0, 0, P0 + C)
     want = oracle.attend_seq(q, np.arange(P0, P0 + C), k, v, 0, 1e7, 0.707, SCALE, 0, None)
     compare_rows(out, want, "prefill after a stalled launch")
+
+
+def test_paged_windowed_decode_stall_takes_the_bounded_exit():
+    # The windowed decode over pages (8 q heads per KV head): 40 sequences x 8
+    # KV heads = 320 windows, two or three per CTA, its producers and both
+    # consumer groups in flight when group 0 stalls.
+    B, hq, hkv = 40, 64, 8
+    positions = [300 + 7 * b for b in range(B)]
+    t4 = kvr.rope_table(1e4, 4096)
+    syn = Synth(2603, dist="plain", device=DEV)
+    pool = kvr.PagedLayout.contiguous(B, hkv, max(positions) + 1, block_size=64)
+    fill_paged(pool, syn, list(range(B)), [p + 1 for p in positions], t4, 0.707)
+    q = syn.q(B, hq, hkv, seq=998)
+    sinks = syn.sinks(hq).to(DEV)
+    pos = torch.tensor(positions, dtype=torch.int64, device=DEV)
+    seq = torch.arange(B, dtype=torch.int32, device=DEV)
+    out = torch.empty(B, hq, 128, dtype=torch.bfloat16, device=DEV)
+    dt = _stalled(lambda: kvr.swa_sink_decode(q, pos, seq, pool, sinks, t4, SCALE, out=out))
+    assert kvr.device_status() & kvr.DEV_TIMEOUT
+    assert dt < 5.0, f"the stalled call took {dt:.2f} s"
+    out = kvr.swa_sink_decode(q, pos, seq, pool, sinks, t4, SCALE)
+    torch.cuda.synchronize()
+    assert kvr.device_status() == 0
+    want = np.zeros((B, hq, 128))
+    sk = sinks.double().cpu().numpy()
+    for b, p in enumerate(positions):
+        k, v = raw_kv(syn, hkv, b, p - 127, p + 1)
+        want[b] = oracle.attend_seq(q[b:b + 1], [p], k, v, p - 127, 1e4, 0.707, SCALE, 128, sk)[0]
+    compare_rows(out, want, "paged windowed decode after a stalled launch")
+
+
+def test_short_chunk_windowed_stall_takes_the_bounded_exit():
+    # Draft verification of a windowed layer: 48 sequences x 3 tokens x 8 KV
+    # heads = 384 units through the short-chunk kernel, group 0 stalled.
+    n, C, hq, hkv = 48, 3, 64, 8
+    P0s = [500 + 11 * s for s in range(n)]
+    t4 = kvr.rope_table(1e4, 4096)
+    syn = Synth(2604, dist="plain", device=DEV)
+    sinks = syn.sinks(hq).to(DEV)
+    ring = kvr.RingLayout.empty(n, hkv)
+    fill_ring(ring, syn, list(range(n)), [P0 - 1 for P0 in P0s], t4, 0.707)
+    ks, vs, ps = [], [], []
+    for s, P0 in enumerate(P0s):
+        k, v = raw_kv(syn, hkv, s, P0, P0 + C)
+        ks.append(k)
+        vs.append(v)
+        ps.append(torch.arange(P0, P0 + C, dtype=torch.int64, device=DEV))
+    stage = kvr.LinearLayout.empty(n * C, hkv)
+    kvr.kv_ring_append_rope(torch.cat(ks).contiguous(), torch.cat(vs).contiguous(), torch.cat(ps), None, t4, 0.707,
+                            stage)
+    q = torch.cat([syn.q(C, hq, hkv, seq=s, start=P0) for s, P0 in enumerate(P0s)]).contiguous()
+    cu = torch.arange(0, n * C + 1, C, dtype=torch.int32, device=DEV)
+    P0 = torch.tensor(P0s, dtype=torch.int64, device=DEV)
+    sq = torch.arange(n, dtype=torch.int32, device=DEV)
+    out = torch.empty(n * C, hq, 128, dtype=torch.bfloat16, device=DEV)
+    call = lambda o=None: kvr.swa_sink_prefill_varlen(q, cu, P0, sq, stage, ring, sinks, t4, SCALE, out=o)
+    dt = _stalled(lambda: call(out))
+    assert kvr.device_status() & kvr.DEV_TIMEOUT
+    assert dt < 5.0, f"the stalled call took {dt:.2f} s"
+    out = call()
+    torch.cuda.synchronize()
+    assert kvr.device_status() == 0
+    sk = sinks.double().cpu().numpy()
+    want = np.concatenate([
+        oracle.attend_seq(q[s * C:(s + 1) * C], np.arange(P0, P0 + C), *raw_kv(syn, hkv, s, P0 - 127, P0 + C),
+                          P0 - 127, 1e4, 0.707, SCALE, 128, sk) for s, P0 in enumerate(P0s)])
+    compare_rows(out, want, "short-chunk windowed attention after a stalled launch")
