@@ -34,6 +34,23 @@ constexpr unsigned ST_FREE_FULL = 32u;
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
+// Prefetch ahead of pdl_wait.  A kernel may read, before its pdl_wait, an
+// index that the kernel ahead of it could still be writing, and use it only
+// to choose bytes to bring into L2: such a read may see an old value, which
+// costs nothing but a useless prefetch, since every value the kernel computes
+// with is read again after pdl_wait.  The early read bypasses L1 (.cg), so no
+// stale line stays there for the later one.  The prefetch itself is
+// prefetch_l2 below.
+__device__ __forceinline__ int ld_early_s32(const int32_t *p) {
+  int v;
+  asm volatile("ld.global.cg.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ long long ld_early_s64(const int64_t *p) {
+  long long v;
+  asm volatile("ld.global.cg.s64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
 __device__ __forceinline__ void flag(unsigned *status, unsigned bits) {
   if (status) atomicOr(status, bits);
 }

@@ -86,6 +86,7 @@ struct SdLayout {
 };
 
 struct SdArgs {
+  const uint16_t *k, *v;  // ring rows (for the L2 prefetch only; the loads go through the tensor maps)
   const int64_t *pos;
   const int32_t *seq;
   const int32_t *slot_pos;
@@ -110,6 +111,12 @@ __device__ __forceinline__ int unit_row(const SdArgs &a, int u, int &p32) {
   if (s < 0 || s >= a.num_seqs) return -2;
   p32 = (int)p;
   return (s * a.hkv + u % a.hkv) * WIN;
+}
+
+// The K and V rows of the unit whose first ring row is `row` into L2.
+__device__ __forceinline__ void prefetch_unit(const SdArgs &a, long long row) {
+  prefetch_l2(a.k + row * DQK, WIN * DQK * 2);
+  prefetch_l2(a.v + row * DV, WIN * DV * 2);
 }
 
 __device__ __forceinline__ void prefetch_tmap(const void *map) {
@@ -161,8 +168,8 @@ __global__ void __launch_bounds__(SdLayout<NT>::THREADS, 1)
   volatile int *sGo = reinterpret_cast<volatile int *>(g + L::OFF_GO);
   const bool producer = warp >= NG * SD_GWARPS;
   // Launched as a programmatic dependent (launch_pdl): the set-up below
-  // overlaps the end of the kernel before it on the stream; no global memory
-  // is touched before pdl_wait.
+  // overlaps the end of the kernel before it on the stream; before pdl_wait
+  // global memory is only read to choose an L2 prefetch (ld_early_s32).
 
   if (tid == 0) {
     for (int pl = 0; pl < NG * R; ++pl) {
@@ -184,6 +191,18 @@ __global__ void __launch_bounds__(SdLayout<NT>::THREADS, 1)
       prefetch_tmap(&tmk);
       prefetch_tmap(&tmv);
       prefetch_tmap(&tmq);
+    }
+    // While the kernel ahead may still run, the ring rows of group pw's first
+    // unit are requested into L2 from a sequence id read early (see
+    // ld_early_s32): the DRAM then streams across the boundary between the
+    // two kernels instead of idling through this CTA's start.  Ids outside
+    // the ring are not prefetched.  (Only the first units: a prefetch of
+    // each next unit inside the loop, which occupies the TMA unit ahead of
+    // the loads that fill the ring, made batch 256 slower, 30 -> 37 us.)
+    if (lane == 0 && pw < nmine) {
+      const int u = unit_id(pw);
+      const int s = ld_early_s32(a.seq + u / a.hkv);
+      if (s >= 0 && s < a.num_seqs) prefetch_unit(a, ((long long)s * a.hkv + u % a.hkv) * WIN);
     }
     pdl_wait();
     // One round of independent loads for the ring rows of the CTA's units.
@@ -595,6 +614,8 @@ cudaError_t launch_swa_decode(const uint16_t *q, const int64_t *pos, const int32
       !make_tma_map_rows3d(&mq, q, (long long)B * hq, DQK, G))
     return cudaErrorInvalidValue;
   SdArgs a;
+  a.k = ring.k;
+  a.v = ring.v;
   a.pos = pos;
   a.seq = seq;
   a.slot_pos = ring.slot_pos;
