@@ -229,7 +229,7 @@ unsigned char g_smem_done[MAX_DEV][MAX_KSLOT];
 void *g_smem_ctx[MAX_DEV];  // the context g_smem_done[dev] is for
 }  // namespace
 
-cudaError_t ensure_smem_limit(int slot, const void *func, int bytes) {
+cudaError_t ensure_smem_limit(int slot, const void *func, int bytes, bool max_carveout) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -242,6 +242,8 @@ cudaError_t ensure_smem_limit(int slot, const void *func, int bytes) {
   }
   if (g_smem_done[dev][slot]) return cudaSuccess;
   e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && max_carveout)
+    e = cudaFuncSetAttribute(func, cudaFuncAttributePreferredSharedMemoryCarveout, (int)cudaSharedmemCarveoutMaxShared);
   if (e == cudaSuccess) g_smem_done[dev][slot] = 1;
   return e;
 }

@@ -74,7 +74,8 @@ constexpr int DPLAN_PREFIX = 64;
 // per-sequence item prefix.  Sequences with a bad position or id get no items
 // (flagged here; the merge zeroes their rows).
 constexpr int DP_CANDS = 16;
-constexpr int DP_INLINE_MAX = 4096;  // batches the split kernel plans itself (prefix in shared memory)
+constexpr int DP_INLINE_MAX = 4096;
+constexpr int FD_EARLY_KEYS = 256;   // keys of a CTA's first item prefetched before the wait (B <= 32)  // batches the split kernel plans itself (prefix in shared memory)
 
 // The plan by one CTA of NT threads: the split length (returned), the item
 // count (*nitems) and the per-sequence item prefix (prefix[0..B]).  Flags bad
@@ -218,15 +219,15 @@ __device__ int decode_plan_block(const int64_t *__restrict__ pos, const int32_t 
 // is sequence b): warp reductions and shuffles only, no block barrier.  Ties
 // between candidates of equal cost go to the lower candidate index.  The
 // split length and the item count go to prefix[B + 1] and prefix[B + 2].
-__device__ void decode_plan_warp(const int64_t *__restrict__ pos, const int32_t *__restrict__ seq, int B, int hkv,
+// Lane b < B passes sequence b's position p and id s (the other lanes
+// anything).
+__device__ void decode_plan_warp(long long p, int s, int B, int hkv,
                                  int num_seqs, int64_t max_pos, long long max_ctx, int R, int32_t *prefix,
                                  unsigned *status) {
   constexpr unsigned FULL = 0xffffffffu;
   const int lane = threadIdx.x & 31;
   unsigned ctx = 0, bad = 0;
   if (lane < B) {
-    const long long p = pos[lane];
-    const int s = seq[lane];
     const bool bp = p < 0 || p >= max_pos || p + 1 > max_ctx, bs = s < 0 || s >= num_seqs;
     if (bp || bs)
       bad = (bp ? ST_BAD_POS : 0u) | (bs ? ST_BAD_SEQ : 0u);
@@ -301,6 +302,44 @@ __global__ void __launch_bounds__(FD_WARPS * 32, 2)
                        float *__restrict__ part_ml, float *__restrict__ part_o, unsigned *status, int window,
                        const float *__restrict__ sinks, uint16_t *__restrict__ out_direct) {
   extern __shared__ __align__(128) uint8_t smem[];
+  const int32_t *prefix = plan + DPLAN_PREFIX;
+  long long pe = 0;  // full layer, B <= 32, warp 0: lane b's early copy of pos[b] (and seq[b])
+  int se = 0;
+  if (!WINDOW && B <= 32 && threadIdx.x < 32) {
+    // Ahead of the wait for the kernel before this one (which may still
+    // run): the plan from positions and sequence ids read early (see
+    // ld_early_s32), and the first keys of this CTA's first item requested
+    // into L2, so the DRAM streams while the kernel ahead drains.  After the
+    // wait the plan is kept only if every position and id reads the same.
+    const int lane = threadIdx.x;
+    int32_t *sPrefix = reinterpret_cast<int32_t *>(smem + FD_SMEM);
+    if (lane < B) {
+      pe = ld_early_s64(pos + lane);
+      se = ld_early_s32(seq + lane);
+    }
+    decode_plan_warp(pe, se, B, pool.hkv, pool.num_seqs, max_pos, max_ctx, gridDim.x, sPrefix, nullptr);
+    __syncwarp();
+    const int L = sPrefix[B + 1];
+    if ((int)blockIdx.x < sPrefix[B + 2]) {
+      const int b = plan_find(sPrefix, B, blockIdx.x);
+      const int local = (int)blockIdx.x - sPrefix[b], split = local / pool.hkv, kv = local % pool.hkv;
+      const long long p = __shfl_sync(0xffffffffu, pe, b);  // (a sequence with items has a valid p and id)
+      const int sq = __shfl_sync(0xffffffffu, se, b), bsz = pool.block_size;
+      const long long k0 = (long long)split * L, k1 = min(k0 + min(L, FD_EARLY_KEYS), p + 1) - 1;
+      const long long blk0 = k0 / bsz;
+      if (lane <= k1 / bsz - blk0) {
+        const int blk = ld_early_s32(pool.block_table + (long long)sq * pool.max_blocks + blk0 + lane);
+        if (blk >= 0 && blk < pool.num_blocks) {
+          const long long first = (blk0 + lane) * bsz;
+          const long long r0 = max(k0, first), r1 = min(k1, first + bsz - 1);
+          const long long hrow = ((long long)blk * pool.hkv + kv) * bsz + (r0 - first);
+          prefetch_l2(pool.k + hrow * DQK, (uint32_t)(r1 - r0 + 1) * DQK * 2);
+          prefetch_l2(pool.v + hrow * DV, (uint32_t)(r1 - r0 + 1) * DV * 2);
+        }
+      }
+      if (lane == 31) prefetch_l2(q + ((long long)b * hq + (long long)kv * G) * DQK, G * DQK * 2);
+    }
+  }
   // launched as a programmatic dependent (launch_pdl); the merge kernel after
   // it may be scheduled as its CTAs leave and reads nothing of this kernel's
   // before this kernel has completed
@@ -321,7 +360,6 @@ __global__ void __launch_bounds__(FD_WARPS * 32, 2)
   // A batch of up to DP_INLINE_MAX sequences is planned by every CTA itself
   // (the same inputs give every CTA the same plan; CTA 0 stores it for the
   // merge); a larger one by full_decode_plan_kernel before this kernel.
-  const int32_t *prefix = plan + DPLAN_PREFIX;
   long long nitems = (long long)B * hkv;
   // windowed layer: bit j of ph is the parity of stage j's next phase, bit j
   // of pend marks a load into stage j not yet seen complete (this warp's
@@ -340,9 +378,21 @@ __global__ void __launch_bounds__(FD_WARPS * 32, 2)
       int32_t *sPrefix = reinterpret_cast<int32_t *>(smem + FD_SMEM);
       int n;
       if (B <= 32) {  // one warp plans, the others wait at the barrier
-        if (warp == 0)
-          decode_plan_warp(pos, seq, B, hkv, pool.num_seqs, max_pos, max_ctx, gridDim.x, sPrefix,
-                           blockIdx.x == 0 ? status : nullptr);
+        if (warp == 0) {
+          long long p = 0;
+          int sq = 0;
+          if (lane < B) {
+            p = pos[lane];
+            sq = seq[lane];
+          }
+          if (!__all_sync(0xffffffffu, p == pe && sq == se)) {
+            decode_plan_warp(p, sq, B, hkv, pool.num_seqs, max_pos, max_ctx, gridDim.x, sPrefix,
+                             blockIdx.x == 0 ? status : nullptr);
+          } else if (blockIdx.x == 0 && lane < B) {  // the early plan stands; its bad entries flagged here
+            const bool bp = p < 0 || p >= max_pos || p + 1 > max_ctx, bs = sq < 0 || sq >= pool.num_seqs;
+            if (bp || bs) flag(status, (bp ? ST_BAD_POS : 0u) | (bs ? ST_BAD_SEQ : 0u));
+          }
+        }
         __syncthreads();
         split_len = sPrefix[B + 1];
         n = sPrefix[B + 2];

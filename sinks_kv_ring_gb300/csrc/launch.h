@@ -25,8 +25,10 @@ bool make_tma_map_rows3d(CUtensorMap *m, const void *ptr, long long rows, int wi
 
 // Raise a kernel's dynamic shared-memory limit once per (kernel slot, device);
 // later launches make no attribute call (so they can sit in a stream capture).
-// `slot` is a small distinct integer per kernel.
-cudaError_t ensure_smem_limit(int slot, const void *func, int bytes);
+// `slot` is a small distinct integer per kernel.  max_carveout: also ask for
+// the largest shared-memory carveout (a kernel that fits two CTAs per SM only
+// with it).
+cudaError_t ensure_smem_limit(int slot, const void *func, int bytes, bool max_carveout = false);
 
 // Launch with programmatic stream serialisation: the kernel may be scheduled
 // before the work ahead of it on the stream has finished, and waits for it on

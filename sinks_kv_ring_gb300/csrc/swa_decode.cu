@@ -56,13 +56,15 @@ constexpr int SD_MAX_UNITS = 128;                   // units per CTA whose ring 
 constexpr unsigned ST_TIMEOUT = 8u;
 
 // Shape of the kernel for NT column tiles of 8 query heads (G <= 8 * NT):
-// NG consumer groups (each with its own producer warp), R chunks of ring per
+// NG_ consumer groups (each with its own producer warp), R chunks of ring per
 // group.  A group's ring places only ever pass between that group's units,
 // which it takes in order, so every wait on a place is for the phase right
-// after the one the group saw last.
-template <int NT>
+// after the one the group saw last.  At G <= 8 the CTA has four groups (one
+// CTA per SM) or two (two CTAs per SM; see launch_nt).
+template <int NT, int NG_>
 struct SdLayout {
-  static constexpr int NG = NT == 1 ? 4 : 2;
+  static constexpr int NG = NG_;
+  static constexpr int CTAS = NT == 1 && NG == 2 ? 2 : 1;  // resident CTAs per SM
   static constexpr int R = NT == 1 ? 3 : 6;
   static constexpr int WARPS = NG * (SD_GWARPS + 1);
   static constexpr int THREADS = WARPS * 32;
@@ -136,11 +138,11 @@ __device__ __forceinline__ float bf_hi(uint32_t x) { return __uint_as_float(x & 
 
 __device__ __forceinline__ bool in_window(int t, int p) { return t >= 0 && t <= p && t > p - WIN; }
 
-template <int NT>
-__global__ void __launch_bounds__(SdLayout<NT>::THREADS, 1)
+template <int NT, int NG_>
+__global__ void __launch_bounds__(SdLayout<NT, NG_>::THREADS, SdLayout<NT, NG_>::CTAS)
     swa_decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                       const __grid_constant__ CUtensorMap tmq, const SdArgs a) {
-  using L = SdLayout<NT>;
+  using L = SdLayout<NT, NG_>;
   constexpr int NG = L::NG, R = L::R;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -585,17 +587,16 @@ __global__ void __launch_bounds__(SdLayout<NT>::THREADS, 1)
   }
 }
 
-template <int NT>
+template <int NT, int NG>
 cudaError_t launch_nt(const CUtensorMap &mk, const CUtensorMap &mv, const CUtensorMap &mq, const SdArgs &a,
-                      int units, cudaStream_t st) {
-  using L = SdLayout<NT>;
-  cudaError_t e = ensure_smem_limit(NT == 1 ? 1 : 12, (const void *)swa_decode_kernel<NT>, L::SMEM);
+                      int units, int per, cudaStream_t st) {
+  using L = SdLayout<NT, NG>;
+  cudaError_t e = ensure_smem_limit(NT == 2 ? 12 : NG == 4 ? 1 : 14, (const void *)swa_decode_kernel<NT, NG>, L::SMEM,
+                                    L::CTAS > 1);
   if (e != cudaSuccess) return e;
-  // As few CTAs as give every CTA the same number of units (or one fewer),
-  // so that no SM is left with an extra unit at the end.
-  const int per = (units + num_sms() - 1) / num_sms();
   const int grid = (units + per - 1) / per;
-  return launch_pdl(swa_decode_kernel<NT>, dim3((unsigned)grid), dim3(L::THREADS), (size_t)L::SMEM, st, mk, mv, mq, a);
+  return launch_pdl(swa_decode_kernel<NT, NG>, dim3((unsigned)grid), dim3(L::THREADS), (size_t)L::SMEM, st, mk, mv,
+                    mq, a);
 }
 
 }  // namespace
@@ -632,7 +633,19 @@ cudaError_t launch_swa_decode(const uint16_t *q, const int64_t *pos, const int32
   a.scale_log2 = softmax_scale * LOG2E;
   a.stall_ns = take_stall();
   const int units = B * hkv;
-  return G <= 8 ? launch_nt<1>(mk, mv, mq, a, units, st) : launch_nt<2>(mk, mv, mq, a, units, st);
+  // Units per CTA: as few CTAs as give every CTA the same number of units
+  // (or one fewer), so that no SM is left with an extra unit at the end.
+  const int sms = num_sms();
+  const int per1 = (units + sms - 1) / sms, per2 = (units + 2 * sms - 1) / (2 * sms);
+  if (G > 8) return launch_nt<2, 2>(mk, mv, mq, a, units, per1, st);
+  // G <= 8: two CTAs of two groups per SM when each CTA then has an even
+  // number of units (both of its groups equally loaded) and no SM more units
+  // than with one CTA of four groups; the next launch's CTAs can then start
+  // on an SM beside this one's last.  (Batch 64 over 8 KV heads: 8.7 -> 8.5
+  // us in graph replay; batch 96, three units per CTA: 12.1 -> 12.6 us, so
+  // not there.)
+  if (per2 % 2 == 0 && 2 * per2 <= per1) return launch_nt<1, 2>(mk, mv, mq, a, units, per2, st);
+  return launch_nt<1, 4>(mk, mv, mq, a, units, per1, st);
 }
 
 }  // namespace kvr

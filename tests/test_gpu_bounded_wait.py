@@ -53,8 +53,9 @@ def _stalled(call):
         kvr.debug_stall_next(0, 1000)
 
 
-def test_windowed_decode_stall_takes_the_bounded_exit():
-    B, hq, hkv = 40, 64, 8
+@pytest.mark.parametrize("B", [40, 64])  # 64 x 8 KV heads: two CTAs of two groups per SM
+def test_windowed_decode_stall_takes_the_bounded_exit(B):
+    hq, hkv = 64, 8
     positions = [300 + 7 * b for b in range(B)]
     t4 = kvr.rope_table(1e4, 4096)
     syn = Synth(2601, dist="plain", device=DEV)

@@ -141,12 +141,14 @@ def test_swa_decode_ragged_ring_fill(dist, tables):
     assert kvr.device_status() == 0
 
 
-@pytest.mark.parametrize("hq", [64, 128])
-def test_swa_decode_many_units_per_cta(hq, tables):
+@pytest.mark.parametrize("B,hq", [(240, 64), (240, 128), (64, 64), (70, 64)])
+def test_swa_decode_many_units_per_cta(B, hq, tables):
     """A batch of 240 sequences puts 12-13 (sequence, KV head) units on every
-    CTA, so the kernel's two consumer groups run many units each and can
-    drift apart: every row against the oracle, and three calls bit-equal."""
-    B, hkv = 240, 8
+    CTA, so the kernel's consumer groups run many units each and can drift
+    apart; 64 and 70 sequences over 8 KV heads take the layout of two CTAs of
+    two groups per SM (two units per CTA): every row against the oracle, and
+    three calls bit-equal."""
+    hkv = 8
     positions = [(b * 977) % 5000 for b in range(B)]  # includes p < 127 (partly filled rings)
     syn = Synth(2111 + hq, dist="plain", device=DEV)
     ring = kvr.RingLayout.empty(B, hkv)
