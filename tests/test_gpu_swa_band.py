@@ -82,6 +82,9 @@ def _stage_for(syn, hkv, P0, C, table, vscale, extra=64):
     (8, 1, 400, 90, 0),       # one KV head
     # many items per CTA: bands slide along the ring, ranges cross KV heads
     (64, 8, 1000, 4096, 0),   # 2048 items
+    (64, 8, 50, 4096, 0),     # 13-14 items per CTA, the window reaches below position 0
+    (64, 8, 1000, 2500, 40),  # 8-9 items per CTA, the 40 oldest ring slots stale
+    (64, 8, 130, 3035, 3),    # 10 items per CTA, the last tile 11 rows
     (128, 8, 300, 2000, 5),   # G = 16: the band moves every other item
     (64, 4, 60, 3000, 0),     # G = 16, the window reaches below position 0
 ])
@@ -101,6 +104,26 @@ def test_swa_band_prefill_matches_oracle(hq, hkv, P0, C, stale, table):
                              sinks.double().cpu().numpy())
     compare(out, want, "band prefill")
     compare_rows_vec(out, want, "band prefill")
+
+
+def test_swa_band_prefill_ring_bands_repeat_bit_for_bit():
+    # 27 items per CTA, as in the 8192-row chunk: three calls agree bit for
+    # bit, and every row against the oracle.
+    hq, hkv, P0, C = 64, 8, 700, 8192
+    table = kvr.rope_table(1e4, P0 + C)
+    syn = Synth(4150, dist="plain", device=DEV)
+    sinks = syn.sinks(hq).to(DEV)
+    ring = _ring_for(syn, hkv, P0, table, 0.707)
+    stage = _stage_for(syn, hkv, P0, C, table, 0.707)
+    q = syn.q(C, hq, hkv, seq=1, start=P0)
+    outs = [kvr.swa_sink_prefill_chunk(q, P0, 1, stage, ring, sinks, table, SCALE) for _ in range(3)]
+    torch.cuda.synchronize()
+    assert kvr.device_status() == 0
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2])
+    k, v = raw_kv(syn, hkv, 1, P0 - 128, P0 + C)
+    want = oracle.attend_seq(q, np.arange(P0, P0 + C), k, v, P0 - 128, 1e4, 0.707, SCALE, 128,
+                             sinks.double().cpu().numpy())
+    compare_rows_vec(outs[0], want, "band prefill, 27-tile runs")
 
 
 def test_swa_band_prefill_shifted_logits(table):
