@@ -718,9 +718,17 @@ def cpu_baseline_decode(work, budget_s=12.0, max_seqs=16):
         oracle.attend_seq(q_s[b:b + 1], [p], ks, vs, lo, 1e4, work.vscale, SCALE, 128, sk, nthreads=cores)
         elapsed += time.perf_counter() - t0
         done += 1
+    # the same on one thread, one sequence-step
+    kf, vf, ks, vs = inputs(0)
+    t0 = time.perf_counter()
+    oracle.attend_seq(q_f[0:1], [p], kf, vf, 0, 1e7, work.vscale, SCALE, 0, None, nthreads=1)
+    oracle.attend_seq(q_s[0:1], [p], ks, vs, lo, 1e4, work.vscale, SCALE, 128, sk, nthreads=1)
+    one = time.perf_counter() - t0
     return {"value": round(done / elapsed, 3), "unit": "tokens/s", "cores": cores, "kind": "oracle",
             "sample": f"{done} sequence-steps (cycling over {nseq} of the {work.B} sequences), all 64 heads, one "
-                      f"windowed + one full layer at context {p + 1}; {elapsed:.1f} s of fp64 oracle on {cores} threads"}
+                      f"windowed + one full layer at context {p + 1}; {elapsed:.1f} s of fp64 oracle on {cores} threads",
+            "single_thread": {"value": round(1.0 / one, 3), "unit": "tokens/s",
+                              "sample": f"1 sequence-step on 1 thread, {one:.2f} s"}}
 
 
 def run_decode(args, kvr, rank):
