@@ -82,7 +82,7 @@ def _oracle_swa(q, syn, hkv, seqs, positions, sinks, vscale):
 # --------------------------------------------------------------------------- windowed decode over pages
 
 @pytest.mark.parametrize("dist", ["shifted", "plain"])
-@pytest.mark.parametrize("bsz", [16, 64])
+@pytest.mark.parametrize("bsz", [16, 32, 64, 128, 256])
 def test_swa_decode_paged_matches_oracle(dist, bsz, tables):
     positions = [0, 1, 5, 15, 16, 126, 127, 128, 129, 143, 144, 300, 1000, 4095, 4096, 70000]
     hq, hkv, vs = 64, 8, 0.707
@@ -105,16 +105,18 @@ def test_swa_decode_paged_matches_oracle(dist, bsz, tables):
 
 @pytest.mark.parametrize("bsz", [16, 64])
 @pytest.mark.parametrize("hq", [64, 128])
-def test_swa_decode_paged_many_items_per_cta(bsz, hq, tables):
-    """Many more (sequence, KV head) items than CTAs, so every CTA streams
-    five or more windows in turn: at 8 q heads per KV head through its two
-    stage sets (each reused several times, its barriers' parities
-    alternating), at 16 through the split kernel's window mode (the next
-    item's ids carried, its window prefetched); positions mixed: short
-    sequences, windows on and off 16-key boundaries.  Two calls must agree
-    bit for bit, and every row must match the oracle."""
-    rng = np.random.default_rng(6401 + bsz)
-    B = 200
+@pytest.mark.parametrize("B", [64, 200])
+def test_swa_decode_paged_many_items_per_cta(bsz, hq, B, tables):
+    """More (sequence, KV head) items than CTAs: at 8 q heads per KV head
+    each CTA streams the subtiles of its items through its ring of eight
+    places (at B = 200 five or more windows, every place reused many times,
+    its barriers' parities alternating; at B = 64 one or two, the first
+    prefetched before the wait on the kernel ahead), at 16 through the split
+    kernel's window mode (the next item's ids carried, its window
+    prefetched); positions mixed: short sequences, windows on and off 16-key
+    boundaries.  Two calls must agree bit for bit, and every row must match
+    the oracle."""
+    rng = np.random.default_rng(6401 + bsz + B)
     positions = [int(x) for x in rng.integers(0, 5000, size=B)]
     positions[:6] = [0, 5, 127, 128, 143, 144]
     hkv, vs = 8, 0.707
