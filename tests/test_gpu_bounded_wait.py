@@ -53,7 +53,9 @@ def _stalled(call):
         kvr.debug_stall_next(0, 1000)
 
 
-@pytest.mark.parametrize("B", [40, 64])  # 64 x 8 KV heads: two CTAs of two groups per SM
+# 16 x 8 KV heads: one unit per CTA of one group; 40: CTAs of four groups;
+# 64: two CTAs of two groups per SM
+@pytest.mark.parametrize("B", [16, 40, 64])
 def test_windowed_decode_stall_takes_the_bounded_exit(B):
     hq, hkv = 64, 8
     positions = [300 + 7 * b for b in range(B)]
