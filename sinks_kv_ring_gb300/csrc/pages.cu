@@ -154,9 +154,30 @@ __global__ void __launch_bounds__(GATHER_THREADS)
     ring_gather_kernel(KvView pages, KvView ring, const int32_t *__restrict__ src_seqs,
                        const int32_t *__restrict__ dst_seqs, const int64_t *__restrict__ end, unsigned *status) {
   __shared__ long long s_row[WIN];
+  const int i = blockIdx.x, kv = blockIdx.y, hkv = ring.hkv;
+  // Before the wait for the kernel ahead (which may still run): the window's
+  // rows requested into L2, block by block (thread j: the window's j-th
+  // block), from the end, source sequence and block ids read early (see
+  // ld_early_s32: a stale value only wastes a prefetch; all is read again
+  // below).  Anything outside the pool is skipped.
+  if (threadIdx.x < 32) {
+    const long long e = ld_early_s64(end + i);
+    const int ss = ld_early_s32(src_seqs + i), bsz = pages.block_size;
+    if (e > 0 && ss >= 0 && ss < pages.num_seqs) {
+      const long long lo = e > WIN ? e - WIN : 0, b0 = lo / bsz, bj = b0 + threadIdx.x;
+      if (bj <= (e - 1) / bsz && bj < pages.max_blocks) {
+        const int blk = ld_early_s32(pages.block_table + (long long)ss * pages.max_blocks + bj);
+        if (blk >= 0 && blk < pages.num_blocks) {
+          const long long r0 = max(lo, bj * bsz), r1 = min(e - 1, bj * bsz + bsz - 1);
+          const long long row = ((long long)blk * pages.hkv + kv) * bsz + (r0 - bj * bsz);
+          prefetch_l2(pages.k + row * DQK, (uint32_t)(r1 - r0 + 1) * DQK * 2);
+          prefetch_l2(pages.v + row * DV, (uint32_t)(r1 - r0 + 1) * DV * 2);
+        }
+      }
+    }
+  }
   pdl_wait();
   pdl_trigger();
-  const int i = blockIdx.x, kv = blockIdx.y, hkv = ring.hkv;
   const int ss = src_seqs[i], ds = dst_seqs[i];
   if (ss < 0 || ss >= pages.num_seqs || ds < 0 || ds >= ring.num_seqs) {
     if (kv == 0 && threadIdx.x == 0) flag(status, ST_BAD_SEQ);
