@@ -59,14 +59,18 @@ constexpr int SP_NB = 16;  // block ids of one window (blocks of >= 16 keys)
 static_assert((WIN + 15 + 15) / 16 + 1 <= SP_NB, "block ids of one window");
 constexpr int SP_OSTRIDE = DV + 4;  // merge rows: the 8 x 4 lanes of a stash store hit 32 banks
 constexpr int SP_MERGE_G = (SP_GWARPS * 8 * 2 + SP_GWARPS * 8 * SP_OSTRIDE + SP_GWARPS * 8) * 4;  // per group
-constexpr int SP_QTILE = 8 * DQK * 2;
+// query tile rows padded to 400 bytes: the eight rows an ldmatrix reads then
+// start in eight different 16-byte bank groups (384-byte rows would all start
+// in the same one)
+constexpr int SP_QROW = DQK * 2 + 16;
+constexpr int SP_QTILE = 8 * SP_QROW;
 static_assert(SP_STAGE % 1024 == 0, "places start on 1024-byte boundaries");
 
 // Shape of a CTA of NGR groups (each: four consumer warps, two producer
 // warps).  Shared memory from a 1024-byte aligned base (the TMA boxes'
 // 128-byte swizzle wants it): the groups' rings, their merge areas (per
 // warp and head: (m, l), O row, factor), then per group and item slot (two
-// per group) the query tile [8][192] (plain rows), the table row, the
+// per group) the query tile [8][192] (rows padded to 400 bytes), the table row, the
 // window's block ids and the item record; the barriers -- full[group][place],
 // empty[group][place], qfull[group][slot], qempty[group][slot], one nothing
 // arrives on (the test hook's stall) -- and the abort flag.
@@ -101,9 +105,9 @@ __device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
 }
 
 // B fragments of Q^T (16 dims x 8 heads per k-step) for the 12 k-steps, from
-// the plain [8][192] query tile: lane l gets head l/4, dims 2(l%4)..
+// the [8][192] query tile (rows SP_QROW bytes apart): lane l gets head l/4, dims 2(l%4)..
 __device__ __forceinline__ void load_qt_frags(const uint8_t *sQ, int lane, uint32_t (&qf)[12][2]) {
-  const uint32_t base = smem_u32(sQ) + (lane & 7) * (DQK * 2);
+  const uint32_t base = smem_u32(sQ) + (lane & 7) * SP_QROW;
 #pragma unroll
   for (int kk = 0; kk < 12; kk += 2)
     ldsm_x4(base + (2 * kk + (lane >> 3)) * 16, qf[kk][0], qf[kk][1], qf[kk + 1][0], qf[kk + 1][1]);
@@ -303,8 +307,10 @@ __global__ void __launch_bounds__(SpL<NGR>::THREADS, SpL<NGR>::CTAS)
           if (lane == 0) tc::mbar_arrive(qb);
         } else {
           tc::mbar_expect_tx_elect(qb, G * DQK * 2 + 256);
-          tc::bulk_load_elect(smem_u32(smem + L::OFF_Q + (gr * 2 + sl) * SP_QTILE),
-                              q + ((long long)b * hq + (long long)kv * G) * DQK, G * DQK * 2, qb);
+          __syncwarp();
+          if (lane < G)  // one padded row per lane
+            tc::bulk_load(smem_u32(smem + L::OFF_Q + (gr * 2 + sl) * SP_QTILE + lane * SP_QROW),
+                          q + ((long long)b * hq + (long long)kv * G + lane) * DQK, DQK * 2, qb);
           tc::bulk_load_elect(smem_u32(smem + L::OFF_CS + (gr * 2 + sl) * 256), table + p * 64, 256, qb);
         }
       }

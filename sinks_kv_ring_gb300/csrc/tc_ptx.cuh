@@ -182,6 +182,12 @@ __device__ __forceinline__ void bulk_load_elect(uint32_t dst, const void *src, u
       "l"(src), "r"(bytes), "r"(bar)
       : "memory");
 }
+// The same copy issued by the calling thread alone.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
 __device__ __forceinline__ void mbar_expect_tx_elect(uint32_t bar, uint32_t bytes) {
   asm volatile(
       "{\n.reg .pred e;\n.reg .b64 st;\nelect.sync _|e, 0xffffffff;\n"
