@@ -14,6 +14,7 @@
 // ring of a sequence whose positions 0..E-1 were appended in order holds, in
 // slot c, the last of them congruent to c.
 #include "launch.h"
+#include "tc_ptx.cuh"
 
 namespace kvr {
 namespace {
@@ -143,48 +144,66 @@ __global__ void __launch_bounds__(RL_THREADS) pages_release_kernel(ReleaseArgs A
   if (threadIdx.x == 0) *A.free_count = base;
 }
 
-// One CTA per (entry, KV head).  The first 128 threads resolve slot c to its
-// source row (-1 when the slot gets no position) into shared memory; then
-// every thread moves 16-byte chunks, GATHER_BATCH loads in flight before
-// their stores.  The KV-head-0 CTA also writes the slot tags.
-constexpr int GATHER_THREADS = 256;
-constexpr int GATHER_BATCH = 5;
+// One CTA per (entry, KV head, K or V), one thread per ring slot.  Slot c is
+// resolved to its source row (-1 when the slot gets no position); the slots
+// form runs whose source rows are consecutive in the pool (positions of one
+// block, in slot order), at most (128 / block size) + 2 of them.  The thread
+// at the head of a run copies it with one bulk copy into the CTA's image of
+// the ring's K (or V), then, once every run has landed, back out to the ring
+// with one bulk store: each byte crosses the SM once, in copies of up to
+// 24 KB.  Slots without a position keep what the ring held.  The CTA of KV
+// head 0's K also writes the slot tags.
+constexpr int GATHER_THREADS = WIN;
+constexpr int GATHER_SMEM = WIN * DQK * 2;  // the image of one ring's K (or V: the first 32 KB)
+constexpr unsigned GATHER_ST_TIMEOUT = 8u;           // KVR_DEV_TIMEOUT
 
-__global__ void __launch_bounds__(GATHER_THREADS)
+__global__ void __launch_bounds__(GATHER_THREADS, 4)
     ring_gather_kernel(KvView pages, KvView ring, const int32_t *__restrict__ src_seqs,
                        const int32_t *__restrict__ dst_seqs, const int64_t *__restrict__ end, unsigned *status) {
+  extern __shared__ __align__(128) uint8_t g_img[];
   __shared__ long long s_row[WIN];
-  const int i = blockIdx.x, kv = blockIdx.y, hkv = ring.hkv;
+  __shared__ unsigned s_brk[WIN / 32];
+  __shared__ __align__(8) uint64_t s_bar;
+  __shared__ uint32_t s_abort;
+  const int i = blockIdx.x, kv = blockIdx.y, hkv = ring.hkv, c = threadIdx.x;
+  const bool isv = blockIdx.z != 0;
+  const int width = isv ? DV : DQK;                             // elements per row
+  const uint16_t *src = isv ? pages.v : pages.k;
+  uint16_t *dstr = isv ? ring.v : ring.k;
+  const uint32_t bar = smem_u32(&s_bar);
   // Before the wait for the kernel ahead (which may still run): the window's
   // rows requested into L2, block by block (thread j: the window's j-th
   // block), from the end, source sequence and block ids read early (see
   // ld_early_s32: a stale value only wastes a prefetch; all is read again
   // below).  Anything outside the pool is skipped.
-  if (threadIdx.x < 32) {
+  if (c < 32) {
     const long long e = ld_early_s64(end + i);
     const int ss = ld_early_s32(src_seqs + i), bsz = pages.block_size;
     if (e > 0 && ss >= 0 && ss < pages.num_seqs) {
-      const long long lo = e > WIN ? e - WIN : 0, b0 = lo / bsz, bj = b0 + threadIdx.x;
+      const long long lo = e > WIN ? e - WIN : 0, b0 = lo / bsz, bj = b0 + c;
       if (bj <= (e - 1) / bsz && bj < pages.max_blocks) {
         const int blk = ld_early_s32(pages.block_table + (long long)ss * pages.max_blocks + bj);
         if (blk >= 0 && blk < pages.num_blocks) {
           const long long r0 = max(lo, bj * bsz), r1 = min(e - 1, bj * bsz + bsz - 1);
           const long long row = ((long long)blk * pages.hkv + kv) * bsz + (r0 - bj * bsz);
-          prefetch_l2(pages.k + row * DQK, (uint32_t)(r1 - r0 + 1) * DQK * 2);
-          prefetch_l2(pages.v + row * DV, (uint32_t)(r1 - r0 + 1) * DV * 2);
+          prefetch_l2(src + row * width, (uint32_t)(r1 - r0 + 1) * width * 2);
         }
       }
     }
+  }
+  if (c == 0) {
+    tc::mbar_init(bar, 1);
+    s_abort = 0;
+    tc::fence_mbar_init();
   }
   pdl_wait();
   pdl_trigger();
   const int ss = src_seqs[i], ds = dst_seqs[i];
   if (ss < 0 || ss >= pages.num_seqs || ds < 0 || ds >= ring.num_seqs) {
-    if (kv == 0 && threadIdx.x == 0) flag(status, ST_BAD_SEQ);
+    if (kv == 0 && !isv && c == 0) flag(status, ST_BAD_SEQ);
     return;
   }
-  if (threadIdx.x < WIN) {
-    const int c = threadIdx.x;
+  {
     const long long e = end[i];
     // the position slot c holds: the largest p < e with p mod 128 == c
     const long long p = e - 1 - (long long)(((e - 1 - c) % WIN + WIN) % WIN);
@@ -196,40 +215,50 @@ __global__ void __launch_bounds__(GATHER_THREADS)
       if (blk >= 0 && blk < pages.num_blocks) {
         row = ((long long)blk * pages.hkv + kv) * pages.block_size + (p - bi * pages.block_size);
         tag = (int32_t)p;
-      } else if (kv == 0) {
+      } else if (kv == 0 && !isv) {
         flag(status, ST_BAD_BLOCK);
       }
     }
     s_row[c] = row;
-    if (kv == 0) ring.slot_pos[(long long)ds * WIN + c] = tag;
+    if (kv == 0 && !isv) ring.slot_pos[(long long)ds * WIN + c] = tag;
   }
-  __syncthreads();
-  uint4 *rk = reinterpret_cast<uint4 *>(ring.k + ((long long)ds * hkv + kv) * WIN * DQK);
-  uint4 *rv = reinterpret_cast<uint4 *>(ring.v + ((long long)ds * hkv + kv) * WIN * DV);
-  constexpr int CK = DQK / 8, CV = DV / 8, CR = CK + CV;  // 16-byte chunks per slot
-  constexpr int TOTAL = WIN * CR;
-  static_assert(TOTAL % (GATHER_THREADS * GATHER_BATCH) == 0, "whole batches");
-  for (int x0 = threadIdx.x; x0 < TOTAL; x0 += GATHER_THREADS * GATHER_BATCH) {
-    uint4 val[GATHER_BATCH];
-    uint4 *dst[GATHER_BATCH];
-#pragma unroll
-    for (int u = 0; u < GATHER_BATCH; ++u) {
-      const int x = x0 + u * GATHER_THREADS, c = x / CR, ch = x % CR;
-      const long long row = s_row[c];
-      dst[u] = nullptr;
-      if (row >= 0) {
-        if (ch < CK) {
-          val[u] = reinterpret_cast<const uint4 *>(pages.k + row * DQK)[ch];
-          dst[u] = rk + c * CK + ch;
-        } else {
-          val[u] = reinterpret_cast<const uint4 *>(pages.v + row * DV)[ch - CK];
-          dst[u] = rv + c * CV + ch - CK;
-        }
+  __syncthreads();  // (also: the barrier's initialisation before any use)
+  // Slot c continues a run when its row follows slot c-1's; every other slot
+  // (a head, or one without a position) ends the run before it.
+  const long long row = s_row[c];
+  const bool cont = row >= 0 && c > 0 && s_row[c - 1] == row - 1;
+  const unsigned brk = __ballot_sync(FULLW, !cont);
+  if ((c & 31) == 0) s_brk[c >> 5] = brk;
+  const int nslots = __syncthreads_count(row >= 0);
+  if (nslots == 0) return;
+  int len = 0;  // slots in the run this thread heads (0: none): up to the next break
+  if (row >= 0 && !cont) {
+    len = WIN - c;
+    for (int k = c + 1, w = k >> 5; w < WIN / 32; ++w) {
+      const unsigned m = w == (k >> 5) ? s_brk[w] & (FULLW << (k & 31)) : s_brk[w];
+      if (m) {
+        len = 32 * w + __ffs((int)m) - 1 - c;
+        break;
       }
     }
-#pragma unroll
-    for (int u = 0; u < GATHER_BATCH; ++u)
-      if (dst[u]) *dst[u] = val[u];
+  }
+  if (c == 0) tc::mbar_expect_tx(bar, (uint32_t)nslots * width * 2);
+  __syncthreads();  // the expected bytes are set before any copy can complete
+  const uint32_t img = smem_u32(g_img);
+  if (len) tc::bulk_load(img + c * width * 2, src + row * width, (uint32_t)len * width * 2, bar);
+  // A wait that gives up (2 s) flags the call and still lets the copies
+  // land (bounded again) before the CTA leaves; nothing is stored then.
+  if (!tc::mbar_wait(bar, 0, &s_abort)) {
+    if (c == 0) flag(status, GATHER_ST_TIMEOUT);
+    uint32_t never = 0;
+    tc::mbar_wait(bar, 0, &never);
+    return;
+  }
+  if (len) {
+    tc::fence_proxy_async_smem();
+    tc::bulk_store(dstr + (((long long)ds * hkv + kv) * WIN + c) * width, img + c * width * 2, (uint32_t)len * width * 2);
+    tc::bulk_commit();
+    tc::bulk_wait_read_all();  // the image is read before the CTA leaves (the grid's end covers the writes)
   }
 }
 
@@ -247,8 +276,11 @@ cudaError_t launch_pages_release(int32_t *table, int num_seqs, int max_blocks, i
 cudaError_t launch_ring_gather(const KvView &pages, const KvView &ring, const int32_t *src_seqs,
                                const int32_t *dst_seqs, const int64_t *end, int n, unsigned *status,
                                cudaStream_t st) {
-  dim3 grid((unsigned)n, (unsigned)ring.hkv);
-  return launch_pdl(ring_gather_kernel, grid, dim3(GATHER_THREADS), 0, st, pages, ring, src_seqs, dst_seqs, end, status);
+  cudaError_t e = ensure_smem_limit(15, (const void *)ring_gather_kernel, GATHER_SMEM, true);
+  if (e != cudaSuccess) return e;
+  dim3 grid((unsigned)n, (unsigned)ring.hkv, 2);
+  return launch_pdl(ring_gather_kernel, grid, dim3(GATHER_THREADS), GATHER_SMEM, st, pages, ring, src_seqs, dst_seqs,
+                    end, status);
 }
 
 }  // namespace kvr

@@ -117,6 +117,12 @@ __device__ __forceinline__ void tma_store_3d(const void *map, int x, int y, int 
                "r"(y), "r"(z), "r"(src)
                : "memory");
 }
+// Bulk copy of `bytes` (a multiple of 16, both addresses 16-byte aligned)
+// from shared to global memory, tracked by the issuing thread's bulk group.
+__device__ __forceinline__ void bulk_store(void *dst, uint32_t src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src), "r"(bytes)
+               : "memory");
+}
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // Wait until every committed bulk store has read its shared-memory source.
 __device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
