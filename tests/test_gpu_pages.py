@@ -339,6 +339,51 @@ def test_ring_gather_matches_oracle_and_appends(tables):
         assert torch.equal(ring.v[2:, h][valid].view(torch.int16), ring2.v[2:, h][valid].view(torch.int16))
 
 
+@pytest.mark.parametrize("bsz", [16, 64, 256])
+def test_ring_gather_runs_across_adjacent_blocks(bsz, tables):
+    # One KV head and a block table of consecutive ids: the pool rows of
+    # neighbouring blocks are adjacent in memory, so a window's slots form
+    # runs longer than a block (split only at the ring's wrap, at a missing
+    # block and where the ids stop being consecutive).  Bit-exact against the
+    # oracle's ring_from_pages.
+    hkv, vs = 1, 0.707
+    ends = [1, 128, 129, 200, 1000, 1000, 777]
+    syn = Synth(6701, dist="shifted", device=DEV)
+    S = len(ends)
+    mb = max(ends) // bsz + 1
+    nblk = S * mb
+    tab = torch.arange(nblk, dtype=torch.int32, device=DEV).reshape(S, mb)
+    tab[5] = torch.flip(tab[5], [0])           # sequence 5: descending ids, runs end at every block edge
+    pool = _nan_pool(nblk, hkv, bsz, tab)
+    for s, e in enumerate(ends):
+        _append_range(pool, syn, s, 0, e, tables[1e4], vs)
+    miss = (777 - 60) // bsz
+    pool.block_table[6, miss] = -1            # sequence 6: a hole inside its window
+    ring = kvr.RingLayout.empty(S, hkv)
+    ring.k.normal_()
+    ring.v.normal_()
+    ring.slot_pos.fill_(-7)
+    k0, v0, t0 = ring.k.clone(), ring.v.clone(), ring.slot_pos.clone()
+    src = torch.arange(S, dtype=torch.int32, device=DEV)
+    assert kvr.device_status() == 0          # (and cleared)
+    kvr.kv_ring_gather_pages(pool, ring, src, src, torch.tensor(ends, dtype=torch.int64, device=DEV))
+    torch.cuda.synchronize()
+    assert kvr.device_status() == kvr.DEV_BAD_BLOCK
+    pk = pool.k.view(torch.int16).cpu().numpy().view(np.uint16)
+    pv = pool.v.view(torch.int16).cpu().numpy().view(np.uint16)
+    tb = pool.block_table.cpu().numpy()
+    rk = ring.k.view(torch.int16).cpu().numpy().view(np.uint16)
+    rv = ring.v.view(torch.int16).cpu().numpy().view(np.uint16)
+    rt = ring.slot_pos.cpu().numpy()
+    k0n = k0.view(torch.int16).cpu().numpy().view(np.uint16)
+    v0n = v0.view(torch.int16).cpu().numpy().view(np.uint16)
+    for s, e in enumerate(ends):
+        wk, wv, wt, fl = opages.ring_from_pages(pk, pv, tb, bsz, s, e, k0n[s], v0n[s], t0[s].cpu().numpy())
+        assert fl == (opages.BAD_BLOCK if s == 6 else 0), s
+        assert np.array_equal(rt[s], wt), s
+        assert np.array_equal(rk[s], wk) and np.array_equal(rv[s], wv), s
+
+
 def test_ring_gather_flags_missing_blocks(tables):
     hkv, bsz = 2, 16
     syn = Synth(6601, device=DEV)
