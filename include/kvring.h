@@ -301,9 +301,11 @@ kvr_status kv_pages_release_window(int32_t *block_table, int32_t num_seqs, int32
  * sequence kept in pages.  A needed position whose block entry is not a
  * block id of the pool gets slot_pos -1 and sets KVR_DEV_BAD_BLOCK; a
  * sequence id outside either layout sets KVR_DEV_BAD_SEQ and the entry is
- * skipped.  pages: PAGED; ring: RING with the same num_kv_heads; src_seqs,
- * dst_seqs [n] int32 and end [n] int64 are device arrays; no two entries
- * may name the same dst sequence.  n = 0 is a no-op.
+ * skipped.  The rows move as bulk copies through shared memory; if they do
+ * not land within 2 s, KVR_DEV_TIMEOUT is set and that entry's K or V rows
+ * are left as they were.  pages: PAGED; ring: RING with the same
+ * num_kv_heads; src_seqs, dst_seqs [n] int32 and end [n] int64 are device
+ * arrays; no two entries may name the same dst sequence.  n = 0 is a no-op.
  */
 kvr_status kv_ring_gather_pages(const kvr_kv_layout *pages, const kvr_kv_layout *ring, const int32_t *src_seqs,
                                 const int32_t *dst_seqs, const int64_t *end, int32_t n, void *stream);
