@@ -553,10 +553,12 @@ def pool_ops_times(work, hbm, peaks_src, copies=None):
     dec = [(lambda st, pl=pl: kvr.swa_sink_decode(work.q_swa, work.pos, work.seq, pl, work.sinks, work.t4, SCALE,
                                                   out=work.out_swa, stream=st)) for pl in pools] * 4
     ms_dec = graph_time_ms(dec)
-    ring = kvr.RingLayout.empty(B, hkv, device=dev)
+    # each launch writes its own destination ring too, so that the written
+    # rows leave L2 for HBM as they would in use (one ring fits in L2)
+    rings_g = [kvr.RingLayout.empty(B, hkv, device=dev) for _ in pools]
     end = torch.full((B,), p + 1, dtype=torch.int64, device=dev)
-    gat = [(lambda st, pl=pl: kvr.kv_ring_gather_pages(pl, ring, work.seq, work.seq, end, stream=st))
-           for pl in pools] * 4
+    gat = [(lambda st, pl=pl, rg=rg: kvr.kv_ring_gather_pages(pl, rg, work.seq, work.seq, end, stream=st))
+           for pl, rg in zip(pools, rings_g)] * 4
     ms_gat = graph_time_ms(gat)
     gat_bytes = 2 * layer_kv_bytes([p + 1] * B, hkv, window=128) + B * 128 * 4
     # release: every sequence has a full table (ids 0..B*mb-1); each call frees
@@ -576,9 +578,11 @@ def pool_ops_times(work, hbm, peaks_src, copies=None):
     dec_gbs = work.bytes_swa() / (ms_dec / 1e3) / 1e9
     gat_gbs = gat_bytes / (ms_gat / 1e3) / 1e9
     # ring snapshot / restore of the whole batch, rotating over the decode workload's ring copies
-    snap = kvr.ring_snapshot_alloc(B, hkv, device=dev)
-    sn = [(lambda st, r=r: kvr.kv_ring_snapshot(r, work.seq, snap, stream=st)) for r in work.rings] * 4
-    rs = [(lambda st, r=r: kvr.kv_ring_restore(r, work.seq, snap, stream=st)) for r in work.rings] * 4
+    # and as many snapshot buffers (one buffer would stay in L2 from launch to launch)
+    del rings_g
+    snaps = [kvr.ring_snapshot_alloc(B, hkv, device=dev) for _ in work.rings]
+    sn = [(lambda st, r=r, sb=sb: kvr.kv_ring_snapshot(r, work.seq, sb, stream=st)) for r, sb in zip(work.rings, snaps)] * 4
+    rs = [(lambda st, r=r, sb=sb: kvr.kv_ring_restore(r, work.seq, sb, stream=st)) for r, sb in zip(work.rings, snaps)] * 4
     ms_sn, ms_rs = graph_time_ms(sn), graph_time_ms(rs)
     copy_bytes = 2 * (kvr.RingLayout.bytes_per_layer(B, hkv) + B * 128 * 4)
     copy = lambda ms: {"graph_ms": round(ms, 5), "bytes": copy_bytes, "GB/s": round(copy_bytes / ms / 1e6, 1),
@@ -588,9 +592,10 @@ def pool_ops_times(work, hbm, peaks_src, copies=None):
                                                  "peak_source": peaks_src})}
     return {
         "kv_ring_snapshot": dict(workload=f"{B} sequences x {hkv} KV heads: rings (slots + tags) to a snapshot, "
-                                          f"rotating over {len(work.rings)} ring copies", **copy(ms_sn)),
-        "kv_ring_restore": dict(workload=f"{B} sequences x {hkv} KV heads: snapshot back into the rings",
-                                **copy(ms_rs)),
+                                          f"rotating over {len(work.rings)} ring copies and as many snapshot buffers",
+                                 **copy(ms_sn)),
+        "kv_ring_restore": dict(workload=f"{B} sequences x {hkv} KV heads: snapshots back into the rings (the same "
+                                         f"rotation)", **copy(ms_rs)),
         "swa_sink_decode_paged": {
             "workload": f"batch {B}, windowed layer kept in pages of {bs} (block table holds the window's {nper} "
                         f"blocks per sequence), graph rotating over {copies} copies", "graph_ms": round(ms_dec, 5),
@@ -600,7 +605,8 @@ def pool_ops_times(work, hbm, peaks_src, copies=None):
                                       "kernel": "swa_paged_kernel",
                                       "traffic": kernel_traffic("swa_paged_kernel")})},
         "kv_ring_gather_pages": {
-            "workload": f"{B} sequences x {hkv} KV heads: the 128-position window from pages into rings",
+            "workload": f"{B} sequences x {hkv} KV heads: the 128-position window from pages into rings, "
+                        f"rotating over {copies} pools and as many destination rings",
             "graph_ms": round(ms_gat, 5), "bytes": gat_bytes, "GB/s": round(gat_gbs, 1),
             "roofline": with_nominal({"bound": "hbm", "achieved": round(gat_gbs, 1), "peak": hbm, "unit": "GB/s",
                                       "frac": round(gat_gbs / hbm, 4), "peak_source": peaks_src})},
