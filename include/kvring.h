@@ -245,8 +245,11 @@ kvr_status full_attn_decode(const kvr_bf16 *q, const int64_t *pos, const int32_t
  *   seqs[i].
  * kv_ring_snapshot copies ring -> snapshot; kv_ring_restore copies
  * snapshot -> ring (slot contents and slot tags, bit for bit).  A sequence
- * id outside the ring sets KVR_DEV_BAD_SEQ and its entry is skipped.  Two
- * entries of one restore must not name the same sequence.  n = 0 is a no-op.
+ * id outside the ring sets KVR_DEV_BAD_SEQ and its entry is skipped.  The
+ * rows move as bulk copies through shared memory; a piece that does not land
+ * within 2 s sets KVR_DEV_TIMEOUT and is not stored.  k_snap and v_snap must
+ * be 16-byte aligned (KVR_EINVAL otherwise).  Two entries of one restore must
+ * not name the same sequence.  n = 0 is a no-op.
  */
 kvr_status kv_ring_snapshot(const kvr_kv_layout *ring, const int32_t *seqs, int32_t n, kvr_bf16 *k_snap,
                             kvr_bf16 *v_snap, int32_t *tags_snap, void *stream);
