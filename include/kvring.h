@@ -136,14 +136,16 @@ kvr_status kvr_device_status(uint32_t *flags, int reset);
  * Test hook for the bounded waits (no counterpart on the pages).  The next
  * `launches` kernels started by swa_sink_decode (over a RING layout, or over
  * a PAGED one with up to 8 q heads per KV head), by the short-chunk part of
- * swa_sink_prefill_varlen or by full_attn_prefill_chunk, in this process,
- * stall on purpose: once their
- * loads are in flight (and, for the prefill, with its tensor memory held),
- * one warp group waits on an internal barrier that nothing completes, with a
+ * swa_sink_prefill_varlen, by full_attn_prefill_chunk, by
+ * kv_ring_gather_pages or by kv_ring_snapshot / kv_ring_restore, in this
+ * process, stall on purpose: once their loads are in flight (and, for the
+ * prefill, with its tensor memory held), one warp group (for the copies: the
+ * first CTA) waits on an internal barrier that nothing completes, with a
  * time limit of limit_ns nanoseconds.  When the limit passes the kernel takes
  * the exit a real stall would take -- the other warps see the abort, the
- * loads and products already issued finish, tensor memory is freed -- and
- * sets KVR_DEV_TIMEOUT; that call's output is unspecified.  launches = 0
+ * loads and products already issued finish, tensor memory is freed, a copy
+ * stores nothing -- and sets KVR_DEV_TIMEOUT; that call's output is
+ * unspecified.  launches = 0
  * turns the hook off.  KVR_EINVAL unless 0 <= launches and
  * 1000 <= limit_ns <= 1e9.  For tests of that exit path only.
  */

@@ -159,18 +159,19 @@ constexpr unsigned GATHER_ST_TIMEOUT = 8u;           // KVR_DEV_TIMEOUT
 
 __global__ void __launch_bounds__(GATHER_THREADS, 4)
     ring_gather_kernel(KvView pages, KvView ring, const int32_t *__restrict__ src_seqs,
-                       const int32_t *__restrict__ dst_seqs, const int64_t *__restrict__ end, unsigned *status) {
+                       const int32_t *__restrict__ dst_seqs, const int64_t *__restrict__ end, unsigned *status,
+                       unsigned long long stall_ns) {
   extern __shared__ __align__(128) uint8_t g_img[];
   __shared__ long long s_row[WIN];
   __shared__ unsigned s_brk[WIN / 32];
-  __shared__ __align__(8) uint64_t s_bar;
+  __shared__ __align__(8) uint64_t s_bar, s_stall;
   __shared__ uint32_t s_abort;
   const int i = blockIdx.x, kv = blockIdx.y, hkv = ring.hkv, c = threadIdx.x;
   const bool isv = blockIdx.z != 0;
   const int width = isv ? DV : DQK;                             // elements per row
   const uint16_t *src = isv ? pages.v : pages.k;
   uint16_t *dstr = isv ? ring.v : ring.k;
-  const uint32_t bar = smem_u32(&s_bar);
+  const uint32_t bar = smem_u32(&s_bar), stall_bar = smem_u32(&s_stall);
   // Before the wait for the kernel ahead (which may still run): the window's
   // rows requested into L2, block by block (thread j: the window's j-th
   // block), from the end, source sequence and block ids read early (see
@@ -193,6 +194,7 @@ __global__ void __launch_bounds__(GATHER_THREADS, 4)
   }
   if (c == 0) {
     tc::mbar_init(bar, 1);
+    tc::mbar_init(stall_bar, 1);
     s_abort = 0;
     tc::fence_mbar_init();
   }
@@ -248,7 +250,10 @@ __global__ void __launch_bounds__(GATHER_THREADS, 4)
   if (len) tc::bulk_load(img + c * width * 2, src + row * width, (uint32_t)len * width * 2, bar);
   // A wait that gives up (2 s) flags the call and still lets the copies
   // land (bounded again) before the CTA leaves; nothing is stored then.
-  if (!tc::mbar_wait(bar, 0, &s_abort)) {
+  // Test hook (stall_ns != 0): the first CTA waits instead on a barrier
+  // nothing completes, with that limit, and takes the same exit.
+  const bool stall = stall_ns && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0;
+  if (!(stall ? tc::mbar_wait(stall_bar, 0, &s_abort, stall_ns) : tc::mbar_wait(bar, 0, &s_abort))) {
     if (c == 0) flag(status, GATHER_ST_TIMEOUT);
     uint32_t never = 0;
     tc::mbar_wait(bar, 0, &never);
@@ -280,7 +285,7 @@ cudaError_t launch_ring_gather(const KvView &pages, const KvView &ring, const in
   if (e != cudaSuccess) return e;
   dim3 grid((unsigned)n, (unsigned)ring.hkv, 2);
   return launch_pdl(ring_gather_kernel, grid, dim3(GATHER_THREADS), GATHER_SMEM, st, pages, ring, src_seqs, dst_seqs,
-                    end, status);
+                    end, status, take_stall());
 }
 
 }  // namespace kvr

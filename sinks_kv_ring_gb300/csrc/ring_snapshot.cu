@@ -21,9 +21,9 @@ constexpr unsigned COPY_ST_TIMEOUT = 8u;                  // KVR_DEV_TIMEOUT
 
 __global__ void __launch_bounds__(COPY_THREADS)
     ring_copy_kernel(KvView ring, const int32_t *__restrict__ seqs, uint16_t *k_snap, uint16_t *v_snap,
-                     int32_t *tags_snap, int to_ring, unsigned *status) {
+                     int32_t *tags_snap, int to_ring, unsigned *status, unsigned long long stall_ns) {
   __shared__ __align__(128) uint8_t buf[COPY_PIECE];
-  __shared__ __align__(8) uint64_t s_bar;
+  __shared__ __align__(8) uint64_t s_bar, s_stall;
   __shared__ uint32_t s_abort;
   pdl_wait();
   pdl_trigger();
@@ -42,15 +42,19 @@ __global__ void __launch_bounds__(COPY_THREADS)
   const uint8_t *src = (to_ring ? snapp : ringp) + off;
   uint8_t *dst = (to_ring ? ringp : snapp) + off;
   if (lane == 0) {
-    const uint32_t bar = smem_u32(&s_bar), sb = smem_u32(buf);
+    const uint32_t bar = smem_u32(&s_bar), stall_bar = smem_u32(&s_stall), sb = smem_u32(buf);
     tc::mbar_init(bar, 1);
+    tc::mbar_init(stall_bar, 1);
     s_abort = 0;
     tc::fence_mbar_init();
     tc::mbar_expect_tx(bar, COPY_PIECE);
     tc::bulk_load(sb, src, COPY_PIECE, bar);
     // a copy that does not land within 2 s: flagged, nothing stored, and
-    // still waited for (bounded) before the CTA leaves
-    if (tc::mbar_wait(bar, 0, &s_abort)) {
+    // still waited for (bounded) before the CTA leaves.  Test hook
+    // (stall_ns != 0): the first CTA waits instead on a barrier nothing
+    // completes, with that limit, and takes the same exit.
+    const bool stall = stall_ns && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0;
+    if (stall ? tc::mbar_wait(stall_bar, 0, &s_abort, stall_ns) : tc::mbar_wait(bar, 0, &s_abort)) {
       tc::fence_proxy_async_smem();
       tc::bulk_store(dst, sb, COPY_PIECE);
       tc::bulk_commit();
@@ -79,7 +83,7 @@ cudaError_t launch_ring_copy(const KvView &ring, const int32_t *seqs, int n, uin
                              int32_t *tags_snap, bool to_ring, unsigned *status, cudaStream_t st) {
   dim3 grid((unsigned)n, (unsigned)ring.hkv, COPY_KPIECES + COPY_VPIECES);
   return launch_pdl(ring_copy_kernel, grid, dim3(COPY_THREADS), 0, st, ring, seqs, k_snap, v_snap, tags_snap,
-                    to_ring ? 1 : 0, status);
+                    to_ring ? 1 : 0, status, take_stall());
 }
 
 }  // namespace kvr

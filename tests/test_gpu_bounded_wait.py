@@ -1,7 +1,8 @@
 """The bounded-wait exit of the pipelined kernels, made to run on purpose.
 
 Every wait of the windowed decode kernels (over rings and over pages), of the
-short-chunk windowed kernel and of the tensor-core prefill kernel has a time
+short-chunk windowed kernel, of the tensor-core prefill kernel and of the
+bulk-copy kernels (ring from pages, ring snapshot / restore) has a time
 limit; when one runs out the kernel sets an abort flag, its other warps
 leave their loops, the loads and products already issued finish, tensor
 memory is freed and the kernel returns with KVR_DEV_TIMEOUT set.  The test
@@ -169,3 +170,72 @@ def test_short_chunk_windowed_stall_takes_the_bounded_exit():
         oracle.attend_seq(q[s * C:(s + 1) * C], np.arange(P0, P0 + C), *raw_kv(syn, hkv, s, P0 - 127, P0 + C),
                           P0 - 127, 1e4, 0.707, SCALE, 128, sk) for s, P0 in enumerate(P0s)])
     compare_rows(out, want, "short-chunk windowed attention after a stalled launch")
+
+
+def test_ring_gather_stall_takes_the_bounded_exit():
+    # Ring from pages, 12 sequences x 8 KV heads (K and V CTAs): the first
+    # CTA's copies are in flight when it stalls; it stores nothing.
+    import oracle.pages as opages
+    hkv, bsz, S = 8, 32, 12
+    ends = [200 + 37 * s for s in range(S)]
+    t4 = kvr.rope_table(1e4, 4096)
+    syn = Synth(2605, dist="plain", device=DEV)
+    pool = kvr.PagedLayout.contiguous(S, hkv, max(ends), block_size=bsz)
+    fill_paged(pool, syn, list(range(S)), ends, t4, 0.707)
+    ring = kvr.RingLayout.empty(S, hkv)
+    seq = torch.arange(S, dtype=torch.int32, device=DEV)
+    end = torch.tensor(ends, dtype=torch.int64, device=DEV)
+    dt = _stalled(lambda: kvr.kv_ring_gather_pages(pool, ring, seq, seq, end))
+    assert kvr.device_status() & kvr.DEV_TIMEOUT
+    assert dt < 5.0, f"the stalled call took {dt:.2f} s"
+    kvr.kv_ring_gather_pages(pool, ring, seq, seq, end)
+    torch.cuda.synchronize()
+    assert kvr.device_status() == 0
+    pk = pool.k.view(torch.int16).cpu().numpy().view(np.uint16)
+    pv = pool.v.view(torch.int16).cpu().numpy().view(np.uint16)
+    tb = pool.block_table.cpu().numpy()
+    rk = ring.k.view(torch.int16).cpu().numpy().view(np.uint16)
+    rv = ring.v.view(torch.int16).cpu().numpy().view(np.uint16)
+    rt = ring.slot_pos.cpu().numpy()
+    for s, e in enumerate(ends):  # every slot holds a position (end >= 128): the base rows do not matter
+        wk, wv, wt, fl = opages.ring_from_pages(pk, pv, tb, bsz, s, e, rk[s], rv[s], rt[s])
+        assert fl == 0 and np.array_equal(rt[s], wt), s
+        assert np.array_equal(rk[s], wk) and np.array_equal(rv[s], wv), s
+
+
+@pytest.mark.parametrize("restore", [False, True])
+def test_ring_snapshot_stall_takes_the_bounded_exit(restore):
+    # Snapshot (or restore) of 12 sequences x 8 KV heads in 16 KB pieces: the
+    # first piece's copy is in flight when its CTA stalls; it stores nothing.
+    S, hkv = 12, 8
+    ring = kvr.RingLayout.empty(S, hkv)
+    ring.k.normal_()
+    ring.v.normal_()
+    ring.slot_pos.copy_(torch.arange(S * 128, dtype=torch.int32, device=DEV).reshape(S, 128))
+    seq = torch.arange(S, dtype=torch.int32, device=DEV)
+    snap = kvr.ring_snapshot_alloc(S, hkv, device=DEV)
+    if restore:
+        kvr.kv_ring_snapshot(ring, seq, snap)
+        k0, v0, t0 = ring.k.clone(), ring.v.clone(), ring.slot_pos.clone()
+        ring.k.zero_()
+        ring.v.zero_()
+        call = lambda: kvr.kv_ring_restore(ring, seq, snap)
+    else:
+        call = lambda: kvr.kv_ring_snapshot(ring, seq, snap)
+    dt = _stalled(call)
+    assert kvr.device_status() & kvr.DEV_TIMEOUT
+    assert dt < 5.0, f"the stalled call took {dt:.2f} s"
+    call()
+    torch.cuda.synchronize()
+    assert kvr.device_status() == 0
+    if restore:
+        assert torch.equal(ring.k.view(torch.int16), k0.view(torch.int16))
+        assert torch.equal(ring.v.view(torch.int16), v0.view(torch.int16))
+        assert torch.equal(ring.slot_pos, t0)
+    else:
+        back = kvr.RingLayout.empty(S, hkv)
+        kvr.kv_ring_restore(back, seq, snap)
+        torch.cuda.synchronize()
+        assert torch.equal(back.k.view(torch.int16), ring.k.view(torch.int16))
+        assert torch.equal(back.v.view(torch.int16), ring.v.view(torch.int16))
+        assert torch.equal(back.slot_pos, ring.slot_pos)
