@@ -147,12 +147,13 @@ __global__ void __launch_bounds__(RL_THREADS) pages_release_kernel(ReleaseArgs A
 // One CTA per (entry, KV head, K or V), one thread per ring slot.  Slot c is
 // resolved to its source row (-1 when the slot gets no position); the slots
 // form runs whose source rows are consecutive in the pool (positions of one
-// block, in slot order), at most (128 / block size) + 2 of them.  The thread
-// at the head of a run copies it with one bulk copy into the CTA's image of
-// the ring's K (or V), then, once every run has landed, back out to the ring
-// with one bulk store: each byte crosses the SM once, in copies of up to
-// 24 KB.  Slots without a position keep what the ring held.  The CTA of KV
-// head 0's K also writes the slot tags.
+// block in slot order, or of neighbouring blocks where their rows adjoin),
+// at most (128 / block size) + 2 of them.  The thread at the head of a run
+// copies it with one bulk copy into the CTA's image of the ring's K (or V),
+// then, once every run has landed, back out to the ring with one bulk store:
+// each byte crosses the SM once, in copies of a block's rows or more.  Slots
+// without a position keep what the ring held.  The CTA of KV head 0's K also
+// writes the slot tags.
 constexpr int GATHER_THREADS = WIN;
 constexpr int GATHER_SMEM = WIN * DQK * 2;  // the image of one ring's K (or V: the first 32 KB)
 constexpr unsigned GATHER_ST_TIMEOUT = 8u;           // KVR_DEV_TIMEOUT
